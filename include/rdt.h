@@ -1,0 +1,220 @@
+/*
+ * rdt.h -- C ABI of librdt.so: one training step of a Qwen3-style decoder
+ * block stack on one GB300 (sm_103a).
+ *
+ * Operations follow the aprender-train ("entrenar") pages:
+ *   cuda_block.rs   (0.32.0): CudaTransformerBlock::forward, ::backward,
+ *                   compute_attention_cuda, optimizer_step;
+ *   cuda_trainer.rs (0.34.0): train_step_inner (fused cross-entropy),
+ *                   gpu_forward / gpu_backward (final norm + LM head),
+ *                   compute_workspace_clip_scale_gpu and
+ *                   fused_clip_workspace_gradients (squared-sum clip),
+ *                   run_nonblock_optimizer_step (AdamW).
+ *
+ * Conventions shared by every call:
+ *  - Pointers are DEVICE pointers unless marked "host". The caller owns and
+ *    allocates every buffer; the library never allocates, frees or
+ *    synchronises (except rdt_device_error, which says so).
+ *  - `stream` is a cudaStream_t passed as void*. Work is enqueued on it and
+ *    the call returns before the GPU finishes.
+ *  - Outputs are overwritten, never accumulated into.
+ *  - Matrices are row-major. Weights are [out, in]; a projection computes
+ *    y = x W^T. Activations are token-major [T, width] with T = batch*seq and
+ *    token t = b*seq + s at position s of sequence b.
+ *  - rdt_bf16 is the bit pattern of a bfloat16. Dense contractions take bf16
+ *    operands (round-to-nearest-even copies of the fp32 masters) and
+ *    accumulate in fp32; norms, softmax, loss and optimizer math are fp32.
+ *  - Every call returns an rdt_status. Host-detectable problems (null
+ *    pointers, unsupported shapes, misaligned pointers, buffers too small)
+ *    return RDT_EINVAL before anything is enqueued; a failed launch returns
+ *    RDT_ECUDA. rdt_last_error() gives a thread-local message for the last
+ *    failure. Device-side waits in the kernels are bounded: one that gives up
+ *    records RDT_ETIMEOUT in the device error word read by
+ *    rdt_device_error().
+ */
+#ifndef RDT_H_
+#define RDT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t rdt_bf16;
+
+typedef enum rdt_status {
+  RDT_OK = 0,
+  RDT_EINVAL = 1,      /* bad argument, shape, alignment or buffer size */
+  RDT_ECUDA = 2,       /* a CUDA runtime call or kernel launch failed */
+  RDT_ETIMEOUT = 3,    /* a bounded device wait gave up (rdt_device_error) */
+  RDT_ENONFINITE = 4,  /* reserved for callers: non-finite gradient norm */
+} rdt_status;
+
+/* Model shape. hidden, head_dim and intermediate must be multiples of 16,
+ * head_dim one of 16, 32, 64, 128; n_heads a multiple of n_kv_heads;
+ * hidden <= 4096. rms_eps is used by every RMSNorm, forward and backward.
+ * RoPE-neox rotates pairs (i, i + head_dim/2) by pos * rope_theta^(-2i/head_dim). */
+typedef struct rdt_config {
+  int32_t hidden;
+  int32_t n_heads;
+  int32_t n_kv_heads;
+  int32_t head_dim;
+  int32_t intermediate;
+  int32_t vocab;
+  float rms_eps;
+  float rope_theta;
+} rdt_config;
+
+/* ---------------------------------------------------------------------------
+ * Parameter layout of one block. A block's trainable tensors live in ONE flat
+ * fp32 array (the masters) in this order, each starting at the offset
+ * rdt_block_param_offsets() reports (multiples of 16 elements):
+ *   WQ [nh*d, H], WK [nkv*d, H], WV [nkv*d, H], WO [H, nh*d],
+ *   WG [I, H], WU [I, H], WD [H, I], G_ATTN [H], G_FFN [H], G_Q [d], G_K [d].
+ * WQ/WK/WV are adjacent, so together they form the stacked [nh*d+2*nkv*d, H]
+ * matrix; WG/WU likewise form [2I, H]. The matching bf16 shadow and the
+ * gradient array use the same layout.
+ * ------------------------------------------------------------------------- */
+enum {
+  RDT_WQ = 0, RDT_WK, RDT_WV, RDT_WO, RDT_WG, RDT_WU, RDT_WD,
+  RDT_G_ATTN, RDT_G_FFN, RDT_G_Q, RDT_G_K, RDT_BLOCK_NTENSORS
+};
+
+/* Validates cfg (RDT_EINVAL on an unsupported shape). */
+rdt_status rdt_check_config(const rdt_config* cfg);
+
+/* Element count of one block's flat parameter array (fp32 or bf16), or -1. */
+int64_t rdt_block_param_count(const rdt_config* cfg);
+
+/* Host arrays of RDT_BLOCK_NTENSORS entries: element offset and element
+ * count of each tensor inside the block's flat array. */
+rdt_status rdt_block_param_offsets(const rdt_config* cfg, int64_t* offsets, int64_t* counts);
+
+/* Bytes of the activations rdt_block_forward saves for rdt_block_backward
+ * (opaque layout, caller-allocated, 256-byte aligned). */
+size_t rdt_block_saved_bytes(const rdt_config* cfg, int32_t batch, int32_t seq);
+/* Scratch bytes of rdt_block_forward / rdt_block_backward (256-byte aligned). */
+size_t rdt_block_workspace_bytes(const rdt_config* cfg, int32_t batch, int32_t seq);
+/* Scratch bytes of rdt_fused_cross_entropy for `tokens` tokens. */
+size_t rdt_head_workspace_bytes(const rdt_config* cfg, int32_t tokens);
+/* Scratch bytes of rdt_sq_sum. */
+size_t rdt_sq_sum_workspace_bytes(void);
+
+/* ---------------------------------------------------------------------------
+ * Block forward (CudaTransformerBlock::forward with compute_attention_cuda;
+ * the fused residual + RMSNorm of the NF4 block's forward):
+ *   xn = RMSNorm(x, G_ATTN); q,k,v = xn Wq^T, xn Wk^T, xn Wv^T;
+ *   per head: RMSNorm over head_dim (G_Q / G_K), then RoPE-neox at the
+ *   token's position in its own sequence;
+ *   o = causal softmax(q k^T / sqrt(d)) v, query head h reading kv head
+ *       h / (nh/nkv); r1 = x + o Wo^T; xn2 = RMSNorm(r1, G_FFN);
+ *   y = r1 + (silu(xn2 Wg^T) * (xn2 Wu^T)) Wd^T.
+ * w      fp32 masters of this block (flat layout; the gains are read here)
+ * w_bf16 bf16 shadow of the same layout (matrices are read here)
+ * x, y   fp32 [batch*seq, hidden]; y must not alias x
+ * saved  rdt_block_saved_bytes() bytes, written; keep for the backward
+ * ws     rdt_block_workspace_bytes() bytes of scratch
+ * ------------------------------------------------------------------------- */
+rdt_status rdt_block_forward(const rdt_config* cfg, int32_t batch, int32_t seq,
+                             const float* w, const rdt_bf16* w_bf16,
+                             const float* x, float* y,
+                             void* saved, size_t saved_bytes,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Block backward (CudaTransformerBlock::backward: backward_ffn,
+ * backward_post_attn_norm, backward_attention with the GQA reduction and the
+ * inverse RoPE, backward_residual_and_input_norm; the per-head QK-norm
+ * backward and its gain gradients, which that path leaves out, are included).
+ * x      the block's forward input, fp32 [T, H]
+ * saved  what rdt_block_forward wrote for the same x and w
+ * dy     upstream gradient fp32 [T, H]
+ * dx     gradient w.r.t. x, fp32 [T, H] (overwritten; may alias dy)
+ * grads  fp32 flat array in the block layout, every tensor overwritten
+ * ------------------------------------------------------------------------- */
+rdt_status rdt_block_backward(const rdt_config* cfg, int32_t batch, int32_t seq,
+                              const float* w, const rdt_bf16* w_bf16,
+                              const float* x, const void* saved, size_t saved_bytes,
+                              const float* dy, float* dx, float* grads,
+                              void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Final RMSNorm + LM head + cross-entropy, forward and backward in one call
+ * (train_step_inner's fused cross-entropy; gpu_forward's final norm and LM
+ * head; gpu_backward's LM-head and final-norm backward). Logits live only in
+ * device scratch; nothing but the caller's copy of loss_partials reaches the
+ * host.
+ *   hn = RMSNorm(h, gamma_f); z = hn W_lm^T;
+ *   loss_partials[t] = logsumexp(z_t) - z_t[targets[t]]   (unscaled NLL);
+ *   dz = (softmax(z_t) - onehot(targets[t])) * loss_scale;
+ *   dh, dgamma_f, dw_lm = gradients of sum_t loss_scale * loss_partials[t].
+ * h        fp32 [tokens, H], the last block's output
+ * gamma_f  fp32 [H]; w_lm bf16 [V, H]
+ * targets  int32 [tokens], device; each must lie in [0, V) (not checked on
+ *          the device: the caller validates ids before upload)
+ * loss_scale  normally 1/tokens (loss = mean NLL)
+ * dh fp32 [tokens, H]; dgamma_f fp32 [H]; dw_lm fp32 [V, H] (all overwritten)
+ * ------------------------------------------------------------------------- */
+rdt_status rdt_fused_cross_entropy(const rdt_config* cfg, int32_t tokens,
+                                   const float* h, const float* gamma_f,
+                                   const rdt_bf16* w_lm, const int32_t* targets,
+                                   float loss_scale, float* loss_partials,
+                                   float* dh, float* dgamma_f, float* dw_lm,
+                                   void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Squared-sum gradient clip (compute_workspace_clip_scale_gpu,
+ * fused_clip_workspace_gradients; contract C-CLIP-001).
+ * rdt_sq_sum: *sumsq = sum over the nbuf buffers of sum(g^2), accumulated in
+ *   fp64 (fp32 within a thread's short run). bufs and lens are HOST arrays of
+ *   device pointers / element counts; each buffer 16-byte aligned.
+ * rdt_clip_scale: norm = sqrt(*sumsq) (the squared sums are not squared
+ *   again); *scale = max_norm / norm if norm > max_norm else 1;
+ *   *nonfinite = 1 if norm is not finite (then *scale = 1), else 0.
+ * ------------------------------------------------------------------------- */
+rdt_status rdt_sq_sum(const float* const* bufs, const int64_t* lens, int32_t nbuf,
+                      double* sumsq, void* ws, size_t ws_bytes, void* stream);
+rdt_status rdt_clip_scale(const double* sumsq, float max_norm, float* scale,
+                          int32_t* nonfinite, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * AdamW over n contiguous fp32 elements (optimizer_step's adamw_step_cuda;
+ * step counted from 1 as run_nonblock_optimizer_step does):
+ *   g' = scale * g; m = b1 m + (1-b1) g'; v = b2 v + (1-b2) g'^2;
+ *   w = w - lr * ( (m/(1-b1^step)) / (sqrt(v/(1-b2^step)) + eps) + wd * w ).
+ * scale     device fp32 scalar from rdt_clip_scale, or NULL for 1
+ * skip_flag device int32, or NULL; when *skip_flag != 0 nothing is written
+ * w_bf16    if not NULL, receives the bf16 (RNE) copy of the updated w
+ * w, g, m, v, w_bf16 16-byte aligned. step >= 1.
+ * ------------------------------------------------------------------------- */
+rdt_status rdt_adamw_step(float* w, const float* g, float* m, float* v, int64_t n,
+                          const float* scale, const int32_t* skip_flag, int32_t step,
+                          float lr, float beta1, float beta2, float eps, float weight_decay,
+                          rdt_bf16* w_bf16, void* stream);
+
+/* The tensor-core GEMM every projection of the path runs on, exposed so it
+ * can be tested on its own: C[M, N] (fp32, row stride ldc) = A' B'^T over K,
+ * with A' = A ([M, K], row stride lda) when a_mn == 0, or the transpose of A
+ * given as [K, M] when a_mn == 1; likewise B' = B ([N, K]) or B^T with B
+ * given as [K, N]. A, B bf16; lda, ldb multiples of 8; ldc a multiple of 4. */
+rdt_status rdt_gemm(const rdt_bf16* A, int32_t a_mn, int64_t lda, const rdt_bf16* B,
+                    int32_t b_mn, int64_t ldb, int32_t M, int32_t N, int32_t K, float* C,
+                    int64_t ldc, void* stream);
+
+/* dst[i] = bf16(src[i]) with round-to-nearest-even; n elements, 16-byte aligned. */
+rdt_status rdt_cast_bf16(const float* src, rdt_bf16* dst, int64_t n, void* stream);
+
+/* Thread-local description of the last failure on this thread ("" if none). */
+const char* rdt_last_error(void);
+
+/* Synchronises the current device, then reads and clears the device error
+ * word of the current device (0 = none, else an rdt_status such as
+ * RDT_ETIMEOUT). Writes it to *code (host). */
+rdt_status rdt_device_error(int32_t* code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RDT_H_ */

@@ -1,0 +1,628 @@
+// C-ABI entry points of librdt.so (declared in include/rdt.h): argument
+// validation, carving of the caller's saved-activation and scratch buffers,
+// and the launch sequence of each call. Nothing here allocates device memory.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/rdt.h"
+#include "internal.h"
+
+using namespace rdt;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+rdt_status fail(rdt_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+// Device error word: bounded waits that give up record a code here.
+__device__ int g_device_error;
+
+int* device_error_ptr() {
+  static int* ptrs[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// Sequential carve of a caller buffer into 256-byte aligned pieces.
+struct Carver {
+  uint8_t* base;
+  size_t off = 0;
+  explicit Carver(void* b) : base(static_cast<uint8_t*>(b)) {}
+  template <typename T>
+  T* take(size_t count) {
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off = align_up(off + count * sizeof(T));
+    return p;
+  }
+};
+
+bool cfg_ok(const rdt_config* c, std::string* why) {
+  if (!c) { *why = "config is null"; return false; }
+  if (c->hidden < 16 || c->hidden > 4096 || c->hidden % 16) {
+    *why = "hidden must be a multiple of 16 in [16, 4096]"; return false;
+  }
+  if (!(c->head_dim == 16 || c->head_dim == 32 || c->head_dim == 64 || c->head_dim == 128)) {
+    *why = "head_dim must be 16, 32, 64 or 128"; return false;
+  }
+  if (c->n_heads < 1 || c->n_kv_heads < 1 || c->n_heads % c->n_kv_heads) {
+    *why = "n_heads must be a positive multiple of n_kv_heads"; return false;
+  }
+  if (c->intermediate < 16 || c->intermediate % 16) {
+    *why = "intermediate must be a positive multiple of 16"; return false;
+  }
+  if (c->vocab < 16 || c->vocab % 16) { *why = "vocab must be a positive multiple of 16"; return false; }
+  if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) {
+    *why = "rms_eps must be >= 0 and rope_theta > 0"; return false;
+  }
+  return true;
+}
+
+struct Dims {
+  int64_t H, nh, nkv, d, I, V, qd, kd, nqkv;
+};
+Dims dims_of(const rdt_config* c) {
+  Dims m;
+  m.H = c->hidden; m.nh = c->n_heads; m.nkv = c->n_kv_heads; m.d = c->head_dim;
+  m.I = c->intermediate; m.V = c->vocab;
+  m.qd = m.nh * m.d; m.kd = m.nkv * m.d; m.nqkv = m.qd + 2 * m.kd;
+  return m;
+}
+
+void block_counts(const Dims& m, int64_t* cnt) {
+  cnt[RDT_WQ] = m.qd * m.H;
+  cnt[RDT_WK] = m.kd * m.H;
+  cnt[RDT_WV] = m.kd * m.H;
+  cnt[RDT_WO] = m.H * m.qd;
+  cnt[RDT_WG] = m.I * m.H;
+  cnt[RDT_WU] = m.I * m.H;
+  cnt[RDT_WD] = m.H * m.I;
+  cnt[RDT_G_ATTN] = m.H;
+  cnt[RDT_G_FFN] = m.H;
+  cnt[RDT_G_Q] = m.d;
+  cnt[RDT_G_K] = m.d;
+}
+void block_offsets(const Dims& m, int64_t* off) {
+  int64_t cnt[RDT_BLOCK_NTENSORS];
+  block_counts(m, cnt);
+  int64_t o = 0;
+  for (int i = 0; i < RDT_BLOCK_NTENSORS; ++i) {
+    off[i] = o;
+    o += cnt[i];  // every count is a multiple of 16
+  }
+}
+
+// Saved activations of one block.
+struct Saved {
+  bf16 *xn, *qkv, *qr, *kr, *o, *xn2, *gu, *s;
+  float *rstd1, *rstd_q, *rstd_k, *lse, *r1, *rstd2;
+};
+size_t carve_saved(const Dims& m, int64_t B, int64_t S, void* base, Saved* sv) {
+  const int64_t T = B * S;
+  Carver c(base);
+  Saved t;
+  t.xn = c.take<bf16>(T * m.H);
+  t.rstd1 = c.take<float>(T);
+  t.qkv = c.take<bf16>(T * m.nqkv);
+  t.qr = c.take<bf16>(T * m.qd);
+  t.kr = c.take<bf16>(T * m.kd);
+  t.rstd_q = c.take<float>(T * m.nh);
+  t.rstd_k = c.take<float>(T * m.nkv);
+  t.o = c.take<bf16>(T * m.qd);
+  t.lse = c.take<float>(B * m.nh * S);
+  t.r1 = c.take<float>(T * m.H);
+  t.xn2 = c.take<bf16>(T * m.H);
+  t.rstd2 = c.take<float>(T);
+  t.gu = c.take<bf16>(T * 2 * m.I);
+  t.s = c.take<bf16>(T * m.I);
+  if (sv) *sv = t;
+  return c.off;
+}
+
+// Scratch of block forward / backward (one layout serves both).
+struct BlockWs {
+  float* cs;
+  bf16 *dy_b, *dgu, *dr1_b, *dout, *dqkv;
+  float *dxn, *dr1, *Dd, *dq, *dk, *partials;
+};
+size_t carve_block_ws(const Dims& m, int64_t B, int64_t S, void* base, BlockWs* w) {
+  const int64_t T = B * S;
+  Carver c(base);
+  BlockWs t;
+  t.cs = c.take<float>(S * m.d);  // [S][d/2] (cos, sin)
+  t.dy_b = c.take<bf16>(T * m.H);
+  t.dgu = c.take<bf16>(T * 2 * m.I);
+  t.dr1_b = c.take<bf16>(T * m.H);
+  t.dout = c.take<bf16>(T * m.qd);
+  t.dqkv = c.take<bf16>(T * m.nqkv);
+  t.dxn = c.take<float>(T * m.H);
+  t.dr1 = c.take<float>(T * m.H);
+  t.Dd = c.take<float>(B * m.nh * S);
+  t.dq = c.take<float>(T * m.qd);
+  t.dk = c.take<float>(T * m.kd);
+  const int64_t pw = m.H > 2 * m.d ? m.H : 2 * m.d;
+  t.partials = c.take<float>(kMaxPartialRows * pw);
+  if (w) *w = t;
+  return c.off;
+}
+
+struct HeadWs {
+  bf16 *hn, *z;
+  float *rstd, *tgt, *lse, *dhn, *partials;
+  float2* part;
+};
+size_t carve_head_ws(const Dims& m, int64_t T, void* base, HeadWs* w) {
+  Carver c(base);
+  HeadWs t;
+  t.hn = c.take<bf16>(T * m.H);
+  t.rstd = c.take<float>(T);
+  t.z = c.take<bf16>(T * m.V);
+  t.part = c.take<float2>(T * gemm_n_tiles((int)m.V));
+  t.tgt = c.take<float>(T);
+  t.lse = c.take<float>(T);
+  t.dhn = c.take<float>(T * m.H);
+  t.partials = c.take<float>(kMaxPartialRows * m.H);
+  if (w) *w = t;
+  return c.off;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+#define RDT_CHECK_CUDA(expr)                                                     \
+  do {                                                                           \
+    cudaError_t e_ = (expr);                                                     \
+    if (e_ != cudaSuccess)                                                       \
+      return fail(RDT_ECUDA, "%s failed: %s", #expr, cudaGetErrorString(e_));    \
+  } while (0)
+
+#define RDT_GEMM(...)                                                                 \
+  do {                                                                                \
+    const char* why_ = "";                                                           \
+    cudaError_t e_ = gemm(__VA_ARGS__, &why_);                                        \
+    if (e_ != cudaSuccess)                                                            \
+      return fail(*why_ ? RDT_EINVAL : RDT_ECUDA, "gemm at line %d: %s %s", __LINE__, \
+                  why_, cudaGetErrorString(e_));                                      \
+  } while (0)
+
+}  // namespace
+
+// =========================================================================
+extern "C" {
+
+const char* rdt_last_error(void) { return g_last_error.c_str(); }
+
+rdt_status rdt_check_config(const rdt_config* cfg) {
+  std::string why;
+  if (!cfg_ok(cfg, &why)) return fail(RDT_EINVAL, "config: %s", why.c_str());
+  return RDT_OK;
+}
+
+int64_t rdt_block_param_count(const rdt_config* cfg) {
+  std::string why;
+  if (!cfg_ok(cfg, &why)) return -1;
+  int64_t cnt[RDT_BLOCK_NTENSORS];
+  block_counts(dims_of(cfg), cnt);
+  int64_t s = 0;
+  for (int i = 0; i < RDT_BLOCK_NTENSORS; ++i) s += cnt[i];
+  return s;
+}
+
+rdt_status rdt_block_param_offsets(const rdt_config* cfg, int64_t* offsets, int64_t* counts) {
+  std::string why;
+  if (!cfg_ok(cfg, &why)) return fail(RDT_EINVAL, "config: %s", why.c_str());
+  if (!offsets || !counts) return fail(RDT_EINVAL, "offsets/counts is null");
+  const Dims m = dims_of(cfg);
+  block_offsets(m, offsets);
+  block_counts(m, counts);
+  return RDT_OK;
+}
+
+size_t rdt_block_saved_bytes(const rdt_config* cfg, int32_t batch, int32_t seq) {
+  std::string why;
+  if (!cfg_ok(cfg, &why) || batch < 1 || seq < 1) return 0;
+  return carve_saved(dims_of(cfg), batch, seq, nullptr, nullptr);
+}
+
+size_t rdt_block_workspace_bytes(const rdt_config* cfg, int32_t batch, int32_t seq) {
+  std::string why;
+  if (!cfg_ok(cfg, &why) || batch < 1 || seq < 1) return 0;
+  return carve_block_ws(dims_of(cfg), batch, seq, nullptr, nullptr);
+}
+
+size_t rdt_head_workspace_bytes(const rdt_config* cfg, int32_t tokens) {
+  std::string why;
+  if (!cfg_ok(cfg, &why) || tokens < 1) return 0;
+  return carve_head_ws(dims_of(cfg), tokens, nullptr, nullptr);
+}
+
+size_t rdt_sq_sum_workspace_bytes(void) { return kMaxSqSumPartials * sizeof(double); }
+
+// -------------------------------------------------------------- block fwd
+rdt_status rdt_block_forward(const rdt_config* cfg, int32_t batch, int32_t seq, const float* w,
+                             const rdt_bf16* w_bf16, const float* x, float* y, void* saved,
+                             size_t saved_bytes, void* ws, size_t ws_bytes, void* stream) {
+  std::string why;
+  if (!cfg_ok(cfg, &why)) return fail(RDT_EINVAL, "config: %s", why.c_str());
+  if (batch < 1 || seq < 1) return fail(RDT_EINVAL, "batch and seq must be >= 1");
+  if (!w || !w_bf16 || !x || !y || !saved || !ws) return fail(RDT_EINVAL, "null pointer");
+  if (!aligned16(w) || !aligned16(w_bf16) || !aligned16(x) || !aligned16(y) ||
+      (reinterpret_cast<uintptr_t>(saved) & 255) || (reinterpret_cast<uintptr_t>(ws) & 255))
+    return fail(RDT_EINVAL, "w/x/y must be 16-byte and saved/ws 256-byte aligned");
+  if (x == y) return fail(RDT_EINVAL, "y must not alias x");
+  const Dims m = dims_of(cfg);
+  if (saved_bytes < carve_saved(m, batch, seq, nullptr, nullptr))
+    return fail(RDT_EINVAL, "saved buffer too small");
+  if (ws_bytes < carve_block_ws(m, batch, seq, nullptr, nullptr))
+    return fail(RDT_EINVAL, "workspace too small");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* err = device_error_ptr();
+  const int T = batch * seq;
+  Saved sv;
+  carve_saved(m, batch, seq, saved, &sv);
+  BlockWs wk;
+  carve_block_ws(m, batch, seq, ws, &wk);
+  int64_t off[RDT_BLOCK_NTENSORS];
+  block_offsets(m, off);
+  const bf16* wb = reinterpret_cast<const bf16*>(w_bf16);
+
+  // input RMSNorm
+  RDT_CHECK_CUDA(rmsnorm_fwd(x, w + off[RDT_G_ATTN], sv.xn, sv.rstd1, T, (int)m.H, cfg->rms_eps, s));
+  // stacked Q/K/V projection: qkv[T, qd+2kd] = xn [Wq; Wk; Wv]^T
+  {
+    Epi e;
+    e.kind = EPI_BF16;
+    e.out = sv.qkv;
+    e.ld_out = m.nqkv;
+    RDT_GEMM(Mat{sv.xn, T, m.H, m.H}, false, Mat{wb + off[RDT_WQ], m.nqkv, m.H, m.H}, false, T,
+             (int)m.nqkv, (int)m.H, e, err, s);
+  }
+  // per-head QK RMSNorm + RoPE-neox
+  RDT_CHECK_CUDA(rope_table(wk.cs, seq, (int)m.d, cfg->rope_theta, s));
+  RDT_CHECK_CUDA(qknorm_rope_fwd(sv.qkv, m.nqkv, sv.qr, sv.kr, sv.rstd_q, sv.rstd_k,
+                                 w + off[RDT_G_Q], w + off[RDT_G_K], wk.cs, T, seq, (int)m.nh,
+                                 (int)m.nkv, (int)m.d, cfg->rms_eps, s));
+  // causal GQA attention
+  RDT_CHECK_CUDA(attn_fwd(sv.qr, m.qd, sv.kr, m.kd, sv.qkv + m.qd + m.kd, m.nqkv, sv.o, sv.lse,
+                          batch, seq, (int)m.nh, (int)m.nkv, (int)m.d, s));
+  // O projection + residual: r1 = x + o Wo^T
+  {
+    Epi e;
+    e.kind = EPI_F32_RESID;
+    e.out = sv.r1;
+    e.ld_out = m.H;
+    e.resid = x;
+    e.ld_resid = m.H;
+    RDT_GEMM(Mat{sv.o, T, m.qd, m.qd}, false, Mat{wb + off[RDT_WO], m.H, m.qd, m.qd}, false, T,
+             (int)m.H, (int)m.qd, e, err, s);
+  }
+  // post-attention RMSNorm
+  RDT_CHECK_CUDA(rmsnorm_fwd(sv.r1, w + off[RDT_G_FFN], sv.xn2, sv.rstd2, T, (int)m.H,
+                             cfg->rms_eps, s));
+  // gate/up projection with the SwiGLU epilogue
+  {
+    Epi e;
+    e.kind = EPI_SWIGLU;
+    e.out = sv.gu;
+    e.ld_out = 2 * m.I;
+    e.out2 = sv.s;
+    e.ld_out2 = m.I;
+    e.half = (int)m.I;
+    RDT_GEMM(Mat{sv.xn2, T, m.H, m.H}, false, Mat{wb + off[RDT_WG], 2 * m.I, m.H, m.H}, false, T,
+             (int)m.I, (int)m.H, e, err, s);
+  }
+  // down projection + residual: y = r1 + s Wd^T
+  {
+    Epi e;
+    e.kind = EPI_F32_RESID;
+    e.out = y;
+    e.ld_out = m.H;
+    e.resid = sv.r1;
+    e.ld_resid = m.H;
+    RDT_GEMM(Mat{sv.s, T, m.I, m.I}, false, Mat{wb + off[RDT_WD], m.H, m.I, m.I}, false, T,
+             (int)m.H, (int)m.I, e, err, s);
+  }
+  return RDT_OK;
+}
+
+// ------------------------------------------------------------- block bwd
+rdt_status rdt_block_backward(const rdt_config* cfg, int32_t batch, int32_t seq, const float* w,
+                              const rdt_bf16* w_bf16, const float* x, const void* saved,
+                              size_t saved_bytes, const float* dy, float* dx, float* grads,
+                              void* ws, size_t ws_bytes, void* stream) {
+  std::string why;
+  if (!cfg_ok(cfg, &why)) return fail(RDT_EINVAL, "config: %s", why.c_str());
+  if (batch < 1 || seq < 1) return fail(RDT_EINVAL, "batch and seq must be >= 1");
+  if (!w || !w_bf16 || !x || !saved || !dy || !dx || !grads || !ws)
+    return fail(RDT_EINVAL, "null pointer");
+  if (!aligned16(w) || !aligned16(w_bf16) || !aligned16(x) || !aligned16(dy) || !aligned16(dx) ||
+      !aligned16(grads) || (reinterpret_cast<uintptr_t>(saved) & 255) ||
+      (reinterpret_cast<uintptr_t>(ws) & 255))
+    return fail(RDT_EINVAL, "pointers must be 16-byte (saved/ws 256-byte) aligned");
+  const Dims m = dims_of(cfg);
+  if (saved_bytes < carve_saved(m, batch, seq, nullptr, nullptr))
+    return fail(RDT_EINVAL, "saved buffer too small");
+  if (ws_bytes < carve_block_ws(m, batch, seq, nullptr, nullptr))
+    return fail(RDT_EINVAL, "workspace too small");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* err = device_error_ptr();
+  const int T = batch * seq;
+  Saved sv;
+  carve_saved(m, batch, seq, const_cast<void*>(saved), &sv);
+  BlockWs wk;
+  carve_block_ws(m, batch, seq, ws, &wk);
+  int64_t off[RDT_BLOCK_NTENSORS];
+  block_offsets(m, off);
+  const bf16* wb = reinterpret_cast<const bf16*>(w_bf16);
+
+  // dy as a bf16 GEMM operand
+  RDT_CHECK_CUDA(cast_bf16(dy, wk.dy_b, (int64_t)T * m.H, s));
+  // ds = dy Wd, with the SwiGLU backward in the epilogue -> dgu = [dg | du]
+  {
+    Epi e;
+    e.kind = EPI_SWIGLU_BWD;
+    e.out = wk.dgu;
+    e.ld_out = 2 * m.I;
+    e.aux = sv.gu;
+    e.ld_aux = 2 * m.I;
+    e.half = (int)m.I;
+    RDT_GEMM(Mat{wk.dy_b, T, m.H, m.H}, false, Mat{wb + off[RDT_WD], m.H, m.I, m.I}, true, T,
+             (int)m.I, (int)m.H, e, err, s);
+  }
+  // dWd = dy^T s
+  {
+    Epi e;
+    e.kind = EPI_F32;
+    e.out = grads + off[RDT_WD];
+    e.ld_out = m.I;
+    RDT_GEMM(Mat{wk.dy_b, T, m.H, m.H}, true, Mat{sv.s, T, m.I, m.I}, true, (int)m.H, (int)m.I, T,
+             e, err, s);
+  }
+  // dxn2 = [dg du] [Wg; Wu]
+  {
+    Epi e;
+    e.kind = EPI_F32;
+    e.out = wk.dxn;
+    e.ld_out = m.H;
+    RDT_GEMM(Mat{wk.dgu, T, 2 * m.I, 2 * m.I}, false, Mat{wb + off[RDT_WG], 2 * m.I, m.H, m.H},
+             true, T, (int)m.H, (int)(2 * m.I), e, err, s);
+  }
+  // [dWg; dWu] = [dg du]^T xn2
+  {
+    Epi e;
+    e.kind = EPI_F32;
+    e.out = grads + off[RDT_WG];
+    e.ld_out = m.H;
+    RDT_GEMM(Mat{wk.dgu, T, 2 * m.I, 2 * m.I}, true, Mat{sv.xn2, T, m.H, m.H}, true,
+             (int)(2 * m.I), (int)m.H, T, e, err, s);
+  }
+  // post-attention RMSNorm backward, identity skip added after it
+  RDT_CHECK_CUDA(rmsnorm_bwd(wk.dxn, sv.r1, sv.rstd2, w + off[RDT_G_FFN], dy, wk.dr1, wk.dr1_b,
+                             grads + off[RDT_G_FFN], wk.partials, T, (int)m.H, s));
+  // do = dr1 Wo
+  {
+    Epi e;
+    e.kind = EPI_BF16;
+    e.out = wk.dout;
+    e.ld_out = m.qd;
+    RDT_GEMM(Mat{wk.dr1_b, T, m.H, m.H}, false, Mat{wb + off[RDT_WO], m.H, m.qd, m.qd}, true, T,
+             (int)m.qd, (int)m.H, e, err, s);
+  }
+  // dWo = dr1^T o
+  {
+    Epi e;
+    e.kind = EPI_F32;
+    e.out = grads + off[RDT_WO];
+    e.ld_out = m.qd;
+    RDT_GEMM(Mat{wk.dr1_b, T, m.H, m.H}, true, Mat{sv.o, T, m.qd, m.qd}, true, (int)m.H,
+             (int)m.qd, T, e, err, s);
+  }
+  // attention backward (GQA reduction inside), dq accumulated in fp32
+  RDT_CHECK_CUDA(attn_bwd_pre(sv.o, wk.dout, wk.Dd, batch, seq, (int)m.nh, (int)m.d, s));
+  RDT_CHECK_CUDA(cudaMemsetAsync(wk.dq, 0, sizeof(float) * T * m.qd, s));
+  RDT_CHECK_CUDA(attn_bwd(sv.qr, m.qd, sv.kr, m.kd, sv.qkv + m.qd + m.kd, m.nqkv, wk.dout, sv.lse,
+                          wk.Dd, wk.dq, wk.dk, wk.dqkv + m.qd + m.kd, m.nqkv, batch, seq,
+                          (int)m.nh, (int)m.nkv, (int)m.d, s));
+  // inverse RoPE + QK-norm backward -> dq, dk columns of dqkv; q/k gain grads
+  RDT_CHECK_CUDA(rope_table(wk.cs, seq, (int)m.d, cfg->rope_theta, s));
+  RDT_CHECK_CUDA(qknorm_rope_bwd(wk.dq, wk.dk, sv.qkv, m.nqkv, sv.rstd_q, sv.rstd_k,
+                                 w + off[RDT_G_Q], w + off[RDT_G_K], wk.cs, wk.dqkv,
+                                 grads + off[RDT_G_Q], wk.partials, T, seq, (int)m.nh, (int)m.nkv,
+                                 (int)m.d, s));
+  // dxn = [dq dk dv] [Wq; Wk; Wv]
+  {
+    Epi e;
+    e.kind = EPI_F32;
+    e.out = wk.dxn;
+    e.ld_out = m.H;
+    RDT_GEMM(Mat{wk.dqkv, T, m.nqkv, m.nqkv}, false, Mat{wb + off[RDT_WQ], m.nqkv, m.H, m.H}, true,
+             T, (int)m.H, (int)m.nqkv, e, err, s);
+  }
+  // [dWq; dWk; dWv] = [dq dk dv]^T xn
+  {
+    Epi e;
+    e.kind = EPI_F32;
+    e.out = grads + off[RDT_WQ];
+    e.ld_out = m.H;
+    RDT_GEMM(Mat{wk.dqkv, T, m.nqkv, m.nqkv}, true, Mat{sv.xn, T, m.H, m.H}, true, (int)m.nqkv,
+             (int)m.H, T, e, err, s);
+  }
+  // input RMSNorm backward + identity skip
+  RDT_CHECK_CUDA(rmsnorm_bwd(wk.dxn, x, sv.rstd1, w + off[RDT_G_ATTN], wk.dr1, dx, nullptr,
+                             grads + off[RDT_G_ATTN], wk.partials, T, (int)m.H, s));
+  return RDT_OK;
+}
+
+// --------------------------------------------------------------- LM head
+rdt_status rdt_fused_cross_entropy(const rdt_config* cfg, int32_t tokens, const float* h,
+                                   const float* gamma_f, const rdt_bf16* w_lm,
+                                   const int32_t* targets, float loss_scale, float* loss_partials,
+                                   float* dh, float* dgamma_f, float* dw_lm, void* ws,
+                                   size_t ws_bytes, void* stream) {
+  std::string why;
+  if (!cfg_ok(cfg, &why)) return fail(RDT_EINVAL, "config: %s", why.c_str());
+  if (tokens < 1) return fail(RDT_EINVAL, "tokens must be >= 1");
+  if (!h || !gamma_f || !w_lm || !targets || !loss_partials || !dh || !dgamma_f || !dw_lm || !ws)
+    return fail(RDT_EINVAL, "null pointer");
+  if (!aligned16(h) || !aligned16(gamma_f) || !aligned16(w_lm) || !aligned16(dh) ||
+      !aligned16(dw_lm) || (reinterpret_cast<uintptr_t>(ws) & 255))
+    return fail(RDT_EINVAL, "pointers must be 16-byte (ws 256-byte) aligned");
+  const Dims m = dims_of(cfg);
+  if (ws_bytes < carve_head_ws(m, tokens, nullptr, nullptr))
+    return fail(RDT_EINVAL, "workspace too small");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* err = device_error_ptr();
+  const int T = tokens;
+  HeadWs wk;
+  carve_head_ws(m, T, ws, &wk);
+  const bf16* wl = reinterpret_cast<const bf16*>(w_lm);
+  const int ntiles = gemm_n_tiles((int)m.V);
+
+  RDT_CHECK_CUDA(rmsnorm_fwd(h, gamma_f, wk.hn, wk.rstd, T, (int)m.H, cfg->rms_eps, s));
+  // logits tile by tile: bf16 copy + per-tile (max, sum exp) + target logit
+  {
+    Epi e;
+    e.kind = EPI_CE;
+    e.out = wk.z;
+    e.ld_out = m.V;
+    e.part = wk.part;
+    e.part_ld = ntiles;
+    e.targets = targets;
+    e.tgt_logit = wk.tgt;
+    RDT_GEMM(Mat{wk.hn, T, m.H, m.H}, false, Mat{wl, m.V, m.H, m.H}, false, T, (int)m.V, (int)m.H,
+             e, err, s);
+  }
+  RDT_CHECK_CUDA(ce_finalize(wk.part, ntiles, ntiles, wk.tgt, wk.lse, loss_partials, T, s));
+  RDT_CHECK_CUDA(ce_grad(wk.z, wk.lse, targets, loss_scale, T, (int)m.V, s));
+  // dhn = dz W_lm
+  {
+    Epi e;
+    e.kind = EPI_F32;
+    e.out = wk.dhn;
+    e.ld_out = m.H;
+    RDT_GEMM(Mat{wk.z, T, m.V, m.V}, false, Mat{wl, m.V, m.H, m.H}, true, T, (int)m.H, (int)m.V,
+             e, err, s);
+  }
+  // dW_lm = dz^T hn
+  {
+    Epi e;
+    e.kind = EPI_F32;
+    e.out = dw_lm;
+    e.ld_out = m.H;
+    RDT_GEMM(Mat{wk.z, T, m.V, m.V}, true, Mat{wk.hn, T, m.H, m.H}, true, (int)m.V, (int)m.H, T, e,
+             err, s);
+  }
+  RDT_CHECK_CUDA(rmsnorm_bwd(wk.dhn, h, wk.rstd, gamma_f, nullptr, dh, nullptr, dgamma_f,
+                             wk.partials, T, (int)m.H, s));
+  return RDT_OK;
+}
+
+// ------------------------------------------------------------ clip / AdamW
+rdt_status rdt_sq_sum(const float* const* bufs, const int64_t* lens, int32_t nbuf, double* sumsq,
+                      void* ws, size_t ws_bytes, void* stream) {
+  if (!bufs || !lens || !sumsq || !ws) return fail(RDT_EINVAL, "null pointer");
+  if (nbuf < 1 || nbuf > 64) return fail(RDT_EINVAL, "nbuf must be in [1, 64]");
+  if (ws_bytes < sizeof(double)) return fail(RDT_EINVAL, "workspace too small");
+  for (int i = 0; i < nbuf; ++i) {
+    if (lens[i] < 0 || (lens[i] > 0 && !bufs[i])) return fail(RDT_EINVAL, "bad buffer %d", i);
+    if (!aligned16(bufs[i])) return fail(RDT_EINVAL, "buffer %d not 16-byte aligned", i);
+  }
+  if (reinterpret_cast<uintptr_t>(ws) & 7) return fail(RDT_EINVAL, "workspace not 8-byte aligned");
+  int maxp = static_cast<int>(ws_bytes / sizeof(double));
+  if (maxp > kMaxSqSumPartials) maxp = kMaxSqSumPartials;
+  RDT_CHECK_CUDA(sq_sum(bufs, lens, nbuf, sumsq, static_cast<double*>(ws), maxp,
+                        static_cast<cudaStream_t>(stream)));
+  return RDT_OK;
+}
+
+rdt_status rdt_clip_scale(const double* sumsq, float max_norm, float* scale, int32_t* nonfinite,
+                          void* stream) {
+  if (!sumsq || !scale) return fail(RDT_EINVAL, "null pointer");
+  if (!(max_norm > 0.f)) return fail(RDT_EINVAL, "max_norm must be > 0");
+  RDT_CHECK_CUDA(clip_scale(sumsq, max_norm, scale, nonfinite, static_cast<cudaStream_t>(stream)));
+  return RDT_OK;
+}
+
+rdt_status rdt_adamw_step(float* w, const float* g, float* m, float* v, int64_t n,
+                          const float* scale, const int32_t* skip_flag, int32_t step, float lr,
+                          float beta1, float beta2, float eps, float weight_decay,
+                          rdt_bf16* w_bf16, void* stream) {
+  if (!w || !g || !m || !v) return fail(RDT_EINVAL, "null pointer");
+  if (n < 0) return fail(RDT_EINVAL, "n must be >= 0");
+  if (step < 1) return fail(RDT_EINVAL, "step must be >= 1 (bias correction)");
+  if (!aligned16(w) || !aligned16(g) || !aligned16(m) || !aligned16(v) ||
+      (w_bf16 && !aligned16(w_bf16)))
+    return fail(RDT_EINVAL, "buffers must be 16-byte aligned");
+  if (n == 0) return RDT_OK;
+  const double bc1 = 1.0 - std::pow(static_cast<double>(beta1), step);
+  const double bc2 = 1.0 - std::pow(static_cast<double>(beta2), step);
+  RDT_CHECK_CUDA(adamw(w, g, m, v, n, scale, skip_flag, lr, beta1, beta2, eps, weight_decay,
+                       static_cast<float>(bc1), static_cast<float>(bc2),
+                       reinterpret_cast<bf16*>(w_bf16), static_cast<cudaStream_t>(stream)));
+  return RDT_OK;
+}
+
+rdt_status rdt_gemm(const rdt_bf16* A, int32_t a_mn, int64_t lda, const rdt_bf16* B,
+                    int32_t b_mn, int64_t ldb, int32_t M, int32_t N, int32_t K, float* C,
+                    int64_t ldc, void* stream) {
+  if (!A || !B || !C) return fail(RDT_EINVAL, "null pointer");
+  if (M < 1 || N < 1 || K < 1) return fail(RDT_EINVAL, "M, N, K must be >= 1");
+  if (lda % 8 || ldb % 8 || ldc % 4 || !aligned16(A) || !aligned16(B) || !aligned16(C))
+    return fail(RDT_EINVAL, "lda/ldb must be multiples of 8, ldc of 4, pointers 16-byte aligned");
+  const int64_t arows = a_mn ? K : M, acols = a_mn ? M : K;
+  const int64_t brows = b_mn ? K : N, bcols = b_mn ? N : K;
+  if (lda < acols || ldb < bcols || ldc < N) return fail(RDT_EINVAL, "leading dimension too small");
+  Epi e;
+  e.kind = EPI_F32;
+  e.out = C;
+  e.ld_out = ldc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* err = device_error_ptr();
+  RDT_GEMM(Mat{A, arows, acols, lda}, a_mn != 0, Mat{B, brows, bcols, ldb}, b_mn != 0, M, N, K, e,
+           err, s);
+  return RDT_OK;
+}
+
+rdt_status rdt_cast_bf16(const float* src, rdt_bf16* dst, int64_t n, void* stream) {
+  if (!src || !dst) return fail(RDT_EINVAL, "null pointer");
+  if (n < 0) return fail(RDT_EINVAL, "n must be >= 0");
+  if (!aligned16(src) || !aligned16(dst)) return fail(RDT_EINVAL, "buffers must be 16-byte aligned");
+  if (n == 0) return RDT_OK;
+  RDT_CHECK_CUDA(cast_bf16(src, reinterpret_cast<bf16*>(dst), n, static_cast<cudaStream_t>(stream)));
+  return RDT_OK;
+}
+
+rdt_status rdt_device_error(int32_t* code) {
+  if (!code) return fail(RDT_EINVAL, "null pointer");
+  RDT_CHECK_CUDA(cudaDeviceSynchronize());
+  int v = 0;
+  RDT_CHECK_CUDA(cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)));
+  const int zero = 0;
+  RDT_CHECK_CUDA(cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)));
+  *code = v;
+  return RDT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,541 @@
+// Persistent tcgen05 BF16 GEMM for sm_103a with fused epilogues.
+//
+// One CTA per SM (192 threads, ~197 KB shared memory, all 512 TMEM columns):
+//   warp 0  TMA producer: streams 128x64 A and 256x64 B tiles (128-byte
+//           swizzle) into a 4-stage shared-memory ring, one mbarrier per stage;
+//   warp 1  MMA issuer: one elected lane issues tcgen05.mma (M=128, N=256,
+//           K=16) into one of two TMEM accumulators (2 x 256 fp32 columns),
+//           then tcgen05.commit frees the smem stage / signals the epilogue;
+//   warps 2-5 epilogue: tcgen05.ld of their 32-lane quarter (one output row per
+//           thread), fused elementwise work, vectorised global stores; the
+//           accumulator is handed back so the next tile's MMAs overlap.
+// Operands may be K-major ([rows, K], K contiguous) or MN-major ([K, rows]);
+// the transposed cases are expressed through the UMMA descriptors, so no
+// operand is ever transposed in memory. Ragged M/N/K edges are zero-filled by
+// TMA and masked in the epilogue.
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace rdt {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
+constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KB
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t MN_CHUNK_BYTES = 64 * BK * 2;  // one 64(MN) x 64(K) box: 8 KB
+constexpr int GEMM_THREADS = 192;
+constexpr int TMEM_COLS = 512;
+constexpr size_t GEMM_SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+
+struct GemmParams {
+  int M, N, K;
+  int m_tiles, n_tiles, k_blocks;
+  int b_tile_rows;  // K-major B: rows advanced per N tile (256, or 128 for SwiGLU)
+  int b_half_off;   // K-major B: row offset of the second 128-row half
+  Epi epi;
+  int* err;
+};
+
+__device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int& mt, int& nt) {
+  // Groups of 8 M-tiles sweep all N tiles, so a wave of CTAs shares A rows
+  // and B columns in L2.
+  constexpr int G = 8;
+  const int per_group = G * n_tiles;
+  const int g = t / per_group;
+  const int first = g * G;
+  const int gs = min(m_tiles - first, G);
+  const int r = t - g * per_group;
+  mt = first + r % gs;
+  nt = r / gs;
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+// -------------------------------------------------------------- epilogues
+template <int EPI>
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tbase, int row,
+                                              int mt, int nt) {
+  const Epi& e = p.epi;
+  const bool row_ok = row < p.M;
+  uint32_t r[32];
+  if constexpr (EPI == EPI_BF16 || EPI == EPI_F32 || EPI == EPI_F32_RESID) {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      const int col0 = nt * BN + c * 32;
+      if (col0 >= p.N) break;
+      tmem_ld32(tbase + c * 32, r);
+      tmem_ld_wait();
+      if (!row_ok) continue;
+      const bool full = col0 + 32 <= p.N;
+      if constexpr (EPI == EPI_BF16) {
+        bf16* out = reinterpret_cast<bf16*>(e.out) + (int64_t)row * e.ld_out + col0;
+        if (full) {
+          uint4* o4 = reinterpret_cast<uint4*>(out);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1]));
+            v.y = pack_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3]));
+            v.z = pack_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5]));
+            v.w = pack_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7]));
+            o4[j] = v;
+          }
+        } else {
+          #pragma unroll
+          for (int j = 0; j < 32; ++j) if (col0 + j < p.N)
+            out[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
+        }
+      } else {
+        float* out = reinterpret_cast<float*>(e.out) + (int64_t)row * e.ld_out + col0;
+        const float* res =
+            (EPI == EPI_F32_RESID) ? e.resid + (int64_t)row * e.ld_resid + col0 : nullptr;
+        if (full) {
+          float4* o4 = reinterpret_cast<float4*>(out);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            float4 v = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                   __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+            if constexpr (EPI == EPI_F32_RESID) {
+              const float4 q = reinterpret_cast<const float4*>(res)[j];
+              v.x += q.x; v.y += q.y; v.z += q.z; v.w += q.w;
+            }
+            o4[j] = v;
+          }
+        } else {
+          #pragma unroll
+          for (int j = 0; j < 32; ++j) if (col0 + j < p.N) {
+            float v = __uint_as_float(r[j]);
+            if constexpr (EPI == EPI_F32_RESID) v += res[j];
+            out[j] = v;
+          }
+        }
+      }
+    }
+  } else if constexpr (EPI == EPI_SWIGLU) {
+    // accumulator columns [0,128) = gate, [128,256) = up for I-columns nt*128 + [0,128)
+    uint32_t u[32];
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      const int col0 = nt * 128 + c * 32;
+      if (col0 >= e.half) break;
+      tmem_ld32(tbase + c * 32, r);
+      tmem_ld32(tbase + 128 + c * 32, u);
+      tmem_ld_wait();
+      if (!row_ok) continue;
+      bf16* gp = reinterpret_cast<bf16*>(e.out) + (int64_t)row * e.ld_out + col0;
+      bf16* up = gp + e.half;
+      bf16* sp = reinterpret_cast<bf16*>(e.out2) + (int64_t)row * e.ld_out2 + col0;
+      if (col0 + 32 <= e.half) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint4 vg, vu, vs;
+          uint32_t* pg = &vg.x;
+          uint32_t* pu = &vu.x;
+          uint32_t* ps = &vs.x;
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const float g0 = __uint_as_float(r[8 * j + 2 * h]);
+            const float g1 = __uint_as_float(r[8 * j + 2 * h + 1]);
+            const float u0 = __uint_as_float(u[8 * j + 2 * h]);
+            const float u1 = __uint_as_float(u[8 * j + 2 * h + 1]);
+            pg[h] = pack_bf16x2(g0, g1);
+            pu[h] = pack_bf16x2(u0, u1);
+            ps[h] = pack_bf16x2(silu_f(g0) * u0, silu_f(g1) * u1);
+          }
+          reinterpret_cast<uint4*>(gp)[j] = vg;
+          reinterpret_cast<uint4*>(up)[j] = vu;
+          reinterpret_cast<uint4*>(sp)[j] = vs;
+        }
+      } else {
+        #pragma unroll
+        for (int j = 0; j < 32; ++j) if (col0 + j < e.half) {
+          const float g = __uint_as_float(r[j]), uu = __uint_as_float(u[j]);
+          gp[j] = __float2bfloat16_rn(g);
+          up[j] = __float2bfloat16_rn(uu);
+          sp[j] = __float2bfloat16_rn(silu_f(g) * uu);
+        }
+      }
+    }
+  } else if constexpr (EPI == EPI_SWIGLU_BWD) {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      const int col0 = nt * BN + c * 32;
+      if (col0 >= p.N) break;
+      tmem_ld32(tbase + c * 32, r);
+      tmem_ld_wait();
+      if (!row_ok) continue;
+      const bf16* gp = e.aux + (int64_t)row * e.ld_aux + col0;
+      const bf16* up = gp + e.half;
+      bf16* dgp = reinterpret_cast<bf16*>(e.out) + (int64_t)row * e.ld_out + col0;
+      bf16* dup = dgp + e.half;
+      if (col0 + 32 <= p.N) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 vg = reinterpret_cast<const uint4*>(gp)[j];
+          const uint4 vu = reinterpret_cast<const uint4*>(up)[j];
+          const uint32_t* pg = &vg.x;
+          const uint32_t* pu = &vu.x;
+          uint4 odg, odu;
+          uint32_t* pdg = &odg.x;
+          uint32_t* pdu = &odu.x;
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            float dgv[2], duv[2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              const float g = q ? bf16hi(pg[h]) : bf16lo(pg[h]);
+              const float uu = q ? bf16hi(pu[h]) : bf16lo(pu[h]);
+              const float ds = __uint_as_float(r[8 * j + 2 * h + q]);
+              const float sg = 1.0f / (1.0f + __expf(-g));
+              dgv[q] = ds * uu * sg * (1.0f + g * (1.0f - sg));
+              duv[q] = ds * g * sg;
+            }
+            pdg[h] = pack_bf16x2(dgv[0], dgv[1]);
+            pdu[h] = pack_bf16x2(duv[0], duv[1]);
+          }
+          reinterpret_cast<uint4*>(dgp)[j] = odg;
+          reinterpret_cast<uint4*>(dup)[j] = odu;
+        }
+      } else {
+        #pragma unroll
+          for (int j = 0; j < 32; ++j) if (col0 + j < p.N) {
+          const float g = __bfloat162float(gp[j]), uu = __bfloat162float(up[j]);
+          const float ds = __uint_as_float(r[j]);
+          const float sg = 1.0f / (1.0f + __expf(-g));
+          dgp[j] = __float2bfloat16_rn(ds * uu * sg * (1.0f + g * (1.0f - sg)));
+          dup[j] = __float2bfloat16_rn(ds * g * sg);
+        }
+      }
+    }
+  } else if constexpr (EPI == EPI_CE) {
+    float mx = -INFINITY, sum = 0.f;
+    const int tgt = row_ok ? e.targets[row] : -1;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      const int col0 = nt * BN + c * 32;
+      if (col0 >= p.N) break;
+      tmem_ld32(tbase + c * 32, r);
+      tmem_ld_wait();
+      if (!row_ok) continue;
+      const int nvalid = min(32, p.N - col0);
+      float cm = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < nvalid) cm = fmaxf(cm, __uint_as_float(r[j]));
+      const float nm = fmaxf(mx, cm);
+      float acc = sum * __expf(mx - nm);
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < nvalid) acc += __expf(__uint_as_float(r[j]) - nm);
+      mx = nm;
+      sum = acc;
+      if (tgt >= col0 && tgt < col0 + nvalid) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j == tgt - col0) e.tgt_logit[row] = __uint_as_float(r[j]);
+      }
+      bf16* out = reinterpret_cast<bf16*>(e.out) + (int64_t)row * e.ld_out + col0;
+      if (nvalid == 32) {
+        uint4* o4 = reinterpret_cast<uint4*>(out);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1]));
+          v.y = pack_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3]));
+          v.z = pack_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5]));
+          v.w = pack_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7]));
+          o4[j] = v;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < nvalid) out[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
+      }
+    }
+    if (row_ok) e.part[(int64_t)row * e.part_ld + nt] = make_float2(mx, sum);
+  }
+}
+
+// ----------------------------------------------------------------- kernel
+template <int A_MN, int B_MN, int EPI>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
+                const __grid_constant__ CUtensorMap tma_b, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * STAGES;
+  const uint32_t tfull0 = empty0 + 8 * STAGES;
+  const uint32_t tempty0 = tfull0 + 16;
+  const uint32_t drain = tempty0 + 16;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, 128);
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tma_a);
+    tma_prefetch_desc(&tma_b);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int ntiles = p.m_tiles * p.n_tiles;
+  const uint32_t smem_base = smem_u32(smem);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      int stage = 0;
+      uint32_t ph = 0;
+      uint32_t pending = 0, pending_par = 0;  // stages with a load in flight
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        int mt, nt;
+        tile_coords(t, p.m_tiles, p.n_tiles, mt, nt);
+        const int m0 = mt * BM;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(empty0 + 8 * stage, ph ^ 1, p.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full0 + 8 * stage;
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          const uint32_t sa = smem_base + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          const int k0 = kb * BK;
+          if (A_MN) {
+            tma_load_2d(sa, &tma_a, fb, m0, k0);
+            tma_load_2d(sa + MN_CHUNK_BYTES, &tma_a, fb, m0 + 64, k0);
+          } else {
+            tma_load_2d(sa, &tma_a, fb, k0, m0);
+          }
+          if (B_MN) {
+            const int n0 = nt * BN;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * MN_CHUNK_BYTES, &tma_b, fb, n0 + 64 * j, k0);
+          } else {
+            const int r0 = nt * p.b_tile_rows;
+            tma_load_2d(sb, &tma_b, fb, k0, r0);
+            tma_load_2d(sb + B_BYTES / 2, &tma_b, fb, k0, r0 + p.b_half_off);
+          }
+          pending |= 1u << stage;
+          pending_par = (pending_par & ~(1u << stage)) | (ph << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        // do not leave while copies into this CTA's shared memory are in flight
+        for (int s = 0; s < STAGES; ++s)
+          if (pending & (1u << s)) mbar_wait(full0 + 8 * s, (pending_par >> s) & 1u, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ----------------------------------------------------------------- MMA
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+      int stage = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t acc_ph = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        if (!mbar_wait(tempty0 + 8 * acc, acc_ph ^ 1, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(full0 + 8 * stage, ph, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_base + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = A_MN ? sdesc_sw128(sa + k * 2048, MN_CHUNK_BYTES, 1024)
+                                     : sdesc_sw128(sa + k * 32, 16, 1024);
+            const uint64_t bd = B_MN ? sdesc_sw128(sb + k * 2048, MN_CHUNK_BYTES, 1024)
+                                     : sdesc_sw128(sb + k * 32, 16, 1024);
+            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0);
+          }
+          tc_commit(empty0 + 8 * stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            ph ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit(tfull0 + 8 * acc);
+        acc ^= 1;
+        if (acc == 0) acc_ph ^= 1;
+      }
+      // make sure no MMA is still writing TMEM before it is released
+      tc_commit(drain);
+      mbar_wait(drain, 0, nullptr);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int acc = 0;
+    uint32_t acc_ph = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+      int mt, nt;
+      tile_coords(t, p.m_tiles, p.n_tiles, mt, nt);
+      if (!mbar_wait(tfull0 + 8 * acc, acc_ph, p.err)) break;
+      tc_fence_after();
+      const int row = mt * BM + q * 32 + lane;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      epilogue_tile<EPI>(p, tbase, row, mt, nt);
+      tc_fence_before();
+      mbar_arrive(tempty0 + 8 * acc);
+      acc ^= 1;
+      if (acc == 0) acc_ph ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------- host
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+// 2-D bf16 map over [rows, cols] (cols contiguous) with a 64 x box_rows box.
+static bool make_map(CUtensorMap* m, const Mat& x, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(x.cols), static_cast<cuuint64_t>(x.rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(x.ld) * 2};
+  cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t es[2] = {1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x.ptr), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int A_MN, int B_MN, int EPI>
+static cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
+                          cudaStream_t s) {
+  static bool attr_done = false;  // per instantiation; the attribute is per function
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<A_MN, B_MN, EPI>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(GEMM_SMEM));
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const int ntiles = p.m_tiles * p.n_tiles;
+  const int grid = ntiles < num_sms() ? ntiles : num_sms();
+  gemm_kernel<A_MN, B_MN, EPI><<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N, int K,
+                 const Epi& epi, int* err, cudaStream_t s, const char** why) {
+  if (M <= 0 || N <= 0 || K <= 0) {
+    *why = "gemm: empty problem";
+    return cudaErrorInvalidValue;
+  }
+  const bool swiglu = epi.kind == EPI_SWIGLU;
+  if (swiglu && b_mn) {
+    *why = "gemm: SwiGLU epilogue needs a K-major B";
+    return cudaErrorInvalidValue;
+  }
+  if ((A.ld % 8) || (B.ld % 8) || (reinterpret_cast<uintptr_t>(A.ptr) & 15) ||
+      (reinterpret_cast<uintptr_t>(B.ptr) & 15)) {
+    *why = "gemm: operands need 16-byte aligned rows";
+    return cudaErrorInvalidValue;
+  }
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, A, a_mn ? 64 : 128) || !make_map(&tb, B, b_mn ? 64 : 128)) {
+    *why = "gemm: cuTensorMapEncodeTiled failed";
+    return cudaErrorInvalidValue;
+  }
+  GemmParams p;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.m_tiles = (M + BM - 1) / BM;
+  p.n_tiles = swiglu ? (N + 127) / 128 : (N + BN - 1) / BN;
+  p.k_blocks = (K + BK - 1) / BK;
+  p.b_tile_rows = swiglu ? 128 : BN;
+  p.b_half_off = swiglu ? epi.half : 128;
+  p.epi = epi;
+  p.err = err;
+#define RDT_GEMM_CASE(AM, BMJ, E) \
+  if (a_mn == (AM) && b_mn == (BMJ) && epi.kind == (E)) return launch<AM, BMJ, E>(ta, tb, p, s);
+  // forward projections: A K-major, B K-major
+  RDT_GEMM_CASE(0, 0, EPI_BF16)
+  RDT_GEMM_CASE(0, 0, EPI_F32)
+  RDT_GEMM_CASE(0, 0, EPI_F32_RESID)
+  RDT_GEMM_CASE(0, 0, EPI_SWIGLU)
+  RDT_GEMM_CASE(0, 0, EPI_CE)
+  // activation gradients dX = dY W: A K-major, B MN-major
+  RDT_GEMM_CASE(0, 1, EPI_BF16)
+  RDT_GEMM_CASE(0, 1, EPI_F32)
+  RDT_GEMM_CASE(0, 1, EPI_SWIGLU_BWD)
+  // weight gradients dW = dY^T X: A MN-major, B MN-major
+  RDT_GEMM_CASE(1, 1, EPI_F32)
+  RDT_GEMM_CASE(1, 1, EPI_BF16)
+#undef RDT_GEMM_CASE
+  *why = "gemm: unsupported operand-major / epilogue combination";
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace rdt

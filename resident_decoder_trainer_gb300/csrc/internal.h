@@ -1,0 +1,118 @@
+// Internal host-side interface between the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rdt {
+
+using bf16 = __nv_bfloat16;
+
+// Epilogue applied to each 128 x 256 fp32 accumulator tile of the GEMM.
+enum EpiKind : int {
+  EPI_BF16 = 0,        // out(bf16)[r, c] = acc
+  EPI_F32 = 1,         // out(f32)[r, c] = acc
+  EPI_F32_RESID = 2,   // out(f32)[r, c] = resid[r, c] + acc
+  EPI_SWIGLU = 3,      // B = [Wg; Wu]: gu[r, c] = g, gu[r, half + c] = u, out2[r, c] = silu(g) u
+  EPI_SWIGLU_BWD = 4,  // acc = ds: out[r, c] = dg, out[r, half + c] = du from aux = gu
+  EPI_CE = 5,          // acc = logits: out(bf16) = z, part[r, tile] = (max, sum exp), tgt_logit
+};
+
+struct Epi {
+  int kind = EPI_F32;
+  void* out = nullptr;
+  int64_t ld_out = 0;
+  const float* resid = nullptr;
+  int64_t ld_resid = 0;
+  void* out2 = nullptr;
+  int64_t ld_out2 = 0;
+  const bf16* aux = nullptr;
+  int64_t ld_aux = 0;
+  int half = 0;
+  float2* part = nullptr;
+  int part_ld = 0;
+  const int32_t* targets = nullptr;
+  float* tgt_logit = nullptr;
+};
+
+// A bf16 row-major matrix in global memory.
+struct Mat {
+  const void* ptr;
+  int64_t rows, cols, ld;
+};
+
+// C[M, N] = A' B'^T over K, where
+//   A' = A        ([M, K], K contiguous) when !a_mn, else A^T with A given as [K, M];
+//   B' = B        ([N, K], K contiguous) when !b_mn, else B^T with B given as [K, N].
+// For EPI_SWIGLU, B is the stacked [2*half, K] matrix and N = half.
+// Returns cudaSuccess or an error; on a host-side rejection *why is set.
+cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N, int K,
+                 const Epi& epi, int* err, cudaStream_t s, const char** why);
+
+// Number of 256-wide N tiles the CE epilogue produces per row (partials width).
+inline int gemm_n_tiles(int N) { return (N + 255) / 256; }
+
+int num_sms();
+
+// Upper bound on the row count of any gain-gradient partials buffer.
+constexpr int kMaxPartialRows = 512;
+// Upper bound on the per-block partials of the squared sum.
+constexpr int kMaxSqSumPartials = 4096;
+
+// ------------------------------------------------------------ elementwise
+cudaError_t rmsnorm_fwd(const float* x, const float* gamma, bf16* y, float* rstd, int T, int H,
+                        float eps, cudaStream_t s);
+// dx = rstd*(dy*g - xhat*mean(dy*g*xhat)) + resid (resid may be null);
+// dx_bf16 optional; dgamma partials [nblk, H] then reduced into dgamma.
+cudaError_t rmsnorm_bwd(const float* dy, const float* x, const float* rstd, const float* gamma,
+                        const float* resid, float* dx, bf16* dx_bf16, float* dgamma,
+                        float* partials, int T, int H, cudaStream_t s);
+int rmsnorm_bwd_partial_rows(int T);
+
+cudaError_t rope_table(float* cs, int S, int d, float theta, cudaStream_t s);
+cudaError_t qknorm_rope_fwd(const bf16* qkv, int64_t ld_qkv, bf16* q_out, bf16* k_out,
+                            float* rstd_q, float* rstd_k, const float* gq, const float* gk,
+                            const float* cs, int T, int S, int nh, int nkv, int d, float eps,
+                            cudaStream_t s);
+// dg_qk: 2*d floats, q-gain gradient then k-gain gradient.
+cudaError_t qknorm_rope_bwd(const float* dq, const float* dk, const bf16* qkv, int64_t ld_qkv,
+                            const float* rstd_q, const float* rstd_k, const float* gq,
+                            const float* gk, const float* cs, bf16* dqkv, float* dg_qk,
+                            float* partials, int T, int S, int nh, int nkv, int d,
+                            cudaStream_t s);
+int qknorm_bwd_partial_rows(int T, int heads);
+
+cudaError_t cast_bf16(const float* src, bf16* dst, int64_t n, cudaStream_t s);
+
+cudaError_t ce_finalize(const float2* part, int part_ld, int ntiles, const float* tgt_logit,
+                        float* lse, float* loss, int T, cudaStream_t s);
+cudaError_t ce_grad(bf16* z, const float* lse, const int32_t* targets, float scale, int T, int V,
+                    cudaStream_t s);
+
+cudaError_t sq_sum(const float* const* bufs, const int64_t* lens, int nbuf, double* out,
+                   double* partials, int max_partials, cudaStream_t s);
+cudaError_t clip_scale(const double* sumsq, float max_norm, float* scale, int32_t* nonfinite,
+                       cudaStream_t s);
+cudaError_t adamw(float* w, const float* g, float* m, float* v, int64_t n, const float* scale,
+                  const int32_t* skip, float lr, float b1, float b2, float eps, float wd,
+                  float bc1, float bc2, bf16* wb, cudaStream_t s);
+
+// ---------------------------------------------------------------- attention
+// q [T, ldq] (head h at column h*d), k/v [T, ldk/ldv] (kv head g at g*d),
+// o [T, nh*d] bf16, lse [B, nh, S] fp32 (natural log).
+cudaError_t attn_fwd(const bf16* q, int64_t ldq, const bf16* k, int64_t ldk, const bf16* v,
+                     int64_t ldv, bf16* o, float* lse, int B, int S, int nh, int nkv, int d,
+                     cudaStream_t s);
+// D[b, h, s] = sum_d dO * O
+cudaError_t attn_bwd_pre(const bf16* o, const bf16* dout, float* D, int B, int S, int nh, int d,
+                         cudaStream_t s);
+// dq (fp32 [T, nh*d], must be zeroed; accumulated), dk fp32 [T, nkv*d],
+// dv bf16 written at dv + t*lddv + g*d.
+cudaError_t attn_bwd(const bf16* q, int64_t ldq, const bf16* k, int64_t ldk, const bf16* v,
+                     int64_t ldv, const bf16* dout, const float* lse, const float* D, float* dq,
+                     float* dk, bf16* dv, int64_t lddv, int B, int S, int nh, int nkv, int d,
+                     cudaStream_t s);
+
+}  // namespace rdt

@@ -1,0 +1,204 @@
+"""Thin ctypes binding of librdt.so (include/rdt.h): argument marshalling only.
+
+Every function takes device pointers as torch tensors (or raw ints) and the
+current torch CUDA stream, calls the C entry point of the same name and
+raises ``RdtError`` with the library's message on a non-zero status. No
+computation happens here; if librdt.so is missing the import fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "librdt.so")
+
+RDT_OK, RDT_EINVAL, RDT_ECUDA, RDT_ETIMEOUT, RDT_ENONFINITE = 0, 1, 2, 3, 4
+TENSOR_NAMES = ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "g_attn", "g_ffn", "g_q", "g_k")
+
+EXPORTS = (
+    "rdt_check_config", "rdt_block_param_count", "rdt_block_param_offsets",
+    "rdt_block_saved_bytes", "rdt_block_workspace_bytes", "rdt_head_workspace_bytes",
+    "rdt_sq_sum_workspace_bytes", "rdt_block_forward", "rdt_block_backward",
+    "rdt_fused_cross_entropy", "rdt_sq_sum", "rdt_clip_scale", "rdt_adamw_step",
+    "rdt_gemm", "rdt_cast_bf16", "rdt_last_error", "rdt_device_error",
+)
+
+
+class RdtError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(f"librdt status {status}: {msg}")
+        self.status = status
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("n_heads", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("intermediate", ctypes.c_int32), ("vocab", ctypes.c_int32),
+                ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float)]
+
+    @classmethod
+    def from_shape(cls, s) -> "Config":
+        return cls(s.hidden, s.n_heads, s.n_kv_heads, s.head_dim, s.intermediate, s.vocab,
+                   s.eps, s.theta)
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "`python -m resident_decoder_trainer_gb300.build` (needs nvcc)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, I64, F32, SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                            ctypes.c_size_t)
+    CP = ctypes.POINTER(Config)
+    sig = {
+        "rdt_check_config": (I32, [CP]),
+        "rdt_block_param_count": (I64, [CP]),
+        "rdt_block_param_offsets": (I32, [CP, P, P]),
+        "rdt_block_saved_bytes": (SZ, [CP, I32, I32]),
+        "rdt_block_workspace_bytes": (SZ, [CP, I32, I32]),
+        "rdt_head_workspace_bytes": (SZ, [CP, I32]),
+        "rdt_sq_sum_workspace_bytes": (SZ, []),
+        "rdt_block_forward": (I32, [CP, I32, I32, P, P, P, P, P, SZ, P, SZ, P]),
+        "rdt_block_backward": (I32, [CP, I32, I32, P, P, P, P, SZ, P, P, P, P, SZ, P]),
+        "rdt_fused_cross_entropy": (I32, [CP, I32, P, P, P, P, F32, P, P, P, P, P, SZ, P]),
+        "rdt_sq_sum": (I32, [P, P, I32, P, P, SZ, P]),
+        "rdt_clip_scale": (I32, [P, F32, P, P, P]),
+        "rdt_adamw_step": (I32, [P, P, P, P, I64, P, P, I32, F32, F32, F32, F32, F32, P, P]),
+        "rdt_gemm": (I32, [P, I32, I64, P, I32, I64, I32, I32, I32, P, I64, P]),
+        "rdt_cast_bf16": (I32, [P, P, I64, P]),
+        "rdt_last_error": (ctypes.c_char_p, []),
+        "rdt_device_error": (I32, [P]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        _lib = _load()
+    return _lib
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream=None) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(status: int):
+    if status != RDT_OK:
+        raise RdtError(status, lib().rdt_last_error().decode())
+
+
+# ------------------------------------------------------------------ layout
+def check_config(cfg: Config):
+    _check(lib().rdt_check_config(ctypes.byref(cfg)))
+
+
+def block_param_count(cfg: Config) -> int:
+    n = lib().rdt_block_param_count(ctypes.byref(cfg))
+    if n < 0:
+        check_config(cfg)
+    return n
+
+
+def block_param_offsets(cfg: Config) -> dict[str, tuple[int, int]]:
+    off = (ctypes.c_int64 * len(TENSOR_NAMES))()
+    cnt = (ctypes.c_int64 * len(TENSOR_NAMES))()
+    _check(lib().rdt_block_param_offsets(ctypes.byref(cfg), off, cnt))
+    return {n: (off[i], cnt[i]) for i, n in enumerate(TENSOR_NAMES)}
+
+
+def block_saved_bytes(cfg: Config, batch: int, seq: int) -> int:
+    return lib().rdt_block_saved_bytes(ctypes.byref(cfg), batch, seq)
+
+
+def block_workspace_bytes(cfg: Config, batch: int, seq: int) -> int:
+    return lib().rdt_block_workspace_bytes(ctypes.byref(cfg), batch, seq)
+
+
+def head_workspace_bytes(cfg: Config, tokens: int) -> int:
+    return lib().rdt_head_workspace_bytes(ctypes.byref(cfg), tokens)
+
+
+def sq_sum_workspace_bytes() -> int:
+    return lib().rdt_sq_sum_workspace_bytes()
+
+
+# ------------------------------------------------------------------- calls
+def block_forward(cfg, batch, seq, w, w_bf16, x, y, saved, ws, stream=None):
+    _check(lib().rdt_block_forward(ctypes.byref(cfg), batch, seq, _ptr(w), _ptr(w_bf16), _ptr(x),
+                                   _ptr(y), _ptr(saved), saved.numel() * saved.element_size(),
+                                   _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def block_backward(cfg, batch, seq, w, w_bf16, x, saved, dy, dx, grads, ws, stream=None):
+    _check(lib().rdt_block_backward(ctypes.byref(cfg), batch, seq, _ptr(w), _ptr(w_bf16), _ptr(x),
+                                    _ptr(saved), saved.numel() * saved.element_size(), _ptr(dy),
+                                    _ptr(dx), _ptr(grads), _ptr(ws),
+                                    ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def fused_cross_entropy(cfg, tokens, h, gamma_f, w_lm, targets, loss_scale, loss_partials, dh,
+                        dgamma_f, dw_lm, ws, stream=None):
+    _check(lib().rdt_fused_cross_entropy(ctypes.byref(cfg), tokens, _ptr(h), _ptr(gamma_f),
+                                         _ptr(w_lm), _ptr(targets), float(loss_scale),
+                                         _ptr(loss_partials), _ptr(dh), _ptr(dgamma_f),
+                                         _ptr(dw_lm), _ptr(ws), ws.numel() * ws.element_size(),
+                                         _stream(stream)))
+
+
+def sq_sum(bufs, sumsq, ws, stream=None):
+    n = len(bufs)
+    ptrs = (ctypes.c_void_p * n)(*[_ptr(b) for b in bufs])
+    lens = (ctypes.c_int64 * n)(*[b.numel() for b in bufs])
+    _check(lib().rdt_sq_sum(ptrs, lens, n, _ptr(sumsq), _ptr(ws),
+                            ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def clip_scale(sumsq, max_norm, scale, nonfinite=None, stream=None):
+    _check(lib().rdt_clip_scale(_ptr(sumsq), float(max_norm), _ptr(scale), _ptr(nonfinite),
+                                _stream(stream)))
+
+
+def adamw_step(w, g, m, v, step, lr, beta1, beta2, eps, weight_decay, scale=None, skip=None,
+               w_bf16=None, n=None, stream=None):
+    n = w.numel() if n is None else n
+    _check(lib().rdt_adamw_step(_ptr(w), _ptr(g), _ptr(m), _ptr(v), n, _ptr(scale), _ptr(skip),
+                                int(step), float(lr), float(beta1), float(beta2), float(eps),
+                                float(weight_decay), _ptr(w_bf16), _stream(stream)))
+
+
+def gemm(a, a_mn, b, b_mn, M, N, K, c, stream=None):
+    """c[M, N] = a' b'^T (see include/rdt.h); a, b bf16 2-D, c fp32 2-D."""
+    _check(lib().rdt_gemm(_ptr(a), int(a_mn), a.stride(0), _ptr(b), int(b_mn), b.stride(0), M, N,
+                          K, _ptr(c), c.stride(0), _stream(stream)))
+
+
+def cast_bf16(src, dst, n=None, stream=None):
+    n = src.numel() if n is None else n
+    _check(lib().rdt_cast_bf16(_ptr(src), _ptr(dst), n, _stream(stream)))
+
+
+def device_error() -> int:
+    code = ctypes.c_int32(0)
+    _check(lib().rdt_device_error(ctypes.byref(code)))
+    return code.value

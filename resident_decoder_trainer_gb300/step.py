@@ -1,0 +1,164 @@
+"""One full training step of a decoder stack, driven through librdt.so.
+
+``DecoderTrainer`` owns the device-resident state in a few flat buffers:
+
+* ``w``  fp32 master weights of every trainable tensor, laid out as
+  [block 0 | block 1 | ... | block L-1 | final-norm gain | LM head], each
+  block in the library's block layout (``rdt.block_param_offsets``);
+* ``wb`` the bf16 shadow of ``w`` (GEMM operands), refreshed by AdamW;
+* ``g``, ``m``, ``v`` the gradients and AdamW moments, same layout.
+
+A step is: every block forward (saving its activations), the fused final
+norm + LM head + cross-entropy (forward and backward), every block backward
+in reverse, one squared sum over all gradients, the clip scale, and one AdamW
+launch over all parameters. The loss partials stay on the device until the
+caller reads them. Every launch is a librdt kernel; torch is used only to
+allocate buffers and for the stream.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import rdt
+from .synth import OPTIM, DecoderShape
+
+
+def _align(n: int, a: int = 64) -> int:
+    return (n + a - 1) // a * a
+
+
+class DecoderTrainer:
+    def __init__(self, shape: DecoderShape, device="cuda", optim=None):
+        self.shape = s = shape
+        self.device = torch.device(device)
+        self.optim = dict(OPTIM if optim is None else optim)
+        self.cfg = rdt.Config.from_shape(s)
+        rdt.check_config(self.cfg)
+        self.per_block = rdt.block_param_count(self.cfg)
+        self.offsets = rdt.block_param_offsets(self.cfg)
+        L, H, V, T = s.layers, s.hidden, s.vocab, s.tokens
+        self.off_gf = L * self.per_block
+        self.off_lm = self.off_gf + _align(H)
+        self.n_params = self.off_lm + V * H
+        dev = self.device
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.w = torch.zeros(self.n_params, **f32)
+        self.wb = torch.zeros(self.n_params, dtype=torch.bfloat16, device=dev)
+        self.g = torch.zeros(self.n_params, **f32)
+        self.m = torch.zeros(self.n_params, **f32)
+        self.v = torch.zeros(self.n_params, **f32)
+        self.saved_bytes = rdt.block_saved_bytes(self.cfg, s.batch, s.seq)
+        self.saved = torch.empty(L * self.saved_bytes, dtype=torch.uint8, device=dev)
+        self.h = torch.empty((L + 1, T, H), **f32)
+        self.dh = torch.empty((T, H), **f32)
+        self.block_ws = torch.empty(rdt.block_workspace_bytes(self.cfg, s.batch, s.seq),
+                                    dtype=torch.uint8, device=dev)
+        self.head_ws = torch.empty(rdt.head_workspace_bytes(self.cfg, T), dtype=torch.uint8,
+                                   device=dev)
+        self.sq_ws = torch.empty(rdt.sq_sum_workspace_bytes(), dtype=torch.uint8, device=dev)
+        self.sumsq = torch.zeros(1, dtype=torch.float64, device=dev)
+        self.scale = torch.ones(1, **f32)
+        self.nonfinite = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.loss_partials = torch.zeros(T, **f32)
+        self.targets = torch.zeros(T, dtype=torch.int32, device=dev)
+        self.step_count = 0
+
+    # -------------------------------------------------------------- views
+    def block_slice(self, buf, layer):
+        return buf[layer * self.per_block:(layer + 1) * self.per_block]
+
+    def tensor(self, buf, layer, name):
+        """View of one trainable tensor inside a flat buffer (shape [out, in] or [n])."""
+        s = self.shape
+        if layer == "head":
+            if name == "g_final":
+                return buf[self.off_gf:self.off_gf + s.hidden]
+            if name == "w_lm":
+                return buf[self.off_lm:self.off_lm + s.vocab * s.hidden].view(s.vocab, s.hidden)
+            raise KeyError(name)
+        off, cnt = self.offsets[name]
+        base = layer * self.per_block + off
+        flat = buf[base:base + cnt]
+        from .synth import block_shapes
+        return flat.view(block_shapes(s)[name])
+
+    def saved_slice(self, layer):
+        return self.saved[layer * self.saved_bytes:(layer + 1) * self.saved_bytes]
+
+    # ------------------------------------------------------------- set-up
+    def load(self, blocks, head):
+        """Copy parameter dicts (from ``synth``) into the flat masters and cast
+        the bf16 shadow."""
+        for li, p in enumerate(blocks):
+            for name, t in p.items():
+                self.tensor(self.w, li, name).copy_(t)
+        for name, t in head.items():
+            self.tensor(self.w, "head", name).copy_(t)
+        self.refresh_shadow()
+
+    def init_random(self, seed=0, std=0.02):
+        """Random-init on the device: matrices ~N(0, std), gains 1 (same
+        distribution as ``synth``, drawn by a device generator)."""
+        gen = torch.Generator(device=self.device)
+        gen.manual_seed(seed)
+        for li in range(self.shape.layers):
+            for name in rdt.TENSOR_NAMES:
+                t = self.tensor(self.w, li, name)
+                if name.startswith("g_"):
+                    t.fill_(1.0)
+                else:
+                    t.normal_(0.0, std, generator=gen)
+        self.tensor(self.w, "head", "g_final").fill_(1.0)
+        self.tensor(self.w, "head", "w_lm").normal_(0.0, std, generator=gen)
+        self.refresh_shadow()
+
+    def refresh_shadow(self):
+        rdt.cast_bf16(self.w, self.wb)
+
+    def reset_optimizer(self):
+        self.m.zero_()
+        self.v.zero_()
+        self.step_count = 0
+
+    # --------------------------------------------------------------- step
+    def forward_backward(self, x=None, targets=None):
+        """Forward, fused CE and full backward; gradients land in ``self.g``.
+        x [T, H] fp32 and targets [T] int32 on the device (or already copied
+        into ``self.h[0]`` / ``self.targets`` when None)."""
+        s, cfg = self.shape, self.cfg
+        if x is not None:
+            self.h[0].copy_(x)
+        if targets is not None:
+            self.targets.copy_(targets)
+        for li in range(s.layers):
+            rdt.block_forward(cfg, s.batch, s.seq, self.block_slice(self.w, li),
+                              self.block_slice(self.wb, li), self.h[li], self.h[li + 1],
+                              self.saved_slice(li), self.block_ws)
+        T = s.tokens
+        rdt.fused_cross_entropy(cfg, T, self.h[s.layers], self.tensor(self.w, "head", "g_final"),
+                                self.tensor(self.wb, "head", "w_lm"), self.targets, 1.0 / T,
+                                self.loss_partials, self.dh,
+                                self.tensor(self.g, "head", "g_final"),
+                                self.tensor(self.g, "head", "w_lm"), self.head_ws)
+        for li in reversed(range(s.layers)):
+            rdt.block_backward(cfg, s.batch, s.seq, self.block_slice(self.w, li),
+                               self.block_slice(self.wb, li), self.h[li], self.saved_slice(li),
+                               self.dh, self.dh, self.block_slice(self.g, li), self.block_ws)
+        return self.loss_partials
+
+    def clip_and_update(self):
+        """Global-norm clip from the squared sum of every gradient, then one
+        AdamW over all parameters (skipped on a non-finite norm)."""
+        o = self.optim
+        rdt.sq_sum([self.g], self.sumsq, self.sq_ws)
+        rdt.clip_scale(self.sumsq, o["max_norm"], self.scale, self.nonfinite)
+        self.step_count += 1
+        rdt.adamw_step(self.w, self.g, self.m, self.v, self.step_count, o["lr"], o["beta1"],
+                       o["beta2"], o["eps"], o["weight_decay"], scale=self.scale,
+                       skip=self.nonfinite, w_bf16=self.wb)
+
+    def train_step(self, x=None, targets=None):
+        """One full step; returns the device tensor of per-token loss partials."""
+        self.forward_backward(x, targets)
+        self.clip_and_update()
+        return self.loss_partials

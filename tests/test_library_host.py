@@ -1,0 +1,108 @@
+"""Host-side checks of librdt.so that need no GPU: it loads, exports every
+symbol include/rdt.h declares, and its layout / size / validation logic is
+right. (No compute call is made here.)"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from resident_decoder_trainer_gb300 import build, rdt, synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return rdt.lib()
+
+
+def _declared_functions():
+    with open(os.path.join(ROOT, "include", "rdt.h")) as fh:
+        text = fh.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rdt_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/rdt.h but not exported"
+    assert set(names) == set(rdt.EXPORTS)
+
+
+def test_block_layout_matches_tensor_shapes(lib):
+    for key in ("tiny", "small", "q4b_block"):
+        s = synth.WORKLOADS[key]
+        cfg = rdt.Config.from_shape(s)
+        offs = rdt.block_param_offsets(cfg)
+        shapes = synth.block_shapes(s)
+        pos = 0
+        for name in rdt.TENSOR_NAMES:
+            off, cnt = offs[name]
+            assert off == pos and off % 16 == 0
+            n = 1
+            for d in shapes[name]:
+                n *= d
+            assert cnt == n
+            pos += cnt
+        assert rdt.block_param_count(cfg) == pos
+    q4b = rdt.Config.from_shape(synth.WORKLOADS["q4b_block"])
+    assert rdt.block_param_count(q4b) == 100_930_816  # 100.93 M per Qwen3-4B block
+
+
+def test_sizes_are_positive_and_aligned(lib):
+    s = synth.WORKLOADS["q4b_full"]
+    cfg = rdt.Config.from_shape(s)
+    for n in (rdt.block_saved_bytes(cfg, s.batch, s.seq),
+              rdt.block_workspace_bytes(cfg, s.batch, s.seq),
+              rdt.head_workspace_bytes(cfg, s.tokens)):
+        assert n > 0 and n % 256 == 0
+    # the head keeps the bf16 logits of every token in scratch
+    assert rdt.head_workspace_bytes(cfg, s.tokens) > 2 * s.tokens * s.vocab
+    assert rdt.sq_sum_workspace_bytes() >= 8
+
+
+@pytest.mark.parametrize("field,value", [("hidden", 40), ("hidden", 8192), ("head_dim", 48),
+                                         ("n_kv_heads", 3), ("intermediate", 100),
+                                         ("vocab", 1000)])
+def test_bad_configs_are_rejected(lib, field, value):
+    cfg = rdt.Config.from_shape(synth.WORKLOADS["tiny"])
+    setattr(cfg, field, value)
+    with pytest.raises(rdt.RdtError) as ei:
+        rdt.check_config(cfg)
+    assert ei.value.status == rdt.RDT_EINVAL
+    assert lib.rdt_block_param_count(ctypes.byref(cfg)) == -1
+    assert rdt.block_saved_bytes(cfg, 1, 32) == 0
+
+
+def test_null_and_misaligned_arguments_fail_before_any_launch(lib):
+    cfg = rdt.Config.from_shape(synth.WORKLOADS["tiny"])
+    P = ctypes.c_void_p
+    st = lib.rdt_block_forward(ctypes.byref(cfg), 1, 32, None, None, None, None, None, 0, None,
+                               0, None)
+    assert st == rdt.RDT_EINVAL and b"null" in lib.rdt_last_error()
+    st = lib.rdt_adamw_step(P(16), P(16), P(16), P(16), 4, None, None, 0, 1e-3, 0.9, 0.95, 1e-8,
+                            0.0, None, None)
+    assert st == rdt.RDT_EINVAL and b"step" in lib.rdt_last_error()
+    st = lib.rdt_adamw_step(P(18), P(16), P(16), P(16), 4, None, None, 1, 1e-3, 0.9, 0.95, 1e-8,
+                            0.0, None, None)
+    assert st == rdt.RDT_EINVAL and b"aligned" in lib.rdt_last_error()
+    st = lib.rdt_clip_scale(P(16), ctypes.c_float(0.0), P(16), None, None)
+    assert st == rdt.RDT_EINVAL
+    st = lib.rdt_gemm(P(16), 0, 12, P(16), 0, 16, 8, 8, 8, P(16), 8, None)
+    assert st == rdt.RDT_EINVAL
+
+
+def test_product_path_has_no_oracle_or_cpu_fallback():
+    pkg = os.path.join(ROOT, "resident_decoder_trainer_gb300")
+    for fn in os.listdir(pkg):
+        if fn.endswith(".py"):
+            with open(os.path.join(pkg, fn)) as fh:
+                src = fh.read()
+            assert not re.search(r"^\s*(import|from)\s+oracle", src, flags=re.M), fn
+    with open(os.path.join(pkg, "rdt.py")) as fh:
+        src = fh.read()
+    assert "raise ImportError" in src  # a missing library fails loudly
