@@ -1,0 +1,384 @@
+#!/usr/bin/env python
+"""Training-step throughput of the GB300 decoder trainer (librdt.so).
+
+One step = forward of every block, fused final norm + LM head + cross-entropy
+(forward and backward), backward of every block, the squared-sum global-norm
+clip and AdamW over every fp32 master weight, on synthetic inputs already
+resident in HBM. Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload q4b_full]
+  python bench.py --impl reference ...   # the FP64 CPU oracle on host cores
+
+Multi-GPU (torchrun): every rank runs an independent replica of the whole
+step (the path has no data-path collective); timing is the max over ranks and
+`value` counts the tokens of all ranks ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "train tokens/s (fwd+bwd+clip+AdamW) at Qwen3-4B shape; % of BF16/HBM roofline"
+UNIT = "tokens/s"
+
+# DRAM traffic per tensor-core GEMM launch, from `ncu` (dram__bytes_read.sum +
+# dram__bytes_write.sum) averaged over the step's launch mix, and the source
+# it was measured on; reported only while gemm.cu is unchanged.
+GEMM_TRAFFIC_BYTES = None
+GEMM_TRAFFIC_SRC_SHA = None
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["rdt", "reference"], default="rdt")
+    ap.add_argument("--workload", default="q4b_full")
+    ap.add_argument("--layers", type=int, default=None, help="override the layer count")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def workload_config(shape, name):
+    return {
+        "workload": (f"{name}: {shape.layers} Qwen3-style blocks (hidden {shape.hidden}, "
+                     f"{shape.n_heads}/{shape.n_kv_heads} heads, head_dim {shape.head_dim}, "
+                     f"SwiGLU {shape.intermediate}) + vocab-{shape.vocab} LM head, "
+                     f"batch {shape.batch} x seq {shape.seq}"),
+        "tokens_per_step": shape.tokens,
+        "layers": shape.layers,
+        "global_batch": shape.batch,
+        "seq_len": shape.seq,
+        "params": None,
+        "optimizer": "global-norm clip 1.0 + AdamW (fp32 master, m, v)",
+        "l2": "inputs larger than L2: each step streams ~150 GB of weights/grads/moments",
+        "parallelism": "replicas",
+    }
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            pk = json.load(fh)
+        return pk, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, \
+            "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+def start_clock_sampler(device_index):
+    fd, path = tempfile.mkstemp(suffix=".csv")
+    os.close(fd)
+    q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    try:
+        fh = open(path, "w")
+        proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                 "-i", str(device_index), "-lms", "200"], stdout=fh,
+                                stderr=subprocess.DEVNULL)
+        return proc, fh, path
+    except Exception:
+        return None, None, path
+
+
+def stop_clock_sampler(handle):
+    proc, fh, path = handle
+    if proc is None:
+        return None
+    proc.terminate()
+    try:
+        proc.wait(timeout=5)
+    except Exception:
+        proc.kill()
+    fh.close()
+    rows = []
+    with open(path) as f:
+        for r in csv.reader(f):
+            if len(r) >= 9:
+                rows.append([c.strip() for c in r])
+    os.unlink(path)
+    if not rows:
+        return None
+    sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+    mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+    load = [s for s in sm if mx and s > 0.3 * max(mx)] or sm
+    return {"sm_mhz": statistics.median(load) if load else None,
+            "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------- CPU oracle
+class OracleSample:
+    """The FP64 oracle timed on a bounded sample of one step, scaled to the
+    whole step: one block forward+backward on one sequence of `seq_tokens`
+    tokens (x layers), the final norm + LM head + CE forward and backward on
+    `head_tokens` tokens (x tokens per step), and clip + AdamW on `opt_params`
+    parameters (x total parameters). Inputs are drawn once (seeded)."""
+
+    def __init__(self, shape, seq_tokens=512, head_tokens=256, opt_params=1 << 24, seed=0):
+        import numpy as np
+        import torch
+        from oracle import model as om
+        from resident_decoder_trainer_gb300 import synth
+
+        self.om, self.shape = om, shape
+        self.seq_tokens, self.head_tokens, self.opt_params = seq_tokens, head_tokens, opt_params
+        self.s_blk = shape.replace(layers=1, batch=1, seq=seq_tokens)
+        blk, x, dy = synth.make_block_inputs(self.s_blk, seed)
+        self.blk = {k: om._f64(v) for k, v in blk.items()}
+        self.x, self.dy = om._f64(x), om._f64(dy)
+        g = torch.Generator().manual_seed(seed + 1)
+        self.h = om._f64(torch.randn(head_tokens, shape.hidden, generator=g))
+        self.wl = om._f64(0.02 * torch.randn(shape.vocab, shape.hidden, generator=g))
+        self.gf = np.ones(shape.hidden)
+        self.tg = np.random.default_rng(seed).integers(0, shape.vocab, head_tokens)
+        rng = np.random.default_rng(seed)
+        self.w = rng.standard_normal(opt_params)
+        self.gr = rng.standard_normal(opt_params) * 1e-3
+        self.m = np.zeros(opt_params)
+        self.v = np.zeros(opt_params)
+        self.n_params = shape.layers * sum(
+            int(np.prod(sh)) for sh in synth.block_shapes(shape).values()) \
+            + shape.hidden + shape.vocab * shape.hidden
+
+    def run(self):
+        om, shape = self.om, self.shape
+        o = {"lr": 1e-3, "beta1": 0.9, "beta2": 0.95, "eps": 1e-8, "weight_decay": 0.1}
+        t0 = time.perf_counter()
+        _, cache = om.block_forward(self.blk, self.x, self.s_blk)
+        om.block_backward(cache, self.dy, self.s_blk)
+        t1 = time.perf_counter()
+        om.head_forward_backward(self.h, self.gf, self.wl, self.tg, shape)
+        t2 = time.perf_counter()
+        sc, _, _ = om.clip_scale([om.squared_sum(self.gr)], 1.0)
+        om.adamw(self.w, self.gr, self.m, self.v, 1, o["lr"], o["beta1"], o["beta2"], o["eps"],
+                 o["weight_decay"], sc)
+        t3 = time.perf_counter()
+        step_s = (shape.tokens * (shape.layers * (t1 - t0) / self.seq_tokens
+                                  + (t2 - t1) / self.head_tokens)
+                  + (t3 - t2) * self.n_params / self.opt_params)
+        try:
+            from threadpoolctl import threadpool_info
+            cores = max(int(i.get("num_threads", 1)) for i in threadpool_info()) or os.cpu_count()
+        except Exception:
+            cores = os.cpu_count()
+        sample = (f"FP64 oracle: 1 block fwd+bwd on 1x{self.seq_tokens} tokens "
+                  f"(x{shape.layers} layers), head+CE fwd+bwd on {self.head_tokens} tokens, "
+                  f"clip+AdamW on {self.opt_params} params; scaled to {shape.tokens} tokens "
+                  f"and {self.n_params} params per step")
+        return {"value": round(shape.tokens / step_s, 3), "unit": UNIT, "cores": cores,
+                "kind": "oracle", "sample": sample, "sample_seconds": round(t3 - t0, 2)}
+
+
+# ------------------------------------------------------------- GPU arm
+def run_rdt(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from resident_decoder_trainer_gb300 import build, rdt, synth
+    from resident_decoder_trainer_gb300.step import DecoderTrainer
+
+    build.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    shape = synth.WORKLOADS[args.workload]
+    if args.layers:
+        shape = shape.replace(layers=args.layers)
+    T = shape.tokens
+    tr = DecoderTrainer(shape, device=dev)
+    tr.init_random(seed=1234 + rank)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4321 + rank)
+    nb = 4
+    xs = [torch.randn(T, shape.hidden, device=dev, generator=gen) for _ in range(nb)]
+    tgs = [torch.randint(0, shape.vocab, (T,), device=dev, generator=gen, dtype=torch.int32)
+           for _ in range(nb)]
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    first_loss = float(tr.train_step(xs[0], tgs[0]).mean())
+    for i in range(1, args.warmup):
+        tr.train_step(xs[i % nb], tgs[i % nb])
+    gemms_per_step = 12 * shape.layers + 3
+    timer = rdt.GemmTimer(gemms_per_step * args.steps)
+    barrier()
+    clk = start_clock_sampler(local_rank)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l0 = rdt.launch_count()
+    with timer:
+        e0.record(stream)
+        for i in range(args.steps):
+            tr.train_step(xs[i % nb], tgs[i % nb])
+        e1.record(stream)
+        barrier()
+    launches = rdt.launch_count() - l0
+    clocks = stop_clock_sampler(clk)
+    dev_ms = e0.elapsed_time(e1)
+    last_loss = float(tr.loss_partials.mean())
+    t = torch.tensor([dev_ms], device=dev, dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    max_ms = float(t.item())
+    value = world * T * args.steps / (max_ms / 1e3)
+
+    res = timer.results()
+    gemm_flops = sum(f for f, _ in res)
+    gemm_ms = sum(ms for _, ms in res)
+    peaks, peak_kind = load_peaks()
+    peak_tf = float(peaks.get("bf16_tflops_sustained") or peaks.get("bf16_tflops"))
+    achieved = gemm_flops / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else None
+    n_launch = len(res)
+    traffic = None
+    if GEMM_TRAFFIC_BYTES is not None:
+        import hashlib
+        with open(os.path.join(ROOT, "resident_decoder_trainer_gb300", "csrc", "gemm.cu"),
+                  "rb") as fh:
+            if hashlib.sha256(fh.read()).hexdigest()[:16] == GEMM_TRAFFIC_SRC_SHA:
+                traffic = GEMM_TRAFFIC_BYTES
+    roofline = {
+        "kernel": "gemm_kernel (tcgen05 BF16, TMEM fp32 accumulators, TMA)",
+        "bound": "tensor", "achieved": round(achieved, 1) if achieved else None,
+        "peak": peak_tf, "unit": "TFLOP/s",
+        "frac": round(achieved / peak_tf, 4) if achieved else None,
+        "peak_source": f"bf16_tflops_sustained of {peak_kind}",
+        "traffic": traffic,
+        "launches_timed": n_launch,
+        "flops_per_launch": gemm_flops / max(n_launch, 1),
+        "ms_per_launch": gemm_ms / max(n_launch, 1),
+        "gemm_share_of_step": round(gemm_ms / max_ms, 4) if max_ms else None,
+    }
+    step_flops = algorithmic_flops(shape)
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (device-generated N(0,1) hidden states, uniform ids;"
+                                  " N(0,0.02) random-init weights)",
+        "config": workload_config(shape, args.workload),
+        "roofline": roofline,
+        "step_tflops": round(step_flops / (max_ms / args.steps / 1e3) / 1e12, 1),
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "loss_first_step": round(first_loss, 5), "loss_last_step": round(last_loss, 5),
+    }
+    out["config"]["params"] = tr.n_params
+    out["config"]["algorithmic_tflop_per_step"] = round(step_flops / 1e12, 2)
+
+    if not args.no_e2e:
+        out["e2e"] = run_e2e(tr, shape, args, dev, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = OracleSample(shape).run()
+    return out
+
+
+def run_e2e(tr, shape, args, dev, world):
+    """Same metric through the public API with HOST buffers: every step copies
+    its inputs from pinned host memory and reads its loss partials back."""
+    import torch
+    T = shape.tokens
+    xh = torch.randn(T, shape.hidden).pin_memory()
+    th = torch.randint(0, shape.vocab, (T,), dtype=torch.int32).pin_memory()
+    lh = torch.empty(T, dtype=torch.float32).pin_memory()
+    xd = torch.empty(T, shape.hidden, device=dev)
+    td = torch.empty(T, dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        xd.copy_(xh, non_blocking=True)
+        td.copy_(th, non_blocking=True)
+        loss = tr.train_step(xd, td)
+        lh.copy_(loss, non_blocking=True)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    return {"value": round(world * T * args.steps / dt, 1), "unit": UNIT,
+            "h2d_bytes_per_step": xh.numel() * 4 + th.numel() * 4,
+            "d2h_bytes_per_step": lh.numel() * 4}
+
+
+def algorithmic_flops(shape):
+    """Dense-contraction FLOPs of one step: 6 x params x tokens for every
+    projection and the LM head, plus 6 causal attention matmuls
+    (2 nh d (S+1)/2 per token each) per layer."""
+    s = shape
+    blk = (s.q_dim + 2 * s.kv_dim) * s.hidden + s.hidden * s.q_dim + 3 * s.intermediate * s.hidden
+    proj = 6.0 * (s.layers * blk + s.vocab * s.hidden) * s.tokens
+    attn = s.layers * 6 * 2.0 * s.n_heads * s.head_dim * (s.seq + 1) / 2 * s.tokens
+    return proj + attn
+
+
+# ------------------------------------------------------------ reference
+def run_reference(args, rank, world):
+    from resident_decoder_trainer_gb300 import synth
+    shape = synth.WORKLOADS[args.workload]
+    if args.layers:
+        shape = shape.replace(layers=args.layers)
+    sampler = OracleSample(shape, seq_tokens=256, head_tokens=64, opt_params=1 << 22)
+    samples = []
+    for i in range(args.warmup + args.steps):
+        r = sampler.run()
+        if i >= args.warmup:
+            samples.append(r)
+    vals = [r["value"] for r in samples]
+    value = statistics.median(vals)
+    cpu = dict(samples[-1])
+    cpu["value"] = value
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(shape.tokens / value * 1e3, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(shape, args.workload),
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    out = run_rdt(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

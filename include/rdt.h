@@ -206,6 +206,21 @@ rdt_status rdt_gemm(const rdt_bf16* A, int32_t a_mn, int64_t lda, const rdt_bf16
 /* dst[i] = bf16(src[i]) with round-to-nearest-even; n elements, 16-byte aligned. */
 rdt_status rdt_cast_bf16(const float* src, rdt_bf16* dst, int64_t n, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Measurement hooks (host-side bookkeeping only; no device memory).
+ * rdt_gemm_timing_arm: while armed, the i-th tensor-core GEMM launch (any
+ *   entry point) records the caller-created cudaEvent_t events[2i] on its
+ *   stream just before the launch and events[2i+1] just after it, and stores
+ *   its algorithmic FLOP count 2*M*N*K in flops[i] (host array), for
+ *   i < capacity. rdt_gemm_timing_disarm stops it and returns the number of
+ *   launches seen (which may exceed capacity; only the first capacity are
+ *   recorded).
+ * rdt_launch_count: kernels this process has launched through the library
+ *   so far (all entry points, all devices). */
+rdt_status rdt_gemm_timing_arm(void* const* events, double* flops, int32_t capacity);
+int64_t rdt_gemm_timing_disarm(void);
+int64_t rdt_launch_count(void);
+
 /* Thread-local description of the last failure on this thread ("" if none). */
 const char* rdt_last_error(void);
 

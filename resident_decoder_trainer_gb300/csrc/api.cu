@@ -5,6 +5,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <string>
 
@@ -43,6 +44,15 @@ int* device_error_ptr() {
   }
   return ptrs[dev];
 }
+
+// ---------------------------------------------------------- measurement hooks
+std::atomic<int64_t> g_launches{0};
+std::mutex g_timing_mu;
+void* const* g_timing_events = nullptr;
+double* g_timing_flops = nullptr;
+int32_t g_timing_cap = 0;
+int64_t g_timing_seen = 0;
+bool g_timing_armed = false;
 
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -209,8 +219,50 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 }  // namespace
 
+namespace rdt {
+void note_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+int64_t gemm_timing_before(cudaStream_t s, double flops) {
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  if (!g_timing_armed) return -1;
+  const int64_t slot = g_timing_seen++;
+  if (slot >= g_timing_cap) return -1;
+  g_timing_flops[slot] = flops;
+  cudaEventRecord(static_cast<cudaEvent_t>(g_timing_events[2 * slot]), s);
+  return slot;
+}
+
+void gemm_timing_after(cudaStream_t s, int64_t slot) {
+  if (slot < 0) return;
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  if (g_timing_armed && slot < g_timing_cap)
+    cudaEventRecord(static_cast<cudaEvent_t>(g_timing_events[2 * slot + 1]), s);
+}
+}  // namespace rdt
+
 // =========================================================================
 extern "C" {
+
+rdt_status rdt_gemm_timing_arm(void* const* events, double* flops, int32_t capacity) {
+  if (!events || !flops || capacity < 1) return fail(RDT_EINVAL, "events/flops/capacity");
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  g_timing_events = events;
+  g_timing_flops = flops;
+  g_timing_cap = capacity;
+  g_timing_seen = 0;
+  g_timing_armed = true;
+  return RDT_OK;
+}
+
+int64_t rdt_gemm_timing_disarm(void) {
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  g_timing_armed = false;
+  g_timing_events = nullptr;
+  g_timing_flops = nullptr;
+  return g_timing_seen;
+}
+
+int64_t rdt_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* rdt_last_error(void) { return g_last_error.c_str(); }
 

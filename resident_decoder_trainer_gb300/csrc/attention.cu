@@ -462,6 +462,7 @@ static cudaError_t fwd_d(const bf16* q, int64_t ldq, const bf16* k, int64_t ldk,
   }
   dim3 grid((S + 127) / 128, nh, B);
   const float scale_log2 = kLog2e / sqrtf((float)D);
+  note_launch();
   attn_fwd_kernel<D><<<grid, 256, fwd_smem<D>(), s>>>(q, ldq, k, ldk, v, ldv, o, lse, S, nh, nkv,
                                                        scale_log2);
   return cudaGetLastError();
@@ -482,6 +483,7 @@ static cudaError_t bwd_d(const bf16* q, int64_t ldq, const bf16* k, int64_t ldk,
   }
   dim3 grid((S + 63) / 64, nkv, B);
   const float scale = 1.0f / sqrtf((float)D);
+  note_launch();
   attn_bwd_kernel<D><<<grid, 128, bwd_smem<D>(), s>>>(q, ldq, k, ldk, v, ldv, dout, lse, Dd, dq, dk,
                                                        dv, lddv, S, nh, nkv, scale,
                                                        scale * kLog2e);
@@ -505,6 +507,7 @@ cudaError_t attn_bwd_pre(const bf16* o, const bf16* dout, float* Dd, int B, int 
   const int T = B * S;
   const int64_t warps = (int64_t)T * nh;
   const int blocks = (int)((warps * 32 + 255) / 256);
+  note_launch();
   attn_bwd_pre_kernel<<<blocks, 256, 0, s>>>(o, dout, Dd, T, S, nh, d);
   return cudaGetLastError();
 }

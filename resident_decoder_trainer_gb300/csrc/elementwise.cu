@@ -146,6 +146,7 @@ __global__ void reduce_cols_kernel(const float* __restrict__ partials, int P, in
 
 #define RDT_NJ_SWITCH(KERNEL, H, GRID, BLOCK, SMEM, STREAM, ...)                           \
   do {                                                                                     \
+    note_launch();                                                                         \
     const int nj_need = ((H) / 4 + 31) / 32;                                               \
     if (nj_need <= 1) KERNEL<1><<<GRID, BLOCK, SMEM, STREAM>>>(__VA_ARGS__);               \
     else if (nj_need <= 2) KERNEL<2><<<GRID, BLOCK, SMEM, STREAM>>>(__VA_ARGS__);          \
@@ -179,6 +180,7 @@ cudaError_t rmsnorm_bwd(const float* dy, const float* x, const float* rstd, cons
                 resid, dx, dx_bf16, partials, T, H);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  note_launch();
   reduce_cols_kernel<<<(H + 255) / 256, 256, 0, s>>>(partials, P, H, dgamma);
   return cudaGetLastError();
 }
@@ -198,6 +200,7 @@ __global__ void rope_table_kernel(float2* __restrict__ cs, int S, int d, double 
 
 cudaError_t rope_table(float* cs, int S, int d, float theta, cudaStream_t s) {
   const int n = S * (d / 2);
+  note_launch();
   rope_table_kernel<<<(n + 255) / 256, 256, 0, s>>>(reinterpret_cast<float2*>(cs), S, d,
                                                     static_cast<double>(theta));
   return cudaGetLastError();
@@ -265,6 +268,7 @@ cudaError_t qknorm_rope_fwd(const bf16* qkv, int64_t ld_qkv, bf16* q_out, bf16* 
                             const float* cs, int T, int S, int nh, int nkv, int d, float eps,
                             cudaStream_t s) {
   const int64_t items = (int64_t)T * (nh + nkv);
+  note_launch();
   qknorm_rope_fwd_kernel<<<(unsigned)((items + 7) / 8), 256, 0, s>>>(
       qkv, ld_qkv, q_out, k_out, rstd_q, rstd_k, gq, gk, reinterpret_cast<const float2*>(cs), T, S,
       nh, nkv, d, eps);
@@ -380,12 +384,14 @@ cudaError_t qknorm_rope_bwd(const float* dq, const float* dk, const bf16* qkv, i
                             float* partials, int T, int S, int nh, int nkv, int d,
                             cudaStream_t s) {
   const int P = qknorm_bwd_partial_rows(T, nh + nkv);
+  note_launch();
   qknorm_rope_bwd_kernel<<<P, 256, 0, s>>>(dq, dk, qkv, ld_qkv, rstd_q, rstd_k, gq, gk,
                                            reinterpret_cast<const float2*>(cs), dqkv, partials, T,
                                            S, nh, nkv, d);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // columns [0, d) -> q gain, [d, 2d) -> k gain
+  note_launch();
   reduce_cols_kernel<<<1, 256, 0, s>>>(partials, P, 2 * d, dg_qk);
   return cudaGetLastError();
 }
@@ -411,10 +417,14 @@ cudaError_t cast_bf16(const float* src, bf16* dst, int64_t n, cudaStream_t s) {
     int64_t blocks = (n4 + 255) / 256;
     const int64_t cap = 8LL * num_sms();
     if (blocks > cap) blocks = cap;
+    note_launch();
     cast_bf16_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(src),
                                                       reinterpret_cast<uint2*>(dst), n4);
   }
-  if (n % 4) cast_bf16_tail_kernel<<<1, 32, 0, s>>>(src, dst, n4 * 4, n);
+  if (n % 4) {
+    note_launch();
+    cast_bf16_tail_kernel<<<1, 32, 0, s>>>(src, dst, n4 * 4, n);
+  }
   return cudaGetLastError();
 }
 
@@ -443,6 +453,7 @@ __global__ void ce_finalize_kernel(const float2* __restrict__ part, int part_ld,
 
 cudaError_t ce_finalize(const float2* part, int part_ld, int ntiles, const float* tgt_logit,
                         float* lse, float* loss, int T, cudaStream_t s) {
+  note_launch();
   ce_finalize_kernel<<<(T + 7) / 8, 256, 0, s>>>(part, part_ld, ntiles, tgt_logit, lse, loss, T);
   return cudaGetLastError();
 }
@@ -478,6 +489,7 @@ cudaError_t ce_grad(bf16* z, const float* lse, const int32_t* targets, float sca
   int64_t blocks = (n + 255) / 256;
   const int64_t cap = 8LL * num_sms();
   if (blocks > cap) blocks = cap;
+  note_launch();
   ce_grad_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<uint4*>(z), lse, targets, scale,
                                                   T, V8);
   return cudaGetLastError();
@@ -555,9 +567,11 @@ cudaError_t sq_sum(const float* const* bufs, const int64_t* lens, int nbuf, doub
   const int64_t cap = 4LL * num_sms();
   if (blocks > cap) blocks = cap;
   if (blocks > max_partials) blocks = max_partials;
+  note_launch();
   sq_sum_kernel<<<(unsigned)blocks, 256, 0, s>>>(tab, partials);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  note_launch();
   sq_sum_final_kernel<<<1, 256, 0, s>>>(partials, (int)blocks, out);
   return cudaGetLastError();
 }
@@ -576,6 +590,7 @@ __global__ void clip_scale_kernel(const double* __restrict__ sumsq, float max_no
 
 cudaError_t clip_scale(const double* sumsq, float max_norm, float* scale, int32_t* nonfinite,
                        cudaStream_t s) {
+  note_launch();
   clip_scale_kernel<<<1, 1, 0, s>>>(sumsq, max_norm, scale, nonfinite);
   return cudaGetLastError();
 }
@@ -642,14 +657,17 @@ cudaError_t adamw(float* w, const float* g, float* m, float* v, int64_t n, const
     int64_t blocks = (n4 + 255) / 256;
     const int64_t cap = 8LL * num_sms();
     if (blocks > cap) blocks = cap;
+    note_launch();
     adamw_kernel<<<(unsigned)blocks, 256, 0, s>>>(
         reinterpret_cast<float4*>(w), reinterpret_cast<const float4*>(g),
         reinterpret_cast<float4*>(m), reinterpret_cast<float4*>(v), n4, scale, skip, lr, b1, b2,
         eps, wd, bc1, bc2, reinterpret_cast<uint2*>(wb));
   }
-  if (n % 4)
+  if (n % 4) {
+    note_launch();
     adamw_tail_kernel<<<1, 32, 0, s>>>(w, g, m, v, n4 * 4, n, scale, skip, lr, b1, b2, eps, wd,
                                        bc1, bc2, wb);
+  }
   return cudaGetLastError();
 }
 

@@ -482,7 +482,10 @@ static cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const Ge
   }
   const int ntiles = p.m_tiles * p.n_tiles;
   const int grid = ntiles < num_sms() ? ntiles : num_sms();
+  const int64_t slot = gemm_timing_before(s, 2.0 * p.M * (double)p.N * p.K);
+  note_launch();
   gemm_kernel<A_MN, B_MN, EPI><<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(ta, tb, p);
+  gemm_timing_after(s, slot);
   return cudaGetLastError();
 }
 

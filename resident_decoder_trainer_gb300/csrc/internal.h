@@ -56,6 +56,12 @@ inline int gemm_n_tiles(int N) { return (N + 255) / 256; }
 
 int num_sms();
 
+// Kernel-launch bookkeeping (librdt-wide): every launch site calls note_launch.
+void note_launch(int n = 1);
+// GEMM timing hook: called around each GEMM launch (see rdt_gemm_timing_arm).
+int64_t gemm_timing_before(cudaStream_t s, double flops);
+void gemm_timing_after(cudaStream_t s, int64_t slot);
+
 // Upper bound on the row count of any gain-gradient partials buffer.
 constexpr int kMaxPartialRows = 512;
 // Upper bound on the per-block partials of the squared sum.

@@ -24,6 +24,7 @@ EXPORTS = (
     "rdt_sq_sum_workspace_bytes", "rdt_block_forward", "rdt_block_backward",
     "rdt_fused_cross_entropy", "rdt_sq_sum", "rdt_clip_scale", "rdt_adamw_step",
     "rdt_gemm", "rdt_cast_bf16", "rdt_last_error", "rdt_device_error",
+    "rdt_gemm_timing_arm", "rdt_gemm_timing_disarm", "rdt_launch_count",
 )
 
 
@@ -71,6 +72,9 @@ def _load() -> ctypes.CDLL:
         "rdt_cast_bf16": (I32, [P, P, I64, P]),
         "rdt_last_error": (ctypes.c_char_p, []),
         "rdt_device_error": (I32, [P]),
+        "rdt_gemm_timing_arm": (I32, [P, P, I32]),
+        "rdt_gemm_timing_disarm": (I64, []),
+        "rdt_launch_count": (I64, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -202,3 +206,36 @@ def device_error() -> int:
     code = ctypes.c_int32(0)
     _check(lib().rdt_device_error(ctypes.byref(code)))
     return code.value
+
+
+def launch_count() -> int:
+    """Kernels launched through librdt so far in this process."""
+    return lib().rdt_launch_count()
+
+
+class GemmTimer:
+    """Per-launch CUDA-event timing of every tensor-core GEMM launched while
+    the context is active (rdt_gemm_timing_arm / _disarm)."""
+
+    def __init__(self, capacity: int):
+        self.capacity = capacity
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * capacity)]
+        for ev in self.events:  # torch creates the CUDA event lazily, on first record
+            ev.record()
+        torch.cuda.synchronize()
+        self._handles = (ctypes.c_void_p * (2 * capacity))(*[ev.cuda_event for ev in self.events])
+        self._flops = (ctypes.c_double * capacity)()
+        self.seen = 0
+
+    def __enter__(self):
+        _check(lib().rdt_gemm_timing_arm(self._handles, self._flops, self.capacity))
+        return self
+
+    def __exit__(self, *exc):
+        self.seen = lib().rdt_gemm_timing_disarm()
+
+    def results(self):
+        """[(flops, milliseconds)] for every recorded launch (call after a sync)."""
+        n = min(self.seen, self.capacity)
+        return [(self._flops[i], self.events[2 * i].elapsed_time(self.events[2 * i + 1]))
+                for i in range(n)]
