@@ -179,6 +179,23 @@ rdt_status rdt_sq_sum(const float* const* bufs, const int64_t* lens, int32_t nbu
 rdt_status rdt_clip_scale(const double* sumsq, float max_norm, float* scale,
                           int32_t* nonfinite, void* stream);
 
+/* rdt_sq_sum for callers that cannot allocate device memory (code inside an
+ * allocator or pool callback, a runtime whose footprint is fixed once it
+ * starts, a plugin whose host gives it no scratch buffer). The pages have no
+ * counterpart of this call: it exists for those callers only. Same result as
+ * rdt_sq_sum; no workspace argument and no allocation of any kind. Its
+ * scratch is a fixed 32 KiB array (4096 fp64 partial sums) inside librdt.so
+ * that every GPU loading the library keeps until the process exits; any total
+ * length fits in it, and more than 64 buffers per call is rejected with
+ * RDT_EINVAL. The first call on a device looks up the array's device address
+ * (make that first call before any stream capture). Every call shares the one
+ * array, so calls that may overlap on the GPU (different streams, or
+ * different host threads on one device) race and must be serialised by the
+ * caller; each call rewrites every partial it reads, so nothing needs
+ * clearing in between. */
+rdt_status rdt_sq_sum_noalloc(const float* const* bufs, const int64_t* lens, int32_t nbuf,
+                              double* sumsq, void* stream);
+
 /* ---------------------------------------------------------------------------
  * AdamW over n contiguous fp32 elements (optimizer_step's adamw_step_cuda;
  * step counted from 1 as run_nonblock_optimizer_step does):

@@ -220,6 +220,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 }  // namespace
 
 namespace rdt {
+void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
+
 void note_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
 int64_t gemm_timing_before(cudaStream_t s, double flops) {

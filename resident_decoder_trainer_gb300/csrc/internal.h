@@ -56,6 +56,9 @@ inline int gemm_n_tiles(int N) { return (N + 255) / 256; }
 
 int num_sms();
 
+// Sets the thread-local message returned by rdt_last_error().
+void set_last_error(const char* msg);
+
 // Kernel-launch bookkeeping (librdt-wide): every launch site calls note_launch.
 void note_launch(int n = 1);
 // GEMM timing hook: called around each GEMM launch (see rdt_gemm_timing_arm).

@@ -25,6 +25,7 @@ EXPORTS = (
     "rdt_fused_cross_entropy", "rdt_sq_sum", "rdt_clip_scale", "rdt_adamw_step",
     "rdt_gemm", "rdt_cast_bf16", "rdt_last_error", "rdt_device_error",
     "rdt_gemm_timing_arm", "rdt_gemm_timing_disarm", "rdt_launch_count",
+    "rdt_sq_sum_noalloc",
 )
 
 
@@ -75,6 +76,7 @@ def _load() -> ctypes.CDLL:
         "rdt_gemm_timing_arm": (I32, [P, P, I32]),
         "rdt_gemm_timing_disarm": (I64, []),
         "rdt_launch_count": (I64, []),
+        "rdt_sq_sum_noalloc": (I32, [P, P, I32, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -176,6 +178,15 @@ def sq_sum(bufs, sumsq, ws, stream=None):
     lens = (ctypes.c_int64 * n)(*[b.numel() for b in bufs])
     _check(lib().rdt_sq_sum(ptrs, lens, n, _ptr(sumsq), _ptr(ws),
                             ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def sq_sum_noalloc(bufs, sumsq, stream=None):
+    """rdt_sq_sum without a workspace: for callers that cannot allocate
+    (the scratch is a fixed array inside the library; see include/rdt.h)."""
+    n = len(bufs)
+    ptrs = (ctypes.c_void_p * n)(*[_ptr(b) for b in bufs])
+    lens = (ctypes.c_int64 * n)(*[b.numel() for b in bufs])
+    _check(lib().rdt_sq_sum_noalloc(ptrs, lens, n, _ptr(sumsq), _stream(stream)))
 
 
 def clip_scale(sumsq, max_norm, scale, nonfinite=None, stream=None):
