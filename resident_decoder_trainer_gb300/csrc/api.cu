@@ -190,7 +190,7 @@ size_t carve_head_ws(const Dims& m, int64_t T, void* base, HeadWs* w) {
   t.hn = c.take<bf16>(T * m.H);
   t.rstd = c.take<float>(T);
   t.z = c.take<bf16>(T * m.V);
-  t.part = c.take<float2>(T * gemm_n_tiles((int)m.V));
+  t.part = c.take<float2>(T * ce_partials_per_row((int)m.V));
   t.tgt = c.take<float>(T);
   t.lse = c.take<float>(T);
   t.dhn = c.take<float>(T * m.H);
@@ -552,7 +552,7 @@ rdt_status rdt_fused_cross_entropy(const rdt_config* cfg, int32_t tokens, const 
   HeadWs wk;
   carve_head_ws(m, T, ws, &wk);
   const bf16* wl = reinterpret_cast<const bf16*>(w_lm);
-  const int ntiles = gemm_n_tiles((int)m.V);
+  const int ntiles = ce_partials_per_row((int)m.V);
 
   RDT_CHECK_CUDA(rmsnorm_fwd(h, gamma_f, wk.hn, wk.rstd, T, (int)m.H, cfg->rms_eps, s));
   // logits tile by tile: bf16 copy + per-tile (max, sum exp) + target logit

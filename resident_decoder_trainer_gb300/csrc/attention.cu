@@ -210,22 +210,28 @@ __global__ void __launch_bounds__(256) attn_fwd_kernel(const bf16* __restrict__ 
 }
 
 // ------------------------------------------------------ backward: D = rowsum(dO o O)
-__global__ void attn_bwd_pre_kernel(const bf16* __restrict__ o, const bf16* __restrict__ dout,
-                                    float* __restrict__ Dd, int T, int S, int nh, int d) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (warp >= T * nh) return;
-  const int t = warp / nh, h = warp % nh;
-  const bf16* op = o + (int64_t)t * nh * d + h * d;
-  const bf16* dp = dout + (int64_t)t * nh * d + h * d;
+// d/8 lanes per (token, head), 8 bf16 (16 bytes) per lane and operand.
+__global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const bf16* __restrict__ o,
+                                                           const bf16* __restrict__ dout,
+                                                           float* __restrict__ Dd, int T, int S,
+                                                           int nh, int d) {
+  const int lph = d / 8;
+  const int64_t gthread = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t item = gthread / lph;  // (token, head)
+  const int sub = static_cast<int>(gthread % lph);
+  const bool valid = item < (int64_t)T * nh;
   float acc = 0.f;
-  for (int i = 2 * lane; i < d; i += 64) {
-    const uint32_t a = *reinterpret_cast<const uint32_t*>(op + i);
-    const uint32_t c = *reinterpret_cast<const uint32_t*>(dp + i);
-    acc += bf16lo(a) * bf16lo(c) + bf16hi(a) * bf16hi(c);
+  if (valid) {
+    const uint4 a = *reinterpret_cast<const uint4*>(o + item * d + 8 * sub);
+    const uint4 c = *reinterpret_cast<const uint4*>(dout + item * d + 8 * sub);
+    const uint32_t* pa = &a.x;
+    const uint32_t* pc = &c.x;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc += bf16lo(pa[e]) * bf16lo(pc[e]) + bf16hi(pa[e]) * bf16hi(pc[e]);
   }
-  acc = warp_sum(acc);
-  if (lane == 0) {
+  for (int off = lph / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (valid && sub == 0) {
+    const int t = static_cast<int>(item / nh), h = static_cast<int>(item % nh);
     const int b = t / S, s = t % S;
     Dd[((int64_t)b * nh + h) * S + s] = acc;
   }
@@ -505,8 +511,8 @@ cudaError_t attn_fwd(const bf16* q, int64_t ldq, const bf16* k, int64_t ldk, con
 cudaError_t attn_bwd_pre(const bf16* o, const bf16* dout, float* Dd, int B, int S, int nh, int d,
                          cudaStream_t s) {
   const int T = B * S;
-  const int64_t warps = (int64_t)T * nh;
-  const int blocks = (int)((warps * 32 + 255) / 256);
+  const int64_t threads = (int64_t)T * nh * (d / 8);
+  const int blocks = (int)((threads + 255) / 256);
   note_launch();
   attn_bwd_pre_kernel<<<blocks, 256, 0, s>>>(o, dout, Dd, T, S, nh, d);
   return cudaGetLastError();

@@ -53,95 +53,101 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_kernel(const float* __restric
   if (lane == 0) rstd[row] = r;
 }
 
-// dx = r*(dy*g - xhat*mean(dy*g*xhat)) + resid; per-CTA partial of sum(dy*xhat).
-template <int NJ>
-__global__ void __launch_bounds__(256) rmsnorm_bwd_kernel(
+// dx = r*(dy*g - xhat*mean(dy*g*xhat)) + resid, single pass over the row.
+// One CTA per group of rows; thread t owns columns [8t, 8t+8) for every row
+// (so its gain-gradient partial needs no cross-thread reduction); the row
+// dot product is a warp shuffle + a fixed-order sum over the CTA's warps.
+__global__ void __launch_bounds__(512) rmsnorm_bwd_kernel(
     const float* __restrict__ dy, const float* __restrict__ x, const float* __restrict__ rstd,
     const float* __restrict__ gamma, const float* __restrict__ resid, float* __restrict__ dx,
     bf16* __restrict__ dxb, float* __restrict__ partials, int T, int H) {
-  extern __shared__ float red[];  // [H]
+  __shared__ float red[2][16];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int H4 = H >> 2;
-  const float4* g4 = reinterpret_cast<const float4*>(gamma);
-  float4 acc[NJ];
+  const int nwarps = blockDim.x >> 5;
+  const int c0 = 8 * threadIdx.x;
+  const bool own = c0 < H;
+  float g[8], acc[8];
 #pragma unroll
-  for (int j = 0; j < NJ; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-
-  for (int row = blockIdx.x * 8 + warp; row < T; row += gridDim.x * 8) {
-    const float4* dyr = reinterpret_cast<const float4*>(dy + (int64_t)row * H);
-    const float4* xr = reinterpret_cast<const float4*>(x + (int64_t)row * H);
+  for (int e = 0; e < 8; ++e) acc[e] = g[e] = 0.f;  // idle lanes must add exact zeros
+  if (own) {
+    const float4 g0 = *reinterpret_cast<const float4*>(gamma + c0);
+    const float4 g1 = *reinterpret_cast<const float4*>(gamma + c0 + 4);
+    g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w;
+    g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
+  }
+  const float invH = 1.0f / H;
+  int buf = 0;
+  for (int row = blockIdx.x; row < T; row += gridDim.x) {
+    const int64_t base = (int64_t)row * H + c0;
+    float a[8] = {}, b[8] = {}, q[8] = {};
+    if (own) {
+      const float4 a0 = *reinterpret_cast<const float4*>(dy + base);
+      const float4 a1 = *reinterpret_cast<const float4*>(dy + base + 4);
+      const float4 b0 = *reinterpret_cast<const float4*>(x + base);
+      const float4 b1 = *reinterpret_cast<const float4*>(x + base + 4);
+      a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w;
+      a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
+      b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w;
+      b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
+      if (resid) {
+        const float4 q0 = *reinterpret_cast<const float4*>(resid + base);
+        const float4 q1 = *reinterpret_cast<const float4*>(resid + base + 4);
+        q[0] = q0.x; q[1] = q0.y; q[2] = q0.z; q[3] = q0.w;
+        q[4] = q1.x; q[5] = q1.y; q[6] = q1.z; q[7] = q1.w;
+      }
+    }
     const float r = rstd[row];
     float dot = 0.f;
 #pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      const int c = lane + 32 * j;
-      if (c < H4) {
-        const float4 a = dyr[c], b = xr[c], g = g4[c];
-        dot += a.x * g.x * b.x + a.y * g.y * b.y + a.z * g.z * b.z + a.w * g.w * b.w;
-      }
-    }
-    dot = warp_sum(dot) * r;  // sum(dy*g*xhat)
-    const float cmean = dot / H;
-    float4* dxr = reinterpret_cast<float4*>(dx + (int64_t)row * H);
-    const float4* rr = resid ? reinterpret_cast<const float4*>(resid + (int64_t)row * H) : nullptr;
-    uint2* dbr = dxb ? reinterpret_cast<uint2*>(dxb + (int64_t)row * H) : nullptr;
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      const int c = lane + 32 * j;
-      if (c < H4) {
-        const float4 a = dyr[c], b = xr[c], g = g4[c];
-        const float4 xh = make_float4(b.x * r, b.y * r, b.z * r, b.w * r);
-        float4 o = make_float4(r * (a.x * g.x - xh.x * cmean), r * (a.y * g.y - xh.y * cmean),
-                               r * (a.z * g.z - xh.z * cmean), r * (a.w * g.w - xh.w * cmean));
-        if (rr) {
-          const float4 q = rr[c];
-          o.x += q.x; o.y += q.y; o.z += q.z; o.w += q.w;
-        }
-        dxr[c] = o;
-        if (dbr) {
-          uint2 ob;
-          ob.x = pack_bf16x2(o.x, o.y);
-          ob.y = pack_bf16x2(o.z, o.w);
-          dbr[c] = ob;
-        }
-        acc[j].x += a.x * xh.x;
-        acc[j].y += a.y * xh.y;
-        acc[j].z += a.z * xh.z;
-        acc[j].w += a.w * xh.w;
-      }
-    }
-  }
-  // fixed-order reduction of the 8 warps' gain partials
-  for (int w = 0; w < 8; ++w) {
-    if (warp == w) {
-#pragma unroll
-      for (int j = 0; j < NJ; ++j) {
-        const int c = lane + 32 * j;
-        if (c < H4) {
-          float4* s4 = reinterpret_cast<float4*>(red) + c;
-          if (w == 0) {
-            *s4 = acc[j];
-          } else {
-            float4 t = *s4;
-            t.x += acc[j].x; t.y += acc[j].y; t.z += acc[j].z; t.w += acc[j].w;
-            *s4 = t;
-          }
-        }
-      }
-    }
+    for (int e = 0; e < 8; ++e) dot += a[e] * g[e] * b[e];
+    dot = warp_sum(dot);
+    if (lane == 0) red[buf][warp] = dot;
     __syncthreads();
+    float tot = 0.f;
+    for (int w = 0; w < nwarps; ++w) tot += red[buf][w];
+    buf ^= 1;
+    const float cmean = tot * r * invH;  // mean(dy*g*xhat)
+    if (own) {
+      float o[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float xh = b[e] * r;
+        o[e] = r * (a[e] * g[e] - xh * cmean) + q[e];
+        acc[e] += a[e] * xh;
+      }
+      *reinterpret_cast<float4*>(dx + base) = make_float4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<float4*>(dx + base + 4) = make_float4(o[4], o[5], o[6], o[7]);
+      if (dxb)
+        *reinterpret_cast<uint4*>(dxb + base) =
+            make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
+                       pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
+    }
   }
-  for (int c = threadIdx.x; c < H; c += blockDim.x) partials[(int64_t)blockIdx.x * H + c] = red[c];
+  if (own) {
+    float* pr = partials + (int64_t)blockIdx.x * H + c0;
+    *reinterpret_cast<float4*>(pr) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    *reinterpret_cast<float4*>(pr + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
 }
 
-// out[c] = sum_p partials[p, c] in order p = 0, 1, ...
-__global__ void reduce_cols_kernel(const float* __restrict__ partials, int P, int W,
-                                   float* __restrict__ out) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= W) return;
+// out[c] = sum_p partials[p, c]: 8 row-strided partial sums per column, then
+// those 8 in order (deterministic).
+__global__ void __launch_bounds__(256) reduce_cols_kernel(const float* __restrict__ partials,
+                                                          int P, int W, float* __restrict__ out) {
+  __shared__ float red[8][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int c = blockIdx.x * 32 + tx;
   float s = 0.f;
-  for (int p = 0; p < P; ++p) s += partials[(int64_t)p * W + c];
-  out[c] = s;
+  if (c < W)
+    for (int p = ty; p < P; p += 8) s += partials[(int64_t)p * W + c];
+  red[ty][tx] = s;
+  __syncthreads();
+  if (ty == 0 && c < W) {
+    float t = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t += red[i][tx];
+    out[c] = t;
+  }
 }
 
 #define RDT_NJ_SWITCH(KERNEL, H, GRID, BLOCK, SMEM, STREAM, ...)                           \
@@ -166,101 +172,131 @@ cudaError_t rmsnorm_fwd(const float* x, const float* gamma, bf16* y, float* rstd
   return cudaGetLastError();
 }
 
-int rmsnorm_bwd_partial_rows(int T) {
-  const int want = (T + 7) / 8;
-  const int cap = min(2 * num_sms(), kMaxPartialRows);
-  return want < cap ? want : cap;
+int rmsnorm_bwd_partial_rows(int T) { return T < kMaxPartialRows ? T : kMaxPartialRows; }
+
+static cudaError_t reduce_cols(const float* partials, int P, int W, float* out, cudaStream_t s) {
+  note_launch();
+  reduce_cols_kernel<<<(W + 31) / 32, 256, 0, s>>>(partials, P, W, out);
+  return cudaGetLastError();
 }
 
 cudaError_t rmsnorm_bwd(const float* dy, const float* x, const float* rstd, const float* gamma,
                         const float* resid, float* dx, bf16* dx_bf16, float* dgamma,
                         float* partials, int T, int H, cudaStream_t s) {
   const int P = rmsnorm_bwd_partial_rows(T);
-  RDT_NJ_SWITCH(rmsnorm_bwd_kernel, H, dim3(P), 256, H * sizeof(float), s, dy, x, rstd, gamma,
-                resid, dx, dx_bf16, partials, T, H);
+  const int threads = ((H / 8 + 31) / 32) * 32;
+  note_launch();
+  rmsnorm_bwd_kernel<<<P, threads, 0, s>>>(dy, x, rstd, gamma, resid, dx, dx_bf16, partials, T, H);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  note_launch();
-  reduce_cols_kernel<<<(H + 255) / 256, 256, 0, s>>>(partials, P, H, dgamma);
-  return cudaGetLastError();
+  return reduce_cols(partials, P, H, dgamma, s);
 }
 
 // ----------------------------------------------------------------- RoPE table
-// cs[s, i] = (cos, sin)(s * theta^(-2i/d)), evaluated in fp64, stored fp32.
-__global__ void rope_table_kernel(float2* __restrict__ cs, int S, int d, double theta) {
-  const int half = d / 2;
+// cs[s, i] = (cos, sin)(s * inv_freq[i]) with inv_freq[i] = theta^(-2i/d)
+// computed in fp64 on the host; the angle is formed and reduced modulo 2*pi
+// in fp64, then evaluated with the fp32 sincosf on |r| <= pi.
+struct InvFreq {
+  double v[64];
+};
+__global__ void rope_table_kernel(float2* __restrict__ cs, int S, int half, const InvFreq f) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= S * half) return;
   const int s = idx / half, i = idx % half;
-  const double inv = pow(theta, -2.0 * i / d);
-  double sn, cn;
-  sincos(static_cast<double>(s) * inv, &sn, &cn);
-  cs[idx] = make_float2(static_cast<float>(cn), static_cast<float>(sn));
+  const double two_pi = 6.283185307179586476925286766559;
+  const double ang = static_cast<double>(s) * f.v[i];
+  const double k = rint(ang / two_pi);
+  const float rr = static_cast<float>(fma(-k, two_pi, ang));
+  float sn, cn;
+  sincosf(rr, &sn, &cn);
+  cs[idx] = make_float2(cn, sn);
 }
 
 cudaError_t rope_table(float* cs, int S, int d, float theta, cudaStream_t s) {
-  const int n = S * (d / 2);
+  const int half = d / 2;
+  InvFreq f;
+  for (int i = 0; i < half && i < 64; ++i)
+    f.v[i] = std::pow(static_cast<double>(theta), -2.0 * i / d);
+  const int n = S * half;
   note_launch();
-  rope_table_kernel<<<(n + 255) / 256, 256, 0, s>>>(reinterpret_cast<float2*>(cs), S, d,
-                                                    static_cast<double>(theta));
+  rope_table_kernel<<<(n + 255) / 256, 256, 0, s>>>(reinterpret_cast<float2*>(cs), S, half, f);
   return cudaGetLastError();
 }
 
 // ----------------------------------------------------- QK RMSNorm + RoPE fwd
-// One warp per (token, head) over nh query heads then nkv key heads. Lane l
-// owns the rotation pairs (2l + 64j, 2l + 1 + 64j) and their partners + d/2.
+// A head of D elements is handled by D/8 lanes, 8 consecutive elements each
+// (16-byte loads); a warp covers 256/D heads per iteration. Lanes of the first
+// half of a head hold elements i < D/2, their partner (lane ^ D/16) the
+// rotation partners i + D/2.
+template <int D>
 __global__ void __launch_bounds__(256) qknorm_rope_fwd_kernel(
     const bf16* __restrict__ qkv, int64_t ld, bf16* __restrict__ qo, bf16* __restrict__ ko,
     float* __restrict__ rq, float* __restrict__ rk, const float* __restrict__ gq,
     const float* __restrict__ gk, const float2* __restrict__ cs, int T, int S, int nh, int nkv,
-    int d, float eps) {
-  const int64_t item = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    float eps) {
+  constexpr int LPH = D / 8, HPW = 32 / LPH, HALF = D / 2, PX = LPH / 2;
   const int lane = threadIdx.x & 31;
+  const int slot = lane / LPH, sub = lane % LPH;
+  const bool first = sub < PX;
   const int heads = nh + nkv;
-  if (item >= (int64_t)T * heads) return;
-  const int t = static_cast<int>(item / heads), hd = static_cast<int>(item % heads);
-  const bool isq = hd < nh;
-  const int h = isq ? hd : hd - nh;
-  const bf16* src = qkv + (int64_t)t * ld + (isq ? h * d : nh * d + h * d);
-  bf16* dst = isq ? qo + (int64_t)t * nh * d + h * d : ko + (int64_t)t * nkv * d + h * d;
-  const float* g = isq ? gq : gk;
-  const int half = d / 2, pos = t % S;
-  float x0[2][2], x1[2][2];
-  float ss = 0.f;
+  const int64_t items = (int64_t)T * heads;
+  const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t it0 = warp_id * HPW; it0 < items; it0 += nwarps * HPW) {
+    const int64_t item = it0 + slot;
+    const bool valid = item < items;
+    const int t = valid ? static_cast<int>(item / heads) : 0;
+    const int hd = valid ? static_cast<int>(item % heads) : 0;
+    const bool isq = hd < nh;
+    const int h = isq ? hd : hd - nh;
+    const bf16* src = qkv + (int64_t)t * ld + (isq ? h * D : nh * D + h * D) + 8 * sub;
+    float xv[8];
+    uint4 raw = valid ? *reinterpret_cast<const uint4*>(src) : make_uint4(0, 0, 0, 0);
+    const uint32_t* rw = &raw.x;
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int i = 2 * lane + 64 * j;
-    if (i < half) {
-      const uint32_t a = *reinterpret_cast<const uint32_t*>(src + i);
-      const uint32_t b = *reinterpret_cast<const uint32_t*>(src + half + i);
-      x0[j][0] = bf16lo(a); x0[j][1] = bf16hi(a);
-      x1[j][0] = bf16lo(b); x1[j][1] = bf16hi(b);
-      ss += x0[j][0] * x0[j][0] + x0[j][1] * x0[j][1] + x1[j][0] * x1[j][0] + x1[j][1] * x1[j][1];
+    for (int e = 0; e < 4; ++e) {
+      xv[2 * e] = bf16lo(rw[e]);
+      xv[2 * e + 1] = bf16hi(rw[e]);
     }
-  }
-  ss = warp_sum(ss);
-  const float r = rsqrtf(ss / d + eps);
+    float ss = 0.f;
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int i = 2 * lane + 64 * j;
-    if (i < half) {
-      float o0[2], o1[2];
+    for (int e = 0; e < 8; ++e) ss += xv[e] * xv[e];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float y0 = x0[j][e] * r * g[i + e];
-        const float y1 = x1[j][e] * r * g[half + i + e];
-        const float2 c = cs[(int64_t)pos * half + i + e];
-        o0[e] = y0 * c.x - y1 * c.y;
-        o1[e] = y1 * c.x + y0 * c.y;
+    for (int o = LPH / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float r = rsqrtf(ss / D + eps);
+    const float* g = (isq ? gq : gk) + 8 * sub;
+    float y[8], yp[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) y[e] = xv[e] * r * g[e];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) yp[e] = __shfl_xor_sync(0xffffffffu, y[e], PX);
+    const int i0 = 8 * (first ? sub : sub - PX);
+    const int pos = t % S;
+    const float2* c = cs + (int64_t)pos * HALF + i0;
+    float out[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float2 cv = c[e];
+      out[e] = first ? y[e] * cv.x - yp[e] * cv.y : y[e] * cv.x + yp[e] * cv.y;
+    }
+    if (valid) {
+      bf16* dst = (isq ? qo + (int64_t)t * nh * D + h * D : ko + (int64_t)t * nkv * D + h * D) +
+                  8 * sub;
+      *reinterpret_cast<uint4*>(dst) =
+          make_uint4(pack_bf16x2(out[0], out[1]), pack_bf16x2(out[2], out[3]),
+                     pack_bf16x2(out[4], out[5]), pack_bf16x2(out[6], out[7]));
+      if (sub == 0) {
+        if (isq) rq[(int64_t)t * nh + h] = r;
+        else rk[(int64_t)t * nkv + h] = r;
       }
-      *reinterpret_cast<uint32_t*>(dst + i) = pack_bf16x2(o0[0], o0[1]);
-      *reinterpret_cast<uint32_t*>(dst + half + i) = pack_bf16x2(o1[0], o1[1]);
     }
   }
-  if (lane == 0) {
-    if (isq) rq[(int64_t)t * nh + h] = r;
-    else rk[(int64_t)t * nkv + h] = r;
-  }
+}
+
+static int elementwise_grid(int64_t warps_needed) {
+  const int64_t blocks = (warps_needed + 7) / 8;
+  const int64_t cap = 16LL * num_sms();
+  return static_cast<int>(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
 }
 
 cudaError_t qknorm_rope_fwd(const bf16* qkv, int64_t ld_qkv, bf16* q_out, bf16* k_out,
@@ -268,114 +304,134 @@ cudaError_t qknorm_rope_fwd(const bf16* qkv, int64_t ld_qkv, bf16* q_out, bf16* 
                             const float* cs, int T, int S, int nh, int nkv, int d, float eps,
                             cudaStream_t s) {
   const int64_t items = (int64_t)T * (nh + nkv);
+  const int grid = elementwise_grid((items * d + 255) / 256);
+  const float2* c2 = reinterpret_cast<const float2*>(cs);
   note_launch();
-  qknorm_rope_fwd_kernel<<<(unsigned)((items + 7) / 8), 256, 0, s>>>(
-      qkv, ld_qkv, q_out, k_out, rstd_q, rstd_k, gq, gk, reinterpret_cast<const float2*>(cs), T, S,
-      nh, nkv, d, eps);
+  switch (d) {
+    case 16: qknorm_rope_fwd_kernel<16><<<grid, 256, 0, s>>>(qkv, ld_qkv, q_out, k_out, rstd_q, rstd_k, gq, gk, c2, T, S, nh, nkv, eps); break;
+    case 32: qknorm_rope_fwd_kernel<32><<<grid, 256, 0, s>>>(qkv, ld_qkv, q_out, k_out, rstd_q, rstd_k, gq, gk, c2, T, S, nh, nkv, eps); break;
+    case 64: qknorm_rope_fwd_kernel<64><<<grid, 256, 0, s>>>(qkv, ld_qkv, q_out, k_out, rstd_q, rstd_k, gq, gk, c2, T, S, nh, nkv, eps); break;
+    case 128: qknorm_rope_fwd_kernel<128><<<grid, 256, 0, s>>>(qkv, ld_qkv, q_out, k_out, rstd_q, rstd_k, gq, gk, c2, T, S, nh, nkv, eps); break;
+    default: return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 
 // ----------------------------------------------------- QK RMSNorm + RoPE bwd
-// Inverse rotation of the incoming gradient, then the RMSNorm backward over
-// head_dim. Gain gradients: per-lane register partials, fixed-order CTA
-// reduction into partials[block, 2*d] (q gains then k gains).
+// Same lane layout as the forward. Inverse rotation of the incoming fp32
+// gradient, then the RMSNorm backward over head_dim. Gain gradients: each lane
+// always owns the same 8 columns, so it accumulates them in registers; lanes
+// of different head slots are combined by shuffles, warps in a fixed order,
+// and each CTA writes one partial row [q gains | k gains].
+template <int D>
 __global__ void __launch_bounds__(256) qknorm_rope_bwd_kernel(
     const float* __restrict__ dq, const float* __restrict__ dk, const bf16* __restrict__ qkv,
     int64_t ld, const float* __restrict__ rq, const float* __restrict__ rk,
     const float* __restrict__ gq, const float* __restrict__ gk, const float2* __restrict__ cs,
-    bf16* __restrict__ dqkv, float* __restrict__ partials, int T, int S, int nh, int nkv, int d) {
-  __shared__ float red[8][2][256];
+    bf16* __restrict__ dqkv, float* __restrict__ partials, int T, int S, int nh, int nkv) {
+  constexpr int LPH = D / 8, HPW = 32 / LPH, HALF = D / 2, PX = LPH / 2;
+  __shared__ float red[8][2 * D];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int slot = lane / LPH, sub = lane % LPH;
+  const bool first = sub < PX;
   const int heads = nh + nkv;
-  const int half = d / 2;
-  float accq[2][2][2] = {}, acck[2][2][2] = {};  // [j][half][e]
   const int64_t items = (int64_t)T * heads;
-  for (int64_t item = (int64_t)blockIdx.x * 8 + warp; item < items; item += (int64_t)gridDim.x * 8) {
-    const int t = static_cast<int>(item / heads), hd = static_cast<int>(item % heads);
+  const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  float accq[8] = {}, acck[8] = {};
+  float gqv[8], gkv[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    gqv[e] = gq[8 * sub + e];
+    gkv[e] = gk[8 * sub + e];
+  }
+  const int i0 = 8 * (first ? sub : sub - PX);
+  for (int64_t it0 = warp_id * HPW; it0 < items; it0 += nwarps * HPW) {
+    const int64_t item = it0 + slot;
+    const bool valid = item < items;
+    const int t = valid ? static_cast<int>(item / heads) : 0;
+    const int hd = valid ? static_cast<int>(item % heads) : 0;
     const bool isq = hd < nh;
     const int h = isq ? hd : hd - nh;
-    const int col = isq ? h * d : nh * d + h * d;
-    const bf16* xs = qkv + (int64_t)t * ld + col;
-    const float* gs = isq ? dq + (int64_t)t * nh * d + h * d : dk + (int64_t)t * nkv * d + h * d;
-    const float* g = isq ? gq : gk;
-    const float r = isq ? rq[(int64_t)t * nh + h] : rk[(int64_t)t * nkv + h];
+    const int col = (isq ? h * D : nh * D + h * D) + 8 * sub;
+    float din[8] = {}, xv[8] = {};
+    float r = 0.f;
+    if (valid) {
+      const float* gsrc = (isq ? dq + (int64_t)t * nh * D + h * D : dk + (int64_t)t * nkv * D + h * D) +
+                          8 * sub;
+      const float4 d0 = *reinterpret_cast<const float4*>(gsrc);
+      const float4 d1 = *reinterpret_cast<const float4*>(gsrc + 4);
+      din[0] = d0.x; din[1] = d0.y; din[2] = d0.z; din[3] = d0.w;
+      din[4] = d1.x; din[5] = d1.y; din[6] = d1.z; din[7] = d1.w;
+      const uint4 raw = *reinterpret_cast<const uint4*>(qkv + (int64_t)t * ld + col);
+      const uint32_t* rw = &raw.x;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        xv[2 * e] = bf16lo(rw[e]);
+        xv[2 * e + 1] = bf16hi(rw[e]);
+      }
+      r = isq ? rq[(int64_t)t * nh + h] : rk[(int64_t)t * nkv + h];
+    }
+    float dp[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) dp[e] = __shfl_xor_sync(0xffffffffu, din[e], PX);
     const int pos = t % S;
-    float xh[2][2][2], dxh[2][2][2];
+    const float2* c = cs + (int64_t)pos * HALF + i0;
+    float xh[8], dxh[8];
     float dot = 0.f;
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int i = 2 * lane + 64 * j;
-      if (i < half) {
-        const uint32_t a = *reinterpret_cast<const uint32_t*>(xs + i);
-        const uint32_t b = *reinterpret_cast<const uint32_t*>(xs + half + i);
-        const float2 d0 = *reinterpret_cast<const float2*>(gs + i);
-        const float2 d1 = *reinterpret_cast<const float2*>(gs + half + i);
-        const float in0[2] = {d0.x, d0.y}, in1[2] = {d1.x, d1.y};
-        const float xv0[2] = {bf16lo(a), bf16hi(a)}, xv1[2] = {bf16lo(b), bf16hi(b)};
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float2 c = cs[(int64_t)pos * half + i + e];
-          const float dn0 = in0[e] * c.x + in1[e] * c.y;  // inverse rotation
-          const float dn1 = in1[e] * c.x - in0[e] * c.y;
-          xh[j][0][e] = xv0[e] * r;
-          xh[j][1][e] = xv1[e] * r;
-          // gain gradient contributions
-          if (isq) {
-            accq[j][0][e] += dn0 * xh[j][0][e];
-            accq[j][1][e] += dn1 * xh[j][1][e];
-          } else {
-            acck[j][0][e] += dn0 * xh[j][0][e];
-            acck[j][1][e] += dn1 * xh[j][1][e];
-          }
-          dxh[j][0][e] = dn0 * g[i + e];
-          dxh[j][1][e] = dn1 * g[half + i + e];
-          dot += dxh[j][0][e] * xh[j][0][e] + dxh[j][1][e] * xh[j][1][e];
-        }
+    for (int e = 0; e < 8; ++e) {
+      const float2 cv = c[e];
+      // inverse rotation: first half d0 c + d1 s, second half d1 c - d0 s
+      const float dn = first ? din[e] * cv.x + dp[e] * cv.y : din[e] * cv.x - dp[e] * cv.y;
+      xh[e] = xv[e] * r;
+      if (valid) {
+        if (isq) accq[e] += dn * xh[e];
+        else acck[e] += dn * xh[e];
       }
+      dxh[e] = dn * (isq ? gqv[e] : gkv[e]);
+      dot += dxh[e] * xh[e];
     }
-    const float cmean = warp_sum(dot) / d;
-    bf16* out = dqkv + (int64_t)t * ld + col;
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int i = 2 * lane + 64 * j;
-      if (i < half) {
-        float o[2][2];
+    for (int o = LPH / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    const float cmean = dot / D;
+    if (valid) {
+      float o8[8];
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) o[hh][e] = r * (dxh[j][hh][e] - xh[j][hh][e] * cmean);
-        *reinterpret_cast<uint32_t*>(out + i) = pack_bf16x2(o[0][0], o[0][1]);
-        *reinterpret_cast<uint32_t*>(out + half + i) = pack_bf16x2(o[1][0], o[1][1]);
-      }
+      for (int e = 0; e < 8; ++e) o8[e] = r * (dxh[e] - xh[e] * cmean);
+      *reinterpret_cast<uint4*>(dqkv + (int64_t)t * ld + col) =
+          make_uint4(pack_bf16x2(o8[0], o8[1]), pack_bf16x2(o8[2], o8[3]),
+                     pack_bf16x2(o8[4], o8[5]), pack_bf16x2(o8[6], o8[7]));
     }
   }
-  // per-warp partials to shared memory, then a fixed-order sum over warps
+  // combine head slots of the warp (lanes with equal sub), fixed order
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int i = 2 * lane + 64 * j;
-    if (i < half) {
+  for (int o = LPH; o < 32; o <<= 1) {
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh)
+    for (int e = 0; e < 8; ++e) {
+      accq[e] += __shfl_xor_sync(0xffffffffu, accq[e], o);
+      acck[e] += __shfl_xor_sync(0xffffffffu, acck[e], o);
+    }
+  }
+  if (slot == 0) {
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          red[warp][0][hh * half + i + e] = accq[j][hh][e];
-          red[warp][1][hh * half + i + e] = acck[j][hh][e];
-        }
+    for (int e = 0; e < 8; ++e) {
+      red[warp][8 * sub + e] = accq[e];
+      red[warp][D + 8 * sub + e] = acck[e];
     }
   }
   __syncthreads();
-  for (int c = threadIdx.x; c < 2 * d; c += blockDim.x) {
-    const int which = c / d, i = c % d;
+  for (int cidx = threadIdx.x; cidx < 2 * D; cidx += blockDim.x) {
     float sum = 0.f;
-    for (int w = 0; w < 8; ++w) sum += red[w][which][i];
-    partials[(int64_t)blockIdx.x * 2 * d + c] = sum;
+    for (int w = 0; w < 8; ++w) sum += red[w][cidx];
+    partials[(int64_t)blockIdx.x * 2 * D + cidx] = sum;
   }
 }
 
 int qknorm_bwd_partial_rows(int T, int heads) {
-  const int64_t want = ((int64_t)T * heads + 7) / 8;
-  const int cap = min(2 * num_sms(), kMaxPartialRows);
-  return want < cap ? static_cast<int>(want) : cap;
+  const int64_t want = ((int64_t)T * heads + 63) / 64;
+  const int cap = kMaxPartialRows;
+  return want < cap ? static_cast<int>(want > 0 ? want : 1) : cap;
 }
 
 cudaError_t qknorm_rope_bwd(const float* dq, const float* dk, const bf16* qkv, int64_t ld_qkv,
@@ -384,16 +440,19 @@ cudaError_t qknorm_rope_bwd(const float* dq, const float* dk, const bf16* qkv, i
                             float* partials, int T, int S, int nh, int nkv, int d,
                             cudaStream_t s) {
   const int P = qknorm_bwd_partial_rows(T, nh + nkv);
+  const float2* c2 = reinterpret_cast<const float2*>(cs);
   note_launch();
-  qknorm_rope_bwd_kernel<<<P, 256, 0, s>>>(dq, dk, qkv, ld_qkv, rstd_q, rstd_k, gq, gk,
-                                           reinterpret_cast<const float2*>(cs), dqkv, partials, T,
-                                           S, nh, nkv, d);
+  switch (d) {
+    case 16: qknorm_rope_bwd_kernel<16><<<P, 256, 0, s>>>(dq, dk, qkv, ld_qkv, rstd_q, rstd_k, gq, gk, c2, dqkv, partials, T, S, nh, nkv); break;
+    case 32: qknorm_rope_bwd_kernel<32><<<P, 256, 0, s>>>(dq, dk, qkv, ld_qkv, rstd_q, rstd_k, gq, gk, c2, dqkv, partials, T, S, nh, nkv); break;
+    case 64: qknorm_rope_bwd_kernel<64><<<P, 256, 0, s>>>(dq, dk, qkv, ld_qkv, rstd_q, rstd_k, gq, gk, c2, dqkv, partials, T, S, nh, nkv); break;
+    case 128: qknorm_rope_bwd_kernel<128><<<P, 256, 0, s>>>(dq, dk, qkv, ld_qkv, rstd_q, rstd_k, gq, gk, c2, dqkv, partials, T, S, nh, nkv); break;
+    default: return cudaErrorInvalidValue;
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // columns [0, d) -> q gain, [d, 2d) -> k gain
-  note_launch();
-  reduce_cols_kernel<<<1, 256, 0, s>>>(partials, P, 2 * d, dg_qk);
-  return cudaGetLastError();
+  return reduce_cols(partials, P, 2 * d, dg_qk, s);
 }
 
 // --------------------------------------------------------------------- cast

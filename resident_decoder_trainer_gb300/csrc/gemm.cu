@@ -1,14 +1,15 @@
 // Persistent tcgen05 BF16 GEMM for sm_103a with fused epilogues.
 //
-// One CTA per SM (192 threads, ~197 KB shared memory, all 512 TMEM columns):
+// One CTA per SM (320 threads, ~197 KB shared memory, all 512 TMEM columns):
 //   warp 0  TMA producer: streams 128x64 A and 256x64 B tiles (128-byte
 //           swizzle) into a 4-stage shared-memory ring, one mbarrier per stage;
 //   warp 1  MMA issuer: one elected lane issues tcgen05.mma (M=128, N=256,
 //           K=16) into one of two TMEM accumulators (2 x 256 fp32 columns),
 //           then tcgen05.commit frees the smem stage / signals the epilogue;
-//   warps 2-5 epilogue: tcgen05.ld of their 32-lane quarter (one output row per
-//           thread), fused elementwise work, vectorised global stores; the
-//           accumulator is handed back so the next tile's MMAs overlap.
+//   warps 2-9 epilogue: two warps per 32-lane TMEM quarter, each taking half of
+//           the tile's columns; tcgen05.ld (one output row per thread), fused
+//           elementwise work, vectorised global stores; the accumulator is
+//           handed back so the next tile's MMAs overlap.
 // Operands may be K-major ([rows, K], K contiguous) or MN-major ([K, rows]);
 // the transposed cases are expressed through the UMMA descriptors, so no
 // operand is ever transposed in memory. Ragged M/N/K edges are zero-filled by
@@ -26,7 +27,8 @@ constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
 constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KB
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t MN_CHUNK_BYTES = 64 * BK * 2;  // one 64(MN) x 64(K) box: 8 KB
-constexpr int GEMM_THREADS = 192;
+constexpr int GEMM_THREADS = 320;
+constexpr int EPI_THREADS = 256;
 constexpr int TMEM_COLS = 512;
 constexpr size_t GEMM_SMEM = STAGES * STAGE_BYTES + 1024 + 256;
 
@@ -57,13 +59,15 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)
 // -------------------------------------------------------------- epilogues
 template <int EPI>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tbase, int row,
-                                              int mt, int nt) {
+                                              int mt, int nt, int half) {
   const Epi& e = p.epi;
   const bool row_ok = row < p.M;
   uint32_t r[32];
+  // this warp's share of the tile: 32-column chunks [c_lo, c_lo + 4)
+  const int c_lo = half * (BN / 64);
   if constexpr (EPI == EPI_BF16 || EPI == EPI_F32 || EPI == EPI_F32_RESID) {
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = c_lo; c < c_lo + BN / 64; ++c) {
       const int col0 = nt * BN + c * 32;
       if (col0 >= p.N) break;
       tmem_ld32(tbase + c * 32, r);
@@ -118,7 +122,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tbas
     // accumulator columns [0,128) = gate, [128,256) = up for I-columns nt*128 + [0,128)
     uint32_t u[32];
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 2 * half; c < 2 * half + 2; ++c) {
       const int col0 = nt * 128 + c * 32;
       if (col0 >= e.half) break;
       tmem_ld32(tbase + c * 32, r);
@@ -160,61 +164,86 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tbas
       }
     }
   } else if constexpr (EPI == EPI_SWIGLU_BWD) {
-#pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    // g and u of the next chunk are loaded while the current one is computed
+    uint4 vg[2][4], vu[2][4];
+    auto load_aux = [&](int c, int slot) {
       const int col0 = nt * BN + c * 32;
-      if (col0 >= p.N) break;
-      tmem_ld32(tbase + c * 32, r);
-      tmem_ld_wait();
-      if (!row_ok) continue;
+      if (!row_ok || col0 >= p.N) return;
       const bf16* gp = e.aux + (int64_t)row * e.ld_aux + col0;
       const bf16* up = gp + e.half;
-      bf16* dgp = reinterpret_cast<bf16*>(e.out) + (int64_t)row * e.ld_out + col0;
-      bf16* dup = dgp + e.half;
       if (col0 + 32 <= p.N) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const uint4 vg = reinterpret_cast<const uint4*>(gp)[j];
-          const uint4 vu = reinterpret_cast<const uint4*>(up)[j];
-          const uint32_t* pg = &vg.x;
-          const uint32_t* pu = &vu.x;
-          uint4 odg, odu;
-          uint32_t* pdg = &odg.x;
-          uint32_t* pdu = &odu.x;
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            float dgv[2], duv[2];
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-              const float g = q ? bf16hi(pg[h]) : bf16lo(pg[h]);
-              const float uu = q ? bf16hi(pu[h]) : bf16lo(pu[h]);
-              const float ds = __uint_as_float(r[8 * j + 2 * h + q]);
-              const float sg = 1.0f / (1.0f + __expf(-g));
-              dgv[q] = ds * uu * sg * (1.0f + g * (1.0f - sg));
-              duv[q] = ds * g * sg;
-            }
-            pdg[h] = pack_bf16x2(dgv[0], dgv[1]);
-            pdu[h] = pack_bf16x2(duv[0], duv[1]);
-          }
-          reinterpret_cast<uint4*>(dgp)[j] = odg;
-          reinterpret_cast<uint4*>(dup)[j] = odu;
+          vg[slot][j] = reinterpret_cast<const uint4*>(gp)[j];
+          vu[slot][j] = reinterpret_cast<const uint4*>(up)[j];
         }
       } else {
-        #pragma unroll
-          for (int j = 0; j < 32; ++j) if (col0 + j < p.N) {
-          const float g = __bfloat162float(gp[j]), uu = __bfloat162float(up[j]);
-          const float ds = __uint_as_float(r[j]);
-          const float sg = 1.0f / (1.0f + __expf(-g));
-          dgp[j] = __float2bfloat16_rn(ds * uu * sg * (1.0f + g * (1.0f - sg)));
-          dup[j] = __float2bfloat16_rn(ds * g * sg);
+        uint16_t* pg = reinterpret_cast<uint16_t*>(&vg[slot][0]);
+        uint16_t* pu = reinterpret_cast<uint16_t*>(&vu[slot][0]);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          pg[j] = (col0 + j < p.N) ? reinterpret_cast<const uint16_t*>(gp)[j] : 0;
+          pu[j] = (col0 + j < p.N) ? reinterpret_cast<const uint16_t*>(up)[j] : 0;
         }
+      }
+    };
+    load_aux(c_lo, 0);
+#pragma unroll
+    for (int ci = 0; ci < BN / 64; ++ci) {
+      const int c = c_lo + ci;
+      const int col0 = nt * BN + c * 32;
+      if (col0 >= p.N) break;
+      tmem_ld32(tbase + c * 32, r);
+      if (ci + 1 < BN / 64) load_aux(c + 1, (ci + 1) & 1);
+      tmem_ld_wait();
+      if (!row_ok) continue;
+      bf16* dgp = reinterpret_cast<bf16*>(e.out) + (int64_t)row * e.ld_out + col0;
+      bf16* dup = dgp + e.half;
+      uint4 odg[4], odu[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t* pg = &vg[ci & 1][j].x;
+        const uint32_t* pu = &vu[ci & 1][j].x;
+        uint32_t* pdg = &odg[j].x;
+        uint32_t* pdu = &odu[j].x;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          float dgv[2], duv[2];
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const float g = q ? bf16hi(pg[h]) : bf16lo(pg[h]);
+            const float uu = q ? bf16hi(pu[h]) : bf16lo(pu[h]);
+            const float ds = __uint_as_float(r[8 * j + 2 * h + q]);
+            const float sg = 1.0f / (1.0f + __expf(-g));
+            dgv[q] = ds * uu * sg * (1.0f + g * (1.0f - sg));
+            duv[q] = ds * g * sg;
+          }
+          pdg[h] = pack_bf16x2(dgv[0], dgv[1]);
+          pdu[h] = pack_bf16x2(duv[0], duv[1]);
+        }
+      }
+      if (col0 + 32 <= p.N) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          reinterpret_cast<uint4*>(dgp)[j] = odg[j];
+          reinterpret_cast<uint4*>(dup)[j] = odu[j];
+        }
+      } else {
+        const uint16_t* sg16 = reinterpret_cast<const uint16_t*>(&odg[0]);
+        const uint16_t* su16 = reinterpret_cast<const uint16_t*>(&odu[0]);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (col0 + j < p.N) {
+            reinterpret_cast<uint16_t*>(dgp)[j] = sg16[j];
+            reinterpret_cast<uint16_t*>(dup)[j] = su16[j];
+          }
       }
     }
   } else if constexpr (EPI == EPI_CE) {
     float mx = -INFINITY, sum = 0.f;
     const int tgt = row_ok ? e.targets[row] : -1;
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = c_lo; c < c_lo + BN / 64; ++c) {
       const int col0 = nt * BN + c * 32;
       if (col0 >= p.N) break;
       tmem_ld32(tbase + c * 32, r);
@@ -255,7 +284,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tbas
           if (j < nvalid) out[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
       }
     }
-    if (row_ok) e.part[(int64_t)row * e.part_ld + nt] = make_float2(mx, sum);
+    if (row_ok) e.part[(int64_t)row * e.part_ld + 2 * nt + half] = make_float2(mx, sum);
   }
 }
 
@@ -286,7 +315,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, 128);
+      mbar_init(tempty0 + 8 * a, EPI_THREADS);
     }
     mbar_init(drain, 1);
     fence_mbar_init();
@@ -403,7 +432,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int q = warp & 3;             // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;   // which half of the tile's columns
     int acc = 0;
     uint32_t acc_ph = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
@@ -413,7 +443,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       tc_fence_after();
       const int row = mt * BM + q * 32 + lane;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      epilogue_tile<EPI>(p, tbase, row, mt, nt);
+      epilogue_tile<EPI>(p, tbase, row, mt, nt, half);
       tc_fence_before();
       mbar_arrive(tempty0 + 8 * acc);
       acc ^= 1;

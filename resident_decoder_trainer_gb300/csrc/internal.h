@@ -17,7 +17,7 @@ enum EpiKind : int {
   EPI_F32_RESID = 2,   // out(f32)[r, c] = resid[r, c] + acc
   EPI_SWIGLU = 3,      // B = [Wg; Wu]: gu[r, c] = g, gu[r, half + c] = u, out2[r, c] = silu(g) u
   EPI_SWIGLU_BWD = 4,  // acc = ds: out[r, c] = dg, out[r, half + c] = du from aux = gu
-  EPI_CE = 5,          // acc = logits: out(bf16) = z, part[r, tile] = (max, sum exp), tgt_logit
+  EPI_CE = 5,          // acc = logits: out(bf16) = z, part[r, 2*tile+half] = (max, sum exp), tgt_logit
 };
 
 struct Epi {
@@ -51,8 +51,9 @@ struct Mat {
 cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N, int K,
                  const Epi& epi, int* err, cudaStream_t s, const char** why);
 
-// Number of 256-wide N tiles the CE epilogue produces per row (partials width).
-inline int gemm_n_tiles(int N) { return (N + 255) / 256; }
+// (max, sum exp) partials per row written by the CE epilogue: one per half of
+// every 256-wide N tile.
+inline int ce_partials_per_row(int N) { return 2 * ((N + 255) / 256); }
 
 int num_sms();
 
