@@ -49,6 +49,9 @@ def parse_args():
     ap.add_argument("--impl", choices=["rdt", "reference"], default="rdt")
     ap.add_argument("--workload", default="q4b_full")
     ap.add_argument("--layers", type=int, default=None, help="override the layer count")
+    ap.add_argument("--kernel", choices=["block", "head"], default=None,
+                    help="time one block forward+backward, or the LM head + CE, alone "
+                         "(small device footprint, for per-kernel numbers and ncu captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -328,6 +331,75 @@ def algorithmic_flops(shape):
     return proj + attn
 
 
+# ---------------------------------------------------------- kernel probes
+def run_probe(args):
+    """One block forward+backward (or the fused LM head + CE) of the workload's
+    shapes on device-resident random inputs, timed with CUDA events."""
+    import torch
+    from resident_decoder_trainer_gb300 import build, rdt, synth
+    build.build()
+    shape = synth.WORKLOADS[args.workload]
+    cfg = rdt.Config.from_shape(shape)
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    T = shape.tokens
+    if args.kernel == "block":
+        n = rdt.block_param_count(cfg)
+        w = torch.empty(n, device=dev)
+        for name, (o, c) in rdt.block_param_offsets(cfg).items():
+            if name.startswith("g_"):
+                w[o:o + c].fill_(1.0)
+            else:
+                w[o:o + c].normal_(0, 0.02, generator=gen)
+        wb = torch.empty(n, dtype=torch.bfloat16, device=dev)
+        rdt.cast_bf16(w, wb)
+        saved = torch.empty(rdt.block_saved_bytes(cfg, shape.batch, shape.seq), dtype=torch.uint8,
+                            device=dev)
+        ws = torch.empty(rdt.block_workspace_bytes(cfg, shape.batch, shape.seq),
+                         dtype=torch.uint8, device=dev)
+        x = torch.randn(T, shape.hidden, device=dev, generator=gen)
+        dy = 1e-3 * torch.randn(T, shape.hidden, device=dev, generator=gen)
+        y, dx = torch.empty_like(x), torch.empty_like(x)
+        grads = torch.empty(n, device=dev)
+
+        def run():
+            rdt.block_forward(cfg, shape.batch, shape.seq, w, wb, x, y, saved, ws)
+            rdt.block_backward(cfg, shape.batch, shape.seq, w, wb, x, saved, dy, dx, grads, ws)
+        s1 = shape.replace(layers=1, vocab=0)
+        flops = algorithmic_flops(s1)
+        what = "one block forward+backward"
+    else:
+        h = torch.randn(T, shape.hidden, device=dev, generator=gen)
+        gf = torch.ones(shape.hidden, device=dev)
+        wl = (0.02 * torch.randn(shape.vocab, shape.hidden, device=dev, generator=gen)).to(
+            torch.bfloat16)
+        tg = torch.randint(0, shape.vocab, (T,), device=dev, generator=gen, dtype=torch.int32)
+        ws = torch.empty(rdt.head_workspace_bytes(cfg, T), dtype=torch.uint8, device=dev)
+        loss = torch.empty(T, device=dev)
+        dh, dgf = torch.empty_like(h), torch.empty_like(gf)
+        dwl = torch.empty(shape.vocab, shape.hidden, device=dev)
+
+        def run():
+            rdt.fused_cross_entropy(cfg, T, h, gf, wl, tg, 1.0 / T, loss, dh, dgf, dwl, ws)
+        flops = 6.0 * shape.vocab * shape.hidden * T
+        what = "final RMSNorm + LM head + cross-entropy, forward+backward"
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    return {"probe": args.kernel, "what": what, "workload": args.workload, "tokens": T,
+            "ms": round(ms, 4), "tokens_per_s": round(T / ms * 1e3, 1),
+            "algorithmic_tflops": round(flops / ms / 1e9, 1), "steps": args.steps,
+            "warmup": args.warmup}
+
+
 # ------------------------------------------------------------ reference
 def run_reference(args, rank, world):
     from resident_decoder_trainer_gb300 import synth
@@ -365,6 +437,9 @@ def main():
         if rank != 0:
             return 0
         print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return 0
+    if args.kernel:
+        print(json.dumps(run_probe(args)), flush=True)
         return 0
     if world > 1:
         import torch

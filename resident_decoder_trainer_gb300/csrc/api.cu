@@ -359,8 +359,12 @@ rdt_status rdt_block_forward(const rdt_config* cfg, int32_t batch, int32_t seq, 
                                  w + off[RDT_G_Q], w + off[RDT_G_K], wk.cs, T, seq, (int)m.nh,
                                  (int)m.nkv, (int)m.d, cfg->rms_eps, s));
   // causal GQA attention
-  RDT_CHECK_CUDA(attn_fwd(sv.qr, m.qd, sv.kr, m.kd, sv.qkv + m.qd + m.kd, m.nqkv, sv.o, sv.lse,
-                          batch, seq, (int)m.nh, (int)m.nkv, (int)m.d, s));
+  if (attn_tc_supported((int)m.d, false))
+    RDT_CHECK_CUDA(attn_fwd_tc(sv.qr, m.qd, sv.kr, m.kd, sv.qkv + m.qd + m.kd, m.nqkv, sv.o,
+                               sv.lse, batch, seq, (int)m.nh, (int)m.nkv, (int)m.d, err, s));
+  else
+    RDT_CHECK_CUDA(attn_fwd(sv.qr, m.qd, sv.kr, m.kd, sv.qkv + m.qd + m.kd, m.nqkv, sv.o, sv.lse,
+                            batch, seq, (int)m.nh, (int)m.nkv, (int)m.d, s));
   // O projection + residual: r1 = x + o Wo^T
   {
     Epi e;
@@ -496,9 +500,14 @@ rdt_status rdt_block_backward(const rdt_config* cfg, int32_t batch, int32_t seq,
   // attention backward (GQA reduction inside), dq accumulated in fp32
   RDT_CHECK_CUDA(attn_bwd_pre(sv.o, wk.dout, wk.Dd, batch, seq, (int)m.nh, (int)m.d, s));
   RDT_CHECK_CUDA(cudaMemsetAsync(wk.dq, 0, sizeof(float) * T * m.qd, s));
-  RDT_CHECK_CUDA(attn_bwd(sv.qr, m.qd, sv.kr, m.kd, sv.qkv + m.qd + m.kd, m.nqkv, wk.dout, sv.lse,
-                          wk.Dd, wk.dq, wk.dk, wk.dqkv + m.qd + m.kd, m.nqkv, batch, seq,
-                          (int)m.nh, (int)m.nkv, (int)m.d, s));
+  if (attn_tc_supported((int)m.d, true))
+    RDT_CHECK_CUDA(attn_bwd_tc(sv.qr, m.qd, sv.kr, m.kd, sv.qkv + m.qd + m.kd, m.nqkv, wk.dout,
+                               sv.lse, wk.Dd, wk.dq, wk.dk, wk.dqkv + m.qd + m.kd, m.nqkv, batch,
+                               seq, (int)m.nh, (int)m.nkv, (int)m.d, err, s));
+  else
+    RDT_CHECK_CUDA(attn_bwd(sv.qr, m.qd, sv.kr, m.kd, sv.qkv + m.qd + m.kd, m.nqkv, wk.dout,
+                            sv.lse, wk.Dd, wk.dq, wk.dk, wk.dqkv + m.qd + m.kd, m.nqkv, batch, seq,
+                            (int)m.nh, (int)m.nkv, (int)m.d, s));
   // inverse RoPE + QK-norm backward -> dq, dk columns of dqkv; q/k gain grads
   RDT_CHECK_CUDA(rope_table(wk.cs, seq, (int)m.d, cfg->rope_theta, s));
   RDT_CHECK_CUDA(qknorm_rope_bwd(wk.dq, wk.dk, sv.qkv, m.nqkv, sv.rstd_q, sv.rstd_k,

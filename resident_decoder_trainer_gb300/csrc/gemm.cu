@@ -486,17 +486,21 @@ int num_sms() {
   return n > 0 ? n : 1;
 }
 
-// 2-D bf16 map over [rows, cols] (cols contiguous) with a 64 x box_rows box.
-static bool make_map(CUtensorMap* m, const Mat& x, int box_rows) {
+bool make_tma_2d(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld,
+                 int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(x.cols), static_cast<cuuint64_t>(x.rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(x.ld) * 2};
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
   cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t es[2] = {1u, 1u};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x.ptr), dims, strides, box,
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static bool make_map(CUtensorMap* m, const Mat& x, int box_rows) {
+  return make_tma_2d(m, x.ptr, x.rows, x.cols, x.ld, box_rows);
 }
 
 template <int A_MN, int B_MN, int EPI>

@@ -57,6 +57,11 @@ inline int ce_partials_per_row(int N) { return 2 * ((N + 255) / 256); }
 
 int num_sms();
 
+// 2-D bf16 TMA map over a row-major [rows, cols] matrix (row stride ld
+// elements) with a box of 64 columns x box_rows rows and 128-byte swizzle.
+bool make_tma_2d(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld,
+                 int box_rows);
+
 // Sets the thread-local message returned by rdt_last_error().
 void set_last_error(const char* msg);
 
@@ -124,5 +129,17 @@ cudaError_t attn_bwd(const bf16* q, int64_t ldq, const bf16* k, int64_t ldk, con
                      int64_t ldv, const bf16* dout, const float* lse, const float* D, float* dq,
                      float* dk, bf16* dv, int64_t lddv, int B, int S, int nh, int nkv, int d,
                      cudaStream_t s);
+
+// tcgen05 flash attention (attention_tc.cu): forward for head_dim 64/128,
+// backward for head_dim 128; same arguments as attn_fwd / attn_bwd plus the
+// device error word for bounded waits.
+bool attn_tc_supported(int d, bool backward);
+cudaError_t attn_fwd_tc(const bf16* q, int64_t ldq, const bf16* k, int64_t ldk, const bf16* v,
+                        int64_t ldv, bf16* o, float* lse, int B, int S, int nh, int nkv, int d,
+                        int* err, cudaStream_t s);
+cudaError_t attn_bwd_tc(const bf16* q, int64_t ldq, const bf16* k, int64_t ldk, const bf16* v,
+                        int64_t ldv, const bf16* dout, const float* lse, const float* D,
+                        float* dq, float* dk, bf16* dv, int64_t lddv, int B, int S, int nh,
+                        int nkv, int d, int* err, cudaStream_t s);
 
 }  // namespace rdt

@@ -80,6 +80,17 @@ def test_block_parity_head_dim_128_mha_odd_seq():
                              intermediate=1376, seq=131, batch=1), seed=3)
 
 
+def test_block_parity_head_dim_128_gqa4_two_sequences():
+    _block_case(ragged_shape(layers=1, hidden=512, n_heads=8, n_kv_heads=2, head_dim=128,
+                             intermediate=1376, seq=300, batch=2), seed=7)
+
+
+def test_block_parity_head_dim_128_long_sequence():
+    # several 128-key tiles per sequence: online-softmax rescaling, multi-tile dK/dV
+    _block_case(ragged_shape(layers=1, hidden=256, n_heads=2, n_kv_heads=1, head_dim=128,
+                             intermediate=512, seq=700, batch=1), seed=9)
+
+
 def test_block_parity_head_dim_32_gqa4():
     _block_case(ragged_shape(layers=1, hidden=128, n_heads=8, n_kv_heads=2, head_dim=32,
                              intermediate=352, seq=97, batch=3), seed=5)
