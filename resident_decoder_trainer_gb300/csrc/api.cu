@@ -156,7 +156,7 @@ size_t carve_saved(const Dims& m, int64_t B, int64_t S, void* base, Saved* sv) {
 struct BlockWs {
   float* cs;
   bf16 *dy_b, *dgu, *dr1_b, *dout, *dqkv;
-  float *dxn, *dr1, *Dd, *dq, *dk, *partials;
+  float *dxn, *dr1, *Dd, *lse2, *dq, *dk, *partials;
 };
 size_t carve_block_ws(const Dims& m, int64_t B, int64_t S, void* base, BlockWs* w) {
   const int64_t T = B * S;
@@ -170,7 +170,8 @@ size_t carve_block_ws(const Dims& m, int64_t B, int64_t S, void* base, BlockWs* 
   t.dqkv = c.take<bf16>(T * m.nqkv);
   t.dxn = c.take<float>(T * m.H);
   t.dr1 = c.take<float>(T * m.H);
-  t.Dd = c.take<float>(B * m.nh * S);
+  t.Dd = c.take<float>(B * m.nh * attn_lse_pad((int)S));
+  t.lse2 = c.take<float>(B * m.nh * attn_lse_pad((int)S));
   t.dq = c.take<float>(T * m.qd);
   t.dk = c.take<float>(T * m.kd);
   const int64_t pw = m.H > 2 * m.d ? m.H : 2 * m.d;
@@ -498,16 +499,26 @@ rdt_status rdt_block_backward(const rdt_config* cfg, int32_t batch, int32_t seq,
              (int)m.qd, T, e, err, s);
   }
   // attention backward (GQA reduction inside), dq accumulated in fp32
-  RDT_CHECK_CUDA(attn_bwd_pre(sv.o, wk.dout, wk.Dd, batch, seq, (int)m.nh, (int)m.d, s));
-  RDT_CHECK_CUDA(cudaMemsetAsync(wk.dq, 0, sizeof(float) * T * m.qd, s));
-  if (attn_tc_supported((int)m.d, true))
+  if (attn_tc_supported((int)m.d, true)) {
+    // tensor-core backward: padded log2-LSE / D rows; every dq element written once
+    const int S_pad = attn_lse_pad(seq);
+    if (S_pad != seq) {
+      RDT_CHECK_CUDA(cudaMemsetAsync(wk.Dd, 0, sizeof(float) * batch * m.nh * S_pad, s));
+      RDT_CHECK_CUDA(cudaMemsetAsync(wk.lse2, 0, sizeof(float) * batch * m.nh * S_pad, s));
+    }
+    RDT_CHECK_CUDA(attn_bwd_pre(sv.o, wk.dout, sv.lse, wk.Dd, wk.lse2, batch, seq, S_pad,
+                                (int)m.nh, (int)m.d, s));
     RDT_CHECK_CUDA(attn_bwd_tc(sv.qr, m.qd, sv.kr, m.kd, sv.qkv + m.qd + m.kd, m.nqkv, wk.dout,
-                               sv.lse, wk.Dd, wk.dq, wk.dk, wk.dqkv + m.qd + m.kd, m.nqkv, batch,
+                               wk.lse2, wk.Dd, wk.dq, wk.dk, wk.dqkv + m.qd + m.kd, m.nqkv, batch,
                                seq, (int)m.nh, (int)m.nkv, (int)m.d, err, s));
-  else
+  } else {
+    RDT_CHECK_CUDA(attn_bwd_pre(sv.o, wk.dout, sv.lse, wk.Dd, nullptr, batch, seq, seq,
+                                (int)m.nh, (int)m.d, s));
+    RDT_CHECK_CUDA(cudaMemsetAsync(wk.dq, 0, sizeof(float) * T * m.qd, s));
     RDT_CHECK_CUDA(attn_bwd(sv.qr, m.qd, sv.kr, m.kd, sv.qkv + m.qd + m.kd, m.nqkv, wk.dout,
                             sv.lse, wk.Dd, wk.dq, wk.dk, wk.dqkv + m.qd + m.kd, m.nqkv, batch, seq,
                             (int)m.nh, (int)m.nkv, (int)m.d, s));
+  }
   // inverse RoPE + QK-norm backward -> dq, dk columns of dqkv; q/k gain grads
   RDT_CHECK_CUDA(rope_table(wk.cs, seq, (int)m.d, cfg->rope_theta, s));
   RDT_CHECK_CUDA(qknorm_rope_bwd(wk.dq, wk.dk, sv.qkv, m.nqkv, sv.rstd_q, sv.rstd_k,

@@ -211,10 +211,14 @@ __global__ void __launch_bounds__(256) attn_fwd_kernel(const bf16* __restrict__ 
 
 // ------------------------------------------------------ backward: D = rowsum(dO o O)
 // d/8 lanes per (token, head), 8 bf16 (16 bytes) per lane and operand.
+// Writes D[(b*nh + h)*S_ld + s] and, if lse2 is given, lse2 (same index) =
+// lse[(b*nh + h)*S + s] * log2(e).
 __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const bf16* __restrict__ o,
                                                            const bf16* __restrict__ dout,
-                                                           float* __restrict__ Dd, int T, int S,
-                                                           int nh, int d) {
+                                                           const float* __restrict__ lse,
+                                                           float* __restrict__ Dd,
+                                                           float* __restrict__ lse2, int T, int S,
+                                                           int S_ld, int nh, int d) {
   const int lph = d / 8;
   const int64_t gthread = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t item = gthread / lph;  // (token, head)
@@ -233,7 +237,9 @@ __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const bf16* __restric
   if (valid && sub == 0) {
     const int t = static_cast<int>(item / nh), h = static_cast<int>(item % nh);
     const int b = t / S, s = t % S;
-    Dd[((int64_t)b * nh + h) * S + s] = acc;
+    const int64_t bh = (int64_t)b * nh + h;
+    Dd[bh * S_ld + s] = acc;
+    if (lse2) lse2[bh * S_ld + s] = lse[bh * S + s] * kLog2e;
   }
 }
 
@@ -508,13 +514,13 @@ cudaError_t attn_fwd(const bf16* q, int64_t ldq, const bf16* k, int64_t ldk, con
   }
 }
 
-cudaError_t attn_bwd_pre(const bf16* o, const bf16* dout, float* Dd, int B, int S, int nh, int d,
-                         cudaStream_t s) {
+cudaError_t attn_bwd_pre(const bf16* o, const bf16* dout, const float* lse, float* Dd,
+                         float* lse2, int B, int S, int S_ld, int nh, int d, cudaStream_t s) {
   const int T = B * S;
   const int64_t threads = (int64_t)T * nh * (d / 8);
   const int blocks = (int)((threads + 255) / 256);
   note_launch();
-  attn_bwd_pre_kernel<<<blocks, 256, 0, s>>>(o, dout, Dd, T, S, nh, d);
+  attn_bwd_pre_kernel<<<blocks, 256, 0, s>>>(o, dout, lse, Dd, lse2, T, S, S_ld, nh, d);
   return cudaGetLastError();
 }
 

@@ -120,9 +120,12 @@ cudaError_t adamw(float* w, const float* g, float* m, float* v, int64_t n, const
 cudaError_t attn_fwd(const bf16* q, int64_t ldq, const bf16* k, int64_t ldk, const bf16* v,
                      int64_t ldv, bf16* o, float* lse, int B, int S, int nh, int nkv, int d,
                      cudaStream_t s);
-// D[b, h, s] = sum_d dO * O
-cudaError_t attn_bwd_pre(const bf16* o, const bf16* dout, float* D, int B, int S, int nh, int d,
-                         cudaStream_t s);
+// D[(b*nh + h)*S_ld + s] = sum_d dO * O; if lse2 != null also
+// lse2[same] = lse[(b*nh + h)*S + s] * log2(e).
+cudaError_t attn_bwd_pre(const bf16* o, const bf16* dout, const float* lse, float* D,
+                         float* lse2, int B, int S, int S_ld, int nh, int d, cudaStream_t s);
+// Row stride (>= S, multiple of 64) of the D / lse2 arrays the tensor-core backward reads.
+int attn_lse_pad(int S);
 // dq (fp32 [T, nh*d], must be zeroed; accumulated), dk fp32 [T, nkv*d],
 // dv bf16 written at dv + t*lddv + g*d.
 cudaError_t attn_bwd(const bf16* q, int64_t ldq, const bf16* k, int64_t ldk, const bf16* v,
@@ -132,7 +135,9 @@ cudaError_t attn_bwd(const bf16* q, int64_t ldq, const bf16* k, int64_t ldk, con
 
 // tcgen05 flash attention (attention_tc.cu): forward for head_dim 64/128,
 // backward for head_dim 128; same arguments as attn_fwd / attn_bwd plus the
-// device error word for bounded waits.
+// device error word for bounded waits. The backward reads lse2 (log2-domain
+// LSE) and D in the padded [B*nh, attn_lse_pad(S)] layout and writes every
+// dq element (no zeroing needed).
 bool attn_tc_supported(int d, bool backward);
 cudaError_t attn_fwd_tc(const bf16* q, int64_t ldq, const bf16* k, int64_t ldk, const bf16* v,
                         int64_t ldv, bf16* o, float* lse, int B, int S, int nh, int nkv, int d,
