@@ -137,7 +137,7 @@ class OracleSample:
     `head_tokens` tokens (x tokens per step), and clip + AdamW on `opt_params`
     parameters (x total parameters). Inputs are drawn once (seeded)."""
 
-    def __init__(self, shape, seq_tokens=512, head_tokens=256, opt_params=1 << 24, seed=0):
+    def __init__(self, shape, seq_tokens=1024, head_tokens=512, opt_params=1 << 25, seed=0):
         import numpy as np
         import torch
         from oracle import model as om

@@ -127,8 +127,8 @@ void block_offsets(const Dims& m, int64_t* off) {
 
 // Saved activations of one block.
 struct Saved {
-  bf16 *xn, *qkv, *qr, *kr, *o, *xn2, *gu, *s;
-  float *rstd1, *rstd_q, *rstd_k, *lse, *r1, *rstd2;
+  bf16 *xn, *vb, *qr, *kr, *o, *xn2, *gu, *s;
+  float *qkv, *rstd1, *rstd_q, *rstd_k, *lse, *r1, *rstd2;
 };
 size_t carve_saved(const Dims& m, int64_t B, int64_t S, void* base, Saved* sv) {
   const int64_t T = B * S;
@@ -136,7 +136,8 @@ size_t carve_saved(const Dims& m, int64_t B, int64_t S, void* base, Saved* sv) {
   Saved t;
   t.xn = c.take<bf16>(T * m.H);
   t.rstd1 = c.take<float>(T);
-  t.qkv = c.take<bf16>(T * m.nqkv);
+  t.qkv = c.take<float>(T * m.nqkv);  // raw projections, fp32 (QK-norm input)
+  t.vb = c.take<bf16>(T * m.kd);      // v as the attention operand
   t.qr = c.take<bf16>(T * m.qd);
   t.kr = c.take<bf16>(T * m.kd);
   t.rstd_q = c.take<float>(T * m.nh);
@@ -345,10 +346,10 @@ rdt_status rdt_block_forward(const rdt_config* cfg, int32_t batch, int32_t seq, 
 
   // input RMSNorm
   RDT_CHECK_CUDA(rmsnorm_fwd(x, w + off[RDT_G_ATTN], sv.xn, sv.rstd1, T, (int)m.H, cfg->rms_eps, s));
-  // stacked Q/K/V projection: qkv[T, qd+2kd] = xn [Wq; Wk; Wv]^T
+  // stacked Q/K/V projection: qkv[T, qd+2kd] = xn [Wq; Wk; Wv]^T (fp32)
   {
     Epi e;
-    e.kind = EPI_BF16;
+    e.kind = EPI_F32;
     e.out = sv.qkv;
     e.ld_out = m.nqkv;
     RDT_GEMM(Mat{sv.xn, T, m.H, m.H}, false, Mat{wb + off[RDT_WQ], m.nqkv, m.H, m.H}, false, T,
@@ -356,15 +357,15 @@ rdt_status rdt_block_forward(const rdt_config* cfg, int32_t batch, int32_t seq, 
   }
   // per-head QK RMSNorm + RoPE-neox
   RDT_CHECK_CUDA(rope_table(wk.cs, seq, (int)m.d, cfg->rope_theta, s));
-  RDT_CHECK_CUDA(qknorm_rope_fwd(sv.qkv, m.nqkv, sv.qr, sv.kr, sv.rstd_q, sv.rstd_k,
+  RDT_CHECK_CUDA(qknorm_rope_fwd(sv.qkv, m.nqkv, sv.qr, sv.kr, sv.vb, sv.rstd_q, sv.rstd_k,
                                  w + off[RDT_G_Q], w + off[RDT_G_K], wk.cs, T, seq, (int)m.nh,
                                  (int)m.nkv, (int)m.d, cfg->rms_eps, s));
   // causal GQA attention
   if (attn_tc_supported((int)m.d, false))
-    RDT_CHECK_CUDA(attn_fwd_tc(sv.qr, m.qd, sv.kr, m.kd, sv.qkv + m.qd + m.kd, m.nqkv, sv.o,
+    RDT_CHECK_CUDA(attn_fwd_tc(sv.qr, m.qd, sv.kr, m.kd, sv.vb, m.kd, sv.o,
                                sv.lse, batch, seq, (int)m.nh, (int)m.nkv, (int)m.d, err, s));
   else
-    RDT_CHECK_CUDA(attn_fwd(sv.qr, m.qd, sv.kr, m.kd, sv.qkv + m.qd + m.kd, m.nqkv, sv.o, sv.lse,
+    RDT_CHECK_CUDA(attn_fwd(sv.qr, m.qd, sv.kr, m.kd, sv.vb, m.kd, sv.o, sv.lse,
                             batch, seq, (int)m.nh, (int)m.nkv, (int)m.d, s));
   // O projection + residual: r1 = x + o Wo^T
   {
@@ -508,14 +509,14 @@ rdt_status rdt_block_backward(const rdt_config* cfg, int32_t batch, int32_t seq,
     }
     RDT_CHECK_CUDA(attn_bwd_pre(sv.o, wk.dout, sv.lse, wk.Dd, wk.lse2, batch, seq, S_pad,
                                 (int)m.nh, (int)m.d, s));
-    RDT_CHECK_CUDA(attn_bwd_tc(sv.qr, m.qd, sv.kr, m.kd, sv.qkv + m.qd + m.kd, m.nqkv, wk.dout,
+    RDT_CHECK_CUDA(attn_bwd_tc(sv.qr, m.qd, sv.kr, m.kd, sv.vb, m.kd, wk.dout,
                                wk.lse2, wk.Dd, wk.dq, wk.dk, wk.dqkv + m.qd + m.kd, m.nqkv, batch,
                                seq, (int)m.nh, (int)m.nkv, (int)m.d, err, s));
   } else {
     RDT_CHECK_CUDA(attn_bwd_pre(sv.o, wk.dout, sv.lse, wk.Dd, nullptr, batch, seq, seq,
                                 (int)m.nh, (int)m.d, s));
     RDT_CHECK_CUDA(cudaMemsetAsync(wk.dq, 0, sizeof(float) * T * m.qd, s));
-    RDT_CHECK_CUDA(attn_bwd(sv.qr, m.qd, sv.kr, m.kd, sv.qkv + m.qd + m.kd, m.nqkv, wk.dout,
+    RDT_CHECK_CUDA(attn_bwd(sv.qr, m.qd, sv.kr, m.kd, sv.vb, m.kd, wk.dout,
                             sv.lse, wk.Dd, wk.dq, wk.dk, wk.dqkv + m.qd + m.kd, m.nqkv, batch, seq,
                             (int)m.nh, (int)m.nkv, (int)m.d, s));
   }

@@ -228,17 +228,19 @@ cudaError_t rope_table(float* cs, int S, int d, float theta, cudaStream_t s) {
 // (16-byte loads); a warp covers 256/D heads per iteration. Lanes of the first
 // half of a head hold elements i < D/2, their partner (lane ^ D/16) the
 // rotation partners i + D/2.
+// Items are (token, head) over nh query heads, nkv key heads and nkv value
+// heads; value heads are only converted to bf16 for the attention.
 template <int D>
 __global__ void __launch_bounds__(256) qknorm_rope_fwd_kernel(
-    const bf16* __restrict__ qkv, int64_t ld, bf16* __restrict__ qo, bf16* __restrict__ ko,
-    float* __restrict__ rq, float* __restrict__ rk, const float* __restrict__ gq,
-    const float* __restrict__ gk, const float2* __restrict__ cs, int T, int S, int nh, int nkv,
-    float eps) {
+    const float* __restrict__ qkv, int64_t ld, bf16* __restrict__ qo, bf16* __restrict__ ko,
+    bf16* __restrict__ vo, float* __restrict__ rq, float* __restrict__ rk,
+    const float* __restrict__ gq, const float* __restrict__ gk, const float2* __restrict__ cs,
+    int T, int S, int nh, int nkv, float eps) {
   constexpr int LPH = D / 8, HPW = 32 / LPH, HALF = D / 2, PX = LPH / 2;
   const int lane = threadIdx.x & 31;
   const int slot = lane / LPH, sub = lane % LPH;
   const bool first = sub < PX;
-  const int heads = nh + nkv;
+  const int heads = nh + 2 * nkv;
   const int64_t items = (int64_t)T * heads;
   const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -248,15 +250,20 @@ __global__ void __launch_bounds__(256) qknorm_rope_fwd_kernel(
     const int t = valid ? static_cast<int>(item / heads) : 0;
     const int hd = valid ? static_cast<int>(item % heads) : 0;
     const bool isq = hd < nh;
-    const int h = isq ? hd : hd - nh;
-    const bf16* src = qkv + (int64_t)t * ld + (isq ? h * D : nh * D + h * D) + 8 * sub;
-    float xv[8];
-    uint4 raw = valid ? *reinterpret_cast<const uint4*>(src) : make_uint4(0, 0, 0, 0);
-    const uint32_t* rw = &raw.x;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      xv[2 * e] = bf16lo(rw[e]);
-      xv[2 * e + 1] = bf16hi(rw[e]);
+    const bool isv = hd >= nh + nkv;
+    const int h = isq ? hd : (isv ? hd - nh - nkv : hd - nh);
+    const float* src = qkv + (int64_t)t * ld + hd * D + 8 * sub;
+    float xv[8] = {};
+    if (valid) {
+      const float4 a = *reinterpret_cast<const float4*>(src);
+      const float4 c = *reinterpret_cast<const float4*>(src + 4);
+      xv[0] = a.x; xv[1] = a.y; xv[2] = a.z; xv[3] = a.w;
+      xv[4] = c.x; xv[5] = c.y; xv[6] = c.z; xv[7] = c.w;
+    }
+    if (valid && isv) {
+      *reinterpret_cast<uint4*>(vo + (int64_t)t * nkv * D + h * D + 8 * sub) =
+          make_uint4(pack_bf16x2(xv[0], xv[1]), pack_bf16x2(xv[2], xv[3]),
+                     pack_bf16x2(xv[4], xv[5]), pack_bf16x2(xv[6], xv[7]));
     }
     float ss = 0.f;
 #pragma unroll
@@ -279,7 +286,7 @@ __global__ void __launch_bounds__(256) qknorm_rope_fwd_kernel(
       const float2 cv = c[e];
       out[e] = first ? y[e] * cv.x - yp[e] * cv.y : y[e] * cv.x + yp[e] * cv.y;
     }
-    if (valid) {
+    if (valid && !isv) {
       bf16* dst = (isq ? qo + (int64_t)t * nh * D + h * D : ko + (int64_t)t * nkv * D + h * D) +
                   8 * sub;
       *reinterpret_cast<uint4*>(dst) =
@@ -299,19 +306,19 @@ static int elementwise_grid(int64_t warps_needed) {
   return static_cast<int>(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
 }
 
-cudaError_t qknorm_rope_fwd(const bf16* qkv, int64_t ld_qkv, bf16* q_out, bf16* k_out,
-                            float* rstd_q, float* rstd_k, const float* gq, const float* gk,
-                            const float* cs, int T, int S, int nh, int nkv, int d, float eps,
-                            cudaStream_t s) {
-  const int64_t items = (int64_t)T * (nh + nkv);
+cudaError_t qknorm_rope_fwd(const float* qkv, int64_t ld_qkv, bf16* q_out, bf16* k_out,
+                            bf16* v_out, float* rstd_q, float* rstd_k, const float* gq,
+                            const float* gk, const float* cs, int T, int S, int nh, int nkv, int d,
+                            float eps, cudaStream_t s) {
+  const int64_t items = (int64_t)T * (nh + 2 * nkv);
   const int grid = elementwise_grid((items * d + 255) / 256);
   const float2* c2 = reinterpret_cast<const float2*>(cs);
   note_launch();
   switch (d) {
-    case 16: qknorm_rope_fwd_kernel<16><<<grid, 256, 0, s>>>(qkv, ld_qkv, q_out, k_out, rstd_q, rstd_k, gq, gk, c2, T, S, nh, nkv, eps); break;
-    case 32: qknorm_rope_fwd_kernel<32><<<grid, 256, 0, s>>>(qkv, ld_qkv, q_out, k_out, rstd_q, rstd_k, gq, gk, c2, T, S, nh, nkv, eps); break;
-    case 64: qknorm_rope_fwd_kernel<64><<<grid, 256, 0, s>>>(qkv, ld_qkv, q_out, k_out, rstd_q, rstd_k, gq, gk, c2, T, S, nh, nkv, eps); break;
-    case 128: qknorm_rope_fwd_kernel<128><<<grid, 256, 0, s>>>(qkv, ld_qkv, q_out, k_out, rstd_q, rstd_k, gq, gk, c2, T, S, nh, nkv, eps); break;
+    case 16: qknorm_rope_fwd_kernel<16><<<grid, 256, 0, s>>>(qkv, ld_qkv, q_out, k_out, v_out, rstd_q, rstd_k, gq, gk, c2, T, S, nh, nkv, eps); break;
+    case 32: qknorm_rope_fwd_kernel<32><<<grid, 256, 0, s>>>(qkv, ld_qkv, q_out, k_out, v_out, rstd_q, rstd_k, gq, gk, c2, T, S, nh, nkv, eps); break;
+    case 64: qknorm_rope_fwd_kernel<64><<<grid, 256, 0, s>>>(qkv, ld_qkv, q_out, k_out, v_out, rstd_q, rstd_k, gq, gk, c2, T, S, nh, nkv, eps); break;
+    case 128: qknorm_rope_fwd_kernel<128><<<grid, 256, 0, s>>>(qkv, ld_qkv, q_out, k_out, v_out, rstd_q, rstd_k, gq, gk, c2, T, S, nh, nkv, eps); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -325,7 +332,7 @@ cudaError_t qknorm_rope_fwd(const bf16* qkv, int64_t ld_qkv, bf16* q_out, bf16* 
 // and each CTA writes one partial row [q gains | k gains].
 template <int D>
 __global__ void __launch_bounds__(256) qknorm_rope_bwd_kernel(
-    const float* __restrict__ dq, const float* __restrict__ dk, const bf16* __restrict__ qkv,
+    const float* __restrict__ dq, const float* __restrict__ dk, const float* __restrict__ qkv,
     int64_t ld, const float* __restrict__ rq, const float* __restrict__ rk,
     const float* __restrict__ gq, const float* __restrict__ gk, const float2* __restrict__ cs,
     bf16* __restrict__ dqkv, float* __restrict__ partials, int T, int S, int nh, int nkv) {
@@ -363,13 +370,10 @@ __global__ void __launch_bounds__(256) qknorm_rope_bwd_kernel(
       const float4 d1 = *reinterpret_cast<const float4*>(gsrc + 4);
       din[0] = d0.x; din[1] = d0.y; din[2] = d0.z; din[3] = d0.w;
       din[4] = d1.x; din[5] = d1.y; din[6] = d1.z; din[7] = d1.w;
-      const uint4 raw = *reinterpret_cast<const uint4*>(qkv + (int64_t)t * ld + col);
-      const uint32_t* rw = &raw.x;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        xv[2 * e] = bf16lo(rw[e]);
-        xv[2 * e + 1] = bf16hi(rw[e]);
-      }
+      const float4 xa = *reinterpret_cast<const float4*>(qkv + (int64_t)t * ld + col);
+      const float4 xb = *reinterpret_cast<const float4*>(qkv + (int64_t)t * ld + col + 4);
+      xv[0] = xa.x; xv[1] = xa.y; xv[2] = xa.z; xv[3] = xa.w;
+      xv[4] = xb.x; xv[5] = xb.y; xv[6] = xb.z; xv[7] = xb.w;
       r = isq ? rq[(int64_t)t * nh + h] : rk[(int64_t)t * nkv + h];
     }
     float dp[8];
@@ -434,7 +438,7 @@ int qknorm_bwd_partial_rows(int T, int heads) {
   return want < cap ? static_cast<int>(want > 0 ? want : 1) : cap;
 }
 
-cudaError_t qknorm_rope_bwd(const float* dq, const float* dk, const bf16* qkv, int64_t ld_qkv,
+cudaError_t qknorm_rope_bwd(const float* dq, const float* dk, const float* qkv, int64_t ld_qkv,
                             const float* rstd_q, const float* rstd_k, const float* gq,
                             const float* gk, const float* cs, bf16* dqkv, float* dg_qk,
                             float* partials, int T, int S, int nh, int nkv, int d,

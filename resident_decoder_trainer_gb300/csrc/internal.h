@@ -87,12 +87,14 @@ cudaError_t rmsnorm_bwd(const float* dy, const float* x, const float* rstd, cons
 int rmsnorm_bwd_partial_rows(int T);
 
 cudaError_t rope_table(float* cs, int S, int d, float theta, cudaStream_t s);
-cudaError_t qknorm_rope_fwd(const bf16* qkv, int64_t ld_qkv, bf16* q_out, bf16* k_out,
-                            float* rstd_q, float* rstd_k, const float* gq, const float* gk,
-                            const float* cs, int T, int S, int nh, int nkv, int d, float eps,
-                            cudaStream_t s);
+// qkv: fp32 raw projections [T, ld] (q | k | v); writes the normalised and
+// rotated q, k and a bf16 copy of v.
+cudaError_t qknorm_rope_fwd(const float* qkv, int64_t ld_qkv, bf16* q_out, bf16* k_out,
+                            bf16* v_out, float* rstd_q, float* rstd_k, const float* gq,
+                            const float* gk, const float* cs, int T, int S, int nh, int nkv, int d,
+                            float eps, cudaStream_t s);
 // dg_qk: 2*d floats, q-gain gradient then k-gain gradient.
-cudaError_t qknorm_rope_bwd(const float* dq, const float* dk, const bf16* qkv, int64_t ld_qkv,
+cudaError_t qknorm_rope_bwd(const float* dq, const float* dk, const float* qkv, int64_t ld_qkv,
                             const float* rstd_q, const float* rstd_k, const float* gq,
                             const float* gk, const float* cs, bf16* dqkv, float* dg_qk,
                             float* partials, int T, int S, int nh, int nkv, int d,
