@@ -1,5 +1,6 @@
 // Causal grouped-query flash attention, forward and backward (bf16 operands,
-// fp32 softmax and accumulation), for head_dim 16/32/64/128.
+// fp32 softmax and accumulation) on mma.sync tiles, for the small head_dim 16
+// and 32; head_dim 64 and 128 run on the tcgen05 kernels (attention_tc.cu).
 //
 // Forward: one CTA per (128-query tile, query head, sequence); 8 warps own 16
 // query rows each; K/V tiles of 64 keys stream through a cp.async double
@@ -12,7 +13,7 @@
 // nh/nkv query heads of its group and over the query tiles at or below the
 // diagonal. dK and dV of the whole group accumulate in registers (the GQA
 // reduction is free); dQ is accumulated into an fp32 buffer with vector
-// reductions.
+// reductions, so its last bits depend on the order the CTAs run in.
 #include "common.cuh"
 #include "internal.h"
 
@@ -508,8 +509,6 @@ cudaError_t attn_fwd(const bf16* q, int64_t ldq, const bf16* k, int64_t ldk, con
   switch (d) {
     case 16: return fwd_d<16>(q, ldq, k, ldk, v, ldv, o, lse, B, S, nh, nkv, s);
     case 32: return fwd_d<32>(q, ldq, k, ldk, v, ldv, o, lse, B, S, nh, nkv, s);
-    case 64: return fwd_d<64>(q, ldq, k, ldk, v, ldv, o, lse, B, S, nh, nkv, s);
-    case 128: return fwd_d<128>(q, ldq, k, ldk, v, ldv, o, lse, B, S, nh, nkv, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -531,8 +530,6 @@ cudaError_t attn_bwd(const bf16* q, int64_t ldq, const bf16* k, int64_t ldk, con
   switch (d) {
     case 16: return bwd_d<16>(q, ldq, k, ldk, v, ldv, dout, lse, Dd, dq, dk, dv, lddv, B, S, nh, nkv, s);
     case 32: return bwd_d<32>(q, ldq, k, ldk, v, ldv, dout, lse, Dd, dq, dk, dv, lddv, B, S, nh, nkv, s);
-    case 64: return bwd_d<64>(q, ldq, k, ldk, v, ldv, dout, lse, Dd, dq, dk, dv, lddv, B, S, nh, nkv, s);
-    case 128: return bwd_d<128>(q, ldq, k, ldk, v, ldv, dout, lse, Dd, dq, dk, dv, lddv, B, S, nh, nkv, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -15,7 +15,8 @@
 // P is written as bf16 into a 128-byte-swizzled shared tile that the MMA
 // reads as its A operand. The log-sum-exp of every row is saved.
 //
-// Backward (head_dim 128) in two kernels, so no dQ atomics are needed:
+// Backward (head_dim 64 or 128) in two kernels, so no dQ atomics are needed
+// and the result does not depend on scheduling:
 //  * dK/dV, one CTA per (128-key tile, kv head, sequence), loops over the
 //    query heads of its group and the 64-query tiles at or below the
 //    diagonal: S^T = K Q^T and dP^T = V dO^T into one of two TMEM buffer
@@ -320,8 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ============================================================= backward
 // The log2-domain LSE and D = rowsum(dO o O) are read from [B*nh, S_pad]
 // arrays (S_pad a multiple of 64) so that 64-query segments are aligned.
+template <int D_>
 struct BwdCfg {
-  static constexpr int D = 128, BKV = 128, BQ = 64;
+  static constexpr int D = D_, BKV = 128, BQ = 64;
   static constexpr uint32_t KV_CHUNK = 128 * 128;  // 64 d-cols x 128 key rows
   static constexpr uint32_t Q_CHUNK = 64 * 128;    // 64 d-cols x 64 query rows
   static constexpr uint32_t KV_BYTES = BKV * D * 2;
@@ -341,6 +343,7 @@ struct BwdCfg {
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
+template <int DH>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tq,
                             const __grid_constant__ CUtensorMap tk,
@@ -350,8 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             int S_pad, float* __restrict__ dk, bf16* __restrict__ dv,
                             int64_t lddv, int B, int S, int nh, int nkv, float scale,
                             float scale_log2, int* err) {
-  using C = BwdCfg;
-  constexpr int D = C::D, BKV = C::BKV, BQ = C::BQ;
+  using C = BwdCfg<DH>;
+  constexpr int D = C::D, BKV = C::BKV, BQ = C::BQ, DCH = D / 64;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -405,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // --------------------------------------------------------- producer
       mbar_arrive_expect_tx(kv_full, 2 * C::KV_BYTES);
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < DCH; ++c) {
         tma_load_2d(sbase + C::OFF_K + c * C::KV_CHUNK, &tk, kv_full, g * D + c * 64, tok0 + n0);
         tma_load_2d(sbase + C::OFF_V + c * C::KV_CHUNK, &tv, kv_full, g * D + c * 64, tok0 + n0);
       }
@@ -422,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m0 = (first_qt + it % per_head) * BQ;
         const uint32_t qf = q_full + 8 * st;
         mbar_arrive_expect_tx(qf, 2 * C::Q_BYTES + 512);
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < DCH; ++c) {
           tma_load_2d(sbase + C::OFF_Q + st * C::Q_BYTES + c * C::Q_CHUNK, &tq, qf,
                       hh * D + c * 64, tok0 + m0);
           tma_load_2d(sbase + C::OFF_DO + st * C::Q_BYTES + c * C::Q_CHUNK, &tdo, qf,
@@ -564,13 +567,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // dK (scaled) and dV of this key tile, summed over the query heads of the group
     if (ok && warp_wait(fin, 0, err)) {
       tc_fence_after();
-      float* dkr = dk + (int64_t)(tok0 + kpos) * (nkv * D) + g * D + half * 64;
-      bf16* dvr = dv + (int64_t)(tok0 + kpos) * lddv + g * D + half * 64;
+      float* dkr = dk + (int64_t)(tok0 + kpos) * (nkv * D) + g * D + half * (D / 2);
+      bf16* dvr = dv + (int64_t)(tok0 + kpos) * lddv + g * D + half * (D / 2);
 #pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
         uint32_t a[32], v[32];
-        tmem_ld32(tmem + lane_base + C::T_DK + half * 64 + c * 32, a);
-        tmem_ld32(tmem + lane_base + C::T_DV + half * 64 + c * 32, v);
+        tmem_ld32(tmem + lane_base + C::T_DK + half * (D / 2) + c * 32, a);
+        tmem_ld32(tmem + lane_base + C::T_DV + half * (D / 2) + c * 32, v);
         tmem_ld_wait();
         if (kpos < S) {
           store_row32_f32(dkr + c * 32, a, scale);
@@ -591,25 +594,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 // dQ (query-stationary): per (128-query tile, head, sequence) the scores and
 // dP are recomputed for every 128-key tile at or below the diagonal and
 // dQ += dS K accumulates in TMEM, so dQ is written once with plain stores.
+template <int D_>
 struct DqCfg {
-  static constexpr int D = 128, BM = 128, BN = 128;
+  static constexpr int D = D_, BM = 128, BN = 128;
   static constexpr uint32_t CHUNK = 128 * 128;  // 64 cols x 128 rows of bf16
   static constexpr uint32_t T_BYTES = 128 * D * 2;
+  static constexpr uint32_t DS_BYTES = BM * BN * 2;
   static constexpr uint32_t OFF_Q = 0, OFF_DO = T_BYTES, OFF_K = 2 * T_BYTES,  // K[2]
       OFF_V = 4 * T_BYTES,                                                       // V[2]
-      OFF_DS = 6 * T_BYTES, OFF_BAR = 7 * T_BYTES;
+      OFF_DS = 6 * T_BYTES, OFF_BAR = OFF_DS + DS_BYTES;
   static constexpr size_t SMEM = OFF_BAR + 256 + 1024;
   static constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 256, TMEM_COLS = 512;
 };
 
+template <int DH>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                           const __grid_constant__ CUtensorMap tv,
                           const __grid_constant__ CUtensorMap tdo, const float* __restrict__ lse2,
                           const float* __restrict__ Dd, int S_pad, float* __restrict__ dq, int B,
                           int S, int nh, int nkv, float scale, float scale_log2, int* err) {
-  using C = DqCfg;
-  constexpr int D = C::D, BM = C::BM, BN = C::BN;
+  using C = DqCfg<DH>;
+  constexpr int D = C::D, BM = C::BM, BN = C::BN, DCH = D / 64;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -661,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       mbar_arrive_expect_tx(qd_full, 2 * C::T_BYTES);
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < DCH; ++c) {
         tma_load_2d(sbase + C::OFF_Q + c * C::CHUNK, &tq, qd_full, h * D + c * 64, tok0 + m0);
         tma_load_2d(sbase + C::OFF_DO + c * C::CHUNK, &tdo, qd_full, h * D + c * 64, tok0 + m0);
       }
@@ -675,11 +681,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         mbar_arrive_expect_tx(k_full + 8 * st, C::T_BYTES);
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < DCH; ++c)
           tma_load_2d(sbase + C::OFF_K + st * C::T_BYTES + c * C::CHUNK, &tk, k_full + 8 * st,
                       g * D + c * 64, tok0 + j * BN);
         mbar_arrive_expect_tx(v_full + 8 * st, C::T_BYTES);
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < DCH; ++c)
           tma_load_2d(sbase + C::OFF_V + st * C::T_BYTES + c * C::CHUNK, &tv, v_full + 8 * st,
                       g * D + c * 64, tok0 + j * BN);
         pending = (pending & ~(3u << (2 * st))) | ((1u | (ph << 1)) << (2 * st));
@@ -801,11 +807,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok && warp_wait(fin, 0, err)) {
       tc_fence_after();
-      float* out = dq + (int64_t)(tok0 + qpos) * (nh * D) + h * D + half * 64;
+      float* out = dq + (int64_t)(tok0 + qpos) * (nh * D) + h * D + half * (D / 2);
 #pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
         uint32_t a[32];
-        tmem_ld32(tmem + lane_base + C::T_DQ + half * 64 + c * 32, a);
+        tmem_ld32(tmem + lane_base + C::T_DQ + half * (D / 2) + c * 32, a);
         tmem_ld_wait();
         if (qvalid) store_row32_f32(out + c * 32, a, scale);
       }
@@ -823,7 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ================================================================== host
 int attn_lse_pad(int S) { return (S + 63) / 64 * 64; }
 
-bool attn_tc_supported(int d, bool backward) { return backward ? d == 128 : (d == 64 || d == 128); }
+bool attn_tc_supported(int d, bool) { return d == 64 || d == 128; }
 
 template <int D>
 static cudaError_t fwd_tc_d(const bf16* q, int64_t ldq, const bf16* k, int64_t ldk, const bf16* v,
@@ -859,12 +865,11 @@ cudaError_t attn_fwd_tc(const bf16* q, int64_t ldq, const bf16* k, int64_t ldk, 
   return cudaErrorInvalidValue;
 }
 
-cudaError_t attn_bwd_tc(const bf16* q, int64_t ldq, const bf16* k, int64_t ldk, const bf16* v,
-                        int64_t ldv, const bf16* dout, const float* lse2, const float* Dd,
-                        float* dq, float* dk, bf16* dv, int64_t lddv, int B, int S, int nh,
-                        int nkv, int d, int* err, cudaStream_t s) {
-  if (d != 128) return cudaErrorInvalidValue;
-  constexpr int D = 128;
+template <int D>
+static cudaError_t bwd_tc_d(const bf16* q, int64_t ldq, const bf16* k, int64_t ldk, const bf16* v,
+                            int64_t ldv, const bf16* dout, const float* lse2, const float* Dd,
+                            float* dq, float* dk, bf16* dv, int64_t lddv, int B, int S, int nh,
+                            int nkv, int* err, cudaStream_t s) {
   const int64_t T = (int64_t)B * S;
   CUtensorMap tq64, tdo64, tq128, tdo128, tk, tv;
   if (!make_tma_2d(&tq64, q, T, (int64_t)nh * D, ldq, 64) ||
@@ -876,12 +881,12 @@ cudaError_t attn_bwd_tc(const bf16* q, int64_t ldq, const bf16* k, int64_t ldk, 
     return cudaErrorInvalidValue;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel,
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)BwdCfg::SMEM);
+                                         (int)BwdCfg<D>::SMEM);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)DqCfg::SMEM);
+    e = cudaFuncSetAttribute(attn_bwd_dq_tc_kernel<D>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DqCfg<D>::SMEM);
     if (e != cudaSuccess) return e;
     attr = true;
   }
@@ -889,15 +894,28 @@ cudaError_t attn_bwd_tc(const bf16* q, int64_t ldq, const bf16* k, int64_t ldk, 
   const int S_pad = attn_lse_pad(S);
   const int n_t = (S + 127) / 128;
   note_launch();
-  attn_bwd_dkdv_tc_kernel<<<n_t * nkv * B, kThreads, BwdCfg::SMEM, s>>>(
+  attn_bwd_dkdv_tc_kernel<D><<<n_t * nkv * B, kThreads, BwdCfg<D>::SMEM, s>>>(
       tq64, tk, tv, tdo64, lse2, Dd, S_pad, dk, dv, lddv, B, S, nh, nkv, scale, scale * kLog2eF,
       err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   note_launch();
-  attn_bwd_dq_tc_kernel<<<n_t * nh * B, kThreads, DqCfg::SMEM, s>>>(
+  attn_bwd_dq_tc_kernel<D><<<n_t * nh * B, kThreads, DqCfg<D>::SMEM, s>>>(
       tq128, tk, tv, tdo128, lse2, Dd, S_pad, dq, B, S, nh, nkv, scale, scale * kLog2eF, err);
   return cudaGetLastError();
+}
+
+cudaError_t attn_bwd_tc(const bf16* q, int64_t ldq, const bf16* k, int64_t ldk, const bf16* v,
+                        int64_t ldv, const bf16* dout, const float* lse2, const float* Dd,
+                        float* dq, float* dk, bf16* dv, int64_t lddv, int B, int S, int nh,
+                        int nkv, int d, int* err, cudaStream_t s) {
+  if (d == 128)
+    return bwd_tc_d<128>(q, ldq, k, ldk, v, ldv, dout, lse2, Dd, dq, dk, dv, lddv, B, S, nh, nkv,
+                         err, s);
+  if (d == 64)
+    return bwd_tc_d<64>(q, ldq, k, ldk, v, ldv, dout, lse2, Dd, dq, dk, dv, lddv, B, S, nh, nkv,
+                        err, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace rdt

@@ -22,21 +22,28 @@
 
 namespace rdt {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
-constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KB
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr uint32_t MN_CHUNK_BYTES = 64 * BK * 2;  // one 64(MN) x 64(K) box: 8 KB
+constexpr int BM = 128, BK = 64;
+constexpr uint32_t A_BYTES = BM * BK * 2;         // 16 KB
+constexpr uint32_t MN_CHUNK_BYTES = 64 * BK * 2;  // one 64-row x 64-col box: 8 KB
 constexpr int GEMM_THREADS = 320;
 constexpr int EPI_THREADS = 256;
 constexpr int TMEM_COLS = 512;
-constexpr size_t GEMM_SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+
+// Tile width N = BN (256 or 192). The ring holds as many 64-deep stages as fit
+// in ~200 KB: 4 of 48 KB for BN = 256, 5 of 40 KB for BN = 192.
+template <int BN_>
+struct Tile {
+  static constexpr int BN = BN_;
+  static constexpr uint32_t B_BYTES = BN * BK * 2;
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = BN == 256 ? 4 : 5;
+  static constexpr size_t SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+};
 
 struct GemmParams {
   int M, N, K;
   int m_tiles, n_tiles, k_blocks;
-  int b_tile_rows;  // K-major B: rows advanced per N tile (256, or 128 for SwiGLU)
-  int b_half_off;   // K-major B: row offset of the second 128-row half
+  int swiglu_half;  // SwiGLU: row offset of the up rows in the stacked [2I, K] B
   Epi epi;
   int* err;
 };
@@ -57,7 +64,7 @@ __device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
 // -------------------------------------------------------------- epilogues
-template <int EPI>
+template <int EPI, int BN>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tbase, int row,
                                               int mt, int nt, int half) {
   const Epi& e = p.epi;
@@ -289,10 +296,12 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tbas
 }
 
 // ----------------------------------------------------------------- kernel
-template <int A_MN, int B_MN, int EPI>
+template <int A_MN, int B_MN, int EPI, int BN>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
                 const __grid_constant__ CUtensorMap tma_b, const GemmParams p) {
+  constexpr int STAGES = Tile<BN>::STAGES;
+  constexpr uint32_t STAGE_BYTES = Tile<BN>::STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -363,11 +372,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           if (B_MN) {
             const int n0 = nt * BN;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * MN_CHUNK_BYTES, &tma_b, fb, n0 + 64 * j, k0);
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(sb + j * MN_CHUNK_BYTES, &tma_b, fb, n0 + 64 * j, k0);
           } else {
-            const int r0 = nt * p.b_tile_rows;
-            tma_load_2d(sb, &tma_b, fb, k0, r0);
-            tma_load_2d(sb + B_BYTES / 2, &tma_b, fb, k0, r0 + p.b_half_off);
+            // 64-row boxes; SwiGLU stacks gate rows nt*128+[0,128) and up rows
+            // half+nt*128+[0,128) into one 256-row tile
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) {
+              const int r = (EPI == EPI_SWIGLU) ? nt * 128 + (j & 1) * 64 + (j >> 1) * p.swiglu_half
+                                                : nt * BN + j * 64;
+              tma_load_2d(sb + j * MN_CHUNK_BYTES, &tma_b, fb, k0, r);
+            }
           }
           pending |= 1u << stage;
           pending_par = (pending_par & ~(1u << stage)) | (ph << stage);
@@ -443,7 +458,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       tc_fence_after();
       const int row = mt * BM + q * 32 + lane;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      epilogue_tile<EPI>(p, tbase, row, mt, nt, half);
+      epilogue_tile<EPI, BN>(p, tbase, row, mt, nt, half);
       tc_fence_before();
       mbar_arrive(tempty0 + 8 * acc);
       acc ^= 1;
@@ -503,14 +518,14 @@ static bool make_map(CUtensorMap* m, const Mat& x, int box_rows) {
   return make_tma_2d(m, x.ptr, x.rows, x.cols, x.ld, box_rows);
 }
 
-template <int A_MN, int B_MN, int EPI>
+template <int A_MN, int B_MN, int EPI, int BN>
 static cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
                           cudaStream_t s) {
   static bool attr_done = false;  // per instantiation; the attribute is per function
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<A_MN, B_MN, EPI>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<A_MN, B_MN, EPI, BN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(GEMM_SMEM));
+                                         static_cast<int>(Tile<BN>::SMEM));
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
@@ -518,7 +533,7 @@ static cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const Ge
   const int grid = ntiles < num_sms() ? ntiles : num_sms();
   const int64_t slot = gemm_timing_before(s, 2.0 * p.M * (double)p.N * p.K);
   note_launch();
-  gemm_kernel<A_MN, B_MN, EPI><<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(ta, tb, p);
+  gemm_kernel<A_MN, B_MN, EPI, BN><<<grid, GEMM_THREADS, Tile<BN>::SMEM, s>>>(ta, tb, p);
   gemm_timing_after(s, slot);
   return cudaGetLastError();
 }
@@ -540,36 +555,55 @@ cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N,
     return cudaErrorInvalidValue;
   }
   CUtensorMap ta, tb;
-  if (!make_map(&ta, A, a_mn ? 64 : 128) || !make_map(&tb, B, b_mn ? 64 : 128)) {
+  if (!make_map(&ta, A, a_mn ? 64 : 128) || !make_map(&tb, B, 64)) {
     *why = "gemm: cuTensorMapEncodeTiled failed";
     return cudaErrorInvalidValue;
+  }
+  // Tile width: 256 unless 192 fills the SMs' last wave clearly better.
+  int bn = 256;
+  if (epi.kind != EPI_SWIGLU && epi.kind != EPI_CE) {
+    const int sms = num_sms();
+    auto eff = [&](int w) {
+      const int64_t tiles = (int64_t)((M + BM - 1) / BM) * ((N + w - 1) / w);
+      const int64_t rounds = (tiles + sms - 1) / sms;
+      return static_cast<double>(M) * N / (static_cast<double>(rounds) * sms * BM * w);
+    };
+    if (eff(192) > 1.03 * eff(256)) bn = 192;
   }
   GemmParams p;
   p.M = M;
   p.N = N;
   p.K = K;
   p.m_tiles = (M + BM - 1) / BM;
-  p.n_tiles = swiglu ? (N + 127) / 128 : (N + BN - 1) / BN;
+  p.n_tiles = swiglu ? (N + 127) / 128 : (N + bn - 1) / bn;
   p.k_blocks = (K + BK - 1) / BK;
-  p.b_tile_rows = swiglu ? 128 : BN;
-  p.b_half_off = swiglu ? epi.half : 128;
+  p.swiglu_half = epi.half;
   p.epi = epi;
   p.err = err;
-#define RDT_GEMM_CASE(AM, BMJ, E) \
-  if (a_mn == (AM) && b_mn == (BMJ) && epi.kind == (E)) return launch<AM, BMJ, E>(ta, tb, p, s);
+#define RDT_GEMM_CASE(AM, BMJ, E, W)                                           \
+  if (a_mn == (AM) && b_mn == (BMJ) && epi.kind == (E) && bn == (W)) \
+    return launch<AM, BMJ, E, W>(ta, tb, p, s);
   // forward projections: A K-major, B K-major
-  RDT_GEMM_CASE(0, 0, EPI_BF16)
-  RDT_GEMM_CASE(0, 0, EPI_F32)
-  RDT_GEMM_CASE(0, 0, EPI_F32_RESID)
-  RDT_GEMM_CASE(0, 0, EPI_SWIGLU)
-  RDT_GEMM_CASE(0, 0, EPI_CE)
+  RDT_GEMM_CASE(0, 0, EPI_BF16, 256)
+  RDT_GEMM_CASE(0, 0, EPI_BF16, 192)
+  RDT_GEMM_CASE(0, 0, EPI_F32, 256)
+  RDT_GEMM_CASE(0, 0, EPI_F32, 192)
+  RDT_GEMM_CASE(0, 0, EPI_F32_RESID, 256)
+  RDT_GEMM_CASE(0, 0, EPI_F32_RESID, 192)
+  RDT_GEMM_CASE(0, 0, EPI_SWIGLU, 256)
+  RDT_GEMM_CASE(0, 0, EPI_CE, 256)
   // activation gradients dX = dY W: A K-major, B MN-major
-  RDT_GEMM_CASE(0, 1, EPI_BF16)
-  RDT_GEMM_CASE(0, 1, EPI_F32)
-  RDT_GEMM_CASE(0, 1, EPI_SWIGLU_BWD)
+  RDT_GEMM_CASE(0, 1, EPI_BF16, 256)
+  RDT_GEMM_CASE(0, 1, EPI_BF16, 192)
+  RDT_GEMM_CASE(0, 1, EPI_F32, 256)
+  RDT_GEMM_CASE(0, 1, EPI_F32, 192)
+  RDT_GEMM_CASE(0, 1, EPI_SWIGLU_BWD, 256)
+  RDT_GEMM_CASE(0, 1, EPI_SWIGLU_BWD, 192)
   // weight gradients dW = dY^T X: A MN-major, B MN-major
-  RDT_GEMM_CASE(1, 1, EPI_F32)
-  RDT_GEMM_CASE(1, 1, EPI_BF16)
+  RDT_GEMM_CASE(1, 1, EPI_F32, 256)
+  RDT_GEMM_CASE(1, 1, EPI_F32, 192)
+  RDT_GEMM_CASE(1, 1, EPI_BF16, 256)
+  RDT_GEMM_CASE(1, 1, EPI_BF16, 192)
 #undef RDT_GEMM_CASE
   *why = "gemm: unsupported operand-major / epilogue combination";
   return cudaErrorInvalidValue;

@@ -117,6 +117,7 @@ cudaError_t adamw(float* w, const float* g, float* m, float* v, int64_t n, const
                   float bc1, float bc2, bf16* wb, cudaStream_t s);
 
 // ---------------------------------------------------------------- attention
+// mma.sync flash attention (attention.cu) for head_dim 16 and 32.
 // q [T, ldq] (head h at column h*d), k/v [T, ldk/ldv] (kv head g at g*d),
 // o [T, nh*d] bf16, lse [B, nh, S] fp32 (natural log).
 cudaError_t attn_fwd(const bf16* q, int64_t ldq, const bf16* k, int64_t ldk, const bf16* v,
@@ -135,8 +136,8 @@ cudaError_t attn_bwd(const bf16* q, int64_t ldq, const bf16* k, int64_t ldk, con
                      float* dk, bf16* dv, int64_t lddv, int B, int S, int nh, int nkv, int d,
                      cudaStream_t s);
 
-// tcgen05 flash attention (attention_tc.cu): forward for head_dim 64/128,
-// backward for head_dim 128; same arguments as attn_fwd / attn_bwd plus the
+// tcgen05 flash attention (attention_tc.cu): forward and backward for
+// head_dim 64/128; same arguments as attn_fwd / attn_bwd plus the
 // device error word for bounded waits. The backward reads lse2 (log2-domain
 // LSE) and D in the padded [B*nh, attn_lse_pad(S)] layout and writes every
 // dq element (no zeroing needed).

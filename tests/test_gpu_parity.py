@@ -91,6 +91,12 @@ def test_block_parity_head_dim_128_long_sequence():
                              intermediate=512, seq=700, batch=1), seed=9)
 
 
+def test_block_parity_head_dim_64_gqa4_long_sequence():
+    # head_dim 64 on the tensor-core kernels: several 128-key tiles, ragged tail
+    _block_case(ragged_shape(layers=1, hidden=256, n_heads=8, n_kv_heads=2, head_dim=64,
+                             intermediate=512, seq=650, batch=1), seed=13)
+
+
 def test_block_parity_head_dim_32_gqa4():
     _block_case(ragged_shape(layers=1, hidden=128, n_heads=8, n_kv_heads=2, head_dim=32,
                              intermediate=352, seq=97, batch=3), seed=5)
