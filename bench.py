@@ -261,7 +261,7 @@ def run_rdt(args, rank, world, local_rank):
             if hashlib.sha256(fh.read()).hexdigest()[:16] == GEMM_TRAFFIC_SRC_SHA:
                 traffic = GEMM_TRAFFIC_BYTES
     roofline = {
-        "kernel": "gemm_kernel (tcgen05 BF16, TMEM fp32 accumulators, TMA)",
+        "kernel": "gemm_kernel / gemm2_kernel (tcgen05 BF16 single-CTA 128x192/256 and CTA-pair 256x256 tiles, TMEM fp32 accumulators, TMA)",
         "bound": "tensor", "achieved": round(achieved, 1) if achieved else None,
         "peak": peak_tf, "unit": "TFLOP/s",
         "frac": round(achieved / peak_tf, 4) if achieved else None,

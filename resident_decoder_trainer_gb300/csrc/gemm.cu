@@ -1,15 +1,19 @@
 // Persistent tcgen05 BF16 GEMM for sm_103a with fused epilogues.
 //
-// One CTA per SM (320 threads, ~197 KB shared memory, all 512 TMEM columns):
-//   warp 0  TMA producer: streams 128x64 A and 256x64 B tiles (128-byte
-//           swizzle) into a 4-stage shared-memory ring, one mbarrier per stage;
-//   warp 1  MMA issuer: one elected lane issues tcgen05.mma (M=128, N=256,
-//           K=16) into one of two TMEM accumulators (2 x 256 fp32 columns),
+// Single-CTA kernel, one CTA per SM (320 threads, ~197 KB shared memory, all
+// 512 TMEM columns):
+//   warp 0  TMA producer: streams 128x64 A and BNx64 B tiles (BN = 256 or
+//           192; 128-byte swizzle) into a 4- or 5-stage shared-memory ring,
+//           one mbarrier per stage;
+//   warp 1  MMA issuer: one elected lane issues tcgen05.mma (M=128, N=BN,
+//           K=16) into one of two TMEM accumulators (2 x BN fp32 columns),
 //           then tcgen05.commit frees the smem stage / signals the epilogue;
 //   warps 2-9 epilogue: two warps per 32-lane TMEM quarter, each taking half of
 //           the tile's columns; tcgen05.ld (one output row per thread), fused
 //           elementwise work, vectorised global stores; the accumulator is
 //           handed back so the next tile's MMAs overlap.
+// CTA-pair kernel (gemm2_kernel, below): the same roles on clusters of two
+// CTAs with 256 x 256 tiles and the pair MMA (cta_group::2).
 // Operands may be K-major ([rows, K], K contiguous) or MN-major ([K, rows]);
 // the transposed cases are expressed through the UMMA descriptors, so no
 // operand is ever transposed in memory. Ragged M/N/K edges are zero-filled by
@@ -44,18 +48,21 @@ struct GemmParams {
   int M, N, K;
   int m_tiles, n_tiles, k_blocks;
   int swiglu_half;  // SwiGLU: row offset of the up rows in the stacked [2I, K] B
+  int group;        // rasterisation: row tiles per group (see tile_coords)
   Epi epi;
   int* err;
 };
 
-__device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int& mt, int& nt) {
-  // Groups of 8 M-tiles sweep all N tiles, so a wave of CTAs shares A rows
-  // and B columns in L2.
-  constexpr int G = 8;
-  const int per_group = G * n_tiles;
+// Tile t -> (row tile, column tile). Groups of p.group row tiles sweep all
+// column tiles, row tile fastest. group = m_tiles keeps all of A resident in L2
+// while B streams through once; group = 1 does the same for B (column tile
+// fastest); the host picks the one whose resident operand fits in L2.
+__device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& mt, int& nt) {
+  const int G = p.group;
+  const int per_group = G * p.n_tiles;
   const int g = t / per_group;
   const int first = g * G;
-  const int gs = min(m_tiles - first, G);
+  const int gs = min(p.m_tiles - first, G);
   const int r = t - g * per_group;
   mt = first + r % gs;
   nt = r / gs;
@@ -351,7 +358,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       bool ok = true;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
         int mt, nt;
-        tile_coords(t, p.m_tiles, p.n_tiles, mt, nt);
+        tile_coords(t, p, mt, nt);
         const int m0 = mt * BM;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, ph ^ 1, p.err)) {
@@ -453,7 +460,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     uint32_t acc_ph = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       int mt, nt;
-      tile_coords(t, p.m_tiles, p.n_tiles, mt, nt);
+      tile_coords(t, p, mt, nt);
       if (!mbar_wait(tfull0 + 8 * acc, acc_ph, p.err)) break;
       tc_fence_after();
       const int row = mt * BM + q * 32 + lane;
@@ -471,6 +478,213 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------ pair kernel
+// The same GEMM on CTA pairs (clusters of 2) with the pair MMA
+// (tcgen05.mma.cta_group::2, 256 x 256 x 16): each CTA loads its own 128 rows
+// of A and 128 of the tile's 256 columns of B, i.e. 32 KB per 64-deep stage
+// instead of the 48 KB a single-CTA 128 x 256 tile needs for the same flops -
+// one third less shared-memory fill per flop, and 6 stages of lookahead.
+// The even CTA's producer arms its full barrier for both CTAs' bytes and both
+// producers' TMA copies complete on it; its lane-0 MMA thread issues the pair
+// MMAs and commits (multicast) to both CTAs' empty / accumulator-full
+// barriers; every epilogue warp of both CTAs hands its accumulator back on the
+// even CTA's accumulator-empty barrier. Each CTA's epilogue reads the 128 rows
+// of the tile its own TMEM holds, with the same epilogues as above.
+template <int BN_>
+struct Tile2 {
+  static_assert(BN_ == 256, "pair tiles are 256 x 256");
+  static constexpr int BN = BN_;      // pair tile width (N of the MMA)
+  static constexpr int BH = BN / 2;   // columns of B each CTA loads
+  static constexpr uint32_t B_BYTES = BH * BK * 2;
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB
+  static constexpr int STAGES = 6;
+  static constexpr size_t SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+};
+
+template <int A_MN, int B_MN, int EPI, int BN>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    gemm2_kernel(const __grid_constant__ CUtensorMap tma_a,
+                 const __grid_constant__ CUtensorMap tma_b, const GemmParams p) {
+  using TL = Tile2<BN>;
+  constexpr int STAGES = TL::STAGES;
+  constexpr int BH = TL::BH;
+  constexpr uint32_t STAGE_BYTES = TL::STAGE_BYTES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * STAGES;
+  const uint32_t tfull0 = empty0 + 8 * STAGES;
+  const uint32_t tempty0 = tfull0 + 16;
+  const uint32_t drain = tempty0 + 16;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the pair MMAs
+  const int pair = static_cast<int>(blockIdx.x) >> 1;
+  const int npairs = static_cast<int>(gridDim.x) >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, 2 * (EPI_THREADS / 32));  // one arrival per epilogue warp
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tma_a);
+    tma_prefetch_desc(&tma_b);
+  }
+  if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t full_even = mapa_shared(full0, 0);
+  const uint32_t tempty_even = mapa_shared(tempty0, 0);
+
+  const int ntiles = p.m_tiles * p.n_tiles;  // m_tiles counts 256-row pair tiles
+  const uint32_t smem_base = smem_u32(smem);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      int stage = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int t = pair; t < ntiles && ok; t += npairs) {
+        int mt, nt;
+        tile_coords(t, p, mt, nt);
+        const int m0 = (2 * mt + static_cast<int>(rank)) * BM;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(empty0 + 8 * stage, ph ^ 1, p.err)) {
+            ok = false;
+            break;
+          }
+          if (rank == 0) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * STAGE_BYTES);
+          const uint32_t fb = full_even + 8 * stage;
+          const uint32_t sa = smem_base + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          const int k0 = kb * BK;
+          if (A_MN) {
+            tma_load_2d_pair(sa, &tma_a, fb, m0, k0);
+            tma_load_2d_pair(sa + MN_CHUNK_BYTES, &tma_a, fb, m0 + 64, k0);
+          } else {
+            tma_load_2d_pair(sa, &tma_a, fb, k0, m0);
+          }
+          if (B_MN) {
+            const int n0 = nt * BN + static_cast<int>(rank) * BH;
+#pragma unroll
+            for (int j = 0; j < BH / 64; ++j)
+              tma_load_2d_pair(sb + j * MN_CHUNK_BYTES, &tma_b, fb, n0 + 64 * j, k0);
+          } else {
+            // one box of 128 rows; SwiGLU: the even CTA loads the 128 gate rows
+            // of I-columns nt*128 + [0,128), the odd CTA the matching up rows
+            const int r = (EPI == EPI_SWIGLU) ? nt * 128 + static_cast<int>(rank) * p.swiglu_half
+                                              : nt * BN + static_cast<int>(rank) * BH;
+            tma_load_2d_pair(sb, &tma_b, fb, k0, r);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            ph ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ----------------------------------------------------------------- MMA
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN, A_MN, B_MN);
+      int stage = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t acc_ph = 0;
+      bool ok = true;
+      for (int t = pair; t < ntiles && ok; t += npairs) {
+        if (!mbar_wait_cluster(tempty0 + 8 * acc, acc_ph ^ 1, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(full0 + 8 * stage, ph, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_base + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = A_MN ? sdesc_sw128(sa + k * 2048, MN_CHUNK_BYTES, 1024)
+                                     : sdesc_sw128(sa + k * 32, 16, 1024);
+            const uint64_t bd = B_MN ? sdesc_sw128(sb + k * 2048, MN_CHUNK_BYTES, 1024)
+                                     : sdesc_sw128(sb + k * 32, 16, 1024);
+            tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
+          }
+          tc_commit_pair_mc(empty0 + 8 * stage, 0x3);
+          if (++stage == STAGES) {
+            stage = 0;
+            ph ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair_mc(tfull0 + 8 * acc, 0x3);
+        acc ^= 1;
+        if (acc == 0) acc_ph ^= 1;
+      }
+      // no pair MMA may still be writing either CTA's TMEM when it is released
+      tc_commit_pair(drain);
+      mbar_wait(drain, 0, nullptr);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    int acc = 0;
+    uint32_t acc_ph = 0;
+    for (int t = pair; t < ntiles; t += npairs) {
+      int mt, nt;
+      tile_coords(t, p, mt, nt);
+      if (!warp_wait(tfull0 + 8 * acc, acc_ph, p.err)) break;
+      tc_fence_after();
+      const int mrow = 2 * mt + static_cast<int>(rank);
+      const int row = mrow * BM + q * 32 + lane;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      epilogue_tile<EPI, BN>(p, tbase, row, mrow, nt, half);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty_even + 8 * acc);
+      acc ^= 1;
+      if (acc == 0) acc_ph ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync();
+  if (p.err && *reinterpret_cast<volatile int*>(p.err) != 0) {
+    // after a timed-out wait, copies issued just before may still be landing
+    // on this pair's shared memory: let them finish before the CTAs exit
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 200000ull) {
+    }
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
 }
 
@@ -538,6 +752,81 @@ static cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const Ge
   return cudaGetLastError();
 }
 
+template <int A_MN, int B_MN, int EPI, int BN>
+static cudaError_t launch2(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
+                           int max_pairs, cudaStream_t s) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(gemm2_kernel<A_MN, B_MN, EPI, BN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(Tile2<BN>::SMEM));
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const int ntiles = p.m_tiles * p.n_tiles;
+  const int pairs = ntiles < max_pairs ? ntiles : max_pairs;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Tile2<BN>::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int64_t slot = gemm_timing_before(s, 2.0 * p.M * (double)p.N * p.K);
+  note_launch();
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm2_kernel<A_MN, B_MN, EPI, BN>, ta, tb, p);
+  gemm_timing_after(s, slot);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// CTA pairs that can be resident at once (clusters of 2 with the pair
+// kernel's shared memory); 0 if clusters cannot be launched.
+static int max_active_pairs() {
+  static int n = -1;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * num_sms(), 1, 1);
+    cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Tile2<256>::SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int c = 0;
+    if (cudaFuncSetAttribute(gemm2_kernel<0, 0, EPI_F32, 256>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(Tile2<256>::SMEM)) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&c, gemm2_kernel<0, 0, EPI_F32, 256>, &cfg) != cudaSuccess)
+      c = 0;
+    cudaGetLastError();
+    n = c;
+  });
+  return n;
+}
+
+// Rows of the A operand per raster group: all row tiles when A fits in the L2
+// budget (B streams once), 1 when B does (A streams once), else as many row
+// tiles as fit.
+static int raster_group(int m_tiles, int n_tiles, int rows_per_tile, int cols_per_tile, int K) {
+  constexpr double kL2Budget = 48.0 * 1024 * 1024;
+  const double a_tile = static_cast<double>(rows_per_tile) * K * 2;
+  const double b_tile = static_cast<double>(cols_per_tile) * K * 2;
+  if (a_tile * m_tiles <= kL2Budget) return m_tiles;
+  if (b_tile * n_tiles <= kL2Budget) return 1;
+  const int g = static_cast<int>(kL2Budget / a_tile);
+  return g < 1 ? 1 : (g > m_tiles ? m_tiles : g);
+}
+
 cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N, int K,
                  const Epi& epi, int* err, cudaStream_t s, const char** why) {
   if (M <= 0 || N <= 0 || K <= 0) {
@@ -554,35 +843,60 @@ cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N,
     *why = "gemm: operands need 16-byte aligned rows";
     return cudaErrorInvalidValue;
   }
+  // Tile shape: single-CTA 128 x 256 or 128 x 192, or CTA-pair 256 x 256.
+  // Cost = waves x per-CTA tile width / mainloop rate, with the rates of the
+  // three shapes measured on the projection and LM-head GEMMs of a Qwen3-4B
+  // step (pair 1.05, single 256 1.0, single 192 0.85): the pair mainloop
+  // moves a third fewer bytes per flop; 192-wide tiles win where they cut a
+  // wave (N = 2560 outputs).
+  constexpr double kRate256 = 1.0, kRate192 = 0.85, kRatePair = 1.05;
+  const bool fixed256 = swiglu || epi.kind == EPI_CE;
+  const int sms = num_sms();
+  const int pairs_max = max_active_pairs();
+  auto cost1 = [&](int w, double rate) {
+    const int64_t tiles = (int64_t)((M + BM - 1) / BM) * ((N + w - 1) / w);
+    return static_cast<double>((tiles + sms - 1) / sms) * w / rate;
+  };
+  bool pair_tiles = false;
+  int bn = 256;
+  double best = cost1(256, kRate256);
+  if (!fixed256 && cost1(192, kRate192) < best) {
+    best = cost1(192, kRate192);
+    bn = 192;
+  }
+  if (pairs_max > 0 && M > BM) {
+    const int64_t tiles = (int64_t)((M + 2 * BM - 1) / (2 * BM)) * ((N + 255) / 256);
+    const double c = static_cast<double>((tiles + pairs_max - 1) / pairs_max) * 256 / kRatePair;
+    if (c < best) {
+      best = c;
+      bn = 256;
+      pair_tiles = true;
+    }
+  }
   CUtensorMap ta, tb;
-  if (!make_map(&ta, A, a_mn ? 64 : 128) || !make_map(&tb, B, 64)) {
+  const int b_box = (pair_tiles && !b_mn) ? 128 : 64;
+  if (!make_map(&ta, A, a_mn ? 64 : 128) || !make_map(&tb, B, b_box)) {
     *why = "gemm: cuTensorMapEncodeTiled failed";
     return cudaErrorInvalidValue;
-  }
-  // Tile width: 256 unless 192 fills the SMs' last wave clearly better.
-  int bn = 256;
-  if (epi.kind != EPI_SWIGLU && epi.kind != EPI_CE) {
-    const int sms = num_sms();
-    auto eff = [&](int w) {
-      const int64_t tiles = (int64_t)((M + BM - 1) / BM) * ((N + w - 1) / w);
-      const int64_t rounds = (tiles + sms - 1) / sms;
-      return static_cast<double>(M) * N / (static_cast<double>(rounds) * sms * BM * w);
-    };
-    if (eff(192) > 1.03 * eff(256)) bn = 192;
   }
   GemmParams p;
   p.M = M;
   p.N = N;
   p.K = K;
-  p.m_tiles = (M + BM - 1) / BM;
+  const int rows_per_tile = pair_tiles ? 2 * BM : BM;
+  p.m_tiles = (M + rows_per_tile - 1) / rows_per_tile;
   p.n_tiles = swiglu ? (N + 127) / 128 : (N + bn - 1) / bn;
   p.k_blocks = (K + BK - 1) / BK;
   p.swiglu_half = epi.half;
+  p.group = raster_group(p.m_tiles, p.n_tiles, rows_per_tile, swiglu ? 256 : bn, K);
   p.epi = epi;
   p.err = err;
 #define RDT_GEMM_CASE(AM, BMJ, E, W)                                           \
-  if (a_mn == (AM) && b_mn == (BMJ) && epi.kind == (E) && bn == (W)) \
+  if (!pair_tiles && a_mn == (AM) && b_mn == (BMJ) && epi.kind == (E) && bn == (W)) \
     return launch<AM, BMJ, E, W>(ta, tb, p, s);
+#define RDT_GEMM2_CASE(AM, BMJ, E, W)                                          \
+  if (pair_tiles && a_mn == (AM) && b_mn == (BMJ) && epi.kind == (E) && bn == (W)) \
+    return launch2<AM, BMJ, E, W>(ta, tb, p, pairs_max, s);
   // forward projections: A K-major, B K-major
   RDT_GEMM_CASE(0, 0, EPI_BF16, 256)
   RDT_GEMM_CASE(0, 0, EPI_BF16, 192)
@@ -592,6 +906,11 @@ cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N,
   RDT_GEMM_CASE(0, 0, EPI_F32_RESID, 192)
   RDT_GEMM_CASE(0, 0, EPI_SWIGLU, 256)
   RDT_GEMM_CASE(0, 0, EPI_CE, 256)
+  RDT_GEMM2_CASE(0, 0, EPI_BF16, 256)
+  RDT_GEMM2_CASE(0, 0, EPI_F32, 256)
+  RDT_GEMM2_CASE(0, 0, EPI_F32_RESID, 256)
+  RDT_GEMM2_CASE(0, 0, EPI_SWIGLU, 256)
+  RDT_GEMM2_CASE(0, 0, EPI_CE, 256)
   // activation gradients dX = dY W: A K-major, B MN-major
   RDT_GEMM_CASE(0, 1, EPI_BF16, 256)
   RDT_GEMM_CASE(0, 1, EPI_BF16, 192)
@@ -599,11 +918,17 @@ cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N,
   RDT_GEMM_CASE(0, 1, EPI_F32, 192)
   RDT_GEMM_CASE(0, 1, EPI_SWIGLU_BWD, 256)
   RDT_GEMM_CASE(0, 1, EPI_SWIGLU_BWD, 192)
+  RDT_GEMM2_CASE(0, 1, EPI_BF16, 256)
+  RDT_GEMM2_CASE(0, 1, EPI_F32, 256)
+  RDT_GEMM2_CASE(0, 1, EPI_SWIGLU_BWD, 256)
   // weight gradients dW = dY^T X: A MN-major, B MN-major
   RDT_GEMM_CASE(1, 1, EPI_F32, 256)
   RDT_GEMM_CASE(1, 1, EPI_F32, 192)
   RDT_GEMM_CASE(1, 1, EPI_BF16, 256)
   RDT_GEMM_CASE(1, 1, EPI_BF16, 192)
+  RDT_GEMM2_CASE(1, 1, EPI_F32, 256)
+  RDT_GEMM2_CASE(1, 1, EPI_BF16, 256)
+#undef RDT_GEMM2_CASE
 #undef RDT_GEMM_CASE
   *why = "gemm: unsupported operand-major / epilogue combination";
   return cudaErrorInvalidValue;

@@ -24,7 +24,10 @@ def _built():
 
 
 # ------------------------------------------------------------------ GEMM
-GEMM_SHAPES = [(128, 256, 64), (300, 520, 200), (37, 40, 24), (1, 16, 16), (257, 513, 1000)]
+# every tile shape the host picks (128 x 192, 128 x 256, CTA-pair 256 x 256),
+# with ragged M, N and K edges
+GEMM_SHAPES = [(128, 256, 64), (300, 520, 200), (37, 40, 24), (1, 16, 16), (257, 513, 1000),
+               (100, 38912, 64), (2048, 2048, 192), (5000, 5000, 40)]
 
 
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1)])
