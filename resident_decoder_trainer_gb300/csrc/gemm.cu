@@ -19,6 +19,7 @@
 // operand is ever transposed in memory. Ragged M/N/K edges are zero-filled by
 // TMA and masked in the epilogue.
 #include <cstdio>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -33,15 +34,26 @@ constexpr int GEMM_THREADS = 320;
 constexpr int EPI_THREADS = 256;
 constexpr int TMEM_COLS = 512;
 
-// Tile width N = BN (256 or 192). The ring holds as many 64-deep stages as fit
-// in ~200 KB: 4 of 48 KB for BN = 256, 5 of 40 KB for BN = 192.
+// Epilogue output staging per epilogue warp (see the epilogues below): 4 KB;
+// 128 x 192 single-CTA tiles keep a 5-stage ring by staging 2 KB per warp
+// (fp32 blocks then go out as two 32 x 16 boxes with 64-byte rows).
+template <int BN, bool PAIR>
+struct OutStage {
+  static constexpr uint32_t BYTES = (BN == 192 && !PAIR) ? 2048 : 4096;
+  static constexpr uint32_t TOTAL = BYTES * (EPI_THREADS / 32);
+};
+
+// Tile width N = BN (256 or 192). Shared memory: a ring of 64-deep stages
+// (4 of 48 KB or 5 of 40 KB), the epilogue's output staging (32 or 16 KB),
+// barriers.
 template <int BN_>
 struct Tile {
   static constexpr int BN = BN_;
   static constexpr uint32_t B_BYTES = BN * BK * 2;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = BN == 256 ? 4 : 5;
-  static constexpr size_t SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr uint32_t OFF_OUT = STAGES * STAGE_BYTES;
+  static constexpr size_t SMEM = OFF_OUT + OutStage<BN, false>::TOTAL + 1024 + 256;
 };
 
 struct GemmParams {
@@ -71,14 +83,82 @@ __device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& mt,
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
 // -------------------------------------------------------------- epilogues
-template <int EPI, int BN>
-__device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tbase, int row,
-                                              int mt, int nt, int half) {
+// Every output goes through a 4 KB staging buffer per epilogue warp: each
+// thread writes its row of a 32-row x 32-column block into the buffer in the
+// TMA swizzle layout (fp32: 128-byte rows, 128-byte swizzle; bf16: 64-byte
+// rows, 64-byte swizzle - conflict-free either way), and one lane stores the
+// block with a TMA bulk tensor store (whole 128-byte lines; the tensor map
+// clips the box at M and, in 16-byte units, at N).
+
+// Output tensor maps: o1 = out (g for SwiGLU, dg for SwiGLU-bwd, logits for
+// CE), o2 = u / du, o3 = s.
+struct OutMaps {
+  CUtensorMap o1, o2, o3;
+};
+
+struct Stage {
+  uint8_t* p;    // this warp's staging buffer
+  uint32_t a;    // its shared-memory address
+  int lane;
+  __device__ __forceinline__ void wait_free() const {
+    if (lane == 0) bulk_wait_read0();
+    __syncwarp();
+  }
+  // row `lane` of a 32 x 32 fp32 block (128-byte rows, 128-byte swizzle)
+  __device__ __forceinline__ void put_f32(uint32_t off, const float (&v)[32]) const {
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      *reinterpret_cast<float4*>(p + off + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+          make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+  }
+  // columns [16h, 16h + 16) of row `lane` of a 32 x 32 fp32 block as a
+  // 32 x 16 block (64-byte rows, 64-byte swizzle)
+  __device__ __forceinline__ void put_f32_half(uint32_t off, const float (&v)[32], int h) const {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      *reinterpret_cast<float4*>(p + off + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) =
+          make_float4(v[16 * h + 4 * k], v[16 * h + 4 * k + 1], v[16 * h + 4 * k + 2],
+                      v[16 * h + 4 * k + 3]);
+  }
+  // row `lane` of a 32 x 32 bf16 block given as 16 packed pairs (64-byte
+  // rows, 64-byte swizzle)
+  __device__ __forceinline__ void put_bf16(uint32_t off, const uint32_t (&w)[16]) const {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      *reinterpret_cast<uint4*>(p + off + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) =
+          make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+  }
+  // make the block visible to the async proxy and store it at (x, y)
+  __device__ __forceinline__ void flush() const {
+    fence_proxy_async_smem();
+    __syncwarp();
+  }
+  __device__ __forceinline__ void store(const CUtensorMap* m, uint32_t off, int x, int y) const {
+    if (lane == 0) tma_store_2d(m, a + off, x, y);
+  }
+  __device__ __forceinline__ void commit() const {
+    if (lane == 0) bulk_commit();
+  }
+};
+
+__device__ __forceinline__ void pack_row_bf16(const float (&v)[32], uint32_t (&w)[16]) {
+#pragma unroll
+  for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(v[2 * k], v[2 * k + 1]);
+}
+
+// One warp's share of a tile: rows row0 + [0, 32) (this warp's TMEM lane
+// quarter) and half `half` of the tile's columns.
+template <int EPI, int BN, uint32_t STG>
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const OutMaps& om,
+                                              uint32_t tbase, int row0, int nt, int half,
+                                              const Stage& st) {
   const Epi& e = p.epi;
+  const int lane = st.lane;
+  const int row = row0 + lane;
   const bool row_ok = row < p.M;
   uint32_t r[32];
-  // this warp's share of the tile: 32-column chunks [c_lo, c_lo + 4)
-  const int c_lo = half * (BN / 64);
+  float v[32];
+  const int c_lo = half * (BN / 64);  // this warp's 32-column chunks [c_lo, c_lo + BN/64)
   if constexpr (EPI == EPI_BF16 || EPI == EPI_F32 || EPI == EPI_F32_RESID) {
 #pragma unroll 1
     for (int c = c_lo; c < c_lo + BN / 64; ++c) {
@@ -86,53 +166,70 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tbas
       if (col0 >= p.N) break;
       tmem_ld32(tbase + c * 32, r);
       tmem_ld_wait();
-      if (!row_ok) continue;
-      const bool full = col0 + 32 <= p.N;
-      if constexpr (EPI == EPI_BF16) {
-        bf16* out = reinterpret_cast<bf16*>(e.out) + (int64_t)row * e.ld_out + col0;
-        if (full) {
-          uint4* o4 = reinterpret_cast<uint4*>(out);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1]));
-            v.y = pack_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3]));
-            v.z = pack_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5]));
-            v.w = pack_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7]));
-            o4[j] = v;
-          }
-        } else {
-          #pragma unroll
-          for (int j = 0; j < 32; ++j) if (col0 + j < p.N)
-            out[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
-        }
-      } else {
-        float* out = reinterpret_cast<float*>(e.out) + (int64_t)row * e.ld_out + col0;
-        const float* res =
-            (EPI == EPI_F32_RESID) ? e.resid + (int64_t)row * e.ld_resid + col0 : nullptr;
-        if (full) {
-          float4* o4 = reinterpret_cast<float4*>(out);
+      for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+      if constexpr (EPI == EPI_F32_RESID) {
+        if (row_ok) {
+          const float* res = e.resid + (int64_t)row * e.ld_resid + col0;
+          if (col0 + 32 <= p.N) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            float4 v = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                   __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-            if constexpr (EPI == EPI_F32_RESID) {
+            for (int j = 0; j < 8; ++j) {
               const float4 q = reinterpret_cast<const float4*>(res)[j];
-              v.x += q.x; v.y += q.y; v.z += q.z; v.w += q.w;
+              v[4 * j] += q.x;
+              v[4 * j + 1] += q.y;
+              v[4 * j + 2] += q.z;
+              v[4 * j + 3] += q.w;
             }
-            o4[j] = v;
-          }
-        } else {
-          #pragma unroll
-          for (int j = 0; j < 32; ++j) if (col0 + j < p.N) {
-            float v = __uint_as_float(r[j]);
-            if constexpr (EPI == EPI_F32_RESID) v += res[j];
-            out[j] = v;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (col0 + j < p.N) v[j] += res[j];
           }
         }
       }
+      if (col0 + 32 > p.N && (p.N & (EPI == EPI_BF16 ? 7 : 3))) {
+        // a bulk store's bounds check works in 16-byte units, so a last chunk
+        // whose row end is not 16-byte aligned is written with plain stores
+        if (row_ok) {
+          if constexpr (EPI == EPI_BF16) {
+            bf16* out = reinterpret_cast<bf16*>(e.out) + (int64_t)row * e.ld_out + col0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (col0 + j < p.N) out[j] = __float2bfloat16_rn(v[j]);
+          } else {
+            float* out = reinterpret_cast<float*>(e.out) + (int64_t)row * e.ld_out + col0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (col0 + j < p.N) out[j] = v[j];
+          }
+        }
+        continue;
+      }
+      st.wait_free();
+      if constexpr (EPI == EPI_BF16) {
+        uint32_t w[16];
+        pack_row_bf16(v, w);
+        st.put_bf16(0, w);
+      } else if constexpr (STG >= 4096) {
+        st.put_f32(0, v);
+      } else {
+        st.put_f32_half(0, v, 0);
+        st.flush();
+        st.store(&om.o1, 0, col0, row0);
+        st.commit();
+        st.wait_free();
+        st.put_f32_half(0, v, 1);
+        st.flush();
+        st.store(&om.o1, 0, col0 + 16, row0);
+        st.commit();
+        continue;
+      }
+      st.flush();
+      st.store(&om.o1, 0, col0, row0);
+      st.commit();
     }
   } else if constexpr (EPI == EPI_SWIGLU) {
+    static_assert(BN == 256 && STG >= 4096, "SwiGLU tiles are 256 wide");
     // accumulator columns [0,128) = gate, [128,256) = up for I-columns nt*128 + [0,128)
     uint32_t u[32];
 #pragma unroll 1
@@ -142,40 +239,27 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tbas
       tmem_ld32(tbase + c * 32, r);
       tmem_ld32(tbase + 128 + c * 32, u);
       tmem_ld_wait();
-      if (!row_ok) continue;
-      bf16* gp = reinterpret_cast<bf16*>(e.out) + (int64_t)row * e.ld_out + col0;
-      bf16* up = gp + e.half;
-      bf16* sp = reinterpret_cast<bf16*>(e.out2) + (int64_t)row * e.ld_out2 + col0;
-      if (col0 + 32 <= e.half) {
+      uint32_t wg[16], wu[16], ws[16];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint4 vg, vu, vs;
-          uint32_t* pg = &vg.x;
-          uint32_t* pu = &vu.x;
-          uint32_t* ps = &vs.x;
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const float g0 = __uint_as_float(r[8 * j + 2 * h]);
-            const float g1 = __uint_as_float(r[8 * j + 2 * h + 1]);
-            const float u0 = __uint_as_float(u[8 * j + 2 * h]);
-            const float u1 = __uint_as_float(u[8 * j + 2 * h + 1]);
-            pg[h] = pack_bf16x2(g0, g1);
-            pu[h] = pack_bf16x2(u0, u1);
-            ps[h] = pack_bf16x2(silu_f(g0) * u0, silu_f(g1) * u1);
-          }
-          reinterpret_cast<uint4*>(gp)[j] = vg;
-          reinterpret_cast<uint4*>(up)[j] = vu;
-          reinterpret_cast<uint4*>(sp)[j] = vs;
-        }
-      } else {
-        #pragma unroll
-        for (int j = 0; j < 32; ++j) if (col0 + j < e.half) {
-          const float g = __uint_as_float(r[j]), uu = __uint_as_float(u[j]);
-          gp[j] = __float2bfloat16_rn(g);
-          up[j] = __float2bfloat16_rn(uu);
-          sp[j] = __float2bfloat16_rn(silu_f(g) * uu);
-        }
+      for (int k = 0; k < 16; ++k) {
+        const float g0 = __uint_as_float(r[2 * k]), g1 = __uint_as_float(r[2 * k + 1]);
+        const float u0 = __uint_as_float(u[2 * k]), u1 = __uint_as_float(u[2 * k + 1]);
+        wg[k] = pack_bf16x2(g0, g1);
+        wu[k] = pack_bf16x2(u0, u1);
+        ws[k] = pack_bf16x2(silu_f(g0) * u0, silu_f(g1) * u1);
       }
+      st.wait_free();
+      st.put_bf16(0, wg);
+      st.put_bf16(2048, wu);
+      st.flush();
+      st.store(&om.o1, 0, col0, row0);
+      st.store(&om.o2, 2048, col0, row0);
+      st.commit();
+      st.wait_free();
+      st.put_bf16(0, ws);
+      st.flush();
+      st.store(&om.o3, 0, col0, row0);
+      st.commit();
     }
   } else if constexpr (EPI == EPI_SWIGLU_BWD) {
     // g and u of the next chunk are loaded while the current one is computed
@@ -210,16 +294,11 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tbas
       tmem_ld32(tbase + c * 32, r);
       if (ci + 1 < BN / 64) load_aux(c + 1, (ci + 1) & 1);
       tmem_ld_wait();
-      if (!row_ok) continue;
-      bf16* dgp = reinterpret_cast<bf16*>(e.out) + (int64_t)row * e.ld_out + col0;
-      bf16* dup = dgp + e.half;
-      uint4 odg[4], odu[4];
+      uint32_t wdg[16], wdu[16];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const uint32_t* pg = &vg[ci & 1][j].x;
         const uint32_t* pu = &vu[ci & 1][j].x;
-        uint32_t* pdg = &odg[j].x;
-        uint32_t* pdu = &odu[j].x;
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
           float dgv[2], duv[2];
@@ -232,28 +311,31 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tbas
             dgv[q] = ds * uu * sg * (1.0f + g * (1.0f - sg));
             duv[q] = ds * g * sg;
           }
-          pdg[h] = pack_bf16x2(dgv[0], dgv[1]);
-          pdu[h] = pack_bf16x2(duv[0], duv[1]);
+          wdg[4 * j + h] = pack_bf16x2(dgv[0], dgv[1]);
+          wdu[4 * j + h] = pack_bf16x2(duv[0], duv[1]);
         }
       }
-      if (col0 + 32 <= p.N) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          reinterpret_cast<uint4*>(dgp)[j] = odg[j];
-          reinterpret_cast<uint4*>(dup)[j] = odu[j];
-        }
+      st.wait_free();
+      st.put_bf16(0, wdg);
+      if constexpr (STG >= 4096) {
+        st.put_bf16(2048, wdu);
+        st.flush();
+        st.store(&om.o1, 0, col0, row0);
+        st.store(&om.o2, 2048, col0, row0);
+        st.commit();
       } else {
-        const uint16_t* sg16 = reinterpret_cast<const uint16_t*>(&odg[0]);
-        const uint16_t* su16 = reinterpret_cast<const uint16_t*>(&odu[0]);
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (col0 + j < p.N) {
-            reinterpret_cast<uint16_t*>(dgp)[j] = sg16[j];
-            reinterpret_cast<uint16_t*>(dup)[j] = su16[j];
-          }
+        st.flush();
+        st.store(&om.o1, 0, col0, row0);
+        st.commit();
+        st.wait_free();
+        st.put_bf16(0, wdu);
+        st.flush();
+        st.store(&om.o2, 0, col0, row0);
+        st.commit();
       }
     }
   } else if constexpr (EPI == EPI_CE) {
+    static_assert(BN == 256, "CE tiles are 256 wide");
     float mx = -INFINITY, sum = 0.f;
     const int tgt = row_ok ? e.targets[row] : -1;
 #pragma unroll 1
@@ -262,7 +344,6 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tbas
       if (col0 >= p.N) break;
       tmem_ld32(tbase + c * 32, r);
       tmem_ld_wait();
-      if (!row_ok) continue;
       const int nvalid = min(32, p.N - col0);
       float cm = -INFINITY;
 #pragma unroll
@@ -275,28 +356,20 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tbas
         if (j < nvalid) acc += __expf(__uint_as_float(r[j]) - nm);
       mx = nm;
       sum = acc;
-      if (tgt >= col0 && tgt < col0 + nvalid) {
+      if (row_ok && tgt >= col0 && tgt < col0 + nvalid) {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
           if (j == tgt - col0) e.tgt_logit[row] = __uint_as_float(r[j]);
       }
-      bf16* out = reinterpret_cast<bf16*>(e.out) + (int64_t)row * e.ld_out + col0;
-      if (nvalid == 32) {
-        uint4* o4 = reinterpret_cast<uint4*>(out);
+      uint32_t w[16];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint4 v;
-          v.x = pack_bf16x2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1]));
-          v.y = pack_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3]));
-          v.z = pack_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5]));
-          v.w = pack_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7]));
-          o4[j] = v;
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < nvalid) out[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
-      }
+      for (int k = 0; k < 16; ++k)
+        w[k] = pack_bf16x2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
+      st.wait_free();
+      st.put_bf16(0, w);
+      st.flush();
+      st.store(&om.o1, 0, col0, row0);
+      st.commit();
     }
     if (row_ok) e.part[(int64_t)row * e.part_ld + 2 * nt + half] = make_float2(mx, sum);
   }
@@ -306,13 +379,15 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tbas
 template <int A_MN, int B_MN, int EPI, int BN>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
-                const __grid_constant__ CUtensorMap tma_b, const GemmParams p) {
+                const __grid_constant__ CUtensorMap tma_b, const __grid_constant__ OutMaps om,
+                const GemmParams p) {
   constexpr int STAGES = Tile<BN>::STAGES;
   constexpr uint32_t STAGE_BYTES = Tile<BN>::STAGE_BYTES;
+  using OS = OutStage<BN, false>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tile<BN>::OFF_OUT + OS::TOTAL);
   // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   const uint32_t full0 = smem_u32(bars);
@@ -331,7 +406,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, EPI_THREADS);
+      mbar_init(tempty0 + 8 * a, EPI_THREADS / 32);  // one arrival per epilogue warp
     }
     mbar_init(drain, 1);
     fence_mbar_init();
@@ -456,21 +531,25 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;             // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;   // which half of the tile's columns
+    uint8_t* stg = smem + Tile<BN>::OFF_OUT + (warp - 2) * OS::BYTES;
+    const Stage st{stg, smem_u32(stg), lane};
     int acc = 0;
     uint32_t acc_ph = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       int mt, nt;
       tile_coords(t, p, mt, nt);
-      if (!mbar_wait(tfull0 + 8 * acc, acc_ph, p.err)) break;
+      if (!warp_wait(tfull0 + 8 * acc, acc_ph, p.err)) break;
       tc_fence_after();
-      const int row = mt * BM + q * 32 + lane;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      epilogue_tile<EPI, BN>(p, tbase, row, mt, nt, half);
+      epilogue_tile<EPI, BN, OS::BYTES>(p, om, tbase, mt * BM + q * 32, nt, half, st);
       tc_fence_before();
-      mbar_arrive(tempty0 + 8 * acc);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
       acc ^= 1;
       if (acc == 0) acc_ph ^= 1;
     }
+    if (lane == 0) bulk_wait0();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -501,13 +580,15 @@ struct Tile2 {
   static constexpr uint32_t B_BYTES = BH * BK * 2;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB
   static constexpr int STAGES = 6;
-  static constexpr size_t SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr uint32_t OFF_OUT = STAGES * STAGE_BYTES;
+  static constexpr size_t SMEM = OFF_OUT + OutStage<BN, true>::TOTAL + 1024 + 256;
 };
 
 template <int A_MN, int B_MN, int EPI, int BN>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm2_kernel(const __grid_constant__ CUtensorMap tma_a,
-                 const __grid_constant__ CUtensorMap tma_b, const GemmParams p) {
+                 const __grid_constant__ CUtensorMap tma_b, const __grid_constant__ OutMaps om,
+                 const GemmParams p) {
   using TL = Tile2<BN>;
   constexpr int STAGES = TL::STAGES;
   constexpr int BH = TL::BH;
@@ -515,7 +596,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  using OS = OutStage<BN, true>;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + TL::OFF_OUT + OS::TOTAL);
   // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   const uint32_t full0 = smem_u32(bars);
@@ -653,6 +735,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
+    uint8_t* stg = smem + TL::OFF_OUT + (warp - 2) * OS::BYTES;
+    const Stage st{stg, smem_u32(stg), lane};
     int acc = 0;
     uint32_t acc_ph = 0;
     for (int t = pair; t < ntiles; t += npairs) {
@@ -661,15 +745,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       if (!warp_wait(tfull0 + 8 * acc, acc_ph, p.err)) break;
       tc_fence_after();
       const int mrow = 2 * mt + static_cast<int>(rank);
-      const int row = mrow * BM + q * 32 + lane;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      epilogue_tile<EPI, BN>(p, tbase, row, mrow, nt, half);
+      epilogue_tile<EPI, BN, OS::BYTES>(p, om, tbase, mrow * BM + q * 32, nt, half, st);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty_even + 8 * acc);
       acc ^= 1;
       if (acc == 0) acc_ph ^= 1;
     }
+    if (lane == 0) bulk_wait0();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -732,9 +817,53 @@ static bool make_map(CUtensorMap* m, const Mat& x, int box_rows) {
   return make_tma_2d(m, x.ptr, x.rows, x.cols, x.ld, box_rows);
 }
 
+// Store map of an output matrix [rows, cols] with row stride ld elements:
+// 32 x 32 boxes, fp32 with 128-byte or bf16 with 64-byte swizzle (the layouts
+// Stage::put_f32 / put_bf16 write).
+static bool make_out_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld,
+                         bool f32, bool narrow = false) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const int es = f32 ? 4 : 2;
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15) || (ld * es) % 16) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * es};
+  // box: 32 rows of 32 elements, or of 16 fp32 (64-byte rows) when narrow
+  cuuint32_t box[2] = {(f32 && narrow) ? 16u : 32u, 32u};
+  cuuint32_t estr[2] = {1u, 1u};
+  return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+             const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             (f32 && !narrow) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The output maps an epilogue stores through (see OutMaps); narrow: fp32
+// blocks are staged as 32 x 16 (OutStage of 2 KB).
+static bool make_out_maps(OutMaps* om, const Epi& e, int M, int N, bool narrow) {
+  memset(om, 0, sizeof(*om));
+  bf16* out = static_cast<bf16*>(e.out);
+  switch (e.kind) {
+    case EPI_F32:
+    case EPI_F32_RESID:
+      return make_out_map(&om->o1, e.out, M, N, e.ld_out, true, narrow);
+    case EPI_BF16:
+    case EPI_CE:
+      return make_out_map(&om->o1, e.out, M, N, e.ld_out, false);
+    case EPI_SWIGLU:
+      return make_out_map(&om->o1, out, M, e.half, e.ld_out, false) &&
+             make_out_map(&om->o2, out + e.half, M, e.half, e.ld_out, false) &&
+             make_out_map(&om->o3, e.out2, M, e.half, e.ld_out2, false);
+    case EPI_SWIGLU_BWD:
+      return make_out_map(&om->o1, out, M, N, e.ld_out, false) &&
+             make_out_map(&om->o2, out + e.half, M, N, e.ld_out, false);
+    default:
+      return false;
+  }
+}
+
 template <int A_MN, int B_MN, int EPI, int BN>
-static cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
-                          cudaStream_t s) {
+static cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const OutMaps& om,
+                          const GemmParams& p, cudaStream_t s) {
   static bool attr_done = false;  // per instantiation; the attribute is per function
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<A_MN, B_MN, EPI, BN>,
@@ -747,14 +876,14 @@ static cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const Ge
   const int grid = ntiles < num_sms() ? ntiles : num_sms();
   const int64_t slot = gemm_timing_before(s, 2.0 * p.M * (double)p.N * p.K);
   note_launch();
-  gemm_kernel<A_MN, B_MN, EPI, BN><<<grid, GEMM_THREADS, Tile<BN>::SMEM, s>>>(ta, tb, p);
+  gemm_kernel<A_MN, B_MN, EPI, BN><<<grid, GEMM_THREADS, Tile<BN>::SMEM, s>>>(ta, tb, om, p);
   gemm_timing_after(s, slot);
   return cudaGetLastError();
 }
 
 template <int A_MN, int B_MN, int EPI, int BN>
-static cudaError_t launch2(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
-                           int max_pairs, cudaStream_t s) {
+static cudaError_t launch2(const CUtensorMap& ta, const CUtensorMap& tb, const OutMaps& om,
+                           const GemmParams& p, int max_pairs, cudaStream_t s) {
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(gemm2_kernel<A_MN, B_MN, EPI, BN>,
@@ -779,7 +908,7 @@ static cudaError_t launch2(const CUtensorMap& ta, const CUtensorMap& tb, const G
   cfg.numAttrs = 1;
   const int64_t slot = gemm_timing_before(s, 2.0 * p.M * (double)p.N * p.K);
   note_launch();
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm2_kernel<A_MN, B_MN, EPI, BN>, ta, tb, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm2_kernel<A_MN, B_MN, EPI, BN>, ta, tb, om, p);
   gemm_timing_after(s, slot);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -879,6 +1008,11 @@ cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N,
     *why = "gemm: cuTensorMapEncodeTiled failed";
     return cudaErrorInvalidValue;
   }
+  OutMaps om;
+  if (!make_out_maps(&om, epi, M, N, !pair_tiles && bn == 192)) {
+    *why = "gemm: outputs need 16-byte aligned rows (cuTensorMapEncodeTiled failed)";
+    return cudaErrorInvalidValue;
+  }
   GemmParams p;
   p.M = M;
   p.N = N;
@@ -893,10 +1027,10 @@ cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N,
   p.err = err;
 #define RDT_GEMM_CASE(AM, BMJ, E, W)                                           \
   if (!pair_tiles && a_mn == (AM) && b_mn == (BMJ) && epi.kind == (E) && bn == (W)) \
-    return launch<AM, BMJ, E, W>(ta, tb, p, s);
+    return launch<AM, BMJ, E, W>(ta, tb, om, p, s);
 #define RDT_GEMM2_CASE(AM, BMJ, E, W)                                          \
   if (pair_tiles && a_mn == (AM) && b_mn == (BMJ) && epi.kind == (E) && bn == (W)) \
-    return launch2<AM, BMJ, E, W>(ta, tb, p, pairs_max, s);
+    return launch2<AM, BMJ, E, W>(ta, tb, om, p, pairs_max, s);
   // forward projections: A K-major, B K-major
   RDT_GEMM_CASE(0, 0, EPI_BF16, 256)
   RDT_GEMM_CASE(0, 0, EPI_BF16, 192)
