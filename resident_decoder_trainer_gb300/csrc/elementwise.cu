@@ -224,78 +224,75 @@ cudaError_t rope_table(float* cs, int S, int d, float theta, cudaStream_t s) {
 }
 
 // ----------------------------------------------------- QK RMSNorm + RoPE fwd
-// A head of D elements is handled by D/8 lanes, 8 consecutive elements each
-// (16-byte loads); a warp covers 256/D heads per iteration. Lanes of the first
-// half of a head hold elements i < D/2, their partner (lane ^ D/16) the
-// rotation partners i + D/2.
-// Items are (token, head) over nh query heads, nkv key heads and nkv value
-// heads; value heads are only converted to bf16 for the attention.
+// A head of D elements is handled by D/4 lanes, 4 consecutive elements each
+// (16-byte fp32 loads); a warp covers 128/D heads per pass. Lanes of the first
+// half of a head hold elements i < D/2, their partner (lane ^ D/8) the
+// rotation partners i + D/2. A CTA walks whole tokens: every lane loads the
+// cos/sin of its 4 rotation pairs once per token and reuses them for all of
+// the token's heads; each warp keeps two head groups of loads in flight.
+// Heads: nh query heads, nkv key heads, nkv value heads (value heads are only
+// converted to bf16 for the attention).
 template <int D>
 __global__ void __launch_bounds__(256) qknorm_rope_fwd_kernel(
     const float* __restrict__ qkv, int64_t ld, bf16* __restrict__ qo, bf16* __restrict__ ko,
     bf16* __restrict__ vo, float* __restrict__ rq, float* __restrict__ rk,
     const float* __restrict__ gq, const float* __restrict__ gk, const float2* __restrict__ cs,
     int T, int S, int nh, int nkv, float eps) {
-  constexpr int LPH = D / 8, HPW = 32 / LPH, HALF = D / 2, PX = LPH / 2;
-  const int lane = threadIdx.x & 31;
+  constexpr int LPH = D / 4, HPW = 32 / LPH, PX = LPH / 2, HALF = D / 2;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int slot = lane / LPH, sub = lane % LPH;
   const bool first = sub < PX;
+  const int i0 = 4 * (first ? sub : sub - PX);
   const int heads = nh + 2 * nkv;
-  const int64_t items = (int64_t)T * heads;
-  const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t it0 = warp_id * HPW; it0 < items; it0 += nwarps * HPW) {
-    const int64_t item = it0 + slot;
-    const bool valid = item < items;
-    const int t = valid ? static_cast<int>(item / heads) : 0;
-    const int hd = valid ? static_cast<int>(item % heads) : 0;
+  const int groups = (heads + HPW - 1) / HPW;
+  const float4 gq4 = reinterpret_cast<const float4*>(gq)[sub];
+  const float4 gk4 = reinterpret_cast<const float4*>(gk)[sub];
+  auto head_out = [&](int t, int hd, const float4& xin, const float4& c01, const float4& c23) {
+    const bool valid = hd < heads;
     const bool isq = hd < nh;
     const bool isv = hd >= nh + nkv;
-    const int h = isq ? hd : (isv ? hd - nh - nkv : hd - nh);
-    const float* src = qkv + (int64_t)t * ld + hd * D + 8 * sub;
-    float xv[8] = {};
-    if (valid) {
-      const float4 a = *reinterpret_cast<const float4*>(src);
-      const float4 c = *reinterpret_cast<const float4*>(src + 4);
-      xv[0] = a.x; xv[1] = a.y; xv[2] = a.z; xv[3] = a.w;
-      xv[4] = c.x; xv[5] = c.y; xv[6] = c.z; xv[7] = c.w;
-    }
-    if (valid && isv) {
-      *reinterpret_cast<uint4*>(vo + (int64_t)t * nkv * D + h * D + 8 * sub) =
-          make_uint4(pack_bf16x2(xv[0], xv[1]), pack_bf16x2(xv[2], xv[3]),
-                     pack_bf16x2(xv[4], xv[5]), pack_bf16x2(xv[6], xv[7]));
-    }
-    float ss = 0.f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) ss += xv[e] * xv[e];
+    const float x[4] = {xin.x, xin.y, xin.z, xin.w};
+    if (valid && isv)
+      *reinterpret_cast<uint2*>(vo + ((int64_t)t * nkv + (hd - nh - nkv)) * D + 4 * sub) =
+          make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
+    float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
 #pragma unroll
     for (int o = LPH / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     const float r = rsqrtf(ss / D + eps);
-    const float* g = (isq ? gq : gk) + 8 * sub;
-    float y[8], yp[8];
+    const float4 g4 = isq ? gq4 : gk4;
+    const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+    float y[4], yp[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) y[e] = xv[e] * r * g[e];
+    for (int e = 0; e < 4; ++e) y[e] = x[e] * r * gv[e];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) yp[e] = __shfl_xor_sync(0xffffffffu, y[e], PX);
-    const int i0 = 8 * (first ? sub : sub - PX);
-    const int pos = t % S;
-    const float2* c = cs + (int64_t)pos * HALF + i0;
-    float out[8];
+    for (int e = 0; e < 4; ++e) yp[e] = __shfl_xor_sync(0xffffffffu, y[e], PX);
+    const float cv[4] = {c01.x, c01.z, c23.x, c23.z}, sv[4] = {c01.y, c01.w, c23.y, c23.w};
+    float out[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float2 cv = c[e];
-      out[e] = first ? y[e] * cv.x - yp[e] * cv.y : y[e] * cv.x + yp[e] * cv.y;
-    }
+    for (int e = 0; e < 4; ++e)
+      out[e] = first ? y[e] * cv[e] - yp[e] * sv[e] : y[e] * cv[e] + yp[e] * sv[e];
     if (valid && !isv) {
-      bf16* dst = (isq ? qo + (int64_t)t * nh * D + h * D : ko + (int64_t)t * nkv * D + h * D) +
-                  8 * sub;
-      *reinterpret_cast<uint4*>(dst) =
-          make_uint4(pack_bf16x2(out[0], out[1]), pack_bf16x2(out[2], out[3]),
-                     pack_bf16x2(out[4], out[5]), pack_bf16x2(out[6], out[7]));
+      bf16* dst = isq ? qo + ((int64_t)t * nh + hd) * D : ko + ((int64_t)t * nkv + (hd - nh)) * D;
+      *reinterpret_cast<uint2*>(dst + 4 * sub) =
+          make_uint2(pack_bf16x2(out[0], out[1]), pack_bf16x2(out[2], out[3]));
       if (sub == 0) {
-        if (isq) rq[(int64_t)t * nh + h] = r;
-        else rk[(int64_t)t * nkv + h] = r;
+        if (isq) rq[(int64_t)t * nh + hd] = r;
+        else rk[(int64_t)t * nkv + (hd - nh)] = r;
       }
+    }
+  };
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    const float4* c4 = reinterpret_cast<const float4*>(cs + (int64_t)(t % S) * HALF + i0);
+    const float4 c01 = c4[0], c23 = c4[1];
+    const float* row = qkv + (int64_t)t * ld + 4 * sub;
+    for (int g0 = warp; g0 < groups; g0 += 16) {
+      const int h0 = g0 * HPW + slot, h1 = (g0 + 8) * HPW + slot;
+      const float4 x0 = h0 < heads ? *reinterpret_cast<const float4*>(row + h0 * D)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 x1 = h1 < heads ? *reinterpret_cast<const float4*>(row + h1 * D)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      head_out(t, h0, x0, c01, c23);
+      if (g0 + 8 < groups) head_out(t, h1, x1, c01, c23);
     }
   }
 }
@@ -310,8 +307,7 @@ cudaError_t qknorm_rope_fwd(const float* qkv, int64_t ld_qkv, bf16* q_out, bf16*
                             bf16* v_out, float* rstd_q, float* rstd_k, const float* gq,
                             const float* gk, const float* cs, int T, int S, int nh, int nkv, int d,
                             float eps, cudaStream_t s) {
-  const int64_t items = (int64_t)T * (nh + 2 * nkv);
-  const int grid = elementwise_grid((items * d + 255) / 256);
+  const int grid = T < 8 * num_sms() ? (T > 0 ? T : 1) : 8 * num_sms();
   const float2* c2 = reinterpret_cast<const float2*>(cs);
   note_launch();
   switch (d) {
@@ -325,103 +321,104 @@ cudaError_t qknorm_rope_fwd(const float* qkv, int64_t ld_qkv, bf16* q_out, bf16*
 }
 
 // ----------------------------------------------------- QK RMSNorm + RoPE bwd
-// Same lane layout as the forward. Inverse rotation of the incoming fp32
-// gradient, then the RMSNorm backward over head_dim. Gain gradients: each lane
-// always owns the same 8 columns, so it accumulates them in registers; lanes
-// of different head slots are combined by shuffles, warps in a fixed order,
-// and each CTA writes one partial row [q gains | k gains].
+// Same lane layout and token walk as the forward. Inverse rotation of the
+// incoming fp32 gradient, then the RMSNorm backward over head_dim. Gain
+// gradients: each lane always owns the same 4 columns, so it accumulates them
+// in registers; lanes of different head slots are combined by shuffles, warps
+// in a fixed order, and each CTA writes one partial row [q gains | k gains].
 template <int D>
 __global__ void __launch_bounds__(256) qknorm_rope_bwd_kernel(
     const float* __restrict__ dq, const float* __restrict__ dk, const float* __restrict__ qkv,
     int64_t ld, const float* __restrict__ rq, const float* __restrict__ rk,
     const float* __restrict__ gq, const float* __restrict__ gk, const float2* __restrict__ cs,
     bf16* __restrict__ dqkv, float* __restrict__ partials, int T, int S, int nh, int nkv) {
-  constexpr int LPH = D / 8, HPW = 32 / LPH, HALF = D / 2, PX = LPH / 2;
+  constexpr int LPH = D / 4, HPW = 32 / LPH, PX = LPH / 2, HALF = D / 2;
   __shared__ float red[8][2 * D];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int slot = lane / LPH, sub = lane % LPH;
   const bool first = sub < PX;
+  const int i0 = 4 * (first ? sub : sub - PX);
   const int heads = nh + nkv;
-  const int64_t items = (int64_t)T * heads;
-  const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  float accq[8] = {}, acck[8] = {};
-  float gqv[8], gkv[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    gqv[e] = gq[8 * sub + e];
-    gkv[e] = gk[8 * sub + e];
-  }
-  const int i0 = 8 * (first ? sub : sub - PX);
-  for (int64_t it0 = warp_id * HPW; it0 < items; it0 += nwarps * HPW) {
-    const int64_t item = it0 + slot;
-    const bool valid = item < items;
-    const int t = valid ? static_cast<int>(item / heads) : 0;
-    const int hd = valid ? static_cast<int>(item % heads) : 0;
-    const bool isq = hd < nh;
-    const int h = isq ? hd : hd - nh;
-    const int col = (isq ? h * D : nh * D + h * D) + 8 * sub;
-    float din[8] = {}, xv[8] = {};
-    float r = 0.f;
-    if (valid) {
-      const float* gsrc = (isq ? dq + (int64_t)t * nh * D + h * D : dk + (int64_t)t * nkv * D + h * D) +
-                          8 * sub;
-      const float4 d0 = *reinterpret_cast<const float4*>(gsrc);
-      const float4 d1 = *reinterpret_cast<const float4*>(gsrc + 4);
-      din[0] = d0.x; din[1] = d0.y; din[2] = d0.z; din[3] = d0.w;
-      din[4] = d1.x; din[5] = d1.y; din[6] = d1.z; din[7] = d1.w;
-      const float4 xa = *reinterpret_cast<const float4*>(qkv + (int64_t)t * ld + col);
-      const float4 xb = *reinterpret_cast<const float4*>(qkv + (int64_t)t * ld + col + 4);
-      xv[0] = xa.x; xv[1] = xa.y; xv[2] = xa.z; xv[3] = xa.w;
-      xv[4] = xb.x; xv[5] = xb.y; xv[6] = xb.z; xv[7] = xb.w;
-      r = isq ? rq[(int64_t)t * nh + h] : rk[(int64_t)t * nkv + h];
+  const int groups = (heads + HPW - 1) / HPW;
+  const float4 gq4 = reinterpret_cast<const float4*>(gq)[sub];
+  const float4 gk4 = reinterpret_cast<const float4*>(gk)[sub];
+  float accq[4] = {}, acck[4] = {};
+  struct In {
+    float4 d, x;
+    float r;
+  };
+  auto load = [&](int t, int hd) {
+    In in{make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f), 0.f};
+    if (hd < heads) {
+      const bool isq = hd < nh;
+      const float* gsrc = isq ? dq + ((int64_t)t * nh + hd) * D : dk + ((int64_t)t * nkv + (hd - nh)) * D;
+      in.d = *reinterpret_cast<const float4*>(gsrc + 4 * sub);
+      in.x = *reinterpret_cast<const float4*>(qkv + (int64_t)t * ld + hd * D + 4 * sub);
+      in.r = isq ? rq[(int64_t)t * nh + hd] : rk[(int64_t)t * nkv + (hd - nh)];
     }
-    float dp[8];
+    return in;
+  };
+  auto head_grad = [&](int t, int hd, const In& in, const float4& c01, const float4& c23) {
+    const bool valid = hd < heads;
+    const bool isq = hd < nh;
+    const float din[4] = {in.d.x, in.d.y, in.d.z, in.d.w};
+    const float xv[4] = {in.x.x, in.x.y, in.x.z, in.x.w};
+    float dp[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) dp[e] = __shfl_xor_sync(0xffffffffu, din[e], PX);
-    const int pos = t % S;
-    const float2* c = cs + (int64_t)pos * HALF + i0;
-    float xh[8], dxh[8];
+    for (int e = 0; e < 4; ++e) dp[e] = __shfl_xor_sync(0xffffffffu, din[e], PX);
+    const float cv[4] = {c01.x, c01.z, c23.x, c23.z}, sv[4] = {c01.y, c01.w, c23.y, c23.w};
+    const float4 g4 = isq ? gq4 : gk4;
+    const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+    float xh[4], dxh[4];
     float dot = 0.f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float2 cv = c[e];
+    for (int e = 0; e < 4; ++e) {
       // inverse rotation: first half d0 c + d1 s, second half d1 c - d0 s
-      const float dn = first ? din[e] * cv.x + dp[e] * cv.y : din[e] * cv.x - dp[e] * cv.y;
-      xh[e] = xv[e] * r;
+      const float dn = first ? din[e] * cv[e] + dp[e] * sv[e] : din[e] * cv[e] - dp[e] * sv[e];
+      xh[e] = xv[e] * in.r;
       if (valid) {
         if (isq) accq[e] += dn * xh[e];
         else acck[e] += dn * xh[e];
       }
-      dxh[e] = dn * (isq ? gqv[e] : gkv[e]);
+      dxh[e] = dn * gv[e];
       dot += dxh[e] * xh[e];
     }
 #pragma unroll
     for (int o = LPH / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
     const float cmean = dot / D;
     if (valid) {
-      float o8[8];
+      float o4[4];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o8[e] = r * (dxh[e] - xh[e] * cmean);
-      *reinterpret_cast<uint4*>(dqkv + (int64_t)t * ld + col) =
-          make_uint4(pack_bf16x2(o8[0], o8[1]), pack_bf16x2(o8[2], o8[3]),
-                     pack_bf16x2(o8[4], o8[5]), pack_bf16x2(o8[6], o8[7]));
+      for (int e = 0; e < 4; ++e) o4[e] = in.r * (dxh[e] - xh[e] * cmean);
+      *reinterpret_cast<uint2*>(dqkv + (int64_t)t * ld + hd * D + 4 * sub) =
+          make_uint2(pack_bf16x2(o4[0], o4[1]), pack_bf16x2(o4[2], o4[3]));
+    }
+  };
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    const float4* c4 = reinterpret_cast<const float4*>(cs + (int64_t)(t % S) * HALF + i0);
+    const float4 c01 = c4[0], c23 = c4[1];
+    for (int g0 = warp; g0 < groups; g0 += 16) {
+      const int h0 = g0 * HPW + slot, h1 = (g0 + 8) * HPW + slot;
+      const In in0 = load(t, h0);
+      const In in1 = load(t, g0 + 8 < groups ? h1 : heads);
+      head_grad(t, h0, in0, c01, c23);
+      if (g0 + 8 < groups) head_grad(t, h1, in1, c01, c23);
     }
   }
   // combine head slots of the warp (lanes with equal sub), fixed order
 #pragma unroll
   for (int o = LPH; o < 32; o <<= 1) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
+    for (int e = 0; e < 4; ++e) {
       accq[e] += __shfl_xor_sync(0xffffffffu, accq[e], o);
       acck[e] += __shfl_xor_sync(0xffffffffu, acck[e], o);
     }
   }
   if (slot == 0) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      red[warp][8 * sub + e] = accq[e];
-      red[warp][D + 8 * sub + e] = acck[e];
+    for (int e = 0; e < 4; ++e) {
+      red[warp][4 * sub + e] = accq[e];
+      red[warp][D + 4 * sub + e] = acck[e];
     }
   }
   __syncthreads();
@@ -432,10 +429,10 @@ __global__ void __launch_bounds__(256) qknorm_rope_bwd_kernel(
   }
 }
 
-int qknorm_bwd_partial_rows(int T, int heads) {
-  const int64_t want = ((int64_t)T * heads + 63) / 64;
+int qknorm_bwd_partial_rows(int T, int) {
+  // one CTA (and one partial row) per token, at most kMaxPartialRows
   const int cap = kMaxPartialRows;
-  return want < cap ? static_cast<int>(want > 0 ? want : 1) : cap;
+  return T < cap ? (T > 0 ? T : 1) : cap;
 }
 
 cudaError_t qknorm_rope_bwd(const float* dq, const float* dk, const float* qkv, int64_t ld_qkv,
