@@ -297,12 +297,6 @@ __global__ void __launch_bounds__(256) qknorm_rope_fwd_kernel(
   }
 }
 
-static int elementwise_grid(int64_t warps_needed) {
-  const int64_t blocks = (warps_needed + 7) / 8;
-  const int64_t cap = 16LL * num_sms();
-  return static_cast<int>(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
-}
-
 cudaError_t qknorm_rope_fwd(const float* qkv, int64_t ld_qkv, bf16* q_out, bf16* k_out,
                             bf16* v_out, float* rstd_q, float* rstd_k, const float* gq,
                             const float* gk, const float* cs, int T, int S, int nh, int nkv, int d,

@@ -34,9 +34,9 @@ constexpr int GEMM_THREADS = 320;
 constexpr int EPI_THREADS = 256;
 constexpr int TMEM_COLS = 512;
 
-// Epilogue output staging per epilogue warp (see the epilogues below): 4 KB;
-// 128 x 192 single-CTA tiles keep a 5-stage ring by staging 2 KB per warp
-// (fp32 blocks then go out as two 32 x 16 boxes with 64-byte rows).
+// Epilogue staging per epilogue warp (two buffers, see the epilogues below):
+// 4 KB; 128 x 192 single-CTA tiles keep a 5-stage ring by staging 2 KB per
+// warp (in units half as wide).
 template <int BN, bool PAIR>
 struct OutStage {
   static constexpr uint32_t BYTES = (BN == 192 && !PAIR) ? 2048 : 4096;
@@ -53,7 +53,7 @@ struct Tile {
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = BN == 256 ? 4 : 5;
   static constexpr uint32_t OFF_OUT = STAGES * STAGE_BYTES;
-  static constexpr size_t SMEM = OFF_OUT + OutStage<BN, false>::TOTAL + 1024 + 256;
+  static constexpr size_t SMEM = OFF_OUT + OutStage<BN, false>::TOTAL + 1024 + 512;
 };
 
 struct GemmParams {
@@ -83,268 +83,166 @@ __device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& mt,
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
 // -------------------------------------------------------------- epilogues
-// Every output goes through a 4 KB staging buffer per epilogue warp: each
-// thread writes its row of a 32-row x 32-column block into the buffer in the
-// TMA swizzle layout (fp32: 128-byte rows, 128-byte swizzle; bf16: 64-byte
-// rows, 64-byte swizzle - conflict-free either way), and one lane stores the
-// block with a TMA bulk tensor store (whole 128-byte lines; the tensor map
-// clips the box at M and, in 16-byte units, at N).
+// Each epilogue warp owns 32 rows (its TMEM lane quarter) and half of the
+// tile's columns, and streams them out in units of UNIT columns through two
+// staging buffers (STG/2 bytes each) in shared memory:
+//   * every thread writes its row of the unit into the buffer in the layout of
+//     a TMA box with the matching swizzle (rows of 16, 32, 64 or 128 bytes;
+//     conflict-free), and one lane writes the box with a bulk tensor store
+//     (whole lines; the tensor map clips it at M and, in 16-byte units, N);
+//   * the buffers alternate, so a unit is written while the previous unit's
+//     store is still reading the other buffer;
+//   * inputs of the residual and SwiGLU-backward epilogues arrive the same way
+//     in reverse: a TMA load of the next unit's residual / g / u box is in
+//     flight while the current unit is computed in place.
+__host__ __device__ constexpr int epi_unit(int kind, uint32_t stg) {
+  return kind == EPI_SWIGLU ? 32                                      // g+u, then s
+         : (kind == EPI_BF16 || kind == EPI_CE) ? (stg >= 4096 ? 32 : 16)
+                                               : (stg >= 4096 ? 16 : 8);  // fp32; g+u in, dg+du out
+}
+__host__ __device__ constexpr int epi_elem_bytes(int kind) {
+  return (kind == EPI_F32 || kind == EPI_F32_RESID) ? 4 : 2;
+}
 
-// Output tensor maps: o1 = out (g for SwiGLU, dg for SwiGLU-bwd, logits for
-// CE), o2 = u / du, o3 = s.
+// Output / input tensor maps: o1 = out (g for SwiGLU, dg for SwiGLU-bwd,
+// logits for CE), o2 = u / du, o3 = s; i1 = residual or g, i2 = u.
 struct OutMaps {
-  CUtensorMap o1, o2, o3;
+  CUtensorMap o1, o2, o3, i1, i2;
 };
 
 struct Stage {
-  uint8_t* p;    // this warp's staging buffer
-  uint32_t a;    // its shared-memory address
+  uint8_t* p;    // this warp's two staging buffers
+  uint32_t a;    // their shared-memory address
+  uint32_t bar;  // this warp's two input mbarriers
   int lane;
-  __device__ __forceinline__ void wait_free() const {
-    if (lane == 0) bulk_wait_read0();
-    __syncwarp();
-  }
-  // row `lane` of a 32 x 32 fp32 block (128-byte rows, 128-byte swizzle)
-  __device__ __forceinline__ void put_f32(uint32_t off, const float (&v)[32]) const {
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-      *reinterpret_cast<float4*>(p + off + lane * 128 + ((k ^ (lane & 7)) << 4)) =
-          make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-  }
-  // columns [16h, 16h + 16) of row `lane` of a 32 x 32 fp32 block as a
-  // 32 x 16 block (64-byte rows, 64-byte swizzle)
-  __device__ __forceinline__ void put_f32_half(uint32_t off, const float (&v)[32], int h) const {
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      *reinterpret_cast<float4*>(p + off + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) =
-          make_float4(v[16 * h + 4 * k], v[16 * h + 4 * k + 1], v[16 * h + 4 * k + 2],
-                      v[16 * h + 4 * k + 3]);
-  }
-  // row `lane` of a 32 x 32 bf16 block given as 16 packed pairs (64-byte
-  // rows, 64-byte swizzle)
-  __device__ __forceinline__ void put_bf16(uint32_t off, const uint32_t (&w)[16]) const {
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      *reinterpret_cast<uint4*>(p + off + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) =
-          make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-  }
-  // make the block visible to the async proxy and store it at (x, y)
-  __device__ __forceinline__ void flush() const {
-    fence_proxy_async_smem();
-    __syncwarp();
-  }
-  __device__ __forceinline__ void store(const CUtensorMap* m, uint32_t off, int x, int y) const {
-    if (lane == 0) tma_store_2d(m, a + off, x, y);
-  }
-  __device__ __forceinline__ void commit() const {
-    if (lane == 0) bulk_commit();
-  }
 };
 
-__device__ __forceinline__ void pack_row_bf16(const float (&v)[32], uint32_t (&w)[16]) {
-#pragma unroll
-  for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(v[2 * k], v[2 * k + 1]);
+// Offset of 16-byte chunk k of row r in a block of 32 rows x RB bytes, as a
+// TMA box with 128/64/32-byte swizzle (RB = 128/64/32) or none (RB = 16).
+template <uint32_t RB>
+__device__ __forceinline__ uint32_t stg_off(int r, int k) {
+  constexpr int sh = RB == 128 ? 0 : RB == 64 ? 1 : RB == 32 ? 2 : 3;
+  constexpr int mask = static_cast<int>(RB / 16) - 1;
+  return r * RB + static_cast<uint32_t>(((k ^ (r >> sh)) & mask) << 4);
 }
 
-// One warp's share of a tile: rows row0 + [0, 32) (this warp's TMEM lane
-// quarter) and half `half` of the tile's columns.
+// Row `lane` of a unit: UNIT fp32 values as fp32 or bf16.
+template <uint32_t RB, int UNIT>
+__device__ __forceinline__ void put_f32(uint8_t* b, int lane, const float* v) {
+#pragma unroll
+  for (int k = 0; k < UNIT / 4; ++k)
+    *reinterpret_cast<float4*>(b + stg_off<RB>(lane, k)) =
+        make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+}
+template <uint32_t RB, int UNIT>
+__device__ __forceinline__ void put_bf16(uint8_t* b, int lane, const float* v) {
+#pragma unroll
+  for (int k = 0; k < UNIT / 8; ++k)
+    *reinterpret_cast<uint4*>(b + stg_off<RB>(lane, k)) =
+        make_uint4(pack_bf16x2(v[8 * k], v[8 * k + 1]), pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
+                   pack_bf16x2(v[8 * k + 4], v[8 * k + 5]),
+                   pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
+}
+template <uint32_t RB, int UNIT>
+__device__ __forceinline__ void get_f32(const uint8_t* b, int lane, float* v) {
+#pragma unroll
+  for (int k = 0; k < UNIT / 4; ++k) {
+    const float4 q = *reinterpret_cast<const float4*>(b + stg_off<RB>(lane, k));
+    v[4 * k] = q.x;
+    v[4 * k + 1] = q.y;
+    v[4 * k + 2] = q.z;
+    v[4 * k + 3] = q.w;
+  }
+}
+template <uint32_t RB, int UNIT>
+__device__ __forceinline__ void get_bf16(const uint8_t* b, int lane, float* v) {
+#pragma unroll
+  for (int k = 0; k < UNIT / 8; ++k) {
+    const uint4 q = *reinterpret_cast<const uint4*>(b + stg_off<RB>(lane, k));
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      v[8 * k + 2 * h] = bf16lo(w[h]);
+      v[8 * k + 2 * h + 1] = bf16hi(w[h]);
+    }
+  }
+}
+
+// One warp's share of a tile (rows row0 + [0, 32), half `half` of the
+// columns). Waits for the accumulator itself (after starting the first input
+// load); returns false if a bounded wait timed out. ucnt counts the warp's
+// units over all its tiles (unit i uses buffer i & 1), eph holds the phase
+// bit of each buffer's input barrier.
 template <int EPI, int BN, uint32_t STG>
-__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const OutMaps& om,
+__device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const OutMaps& om,
                                               uint32_t tbase, int row0, int nt, int half,
-                                              const Stage& st) {
+                                              const Stage& st, uint32_t& ucnt, uint32_t& eph,
+                                              uint32_t tfull, uint32_t tfull_ph) {
+  constexpr int UNIT = epi_unit(EPI, STG);
+  constexpr uint32_t BUF = STG / 2;
+  constexpr uint32_t RB = UNIT * epi_elem_bytes(EPI);
+  constexpr uint32_t BLK = 32 * RB;
+  constexpr bool LOADS = EPI == EPI_F32_RESID || EPI == EPI_SWIGLU_BWD;
+  constexpr int CPW = EPI == EPI_SWIGLU ? 64 : BN / 2;  // columns per warp
+  constexpr int NCH = CPW / 32;                          // 32-column TMEM chunks
+  constexpr int UPC = 32 / UNIT;                         // units per chunk
+  constexpr int NU = NCH * UPC;
+  static_assert((EPI != EPI_SWIGLU && EPI != EPI_CE) || (BN == 256 && STG >= 4096),
+                "SwiGLU and CE tiles are 256 wide");
+  static_assert(BLK * (EPI == EPI_SWIGLU ? 1 : EPI == EPI_SWIGLU_BWD ? 2 : 1) <= BUF,
+                "unit does not fit its staging buffer");
   const Epi& e = p.epi;
   const int lane = st.lane;
   const int row = row0 + lane;
   const bool row_ok = row < p.M;
+  const int ncols = EPI == EPI_SWIGLU ? e.half : p.N;
+  const int col_w = EPI == EPI_SWIGLU ? nt * 128 + half * 64 : nt * BN + half * (BN / 2);
+  const uint32_t tcol_w = EPI == EPI_SWIGLU ? half * 64 : half * (BN / 2);
+
+  auto issue_load = [&](int col, uint32_t bi) {
+    if (lane != 0) return;
+    const uint32_t b = st.bar + 8 * bi;
+    const uint32_t dst = st.a + bi * BUF;
+    if constexpr (EPI == EPI_F32_RESID) {
+      mbar_arrive_expect_tx(b, BLK);
+      tma_load_2d(dst, &om.i1, b, col, row0);
+    } else if constexpr (EPI == EPI_SWIGLU_BWD) {
+      mbar_arrive_expect_tx(b, 2 * BLK);
+      tma_load_2d(dst, &om.i1, b, col, row0);
+      tma_load_2d(dst + BLK, &om.i2, b, col, row0);
+    }
+  };
+  if constexpr (LOADS) {
+    if (lane == 0) bulk_wait_read0();  // both buffers free
+    __syncwarp();
+    if (col_w < ncols) issue_load(col_w, ucnt & 1);
+  }
+  if (!warp_wait(tfull, tfull_ph, p.err)) {
+    if constexpr (LOADS) {
+      // do not leave the copy into this warp's buffer in flight
+      if (col_w < ncols) {
+        mbar_wait(st.bar + 8 * (ucnt & 1), (eph >> (ucnt & 1)) & 1u, nullptr);
+        eph ^= 1u << (ucnt & 1);
+        ++ucnt;
+      }
+    }
+    return false;
+  }
+  tc_fence_after();
+
   uint32_t r[32];
-  float v[32];
-  const int c_lo = half * (BN / 64);  // this warp's 32-column chunks [c_lo, c_lo + BN/64)
-  if constexpr (EPI == EPI_BF16 || EPI == EPI_F32 || EPI == EPI_F32_RESID) {
+  uint32_t r2[EPI == EPI_SWIGLU ? 32 : 1];
+  float mx = -INFINITY, sum = 0.f;
+  const int tgt = (EPI == EPI_CE && row_ok) ? e.targets[row] : -1;
 #pragma unroll 1
-    for (int c = c_lo; c < c_lo + BN / 64; ++c) {
-      const int col0 = nt * BN + c * 32;
-      if (col0 >= p.N) break;
-      tmem_ld32(tbase + c * 32, r);
-      tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-      if constexpr (EPI == EPI_F32_RESID) {
-        if (row_ok) {
-          const float* res = e.resid + (int64_t)row * e.ld_resid + col0;
-          if (col0 + 32 <= p.N) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float4 q = reinterpret_cast<const float4*>(res)[j];
-              v[4 * j] += q.x;
-              v[4 * j + 1] += q.y;
-              v[4 * j + 2] += q.z;
-              v[4 * j + 3] += q.w;
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (col0 + j < p.N) v[j] += res[j];
-          }
-        }
-      }
-      if (col0 + 32 > p.N && (p.N & (EPI == EPI_BF16 ? 7 : 3))) {
-        // a bulk store's bounds check works in 16-byte units, so a last chunk
-        // whose row end is not 16-byte aligned is written with plain stores
-        if (row_ok) {
-          if constexpr (EPI == EPI_BF16) {
-            bf16* out = reinterpret_cast<bf16*>(e.out) + (int64_t)row * e.ld_out + col0;
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (col0 + j < p.N) out[j] = __float2bfloat16_rn(v[j]);
-          } else {
-            float* out = reinterpret_cast<float*>(e.out) + (int64_t)row * e.ld_out + col0;
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (col0 + j < p.N) out[j] = v[j];
-          }
-        }
-        continue;
-      }
-      st.wait_free();
-      if constexpr (EPI == EPI_BF16) {
-        uint32_t w[16];
-        pack_row_bf16(v, w);
-        st.put_bf16(0, w);
-      } else if constexpr (STG >= 4096) {
-        st.put_f32(0, v);
-      } else {
-        st.put_f32_half(0, v, 0);
-        st.flush();
-        st.store(&om.o1, 0, col0, row0);
-        st.commit();
-        st.wait_free();
-        st.put_f32_half(0, v, 1);
-        st.flush();
-        st.store(&om.o1, 0, col0 + 16, row0);
-        st.commit();
-        continue;
-      }
-      st.flush();
-      st.store(&om.o1, 0, col0, row0);
-      st.commit();
-    }
-  } else if constexpr (EPI == EPI_SWIGLU) {
-    static_assert(BN == 256 && STG >= 4096, "SwiGLU tiles are 256 wide");
-    // accumulator columns [0,128) = gate, [128,256) = up for I-columns nt*128 + [0,128)
-    uint32_t u[32];
-#pragma unroll 1
-    for (int c = 2 * half; c < 2 * half + 2; ++c) {
-      const int col0 = nt * 128 + c * 32;
-      if (col0 >= e.half) break;
-      tmem_ld32(tbase + c * 32, r);
-      tmem_ld32(tbase + 128 + c * 32, u);
-      tmem_ld_wait();
-      uint32_t wg[16], wu[16], ws[16];
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float g0 = __uint_as_float(r[2 * k]), g1 = __uint_as_float(r[2 * k + 1]);
-        const float u0 = __uint_as_float(u[2 * k]), u1 = __uint_as_float(u[2 * k + 1]);
-        wg[k] = pack_bf16x2(g0, g1);
-        wu[k] = pack_bf16x2(u0, u1);
-        ws[k] = pack_bf16x2(silu_f(g0) * u0, silu_f(g1) * u1);
-      }
-      st.wait_free();
-      st.put_bf16(0, wg);
-      st.put_bf16(2048, wu);
-      st.flush();
-      st.store(&om.o1, 0, col0, row0);
-      st.store(&om.o2, 2048, col0, row0);
-      st.commit();
-      st.wait_free();
-      st.put_bf16(0, ws);
-      st.flush();
-      st.store(&om.o3, 0, col0, row0);
-      st.commit();
-    }
-  } else if constexpr (EPI == EPI_SWIGLU_BWD) {
-    // g and u of the next chunk are loaded while the current one is computed
-    uint4 vg[2][4], vu[2][4];
-    auto load_aux = [&](int c, int slot) {
-      const int col0 = nt * BN + c * 32;
-      if (!row_ok || col0 >= p.N) return;
-      const bf16* gp = e.aux + (int64_t)row * e.ld_aux + col0;
-      const bf16* up = gp + e.half;
-      if (col0 + 32 <= p.N) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          vg[slot][j] = reinterpret_cast<const uint4*>(gp)[j];
-          vu[slot][j] = reinterpret_cast<const uint4*>(up)[j];
-        }
-      } else {
-        uint16_t* pg = reinterpret_cast<uint16_t*>(&vg[slot][0]);
-        uint16_t* pu = reinterpret_cast<uint16_t*>(&vu[slot][0]);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          pg[j] = (col0 + j < p.N) ? reinterpret_cast<const uint16_t*>(gp)[j] : 0;
-          pu[j] = (col0 + j < p.N) ? reinterpret_cast<const uint16_t*>(up)[j] : 0;
-        }
-      }
-    };
-    load_aux(c_lo, 0);
-#pragma unroll
-    for (int ci = 0; ci < BN / 64; ++ci) {
-      const int c = c_lo + ci;
-      const int col0 = nt * BN + c * 32;
-      if (col0 >= p.N) break;
-      tmem_ld32(tbase + c * 32, r);
-      if (ci + 1 < BN / 64) load_aux(c + 1, (ci + 1) & 1);
-      tmem_ld_wait();
-      uint32_t wdg[16], wdu[16];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t* pg = &vg[ci & 1][j].x;
-        const uint32_t* pu = &vu[ci & 1][j].x;
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          float dgv[2], duv[2];
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const float g = q ? bf16hi(pg[h]) : bf16lo(pg[h]);
-            const float uu = q ? bf16hi(pu[h]) : bf16lo(pu[h]);
-            const float ds = __uint_as_float(r[8 * j + 2 * h + q]);
-            const float sg = 1.0f / (1.0f + __expf(-g));
-            dgv[q] = ds * uu * sg * (1.0f + g * (1.0f - sg));
-            duv[q] = ds * g * sg;
-          }
-          wdg[4 * j + h] = pack_bf16x2(dgv[0], dgv[1]);
-          wdu[4 * j + h] = pack_bf16x2(duv[0], duv[1]);
-        }
-      }
-      st.wait_free();
-      st.put_bf16(0, wdg);
-      if constexpr (STG >= 4096) {
-        st.put_bf16(2048, wdu);
-        st.flush();
-        st.store(&om.o1, 0, col0, row0);
-        st.store(&om.o2, 2048, col0, row0);
-        st.commit();
-      } else {
-        st.flush();
-        st.store(&om.o1, 0, col0, row0);
-        st.commit();
-        st.wait_free();
-        st.put_bf16(0, wdu);
-        st.flush();
-        st.store(&om.o2, 0, col0, row0);
-        st.commit();
-      }
-    }
-  } else if constexpr (EPI == EPI_CE) {
-    static_assert(BN == 256, "CE tiles are 256 wide");
-    float mx = -INFINITY, sum = 0.f;
-    const int tgt = row_ok ? e.targets[row] : -1;
-#pragma unroll 1
-    for (int c = c_lo; c < c_lo + BN / 64; ++c) {
-      const int col0 = nt * BN + c * 32;
-      if (col0 >= p.N) break;
-      tmem_ld32(tbase + c * 32, r);
-      tmem_ld_wait();
-      const int nvalid = min(32, p.N - col0);
+  for (int c = 0; c < NCH; ++c) {
+    const int ccol = col_w + c * 32;
+    if (ccol >= ncols) break;
+    tmem_ld32(tbase + tcol_w + c * 32, r);
+    if constexpr (EPI == EPI_SWIGLU) tmem_ld32(tbase + 128 + tcol_w + c * 32, r2);
+    tmem_ld_wait();
+    if constexpr (EPI == EPI_CE) {
+      const int nvalid = min(32, p.N - ccol);
       float cm = -INFINITY;
 #pragma unroll
       for (int j = 0; j < 32; ++j)
@@ -356,23 +254,140 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const OutMaps
         if (j < nvalid) acc += __expf(__uint_as_float(r[j]) - nm);
       mx = nm;
       sum = acc;
-      if (row_ok && tgt >= col0 && tgt < col0 + nvalid) {
+      if (row_ok && tgt >= ccol && tgt < ccol + nvalid) {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          if (j == tgt - col0) e.tgt_logit[row] = __uint_as_float(r[j]);
+          if (j == tgt - ccol) e.tgt_logit[row] = __uint_as_float(r[j]);
       }
-      uint32_t w[16];
-#pragma unroll
-      for (int k = 0; k < 16; ++k)
-        w[k] = pack_bf16x2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
-      st.wait_free();
-      st.put_bf16(0, w);
-      st.flush();
-      st.store(&om.o1, 0, col0, row0);
-      st.commit();
     }
+#pragma unroll
+    for (int j = 0; j < UPC; ++j) {
+      const int u = c * UPC + j;
+      const int col = ccol + j * UNIT;
+      if (col >= ncols) break;
+      const uint32_t bi = ucnt & 1;
+      uint8_t* buf = st.p + bi * BUF;
+      const uint32_t bufa = st.a + bi * BUF;
+      float v[UNIT];
+#pragma unroll
+      for (int k = 0; k < UNIT; ++k) v[k] = __uint_as_float(r[j * UNIT + k]);
+      ++ucnt;
+      if constexpr (LOADS) {
+        const bool next = u + 1 < NU && col + UNIT < ncols;
+        if (next) {
+          // the other buffer's last store (the previous unit's) has been read: refill it
+          if (lane == 0) bulk_wait_read0();
+          __syncwarp();
+          issue_load(col + UNIT, bi ^ 1u);
+        }
+        if (!warp_wait(st.bar + 8 * bi, (eph >> bi) & 1u, p.err)) {
+          // do not leave copies into this warp's buffers in flight
+          mbar_wait(st.bar + 8 * bi, (eph >> bi) & 1u, nullptr);
+          if (next) mbar_wait(st.bar + 8 * (bi ^ 1u), (eph >> (bi ^ 1u)) & 1u, nullptr);
+          return false;
+        }
+        eph ^= 1u << bi;
+      } else {
+        // this buffer's last store (unit u - 2) has been read
+        if (lane == 0) bulk_wait_read1();
+        __syncwarp();
+      }
+      if constexpr (EPI == EPI_F32 || EPI == EPI_F32_RESID || EPI == EPI_BF16 || EPI == EPI_CE) {
+        if (col + UNIT > ncols && (ncols & (EPI == EPI_F32 || EPI == EPI_F32_RESID ? 3 : 7))) {
+          // a bulk store's bounds check works in 16-byte units, so a last unit
+          // whose row end is not 16-byte aligned is written with plain stores
+          if constexpr (EPI == EPI_F32_RESID) {
+            if (row_ok) {
+              const float* res = e.resid + (int64_t)row * e.ld_resid + col;
+#pragma unroll
+              for (int k = 0; k < UNIT; ++k)
+                if (col + k < ncols) v[k] += res[k];
+            }
+          }
+          if (row_ok) {
+#pragma unroll
+            for (int k = 0; k < UNIT; ++k) {
+              if (col + k >= ncols) continue;
+              if constexpr (EPI == EPI_F32 || EPI == EPI_F32_RESID)
+                reinterpret_cast<float*>(e.out)[(int64_t)row * e.ld_out + col + k] = v[k];
+              else
+                reinterpret_cast<bf16*>(e.out)[(int64_t)row * e.ld_out + col + k] =
+                    __float2bfloat16_rn(v[k]);
+            }
+          }
+          continue;
+        }
+        if constexpr (EPI == EPI_F32_RESID) {
+          float q[UNIT];
+          get_f32<RB, UNIT>(buf, lane, q);
+#pragma unroll
+          for (int k = 0; k < UNIT; ++k) v[k] += q[k];
+        }
+        if constexpr (EPI == EPI_F32 || EPI == EPI_F32_RESID) put_f32<RB, UNIT>(buf, lane, v);
+        else put_bf16<RB, UNIT>(buf, lane, v);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&om.o1, bufa, col, row0);
+          bulk_commit();
+        }
+      } else if constexpr (EPI == EPI_SWIGLU) {
+        // three 2 KB outputs per 32-column unit: g and u fill the warp's whole
+        // 4 KB staging, then s (fewer, larger bulk stores than double buffering
+        // narrower units)
+        float uu[UNIT], sv[UNIT];
+#pragma unroll
+        for (int k = 0; k < UNIT; ++k) {
+          uu[k] = __uint_as_float(r2[j * UNIT + k]);
+          sv[k] = silu_f(v[k]) * uu[k];
+        }
+        if (lane == 0) bulk_wait_read0();
+        __syncwarp();
+        put_bf16<RB, UNIT>(st.p, lane, v);
+        put_bf16<RB, UNIT>(st.p + BLK, lane, uu);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&om.o1, st.a, col, row0);
+          tma_store_2d(&om.o2, st.a + BLK, col, row0);
+          bulk_commit();
+          bulk_wait_read0();
+        }
+        __syncwarp();
+        put_bf16<RB, UNIT>(st.p, lane, sv);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&om.o3, st.a, col, row0);
+          bulk_commit();
+        }
+      } else if constexpr (EPI == EPI_SWIGLU_BWD) {
+        // ds (accumulator) with the saved g, u -> dg = ds u silu'(g), du = ds silu(g)
+        float g[UNIT], uu[UNIT], dg[UNIT], du[UNIT];
+        get_bf16<RB, UNIT>(buf, lane, g);
+        get_bf16<RB, UNIT>(buf + BLK, lane, uu);
+#pragma unroll
+        for (int k = 0; k < UNIT; ++k) {
+          const float sg = 1.0f / (1.0f + __expf(-g[k]));
+          dg[k] = v[k] * uu[k] * sg * (1.0f + g[k] * (1.0f - sg));
+          du[k] = v[k] * g[k] * sg;
+        }
+        put_bf16<RB, UNIT>(buf, lane, dg);
+        put_bf16<RB, UNIT>(buf + BLK, lane, du);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&om.o1, bufa, col, row0);
+          tma_store_2d(&om.o2, bufa + BLK, col, row0);
+          bulk_commit();
+        }
+      }
+    }
+  }
+  if constexpr (EPI == EPI_CE) {
     if (row_ok) e.part[(int64_t)row * e.part_ld + 2 * nt + half] = make_float2(mx, sum);
   }
+  return true;
 }
 
 // ----------------------------------------------------------------- kernel
@@ -388,13 +403,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tile<BN>::OFF_OUT + OS::TOTAL);
-  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, epilogue inputs[8][2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 21);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * STAGES;
   const uint32_t tfull0 = empty0 + 8 * STAGES;
   const uint32_t tempty0 = tfull0 + 16;
   const uint32_t drain = tempty0 + 16;
+  const uint32_t ebar0 = drain + 8;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -409,6 +425,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       mbar_init(tempty0 + 8 * a, EPI_THREADS / 32);  // one arrival per epilogue warp
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < 16; ++i) mbar_init(ebar0 + 8 * i, 1);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -532,16 +549,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int q = warp & 3;             // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;   // which half of the tile's columns
     uint8_t* stg = smem + Tile<BN>::OFF_OUT + (warp - 2) * OS::BYTES;
-    const Stage st{stg, smem_u32(stg), lane};
+    const Stage st{stg, smem_u32(stg), ebar0 + 16 * (warp - 2), lane};
+    uint32_t ucnt = 0, eph = 0;
     int acc = 0;
     uint32_t acc_ph = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       int mt, nt;
       tile_coords(t, p, mt, nt);
-      if (!warp_wait(tfull0 + 8 * acc, acc_ph, p.err)) break;
-      tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      epilogue_tile<EPI, BN, OS::BYTES>(p, om, tbase, mt * BM + q * 32, nt, half, st);
+      if (!epilogue_tile<EPI, BN, OS::BYTES>(p, om, tbase, mt * BM + q * 32, nt, half, st, ucnt,
+                                             eph, tfull0 + 8 * acc, acc_ph))
+        break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
@@ -581,7 +599,7 @@ struct Tile2 {
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB
   static constexpr int STAGES = 6;
   static constexpr uint32_t OFF_OUT = STAGES * STAGE_BYTES;
-  static constexpr size_t SMEM = OFF_OUT + OutStage<BN, true>::TOTAL + 1024 + 256;
+  static constexpr size_t SMEM = OFF_OUT + OutStage<BN, true>::TOTAL + 1024 + 512;
 };
 
 template <int A_MN, int B_MN, int EPI, int BN>
@@ -598,13 +616,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   using OS = OutStage<BN, true>;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + TL::OFF_OUT + OS::TOTAL);
-  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, epilogue inputs[8][2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 21);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * STAGES;
   const uint32_t tfull0 = empty0 + 8 * STAGES;
   const uint32_t tempty0 = tfull0 + 16;
   const uint32_t drain = tempty0 + 16;
+  const uint32_t ebar0 = drain + 8;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -622,6 +641,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       mbar_init(tempty0 + 8 * a, 2 * (EPI_THREADS / 32));  // one arrival per epilogue warp
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < 16; ++i) mbar_init(ebar0 + 8 * i, 1);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -736,17 +756,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
     uint8_t* stg = smem + TL::OFF_OUT + (warp - 2) * OS::BYTES;
-    const Stage st{stg, smem_u32(stg), lane};
+    const Stage st{stg, smem_u32(stg), ebar0 + 16 * (warp - 2), lane};
+    uint32_t ucnt = 0, eph = 0;
     int acc = 0;
     uint32_t acc_ph = 0;
     for (int t = pair; t < ntiles; t += npairs) {
       int mt, nt;
       tile_coords(t, p, mt, nt);
-      if (!warp_wait(tfull0 + 8 * acc, acc_ph, p.err)) break;
-      tc_fence_after();
       const int mrow = 2 * mt + static_cast<int>(rank);
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      epilogue_tile<EPI, BN, OS::BYTES>(p, om, tbase, mrow * BM + q * 32, nt, half, st);
+      if (!epilogue_tile<EPI, BN, OS::BYTES>(p, om, tbase, mrow * BM + q * 32, nt, half, st,
+                                             ucnt, eph, tfull0 + 8 * acc, acc_ph))
+        break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty_even + 8 * acc);
@@ -817,45 +838,53 @@ static bool make_map(CUtensorMap* m, const Mat& x, int box_rows) {
   return make_tma_2d(m, x.ptr, x.rows, x.cols, x.ld, box_rows);
 }
 
-// Store map of an output matrix [rows, cols] with row stride ld elements:
-// 32 x 32 boxes, fp32 with 128-byte or bf16 with 64-byte swizzle (the layouts
-// Stage::put_f32 / put_bf16 write).
-static bool make_out_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld,
-                         bool f32, bool narrow = false) {
+// Map of an epilogue operand [rows, cols] (row stride ld elements, fp32 or
+// bf16) with 32-row boxes of `unit` columns and the swizzle that matches the
+// box's row bytes (128/64/32 B; none for 16 B), as stg_off lays them out.
+static bool make_box_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld,
+                         bool f32, int unit) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const int es = f32 ? 4 : 2;
   if ((reinterpret_cast<uintptr_t>(ptr) & 15) || (ld * es) % 16) return false;
+  const int rb = unit * es;
+  const CUtensorMapSwizzle sw = rb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : rb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                : rb == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                           : CU_TENSOR_MAP_SWIZZLE_NONE;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * es};
-  // box: 32 rows of 32 elements, or of 16 fp32 (64-byte rows) when narrow
-  cuuint32_t box[2] = {(f32 && narrow) ? 16u : 32u, 32u};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(unit), 32u};
   cuuint32_t estr[2] = {1u, 1u};
   return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-             const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             (f32 && !narrow) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+             const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The output maps an epilogue stores through (see OutMaps); narrow: fp32
-// blocks are staged as 32 x 16 (OutStage of 2 KB).
-static bool make_out_maps(OutMaps* om, const Epi& e, int M, int N, bool narrow) {
+// The maps an epilogue stores through and loads from (see OutMaps), for
+// staging buffers of `stg` bytes per warp.
+static bool make_out_maps(OutMaps* om, const Epi& e, int M, int N, uint32_t stg) {
   memset(om, 0, sizeof(*om));
+  const int u = epi_unit(e.kind, stg);
   bf16* out = static_cast<bf16*>(e.out);
   switch (e.kind) {
     case EPI_F32:
+      return make_box_map(&om->o1, e.out, M, N, e.ld_out, true, u);
     case EPI_F32_RESID:
-      return make_out_map(&om->o1, e.out, M, N, e.ld_out, true, narrow);
+      return make_box_map(&om->o1, e.out, M, N, e.ld_out, true, u) &&
+             make_box_map(&om->i1, e.resid, M, N, e.ld_resid, true, u);
     case EPI_BF16:
     case EPI_CE:
-      return make_out_map(&om->o1, e.out, M, N, e.ld_out, false);
+      return make_box_map(&om->o1, e.out, M, N, e.ld_out, false, u);
     case EPI_SWIGLU:
-      return make_out_map(&om->o1, out, M, e.half, e.ld_out, false) &&
-             make_out_map(&om->o2, out + e.half, M, e.half, e.ld_out, false) &&
-             make_out_map(&om->o3, e.out2, M, e.half, e.ld_out2, false);
+      return make_box_map(&om->o1, out, M, e.half, e.ld_out, false, u) &&
+             make_box_map(&om->o2, out + e.half, M, e.half, e.ld_out, false, u) &&
+             make_box_map(&om->o3, e.out2, M, e.half, e.ld_out2, false, u);
     case EPI_SWIGLU_BWD:
-      return make_out_map(&om->o1, out, M, N, e.ld_out, false) &&
-             make_out_map(&om->o2, out + e.half, M, N, e.ld_out, false);
+      return make_box_map(&om->o1, out, M, N, e.ld_out, false, u) &&
+             make_box_map(&om->o2, out + e.half, M, N, e.ld_out, false, u) &&
+             make_box_map(&om->i1, e.aux, M, N, e.ld_aux, false, u) &&
+             make_box_map(&om->i2, e.aux + e.half, M, N, e.ld_aux, false, u);
     default:
       return false;
   }
@@ -1009,7 +1038,7 @@ cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N,
     return cudaErrorInvalidValue;
   }
   OutMaps om;
-  if (!make_out_maps(&om, epi, M, N, !pair_tiles && bn == 192)) {
+  if (!make_out_maps(&om, epi, M, N, (!pair_tiles && bn == 192) ? 2048u : 4096u)) {
     *why = "gemm: outputs need 16-byte aligned rows (cuTensorMapEncodeTiled failed)";
     return cudaErrorInvalidValue;
   }
