@@ -344,6 +344,7 @@ def run_probe(args):
     gen = torch.Generator(device=dev)
     gen.manual_seed(7)
     T = shape.tokens
+    sq = torch.zeros(1, dtype=torch.float64, device=dev)
     if args.kernel == "block":
         n = rdt.block_param_count(cfg)
         w = torch.empty(n, device=dev)
@@ -365,7 +366,8 @@ def run_probe(args):
 
         def run():
             rdt.block_forward(cfg, shape.batch, shape.seq, w, wb, x, y, saved, ws)
-            rdt.block_backward(cfg, shape.batch, shape.seq, w, wb, x, saved, dy, dx, grads, ws)
+            rdt.block_backward(cfg, shape.batch, shape.seq, w, wb, x, saved, dy, dx, grads, ws,
+                               grad_sq=sq)
         s1 = shape.replace(layers=1, vocab=0)
         flops = algorithmic_flops(s1)
         what = "one block forward+backward"
@@ -381,7 +383,8 @@ def run_probe(args):
         dwl = torch.empty(shape.vocab, shape.hidden, device=dev)
 
         def run():
-            rdt.fused_cross_entropy(cfg, T, h, gf, wl, tg, 1.0 / T, loss, dh, dgf, dwl, ws)
+            rdt.fused_cross_entropy(cfg, T, h, gf, wl, tg, 1.0 / T, loss, dh, dgf, dwl, ws,
+                                    grad_sq=sq)
         flops = 6.0 * shape.vocab * shape.hidden * T
         what = "final RMSNorm + LM head + cross-entropy, forward+backward"
     for _ in range(args.warmup):

@@ -133,11 +133,16 @@ rdt_status rdt_block_forward(const rdt_config* cfg, int32_t batch, int32_t seq,
  * dy     upstream gradient fp32 [T, H]
  * dx     gradient w.r.t. x, fp32 [T, H] (overwritten; may alias dy)
  * grads  fp32 flat array in the block layout, every tensor overwritten
+ * grad_sq  optional (may be null) fp64 device scalar: *grad_sq += the sum of
+ *          the squares of every gradient this call writes (the global-norm
+ *          clip's squared sum, accumulated by the weight-gradient GEMMs'
+ *          epilogues and the gain reductions as they produce the values;
+ *          fixed summation order, so the same inputs give the same bits)
  * ------------------------------------------------------------------------- */
 rdt_status rdt_block_backward(const rdt_config* cfg, int32_t batch, int32_t seq,
                               const float* w, const rdt_bf16* w_bf16,
                               const float* x, const void* saved, size_t saved_bytes,
-                              const float* dy, float* dx, float* grads,
+                              const float* dy, float* dx, float* grads, double* grad_sq,
                               void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
@@ -156,12 +161,16 @@ rdt_status rdt_block_backward(const rdt_config* cfg, int32_t batch, int32_t seq,
  *          the device: the caller validates ids before upload)
  * loss_scale  normally 1/tokens (loss = mean NLL)
  * dh fp32 [tokens, H]; dgamma_f fp32 [H]; dw_lm fp32 [V, H] (all overwritten)
+ * grad_sq  optional (may be null) fp64 device scalar: *grad_sq = the sum of
+ *          the squares of dgamma_f and dw_lm (a step's backward starts here,
+ *          so this call starts the clip's squared sum that each
+ *          rdt_block_backward then adds to)
  * ------------------------------------------------------------------------- */
 rdt_status rdt_fused_cross_entropy(const rdt_config* cfg, int32_t tokens,
                                    const float* h, const float* gamma_f,
                                    const rdt_bf16* w_lm, const int32_t* targets,
                                    float loss_scale, float* loss_partials,
-                                   float* dh, float* dgamma_f, float* dw_lm,
+                                   float* dh, float* dgamma_f, float* dw_lm, double* grad_sq,
                                    void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------

@@ -158,6 +158,7 @@ struct BlockWs {
   float* cs;
   bf16 *dy_b, *dgu, *dr1_b, *dout, *dqkv;
   float *dxn, *dr1, *Dd, *lse2, *dq, *dk, *partials;
+  double* sqp;  // squared-sum slots of the weight-gradient GEMMs
 };
 size_t carve_block_ws(const Dims& m, int64_t B, int64_t S, void* base, BlockWs* w) {
   const int64_t T = B * S;
@@ -177,6 +178,10 @@ size_t carve_block_ws(const Dims& m, int64_t B, int64_t S, void* base, BlockWs* 
   t.dk = c.take<float>(T * m.kd);
   const int64_t pw = m.H > 2 * m.d ? m.H : 2 * m.d;
   t.partials = c.take<float>(kMaxPartialRows * pw);
+  t.sqp = c.take<double>(gemm_sq_slots_bound((int)m.H, (int)m.I) +
+                         gemm_sq_slots_bound((int)(2 * m.I), (int)m.H) +
+                         gemm_sq_slots_bound((int)m.H, (int)m.qd) +
+                         gemm_sq_slots_bound((int)m.nqkv, (int)m.H));
   if (w) *w = t;
   return c.off;
 }
@@ -185,6 +190,7 @@ struct HeadWs {
   bf16 *hn, *z;
   float *rstd, *tgt, *lse, *dhn, *partials;
   float2* part;
+  double* sqp;  // squared-sum slots of the dW_lm GEMM
 };
 size_t carve_head_ws(const Dims& m, int64_t T, void* base, HeadWs* w) {
   Carver c(base);
@@ -197,6 +203,7 @@ size_t carve_head_ws(const Dims& m, int64_t T, void* base, HeadWs* w) {
   t.lse = c.take<float>(T);
   t.dhn = c.take<float>(T * m.H);
   t.partials = c.take<float>(kMaxPartialRows * m.H);
+  t.sqp = c.take<double>(gemm_sq_slots_bound((int)m.V, (int)m.H));
   if (w) *w = t;
   return c.off;
 }
@@ -411,7 +418,7 @@ rdt_status rdt_block_forward(const rdt_config* cfg, int32_t batch, int32_t seq, 
 rdt_status rdt_block_backward(const rdt_config* cfg, int32_t batch, int32_t seq, const float* w,
                               const rdt_bf16* w_bf16, const float* x, const void* saved,
                               size_t saved_bytes, const float* dy, float* dx, float* grads,
-                              void* ws, size_t ws_bytes, void* stream) {
+                              double* grad_sq, void* ws, size_t ws_bytes, void* stream) {
   std::string why;
   if (!cfg_ok(cfg, &why)) return fail(RDT_EINVAL, "config: %s", why.c_str());
   if (batch < 1 || seq < 1) return fail(RDT_EINVAL, "batch and seq must be >= 1");
@@ -451,14 +458,23 @@ rdt_status rdt_block_backward(const rdt_config* cfg, int32_t batch, int32_t seq,
     RDT_GEMM(Mat{wk.dy_b, T, m.H, m.H}, false, Mat{wb + off[RDT_WD], m.H, m.I, m.I}, true, T,
              (int)m.I, (int)m.H, e, err, s);
   }
+  // squared sums of the weight gradients, written by their GEMMs' epilogues
+  int64_t sq_n = 0, sq_cnt = 0;
+  auto sq_slots = [&](Epi& e) {
+    if (!grad_sq) return;
+    e.sq_part = wk.sqp + sq_n;
+    e.sq_count = &sq_cnt;
+  };
   // dWd = dy^T s
   {
     Epi e;
     e.kind = EPI_F32;
     e.out = grads + off[RDT_WD];
     e.ld_out = m.I;
+    sq_slots(e);
     RDT_GEMM(Mat{wk.dy_b, T, m.H, m.H}, true, Mat{sv.s, T, m.I, m.I}, true, (int)m.H, (int)m.I, T,
              e, err, s);
+    if (grad_sq) sq_n += sq_cnt;
   }
   // dxn2 = [dg du] [Wg; Wu]
   {
@@ -475,8 +491,10 @@ rdt_status rdt_block_backward(const rdt_config* cfg, int32_t batch, int32_t seq,
     e.kind = EPI_F32;
     e.out = grads + off[RDT_WG];
     e.ld_out = m.H;
+    sq_slots(e);
     RDT_GEMM(Mat{wk.dgu, T, 2 * m.I, 2 * m.I}, true, Mat{sv.xn2, T, m.H, m.H}, true,
              (int)(2 * m.I), (int)m.H, T, e, err, s);
+    if (grad_sq) sq_n += sq_cnt;
   }
   // post-attention RMSNorm backward, identity skip added after it
   RDT_CHECK_CUDA(rmsnorm_bwd(wk.dxn, sv.r1, sv.rstd2, w + off[RDT_G_FFN], dy, wk.dr1, wk.dr1_b,
@@ -496,8 +514,10 @@ rdt_status rdt_block_backward(const rdt_config* cfg, int32_t batch, int32_t seq,
     e.kind = EPI_F32;
     e.out = grads + off[RDT_WO];
     e.ld_out = m.qd;
+    sq_slots(e);
     RDT_GEMM(Mat{wk.dr1_b, T, m.H, m.H}, true, Mat{sv.o, T, m.qd, m.qd}, true, (int)m.H,
              (int)m.qd, T, e, err, s);
+    if (grad_sq) sq_n += sq_cnt;
   }
   // attention backward (GQA reduction inside), dq accumulated in fp32
   if (attn_tc_supported((int)m.d, true)) {
@@ -541,12 +561,21 @@ rdt_status rdt_block_backward(const rdt_config* cfg, int32_t batch, int32_t seq,
     e.kind = EPI_F32;
     e.out = grads + off[RDT_WQ];
     e.ld_out = m.H;
+    sq_slots(e);
     RDT_GEMM(Mat{wk.dqkv, T, m.nqkv, m.nqkv}, true, Mat{sv.xn, T, m.H, m.H}, true, (int)m.nqkv,
              (int)m.H, T, e, err, s);
+    if (grad_sq) sq_n += sq_cnt;
   }
   // input RMSNorm backward + identity skip
   RDT_CHECK_CUDA(rmsnorm_bwd(wk.dxn, x, sv.rstd1, w + off[RDT_G_ATTN], wk.dr1, dx, nullptr,
                              grads + off[RDT_G_ATTN], wk.partials, T, (int)m.H, s));
+  if (grad_sq) {
+    // += the weight-gradient slots and the four gains, in a fixed order
+    const float* gains[4] = {grads + off[RDT_G_ATTN], grads + off[RDT_G_FFN],
+                             grads + off[RDT_G_Q], grads + off[RDT_G_K]};
+    const int64_t lens[4] = {m.H, m.H, m.d, m.d};
+    RDT_CHECK_CUDA(sq_reduce(wk.sqp, sq_n, gains, lens, 4, grad_sq, true, s));
+  }
   return RDT_OK;
 }
 
@@ -554,8 +583,8 @@ rdt_status rdt_block_backward(const rdt_config* cfg, int32_t batch, int32_t seq,
 rdt_status rdt_fused_cross_entropy(const rdt_config* cfg, int32_t tokens, const float* h,
                                    const float* gamma_f, const rdt_bf16* w_lm,
                                    const int32_t* targets, float loss_scale, float* loss_partials,
-                                   float* dh, float* dgamma_f, float* dw_lm, void* ws,
-                                   size_t ws_bytes, void* stream) {
+                                   float* dh, float* dgamma_f, float* dw_lm, double* grad_sq,
+                                   void* ws, size_t ws_bytes, void* stream) {
   std::string why;
   if (!cfg_ok(cfg, &why)) return fail(RDT_EINVAL, "config: %s", why.c_str());
   if (tokens < 1) return fail(RDT_EINVAL, "tokens must be >= 1");
@@ -601,16 +630,27 @@ rdt_status rdt_fused_cross_entropy(const rdt_config* cfg, int32_t tokens, const 
              e, err, s);
   }
   // dW_lm = dz^T hn
+  int64_t sq_n = 0;
   {
     Epi e;
     e.kind = EPI_F32;
     e.out = dw_lm;
     e.ld_out = m.H;
+    if (grad_sq) {
+      e.sq_part = wk.sqp;
+      e.sq_count = &sq_n;
+    }
     RDT_GEMM(Mat{wk.z, T, m.V, m.V}, true, Mat{wk.hn, T, m.H, m.H}, true, (int)m.V, (int)m.H, T, e,
              err, s);
   }
   RDT_CHECK_CUDA(rmsnorm_bwd(wk.dhn, h, wk.rstd, gamma_f, nullptr, dh, nullptr, dgamma_f,
                              wk.partials, T, (int)m.H, s));
+  if (grad_sq) {
+    // = the dW_lm slots and the final gain's squares (the first gradients of a step)
+    const float* gains[1] = {dgamma_f};
+    const int64_t lens[1] = {m.H};
+    RDT_CHECK_CUDA(sq_reduce(wk.sqp, sq_n, gains, lens, 1, grad_sq, false, s));
+  }
   return RDT_OK;
 }
 

@@ -450,6 +450,55 @@ cudaError_t qknorm_rope_bwd(const float* dq, const float* dk, const float* qkv, 
   return reduce_cols(partials, P, 2 * d, dg_qk, s);
 }
 
+// ----------------------------------------------------- fused squared sums
+// One CTA: fixed per-thread strides and a fixed tree, so the result is the
+// same bits on every run.
+struct SmallBufs {
+  const float* p[4];
+  int64_t n[4];
+};
+__global__ void __launch_bounds__(1024) sq_reduce_kernel(const double* __restrict__ parts,
+                                                         int64_t n, const SmallBufs sb, int nsmall,
+                                                         double* out, int accumulate) {
+  __shared__ double red[1024];
+  double acc = 0.0;
+  // eight independent loads in flight per thread, then the remainder
+  int64_t i = threadIdx.x;
+  for (; i + 7 * 1024 < n; i += 8 * 1024) {
+    double a[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) a[k] = parts[i + k * 1024];
+    acc += ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+  }
+  for (; i < n; i += 1024) acc += parts[i];
+  for (int b = 0; b < nsmall; ++b)
+    for (int64_t i = threadIdx.x; i < sb.n[b]; i += blockDim.x) {
+      const double v = sb.p[b][i];
+      acc += v * v;
+    }
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int h = 512; h > 0; h >>= 1) {
+    if (static_cast<int>(threadIdx.x) < h) red[threadIdx.x] += red[threadIdx.x + h];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *out = (accumulate ? *out : 0.0) + red[0];
+}
+
+cudaError_t sq_reduce(const double* parts, int64_t n, const float* const* small,
+                      const int64_t* small_len, int nsmall, double* out, bool accumulate,
+                      cudaStream_t s) {
+  if (nsmall < 0 || nsmall > 4) return cudaErrorInvalidValue;
+  SmallBufs sb = {};
+  for (int i = 0; i < nsmall; ++i) {
+    sb.p[i] = small[i];
+    sb.n[i] = small_len[i];
+  }
+  note_launch();
+  sq_reduce_kernel<<<1, 1024, 0, s>>>(parts, n, sb, nsmall, out, accumulate ? 1 : 0);
+  return cudaGetLastError();
+}
+
 // --------------------------------------------------------------------- cast
 __global__ void cast_bf16_kernel(const float4* __restrict__ src, uint2* __restrict__ dst,
                                  int64_t n4) {

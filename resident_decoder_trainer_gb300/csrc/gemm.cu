@@ -61,6 +61,7 @@ struct GemmParams {
   int m_tiles, n_tiles, k_blocks;
   int swiglu_half;  // SwiGLU: row offset of the up rows in the stacked [2I, K] B
   int group;        // rasterisation: row tiles per group (see tile_coords)
+  int sq_slots;     // squared-sum slots per tile (8 single-CTA, 16 pair)
   Epi epi;
   int* err;
 };
@@ -177,7 +178,8 @@ template <int EPI, int BN, uint32_t STG>
 __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const OutMaps& om,
                                               uint32_t tbase, int row0, int nt, int half,
                                               const Stage& st, uint32_t& ucnt, uint32_t& eph,
-                                              uint32_t tfull, uint32_t tfull_ph) {
+                                              uint32_t tfull, uint32_t tfull_ph, int tile,
+                                              int slot) {
   constexpr int UNIT = epi_unit(EPI, STG);
   constexpr uint32_t BUF = STG / 2;
   constexpr uint32_t RB = UNIT * epi_elem_bytes(EPI);
@@ -232,6 +234,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const OutMaps
 
   uint32_t r[32];
   uint32_t r2[EPI == EPI_SWIGLU ? 32 : 1];
+  float sq = 0.f;  // EPI_F32 with sq_part: sum of squares of this warp's values
   float mx = -INFINITY, sum = 0.f;
   const int tgt = (EPI == EPI_CE && row_ok) ? e.targets[row] : -1;
 #pragma unroll 1
@@ -271,6 +274,13 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const OutMaps
       float v[UNIT];
 #pragma unroll
       for (int k = 0; k < UNIT; ++k) v[k] = __uint_as_float(r[j * UNIT + k]);
+      if constexpr (EPI == EPI_F32) {
+        // out-of-range rows and columns hold exact zeros (zero-filled operands)
+        if (e.sq_part) {
+#pragma unroll
+          for (int k = 0; k < UNIT; ++k) sq = fmaf(v[k], v[k], sq);
+        }
+      }
       ++ucnt;
       if constexpr (LOADS) {
         const bool next = u + 1 < NU && col + UNIT < ncols;
@@ -386,6 +396,14 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const OutMaps
   }
   if constexpr (EPI == EPI_CE) {
     if (row_ok) e.part[(int64_t)row * e.part_ld + 2 * nt + half] = make_float2(mx, sum);
+  }
+  if constexpr (EPI == EPI_F32) {
+    if (e.sq_part) {
+      double d = sq;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+      if (lane == 0) e.sq_part[(int64_t)tile * p.sq_slots + slot] = d;
+    }
   }
   return true;
 }
@@ -558,7 +576,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       tile_coords(t, p, mt, nt);
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       if (!epilogue_tile<EPI, BN, OS::BYTES>(p, om, tbase, mt * BM + q * 32, nt, half, st, ucnt,
-                                             eph, tfull0 + 8 * acc, acc_ph))
+                                             eph, tfull0 + 8 * acc, acc_ph, t, warp - 2))
         break;
       tc_fence_before();
       __syncwarp();
@@ -766,7 +784,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const int mrow = 2 * mt + static_cast<int>(rank);
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       if (!epilogue_tile<EPI, BN, OS::BYTES>(p, om, tbase, mrow * BM + q * 32, nt, half, st,
-                                             ucnt, eph, tfull0 + 8 * acc, acc_ph))
+                                             ucnt, eph, tfull0 + 8 * acc, acc_ph, t,
+                                             static_cast<int>(rank) * 8 + (warp - 2)))
         break;
       tc_fence_before();
       __syncwarp();
@@ -985,6 +1004,10 @@ static int raster_group(int m_tiles, int n_tiles, int rows_per_tile, int cols_pe
   return g < 1 ? 1 : (g > m_tiles ? m_tiles : g);
 }
 
+int64_t gemm_sq_slots_bound(int M, int N) {
+  return static_cast<int64_t>((M + BM - 1) / BM) * ((N + 127) / 128) * 16;
+}
+
 cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N, int K,
                  const Epi& epi, int* err, cudaStream_t s, const char** why) {
   if (M <= 0 || N <= 0 || K <= 0) {
@@ -1052,8 +1075,17 @@ cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N,
   p.k_blocks = (K + BK - 1) / BK;
   p.swiglu_half = epi.half;
   p.group = raster_group(p.m_tiles, p.n_tiles, rows_per_tile, swiglu ? 256 : bn, K);
+  p.sq_slots = pair_tiles ? 16 : 8;
   p.epi = epi;
+  p.epi.sq_count = nullptr;
   p.err = err;
+  if (epi.sq_part) {
+    if (epi.kind != EPI_F32 || !epi.sq_count) {
+      *why = "gemm: squared-sum slots need the fp32 epilogue and a count";
+      return cudaErrorInvalidValue;
+    }
+    *epi.sq_count = static_cast<int64_t>(p.m_tiles) * p.n_tiles * p.sq_slots;
+  }
 #define RDT_GEMM_CASE(AM, BMJ, E, W)                                           \
   if (!pair_tiles && a_mn == (AM) && b_mn == (BMJ) && epi.kind == (E) && bn == (W)) \
     return launch<AM, BMJ, E, W>(ta, tb, om, p, s);

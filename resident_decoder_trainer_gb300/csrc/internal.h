@@ -35,7 +35,15 @@ struct Epi {
   int part_ld = 0;
   const int32_t* targets = nullptr;
   float* tgt_logit = nullptr;
+  // EPI_F32 only: when set, every epilogue warp writes the fp64 sum of the
+  // squares of the values it stored, one slot per (tile, warp), and the host
+  // gemm() sets *sq_count to the number of slots written (tiles x 8 or 16).
+  double* sq_part = nullptr;
+  int64_t* sq_count = nullptr;
 };
+
+// Upper bound of the squared-sum slots a gemm() of [M, N] writes.
+int64_t gemm_sq_slots_bound(int M, int N);
 
 // A bf16 row-major matrix in global memory.
 struct Mat {
@@ -101,6 +109,11 @@ cudaError_t qknorm_rope_bwd(const float* dq, const float* dk, const float* qkv, 
                             cudaStream_t s);
 int qknorm_bwd_partial_rows(int T, int heads);
 
+// *out (= or +=, per `accumulate`) the fp64 sum of parts[0, n) plus the sums
+// of squares of up to 4 small fp32 arrays, in a fixed order (one CTA).
+cudaError_t sq_reduce(const double* parts, int64_t n, const float* const* small,
+                      const int64_t* small_len, int nsmall, double* out, bool accumulate,
+                      cudaStream_t s);
 cudaError_t cast_bf16(const float* src, bf16* dst, int64_t n, cudaStream_t s);
 
 cudaError_t ce_finalize(const float2* part, int part_ld, int ntiles, const float* tgt_logit,

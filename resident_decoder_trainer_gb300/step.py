@@ -55,7 +55,6 @@ class DecoderTrainer:
                                     dtype=torch.uint8, device=dev)
         self.head_ws = torch.empty(rdt.head_workspace_bytes(self.cfg, T), dtype=torch.uint8,
                                    device=dev)
-        self.sq_ws = torch.empty(rdt.sq_sum_workspace_bytes(), dtype=torch.uint8, device=dev)
         self.sumsq = torch.zeros(1, dtype=torch.float64, device=dev)
         self.scale = torch.ones(1, **f32)
         self.nonfinite = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -139,18 +138,20 @@ class DecoderTrainer:
                                 self.tensor(self.wb, "head", "w_lm"), self.targets, 1.0 / T,
                                 self.loss_partials, self.dh,
                                 self.tensor(self.g, "head", "g_final"),
-                                self.tensor(self.g, "head", "w_lm"), self.head_ws)
+                                self.tensor(self.g, "head", "w_lm"), self.head_ws,
+                                grad_sq=self.sumsq)
         for li in reversed(range(s.layers)):
             rdt.block_backward(cfg, s.batch, s.seq, self.block_slice(self.w, li),
                                self.block_slice(self.wb, li), self.h[li], self.saved_slice(li),
-                               self.dh, self.dh, self.block_slice(self.g, li), self.block_ws)
+                               self.dh, self.dh, self.block_slice(self.g, li), self.block_ws,
+                               grad_sq=self.sumsq)
         return self.loss_partials
 
     def clip_and_update(self):
-        """Global-norm clip from the squared sum of every gradient, then one
-        AdamW over all parameters (skipped on a non-finite norm)."""
+        """Global-norm clip from the squared sum of every gradient (summed by
+        the backward calls into ``self.sumsq`` as they produce the gradients),
+        then one AdamW over all parameters (skipped on a non-finite norm)."""
         o = self.optim
-        rdt.sq_sum([self.g], self.sumsq, self.sq_ws)
         rdt.clip_scale(self.sumsq, o["max_norm"], self.scale, self.nonfinite)
         self.step_count += 1
         rdt.adamw_step(self.w, self.g, self.m, self.v, self.step_count, o["lr"], o["beta1"],

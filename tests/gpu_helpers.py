@@ -31,8 +31,13 @@ def to_np(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def gpu_block(shape, p, x, dy):
-    """Block forward + backward on the GPU. p: dict of CPU fp32 tensors."""
+SQ_START = 0.25  # grad_sq value before a block backward adds its squared sum
+
+
+def gpu_block(shape, p, x, dy, with_sq=False):
+    """Block forward + backward on the GPU. p: dict of CPU fp32 tensors.
+    with_sq: also return the fused squared sum the backward added to a
+    scalar that held SQ_START."""
     cfg = rdt.Config.from_shape(shape)
     n = rdt.block_param_count(cfg)
     offs = rdt.block_param_offsets(cfg)
@@ -51,10 +56,14 @@ def gpu_block(shape, p, x, dy):
     dyd = dy.to("cuda").contiguous()
     dx = torch.empty_like(xd)
     grads = torch.full((n,), float("nan"), dtype=torch.float32, device="cuda")
-    rdt.block_backward(cfg, shape.batch, shape.seq, w, wb, xd, saved, dyd, dx, grads, ws)
+    sq = torch.full((1,), SQ_START, dtype=torch.float64, device="cuda")
+    rdt.block_backward(cfg, shape.batch, shape.seq, w, wb, xd, saved, dyd, dx, grads, ws,
+                       grad_sq=sq if with_sq else None)
     torch.cuda.synchronize()
     g = {name: grads[o:o + c].view(synth.block_shapes(shape)[name]) for name, (o, c) in
          offs.items()}
+    if with_sq:
+        return y, dx, g, float(sq)
     return y, dx, g
 
 
@@ -70,8 +79,10 @@ def gpu_head(shape, h, g_final, w_lm, targets):
     dh = torch.empty_like(hd)
     dgf = torch.empty_like(gf)
     dwl = torch.empty(w_lm.shape, dtype=torch.float32, device="cuda")
-    rdt.fused_cross_entropy(cfg, T, hd, gf, wl, tg, 1.0 / T, loss, dh, dgf, dwl, ws)
+    sq = torch.full((1,), float("nan"), dtype=torch.float64, device="cuda")
+    rdt.fused_cross_entropy(cfg, T, hd, gf, wl, tg, 1.0 / T, loss, dh, dgf, dwl, ws, grad_sq=sq)
     torch.cuda.synchronize()
+    gpu_head.last_sq = float(sq)
     return loss, dh, dgf, dwl
 
 

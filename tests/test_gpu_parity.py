@@ -10,8 +10,8 @@ from oracle import model as om
 from resident_decoder_trainer_gb300 import rdt, synth
 from resident_decoder_trainer_gb300.step import DecoderTrainer
 
-from gpu_helpers import (ADAMW_REL, FWD_REL_L2, GRAD_REL_L2, LOSS_REL, ensure_built, gpu_block,
-                         gpu_head, ragged_shape, rel_l2, to_np)
+from gpu_helpers import (ADAMW_REL, FWD_REL_L2, GRAD_REL_L2, LOSS_REL, SQ_START, ensure_built,
+                         gpu_block, gpu_head, ragged_shape, rel_l2, to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -61,8 +61,12 @@ def _block_case(shape, seed=0):
     blk, x, dy = synth.make_block_inputs(shape, seed)
     y_ref, cache = om.block_forward(blk, x, shape)
     dx_ref, g_ref = om.block_backward(cache, dy, shape)
-    y, dx, g = gpu_block(shape, blk, x, dy)
+    y, dx, g, sq = gpu_block(shape, blk, x, dy, with_sq=True)
     x64 = to_np(x)
+    # the squared sum the backward fused into its weight-gradient epilogues
+    # and gain reductions is the sum of squares of the gradients it returned
+    ref_sq = SQ_START + sum(float(np.sum(to_np(t) ** 2)) for t in g.values())
+    assert abs(sq - ref_sq) / ref_sq < 1e-6, (sq, ref_sq)
     assert rel_l2(to_np(y) - x64, y_ref - x64) < FWD_REL_L2
     assert rel_l2(to_np(dx), dx_ref) < GRAD_REL_L2
     for name in g_ref:
@@ -121,6 +125,8 @@ def test_fused_cross_entropy_parity(shape):
     assert rel_l2(to_np(dh), ref["dh"]) < GRAD_REL_L2
     assert rel_l2(to_np(dgf), ref["g_final"]) < GRAD_REL_L2
     assert rel_l2(to_np(dwl), ref["w_lm"]) < GRAD_REL_L2
+    ref_sq = float(np.sum(to_np(dgf) ** 2) + np.sum(to_np(dwl) ** 2))
+    assert abs(gpu_head.last_sq - ref_sq) / ref_sq < 1e-6
 
 
 def test_cross_entropy_of_zero_head_is_log_vocab():
@@ -198,15 +204,17 @@ def _full_step_case(shape, seed=0):
         err = rel_l2(to_np(tr.tensor(tr.g, li, name)), gref)
         worst = max(worst, err)
         assert err < GRAD_REL_L2, f"{li}.{name}: rel L2 {err:.3e}"
-    # clip on the GPU's own gradients: norm from the squared sum, not re-squared
-    rdt.sq_sum([tr.g], tr.sumsq, tr.sq_ws)
-    torch.cuda.synchronize()
+    # clip on the GPU's own gradients: the squared sum the backward fused into
+    # its gradient producers, norm from it (not re-squared)
     g_all = to_np(tr.g)
     assert abs(float(tr.sumsq) - float(np.sum(g_all * g_all))) / float(np.sum(g_all * g_all)) < 1e-6
     assert abs(math.sqrt(float(tr.sumsq)) - ref["norm"]) / ref["norm"] < GRAD_REL_L2
-    # AdamW given identical gradients: feed the oracle's gradients
+    # AdamW given identical gradients: feed the oracle's gradients and their
+    # squared sum (the standalone rdt_sq_sum)
     for (li, name), gref in ref["grads"].items():
         tr.tensor(tr.g, li, name).copy_(torch.from_numpy(gref).float())
+    ws = torch.empty(rdt.sq_sum_workspace_bytes(), dtype=torch.uint8, device="cuda")
+    rdt.sq_sum([tr.g], tr.sumsq, ws)
     tr.clip_and_update()
     torch.cuda.synchronize()
     for (li, name), wref in ref["params"].items():

@@ -191,9 +191,8 @@ def test_q4b_full_step_at_full_size(q4b_full_inputs):
     ref = om.head_forward_backward(h, oh["g_final"], oh["w_lm"], tg.numpy()[rows], pshape)
     assert np.max(np.abs(lp[rows] - ref["loss_partials"]) / ref["loss_partials"]) < 10 * LOSS_REL
     assert abs(lp[rows].mean() - ref["loss"]) / ref["loss"] < LOSS_REL
-    # squared sum over every gradient, in fp64 on the host, chunk by chunk
-    rdt.sq_sum([tr.g], tr.sumsq, tr.sq_ws)
-    torch.cuda.synchronize()
+    # squared sum over every gradient (fused into the backward's gradient
+    # producers) against fp64 on the host, chunk by chunk
     want = 0.0
     chunk = 1 << 26
     for i in range(0, tr.n_params, chunk):
