@@ -64,16 +64,21 @@ struct FwdCfg {
   static constexpr uint32_t CHUNK = 128 * 128;  // 64 cols x 128 rows of bf16
   static constexpr uint32_t Q_BYTES = BM * D * 2;
   static constexpr uint32_t KV_BYTES = BN * D * 2;
-  static constexpr uint32_t P_BYTES = BM * BN * 2;
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;       // [2]
   static constexpr uint32_t OFF_V = OFF_K + 2 * KV_BYTES;  // [2]
-  static constexpr uint32_t OFF_P = OFF_V + 2 * KV_BYTES;
-  static constexpr uint32_t OFF_RED = OFF_P + P_BYTES;  // float [2][2][128] maxima, [2][128] sums
+  static constexpr uint32_t OFF_RED = OFF_V + 2 * KV_BYTES;  // float [2][2][128] maxima, [2][128] sums
   static constexpr uint32_t OFF_BAR = OFF_RED + 3 * 2 * 128 * 4;
   static constexpr size_t SMEM = OFF_BAR + 256 + 1024;
+  // TMEM: two S buffers (128 fp32 columns each; P is written over the first
+  // 64 columns of its S buffer as packed bf16), O after them
   static constexpr uint32_t TMEM_S = 0, TMEM_O = 256, TMEM_COLS = 512;
 };
+
+// Rows rescale O only when their running maximum grows by more than 2^8 (in
+// the log2 domain): below that the stale maximum is kept, P stays <= 2^8 and
+// the result is the same (O and l are both relative to the stale maximum).
+constexpr float kRescaleLog2 = 8.f;
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -89,8 +94,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + C::OFF_BAR;
   const uint32_t q_full = bar0, k_full = bar0 + 8, v_full = bar0 + 24, kv_empty = bar0 + 40,
-                 s_full = bar0 + 56, s_free = bar0 + 72, p_full = bar0 + 88, o_done = bar0 + 96,
-                 drain = bar0 + 104;
+                 s_full = bar0 + 56, p_full = bar0 + 72, o_done = bar0 + 80, drain = bar0 + 88;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 128);
   float* red_max = reinterpret_cast<float*>(smem + C::OFF_RED);  // [2 parity][2 half][128 rows]
   float* red_sum = red_max + 2 * 2 * 128;                        // [2 half][128 rows]
@@ -113,7 +117,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(v_full + 8 * i, 1);
       mbar_init(kv_empty + 8 * i, 1);
       mbar_init(s_full + 8 * i, 1);
-      mbar_init(s_free + 8 * i, kEltThreads);
     }
     mbar_init(p_full, kEltThreads);
     mbar_init(o_done, 1);
@@ -175,9 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = mbar_wait(q_full, 0, err);
       auto issue_s = [&](int j) -> bool {
         const int st = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait(k_full + 8 * st, ph, err)) return false;
-        if (!mbar_wait(s_free + 8 * st, ph ^ 1, err)) return false;
+        if (!mbar_wait(k_full + 8 * st, (j >> 1) & 1, err)) return false;
         tc_fence_after();
         const uint32_t kb = sbase + C::OFF_K + st * C::KV_BYTES;
 #pragma unroll
@@ -191,22 +192,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       if (ok) ok = issue_s(0);
       for (int j = 0; j < n_tiles && ok; ++j) {
-        if (j + 1 < n_tiles && !issue_s(j + 1)) {
-          ok = false;
-          break;
-        }
         const int st = j & 1;
+        if (j + 1 < n_tiles) {
+          // S buffer (j+1)&1 still holds P_{j-1}, read by P_{j-1} V
+          if (j >= 1 && !mbar_wait(o_done, (j - 1) & 1, err)) {
+            ok = false;
+            break;
+          }
+          if (!issue_s(j + 1)) {
+            ok = false;
+            break;
+          }
+        }
         if (!mbar_wait(p_full, j & 1, err) || !mbar_wait(v_full + 8 * st, (j >> 1) & 1, err)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t vb = sbase + C::OFF_V + st * C::KV_BYTES;
+        // O += P V with P (bf16, in TMEM over S buffer st) as the A operand
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
-          tc_mma_bf16(tmem + C::TMEM_O,
-                      sdesc_sw128(sbase + C::OFF_P + (k >> 2) * C::CHUNK + (k & 3) * 32, 16, 1024),
-                      sdesc_sw128(vb + k * 2048, C::CHUNK, 1024), idesc_o, (j | k) != 0);
+          tc_mma_bf16_ts(tmem + C::TMEM_O, tmem + C::TMEM_S + st * BN + k * 8,
+                         sdesc_sw128(vb + k * 2048, C::CHUNK, 1024), idesc_o, (j | k) != 0);
         tc_commit(o_done);
         tc_commit(kv_empty + 8 * st);
       }
@@ -220,7 +228,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = quarter * 32 + lane;
     const int qpos = m0 + row;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    uint8_t* p_tile = smem + C::OFF_P;
     float m_run = -INFINITY, l_part = 0.f;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
@@ -231,12 +238,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       uint32_t sv[64];
-      const uint32_t ts = tmem + lane_base + C::TMEM_S + st * BN + half * 64;
-      tmem_ld32(ts, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-      tmem_ld32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      const uint32_t ts = tmem + lane_base + C::TMEM_S + st * BN;
+      tmem_ld32(ts + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      tmem_ld32(ts + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
       tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(s_free + 8 * st);
       const int c0 = j * BN + half * 64;  // key position of sv[0]
       float mx = -INFINITY;
       const bool edge = (c0 + 64 > qpos) || (c0 + 64 > S);
@@ -247,47 +252,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         sv[c] = __float_as_uint(x);
         mx = fmaxf(mx, x);
       }
-      // row maximum over both halves of the row
+      // row maximum over both halves of the row (both halves have finished
+      // reading this S buffer once past the barrier, so P may overwrite it)
       red_max[(st * 2 + half) * 128 + row] = mx;
       named_bar_sync(1 + quarter, 64);
-      mx = fmaxf(fmaxf(mx, red_max[(st * 2 + (half ^ 1)) * 128 + row]), m_run);
-      const float alpha = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - mx);
-      m_run = mx;
+      mx = fmaxf(mx, red_max[(st * 2 + (half ^ 1)) * 128 + row]);
+      float alpha = 1.f;
+      if (mx > m_run + kRescaleLog2) {
+        alpha = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - mx);
+        m_run = mx;
+      }
       float sum = 0.f;
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
-        const float p0 = ex2_approx(__uint_as_float(sv[c]) - mx);
-        const float p1 = ex2_approx(__uint_as_float(sv[c + 1]) - mx);
+        const float p0 = ex2_approx(__uint_as_float(sv[c]) - m_run);
+        const float p1 = ex2_approx(__uint_as_float(sv[c + 1]) - m_run);
         sum += p0 + p1;
         sv[c / 2] = pack_bf16x2(p0, p1);
       }
       l_part = l_part * alpha + sum;
-      if (j > 0) {
-        // O and the P tile are in use by the previous P V product until it completes
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        // O is being accumulated by P_{j-1} V until it completes
         if (!warp_wait(o_done, (j - 1) & 1, err)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-          for (int c = 0; c < D / 64; ++c) {
-            uint32_t ov[32];
-            const uint32_t to = tmem + lane_base + C::TMEM_O + half * (D / 2) + c * 32;
-            tmem_ld32(to, ov);
-            tmem_ld_wait();
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t ov[32];
+          const uint32_t to = tmem + lane_base + C::TMEM_O + half * (D / 2) + c * 32;
+          tmem_ld32(to, ov);
+          tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tmem_st32(to, ov);
-          }
-          tmem_st_wait();
+          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+          tmem_st32(to, ov);
         }
       }
-#pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8)
-        *reinterpret_cast<uint4*>(p_tile + half * C::CHUNK + sw128_offset(row, c8)) =
-            make_uint4(sv[4 * c8], sv[4 * c8 + 1], sv[4 * c8 + 2], sv[4 * c8 + 3]);
-      fence_proxy_async_smem();
+      // P (bf16 pairs) over the first 64 columns of this S buffer: keys
+      // [64 half, 64 half + 64) -> columns [32 half, 32 half + 32)
+      tmem_st32(ts + half * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_full);
     }

@@ -35,11 +35,12 @@ constexpr int EPI_THREADS = 256;
 constexpr int TMEM_COLS = 512;
 
 // Epilogue staging per epilogue warp (two buffers, see the epilogues below):
-// 4 KB; 128 x 192 single-CTA tiles keep a 5-stage ring by staging 2 KB per
-// warp (in units half as wide).
+// 4 KB; 128 x 192 tiles keep a 5-stage ring by staging 2 KB per warp (in
+// units half as wide).
+__host__ __device__ constexpr uint32_t OutStageBytes(int bn) { return bn == 192 ? 2048 : 4096; }
 template <int BN, bool PAIR>
 struct OutStage {
-  static constexpr uint32_t BYTES = (BN == 192 && !PAIR) ? 2048 : 4096;
+  static constexpr uint32_t BYTES = OutStageBytes(BN);
   static constexpr uint32_t TOTAL = BYTES * (EPI_THREADS / 32);
 };
 
@@ -519,6 +520,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (lane == 0) {
       // ----------------------------------------------------------------- MMA
       constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+      const uint64_t a_desc0 = sdesc_sw128(smem_base, A_MN ? MN_CHUNK_BYTES : 16, 1024);
+      const uint64_t b_desc0 = sdesc_sw128(smem_base + A_BYTES, B_MN ? MN_CHUNK_BYTES : 16, 1024);
       int stage = 0;
       uint32_t ph = 0;
       int acc = 0;
@@ -537,14 +540,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_base + stage * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
+          // descriptors of this stage: the ring's first stage plus the stage
+          // offset, then one K=16 step = 32 B (K-major) or 2048 B (MN-major)
+          const uint64_t ad0 = a_desc0 + static_cast<uint64_t>(stage) * (STAGE_BYTES >> 4);
+          const uint64_t bd0 = b_desc0 + static_cast<uint64_t>(stage) * (STAGE_BYTES >> 4);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
-            const uint64_t ad = A_MN ? sdesc_sw128(sa + k * 2048, MN_CHUNK_BYTES, 1024)
-                                     : sdesc_sw128(sa + k * 32, 16, 1024);
-            const uint64_t bd = B_MN ? sdesc_sw128(sb + k * 2048, MN_CHUNK_BYTES, 1024)
-                                     : sdesc_sw128(sb + k * 32, 16, 1024);
+            const uint64_t ad = ad0 + static_cast<uint64_t>(k) * ((A_MN ? 2048 : 32) >> 4);
+            const uint64_t bd = bd0 + static_cast<uint64_t>(k) * ((B_MN ? 2048 : 32) >> 4);
             tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0);
           }
           tc_commit(empty0 + 8 * stage);
@@ -610,7 +613,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 // of the tile its own TMEM holds, with the same epilogues as above.
 template <int BN_>
 struct Tile2 {
-  static_assert(BN_ == 256, "pair tiles are 256 x 256");
+  static_assert(BN_ == 256, "pair tiles are 256 x 256 (256 x 192 pairs measured slower than 128 x 192 single tiles)");
   static constexpr int BN = BN_;      // pair tile width (N of the MMA)
   static constexpr int BH = BN / 2;   // columns of B each CTA loads
   static constexpr uint32_t B_BYTES = BH * BK * 2;
@@ -709,7 +712,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             for (int j = 0; j < BH / 64; ++j)
               tma_load_2d_pair(sb + j * MN_CHUNK_BYTES, &tma_b, fb, n0 + 64 * j, k0);
           } else {
-            // one box of 128 rows; SwiGLU: the even CTA loads the 128 gate rows
+            // one box of BN/2 rows; SwiGLU: the even CTA loads the 128 gate rows
             // of I-columns nt*128 + [0,128), the odd CTA the matching up rows
             const int r = (EPI == EPI_SWIGLU) ? nt * 128 + static_cast<int>(rank) * p.swiglu_half
                                               : nt * BN + static_cast<int>(rank) * BH;
@@ -726,6 +729,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (lane == 0 && rank == 0) {
       // ----------------------------------------------------------------- MMA
       constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN, A_MN, B_MN);
+      const uint64_t a_desc0 = sdesc_sw128(smem_base, A_MN ? MN_CHUNK_BYTES : 16, 1024);
+      const uint64_t b_desc0 = sdesc_sw128(smem_base + A_BYTES, B_MN ? MN_CHUNK_BYTES : 16, 1024);
       int stage = 0;
       uint32_t ph = 0;
       int acc = 0;
@@ -744,14 +749,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_base + stage * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
+          // descriptors of this stage: the ring's first stage plus the stage
+          // offset, then one K=16 step = 32 B (K-major) or 2048 B (MN-major)
+          const uint64_t ad0 = a_desc0 + static_cast<uint64_t>(stage) * (STAGE_BYTES >> 4);
+          const uint64_t bd0 = b_desc0 + static_cast<uint64_t>(stage) * (STAGE_BYTES >> 4);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
-            const uint64_t ad = A_MN ? sdesc_sw128(sa + k * 2048, MN_CHUNK_BYTES, 1024)
-                                     : sdesc_sw128(sa + k * 32, 16, 1024);
-            const uint64_t bd = B_MN ? sdesc_sw128(sb + k * 2048, MN_CHUNK_BYTES, 1024)
-                                     : sdesc_sw128(sb + k * 32, 16, 1024);
+            const uint64_t ad = ad0 + static_cast<uint64_t>(k) * ((A_MN ? 2048 : 32) >> 4);
+            const uint64_t bd = bd0 + static_cast<uint64_t>(k) * ((B_MN ? 2048 : 32) >> 4);
             tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
           }
           tc_commit_pair_mc(empty0 + 8 * stage, 0x3);
@@ -1046,22 +1051,24 @@ cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N,
     bn = 192;
   }
   if (pairs_max > 0 && M > BM) {
-    const int64_t tiles = (int64_t)((M + 2 * BM - 1) / (2 * BM)) * ((N + 255) / 256);
-    const double c = static_cast<double>((tiles + pairs_max - 1) / pairs_max) * 256 / kRatePair;
-    if (c < best) {
-      best = c;
+    auto cost2 = [&](int w, double rate) {
+      const int64_t tiles = (int64_t)((M + 2 * BM - 1) / (2 * BM)) * ((N + w - 1) / w);
+      return static_cast<double>((tiles + pairs_max - 1) / pairs_max) * w / rate;
+    };
+    if (cost2(256, kRatePair) < best) {
+      best = cost2(256, kRatePair);
       bn = 256;
       pair_tiles = true;
     }
   }
   CUtensorMap ta, tb;
-  const int b_box = (pair_tiles && !b_mn) ? 128 : 64;
+  const int b_box = (pair_tiles && !b_mn) ? bn / 2 : 64;
   if (!make_map(&ta, A, a_mn ? 64 : 128) || !make_map(&tb, B, b_box)) {
     *why = "gemm: cuTensorMapEncodeTiled failed";
     return cudaErrorInvalidValue;
   }
   OutMaps om;
-  if (!make_out_maps(&om, epi, M, N, (!pair_tiles && bn == 192) ? 2048u : 4096u)) {
+  if (!make_out_maps(&om, epi, M, N, OutStageBytes(bn))) {
     *why = "gemm: outputs need 16-byte aligned rows (cuTensorMapEncodeTiled failed)";
     return cudaErrorInvalidValue;
   }
