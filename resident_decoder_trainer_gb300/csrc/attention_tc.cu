@@ -333,20 +333,27 @@ struct BwdCfg {
   static constexpr uint32_t Q_CHUNK = 64 * 128;    // 64 d-cols x 64 query rows
   static constexpr uint32_t KV_BYTES = BKV * D * 2;
   static constexpr uint32_t Q_BYTES = BQ * D * 2;
-  static constexpr uint32_t T_BYTES = BKV * BQ * 2;  // P^T / dS^T tiles: 128 rows x 128 B
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = OFF_K + KV_BYTES;
   static constexpr uint32_t OFF_Q = OFF_V + KV_BYTES;      // [2]
   static constexpr uint32_t OFF_DO = OFF_Q + 2 * Q_BYTES;  // [2]
-  static constexpr uint32_t OFF_PT = OFF_DO + 2 * Q_BYTES;
-  static constexpr uint32_t OFF_DST = OFF_PT + T_BYTES;
-  static constexpr uint32_t OFF_LD = OFF_DST + T_BYTES;  // float [2 stages][lse2, D][64]
+  static constexpr uint32_t OFF_LD = OFF_DO + 2 * Q_BYTES;  // float [2 stages][lse2, D][64]
   static constexpr uint32_t OFF_BAR = OFF_LD + 2 * 2 * 64 * 4;
   static constexpr size_t SMEM = OFF_BAR + 256 + 1024;
-  // TMEM columns: dK, dV, then two (S^T, dP^T) buffer pairs of 64 + 64 columns
+  // TMEM columns: dK, dV, then two (S^T, dP^T) buffer pairs of 64 + 64
+  // columns; P^T and dS^T (packed bf16) are written back over their own S^T /
+  // dP^T columns and read from there as the A operands of dV += P^T dO and
+  // dK += dS^T Q.
   static constexpr uint32_t T_DK = 0, T_DV = 128, T_S = 256;
   static constexpr uint32_t TMEM_COLS = 512;
 };
+
+// TMEM column (relative to an S^T / dP^T block) of the packed bf16 A operand
+// for K step kk (16 queries): the lanes of warp half h pack their 32 queries
+// into columns [32 h, 32 h + 16).
+__device__ __forceinline__ uint32_t packed_kstep_col(int kk) {
+  return static_cast<uint32_t>((kk >> 1) * 32 + (kk & 1) * 8);
+}
 
 template <int DH>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -366,8 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + C::OFF_BAR;
   const uint32_t kv_full = bar0, q_full = bar0 + 8, q_empty = bar0 + 24, s_full = bar0 + 40,
-                 s_used = bar0 + 56, p_ready = bar0 + 72, pd_free = bar0 + 80, fin = bar0 + 88,
-                 drain = bar0 + 96;
+                 p_ready = bar0 + 56, done = bar0 + 72, fin = bar0 + 88, drain = bar0 + 96;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 128);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -389,10 +395,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(q_full + 8 * i, 1);
       mbar_init(q_empty + 8 * i, 1);
       mbar_init(s_full + 8 * i, 1);
-      mbar_init(s_used + 8 * i, kEltThreads);
+      mbar_init(p_ready + 8 * i, kEltThreads);
+      mbar_init(done + 8 * i, 1);
     }
-    mbar_init(p_ready, kEltThreads);
-    mbar_init(pd_free, 1);
     mbar_init(fin, 1);
     mbar_init(drain, 1);
     fence_mbar_init();
@@ -452,25 +457,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // -------------------------------------------------------------- MMA
       constexpr uint32_t id_s = idesc_bf16_f32(128, BQ, 0, 0);  // S^T, dP^T
-      constexpr uint32_t id_kv = idesc_bf16_f32(128, D, 0, 1);  // dV, dK
+      constexpr uint32_t id_kv = idesc_bf16_f32(128, D, 0, 1);  // dV, dK (A from TMEM)
+      const uint64_t k_desc = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
+      const uint64_t v_desc = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
       bool ok = mbar_wait(kv_full, 0, err);
       auto issue_s = [&](int it) -> bool {
         const int st = it & 1;
         const uint32_t ph = (it >> 1) & 1;
         if (!mbar_wait(q_full + 8 * st, ph, err)) return false;
-        if (!mbar_wait(s_used + 8 * st, ph ^ 1, err)) return false;  // buffer pair consumed
+        // buffer pair st still holds P^T / dS^T of iteration it - 2
+        if (it >= 2 && !mbar_wait(done + 8 * st, ph ^ 1, err)) return false;
         tc_fence_after();
-        const uint32_t qb = sbase + C::OFF_Q + st * C::Q_BYTES;
-        const uint32_t ob = sbase + C::OFF_DO + st * C::Q_BYTES;
+        const uint64_t q_desc = sdesc_sw128(sbase + C::OFF_Q + st * C::Q_BYTES, 16, 1024);
+        const uint64_t o_desc = sdesc_sw128(sbase + C::OFF_DO + st * C::Q_BYTES, 16, 1024);
         const uint32_t ts = tmem + C::T_S + st * 128;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t koff = (k >> 2) * C::KV_CHUNK + (k & 3) * 32;
-          const uint32_t qoff = (k >> 2) * C::Q_CHUNK + (k & 3) * 32;
-          tc_mma_bf16(ts, sdesc_sw128(sbase + C::OFF_K + koff, 16, 1024),
-                      sdesc_sw128(qb + qoff, 16, 1024), id_s, k > 0);
-          tc_mma_bf16(ts + 64, sdesc_sw128(sbase + C::OFF_V + koff, 16, 1024),
-                      sdesc_sw128(ob + qoff, 16, 1024), id_s, k > 0);
+          const uint64_t kv_off = ((k >> 2) * C::KV_CHUNK + (k & 3) * 32) >> 4;
+          const uint64_t q_off = ((k >> 2) * C::Q_CHUNK + (k & 3) * 32) >> 4;
+          tc_mma_bf16(ts, k_desc + kv_off, q_desc + q_off, id_s, k > 0);
+          tc_mma_bf16(ts + 64, v_desc + kv_off, o_desc + q_off, id_s, k > 0);
         }
         tc_commit(s_full + 8 * st);
         return true;
@@ -482,22 +488,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        if (!mbar_wait(p_ready, it & 1, err)) {
+        if (!mbar_wait(p_ready + 8 * st, (it >> 1) & 1, err)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t qb = sbase + C::OFF_Q + st * C::Q_BYTES;
         const uint32_t ob = sbase + C::OFF_DO + st * C::Q_BYTES;
+        const uint32_t ts = tmem + C::T_S + st * 128;
 #pragma unroll
         for (int k = 0; k < BQ / 16; ++k) {
           // dV += P^T dO ; dK += dS^T Q   (K dimension = query rows)
-          tc_mma_bf16(tmem + C::T_DV, sdesc_sw128(sbase + C::OFF_PT + k * 32, 16, 1024),
-                      sdesc_sw128(ob + k * 2048, C::Q_CHUNK, 1024), id_kv, (it | k) != 0);
-          tc_mma_bf16(tmem + C::T_DK, sdesc_sw128(sbase + C::OFF_DST + k * 32, 16, 1024),
-                      sdesc_sw128(qb + k * 2048, C::Q_CHUNK, 1024), id_kv, (it | k) != 0);
+          tc_mma_bf16_ts(tmem + C::T_DV, ts + packed_kstep_col(k),
+                         sdesc_sw128(ob + k * 2048, C::Q_CHUNK, 1024), id_kv, (it | k) != 0);
+          tc_mma_bf16_ts(tmem + C::T_DK, ts + 64 + packed_kstep_col(k),
+                         sdesc_sw128(qb + k * 2048, C::Q_CHUNK, 1024), id_kv, (it | k) != 0);
         }
-        tc_commit(pd_free);
+        tc_commit(done + 8 * st);
         tc_commit(q_empty + 8 * st);
       }
       tc_commit(fin);
@@ -525,8 +532,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(ts, sv);
       tmem_ld32(ts + 64, dp);
       tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(s_used + 8 * st);
       const float4* l4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + st * 512) + half * 8;
       const float4* d4 =
           reinterpret_cast<const float4*>(smem + C::OFF_LD + st * 512 + 256) + half * 8;
@@ -551,23 +556,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         dp[2 * c4] = pack_bf16x2(dsv[0], dsv[1]);
         dp[2 * c4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
       }
-      if (it > 0 && !warp_wait(pd_free, (it - 1) & 1, err)) {
-        ok = false;
-        break;
-      }
-      uint8_t* pt = smem + C::OFF_PT;
-      uint8_t* dst = smem + C::OFF_DST;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint32_t off = sw128_offset(row, 4 * half + c);
-        *reinterpret_cast<uint4*>(pt + off) =
-            make_uint4(sv[4 * c], sv[4 * c + 1], sv[4 * c + 2], sv[4 * c + 3]);
-        *reinterpret_cast<uint4*>(dst + off) =
-            make_uint4(dp[4 * c], dp[4 * c + 1], dp[4 * c + 2], dp[4 * c + 3]);
-      }
-      fence_proxy_async_smem();
+      // over this warp's own S^T / dP^T columns (no other warp reads them)
+      tmem_st16(ts, *reinterpret_cast<uint32_t(*)[16]>(&sv[0]));
+      tmem_st16(ts + 64, *reinterpret_cast<uint32_t(*)[16]>(&dp[0]));
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(p_ready);
+      mbar_arrive(p_ready + 8 * st);
     }
     // dK (scaled) and dV of this key tile, summed over the query heads of the group
     if (ok && warp_wait(fin, 0, err)) {
