@@ -71,6 +71,10 @@ WORKLOADS = {
     "q4b_block": DecoderShape(layers=1, hidden=2560, n_heads=32, n_kv_heads=8, head_dim=128,
                               intermediate=9728, vocab=151936, seq=2048, batch=1, eps=1e-6,
                               theta=1e6),
+    # the NF4-frozen block with LoRA adapters runs at the single-block shape
+    "q4b_nf4": DecoderShape(layers=1, hidden=2560, n_heads=32, n_kv_heads=8, head_dim=128,
+                            intermediate=9728, vocab=151936, seq=2048, batch=1, eps=1e-6,
+                            theta=1e6),
     "q4b_full": DecoderShape(layers=36, hidden=2560, n_heads=32, n_kv_heads=8, head_dim=128,
                              intermediate=9728, vocab=151936, seq=1024, batch=4, eps=1e-6,
                              theta=1e6),
@@ -148,3 +152,48 @@ def make_block_inputs(s: DecoderShape, seed: int = 0, device="cpu"):
     x = _normal((s.tokens, s.hidden), 1.0, gen, device)
     dy = draw_upstream(s, gen, device)
     return blk, x, dy
+
+
+# ------------------------------------------------------------------ NF4 + LoRA
+# The NF4-frozen block workload: packed 4-bit codes uniform over 0..15 (two
+# per byte), one fp32 scale per 64 consecutive weight elements drawn as
+# 3|N(0, 0.02)|, frozen gains of 1, LoRA rank 16 / alpha 32 on all seven
+# projections with A ~ N(0, 0.02) [rank, in] and B = 0 [out, rank] (or
+# N(0, b_std) when a test wants the adapter path live).
+LORA = dict(rank=16, alpha=32.0)
+NF4_PROJECTIONS = ("wq", "wk", "wv", "wo", "wg", "wu", "wd")
+
+
+def draw_nf4_block(s: DecoderShape, gen: torch.Generator, rank=None, b_std=0.0, device="cpu"):
+    """(base, gains, lora): base[name] = (packed uint8 [out, in/2], absmax fp32
+    [out*in/64]); gains fp32 ones; lora['a_q'..'a_d'] fp32 [rank, in] and
+    lora['b_q'..'b_d'] fp32 [out, rank]."""
+    rank = rank or LORA["rank"]
+    shp = block_shapes(s)
+    base = {}
+    for name in NF4_PROJECTIONS:
+        out, inn = shp[name]
+        packed = torch.randint(0, 256, (out, inn // 2), generator=gen, dtype=torch.int32,
+                               device=device).to(torch.uint8)
+        absmax = (_normal((out * inn // 64,), 0.02, gen, device).abs() * 3.0)
+        base[name] = (packed, absmax)
+    gains = {g: torch.ones(shp[g], dtype=torch.float32, device=device)
+             for g in ("g_attn", "g_ffn", "g_q", "g_k")}
+    lora = {}
+    for name in NF4_PROJECTIONS:
+        out, inn = shp[name]
+        lora["a_" + name[1:]] = _normal((rank, inn), 0.02, gen, device)
+    for name in NF4_PROJECTIONS:
+        out, inn = shp[name]
+        lora["b_" + name[1:]] = (_normal((out, rank), b_std, gen, device) if b_std > 0
+                                 else torch.zeros((out, rank), dtype=torch.float32, device=device))
+    return base, gains, lora
+
+
+def make_nf4_inputs(s: DecoderShape, seed: int = 0, rank=None, b_std=0.0, device="cpu"):
+    """NF4 block workload: (base, gains, lora, x, dy)."""
+    gen = make_generator(seed, device)
+    base, gains, lora = draw_nf4_block(s, gen, rank=rank, b_std=b_std, device=device)
+    x = _normal((s.tokens, s.hidden), 1.0, gen, device)
+    dy = draw_upstream(s, gen, device)
+    return base, gains, lora, x, dy
