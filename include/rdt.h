@@ -229,6 +229,23 @@ rdt_status rdt_gemm(const rdt_bf16* A, int32_t a_mn, int64_t lda, const rdt_bf16
                     int32_t b_mn, int64_t ldb, int32_t M, int32_t N, int32_t K, float* C,
                     int64_t ldc, void* stream);
 
+/* The NF4 GEMM of the NF4-frozen block (CudaNf4TransformerBlock in
+ * cuda_block.rs: frozen projection weights stored as packed 4-bit NormalFloat
+ * codes with one fp32 scale per 64-element block), exposed for tests:
+ * C[M, N] (fp32, row stride ldc) = A [M, K1] (bf16, lda) times B^T, plus an
+ * optional tail A2 [M, K2] times B2^T (K2 <= 64; the LoRA term folded in as
+ * extra K). W is [w_rows, w_cols] row-major: codes uint8 [w_rows, w_cols/2]
+ * (element 2j in the low nibble of byte j), scales fp32 [w_rows, w_cols/64];
+ * W = level[code] * scale, levels the 16 NormalFloat-4 values of QLoRA.
+ * b_mn == 0: B = W (N = w_rows, K1 = w_cols; y = x W^T), B2 [N, K2] (ldb2);
+ * b_mn == 1: B = W^T (N = w_cols, K1 = w_rows; dX = dY W), B2 [K2, N].
+ * w_cols % 256 == 0 and w_rows % 64 == 0; leading dimensions in elements,
+ * bf16 ones multiples of 8, ldc a multiple of 4; 16-byte aligned pointers. */
+rdt_status rdt_gemm_nf4(const rdt_bf16* A, int64_t lda, const uint8_t* codes,
+                        const float* scales, int64_t w_rows, int64_t w_cols, int32_t b_mn,
+                        const rdt_bf16* A2, int64_t lda2, const rdt_bf16* B2, int64_t ldb2,
+                        int32_t K2, int32_t M, float* C, int64_t ldc, void* stream);
+
 /* dst[i] = bf16(src[i]) with round-to-nearest-even; n elements, 16-byte aligned. */
 rdt_status rdt_cast_bf16(const float* src, rdt_bf16* dst, int64_t n, void* stream);
 

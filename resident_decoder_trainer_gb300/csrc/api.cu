@@ -226,6 +226,15 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
                   why_, cudaGetErrorString(e_));                                      \
   } while (0)
 
+#define RDT_GEMM_NF4(...)                                                             \
+  do {                                                                                \
+    const char* why_ = "";                                                           \
+    cudaError_t e_ = gemm_nf4(__VA_ARGS__, &why_);                                    \
+    if (e_ != cudaSuccess)                                                            \
+      return fail(*why_ ? RDT_EINVAL : RDT_ECUDA, "nf4 gemm at line %d: %s %s",        \
+                  __LINE__, why_, cudaGetErrorString(e_));                            \
+  } while (0)
+
 }  // namespace
 
 namespace rdt {
@@ -717,6 +726,38 @@ rdt_status rdt_gemm(const rdt_bf16* A, int32_t a_mn, int64_t lda, const rdt_bf16
   int* err = device_error_ptr();
   RDT_GEMM(Mat{A, arows, acols, lda}, a_mn != 0, Mat{B, brows, bcols, ldb}, b_mn != 0, M, N, K, e,
            err, s);
+  return RDT_OK;
+}
+
+rdt_status rdt_gemm_nf4(const rdt_bf16* A, int64_t lda, const uint8_t* codes,
+                        const float* scales, int64_t w_rows, int64_t w_cols, int32_t b_mn,
+                        const rdt_bf16* A2, int64_t lda2, const rdt_bf16* B2, int64_t ldb2,
+                        int32_t K2, int32_t M, float* C, int64_t ldc, void* stream) {
+  if (!A || !codes || !scales || !C) return fail(RDT_EINVAL, "null pointer");
+  if (M < 1 || w_rows < 1 || w_cols < 1) return fail(RDT_EINVAL, "M and W's dims must be >= 1");
+  if (K2 < 0 || K2 > 64 || (K2 > 0 && (!A2 || !B2)))
+    return fail(RDT_EINVAL, "K2 must be in [0, 64] with A2 and B2 given when K2 > 0");
+  if (w_cols % 256 || w_rows % 64) return fail(RDT_EINVAL, "W needs cols % 256 == 0, rows % 64 == 0");
+  const int64_t N = b_mn ? w_cols : w_rows, K1 = b_mn ? w_rows : w_cols;
+  if (lda % 8 || ldc % 4 || lda < K1 || ldc < N || !aligned16(A) || !aligned16(C) ||
+      !aligned16(codes) || !aligned16(scales))
+    return fail(RDT_EINVAL, "lda >= K (multiple of 8), ldc >= N (multiple of 4), 16-byte pointers");
+  if (K2 > 0 && (lda2 % 8 || ldb2 % 8 || lda2 < K2 || ldb2 < (b_mn ? N : K2) ||
+                 !aligned16(A2) || !aligned16(B2)))
+    return fail(RDT_EINVAL, "tail operands: lda2 >= K2, ldb2 >= its row length, multiples of 8");
+  Epi e;
+  e.kind = EPI_F32;
+  e.out = C;
+  e.ld_out = ldc;
+  const Mat a{A, M, K1, lda};
+  const Mat a2{A2, M, K2, lda2};
+  const Mat b2{B2, b_mn ? K2 : N, b_mn ? N : K2, ldb2};
+  const char* why = "";
+  const cudaError_t ce = gemm_nf4(a, Nf4Mat{codes, scales, w_rows, w_cols}, b_mn != 0,
+                                  K2 > 0 ? &a2 : nullptr, K2 > 0 ? &b2 : nullptr, K2, M, e,
+                                  device_error_ptr(), static_cast<cudaStream_t>(stream), &why);
+  if (ce == cudaErrorInvalidValue && why[0]) return fail(RDT_EINVAL, "%s", why);
+  if (ce != cudaSuccess) return fail(RDT_ECUDA, "%s", cudaGetErrorString(ce));
   return RDT_OK;
 }
 

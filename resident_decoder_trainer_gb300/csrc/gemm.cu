@@ -63,6 +63,7 @@ struct GemmParams {
   int swiglu_half;  // SwiGLU: row offset of the up rows in the stacked [2I, K] B
   int group;        // rasterisation: row tiles per group (see tile_coords)
   int sq_slots;     // squared-sum slots per tile (8 single-CTA, 16 pair)
+  int kb_main;      // NF4 GEMM: k-blocks of the decoded operand; the rest are the tail
   Epi epi;
   int* err;
 };
@@ -589,6 +590,325 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     if (lane == 0) bulk_wait0();
     __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------- NF4 kernel
+// The single-CTA GEMM with a frozen NF4 weight as its B operand, decoded into
+// the shared-memory tile on the way (no bf16 copy of the weight exists), plus
+// an optional tail k-block of ordinary bf16 operands (the LoRA term folded in
+// as extra K: [X | U] [W | B]^T forward, [dY | dU] [W ; A] backward).
+//
+// W is [rows, cols] row-major with two 4-bit codes per byte (element 2j in the
+// low nibble of byte j) and one fp32 scale per 64 consecutive elements of a
+// row (cols % 256 == 0, so each 64-element block lies in one row and the
+// scale array's row stride is a multiple of 16 bytes). K-major use (forward,
+// B(n, k) = W[n][k]) and MN-major use (dX, B(n, k) = W[k][n]) both decode one
+// 64-element block into one 128-byte row of the 128-byte-swizzled tile.
+//
+// Roles (448 threads): warp 0 TMA producer (A, the codes [64 rows x 32 B or
+// 64 rows x 128 B boxes] and the scales [64 rows x 4 fp32] of each stage into
+// a raw area of the stage; the tail's A and B straight into the tile), warp 1
+// MMA, warps 2-9 epilogue (as above), warps 10-13 decode: wait for a stage's
+// raw bytes, turn them into the bf16 B tile, and arrive on the stage's full
+// barrier, which the MMA waits for.
+constexpr int NF4_THREADS = 448;
+constexpr int NF4_BN = 256;
+
+struct TileN4 {
+  static constexpr uint32_t B_BYTES = NF4_BN * BK * 2;                  // 32 KB
+  static constexpr uint32_t CODE_BYTES = NF4_BN * BK / 2;               // 8 KB
+  static constexpr uint32_t ABS_BYTES = 4096;                           // <= 256 rows x 16 B
+  static constexpr uint32_t OFF_B = A_BYTES;
+  static constexpr uint32_t OFF_CODE = OFF_B + B_BYTES;
+  static constexpr uint32_t OFF_ABS = OFF_CODE + CODE_BYTES;
+  static constexpr uint32_t STAGE_BYTES = OFF_ABS + ABS_BYTES;          // 60 KB
+  static constexpr int STAGES = 3;
+  static constexpr uint32_t OFF_OUT = STAGES * STAGE_BYTES;
+  static constexpr size_t SMEM = OFF_OUT + OutStage<NF4_BN, false>::TOTAL + 1024 + 512;
+};
+
+// Codes / scales maps of the NF4 operand and the tail's A.
+struct Nf4Maps {
+  CUtensorMap codes, scales, a2;
+};
+
+// The sixteen NormalFloat-4 levels (QLoRA), ascending by code.
+__constant__ float kNf4Levels[16] = {
+    -1.0f, -0.6961928009986877f, -0.5250730514526367f, -0.39491748809814453f,
+    -0.28444138169288635f, -0.18477343022823334f, -0.09105003625154495f, 0.0f,
+    0.07958029955625534f, 0.16093020141124725f, 0.24611230194568634f, 0.33791524171829224f,
+    0.44070982933044434f, 0.5626170039176941f, 0.7229568362236023f, 1.0f};
+
+// Decode one 64-element block (32 code bytes at `codes`, scale `sc`) into row
+// `row` of a 128-byte-swizzled tile at `dst` (8 chunks of 8 bf16).
+__device__ __forceinline__ void nf4_decode_row(const uint8_t* codes, float sc,
+                                               const float* levels, uint8_t* dst, int row) {
+  const uint4 c0 = reinterpret_cast<const uint4*>(codes)[0];
+  const uint4 c1 = reinterpret_cast<const uint4*>(codes)[1];
+  const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+  for (int c8 = 0; c8 < 8; ++c8) {
+    // 4 code bytes -> 8 elements
+    const uint32_t b = w[c8];
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t byte = (b >> (8 * q)) & 0xFFu;
+      o[q] = pack_bf16x2(levels[byte & 0xFu] * sc, levels[byte >> 4] * sc);
+    }
+    *reinterpret_cast<uint4*>(dst + sw128_offset(row, c8)) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+template <int B_MN, int EPI>
+__global__ void __launch_bounds__(NF4_THREADS, 1)
+    gemm_nf4_kernel(const __grid_constant__ CUtensorMap tma_a,
+                    const __grid_constant__ CUtensorMap tma_b2,
+                    const __grid_constant__ Nf4Maps nm, const __grid_constant__ OutMaps om,
+                    const GemmParams p) {
+  constexpr int BN = NF4_BN;
+  constexpr int STAGES = TileN4::STAGES;
+  constexpr uint32_t STAGE_BYTES = TileN4::STAGE_BYTES;
+  using OS = OutStage<BN, false>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + TileN4::OFF_OUT + OS::TOTAL);
+  // bars: raw[S], full[S], empty[S], tfull[2], tempty[2], drain, epilogue inputs[8][2];
+  // then the TMEM address and the 16 levels
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 21);
+  float* levels = reinterpret_cast<float*>(bars + 3 * STAGES + 22);
+  const uint32_t raw0 = smem_u32(bars);
+  const uint32_t full0 = raw0 + 8 * STAGES;
+  const uint32_t empty0 = full0 + 8 * STAGES;
+  const uint32_t tfull0 = empty0 + 8 * STAGES;
+  const uint32_t tempty0 = tfull0 + 16;
+  const uint32_t drain = tempty0 + 16;
+  const uint32_t ebar0 = drain + 8;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(raw0 + 8 * s, 1);
+      mbar_init(full0 + 8 * s, 4);  // one arrival per decode warp
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, EPI_THREADS / 32);
+    }
+    mbar_init(drain, 1);
+    for (int i = 0; i < 16; ++i) mbar_init(ebar0 + 8 * i, 1);
+    fence_mbar_init();
+  }
+  if (threadIdx.x < 16) levels[threadIdx.x] = kNf4Levels[threadIdx.x];
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tma_a);
+    tma_prefetch_desc(&tma_b2);
+    tma_prefetch_desc(&nm.codes);
+    tma_prefetch_desc(&nm.scales);
+    tma_prefetch_desc(&nm.a2);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int ntiles = p.m_tiles * p.n_tiles;
+  const uint32_t smem_base = smem_u32(smem);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      int stage = 0;
+      uint32_t ph = 0;
+      uint32_t pending = 0, pending_par = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        int mt, nt;
+        tile_coords(t, p, mt, nt);
+        const int m0 = mt * BM;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(empty0 + 8 * stage, ph ^ 1, p.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t rb = raw0 + 8 * stage;
+          const uint32_t sa = smem_base + stage * STAGE_BYTES;
+          const uint32_t sb = sa + TileN4::OFF_B;
+          const uint32_t sc = sa + TileN4::OFF_CODE;
+          const uint32_t ss = sa + TileN4::OFF_ABS;
+          const int k0 = kb * BK;
+          if (kb < p.kb_main) {
+            mbar_arrive_expect_tx(rb, A_BYTES + (B_MN ? 64 * 128 + 64 * 16
+                                                       : TileN4::CODE_BYTES + NF4_BN * 16));
+            tma_load_2d(sa, &tma_a, rb, k0, m0);
+            if (B_MN) {
+              // W rows k0..k0+63, columns nt*256..: 128 code bytes and 4 scales per row
+              tma_load_2d(sc, &nm.codes, rb, nt * (BN / 2), k0);
+              tma_load_2d(ss, &nm.scales, rb, nt * (BN / 64), k0);
+            } else {
+#pragma unroll
+              for (int j = 0; j < BN / 64; ++j) {
+                const int r = (EPI == EPI_SWIGLU)
+                                  ? nt * 128 + (j & 1) * 64 + (j >> 1) * p.swiglu_half
+                                  : nt * BN + j * 64;
+                tma_load_2d(sc + j * 2048, &nm.codes, rb, k0 / 2, r);
+                tma_load_2d(ss + j * 1024, &nm.scales, rb, kb & ~3, r);
+              }
+            }
+          } else {
+            // tail: ordinary bf16 A and B for k beyond the decoded operand
+            const int kt = k0 - p.kb_main * BK;
+            mbar_arrive_expect_tx(rb, A_BYTES + TileN4::B_BYTES);
+            tma_load_2d(sa, &nm.a2, rb, kt, m0);
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) {
+              if (B_MN) {
+                tma_load_2d(sb + j * MN_CHUNK_BYTES, &tma_b2, rb, nt * BN + 64 * j, kt);
+              } else {
+                const int r = (EPI == EPI_SWIGLU)
+                                  ? nt * 128 + (j & 1) * 64 + (j >> 1) * p.swiglu_half
+                                  : nt * BN + j * 64;
+                tma_load_2d(sb + j * MN_CHUNK_BYTES, &tma_b2, rb, kt, r);
+              }
+            }
+          }
+          pending |= 1u << stage;
+          pending_par = (pending_par & ~(1u << stage)) | (ph << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < STAGES; ++s)
+          if (pending & (1u << s)) mbar_wait(raw0 + 8 * s, (pending_par >> s) & 1u, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ----------------------------------------------------------------- MMA
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 0, B_MN);
+      const uint64_t a_desc0 = sdesc_sw128(smem_base, 16, 1024);
+      const uint64_t b_desc0 =
+          sdesc_sw128(smem_base + TileN4::OFF_B, B_MN ? MN_CHUNK_BYTES : 16, 1024);
+      int stage = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t acc_ph = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        if (!mbar_wait(tempty0 + 8 * acc, acc_ph ^ 1, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(full0 + 8 * stage, ph, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad0 = a_desc0 + static_cast<uint64_t>(stage) * (STAGE_BYTES >> 4);
+          const uint64_t bd0 = b_desc0 + static_cast<uint64_t>(stage) * (STAGE_BYTES >> 4);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = ad0 + static_cast<uint64_t>(k) * (32 >> 4);
+            const uint64_t bd = bd0 + static_cast<uint64_t>(k) * ((B_MN ? 2048 : 32) >> 4);
+            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0);
+          }
+          tc_commit(empty0 + 8 * stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            ph ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit(tfull0 + 8 * acc);
+        acc ^= 1;
+        if (acc == 0) acc_ph ^= 1;
+      }
+      tc_commit(drain);
+      mbar_wait(drain, 0, nullptr);
+    }
+  } else if (warp < 10) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    uint8_t* stg = smem + TileN4::OFF_OUT + (warp - 2) * OS::BYTES;
+    const Stage st{stg, smem_u32(stg), ebar0 + 16 * (warp - 2), lane};
+    uint32_t ucnt = 0, eph = 0;
+    int acc = 0;
+    uint32_t acc_ph = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+      int mt, nt;
+      tile_coords(t, p, mt, nt);
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      if (!epilogue_tile<EPI, BN, OS::BYTES>(p, om, tbase, mt * BM + q * 32, nt, half, st, ucnt,
+                                             eph, tfull0 + 8 * acc, acc_ph, t, warp - 2))
+        break;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+      acc ^= 1;
+      if (acc == 0) acc_ph ^= 1;
+    }
+    if (lane == 0) bulk_wait0();
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- decode
+    const int dt = static_cast<int>(threadIdx.x) - 320;  // 0..127
+    int stage = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      for (int kb = 0; kb < p.k_blocks; ++kb) {
+        if (!warp_wait(raw0 + 8 * stage, ph, p.err)) {
+          ok = false;
+          break;
+        }
+        if (kb < p.kb_main) {
+          uint8_t* sp = smem + stage * STAGE_BYTES;
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int u = dt + 128 * i;  // one 64-element block of W per u
+            if (B_MN) {
+              const int k_row = u & 63, ch = u >> 6;
+              const float sc =
+                  *reinterpret_cast<const float*>(sp + TileN4::OFF_ABS + k_row * 16 + ch * 4);
+              nf4_decode_row(sp + TileN4::OFF_CODE + k_row * 128 + ch * 32, sc, levels,
+                             sp + TileN4::OFF_B + ch * MN_CHUNK_BYTES, k_row);
+            } else {
+              const float sc = *reinterpret_cast<const float*>(sp + TileN4::OFF_ABS + u * 16 +
+                                                               (kb & 3) * 4);
+              nf4_decode_row(sp + TileN4::OFF_CODE + u * 32, sc, levels,
+                             sp + TileN4::OFF_B, u);
+            }
+          }
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full0 + 8 * stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          ph ^= 1;
+        }
+      }
+    }
   }
 
   tc_fence_before();
@@ -1133,6 +1453,131 @@ cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N,
 #undef RDT_GEMM2_CASE
 #undef RDT_GEMM_CASE
   *why = "gemm: unsupported operand-major / epilogue combination";
+  return cudaErrorInvalidValue;
+}
+
+// ------------------------------------------------------------- NF4 host
+static bool make_u8_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols_bytes,
+                        int box_cols, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || (reinterpret_cast<uintptr_t>(ptr) & 15) || (cols_bytes % 16)) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols_bytes), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols_bytes)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t es[2] = {1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+static bool make_f32_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols,
+                         int box_cols, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || (reinterpret_cast<uintptr_t>(ptr) & 15) || ((cols * 4) % 16)) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t es[2] = {1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int B_MN, int EPI>
+static cudaError_t launch_nf4(const CUtensorMap& ta, const CUtensorMap& tb2, const Nf4Maps& nm,
+                              const OutMaps& om, const GemmParams& p, cudaStream_t s) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_nf4_kernel<B_MN, EPI>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(TileN4::SMEM));
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const int ntiles = p.m_tiles * p.n_tiles;
+  const int grid = ntiles < num_sms() ? ntiles : num_sms();
+  const int64_t slot = gemm_timing_before(s, 2.0 * p.M * (double)p.N * p.K);
+  note_launch();
+  gemm_nf4_kernel<B_MN, EPI><<<grid, NF4_THREADS, TileN4::SMEM, s>>>(ta, tb2, nm, om, p);
+  gemm_timing_after(s, slot);
+  return cudaGetLastError();
+}
+
+cudaError_t gemm_nf4(const Mat& A, const Nf4Mat& W, bool b_mn, const Mat* A2, const Mat* B2,
+                     int K2, int M, const Epi& epi, int* err, cudaStream_t s, const char** why) {
+  const int N = static_cast<int>(b_mn ? W.cols : W.rows);
+  const int K1 = static_cast<int>(b_mn ? W.rows : W.cols);
+  if (M <= 0 || N <= 0 || K1 <= 0 || K2 < 0 || K2 > BK) {
+    *why = "gemm_nf4: empty problem or a tail wider than 64";
+    return cudaErrorInvalidValue;
+  }
+  if (W.cols % 256 || W.rows % 64 || (K2 > 0 && (!A2 || !B2))) {
+    *why = "gemm_nf4: NF4 weights need cols % 256 == 0 and rows % 64 == 0";
+    return cudaErrorInvalidValue;
+  }
+  const bool swiglu = epi.kind == EPI_SWIGLU;
+  if (swiglu && b_mn) {
+    *why = "gemm_nf4: SwiGLU epilogue needs a K-major B";
+    return cudaErrorInvalidValue;
+  }
+  if ((A.ld % 8) || (reinterpret_cast<uintptr_t>(A.ptr) & 15) ||
+      (K2 > 0 && ((A2->ld % 8) || (B2->ld % 8) || (reinterpret_cast<uintptr_t>(A2->ptr) & 15) ||
+                  (reinterpret_cast<uintptr_t>(B2->ptr) & 15)))) {
+    *why = "gemm_nf4: operands need 16-byte aligned rows";
+    return cudaErrorInvalidValue;
+  }
+  CUtensorMap ta, tb2;
+  Nf4Maps nm;
+  bool ok = make_map(&ta, A, 128);
+  ok = ok && make_u8_map(&nm.codes, W.codes, W.rows, W.cols / 2, b_mn ? 128 : 32, 64);
+  ok = ok && make_f32_map(&nm.scales, W.scales, W.rows, W.cols / 64, 4, 64);
+  if (K2 > 0) {
+    ok = ok && make_map(&nm.a2, *A2, 128) && make_map(&tb2, *B2, 64);
+  } else {
+    nm.a2 = ta;
+    tb2 = ta;
+  }
+  if (!ok) {
+    *why = "gemm_nf4: cuTensorMapEncodeTiled failed";
+    return cudaErrorInvalidValue;
+  }
+  OutMaps om;
+  if (!make_out_maps(&om, epi, M, N, OutStageBytes(NF4_BN))) {
+    *why = "gemm_nf4: outputs need 16-byte aligned rows";
+    return cudaErrorInvalidValue;
+  }
+  GemmParams p;
+  p.M = M;
+  p.N = N;
+  p.K = K1 + K2;
+  p.m_tiles = (M + BM - 1) / BM;
+  p.n_tiles = swiglu ? (N + 127) / 128 : (N + NF4_BN - 1) / NF4_BN;
+  p.kb_main = K1 / BK;
+  p.k_blocks = p.kb_main + (K2 > 0 ? 1 : 0);
+  p.swiglu_half = epi.half;
+  p.group = raster_group(p.m_tiles, p.n_tiles, BM, swiglu ? 256 : NF4_BN, p.K);
+  p.sq_slots = 8;
+  p.epi = epi;
+  p.epi.sq_count = nullptr;
+  p.err = err;
+  if (epi.sq_part) {
+    if (epi.kind != EPI_F32 || !epi.sq_count) {
+      *why = "gemm_nf4: squared-sum slots need the fp32 epilogue and a count";
+      return cudaErrorInvalidValue;
+    }
+    *epi.sq_count = static_cast<int64_t>(p.m_tiles) * p.n_tiles * p.sq_slots;
+  }
+#define RDT_NF4_CASE(BMJ, E) \
+  if (b_mn == (BMJ) && epi.kind == (E)) return launch_nf4<BMJ, E>(ta, tb2, nm, om, p, s);
+  // forward through W: y = x W^T (K-major)
+  RDT_NF4_CASE(0, EPI_F32)
+  RDT_NF4_CASE(0, EPI_F32_RESID)
+  RDT_NF4_CASE(0, EPI_SWIGLU)
+  // activation gradients through W: dX = dY W (MN-major)
+  RDT_NF4_CASE(1, EPI_F32)
+  RDT_NF4_CASE(1, EPI_BF16)
+  RDT_NF4_CASE(1, EPI_SWIGLU_BWD)
+#undef RDT_NF4_CASE
+  *why = "gemm_nf4: unsupported operand-major / epilogue combination";
   return cudaErrorInvalidValue;
 }
 

@@ -59,6 +59,24 @@ struct Mat {
 cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N, int K,
                  const Epi& epi, int* err, cudaStream_t s, const char** why);
 
+// A frozen NF4 weight W [rows, cols] (row-major, two 4-bit codes per byte,
+// element 2j in the low nibble of byte j; one fp32 scale per 64 consecutive
+// elements of a row; cols % 256 == 0).
+struct Nf4Mat {
+  const uint8_t* codes;
+  const float* scales;
+  int64_t rows, cols;
+};
+
+// C[M, N] = A' B'^T with B decoded from NF4 on the way: !b_mn: B = W (N =
+// rows, K = cols; y = x W^T); b_mn: B = W^T (N = cols, K = rows; dX = dY W).
+// A is K-major bf16 [M, K]. K2 > 0 (<= 64) appends a tail of ordinary bf16
+// operands: A2 [M, K2] K-major and B2 ([N, K2] K-major when !b_mn, [K2, N]
+// MN-major when b_mn). Epilogues as gemm() (F32, F32_RESID, SWIGLU forward;
+// F32, BF16, SWIGLU_BWD backward).
+cudaError_t gemm_nf4(const Mat& A, const Nf4Mat& W, bool b_mn, const Mat* A2, const Mat* B2,
+                     int K2, int M, const Epi& epi, int* err, cudaStream_t s, const char** why);
+
 // (max, sum exp) partials per row written by the CE epilogue: one per half of
 // every 256-wide N tile.
 inline int ce_partials_per_row(int N) { return 2 * ((N + 255) / 256); }

@@ -25,7 +25,7 @@ EXPORTS = (
     "rdt_fused_cross_entropy", "rdt_sq_sum", "rdt_clip_scale", "rdt_adamw_step",
     "rdt_gemm", "rdt_cast_bf16", "rdt_last_error", "rdt_device_error",
     "rdt_gemm_timing_arm", "rdt_gemm_timing_disarm", "rdt_launch_count",
-    "rdt_sq_sum_noalloc",
+    "rdt_sq_sum_noalloc", "rdt_gemm_nf4",
 )
 
 
@@ -70,6 +70,8 @@ def _load() -> ctypes.CDLL:
         "rdt_clip_scale": (I32, [P, F32, P, P, P]),
         "rdt_adamw_step": (I32, [P, P, P, P, I64, P, P, I32, F32, F32, F32, F32, F32, P, P]),
         "rdt_gemm": (I32, [P, I32, I64, P, I32, I64, I32, I32, I32, P, I64, P]),
+        "rdt_gemm_nf4": (I32, [P, I64, P, P, I64, I64, I32, P, I64, P, I64, I32, I32, P, I64,
+                               P]),
         "rdt_cast_bf16": (I32, [P, P, I64, P]),
         "rdt_last_error": (ctypes.c_char_p, []),
         "rdt_device_error": (I32, [P]),
@@ -211,6 +213,16 @@ def gemm(a, a_mn, b, b_mn, M, N, K, c, stream=None):
     """c[M, N] = a' b'^T (see include/rdt.h); a, b bf16 2-D, c fp32 2-D."""
     _check(lib().rdt_gemm(_ptr(a), int(a_mn), a.stride(0), _ptr(b), int(b_mn), b.stride(0), M, N,
                           K, _ptr(c), c.stride(0), _stream(stream)))
+
+
+def gemm_nf4(a, codes, scales, w_rows, w_cols, b_mn, c, a2=None, b2=None, stream=None):
+    """c[M, N] = a B^T (+ a2 b2'^T) with B decoded from NF4 (see include/rdt.h);
+    a, a2, b2 bf16 2-D, codes uint8, scales fp32, c fp32 2-D."""
+    k2 = 0 if a2 is None else a2.shape[1]
+    _check(lib().rdt_gemm_nf4(_ptr(a), a.stride(0), _ptr(codes), _ptr(scales), w_rows, w_cols,
+                              int(b_mn), _ptr(a2), 0 if a2 is None else a2.stride(0), _ptr(b2),
+                              0 if b2 is None else b2.stride(0), k2, a.shape[0], _ptr(c),
+                              c.stride(0), _stream(stream)))
 
 
 def cast_bf16(src, dst, n=None, stream=None):
