@@ -250,6 +250,82 @@ rdt_status rdt_gemm_nf4(const rdt_bf16* A, int64_t lda, const uint8_t* codes,
 rdt_status rdt_cast_bf16(const float* src, rdt_bf16* dst, int64_t n, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * NF4-frozen block with LoRA adapters (CudaNf4TransformerBlock in
+ * cuda_block.rs: the seven projection weights frozen as packed 4-bit
+ * NormalFloat codes, one fp32 scale per block of 64 consecutive elements of
+ * the row-major [out, in] weight; lora_scale = alpha / rank as in
+ * cuda_trainer.rs; lora_forward in wgpu_trainer.rs: y = x W^T +
+ * (alpha/rank) (x A^T) B^T with A [rank, in], B [out, rank]). The block is
+ * the block above with every projection replaced by that LoRA projection on
+ * the dequantized W = level[code] * scale (levels: the 16 NormalFloat-4
+ * values of QLoRA); the norm gains are frozen and only the adapters get
+ * gradients.
+ *
+ * Constraints (rdt_nf4_check): rdt_check_config's, hidden, n_heads*head_dim
+ * and intermediate multiples of 256, n_kv_heads*head_dim a multiple of 64,
+ * rank 8 or 16 (the stacked Q/K/V adapters, 3*rank columns, fit one 64-deep
+ * GEMM step).
+ *
+ * codes   uint8, the seven projections' packed codes back to back in the
+ *         order q, k, v, o, gate, up, down, each [out, in/2] row-major with
+ *         element 2j in the low nibble of byte j (rdt_nf4_offsets: byte offsets)
+ * scales  fp32, the seven projections' block scales in the same order, each
+ *         [out, in/64] (rdt_nf4_offsets: element offsets)
+ * gains   fp32 [hidden | hidden | head_dim | head_dim]: input-norm,
+ *         post-attention-norm, q-norm and k-norm gains (frozen)
+ * lora    fp32 adapters, tensors RDT_LORA_* back to back (rdt_lora_param_offsets);
+ *         A's are [rank, in], B's [out, rank]
+ * shadow  bf16 operand copy of the adapters the GEMMs read, rdt_lora_shadow_count
+ *         elements, written by rdt_lora_shadow from lora (call it after every
+ *         update of lora)
+ * ------------------------------------------------------------------------- */
+enum {
+  RDT_LORA_A_Q, RDT_LORA_A_K, RDT_LORA_A_V, RDT_LORA_A_O, RDT_LORA_A_G, RDT_LORA_A_U,
+  RDT_LORA_A_D, RDT_LORA_B_Q, RDT_LORA_B_K, RDT_LORA_B_V, RDT_LORA_B_O, RDT_LORA_B_G,
+  RDT_LORA_B_U, RDT_LORA_B_D, RDT_LORA_NTENSORS
+};
+
+/* RDT_OK when cfg and rank meet the constraints above, else RDT_EINVAL. */
+rdt_status rdt_nf4_check(const rdt_config* cfg, int32_t rank);
+/* Total code bytes / scale elements of the seven projections (-1 if invalid). */
+int64_t rdt_nf4_code_bytes(const rdt_config* cfg);
+int64_t rdt_nf4_scale_count(const rdt_config* cfg);
+/* Host arrays of 7 entries (q, k, v, o, gate, up, down): byte offsets into
+ * codes and element offsets into scales. */
+rdt_status rdt_nf4_offsets(const rdt_config* cfg, int64_t* code_offsets, int64_t* scale_offsets);
+/* Adapter layout: element count; host arrays of RDT_LORA_NTENSORS offsets and counts. */
+int64_t rdt_lora_param_count(const rdt_config* cfg, int32_t rank);
+rdt_status rdt_lora_param_offsets(const rdt_config* cfg, int32_t rank, int64_t* offsets,
+                                  int64_t* counts);
+/* bf16 elements of the adapters' operand copy; rdt_lora_shadow writes it. */
+int64_t rdt_lora_shadow_count(const rdt_config* cfg, int32_t rank);
+rdt_status rdt_lora_shadow(const rdt_config* cfg, int32_t rank, const float* lora,
+                           rdt_bf16* shadow, void* stream);
+/* Saved-activation and scratch bytes of the NF4 block calls (256-byte aligned). */
+size_t rdt_nf4_saved_bytes(const rdt_config* cfg, int32_t rank, int32_t batch, int32_t seq);
+size_t rdt_nf4_workspace_bytes(const rdt_config* cfg, int32_t rank, int32_t batch, int32_t seq);
+
+/* Forward of the NF4 + LoRA block: x, y fp32 [batch*seq, hidden] (y must not
+ * alias x); saved written for rdt_nf4_block_backward. */
+rdt_status rdt_nf4_block_forward(const rdt_config* cfg, int32_t rank, float alpha, int32_t batch,
+                                 int32_t seq, const uint8_t* codes, const float* scales,
+                                 const float* gains, const rdt_bf16* shadow, const float* x,
+                                 float* y, void* saved, size_t saved_bytes, void* ws,
+                                 size_t ws_bytes, void* stream);
+/* Backward of the NF4 + LoRA block: dx fp32 [batch*seq, hidden] (may alias
+ * dy); lora_grads fp32 in the adapter layout, every tensor overwritten;
+ * grad_sq optional (may be null): *grad_sq += the sum of the squares of the
+ * adapter gradients (fixed summation order). The frozen weights and gains get
+ * no gradient. */
+rdt_status rdt_nf4_block_backward(const rdt_config* cfg, int32_t rank, float alpha,
+                                  int32_t batch, int32_t seq, const uint8_t* codes,
+                                  const float* scales, const float* gains,
+                                  const rdt_bf16* shadow, const float* x, const void* saved,
+                                  size_t saved_bytes, const float* dy, float* dx,
+                                  float* lora_grads, double* grad_sq, void* ws, size_t ws_bytes,
+                                  void* stream);
+
+/* ---------------------------------------------------------------------------
  * Measurement hooks (host-side bookkeeping only; no device memory).
  * rdt_gemm_timing_arm: while armed, the i-th tensor-core GEMM launch (any
  *   entry point) records the caller-created cudaEvent_t events[2i] on its

@@ -260,6 +260,146 @@ void gemm_timing_after(cudaStream_t s, int64_t slot) {
 }
 }  // namespace rdt
 
+// ------------------------------------------------------- NF4 + LoRA layout
+namespace {
+
+bool nf4_ok(const rdt_config* c, int rank, std::string* why) {
+  if (!cfg_ok(c, why)) return false;
+  const Dims m = dims_of(c);
+  if (m.H % 256 || m.qd % 256 || m.I % 256) {
+    *why = "NF4: hidden, n_heads*head_dim and intermediate must be multiples of 256";
+    return false;
+  }
+  if (m.kd % 64) {
+    *why = "NF4: n_kv_heads*head_dim must be a multiple of 64";
+    return false;
+  }
+  if (rank != 8 && rank != 16) {
+    *why = "NF4: LoRA rank must be 8 or 16";
+    return false;
+  }
+  return true;
+}
+
+// Projections in storage order: q, k, v, o, gate, up, down as [out, in].
+void nf4_dims(const Dims& m, int64_t* out, int64_t* in) {
+  const int64_t o[7] = {m.qd, m.kd, m.kd, m.H, m.I, m.I, m.H};
+  const int64_t i[7] = {m.H, m.H, m.H, m.qd, m.H, m.H, m.I};
+  for (int k = 0; k < 7; ++k) {
+    out[k] = o[k];
+    in[k] = i[k];
+  }
+}
+void nf4_layout(const Dims& m, int64_t* code_off, int64_t* scale_off, int64_t* code_total,
+                int64_t* scale_total) {
+  int64_t out[7], in[7];
+  nf4_dims(m, out, in);
+  int64_t c = 0, sc = 0;
+  for (int k = 0; k < 7; ++k) {
+    if (code_off) code_off[k] = c;
+    if (scale_off) scale_off[k] = sc;
+    c += out[k] * in[k] / 2;
+    sc += out[k] * in[k] / 64;
+  }
+  if (code_total) *code_total = c;
+  if (scale_total) *scale_total = sc;
+}
+void lora_layout(const Dims& m, int64_t r, int64_t* off, int64_t* cnt) {
+  int64_t out[7], in[7];
+  nf4_dims(m, out, in);
+  int64_t c[RDT_LORA_NTENSORS];
+  for (int k = 0; k < 7; ++k) {
+    c[RDT_LORA_A_Q + k] = r * in[k];
+    c[RDT_LORA_B_Q + k] = out[k] * r;
+  }
+  int64_t o = 0;
+  for (int k = 0; k < RDT_LORA_NTENSORS; ++k) {
+    if (off) off[k] = o;
+    if (cnt) cnt[k] = c[k];
+    o += c[k];
+  }
+}
+// Shadow (bf16): the A's as in the adapter layout, then the B stacks:
+// [Bq; Bk; Bv] block diagonal [nqkv, 3r], Bo [H, r], [Bg; Bu] block diagonal
+// [2I, 2r], Bd [H, r].
+struct LoraShadow {
+  const bf16 *a_qkv, *a_o, *a_gu, *a_d, *b_qkv, *b_o, *b_gu, *b_d;
+  int64_t total;
+};
+LoraShadow lora_shadow_layout(const Dims& m, int64_t r, const bf16* base) {
+  int64_t off[RDT_LORA_NTENSORS], cnt[RDT_LORA_NTENSORS];
+  lora_layout(m, r, off, cnt);
+  const int64_t a_end = off[RDT_LORA_B_Q];
+  LoraShadow t;
+  t.a_qkv = base + off[RDT_LORA_A_Q];
+  t.a_o = base + off[RDT_LORA_A_O];
+  t.a_gu = base + off[RDT_LORA_A_G];
+  t.a_d = base + off[RDT_LORA_A_D];
+  int64_t o = a_end;
+  t.b_qkv = base + o;
+  o += m.nqkv * 3 * r;
+  t.b_o = base + o;
+  o += m.H * r;
+  t.b_gu = base + o;
+  o += 2 * m.I * 2 * r;
+  t.b_d = base + o;
+  o += m.H * r;
+  t.total = o;
+  return t;
+}
+
+// Saved by the NF4 forward beyond the block's: the scaled down-projections
+// U = s x A^T of the four GEMM inputs (bf16 [T, 3r], [T, r], [T, 2r], [T, r]).
+struct Nf4Saved {
+  bf16 *u_qkv, *u_o, *u_gu, *u_d;
+};
+size_t carve_nf4_saved(const Dims& m, int64_t r, int64_t B, int64_t S, void* base, Saved* sv,
+                       Nf4Saved* nv) {
+  const size_t head = carve_saved(m, B, S, base, sv);
+  const int64_t T = B * S;
+  Carver c(base ? static_cast<uint8_t*>(base) + head : nullptr);
+  Nf4Saved t;
+  t.u_qkv = c.take<bf16>(T * 3 * r);
+  t.u_o = c.take<bf16>(T * r);
+  t.u_gu = c.take<bf16>(T * 2 * r);
+  t.u_d = c.take<bf16>(T * r);
+  if (nv) *nv = t;
+  return head + c.off;
+}
+// Scratch of the NF4 backward beyond the block's: dU = s dY B per GEMM and
+// sinks for the frozen gains' gradients.
+struct Nf4Ws {
+  bf16 *du_qkv, *du_o, *du_gu, *du_d;
+  float* gain_sink;
+  double* sqp;  // squared-sum slots of the adapter-gradient GEMMs
+};
+// Squared-sum slots the fourteen adapter-gradient GEMMs write at most.
+int64_t lora_sq_slots_bound(const Dims& m, int64_t r) {
+  const int R = (int)r;
+  return gemm_sq_slots_bound((int)m.H, R) + gemm_sq_slots_bound(R, (int)m.I) +
+         2 * gemm_sq_slots_bound((int)m.I, R) + gemm_sq_slots_bound(2 * R, (int)m.H) +
+         gemm_sq_slots_bound((int)m.H, R) + gemm_sq_slots_bound(R, (int)m.qd) +
+         gemm_sq_slots_bound((int)m.qd, R) + 2 * gemm_sq_slots_bound((int)m.kd, R) +
+         gemm_sq_slots_bound(3 * R, (int)m.H);
+}
+size_t carve_nf4_ws(const Dims& m, int64_t r, int64_t B, int64_t S, void* base, BlockWs* wk,
+                    Nf4Ws* nw) {
+  const size_t head = carve_block_ws(m, B, S, base, wk);
+  const int64_t T = B * S;
+  Carver c(base ? static_cast<uint8_t*>(base) + head : nullptr);
+  Nf4Ws t;
+  t.du_qkv = c.take<bf16>(T * 3 * r);
+  t.du_o = c.take<bf16>(T * r);
+  t.du_gu = c.take<bf16>(T * 2 * r);
+  t.du_d = c.take<bf16>(T * r);
+  t.gain_sink = c.take<float>(2 * m.H + 2 * m.d);
+  t.sqp = c.take<double>(lora_sq_slots_bound(m, r));
+  if (nw) *nw = t;
+  return head + c.off;
+}
+
+}  // namespace
+
 // =========================================================================
 extern "C" {
 
@@ -778,6 +918,397 @@ rdt_status rdt_device_error(int32_t* code) {
   const int zero = 0;
   RDT_CHECK_CUDA(cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)));
   *code = v;
+  return RDT_OK;
+}
+
+// ------------------------------------------------- NF4 + LoRA block: layout
+rdt_status rdt_nf4_check(const rdt_config* cfg, int32_t rank) {
+  std::string why;
+  if (!nf4_ok(cfg, rank, &why)) return fail(RDT_EINVAL, "%s", why.c_str());
+  return RDT_OK;
+}
+
+int64_t rdt_nf4_code_bytes(const rdt_config* cfg) {
+  std::string why;
+  if (!nf4_ok(cfg, 16, &why)) return -1;
+  int64_t c;
+  nf4_layout(dims_of(cfg), nullptr, nullptr, &c, nullptr);
+  return c;
+}
+
+int64_t rdt_nf4_scale_count(const rdt_config* cfg) {
+  std::string why;
+  if (!nf4_ok(cfg, 16, &why)) return -1;
+  int64_t sc;
+  nf4_layout(dims_of(cfg), nullptr, nullptr, nullptr, &sc);
+  return sc;
+}
+
+rdt_status rdt_nf4_offsets(const rdt_config* cfg, int64_t* code_offsets, int64_t* scale_offsets) {
+  std::string why;
+  if (!nf4_ok(cfg, 16, &why)) return fail(RDT_EINVAL, "%s", why.c_str());
+  if (!code_offsets || !scale_offsets) return fail(RDT_EINVAL, "null pointer");
+  nf4_layout(dims_of(cfg), code_offsets, scale_offsets, nullptr, nullptr);
+  return RDT_OK;
+}
+
+int64_t rdt_lora_param_count(const rdt_config* cfg, int32_t rank) {
+  std::string why;
+  if (!nf4_ok(cfg, rank, &why)) return -1;
+  int64_t off[RDT_LORA_NTENSORS], cnt[RDT_LORA_NTENSORS];
+  lora_layout(dims_of(cfg), rank, off, cnt);
+  return off[RDT_LORA_NTENSORS - 1] + cnt[RDT_LORA_NTENSORS - 1];
+}
+
+rdt_status rdt_lora_param_offsets(const rdt_config* cfg, int32_t rank, int64_t* offsets,
+                                  int64_t* counts) {
+  std::string why;
+  if (!nf4_ok(cfg, rank, &why)) return fail(RDT_EINVAL, "%s", why.c_str());
+  if (!offsets || !counts) return fail(RDT_EINVAL, "null pointer");
+  lora_layout(dims_of(cfg), rank, offsets, counts);
+  return RDT_OK;
+}
+
+int64_t rdt_lora_shadow_count(const rdt_config* cfg, int32_t rank) {
+  std::string why;
+  if (!nf4_ok(cfg, rank, &why)) return -1;
+  return lora_shadow_layout(dims_of(cfg), rank, nullptr).total;
+}
+
+rdt_status rdt_lora_shadow(const rdt_config* cfg, int32_t rank, const float* lora,
+                           rdt_bf16* shadow, void* stream) {
+  std::string why;
+  if (!nf4_ok(cfg, rank, &why)) return fail(RDT_EINVAL, "%s", why.c_str());
+  if (!lora || !shadow) return fail(RDT_EINVAL, "null pointer");
+  if (!aligned16(lora) || !aligned16(shadow)) return fail(RDT_EINVAL, "pointers must be 16-byte aligned");
+  const Dims m = dims_of(cfg);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bf16* base = reinterpret_cast<bf16*>(shadow);
+  const LoraShadow L = lora_shadow_layout(m, rank, base);
+  int64_t off[RDT_LORA_NTENSORS], cnt[RDT_LORA_NTENSORS];
+  lora_layout(m, rank, off, cnt);
+  // the A's keep their layout; the B's become the stacked tail operands
+  RDT_CHECK_CUDA(cast_bf16(lora, base, off[RDT_LORA_B_Q], s));
+  {
+    const float* p[3] = {lora + off[RDT_LORA_B_Q], lora + off[RDT_LORA_B_K], lora + off[RDT_LORA_B_V]};
+    const int64_t rows[3] = {m.qd, m.kd, m.kd};
+    RDT_CHECK_CUDA(lora_bstack(p, rows, 3, rank, const_cast<bf16*>(L.b_qkv), s));
+  }
+  RDT_CHECK_CUDA(cast_bf16(lora + off[RDT_LORA_B_O], const_cast<bf16*>(L.b_o), m.H * rank, s));
+  {
+    const float* p[2] = {lora + off[RDT_LORA_B_G], lora + off[RDT_LORA_B_U]};
+    const int64_t rows[2] = {m.I, m.I};
+    RDT_CHECK_CUDA(lora_bstack(p, rows, 2, rank, const_cast<bf16*>(L.b_gu), s));
+  }
+  RDT_CHECK_CUDA(cast_bf16(lora + off[RDT_LORA_B_D], const_cast<bf16*>(L.b_d), m.H * rank, s));
+  return RDT_OK;
+}
+
+size_t rdt_nf4_saved_bytes(const rdt_config* cfg, int32_t rank, int32_t batch, int32_t seq) {
+  std::string why;
+  if (!nf4_ok(cfg, rank, &why) || batch < 1 || seq < 1) return 0;
+  return carve_nf4_saved(dims_of(cfg), rank, batch, seq, nullptr, nullptr, nullptr);
+}
+
+size_t rdt_nf4_workspace_bytes(const rdt_config* cfg, int32_t rank, int32_t batch, int32_t seq) {
+  std::string why;
+  if (!nf4_ok(cfg, rank, &why) || batch < 1 || seq < 1) return 0;
+  return carve_nf4_ws(dims_of(cfg), rank, batch, seq, nullptr, nullptr, nullptr);
+}
+
+// ------------------------------------------------ NF4 + LoRA block: forward
+rdt_status rdt_nf4_block_forward(const rdt_config* cfg, int32_t rank, float alpha, int32_t batch,
+                                 int32_t seq, const uint8_t* codes, const float* scales,
+                                 const float* gains, const rdt_bf16* shadow, const float* x,
+                                 float* y, void* saved, size_t saved_bytes, void* ws,
+                                 size_t ws_bytes, void* stream) {
+  std::string why;
+  if (!nf4_ok(cfg, rank, &why)) return fail(RDT_EINVAL, "%s", why.c_str());
+  if (batch < 1 || seq < 1) return fail(RDT_EINVAL, "batch and seq must be >= 1");
+  if (!(alpha == alpha)) return fail(RDT_EINVAL, "alpha must be a number");
+  if (!codes || !scales || !gains || !shadow || !x || !y || !saved || !ws)
+    return fail(RDT_EINVAL, "null pointer");
+  if (!aligned16(codes) || !aligned16(scales) || !aligned16(gains) || !aligned16(shadow) ||
+      !aligned16(x) || !aligned16(y) || (reinterpret_cast<uintptr_t>(saved) & 255) ||
+      (reinterpret_cast<uintptr_t>(ws) & 255))
+    return fail(RDT_EINVAL, "pointers must be 16-byte (saved/ws 256-byte) aligned");
+  if (x == y) return fail(RDT_EINVAL, "y must not alias x");
+  const Dims m = dims_of(cfg);
+  const int64_t r = rank;
+  if (saved_bytes < carve_nf4_saved(m, r, batch, seq, nullptr, nullptr, nullptr))
+    return fail(RDT_EINVAL, "saved buffer too small");
+  if (ws_bytes < carve_nf4_ws(m, r, batch, seq, nullptr, nullptr, nullptr))
+    return fail(RDT_EINVAL, "workspace too small");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* err = device_error_ptr();
+  const int T = batch * seq;
+  const float sc = alpha / static_cast<float>(rank);
+  Saved sv;
+  Nf4Saved nv;
+  carve_nf4_saved(m, r, batch, seq, saved, &sv, &nv);
+  BlockWs wk;
+  carve_nf4_ws(m, r, batch, seq, ws, &wk, nullptr);
+  const LoraShadow L = lora_shadow_layout(m, r, reinterpret_cast<const bf16*>(shadow));
+  int64_t co[7], so[7];
+  nf4_layout(m, co, so, nullptr, nullptr);
+  auto W = [&](int k, int64_t rows, int64_t cols) {
+    return Nf4Mat{codes + co[k], scales + so[k], rows, cols};
+  };
+  const float *g_attn = gains, *g_ffn = gains + m.H, *g_q = gains + 2 * m.H,
+              *g_k = gains + 2 * m.H + m.d;
+  // U = s x A^T, the adapters' scaled down-projection (bf16 [T, n])
+  auto down = [&](const bf16* xin, int64_t in, const bf16* a, int64_t n, bf16* u) -> rdt_status {
+    Epi e;
+    e.kind = EPI_BF16;
+    e.out = u;
+    e.ld_out = n;
+    e.scale = sc;
+    RDT_GEMM(Mat{xin, T, in, in}, false, Mat{a, n, in, in}, false, T, (int)n, (int)in, e, err, s);
+    return RDT_OK;
+  };
+  rdt_status st;
+
+  // input RMSNorm
+  RDT_CHECK_CUDA(rmsnorm_fwd(x, g_attn, sv.xn, sv.rstd1, T, (int)m.H, cfg->rms_eps, s));
+  // qkv = xn [Wq; Wk; Wv]^T + U_qkv [Bq 0 0; 0 Bk 0; 0 0 Bv]^T
+  if ((st = down(sv.xn, m.H, L.a_qkv, 3 * r, nv.u_qkv)) != RDT_OK) return st;
+  {
+    Epi e;
+    e.kind = EPI_F32;
+    e.out = sv.qkv;
+    e.ld_out = m.nqkv;
+    const Mat a2{nv.u_qkv, T, 3 * r, 3 * r}, b2{L.b_qkv, m.nqkv, 3 * r, 3 * r};
+    RDT_GEMM_NF4(Mat{sv.xn, T, m.H, m.H}, W(0, m.nqkv, m.H), false, &a2, &b2, (int)(3 * r), T, e,
+                 err, s);
+  }
+  // per-head QK RMSNorm + RoPE-neox, causal GQA attention
+  RDT_CHECK_CUDA(rope_table(wk.cs, seq, (int)m.d, cfg->rope_theta, s));
+  RDT_CHECK_CUDA(qknorm_rope_fwd(sv.qkv, m.nqkv, sv.qr, sv.kr, sv.vb, sv.rstd_q, sv.rstd_k, g_q,
+                                 g_k, wk.cs, T, seq, (int)m.nh, (int)m.nkv, (int)m.d,
+                                 cfg->rms_eps, s));
+  if (attn_tc_supported((int)m.d, false))
+    RDT_CHECK_CUDA(attn_fwd_tc(sv.qr, m.qd, sv.kr, m.kd, sv.vb, m.kd, sv.o, sv.lse, batch, seq,
+                               (int)m.nh, (int)m.nkv, (int)m.d, err, s));
+  else
+    RDT_CHECK_CUDA(attn_fwd(sv.qr, m.qd, sv.kr, m.kd, sv.vb, m.kd, sv.o, sv.lse, batch, seq,
+                            (int)m.nh, (int)m.nkv, (int)m.d, s));
+  // r1 = x + o Wo^T + U_o Bo^T
+  if ((st = down(sv.o, m.qd, L.a_o, r, nv.u_o)) != RDT_OK) return st;
+  {
+    Epi e;
+    e.kind = EPI_F32_RESID;
+    e.out = sv.r1;
+    e.ld_out = m.H;
+    e.resid = x;
+    e.ld_resid = m.H;
+    const Mat a2{nv.u_o, T, r, r}, b2{L.b_o, m.H, r, r};
+    RDT_GEMM_NF4(Mat{sv.o, T, m.qd, m.qd}, W(3, m.H, m.qd), false, &a2, &b2, (int)r, T, e, err, s);
+  }
+  // post-attention RMSNorm
+  RDT_CHECK_CUDA(rmsnorm_fwd(sv.r1, g_ffn, sv.xn2, sv.rstd2, T, (int)m.H, cfg->rms_eps, s));
+  // [g | u] = xn2 [Wg; Wu]^T + U_gu [Bg 0; 0 Bu]^T with the SwiGLU epilogue
+  if ((st = down(sv.xn2, m.H, L.a_gu, 2 * r, nv.u_gu)) != RDT_OK) return st;
+  {
+    Epi e;
+    e.kind = EPI_SWIGLU;
+    e.out = sv.gu;
+    e.ld_out = 2 * m.I;
+    e.out2 = sv.s;
+    e.ld_out2 = m.I;
+    e.half = (int)m.I;
+    const Mat a2{nv.u_gu, T, 2 * r, 2 * r}, b2{L.b_gu, 2 * m.I, 2 * r, 2 * r};
+    RDT_GEMM_NF4(Mat{sv.xn2, T, m.H, m.H}, W(4, 2 * m.I, m.H), false, &a2, &b2, (int)(2 * r), T, e,
+                 err, s);
+  }
+  // y = r1 + s Wd^T + U_d Bd^T
+  if ((st = down(sv.s, m.I, L.a_d, r, nv.u_d)) != RDT_OK) return st;
+  {
+    Epi e;
+    e.kind = EPI_F32_RESID;
+    e.out = y;
+    e.ld_out = m.H;
+    e.resid = sv.r1;
+    e.ld_resid = m.H;
+    const Mat a2{nv.u_d, T, r, r}, b2{L.b_d, m.H, r, r};
+    RDT_GEMM_NF4(Mat{sv.s, T, m.I, m.I}, W(6, m.H, m.I), false, &a2, &b2, (int)r, T, e, err, s);
+  }
+  return RDT_OK;
+}
+
+// ----------------------------------------------- NF4 + LoRA block: backward
+rdt_status rdt_nf4_block_backward(const rdt_config* cfg, int32_t rank, float alpha,
+                                  int32_t batch, int32_t seq, const uint8_t* codes,
+                                  const float* scales, const float* gains,
+                                  const rdt_bf16* shadow, const float* x, const void* saved,
+                                  size_t saved_bytes, const float* dy, float* dx,
+                                  float* lora_grads, double* grad_sq, void* ws, size_t ws_bytes,
+                                  void* stream) {
+  std::string why;
+  if (!nf4_ok(cfg, rank, &why)) return fail(RDT_EINVAL, "%s", why.c_str());
+  if (batch < 1 || seq < 1) return fail(RDT_EINVAL, "batch and seq must be >= 1");
+  if (!(alpha == alpha)) return fail(RDT_EINVAL, "alpha must be a number");
+  if (!codes || !scales || !gains || !shadow || !x || !saved || !dy || !dx || !lora_grads || !ws)
+    return fail(RDT_EINVAL, "null pointer");
+  if (!aligned16(codes) || !aligned16(scales) || !aligned16(gains) || !aligned16(shadow) ||
+      !aligned16(x) || !aligned16(dy) || !aligned16(dx) || !aligned16(lora_grads) ||
+      (reinterpret_cast<uintptr_t>(saved) & 255) || (reinterpret_cast<uintptr_t>(ws) & 255))
+    return fail(RDT_EINVAL, "pointers must be 16-byte (saved/ws 256-byte) aligned");
+  const Dims m = dims_of(cfg);
+  const int64_t r = rank;
+  if (saved_bytes < carve_nf4_saved(m, r, batch, seq, nullptr, nullptr, nullptr))
+    return fail(RDT_EINVAL, "saved buffer too small");
+  if (ws_bytes < carve_nf4_ws(m, r, batch, seq, nullptr, nullptr, nullptr))
+    return fail(RDT_EINVAL, "workspace too small");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* err = device_error_ptr();
+  const int T = batch * seq;
+  const float sc = alpha / static_cast<float>(rank);
+  Saved sv;
+  Nf4Saved nv;
+  carve_nf4_saved(m, r, batch, seq, const_cast<void*>(saved), &sv, &nv);
+  BlockWs wk;
+  Nf4Ws nw;
+  carve_nf4_ws(m, r, batch, seq, ws, &wk, &nw);
+  const LoraShadow L = lora_shadow_layout(m, r, reinterpret_cast<const bf16*>(shadow));
+  int64_t co[7], so[7];
+  nf4_layout(m, co, so, nullptr, nullptr);
+  auto W = [&](int k, int64_t rows, int64_t cols) {
+    return Nf4Mat{codes + co[k], scales + so[k], rows, cols};
+  };
+  int64_t lo[RDT_LORA_NTENSORS], lc[RDT_LORA_NTENSORS];
+  lora_layout(m, r, lo, lc);
+  float* G = lora_grads;
+  const float *g_attn = gains, *g_ffn = gains + m.H, *g_q = gains + 2 * m.H,
+              *g_k = gains + 2 * m.H + m.d;
+  int64_t sq_n = 0, sq_cnt = 0;
+  // dU = s dY B (bf16 [T, n]): B as stored, [K = out, N = n]
+  auto up = [&](const bf16* dyb, int64_t out, const bf16* b, int64_t n, bf16* du) -> rdt_status {
+    Epi e;
+    e.kind = EPI_BF16;
+    e.out = du;
+    e.ld_out = n;
+    e.scale = sc;
+    RDT_GEMM(Mat{dyb, T, out, out}, false, Mat{b, out, n, n}, true, T, (int)n, (int)out, e, err,
+             s);
+    return RDT_OK;
+  };
+  // C[M, N] = P^T Q over the T tokens (P [T, M], Q [T, N] as stored), fp32 into
+  // the adapter gradient at lora_grads + off, with squared-sum slots
+  auto tn = [&](const bf16* P, int64_t M, int64_t ldp, const bf16* Q, int64_t N, int64_t ldq,
+                int tensor) -> rdt_status {
+    Epi e;
+    e.kind = EPI_F32;
+    e.out = G + lo[tensor];
+    e.ld_out = N;
+    if (grad_sq) {
+      e.sq_part = nw.sqp + sq_n;
+      e.sq_count = &sq_cnt;
+    }
+    RDT_GEMM(Mat{P, T, M, ldp}, true, Mat{Q, T, N, ldq}, true, (int)M, (int)N, T, e, err, s);
+    if (grad_sq) sq_n += sq_cnt;
+    return RDT_OK;
+  };
+  rdt_status st;
+
+  // dy as a bf16 GEMM operand
+  RDT_CHECK_CUDA(cast_bf16(dy, wk.dy_b, (int64_t)T * m.H, s));
+  // down projection: ds = dy Wd + dU_d Ad with the SwiGLU backward in the epilogue
+  if ((st = up(wk.dy_b, m.H, L.b_d, r, nw.du_d)) != RDT_OK) return st;
+  {
+    Epi e;
+    e.kind = EPI_SWIGLU_BWD;
+    e.out = wk.dgu;
+    e.ld_out = 2 * m.I;
+    e.aux = sv.gu;
+    e.ld_aux = 2 * m.I;
+    e.half = (int)m.I;
+    const Mat a2{nw.du_d, T, r, r}, b2{L.a_d, r, m.I, m.I};
+    RDT_GEMM_NF4(Mat{wk.dy_b, T, m.H, m.H}, W(6, m.H, m.I), true, &a2, &b2, (int)r, T, e, err, s);
+  }
+  // dBd = dy^T U_d, dAd = dU_d^T s
+  if ((st = tn(wk.dy_b, m.H, m.H, nv.u_d, r, r, RDT_LORA_B_D)) != RDT_OK) return st;
+  if ((st = tn(nw.du_d, r, r, sv.s, m.I, m.I, RDT_LORA_A_D)) != RDT_OK) return st;
+  // gate/up: dxn2 = [dg du] [Wg; Wu] + dU_gu [Ag; Au]
+  if ((st = up(wk.dgu, 2 * m.I, L.b_gu, 2 * r, nw.du_gu)) != RDT_OK) return st;
+  {
+    Epi e;
+    e.kind = EPI_F32;
+    e.out = wk.dxn;
+    e.ld_out = m.H;
+    const Mat a2{nw.du_gu, T, 2 * r, 2 * r}, b2{L.a_gu, 2 * r, m.H, m.H};
+    RDT_GEMM_NF4(Mat{wk.dgu, T, 2 * m.I, 2 * m.I}, W(4, 2 * m.I, m.H), true, &a2, &b2,
+                 (int)(2 * r), T, e, err, s);
+  }
+  // dBg = dg^T U_g, dBu = du^T U_u, [dAg; dAu] = dU_gu^T xn2
+  if ((st = tn(wk.dgu, m.I, 2 * m.I, nv.u_gu, r, 2 * r, RDT_LORA_B_G)) != RDT_OK) return st;
+  if ((st = tn(wk.dgu + m.I, m.I, 2 * m.I, nv.u_gu + r, r, 2 * r, RDT_LORA_B_U)) != RDT_OK)
+    return st;
+  if ((st = tn(nw.du_gu, 2 * r, 2 * r, sv.xn2, m.H, m.H, RDT_LORA_A_G)) != RDT_OK) return st;
+  // post-attention RMSNorm backward (frozen gain), identity skip added after it
+  RDT_CHECK_CUDA(rmsnorm_bwd(wk.dxn, sv.r1, sv.rstd2, g_ffn, dy, wk.dr1, wk.dr1_b, nw.gain_sink,
+                             wk.partials, T, (int)m.H, s));
+  // O projection: do = dr1 Wo + dU_o Ao (bf16)
+  if ((st = up(wk.dr1_b, m.H, L.b_o, r, nw.du_o)) != RDT_OK) return st;
+  {
+    Epi e;
+    e.kind = EPI_BF16;
+    e.out = wk.dout;
+    e.ld_out = m.qd;
+    const Mat a2{nw.du_o, T, r, r}, b2{L.a_o, r, m.qd, m.qd};
+    RDT_GEMM_NF4(Mat{wk.dr1_b, T, m.H, m.H}, W(3, m.H, m.qd), true, &a2, &b2, (int)r, T, e, err,
+                 s);
+  }
+  // dBo = dr1^T U_o, dAo = dU_o^T o
+  if ((st = tn(wk.dr1_b, m.H, m.H, nv.u_o, r, r, RDT_LORA_B_O)) != RDT_OK) return st;
+  if ((st = tn(nw.du_o, r, r, sv.o, m.qd, m.qd, RDT_LORA_A_O)) != RDT_OK) return st;
+  // attention backward
+  if (attn_tc_supported((int)m.d, true)) {
+    const int S_pad = attn_lse_pad(seq);
+    if (S_pad != seq) {
+      RDT_CHECK_CUDA(cudaMemsetAsync(wk.Dd, 0, sizeof(float) * batch * m.nh * S_pad, s));
+      RDT_CHECK_CUDA(cudaMemsetAsync(wk.lse2, 0, sizeof(float) * batch * m.nh * S_pad, s));
+    }
+    RDT_CHECK_CUDA(attn_bwd_pre(sv.o, wk.dout, sv.lse, wk.Dd, wk.lse2, batch, seq, S_pad,
+                                (int)m.nh, (int)m.d, s));
+    RDT_CHECK_CUDA(attn_bwd_tc(sv.qr, m.qd, sv.kr, m.kd, sv.vb, m.kd, wk.dout, wk.lse2, wk.Dd,
+                               wk.dq, wk.dk, wk.dqkv + m.qd + m.kd, m.nqkv, batch, seq, (int)m.nh,
+                               (int)m.nkv, (int)m.d, err, s));
+  } else {
+    RDT_CHECK_CUDA(attn_bwd_pre(sv.o, wk.dout, sv.lse, wk.Dd, nullptr, batch, seq, seq,
+                                (int)m.nh, (int)m.d, s));
+    RDT_CHECK_CUDA(cudaMemsetAsync(wk.dq, 0, sizeof(float) * T * m.qd, s));
+    RDT_CHECK_CUDA(attn_bwd(sv.qr, m.qd, sv.kr, m.kd, sv.vb, m.kd, wk.dout, sv.lse, wk.Dd, wk.dq,
+                            wk.dk, wk.dqkv + m.qd + m.kd, m.nqkv, batch, seq, (int)m.nh,
+                            (int)m.nkv, (int)m.d, s));
+  }
+  // inverse RoPE + QK-norm backward (frozen gains) -> dq, dk columns of dqkv
+  RDT_CHECK_CUDA(rope_table(wk.cs, seq, (int)m.d, cfg->rope_theta, s));
+  RDT_CHECK_CUDA(qknorm_rope_bwd(wk.dq, wk.dk, sv.qkv, m.nqkv, sv.rstd_q, sv.rstd_k, g_q, g_k,
+                                 wk.cs, wk.dqkv, nw.gain_sink + m.H, wk.partials, T, seq,
+                                 (int)m.nh, (int)m.nkv, (int)m.d, s));
+  // Q/K/V: dxn = dqkv [Wq; Wk; Wv] + dU_qkv [Aq; Ak; Av]
+  if ((st = up(wk.dqkv, m.nqkv, L.b_qkv, 3 * r, nw.du_qkv)) != RDT_OK) return st;
+  {
+    Epi e;
+    e.kind = EPI_F32;
+    e.out = wk.dxn;
+    e.ld_out = m.H;
+    const Mat a2{nw.du_qkv, T, 3 * r, 3 * r}, b2{L.a_qkv, 3 * r, m.H, m.H};
+    RDT_GEMM_NF4(Mat{wk.dqkv, T, m.nqkv, m.nqkv}, W(0, m.nqkv, m.H), true, &a2, &b2, (int)(3 * r),
+                 T, e, err, s);
+  }
+  // dBq = dq^T U_q, dBk = dk^T U_k, dBv = dv^T U_v, [dAq; dAk; dAv] = dU_qkv^T xn
+  if ((st = tn(wk.dqkv, m.qd, m.nqkv, nv.u_qkv, r, 3 * r, RDT_LORA_B_Q)) != RDT_OK) return st;
+  if ((st = tn(wk.dqkv + m.qd, m.kd, m.nqkv, nv.u_qkv + r, r, 3 * r, RDT_LORA_B_K)) != RDT_OK)
+    return st;
+  if ((st = tn(wk.dqkv + m.qd + m.kd, m.kd, m.nqkv, nv.u_qkv + 2 * r, r, 3 * r, RDT_LORA_B_V)) !=
+      RDT_OK)
+    return st;
+  if ((st = tn(nw.du_qkv, 3 * r, 3 * r, sv.xn, m.H, m.H, RDT_LORA_A_Q)) != RDT_OK) return st;
+  // input RMSNorm backward (frozen gain) + identity skip
+  RDT_CHECK_CUDA(rmsnorm_bwd(wk.dxn, x, sv.rstd1, g_attn, wk.dr1, dx, nullptr, nw.gain_sink,
+                             wk.partials, T, (int)m.H, s));
+  if (grad_sq) RDT_CHECK_CUDA(sq_reduce(nw.sqp, sq_n, nullptr, nullptr, 0, grad_sq, true, s));
   return RDT_OK;
 }
 

@@ -499,6 +499,52 @@ cudaError_t sq_reduce(const double* parts, int64_t n, const float* const* small,
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------ LoRA B stacks
+struct BPieces {
+  const float* p[3];
+  int64_t rows[3];
+};
+__global__ void lora_bstack_kernel(const BPieces bp, int np, int r, int64_t total_rows,
+                                   bf16* __restrict__ out) {
+  const int64_t cols = static_cast<int64_t>(np) * r;
+  const int64_t n = total_rows * cols;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = i / cols;
+    const int col = static_cast<int>(i % cols);
+    int64_t off = 0;
+    float v = 0.f;
+    for (int q = 0; q < np; ++q) {
+      if (row >= off && row < off + bp.rows[q]) {
+        if (col / r == q) v = bp.p[q][(row - off) * r + col % r];
+        break;
+      }
+      off += bp.rows[q];
+    }
+    out[i] = __float2bfloat16_rn(v);
+  }
+}
+
+cudaError_t lora_bstack(const float* const* pieces, const int64_t* rows, int np, int r,
+                        bf16* out, cudaStream_t s) {
+  if (np < 1 || np > 3 || r < 1) return cudaErrorInvalidValue;
+  BPieces bp = {};
+  int64_t total = 0;
+  for (int q = 0; q < np; ++q) {
+    bp.p[q] = pieces[q];
+    bp.rows[q] = rows[q];
+    total += rows[q];
+  }
+  const int64_t n = total * np * r;
+  int64_t blocks = (n + 255) / 256;
+  const int64_t cap = 8LL * num_sms();
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  note_launch();
+  lora_bstack_kernel<<<(unsigned)blocks, 256, 0, s>>>(bp, np, r, total, out);
+  return cudaGetLastError();
+}
+
 // --------------------------------------------------------------------- cast
 __global__ void cast_bf16_kernel(const float4* __restrict__ src, uint2* __restrict__ dst,
                                  int64_t n4) {

@@ -276,6 +276,10 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const OutMaps
       float v[UNIT];
 #pragma unroll
       for (int k = 0; k < UNIT; ++k) v[k] = __uint_as_float(r[j * UNIT + k]);
+      if constexpr (EPI == EPI_BF16) {
+#pragma unroll
+        for (int k = 0; k < UNIT; ++k) v[k] *= e.scale;
+      }
       if constexpr (EPI == EPI_F32) {
         // out-of-range rows and columns hold exact zeros (zero-filled operands)
         if (e.sq_part) {
@@ -1504,8 +1508,14 @@ static cudaError_t launch_nf4(const CUtensorMap& ta, const CUtensorMap& tb2, con
 
 cudaError_t gemm_nf4(const Mat& A, const Nf4Mat& W, bool b_mn, const Mat* A2, const Mat* B2,
                      int K2, int M, const Epi& epi, int* err, cudaStream_t s, const char** why) {
-  const int N = static_cast<int>(b_mn ? W.cols : W.rows);
+  const bool swiglu = epi.kind == EPI_SWIGLU;
+  // SwiGLU: W is the stacked [Wg; Wu] and N the width of one half
+  const int N = static_cast<int>(b_mn ? W.cols : (swiglu ? W.rows / 2 : W.rows));
   const int K1 = static_cast<int>(b_mn ? W.rows : W.cols);
+  if (swiglu && (epi.half != N || W.rows != 2 * static_cast<int64_t>(N) || N % 128)) {
+    *why = "gemm_nf4: SwiGLU needs W = [Wg; Wu] with half = rows / 2, a multiple of 128";
+    return cudaErrorInvalidValue;
+  }
   if (M <= 0 || N <= 0 || K1 <= 0 || K2 < 0 || K2 > BK) {
     *why = "gemm_nf4: empty problem or a tail wider than 64";
     return cudaErrorInvalidValue;
@@ -1514,7 +1524,6 @@ cudaError_t gemm_nf4(const Mat& A, const Nf4Mat& W, bool b_mn, const Mat* A2, co
     *why = "gemm_nf4: NF4 weights need cols % 256 == 0 and rows % 64 == 0";
     return cudaErrorInvalidValue;
   }
-  const bool swiglu = epi.kind == EPI_SWIGLU;
   if (swiglu && b_mn) {
     *why = "gemm_nf4: SwiGLU epilogue needs a K-major B";
     return cudaErrorInvalidValue;

@@ -40,6 +40,8 @@ struct Epi {
   // gemm() sets *sq_count to the number of slots written (tiles x 8 or 16).
   double* sq_part = nullptr;
   int64_t* sq_count = nullptr;
+  // EPI_BF16 only: out = bf16(scale * acc)
+  float scale = 1.0f;
 };
 
 // Upper bound of the squared-sum slots a gemm() of [M, N] writes.
@@ -132,6 +134,10 @@ int qknorm_bwd_partial_rows(int T, int heads);
 cudaError_t sq_reduce(const double* parts, int64_t n, const float* const* small,
                       const int64_t* small_len, int nsmall, double* out, bool accumulate,
                       cudaStream_t s);
+// out [sum of rows, np*r] bf16, block diagonal: rows of piece p (fp32
+// [rows_p, r], row-major) land in columns [p r, (p+1) r), zeros elsewhere.
+cudaError_t lora_bstack(const float* const* pieces, const int64_t* rows, int np, int r,
+                        bf16* out, cudaStream_t s);
 cudaError_t cast_bf16(const float* src, bf16* dst, int64_t n, cudaStream_t s);
 
 cudaError_t ce_finalize(const float2* part, int part_ld, int ntiles, const float* tgt_logit,

@@ -17,6 +17,9 @@ LIB_PATH = os.path.join(_HERE, "librdt.so")
 
 RDT_OK, RDT_EINVAL, RDT_ECUDA, RDT_ETIMEOUT, RDT_ENONFINITE = 0, 1, 2, 3, 4
 TENSOR_NAMES = ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "g_attn", "g_ffn", "g_q", "g_k")
+NF4_NAMES = ("wq", "wk", "wv", "wo", "wg", "wu", "wd")
+LORA_NAMES = ("a_q", "a_k", "a_v", "a_o", "a_g", "a_u", "a_d",
+              "b_q", "b_k", "b_v", "b_o", "b_g", "b_u", "b_d")
 
 EXPORTS = (
     "rdt_check_config", "rdt_block_param_count", "rdt_block_param_offsets",
@@ -25,7 +28,10 @@ EXPORTS = (
     "rdt_fused_cross_entropy", "rdt_sq_sum", "rdt_clip_scale", "rdt_adamw_step",
     "rdt_gemm", "rdt_cast_bf16", "rdt_last_error", "rdt_device_error",
     "rdt_gemm_timing_arm", "rdt_gemm_timing_disarm", "rdt_launch_count",
-    "rdt_sq_sum_noalloc", "rdt_gemm_nf4",
+    "rdt_sq_sum_noalloc", "rdt_gemm_nf4", "rdt_nf4_check", "rdt_nf4_code_bytes",
+    "rdt_nf4_scale_count", "rdt_nf4_offsets", "rdt_lora_param_count", "rdt_lora_param_offsets",
+    "rdt_lora_shadow_count", "rdt_lora_shadow", "rdt_nf4_saved_bytes", "rdt_nf4_workspace_bytes",
+    "rdt_nf4_block_forward", "rdt_nf4_block_backward",
 )
 
 
@@ -79,6 +85,20 @@ def _load() -> ctypes.CDLL:
         "rdt_gemm_timing_disarm": (I64, []),
         "rdt_launch_count": (I64, []),
         "rdt_sq_sum_noalloc": (I32, [P, P, I32, P, P]),
+        "rdt_nf4_check": (I32, [CP, I32]),
+        "rdt_nf4_code_bytes": (I64, [CP]),
+        "rdt_nf4_scale_count": (I64, [CP]),
+        "rdt_nf4_offsets": (I32, [CP, P, P]),
+        "rdt_lora_param_count": (I64, [CP, I32]),
+        "rdt_lora_param_offsets": (I32, [CP, I32, P, P]),
+        "rdt_lora_shadow_count": (I64, [CP, I32]),
+        "rdt_lora_shadow": (I32, [CP, I32, P, P, P]),
+        "rdt_nf4_saved_bytes": (SZ, [CP, I32, I32, I32]),
+        "rdt_nf4_workspace_bytes": (SZ, [CP, I32, I32, I32]),
+        "rdt_nf4_block_forward": (I32, [CP, I32, F32, I32, I32, P, P, P, P, P, P, P, SZ, P, SZ,
+                                        P]),
+        "rdt_nf4_block_backward": (I32, [CP, I32, F32, I32, I32, P, P, P, P, P, P, SZ, P, P, P,
+                                         P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -223,6 +243,83 @@ def gemm_nf4(a, codes, scales, w_rows, w_cols, b_mn, c, a2=None, b2=None, stream
                               int(b_mn), _ptr(a2), 0 if a2 is None else a2.stride(0), _ptr(b2),
                               0 if b2 is None else b2.stride(0), k2, a.shape[0], _ptr(c),
                               c.stride(0), _stream(stream)))
+
+
+# ------------------------------------------------- NF4 + LoRA block
+def nf4_check(cfg: Config, rank: int):
+    _check(lib().rdt_nf4_check(ctypes.byref(cfg), int(rank)))
+
+
+def nf4_sizes(cfg: Config) -> tuple[int, int]:
+    """(code bytes, scale elements) of the seven frozen projections."""
+    nc = lib().rdt_nf4_code_bytes(ctypes.byref(cfg))
+    ns = lib().rdt_nf4_scale_count(ctypes.byref(cfg))
+    if nc < 0 or ns < 0:
+        nf4_check(cfg, 16)
+    return nc, ns
+
+
+def nf4_offsets(cfg: Config) -> dict[str, tuple[int, int]]:
+    """{projection: (code byte offset, scale element offset)}."""
+    co = (ctypes.c_int64 * 7)()
+    so = (ctypes.c_int64 * 7)()
+    _check(lib().rdt_nf4_offsets(ctypes.byref(cfg), co, so))
+    return {n: (co[i], so[i]) for i, n in enumerate(NF4_NAMES)}
+
+
+def lora_param_count(cfg: Config, rank: int) -> int:
+    n = lib().rdt_lora_param_count(ctypes.byref(cfg), int(rank))
+    if n < 0:
+        nf4_check(cfg, rank)
+    return n
+
+
+def lora_param_offsets(cfg: Config, rank: int) -> dict[str, tuple[int, int]]:
+    off = (ctypes.c_int64 * len(LORA_NAMES))()
+    cnt = (ctypes.c_int64 * len(LORA_NAMES))()
+    _check(lib().rdt_lora_param_offsets(ctypes.byref(cfg), int(rank), off, cnt))
+    return {n: (off[i], cnt[i]) for i, n in enumerate(LORA_NAMES)}
+
+
+def lora_shadow_count(cfg: Config, rank: int) -> int:
+    n = lib().rdt_lora_shadow_count(ctypes.byref(cfg), int(rank))
+    if n < 0:
+        nf4_check(cfg, rank)
+    return n
+
+
+def lora_shadow(cfg, rank, lora, shadow, stream=None):
+    _check(lib().rdt_lora_shadow(ctypes.byref(cfg), int(rank), _ptr(lora), _ptr(shadow),
+                                 _stream(stream)))
+
+
+def nf4_saved_bytes(cfg: Config, rank: int, batch: int, seq: int) -> int:
+    return lib().rdt_nf4_saved_bytes(ctypes.byref(cfg), int(rank), batch, seq)
+
+
+def nf4_workspace_bytes(cfg: Config, rank: int, batch: int, seq: int) -> int:
+    return lib().rdt_nf4_workspace_bytes(ctypes.byref(cfg), int(rank), batch, seq)
+
+
+def nf4_block_forward(cfg, rank, alpha, batch, seq, codes, scales, gains, shadow, x, y, saved, ws,
+                      stream=None):
+    _check(lib().rdt_nf4_block_forward(ctypes.byref(cfg), int(rank), float(alpha), batch, seq,
+                                       _ptr(codes), _ptr(scales), _ptr(gains), _ptr(shadow),
+                                       _ptr(x), _ptr(y), _ptr(saved),
+                                       saved.numel() * saved.element_size(), _ptr(ws),
+                                       ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def nf4_block_backward(cfg, rank, alpha, batch, seq, codes, scales, gains, shadow, x, saved, dy,
+                       dx, lora_grads, ws, grad_sq=None, stream=None):
+    """grad_sq: optional fp64 device scalar; += the squared sum of lora_grads."""
+    _check(lib().rdt_nf4_block_backward(ctypes.byref(cfg), int(rank), float(alpha), batch, seq,
+                                        _ptr(codes), _ptr(scales), _ptr(gains), _ptr(shadow),
+                                        _ptr(x), _ptr(saved),
+                                        saved.numel() * saved.element_size(), _ptr(dy), _ptr(dx),
+                                        _ptr(lora_grads),
+                                        None if grad_sq is None else _ptr(grad_sq), _ptr(ws),
+                                        ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def cast_bf16(src, dst, n=None, stream=None):

@@ -93,3 +93,47 @@ def ragged_shape(**kw):
                 vocab=1008, seq=200, batch=2, eps=1e-6, theta=1e4)
     base.update(kw)
     return synth.DecoderShape(**base)
+
+
+def nf4_buffers(shape, rank, base, gains, lora):
+    """Device buffers of the NF4 + LoRA block in the library's layouts: codes
+    (uint8), scales, gains, lora (fp32) and the bf16 adapter shadow."""
+    cfg = rdt.Config.from_shape(shape)
+    nc, ns = rdt.nf4_sizes(cfg)
+    offs = rdt.nf4_offsets(cfg)
+    codes = torch.zeros(nc, dtype=torch.uint8)
+    scales = torch.zeros(ns, dtype=torch.float32)
+    for name, (co, so) in offs.items():
+        packed, absmax = base[name]
+        codes[co:co + packed.numel()] = packed.reshape(-1)
+        scales[so:so + absmax.numel()] = absmax.reshape(-1)
+    g = torch.cat([gains[k].reshape(-1) for k in ("g_attn", "g_ffn", "g_q", "g_k")])
+    lo = rdt.lora_param_offsets(cfg, rank)
+    lw = torch.zeros(rdt.lora_param_count(cfg, rank), dtype=torch.float32)
+    for name, (o, c) in lo.items():
+        lw[o:o + c] = lora[name].reshape(-1)
+    lw = lw.cuda()
+    shadow = torch.empty(rdt.lora_shadow_count(cfg, rank), dtype=torch.bfloat16, device="cuda")
+    rdt.lora_shadow(cfg, rank, lw, shadow)
+    return cfg, codes.cuda(), scales.cuda(), g.cuda(), lw, shadow
+
+
+def gpu_nf4_block(shape, rank, alpha, base, gains, lora, x, dy):
+    """NF4 + LoRA block forward + backward on the GPU: (y, dx, adapter grads
+    {name: tensor}, fused squared sum added to SQ_START)."""
+    cfg, codes, scales, g, lw, shadow = nf4_buffers(shape, rank, base, gains, lora)
+    B, S = shape.batch, shape.seq
+    saved = torch.empty(rdt.nf4_saved_bytes(cfg, rank, B, S), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(rdt.nf4_workspace_bytes(cfg, rank, B, S), dtype=torch.uint8, device="cuda")
+    xd = x.to("cuda").contiguous()
+    y = torch.empty_like(xd)
+    rdt.nf4_block_forward(cfg, rank, alpha, B, S, codes, scales, g, shadow, xd, y, saved, ws)
+    dx = torch.empty_like(xd)
+    grads = torch.full_like(lw, float("nan"))
+    sq = torch.full((1,), SQ_START, dtype=torch.float64, device="cuda")
+    rdt.nf4_block_backward(cfg, rank, alpha, B, S, codes, scales, g, shadow, xd, saved,
+                           dy.to("cuda").contiguous(), dx, grads, ws, grad_sq=sq)
+    torch.cuda.synchronize()
+    out = {name: grads[o:o + c].view(lora[name].shape)
+           for name, (o, c) in rdt.lora_param_offsets(cfg, rank).items()}
+    return y, dx, out, float(sq)

@@ -96,6 +96,56 @@ def test_null_and_misaligned_arguments_fail_before_any_launch(lib):
     assert st == rdt.RDT_EINVAL
 
 
+def test_nf4_and_lora_layouts_match_tensor_shapes(lib):
+    s = synth.WORKLOADS["q4b_nf4"]
+    cfg = rdt.Config.from_shape(s)
+    rank = synth.LORA["rank"]
+    rdt.nf4_check(cfg, rank)
+    shapes = synth.block_shapes(s)
+    offs = rdt.nf4_offsets(cfg)
+    pc = ps = 0
+    for name in rdt.NF4_NAMES:
+        out, inn = shapes[name]
+        assert offs[name] == (pc, ps)
+        pc += out * inn // 2
+        ps += out * inn // 64
+    assert rdt.nf4_sizes(cfg) == (pc, ps)
+    # 4.5 bits per frozen weight: 4-bit codes plus one fp32 scale per 64
+    n_w = 2 * pc
+    assert n_w == rdt.block_param_count(cfg) - 2 * s.hidden - 2 * s.head_dim
+    lo = rdt.lora_param_offsets(cfg, rank)
+    pos = 0
+    for name in rdt.LORA_NAMES:
+        proj = "w" + name[2:]
+        out, inn = shapes[proj]
+        want = rank * inn if name.startswith("a_") else out * rank
+        assert lo[name] == (pos, want)
+        pos += want
+    assert rdt.lora_param_count(cfg, rank) == pos
+    n_a = sum(rank * shapes[p][1] for p in rdt.NF4_NAMES)
+    stacked = (s.q_dim + 2 * s.kv_dim) * 3 * rank + s.hidden * rank + \
+        2 * s.intermediate * 2 * rank + s.hidden * rank
+    assert rdt.lora_shadow_count(cfg, rank) == n_a + stacked
+    for n in (rdt.nf4_saved_bytes(cfg, rank, s.batch, s.seq),
+              rdt.nf4_workspace_bytes(cfg, rank, s.batch, s.seq)):
+        assert n > 0 and n % 256 == 0
+    assert rdt.nf4_saved_bytes(cfg, rank, s.batch, s.seq) > \
+        rdt.block_saved_bytes(cfg, s.batch, s.seq)
+
+
+@pytest.mark.parametrize("field,value,rank", [("hidden", 320, 16), ("intermediate", 688, 16),
+                                              ("hidden", 2576, 16), ("hidden", 256, 4),
+                                              ("hidden", 256, 32)])
+def test_nf4_constraints_are_enforced(lib, field, value, rank):
+    cfg = rdt.Config.from_shape(synth.WORKLOADS["q4b_nf4"])
+    setattr(cfg, field, value)
+    with pytest.raises(rdt.RdtError) as ei:
+        rdt.nf4_check(cfg, rank)
+    assert ei.value.status == rdt.RDT_EINVAL
+    assert lib.rdt_lora_param_count(ctypes.byref(cfg), rank) == -1
+    assert rdt.nf4_saved_bytes(cfg, rank, 1, 32) == 0
+
+
 def test_product_path_has_no_oracle_or_cpu_fallback():
     pkg = os.path.join(ROOT, "resident_decoder_trainer_gb300")
     for fn in os.listdir(pkg):
