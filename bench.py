@@ -7,6 +7,7 @@ clip and AdamW over every fp32 master weight, on synthetic inputs already
 resident in HBM. Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload q4b_full]
+  python bench.py --workload q4b_nf4     # NF4-frozen block + LoRA, adapters-only step
   python bench.py --impl reference ...   # the FP64 CPU oracle on host cores
 
 Multi-GPU (torchrun): every rank runs an independent replica of the whole
@@ -331,6 +332,196 @@ def algorithmic_flops(shape):
     return proj + attn
 
 
+# ------------------------------------------------- NF4 + LoRA workload
+NF4_WORKLOADS = ("q4b_nf4",)
+
+
+def nf4_workload_config(shape, name, rank, alpha):
+    return {
+        "workload": (f"{name}: one Qwen3-style block (hidden {shape.hidden}, {shape.n_heads}/"
+                     f"{shape.n_kv_heads} heads, head_dim {shape.head_dim}, SwiGLU "
+                     f"{shape.intermediate}) with frozen NF4 projections (64-weight blocks, "
+                     f"fp32 scales) and LoRA rank {rank} / alpha {alpha:g} on all seven; "
+                     f"batch {shape.batch} x seq {shape.seq}"),
+        "tokens_per_step": shape.tokens,
+        "layers": shape.layers,
+        "global_batch": shape.batch,
+        "seq_len": shape.seq,
+        "params": None,
+        "optimizer": "global-norm clip 1.0 + AdamW over the adapters (fp32 master, m, v)",
+        "l2": "flushed: a 256 MB buffer is written between timed steps",
+        "parallelism": "replicas",
+    }
+
+
+def nf4_algorithmic_flops(shape, rank):
+    """Dense-contraction FLOPs of one adapters-only step: forward and input
+    gradient through the seven frozen projections (4 x params x tokens; no
+    weight gradient), the six causal attention matmuls, and the LoRA terms
+    (6 T r (in + out) per projection: U, its tail product, dU, the tail of
+    the input gradient, dA and dB)."""
+    from resident_decoder_trainer_gb300 import synth
+    s = shape
+    shp = synth.block_shapes(s)
+    proj = sum(shp[n][0] * shp[n][1] for n in synth.NF4_PROJECTIONS)
+    lora = sum(shp[n][0] + shp[n][1] for n in synth.NF4_PROJECTIONS)
+    attn = 6 * 2.0 * s.n_heads * s.head_dim * (s.seq + 1) / 2 * s.tokens
+    return 4.0 * proj * s.tokens + 6.0 * rank * lora * s.tokens + attn
+
+
+class Nf4OracleSample:
+    """The FP64 NF4 + LoRA oracle timed on a bounded sample of one step: the
+    block forward+backward on one sequence of `seq_tokens` tokens (scaled to
+    the step's tokens) plus the adapters' clip + AdamW (the full adapter set)."""
+
+    def __init__(self, shape, rank, alpha, seq_tokens=1024, seed=0):
+        import numpy as np
+        from oracle import model as om
+        from oracle import nf4 as on
+        from resident_decoder_trainer_gb300 import synth
+        self.om, self.on, self.np = om, on, np
+        self.shape, self.rank, self.alpha, self.seq_tokens = shape, rank, alpha, seq_tokens
+        self.s_blk = shape.replace(layers=1, batch=1, seq=seq_tokens)
+        base, gains, lora, x, dy = synth.make_nf4_inputs(self.s_blk, seed=seed, rank=rank,
+                                                         b_std=0.02)
+        shp = synth.block_shapes(self.s_blk)
+        self.base = {k: on.nf4_dequantize(p.numpy(), a.numpy(), *shp[k])
+                     for k, (p, a) in base.items()}
+        self.gains = {k: v.numpy().astype(np.float64) for k, v in gains.items()}
+        self.lora = {k: v.numpy().astype(np.float64) for k, v in lora.items()}
+        self.x, self.dy = om._f64(x), om._f64(dy)
+
+    def run(self):
+        import time as _t
+        from resident_decoder_trainer_gb300 import synth
+        t0 = _t.perf_counter()
+        self.on.lora_step(self.base, self.gains, self.lora, self.x, self.dy, self.s_blk,
+                          self.rank, self.alpha, synth.OPTIM)
+        dt = _t.perf_counter() - t0
+        step_s = dt * self.shape.tokens / self.seq_tokens
+        try:
+            from threadpoolctl import threadpool_info
+            cores = max(int(i.get("num_threads", 1)) for i in threadpool_info()) or os.cpu_count()
+        except Exception:
+            cores = os.cpu_count()
+        sample = (f"FP64 NF4+LoRA oracle: block fwd+bwd + adapter clip+AdamW on "
+                  f"1x{self.seq_tokens} tokens, scaled to {self.shape.tokens} tokens per step")
+        return {"value": round(self.shape.tokens / step_s, 3), "unit": UNIT, "cores": cores,
+                "kind": "oracle", "sample": sample, "sample_seconds": round(dt, 2)}
+
+
+def run_nf4(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from resident_decoder_trainer_gb300 import build, rdt, synth
+    from resident_decoder_trainer_gb300.nf4_step import Nf4LoraTrainer
+
+    build.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    shape = synth.WORKLOADS[args.workload]
+    T = shape.tokens
+    tr = Nf4LoraTrainer(shape, device=dev)
+    tr.init_random(seed=1234 + rank)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4321 + rank)
+    nb = 4
+    xs = [torch.randn(T, shape.hidden, device=dev, generator=gen) for _ in range(nb)]
+    dys = [1e-3 * torch.randn(T, shape.hidden, device=dev, generator=gen) for _ in range(nb)]
+    # the step's working set (~1.5 GB) would otherwise sit in L2 between steps
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        tr.train_step(xs[i % nb], dys[i % nb])
+    timer = rdt.GemmTimer(32 * args.steps)
+    barrier()
+    clk = start_clock_sampler(local_rank)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    l0 = rdt.launch_count()
+    with timer:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)  # outside the timed events: evicts the previous step
+            evs[i][0].record(stream)
+            tr.train_step(xs[i % nb], dys[i % nb])
+            evs[i][1].record(stream)
+        barrier()
+    launches = rdt.launch_count() - l0
+    clocks = stop_clock_sampler(clk)
+    dev_ms = sum(a.elapsed_time(b) for a, b in evs)
+    t = torch.tensor([dev_ms], device=dev, dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    max_ms = float(t.item())
+    value = world * T * args.steps / (max_ms / 1e3)
+
+    res = timer.results(with_kind=True)
+    nf4 = [(f, ms) for f, ms, k in res if k == "nf4"]
+    other = [(f, ms) for f, ms, k in res if k != "nf4"]
+    nf4_flops, nf4_ms = sum(f for f, _ in nf4), sum(ms for _, ms in nf4)
+    peaks, peak_kind = load_peaks()
+    peak_tf = float(peaks.get("bf16_tflops_sustained") or peaks.get("bf16_tflops"))
+    achieved = nf4_flops / (nf4_ms / 1e3) / 1e12 if nf4_ms > 0 else None
+    roofline = {
+        "kernel": "gemm_nf4_kernel (tcgen05 BF16 128x256 tiles, B decoded from 4-bit NF4 codes "
+                  "+ per-64 fp32 scales into shared memory by four decode warps, LoRA term "
+                  "as a bf16 tail k-block)",
+        "bound": "tensor", "achieved": round(achieved, 1) if achieved else None,
+        "peak": peak_tf, "unit": "TFLOP/s",
+        "frac": round(achieved / peak_tf, 4) if achieved else None,
+        "peak_source": f"bf16_tflops_sustained of {peak_kind}",
+        "traffic": None,
+        "launches_timed": len(nf4),
+        "flops_per_launch": nf4_flops / max(len(nf4), 1),
+        "ms_per_launch": nf4_ms / max(len(nf4), 1),
+        "nf4_gemm_share_of_step": round(nf4_ms / max_ms, 4) if max_ms else None,
+        "adapter_gemm_share_of_step": round(sum(ms for _, ms in other) / max_ms, 4)
+        if max_ms else None,
+    }
+    step_flops = nf4_algorithmic_flops(shape, tr.rank)
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 (NF4-decoded weights)",
+        "data": "synthetic (device-generated N(0,1) inputs, N(0,1e-3) upstream gradients, "
+                "uniform NF4 codes, 3|N(0,0.02)| scales, A ~ N(0,0.02), B = 0)",
+        "config": nf4_workload_config(shape, args.workload, tr.rank, tr.alpha),
+        "roofline": roofline,
+        "step_tflops": round(step_flops / (max_ms / args.steps / 1e3) / 1e12, 1),
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+    }
+    out["config"]["params"] = tr.n_params
+    out["config"]["algorithmic_tflop_per_step"] = round(step_flops / 1e12, 3)
+    if not args.no_e2e:
+        xh = [x.cpu().pin_memory() for x in xs[:2]]
+        dyh = [d.cpu().pin_memory() for d in dys[:2]]
+        sq_h = torch.empty(1, dtype=torch.float64).pin_memory()
+        xd, dyd = torch.empty_like(xs[0]), torch.empty_like(dys[0])
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            xd.copy_(xh[i % 2], non_blocking=True)
+            dyd.copy_(dyh[i % 2], non_blocking=True)
+            tr.train_step(xd, dyd)
+            sq_h.copy_(tr.sumsq, non_blocking=True)
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        out["e2e"] = {"value": round(world * T * args.steps / dt, 1), "unit": UNIT,
+                      "h2d_bytes_per_step": 2 * T * shape.hidden * 4,
+                      "d2h_bytes_per_step": 8}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = Nf4OracleSample(shape, tr.rank, tr.alpha).run()
+    return out
+
+
 # ---------------------------------------------------------- kernel probes
 def run_probe(args):
     """One block forward+backward (or the fused LM head + CE) of the workload's
@@ -404,8 +595,35 @@ def run_probe(args):
 
 
 # ------------------------------------------------------------ reference
+def run_reference_nf4(args, world):
+    from resident_decoder_trainer_gb300 import synth
+    shape = synth.WORKLOADS[args.workload]
+    rank_, alpha = synth.LORA["rank"], synth.LORA["alpha"]
+    sampler = Nf4OracleSample(shape, rank_, alpha, seq_tokens=256)
+    samples = []
+    for i in range(args.warmup + args.steps):
+        r = sampler.run()
+        if i >= args.warmup:
+            samples.append(r)
+    value = statistics.median(r["value"] for r in samples)
+    cpu = dict(samples[-1])
+    cpu["value"] = value
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(shape.tokens / value * 1e3, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": nf4_workload_config(shape, args.workload, rank_, alpha),
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
 def run_reference(args, rank, world):
     from resident_decoder_trainer_gb300 import synth
+    if args.workload in NF4_WORKLOADS:
+        return run_reference_nf4(args, world)
     shape = synth.WORKLOADS[args.workload]
     if args.layers:
         shape = shape.replace(layers=args.layers)
@@ -449,7 +667,10 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
-    out = run_rdt(args, rank, world, local_rank)
+    if args.workload in NF4_WORKLOADS:
+        out = run_nf4(args, rank, world, local_rank)
+    else:
+        out = run_rdt(args, rank, world, local_rank)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

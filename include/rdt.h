@@ -330,13 +330,15 @@ rdt_status rdt_nf4_block_backward(const rdt_config* cfg, int32_t rank, float alp
  * rdt_gemm_timing_arm: while armed, the i-th tensor-core GEMM launch (any
  *   entry point) records the caller-created cudaEvent_t events[2i] on its
  *   stream just before the launch and events[2i+1] just after it, and stores
- *   its algorithmic FLOP count 2*M*N*K in flops[i] (host array), for
- *   i < capacity. rdt_gemm_timing_disarm stops it and returns the number of
+ *   its algorithmic FLOP count 2*M*N*K in flops[i] and, when kinds is not
+ *   null, its kernel in kinds[i] (0: bf16 single-CTA tiles, 1: bf16 CTA-pair
+ *   tiles, 2: NF4-decoding kernel; host arrays), for i < capacity. rdt_gemm_timing_disarm stops it and returns the number of
  *   launches seen (which may exceed capacity; only the first capacity are
  *   recorded).
  * rdt_launch_count: kernels this process has launched through the library
  *   so far (all entry points, all devices). */
-rdt_status rdt_gemm_timing_arm(void* const* events, double* flops, int32_t capacity);
+rdt_status rdt_gemm_timing_arm(void* const* events, double* flops, int32_t* kinds,
+                               int32_t capacity);
 int64_t rdt_gemm_timing_disarm(void);
 int64_t rdt_launch_count(void);
 

@@ -50,6 +50,7 @@ std::atomic<int64_t> g_launches{0};
 std::mutex g_timing_mu;
 void* const* g_timing_events = nullptr;
 double* g_timing_flops = nullptr;
+int32_t* g_timing_kinds = nullptr;
 int32_t g_timing_cap = 0;
 int64_t g_timing_seen = 0;
 bool g_timing_armed = false;
@@ -242,12 +243,13 @@ void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
 
 void note_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
-int64_t gemm_timing_before(cudaStream_t s, double flops) {
+int64_t gemm_timing_before(cudaStream_t s, double flops, int kind) {
   std::lock_guard<std::mutex> lk(g_timing_mu);
   if (!g_timing_armed) return -1;
   const int64_t slot = g_timing_seen++;
   if (slot >= g_timing_cap) return -1;
   g_timing_flops[slot] = flops;
+  if (g_timing_kinds) g_timing_kinds[slot] = kind;
   cudaEventRecord(static_cast<cudaEvent_t>(g_timing_events[2 * slot]), s);
   return slot;
 }
@@ -403,11 +405,13 @@ size_t carve_nf4_ws(const Dims& m, int64_t r, int64_t B, int64_t S, void* base, 
 // =========================================================================
 extern "C" {
 
-rdt_status rdt_gemm_timing_arm(void* const* events, double* flops, int32_t capacity) {
+rdt_status rdt_gemm_timing_arm(void* const* events, double* flops, int32_t* kinds,
+                               int32_t capacity) {
   if (!events || !flops || capacity < 1) return fail(RDT_EINVAL, "events/flops/capacity");
   std::lock_guard<std::mutex> lk(g_timing_mu);
   g_timing_events = events;
   g_timing_flops = flops;
+  g_timing_kinds = kinds;
   g_timing_cap = capacity;
   g_timing_seen = 0;
   g_timing_armed = true;
@@ -419,6 +423,7 @@ int64_t rdt_gemm_timing_disarm(void) {
   g_timing_armed = false;
   g_timing_events = nullptr;
   g_timing_flops = nullptr;
+  g_timing_kinds = nullptr;
   return g_timing_seen;
 }
 

@@ -651,24 +651,55 @@ __constant__ float kNf4Levels[16] = {
     0.07958029955625534f, 0.16093020141124725f, 0.24611230194568634f, 0.33791524171829224f,
     0.44070982933044434f, 0.5626170039176941f, 0.7229568362236023f, 1.0f};
 
-// Decode one 64-element block (32 code bytes at `codes`, scale `sc`) into row
-// `row` of a 128-byte-swizzled tile at `dst` (8 chunks of 8 bf16).
-__device__ __forceinline__ void nf4_decode_row(const uint8_t* codes, float sc,
-                                               const float* levels, uint8_t* dst, int row) {
-  const uint4 c0 = reinterpret_cast<const uint4*>(codes)[0];
-  const uint4 c1 = reinterpret_cast<const uint4*>(codes)[1];
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// The 16 products T[c] = bf16(level[c] * sc) of one 64-weight block, as byte
+// planes: lo[q] holds the low bytes of T[4q .. 4q+3], hi[q] the high bytes.
+__device__ __forceinline__ void nf4_planes(float sc, uint32_t (&lo)[4], uint32_t (&hi)[4]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t p0 = pack_bf16x2(kNf4Levels[4 * q] * sc, kNf4Levels[4 * q + 1] * sc);
+    const uint32_t p1 = pack_bf16x2(kNf4Levels[4 * q + 2] * sc, kNf4Levels[4 * q + 3] * sc);
+    lo[q] = prmt(p0, p1, 0x6420);
+    hi[q] = prmt(p0, p1, 0x7531);
+  }
+}
+
+// T[c] for the four codes in the low 16 bits of s (code j in bits 4j..4j+3)
+// as two bf16 pairs (code 0 in the low half of .x). A byte permute indexes 8
+// bytes, so each plane is looked up in its lower (codes 0-7) and upper
+// (8-15, selector bit 3 flipped) halves and the two merged on bit 3 of the code.
+__device__ __forceinline__ uint2 nf4_lookup4(uint32_t s, const uint32_t (&lo)[4],
+                                             const uint32_t (&hi)[4]) {
+  const uint32_t sx = s ^ 0x8888u;
+  const uint32_t la = prmt(lo[0], lo[1], s), lb = prmt(lo[2], lo[3], sx);
+  const uint32_t ha = prmt(hi[0], hi[1], s), hb = prmt(hi[2], hi[3], sx);
+  // byte j of c carries bit 3 of code j in its top bit; replicate it
+  const uint32_t a = prmt(s, 0u, 0x1100);
+  const uint32_t c = (a & 0x80008000u) | ((a << 4) & 0x00800080u);
+  const uint32_t m = prmt(c, 0u, 0xBA98);
+  const uint32_t l = (la & ~m) | (lb & m);
+  const uint32_t h = (ha & ~m) | (hb & m);
+  return make_uint2(prmt(l, h, 0x5140), prmt(l, h, 0x7362));
+}
+
+// Decode one 64-weight run (32 code bytes as two 16-byte chunks c0, c1; one
+// scale) into the 128-byte row `row` of a 128-byte-swizzled bf16 tile at dst.
+__device__ __forceinline__ void nf4_decode_run(uint4 c0, uint4 c1, float sc, uint8_t* dst,
+                                               int row) {
+  uint32_t lo[4], hi[4];
+  nf4_planes(sc, lo, hi);
   const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
   for (int c8 = 0; c8 < 8; ++c8) {
-    // 4 code bytes -> 8 elements
-    const uint32_t b = w[c8];
-    uint32_t o[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint32_t byte = (b >> (8 * q)) & 0xFFu;
-      o[q] = pack_bf16x2(levels[byte & 0xFu] * sc, levels[byte >> 4] * sc);
-    }
-    *reinterpret_cast<uint4*>(dst + sw128_offset(row, c8)) = make_uint4(o[0], o[1], o[2], o[3]);
+    // 4 code bytes = 8 weights, element 2j in the low nibble of byte j
+    const uint2 e0 = nf4_lookup4(w[c8] & 0xFFFFu, lo, hi);
+    const uint2 e1 = nf4_lookup4(w[c8] >> 16, lo, hi);
+    *reinterpret_cast<uint4*>(dst + sw128_offset(row, c8)) = make_uint4(e0.x, e0.y, e1.x, e1.y);
   }
 }
 
@@ -687,9 +718,8 @@ __global__ void __launch_bounds__(NF4_THREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + TileN4::OFF_OUT + OS::TOTAL);
   // bars: raw[S], full[S], empty[S], tfull[2], tempty[2], drain, epilogue inputs[8][2];
-  // then the TMEM address and the 16 levels
+  // then the TMEM address
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 21);
-  float* levels = reinterpret_cast<float*>(bars + 3 * STAGES + 22);
   const uint32_t raw0 = smem_u32(bars);
   const uint32_t full0 = raw0 + 8 * STAGES;
   const uint32_t empty0 = full0 + 8 * STAGES;
@@ -715,7 +745,6 @@ __global__ void __launch_bounds__(NF4_THREADS, 1)
     for (int i = 0; i < 16; ++i) mbar_init(ebar0 + 8 * i, 1);
     fence_mbar_init();
   }
-  if (threadIdx.x < 16) levels[threadIdx.x] = kNf4Levels[threadIdx.x];
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tma_a);
     tma_prefetch_desc(&tma_b2);
@@ -891,16 +920,20 @@ __global__ void __launch_bounds__(NF4_THREADS, 1)
           for (int i = 0; i < 2; ++i) {
             const int u = dt + 128 * i;  // one 64-element block of W per u
             if (B_MN) {
+              // W row k0 + k_row, columns ch*64..: 32 code bytes in a 128-byte-swizzled row
               const int k_row = u & 63, ch = u >> 6;
+              const uint8_t* cr = sp + TileN4::OFF_CODE + k_row * 128;
+              const uint4 c0 = *reinterpret_cast<const uint4*>(cr + (((2 * ch) ^ (k_row & 7)) << 4));
+              const uint4 c1 =
+                  *reinterpret_cast<const uint4*>(cr + (((2 * ch + 1) ^ (k_row & 7)) << 4));
               const float sc =
                   *reinterpret_cast<const float*>(sp + TileN4::OFF_ABS + k_row * 16 + ch * 4);
-              nf4_decode_row(sp + TileN4::OFF_CODE + k_row * 128 + ch * 32, sc, levels,
-                             sp + TileN4::OFF_B + ch * MN_CHUNK_BYTES, k_row);
+              nf4_decode_run(c0, c1, sc, sp + TileN4::OFF_B + ch * MN_CHUNK_BYTES, k_row);
             } else {
+              const uint4* cr = reinterpret_cast<const uint4*>(sp + TileN4::OFF_CODE + u * 32);
               const float sc = *reinterpret_cast<const float*>(sp + TileN4::OFF_ABS + u * 16 +
                                                                (kb & 3) * 4);
-              nf4_decode_row(sp + TileN4::OFF_CODE + u * 32, sc, levels,
-                             sp + TileN4::OFF_B, u);
+              nf4_decode_run(cr[0], cr[1], sc, sp + TileN4::OFF_B, u);
             }
           }
           fence_proxy_async_smem();
@@ -920,6 +953,291 @@ __global__ void __launch_bounds__(NF4_THREADS, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------- NF4 pair kernel
+// The NF4 GEMM on CTA pairs (clusters of 2, tcgen05.mma.cta_group::2 with
+// 256 x 256 x 16 tiles): each CTA stages its own 128 rows of A and decodes
+// only its 128 of the tile's 256 B columns, half the decode work per MMA
+// flop of the single-CTA kernel. TMA brings each CTA's codes and scales to a
+// local "raw" barrier; A (and the tail's A2 / B2) complete on the even CTA's
+// "full" barrier, on which both CTAs' decode warps also arrive after a
+// generic-to-async proxy fence over their decoded tiles. The even CTA's MMA
+// thread commits to both CTAs' "empty" barriers; the epilogue is the pair
+// GEMM's.
+struct TileN4P {
+  static constexpr int BH = NF4_BN / 2;                      // B columns per CTA
+  static constexpr uint32_t B_BYTES = BH * BK * 2;           // 16 KB
+  static constexpr uint32_t CODE_BYTES = BH * BK / 2;        // 4 KB
+  static constexpr uint32_t ABS_BYTES = 2048;                // <= 128 rows x 16 B
+  static constexpr uint32_t OFF_B = A_BYTES;
+  static constexpr uint32_t OFF_CODE = OFF_B + B_BYTES;
+  static constexpr uint32_t OFF_ABS = OFF_CODE + CODE_BYTES;
+  static constexpr uint32_t STAGE_BYTES = OFF_ABS + ABS_BYTES;  // 38 KB
+  static constexpr int STAGES = 5;
+  static constexpr uint32_t OFF_OUT = STAGES * STAGE_BYTES;
+  static constexpr size_t SMEM = OFF_OUT + OutStage<NF4_BN, true>::TOTAL + 1024 + 512;
+};
+static_assert(TileN4P::SMEM <= 232448, "NF4 pair tile exceeds the shared memory of a CTA");
+static_assert(TileN4P::STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
+
+template <int B_MN, int EPI>
+__global__ void __launch_bounds__(NF4_THREADS, 1)
+    gemm2_nf4_kernel(const __grid_constant__ CUtensorMap tma_a,
+                     const __grid_constant__ CUtensorMap tma_b2,
+                     const __grid_constant__ Nf4Maps nm, const __grid_constant__ OutMaps om,
+                     const GemmParams p) {
+  constexpr int BN = NF4_BN;
+  constexpr int BH = TileN4P::BH;
+  constexpr int STAGES = TileN4P::STAGES;
+  constexpr uint32_t STAGE_BYTES = TileN4P::STAGE_BYTES;
+  using OS = OutStage<BN, true>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + TileN4P::OFF_OUT + OS::TOTAL);
+  // bars: raw[S], full[S], empty[S], tfull[2], tempty[2], drain, epilogue inputs[8][2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 21);
+  const uint32_t raw0 = smem_u32(bars);
+  const uint32_t full0 = raw0 + 8 * STAGES;
+  const uint32_t empty0 = full0 + 8 * STAGES;
+  const uint32_t tfull0 = empty0 + 8 * STAGES;
+  const uint32_t tempty0 = tfull0 + 16;
+  const uint32_t drain = tempty0 + 16;
+  const uint32_t ebar0 = drain + 8;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the pair MMAs
+  const int pair = static_cast<int>(blockIdx.x) >> 1;
+  const int npairs = static_cast<int>(gridDim.x) >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(raw0 + 8 * s, 1);
+      mbar_init(full0 + 8 * s, 1 + 2 * 4);  // even producer + both CTAs' decode warps
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, 2 * (EPI_THREADS / 32));
+    }
+    mbar_init(drain, 1);
+    for (int i = 0; i < 16; ++i) mbar_init(ebar0 + 8 * i, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tma_a);
+    tma_prefetch_desc(&tma_b2);
+    tma_prefetch_desc(&nm.codes);
+    tma_prefetch_desc(&nm.scales);
+    tma_prefetch_desc(&nm.a2);
+  }
+  if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t full_even = mapa_shared(full0, 0);
+  const uint32_t tempty_even = mapa_shared(tempty0, 0);
+
+  const int ntiles = p.m_tiles * p.n_tiles;  // m_tiles counts 256-row pair tiles
+  const uint32_t smem_base = smem_u32(smem);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      int stage = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int t = pair; t < ntiles && ok; t += npairs) {
+        int mt, nt;
+        tile_coords(t, p, mt, nt);
+        const int m0 = (2 * mt + static_cast<int>(rank)) * BM;
+        // first of this CTA's 128 B rows (K-major) / columns (MN-major)
+        const int r0 = (EPI == EPI_SWIGLU) ? nt * 128 + static_cast<int>(rank) * p.swiglu_half
+                                           : nt * BN + static_cast<int>(rank) * BH;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(empty0 + 8 * stage, ph ^ 1, p.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t rb = raw0 + 8 * stage;
+          const uint32_t fb = full_even + 8 * stage;
+          const uint32_t sa = smem_base + stage * STAGE_BYTES;
+          const uint32_t sb = sa + TileN4P::OFF_B;
+          const uint32_t sc = sa + TileN4P::OFF_CODE;
+          const uint32_t ss = sa + TileN4P::OFF_ABS;
+          const int k0 = kb * BK;
+          if (kb < p.kb_main) {
+            if (rank == 0) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * A_BYTES);
+            tma_load_2d_pair(sa, &tma_a, fb, k0, m0);
+            if (B_MN) {
+              // W rows k0..k0+63, this CTA's 128 columns: 64 code bytes and the
+              // 4 scales of the tile's 256 columns per row
+              mbar_arrive_expect_tx(rb, 64 * 64 + 64 * 16);
+              tma_load_2d(sc, &nm.codes, rb, r0 / 2, k0);
+              tma_load_2d(ss, &nm.scales, rb, nt * (BN / 64), k0);
+            } else {
+              // this CTA's 128 W rows, 32 code bytes and 4 scales each, 64 rows per box
+              mbar_arrive_expect_tx(rb, TileN4P::CODE_BYTES + BH * 16);
+#pragma unroll
+              for (int j = 0; j < BH / 64; ++j) {
+                tma_load_2d(sc + j * 2048, &nm.codes, rb, k0 / 2, r0 + 64 * j);
+                tma_load_2d(ss + j * 1024, &nm.scales, rb, kb & ~3, r0 + 64 * j);
+              }
+            }
+          } else {
+            // tail: ordinary bf16 A2 and B2; the decode warps only pass through
+            const int kt = k0 - p.kb_main * BK;
+            if (rank == 0) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * (A_BYTES + TileN4P::B_BYTES));
+            tma_load_2d_pair(sa, &nm.a2, fb, kt, m0);
+#pragma unroll
+            for (int j = 0; j < BH / 64; ++j) {
+              if (B_MN)
+                tma_load_2d_pair(sb + j * MN_CHUNK_BYTES, &tma_b2, fb, r0 + 64 * j, kt);
+              else
+                tma_load_2d_pair(sb + j * MN_CHUNK_BYTES, &tma_b2, fb, kt, r0 + 64 * j);
+            }
+            mbar_arrive(rb);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            ph ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ----------------------------------------------------------------- MMA
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN, 0, B_MN);
+      const uint64_t a_desc0 = sdesc_sw128(smem_base, 16, 1024);
+      const uint64_t b_desc0 =
+          sdesc_sw128(smem_base + TileN4P::OFF_B, B_MN ? MN_CHUNK_BYTES : 16, 1024);
+      int stage = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t acc_ph = 0;
+      bool ok = true;
+      for (int t = pair; t < ntiles && ok; t += npairs) {
+        if (!mbar_wait_cluster(tempty0 + 8 * acc, acc_ph ^ 1, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(full0 + 8 * stage, ph, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad0 = a_desc0 + static_cast<uint64_t>(stage) * (STAGE_BYTES >> 4);
+          const uint64_t bd0 = b_desc0 + static_cast<uint64_t>(stage) * (STAGE_BYTES >> 4);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = ad0 + static_cast<uint64_t>(k) * (32 >> 4);
+            const uint64_t bd = bd0 + static_cast<uint64_t>(k) * ((B_MN ? 2048 : 32) >> 4);
+            tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
+          }
+          tc_commit_pair_mc(empty0 + 8 * stage, 0x3);
+          if (++stage == STAGES) {
+            stage = 0;
+            ph ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair_mc(tfull0 + 8 * acc, 0x3);
+        acc ^= 1;
+        if (acc == 0) acc_ph ^= 1;
+      }
+      tc_commit_pair(drain);
+      mbar_wait(drain, 0, nullptr);
+    }
+  } else if (warp < 10) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    uint8_t* stg = smem + TileN4P::OFF_OUT + (warp - 2) * OS::BYTES;
+    const Stage st{stg, smem_u32(stg), ebar0 + 16 * (warp - 2), lane};
+    uint32_t ucnt = 0, eph = 0;
+    int acc = 0;
+    uint32_t acc_ph = 0;
+    for (int t = pair; t < ntiles; t += npairs) {
+      int mt, nt;
+      tile_coords(t, p, mt, nt);
+      const int mrow = 2 * mt + static_cast<int>(rank);
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      if (!epilogue_tile<EPI, BN, OS::BYTES>(p, om, tbase, mrow * BM + q * 32, nt, half, st,
+                                             ucnt, eph, tfull0 + 8 * acc, acc_ph, t,
+                                             static_cast<int>(rank) * 8 + (warp - 2)))
+        break;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty_even + 8 * acc);
+      acc ^= 1;
+      if (acc == 0) acc_ph ^= 1;
+    }
+    if (lane == 0) bulk_wait0();
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- decode
+    const int dt = static_cast<int>(threadIdx.x) - 320;  // 0..127
+    int stage = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int t = pair; t < ntiles && ok; t += npairs) {
+      for (int kb = 0; kb < p.k_blocks; ++kb) {
+        if (!warp_wait(raw0 + 8 * stage, ph, p.err)) {
+          ok = false;
+          break;
+        }
+        if (kb < p.kb_main) {
+          uint8_t* sp = smem + stage * STAGE_BYTES;
+          if (B_MN) {
+            // W row k0 + k_row, this CTA's columns ch*64..: 32 of the row's 64
+            // code bytes, 64-byte-swizzled
+            const int k_row = dt & 63, ch = dt >> 6;
+            const uint8_t* cr = sp + TileN4P::OFF_CODE + k_row * 64;
+            const int sw = (k_row >> 1) & 3;
+            const uint4 c0 = *reinterpret_cast<const uint4*>(cr + (((2 * ch) ^ sw) << 4));
+            const uint4 c1 = *reinterpret_cast<const uint4*>(cr + (((2 * ch + 1) ^ sw) << 4));
+            const float sc = *reinterpret_cast<const float*>(
+                sp + TileN4P::OFF_ABS + k_row * 16 + (static_cast<int>(rank) * 2 + ch) * 4);
+            nf4_decode_run(c0, c1, sc, sp + TileN4P::OFF_B + ch * MN_CHUNK_BYTES, k_row);
+          } else {
+            const uint4* cr = reinterpret_cast<const uint4*>(sp + TileN4P::OFF_CODE + dt * 32);
+            const float sc = *reinterpret_cast<const float*>(sp + TileN4P::OFF_ABS + dt * 16 +
+                                                             (kb & 3) * 4);
+            nf4_decode_run(cr[0], cr[1], sc, sp + TileN4P::OFF_B, dt);
+          }
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(full_even + 8 * stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          ph ^= 1;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync();
+  if (p.err && *reinterpret_cast<volatile int*>(p.err) != 0) {
+    // after a timed-out wait, copies issued just before may still be landing
+    // on this pair's shared memory: let them finish before the CTAs exit
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 200000ull) {
+    }
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
 }
 
@@ -1251,7 +1569,7 @@ static cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const Ou
   }
   const int ntiles = p.m_tiles * p.n_tiles;
   const int grid = ntiles < num_sms() ? ntiles : num_sms();
-  const int64_t slot = gemm_timing_before(s, 2.0 * p.M * (double)p.N * p.K);
+  const int64_t slot = gemm_timing_before(s, 2.0 * p.M * (double)p.N * p.K, GEMM_KIND_SINGLE);
   note_launch();
   gemm_kernel<A_MN, B_MN, EPI, BN><<<grid, GEMM_THREADS, Tile<BN>::SMEM, s>>>(ta, tb, om, p);
   gemm_timing_after(s, slot);
@@ -1283,7 +1601,7 @@ static cudaError_t launch2(const CUtensorMap& ta, const CUtensorMap& tb, const O
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const int64_t slot = gemm_timing_before(s, 2.0 * p.M * (double)p.N * p.K);
+  const int64_t slot = gemm_timing_before(s, 2.0 * p.M * (double)p.N * p.K, GEMM_KIND_PAIR);
   note_launch();
   cudaError_t e = cudaLaunchKernelEx(&cfg, gemm2_kernel<A_MN, B_MN, EPI, BN>, ta, tb, om, p);
   gemm_timing_after(s, slot);
@@ -1462,7 +1780,7 @@ cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N,
 
 // ------------------------------------------------------------- NF4 host
 static bool make_u8_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols_bytes,
-                        int box_cols, int box_rows) {
+                        int box_cols, int box_rows, CUtensorMapSwizzle sw) {
   EncodeTiledFn enc = encode_fn();
   if (!enc || (reinterpret_cast<uintptr_t>(ptr) & 15) || (cols_bytes % 16)) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols_bytes), static_cast<cuuint64_t>(rows)};
@@ -1470,7 +1788,7 @@ static bool make_u8_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t c
   cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t es[2] = {1u, 1u};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 static bool make_f32_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols,
@@ -1487,6 +1805,68 @@ static bool make_f32_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t 
 }
 
 template <int B_MN, int EPI>
+static cudaError_t launch_nf4_pair(const CUtensorMap& ta, const CUtensorMap& tb2,
+                                   const Nf4Maps& nm, const OutMaps& om, const GemmParams& p,
+                                   int max_pairs, cudaStream_t s) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(gemm2_nf4_kernel<B_MN, EPI>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(TileN4P::SMEM));
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const int ntiles = p.m_tiles * p.n_tiles;
+  const int pairs = ntiles < max_pairs ? ntiles : max_pairs;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(NF4_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = TileN4P::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int64_t slot = gemm_timing_before(s, 2.0 * p.M * (double)p.N * p.K, GEMM_KIND_NF4);
+  note_launch();
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm2_nf4_kernel<B_MN, EPI>, ta, tb2, nm, om, p);
+  gemm_timing_after(s, slot);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// CTA pairs of the NF4 pair kernel that can be resident at once (0: none).
+static int max_active_nf4_pairs() {
+  static int n = -1;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * num_sms(), 1, 1);
+    cfg.blockDim = dim3(NF4_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = TileN4P::SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int c = 0;
+    if (cudaFuncSetAttribute(gemm2_nf4_kernel<0, EPI_F32>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(TileN4P::SMEM)) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&c, gemm2_nf4_kernel<0, EPI_F32>, &cfg) != cudaSuccess)
+      c = 0;
+    cudaGetLastError();
+    n = c;
+  });
+  return n;
+}
+
+template <int B_MN, int EPI>
 static cudaError_t launch_nf4(const CUtensorMap& ta, const CUtensorMap& tb2, const Nf4Maps& nm,
                               const OutMaps& om, const GemmParams& p, cudaStream_t s) {
   static bool attr_done = false;
@@ -1499,7 +1879,7 @@ static cudaError_t launch_nf4(const CUtensorMap& ta, const CUtensorMap& tb2, con
   }
   const int ntiles = p.m_tiles * p.n_tiles;
   const int grid = ntiles < num_sms() ? ntiles : num_sms();
-  const int64_t slot = gemm_timing_before(s, 2.0 * p.M * (double)p.N * p.K);
+  const int64_t slot = gemm_timing_before(s, 2.0 * p.M * (double)p.N * p.K, GEMM_KIND_NF4);
   note_launch();
   gemm_nf4_kernel<B_MN, EPI><<<grid, NF4_THREADS, TileN4::SMEM, s>>>(ta, tb2, nm, om, p);
   gemm_timing_after(s, slot);
@@ -1534,10 +1914,19 @@ cudaError_t gemm_nf4(const Mat& A, const Nf4Mat& W, bool b_mn, const Mat* A2, co
     *why = "gemm_nf4: operands need 16-byte aligned rows";
     return cudaErrorInvalidValue;
   }
+  // CTA pairs whenever there are two 128-row halves to pair (and clusters launch)
+  const int pairs_max = max_active_nf4_pairs();
+  const bool pair_tiles = pairs_max > 0 && M > BM;
   CUtensorMap ta, tb2;
   Nf4Maps nm;
   bool ok = make_map(&ta, A, 128);
-  ok = ok && make_u8_map(&nm.codes, W.codes, W.rows, W.cols / 2, b_mn ? 128 : 32, 64);
+  // MN-major code rows (128 bytes per CTA, 64 per CTA of a pair) swizzled so
+  // the decode warps' reads spread over the banks
+  const CUtensorMapSwizzle csw = !b_mn        ? CU_TENSOR_MAP_SWIZZLE_NONE
+                                 : pair_tiles ? CU_TENSOR_MAP_SWIZZLE_64B
+                                              : CU_TENSOR_MAP_SWIZZLE_128B;
+  ok = ok && make_u8_map(&nm.codes, W.codes, W.rows, W.cols / 2,
+                         b_mn ? (pair_tiles ? 64 : 128) : 32, 64, csw);
   ok = ok && make_f32_map(&nm.scales, W.scales, W.rows, W.cols / 64, 4, 64);
   if (K2 > 0) {
     ok = ok && make_map(&nm.a2, *A2, 128) && make_map(&tb2, *B2, 64);
@@ -1558,13 +1947,14 @@ cudaError_t gemm_nf4(const Mat& A, const Nf4Mat& W, bool b_mn, const Mat* A2, co
   p.M = M;
   p.N = N;
   p.K = K1 + K2;
-  p.m_tiles = (M + BM - 1) / BM;
+  const int rows_per_tile = pair_tiles ? 2 * BM : BM;
+  p.m_tiles = (M + rows_per_tile - 1) / rows_per_tile;
   p.n_tiles = swiglu ? (N + 127) / 128 : (N + NF4_BN - 1) / NF4_BN;
   p.kb_main = K1 / BK;
   p.k_blocks = p.kb_main + (K2 > 0 ? 1 : 0);
   p.swiglu_half = epi.half;
-  p.group = raster_group(p.m_tiles, p.n_tiles, BM, swiglu ? 256 : NF4_BN, p.K);
-  p.sq_slots = 8;
+  p.group = raster_group(p.m_tiles, p.n_tiles, rows_per_tile, swiglu ? 256 : NF4_BN, p.K);
+  p.sq_slots = pair_tiles ? 16 : 8;
   p.epi = epi;
   p.epi.sq_count = nullptr;
   p.err = err;
@@ -1575,8 +1965,10 @@ cudaError_t gemm_nf4(const Mat& A, const Nf4Mat& W, bool b_mn, const Mat* A2, co
     }
     *epi.sq_count = static_cast<int64_t>(p.m_tiles) * p.n_tiles * p.sq_slots;
   }
-#define RDT_NF4_CASE(BMJ, E) \
-  if (b_mn == (BMJ) && epi.kind == (E)) return launch_nf4<BMJ, E>(ta, tb2, nm, om, p, s);
+#define RDT_NF4_CASE(BMJ, E)                                                   \
+  if (b_mn == (BMJ) && epi.kind == (E))                                        \
+    return pair_tiles ? launch_nf4_pair<BMJ, E>(ta, tb2, nm, om, p, pairs_max, s) \
+                      : launch_nf4<BMJ, E>(ta, tb2, nm, om, p, s);
   // forward through W: y = x W^T (K-major)
   RDT_NF4_CASE(0, EPI_F32)
   RDT_NF4_CASE(0, EPI_F32_RESID)

@@ -96,7 +96,10 @@ void set_last_error(const char* msg);
 // Kernel-launch bookkeeping (librdt-wide): every launch site calls note_launch.
 void note_launch(int n = 1);
 // GEMM timing hook: called around each GEMM launch (see rdt_gemm_timing_arm).
-int64_t gemm_timing_before(cudaStream_t s, double flops);
+// kind: GEMM_KIND_SINGLE (one CTA per tile), GEMM_KIND_PAIR (CTA pair),
+// GEMM_KIND_NF4 (NF4-decoding kernel).
+enum GemmKind : int { GEMM_KIND_SINGLE = 0, GEMM_KIND_PAIR = 1, GEMM_KIND_NF4 = 2 };
+int64_t gemm_timing_before(cudaStream_t s, double flops, int kind);
 void gemm_timing_after(cudaStream_t s, int64_t slot);
 
 // Upper bound on the row count of any gain-gradient partials buffer.

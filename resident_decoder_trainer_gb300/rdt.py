@@ -81,7 +81,7 @@ def _load() -> ctypes.CDLL:
         "rdt_cast_bf16": (I32, [P, P, I64, P]),
         "rdt_last_error": (ctypes.c_char_p, []),
         "rdt_device_error": (I32, [P]),
-        "rdt_gemm_timing_arm": (I32, [P, P, I32]),
+        "rdt_gemm_timing_arm": (I32, [P, P, P, I32]),
         "rdt_gemm_timing_disarm": (I64, []),
         "rdt_launch_count": (I64, []),
         "rdt_sq_sum_noalloc": (I32, [P, P, I32, P, P]),
@@ -350,17 +350,26 @@ class GemmTimer:
         torch.cuda.synchronize()
         self._handles = (ctypes.c_void_p * (2 * capacity))(*[ev.cuda_event for ev in self.events])
         self._flops = (ctypes.c_double * capacity)()
+        self._kinds = (ctypes.c_int32 * capacity)()
         self.seen = 0
 
     def __enter__(self):
-        _check(lib().rdt_gemm_timing_arm(self._handles, self._flops, self.capacity))
+        _check(lib().rdt_gemm_timing_arm(self._handles, self._flops, self._kinds,
+                                         self.capacity))
         return self
 
     def __exit__(self, *exc):
         self.seen = lib().rdt_gemm_timing_disarm()
 
-    def results(self):
-        """[(flops, milliseconds)] for every recorded launch (call after a sync)."""
+    KINDS = ("single", "pair", "nf4")
+
+    def results(self, with_kind=False):
+        """[(flops, milliseconds)] (or (flops, ms, kind) with kind one of
+        KINDS) for every recorded launch (call after a sync)."""
         n = min(self.seen, self.capacity)
-        return [(self._flops[i], self.events[2 * i].elapsed_time(self.events[2 * i + 1]))
-                for i in range(n)]
+        out = []
+        for i in range(n):
+            ms = self.events[2 * i].elapsed_time(self.events[2 * i + 1])
+            out.append((self._flops[i], ms, self.KINDS[self._kinds[i]]) if with_kind
+                       else (self._flops[i], ms))
+        return out
