@@ -224,10 +224,14 @@ rdt_status rdt_adamw_step(float* w, const float* g, float* m, float* v, int64_t 
  * can be tested on its own: C[M, N] (fp32, row stride ldc) = A' B'^T over K,
  * with A' = A ([M, K], row stride lda) when a_mn == 0, or the transpose of A
  * given as [K, M] when a_mn == 1; likewise B' = B ([N, K]) or B^T with B
- * given as [K, N]. A, B bf16; lda, ldb multiples of 8; ldc a multiple of 4. */
+ * given as [K, N]. A, B bf16; lda, ldb multiples of 8; ldc a multiple of 4.
+ * split_ws (optional, 16-byte aligned, split_ws_floats fp32 elements): scratch
+ * that lets a problem with too few 128 x 256 output tiles to fill the GPU run
+ * as K-slices whose partials are then summed in slice order (the NF4 block's
+ * adapter GEMMs take this path); null: one pass over K. */
 rdt_status rdt_gemm(const rdt_bf16* A, int32_t a_mn, int64_t lda, const rdt_bf16* B,
                     int32_t b_mn, int64_t ldb, int32_t M, int32_t N, int32_t K, float* C,
-                    int64_t ldc, void* stream);
+                    int64_t ldc, float* split_ws, int64_t split_ws_floats, void* stream);
 
 /* The NF4 GEMM of the NF4-frozen block (CudaNf4TransformerBlock in
  * cuda_block.rs: frozen projection weights stored as packed 4-bit NormalFloat

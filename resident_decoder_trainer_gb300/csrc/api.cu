@@ -2,6 +2,7 @@
 // validation, carving of the caller's saved-activation and scratch buffers,
 // and the launch sequence of each call. Nothing here allocates device memory.
 #include <cmath>
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -374,6 +375,8 @@ struct Nf4Ws {
   bf16 *du_qkv, *du_o, *du_gu, *du_d;
   float* gain_sink;
   double* sqp;  // squared-sum slots of the adapter-gradient GEMMs
+  float* split;  // split-K partials of the adapter GEMMs (few output tiles, long K)
+  int64_t split_floats;
 };
 // Squared-sum slots the fourteen adapter-gradient GEMMs write at most.
 int64_t lora_sq_slots_bound(const Dims& m, int64_t r) {
@@ -396,6 +399,12 @@ size_t carve_nf4_ws(const Dims& m, int64_t r, int64_t B, int64_t S, void* base, 
   t.du_d = c.take<bf16>(T * r);
   t.gain_sink = c.take<float>(2 * m.H + 2 * m.d);
   t.sqp = c.take<double>(lora_sq_slots_bound(m, r));
+  // room for 8 K-slices of the widest [r..3r, out] adapter gradient or 16 of
+  // the [T, 3r] down-projections
+  const int64_t wide = std::max(std::max(m.H, m.I), std::max(m.qd, m.nqkv));
+  const int64_t t_pad = (T + 127) / 128 * 128;
+  t.split_floats = std::max<int64_t>(8 * 128 * wide, 16 * t_pad * 3 * r);
+  t.split = c.take<float>(t.split_floats);
   if (nw) *nw = t;
   return head + c.off;
 }
@@ -855,7 +864,7 @@ rdt_status rdt_adamw_step(float* w, const float* g, float* m, float* v, int64_t 
 
 rdt_status rdt_gemm(const rdt_bf16* A, int32_t a_mn, int64_t lda, const rdt_bf16* B,
                     int32_t b_mn, int64_t ldb, int32_t M, int32_t N, int32_t K, float* C,
-                    int64_t ldc, void* stream) {
+                    int64_t ldc, float* split_ws, int64_t split_ws_floats, void* stream) {
   if (!A || !B || !C) return fail(RDT_EINVAL, "null pointer");
   if (M < 1 || N < 1 || K < 1) return fail(RDT_EINVAL, "M, N, K must be >= 1");
   if (lda % 8 || ldb % 8 || ldc % 4 || !aligned16(A) || !aligned16(B) || !aligned16(C))
@@ -863,10 +872,14 @@ rdt_status rdt_gemm(const rdt_bf16* A, int32_t a_mn, int64_t lda, const rdt_bf16
   const int64_t arows = a_mn ? K : M, acols = a_mn ? M : K;
   const int64_t brows = b_mn ? K : N, bcols = b_mn ? N : K;
   if (lda < acols || ldb < bcols || ldc < N) return fail(RDT_EINVAL, "leading dimension too small");
+  if (split_ws && (!aligned16(split_ws) || split_ws_floats < 0))
+    return fail(RDT_EINVAL, "split_ws must be 16-byte aligned with a non-negative size");
   Epi e;
   e.kind = EPI_F32;
   e.out = C;
   e.ld_out = ldc;
+  e.split_ws = split_ws;
+  e.split_ws_floats = split_ws ? split_ws_floats : 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* err = device_error_ptr();
   RDT_GEMM(Mat{A, arows, acols, lda}, a_mn != 0, Mat{B, brows, bcols, ldb}, b_mn != 0, M, N, K, e,
@@ -1052,7 +1065,8 @@ rdt_status rdt_nf4_block_forward(const rdt_config* cfg, int32_t rank, float alph
   Nf4Saved nv;
   carve_nf4_saved(m, r, batch, seq, saved, &sv, &nv);
   BlockWs wk;
-  carve_nf4_ws(m, r, batch, seq, ws, &wk, nullptr);
+  Nf4Ws nw;
+  carve_nf4_ws(m, r, batch, seq, ws, &wk, &nw);
   const LoraShadow L = lora_shadow_layout(m, r, reinterpret_cast<const bf16*>(shadow));
   int64_t co[7], so[7];
   nf4_layout(m, co, so, nullptr, nullptr);
@@ -1068,6 +1082,8 @@ rdt_status rdt_nf4_block_forward(const rdt_config* cfg, int32_t rank, float alph
     e.out = u;
     e.ld_out = n;
     e.scale = sc;
+    e.split_ws = nw.split;
+    e.split_ws_floats = nw.split_floats;
     RDT_GEMM(Mat{xin, T, in, in}, false, Mat{a, n, in, in}, false, T, (int)n, (int)in, e, err, s);
     return RDT_OK;
   };
@@ -1193,6 +1209,8 @@ rdt_status rdt_nf4_block_backward(const rdt_config* cfg, int32_t rank, float alp
     e.out = du;
     e.ld_out = n;
     e.scale = sc;
+    e.split_ws = nw.split;
+    e.split_ws_floats = nw.split_floats;
     RDT_GEMM(Mat{dyb, T, out, out}, false, Mat{b, out, n, n}, true, T, (int)n, (int)out, e, err,
              s);
     return RDT_OK;
@@ -1205,6 +1223,8 @@ rdt_status rdt_nf4_block_backward(const rdt_config* cfg, int32_t rank, float alp
     e.kind = EPI_F32;
     e.out = G + lo[tensor];
     e.ld_out = N;
+    e.split_ws = nw.split;
+    e.split_ws_floats = nw.split_floats;
     if (grad_sq) {
       e.sq_part = nw.sqp + sq_n;
       e.sq_count = &sq_cnt;

@@ -18,6 +18,7 @@
 // the transposed cases are expressed through the UMMA descriptors, so no
 // operand is ever transposed in memory. Ragged M/N/K edges are zero-filled by
 // TMA and masked in the epilogue.
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -64,6 +65,11 @@ struct GemmParams {
   int group;        // rasterisation: row tiles per group (see tile_coords)
   int sq_slots;     // squared-sum slots per tile (8 single-CTA, 16 pair)
   int kb_main;      // NF4 GEMM: k-blocks of the decoded operand; the rest are the tail
+  // split-K (single-CTA kernel): work unit u is tile u % tiles over k-blocks
+  // [s kb_split, (s + 1) kb_split) with s = u / tiles; its fp32 partial lands
+  // in rows s m_pad + (tile rows) of the output. splits = 1: whole K.
+  int splits, kb_split, m_pad;
+  int m_epi;        // rows the epilogue may write (M, or splits m_pad)
   Epi epi;
   int* err;
 };
@@ -198,7 +204,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const OutMaps
   const Epi& e = p.epi;
   const int lane = st.lane;
   const int row = row0 + lane;
-  const bool row_ok = row < p.M;
+  const bool row_ok = row < p.m_epi;
   const int ncols = EPI == EPI_SWIGLU ? e.half : p.N;
   const int col_w = EPI == EPI_SWIGLU ? nt * 128 + half * 64 : nt * BN + half * (BN / 2);
   const uint32_t tcol_w = EPI == EPI_SWIGLU ? half * 64 : half * (BN / 2);
@@ -463,6 +469,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const int ntiles = p.m_tiles * p.n_tiles;
+  const int nunits = ntiles * p.splits;
   const uint32_t smem_base = smem_u32(smem);
 
   if (warp == 0) {
@@ -472,11 +479,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       uint32_t ph = 0;
       uint32_t pending = 0, pending_par = 0;  // stages with a load in flight
       bool ok = true;
-      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
         int mt, nt;
-        tile_coords(t, p, mt, nt);
+        tile_coords(u % ntiles, p, mt, nt);
         const int m0 = mt * BM;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        const int kb0 = (u / ntiles) * p.kb_split;
+        const int kb1 = min(p.k_blocks, kb0 + p.kb_split);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, ph ^ 1, p.err)) {
             ok = false;
             break;
@@ -532,14 +541,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       int acc = 0;
       uint32_t acc_ph = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
         if (!mbar_wait(tempty0 + 8 * acc, acc_ph ^ 1, p.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        const int kb0 = (u / ntiles) * p.kb_split;
+        const int kb1 = min(p.k_blocks, kb0 + p.kb_split);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(full0 + 8 * stage, ph, p.err)) {
             ok = false;
             break;
@@ -553,7 +564,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t ad = ad0 + static_cast<uint64_t>(k) * ((A_MN ? 2048 : 32) >> 4);
             const uint64_t bd = bd0 + static_cast<uint64_t>(k) * ((B_MN ? 2048 : 32) >> 4);
-            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0);
+            tc_mma_bf16(d_tmem, ad, bd, idesc, kb != kb0 || k != 0);
           }
           tc_commit(empty0 + 8 * stage);
           if (++stage == STAGES) {
@@ -579,12 +590,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     uint32_t ucnt = 0, eph = 0;
     int acc = 0;
     uint32_t acc_ph = 0;
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
       int mt, nt;
+      const int t = u % ntiles;
       tile_coords(t, p, mt, nt);
+      const int row0 = (u / ntiles) * p.m_pad + mt * BM + q * 32;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      if (!epilogue_tile<EPI, BN, OS::BYTES>(p, om, tbase, mt * BM + q * 32, nt, half, st, ucnt,
-                                             eph, tfull0 + 8 * acc, acc_ph, t, warp - 2))
+      if (!epilogue_tile<EPI, BN, OS::BYTES>(p, om, tbase, row0, nt, half, st, ucnt, eph,
+                                             tfull0 + 8 * acc, acc_ph, t, warp - 2))
         break;
       tc_fence_before();
       __syncwarp();
@@ -1567,8 +1580,8 @@ static cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const Ou
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  const int ntiles = p.m_tiles * p.n_tiles;
-  const int grid = ntiles < num_sms() ? ntiles : num_sms();
+  const int nunits = p.m_tiles * p.n_tiles * p.splits;
+  const int grid = nunits < num_sms() ? nunits : num_sms();
   const int64_t slot = gemm_timing_before(s, 2.0 * p.M * (double)p.N * p.K, GEMM_KIND_SINGLE);
   note_launch();
   gemm_kernel<A_MN, B_MN, EPI, BN><<<grid, GEMM_THREADS, Tile<BN>::SMEM, s>>>(ta, tb, om, p);
@@ -1655,6 +1668,135 @@ int64_t gemm_sq_slots_bound(int M, int N) {
   return static_cast<int64_t>((M + BM - 1) / BM) * ((N + 127) / 128) * 16;
 }
 
+// Sum of the split-K partials (fp32 slabs of m_pad x ldw, added in split
+// order) with the F32 or BF16 epilogue, four columns per thread (N % 4 == 0;
+// the host falls back to one); F32 also writes one fp64 squared-sum slot per
+// block (fixed grid and order: deterministic).
+template <int V>
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(
+    const float* __restrict__ ws, int splits, int64_t slab, int64_t ldw, int M, int N, int kind,
+    void* __restrict__ out, int64_t ld_out, float scale, double* __restrict__ sq_part) {
+  __shared__ double red[8];
+  double acc = 0.0;
+  const int nv = N / V;
+  const int64_t n = static_cast<int64_t>(M) * nv;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / nv;
+    const int64_t c = (i - r * nv) * V;
+    const float* w = ws + r * ldw + c;
+    float v[V];
+    if constexpr (V == 4) {
+      const float4 a = *reinterpret_cast<const float4*>(w);
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    } else {
+      v[0] = w[0];
+    }
+    for (int sp = 1; sp < splits; ++sp) {
+      if constexpr (V == 4) {
+        const float4 a = *reinterpret_cast<const float4*>(w + sp * slab);
+        v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w;
+      } else {
+        v[0] += w[sp * slab];
+      }
+    }
+    if (kind == EPI_F32) {
+      float* o = static_cast<float*>(out) + r * ld_out + c;
+      if constexpr (V == 4) *reinterpret_cast<float4*>(o) = make_float4(v[0], v[1], v[2], v[3]);
+      else o[0] = v[0];
+#pragma unroll
+      for (int k = 0; k < V; ++k) acc += static_cast<double>(v[k]) * v[k];
+    } else {
+      bf16* o = static_cast<bf16*>(out) + r * ld_out + c;
+      if constexpr (V == 4)
+        *reinterpret_cast<uint2*>(o) =
+            make_uint2(pack_bf16x2(scale * v[0], scale * v[1]), pack_bf16x2(scale * v[2], scale * v[3]));
+      else
+        o[0] = __float2bfloat16_rn(scale * v[0]);
+    }
+  }
+  if (!sq_part) return;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double t = 0.0;
+    for (int w = 0; w < 8; ++w) t += red[w];
+    sq_part[blockIdx.x] = t;
+  }
+}
+
+// C = A' B'^T as `splits` K-slices on single-CTA 128 x 256 tiles whose fp32
+// partials go to epi.split_ws, then splitk_reduce_kernel.
+static cudaError_t gemm_splitk(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N,
+                               int K, int splits, const Epi& epi, int* err, cudaStream_t s,
+                               const char** why) {
+  const int kbs = (K + BK - 1) / BK;
+  const int kb_split = (kbs + splits - 1) / splits;
+  splits = (kbs + kb_split - 1) / kb_split;  // no empty slice
+  const int m_tiles = (M + BM - 1) / BM;
+  const int64_t m_pad = static_cast<int64_t>(m_tiles) * BM;
+  const int64_t ldw = (N + 3) / 4 * 4;
+  Epi pe;
+  pe.kind = EPI_F32;
+  pe.out = epi.split_ws;
+  pe.ld_out = ldw;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, A, a_mn ? 64 : 128) || !make_map(&tb, B, 64)) {
+    *why = "gemm: cuTensorMapEncodeTiled failed";
+    return cudaErrorInvalidValue;
+  }
+  OutMaps om;
+  if (!make_out_maps(&om, pe, static_cast<int>(splits * m_pad), N, OutStageBytes(256))) {
+    *why = "gemm: split-K scratch needs 16-byte alignment";
+    return cudaErrorInvalidValue;
+  }
+  GemmParams p;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.m_tiles = m_tiles;
+  p.n_tiles = (N + 255) / 256;
+  p.k_blocks = kbs;
+  p.swiglu_half = 0;
+  p.group = raster_group(p.m_tiles, p.n_tiles, BM, 256, K);
+  p.sq_slots = 8;
+  p.kb_main = kbs;
+  p.splits = splits;
+  p.kb_split = kb_split;
+  p.m_pad = static_cast<int>(m_pad);
+  p.m_epi = static_cast<int>(splits * m_pad);
+  p.epi = pe;
+  p.err = err;
+  cudaError_t e = cudaErrorInvalidValue;
+  if (!a_mn && !b_mn) e = launch<0, 0, EPI_F32, 256>(ta, tb, om, p, s);
+  else if (!a_mn && b_mn) e = launch<0, 1, EPI_F32, 256>(ta, tb, om, p, s);
+  else if (a_mn && b_mn) e = launch<1, 1, EPI_F32, 256>(ta, tb, om, p, s);
+  else *why = "gemm: unsupported operand-major combination for split-K";
+  if (e != cudaSuccess) return e;
+  // four columns per thread when rows of the output stay 16 (fp32) / 8 (bf16) byte aligned
+  const int es = epi.kind == EPI_F32 ? 4 : 2;
+  const bool vec = N % 4 == 0 && (epi.ld_out * es) % (4 * es) == 0 &&
+                   (reinterpret_cast<uintptr_t>(epi.out) % (4 * es)) == 0;
+  const int64_t items = static_cast<int64_t>(M) * (vec ? N / 4 : N);
+  const bool sq = epi.kind == EPI_F32 && epi.sq_part;
+  int64_t nblk = (items + 255) / 256;
+  nblk = std::max<int64_t>(1, std::min<int64_t>(nblk, sq ? gemm_sq_slots_bound(M, N)
+                                                         : 8LL * num_sms()));
+  if (sq) *epi.sq_count = nblk;
+  note_launch();
+  if (vec)
+    splitk_reduce_kernel<4><<<static_cast<unsigned>(nblk), 256, 0, s>>>(
+        epi.split_ws, splits, m_pad * ldw, ldw, M, N, epi.kind, epi.out, epi.ld_out, epi.scale,
+        sq ? epi.sq_part : nullptr);
+  else
+    splitk_reduce_kernel<1><<<static_cast<unsigned>(nblk), 256, 0, s>>>(
+        epi.split_ws, splits, m_pad * ldw, ldw, M, N, epi.kind, epi.out, epi.ld_out, epi.scale,
+        sq ? epi.sq_part : nullptr);
+  return cudaGetLastError();
+}
+
 cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N, int K,
                  const Epi& epi, int* err, cudaStream_t s, const char** why) {
   if (M <= 0 || N <= 0 || K <= 0) {
@@ -1703,6 +1845,16 @@ cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N,
       pair_tiles = true;
     }
   }
+  if (epi.split_ws && (epi.kind == EPI_F32 || epi.kind == EPI_BF16)) {
+    const int64_t tiles1 = (int64_t)((M + BM - 1) / BM) * ((N + 255) / 256);
+    const int kbs = (K + BK - 1) / BK;
+    const int64_t m_pad = (int64_t)((M + BM - 1) / BM) * BM;
+    const int64_t ldw = (N + 3) / 4 * 4;
+    int64_t splits = std::min<int64_t>(sms / tiles1, kbs / 4);
+    while (splits > 1 && splits * m_pad * ldw > epi.split_ws_floats) --splits;
+    if (splits >= 2)
+      return gemm_splitk(A, a_mn, B, b_mn, M, N, K, static_cast<int>(splits), epi, err, s, why);
+  }
   CUtensorMap ta, tb;
   const int b_box = (pair_tiles && !b_mn) ? bn / 2 : 64;
   if (!make_map(&ta, A, a_mn ? 64 : 128) || !make_map(&tb, B, b_box)) {
@@ -1725,6 +1877,10 @@ cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N,
   p.swiglu_half = epi.half;
   p.group = raster_group(p.m_tiles, p.n_tiles, rows_per_tile, swiglu ? 256 : bn, K);
   p.sq_slots = pair_tiles ? 16 : 8;
+  p.splits = 1;
+  p.kb_split = p.k_blocks;
+  p.m_pad = p.m_tiles * rows_per_tile;
+  p.m_epi = M;
   p.epi = epi;
   p.epi.sq_count = nullptr;
   p.err = err;
@@ -1955,6 +2111,10 @@ cudaError_t gemm_nf4(const Mat& A, const Nf4Mat& W, bool b_mn, const Mat* A2, co
   p.swiglu_half = epi.half;
   p.group = raster_group(p.m_tiles, p.n_tiles, rows_per_tile, swiglu ? 256 : NF4_BN, p.K);
   p.sq_slots = pair_tiles ? 16 : 8;
+  p.splits = 1;
+  p.kb_split = p.k_blocks;
+  p.m_pad = p.m_tiles * rows_per_tile;
+  p.m_epi = M;
   p.epi = epi;
   p.epi.sq_count = nullptr;
   p.err = err;

@@ -42,6 +42,11 @@ struct Epi {
   int64_t* sq_count = nullptr;
   // EPI_BF16 only: out = bf16(scale * acc)
   float scale = 1.0f;
+  // F32 / BF16: fp32 scratch gemm() may use to split K across CTAs when the
+  // problem has too few output tiles to fill the GPU (split_ws_floats floats,
+  // 16-byte aligned); the partials are summed in a fixed order.
+  float* split_ws = nullptr;
+  int64_t split_ws_floats = 0;
 };
 
 // Upper bound of the squared-sum slots a gemm() of [M, N] writes.

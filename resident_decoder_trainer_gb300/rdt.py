@@ -75,7 +75,7 @@ def _load() -> ctypes.CDLL:
         "rdt_sq_sum": (I32, [P, P, I32, P, P, SZ, P]),
         "rdt_clip_scale": (I32, [P, F32, P, P, P]),
         "rdt_adamw_step": (I32, [P, P, P, P, I64, P, P, I32, F32, F32, F32, F32, F32, P, P]),
-        "rdt_gemm": (I32, [P, I32, I64, P, I32, I64, I32, I32, I32, P, I64, P]),
+        "rdt_gemm": (I32, [P, I32, I64, P, I32, I64, I32, I32, I32, P, I64, P, I64, P]),
         "rdt_gemm_nf4": (I32, [P, I64, P, P, I64, I64, I32, P, I64, P, I64, I32, I32, P, I64,
                                P]),
         "rdt_cast_bf16": (I32, [P, P, I64, P]),
@@ -229,10 +229,12 @@ def adamw_step(w, g, m, v, step, lr, beta1, beta2, eps, weight_decay, scale=None
                                 float(weight_decay), _ptr(w_bf16), _stream(stream)))
 
 
-def gemm(a, a_mn, b, b_mn, M, N, K, c, stream=None):
-    """c[M, N] = a' b'^T (see include/rdt.h); a, b bf16 2-D, c fp32 2-D."""
+def gemm(a, a_mn, b, b_mn, M, N, K, c, split_ws=None, stream=None):
+    """c[M, N] = a' b'^T (see include/rdt.h); a, b bf16 2-D, c fp32 2-D;
+    split_ws: optional fp32 scratch for the split-K path."""
     _check(lib().rdt_gemm(_ptr(a), int(a_mn), a.stride(0), _ptr(b), int(b_mn), b.stride(0), M, N,
-                          K, _ptr(c), c.stride(0), _stream(stream)))
+                          K, _ptr(c), c.stride(0), _ptr(split_ws),
+                          0 if split_ws is None else split_ws.numel(), _stream(stream)))
 
 
 def gemm_nf4(a, codes, scales, w_rows, w_cols, b_mn, c, a2=None, b2=None, stream=None):

@@ -56,6 +56,43 @@ def test_gemm_matches_fp32_matmul_of_bf16_operands(a_mn, b_mn, M, N, K):
     assert torch.isnan(c[:, N:]).all()  # nothing written past N
 
 
+SPLITK_SHAPES = [(2048, 16, 2560, 0, 0), (2048, 48, 9728, 0, 1), (16, 2560, 2048, 1, 1),
+                 (40, 1000, 3000, 1, 1), (300, 24, 4100, 0, 1), (9728, 16, 2048, 1, 1)]
+
+
+@pytest.mark.parametrize("M,N,K,a_mn,b_mn", SPLITK_SHAPES)
+def test_split_k_gemm_matches_fp64(M, N, K, a_mn, b_mn):
+    """Skinny problems (few 128 x 256 output tiles, long K) given scratch run as
+    K-slices summed in slice order: same values as the fp64 product, nothing
+    written past N, and bit-identical on a second run."""
+    g = torch.Generator(device="cpu").manual_seed(M + 3 * N + 7 * K)
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    B = torch.randn(N, K, generator=g).to(torch.bfloat16)
+    ref = A.double() @ B.double().T
+
+    def stored(X, mn):
+        Y = X.T.contiguous() if mn else X.contiguous()
+        ld = (Y.shape[1] + 7) // 8 * 8
+        buf = torch.zeros(Y.shape[0], ld, dtype=torch.bfloat16)
+        buf[:, :Y.shape[1]] = Y
+        return buf.cuda()
+
+    a, b = stored(A, a_mn), stored(B, b_mn)
+    ldc = (N + 3) // 4 * 4 + 4
+    ws = torch.empty(16 << 20, device="cuda")
+    outs = []
+    for _ in range(2):
+        c = torch.full((M, ldc), float("nan"), device="cuda")
+        rdt.gemm(a, a_mn, b, b_mn, M, N, K, c, split_ws=ws)
+        torch.cuda.synchronize()
+        outs.append(c)
+    out = outs[0][:, :N].double().cpu()
+    assert torch.isfinite(out).all()
+    assert rel_l2(out.numpy(), ref.numpy()) < 1e-5
+    assert torch.isnan(outs[0][:, N:]).all()
+    assert torch.equal(outs[0][:, :N], outs[1][:, :N])
+
+
 # ------------------------------------------------------------------ block
 def _block_case(shape, seed=0):
     blk, x, dy = synth.make_block_inputs(shape, seed)

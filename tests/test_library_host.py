@@ -92,7 +92,7 @@ def test_null_and_misaligned_arguments_fail_before_any_launch(lib):
     assert st == rdt.RDT_EINVAL and b"aligned" in lib.rdt_last_error()
     st = lib.rdt_clip_scale(P(16), ctypes.c_float(0.0), P(16), None, None)
     assert st == rdt.RDT_EINVAL
-    st = lib.rdt_gemm(P(16), 0, 12, P(16), 0, 16, 8, 8, 8, P(16), 8, None)
+    st = lib.rdt_gemm(P(16), 0, 12, P(16), 0, 16, 8, 8, 8, P(16), 8, None, 0, None)
     assert st == rdt.RDT_EINVAL
 
 
