@@ -244,11 +244,14 @@ rdt_status rdt_gemm(const rdt_bf16* A, int32_t a_mn, int64_t lda, const rdt_bf16
  * b_mn == 0: B = W (N = w_rows, K1 = w_cols; y = x W^T), B2 [N, K2] (ldb2);
  * b_mn == 1: B = W^T (N = w_cols, K1 = w_rows; dX = dY W), B2 [K2, N].
  * w_cols % 256 == 0 and w_rows % 64 == 0; leading dimensions in elements,
- * bf16 ones multiples of 8, ldc a multiple of 4; 16-byte aligned pointers. */
+ * bf16 ones multiples of 8, ldc a multiple of 4; 16-byte aligned pointers.
+ * split_ws (optional, as in rdt_gemm): scratch for running the problem as
+ * K-slices when its tiles would leave most of the GPU idle. */
 rdt_status rdt_gemm_nf4(const rdt_bf16* A, int64_t lda, const uint8_t* codes,
                         const float* scales, int64_t w_rows, int64_t w_cols, int32_t b_mn,
                         const rdt_bf16* A2, int64_t lda2, const rdt_bf16* B2, int64_t ldb2,
-                        int32_t K2, int32_t M, float* C, int64_t ldc, void* stream);
+                        int32_t K2, int32_t M, float* C, int64_t ldc, float* split_ws,
+                        int64_t split_ws_floats, void* stream);
 
 /* dst[i] = bf16(src[i]) with round-to-nearest-even; n elements, 16-byte aligned. */
 rdt_status rdt_cast_bf16(const float* src, rdt_bf16* dst, int64_t n, void* stream);

@@ -399,11 +399,14 @@ size_t carve_nf4_ws(const Dims& m, int64_t r, int64_t B, int64_t S, void* base, 
   t.du_d = c.take<bf16>(T * r);
   t.gain_sink = c.take<float>(2 * m.H + 2 * m.d);
   t.sqp = c.take<double>(lora_sq_slots_bound(m, r));
-  // room for 8 K-slices of the widest [r..3r, out] adapter gradient or 16 of
+  // room for 8 K-slices of the widest [r..3r, out] adapter gradient, 16 of
   // the [T, 3r] down-projections
   const int64_t wide = std::max(std::max(m.H, m.I), std::max(m.qd, m.nqkv));
   const int64_t t_pad = (T + 127) / 128 * 128;
-  t.split_floats = std::max<int64_t>(8 * 128 * wide, 16 * t_pad * 3 * r);
+  // ... or 4 of the [T, hidden] outputs of the NF4 projections (256-row pair tiles)
+  const int64_t t_pad2 = (T + 255) / 256 * 256;
+  t.split_floats = std::max<int64_t>(std::max<int64_t>(8 * 128 * wide, 16 * t_pad * 3 * r),
+                                     4 * t_pad2 * m.H);
   t.split = c.take<float>(t.split_floats);
   if (nw) *nw = t;
   return head + c.off;
@@ -890,7 +893,8 @@ rdt_status rdt_gemm(const rdt_bf16* A, int32_t a_mn, int64_t lda, const rdt_bf16
 rdt_status rdt_gemm_nf4(const rdt_bf16* A, int64_t lda, const uint8_t* codes,
                         const float* scales, int64_t w_rows, int64_t w_cols, int32_t b_mn,
                         const rdt_bf16* A2, int64_t lda2, const rdt_bf16* B2, int64_t ldb2,
-                        int32_t K2, int32_t M, float* C, int64_t ldc, void* stream) {
+                        int32_t K2, int32_t M, float* C, int64_t ldc, float* split_ws,
+                        int64_t split_ws_floats, void* stream) {
   if (!A || !codes || !scales || !C) return fail(RDT_EINVAL, "null pointer");
   if (M < 1 || w_rows < 1 || w_cols < 1) return fail(RDT_EINVAL, "M and W's dims must be >= 1");
   if (K2 < 0 || K2 > 64 || (K2 > 0 && (!A2 || !B2)))
@@ -903,10 +907,14 @@ rdt_status rdt_gemm_nf4(const rdt_bf16* A, int64_t lda, const uint8_t* codes,
   if (K2 > 0 && (lda2 % 8 || ldb2 % 8 || lda2 < K2 || ldb2 < (b_mn ? N : K2) ||
                  !aligned16(A2) || !aligned16(B2)))
     return fail(RDT_EINVAL, "tail operands: lda2 >= K2, ldb2 >= its row length, multiples of 8");
+  if (split_ws && (!aligned16(split_ws) || split_ws_floats < 0))
+    return fail(RDT_EINVAL, "split_ws must be 16-byte aligned with a non-negative size");
   Epi e;
   e.kind = EPI_F32;
   e.out = C;
   e.ld_out = ldc;
+  e.split_ws = split_ws;
+  e.split_ws_floats = split_ws ? split_ws_floats : 0;
   const Mat a{A, M, K1, lda};
   const Mat a2{A2, M, K2, lda2};
   const Mat b2{B2, b_mn ? K2 : N, b_mn ? N : K2, ldb2};
@@ -1099,6 +1107,8 @@ rdt_status rdt_nf4_block_forward(const rdt_config* cfg, int32_t rank, float alph
     e.out = sv.qkv;
     e.ld_out = m.nqkv;
     const Mat a2{nv.u_qkv, T, 3 * r, 3 * r}, b2{L.b_qkv, m.nqkv, 3 * r, 3 * r};
+    e.split_ws = nw.split;
+    e.split_ws_floats = nw.split_floats;
     RDT_GEMM_NF4(Mat{sv.xn, T, m.H, m.H}, W(0, m.nqkv, m.H), false, &a2, &b2, (int)(3 * r), T, e,
                  err, s);
   }
@@ -1123,6 +1133,8 @@ rdt_status rdt_nf4_block_forward(const rdt_config* cfg, int32_t rank, float alph
     e.resid = x;
     e.ld_resid = m.H;
     const Mat a2{nv.u_o, T, r, r}, b2{L.b_o, m.H, r, r};
+    e.split_ws = nw.split;
+    e.split_ws_floats = nw.split_floats;
     RDT_GEMM_NF4(Mat{sv.o, T, m.qd, m.qd}, W(3, m.H, m.qd), false, &a2, &b2, (int)r, T, e, err, s);
   }
   // post-attention RMSNorm
@@ -1151,6 +1163,8 @@ rdt_status rdt_nf4_block_forward(const rdt_config* cfg, int32_t rank, float alph
     e.resid = sv.r1;
     e.ld_resid = m.H;
     const Mat a2{nv.u_d, T, r, r}, b2{L.b_d, m.H, r, r};
+    e.split_ws = nw.split;
+    e.split_ws_floats = nw.split_floats;
     RDT_GEMM_NF4(Mat{sv.s, T, m.I, m.I}, W(6, m.H, m.I), false, &a2, &b2, (int)r, T, e, err, s);
   }
   return RDT_OK;
@@ -1261,6 +1275,8 @@ rdt_status rdt_nf4_block_backward(const rdt_config* cfg, int32_t rank, float alp
     e.out = wk.dxn;
     e.ld_out = m.H;
     const Mat a2{nw.du_gu, T, 2 * r, 2 * r}, b2{L.a_gu, 2 * r, m.H, m.H};
+    e.split_ws = nw.split;
+    e.split_ws_floats = nw.split_floats;
     RDT_GEMM_NF4(Mat{wk.dgu, T, 2 * m.I, 2 * m.I}, W(4, 2 * m.I, m.H), true, &a2, &b2,
                  (int)(2 * r), T, e, err, s);
   }
@@ -1319,6 +1335,8 @@ rdt_status rdt_nf4_block_backward(const rdt_config* cfg, int32_t rank, float alp
     e.out = wk.dxn;
     e.ld_out = m.H;
     const Mat a2{nw.du_qkv, T, 3 * r, 3 * r}, b2{L.a_qkv, 3 * r, m.H, m.H};
+    e.split_ws = nw.split;
+    e.split_ws_floats = nw.split_floats;
     RDT_GEMM_NF4(Mat{wk.dqkv, T, m.nqkv, m.nqkv}, W(0, m.nqkv, m.H), true, &a2, &b2, (int)(3 * r),
                  T, e, err, s);
   }

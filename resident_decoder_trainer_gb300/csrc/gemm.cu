@@ -1056,6 +1056,7 @@ __global__ void __launch_bounds__(NF4_THREADS, 1)
   const uint32_t tempty_even = mapa_shared(tempty0, 0);
 
   const int ntiles = p.m_tiles * p.n_tiles;  // m_tiles counts 256-row pair tiles
+  const int nunits = ntiles * p.splits;       // tiles x K-slices
   const uint32_t smem_base = smem_u32(smem);
 
   if (warp == 0) {
@@ -1064,14 +1065,16 @@ __global__ void __launch_bounds__(NF4_THREADS, 1)
       int stage = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int t = pair; t < ntiles && ok; t += npairs) {
+      for (int u = pair; u < nunits && ok; u += npairs) {
         int mt, nt;
-        tile_coords(t, p, mt, nt);
+        tile_coords(u % ntiles, p, mt, nt);
         const int m0 = (2 * mt + static_cast<int>(rank)) * BM;
+        const int kb0 = (u / ntiles) * p.kb_split;
+        const int kb1 = min(p.k_blocks, kb0 + p.kb_split);
         // first of this CTA's 128 B rows (K-major) / columns (MN-major)
         const int r0 = (EPI == EPI_SWIGLU) ? nt * 128 + static_cast<int>(rank) * p.swiglu_half
                                            : nt * BN + static_cast<int>(rank) * BH;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, ph ^ 1, p.err)) {
             ok = false;
             break;
@@ -1134,14 +1137,16 @@ __global__ void __launch_bounds__(NF4_THREADS, 1)
       int acc = 0;
       uint32_t acc_ph = 0;
       bool ok = true;
-      for (int t = pair; t < ntiles && ok; t += npairs) {
+      for (int u = pair; u < nunits && ok; u += npairs) {
         if (!mbar_wait_cluster(tempty0 + 8 * acc, acc_ph ^ 1, p.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        const int kb0 = (u / ntiles) * p.kb_split;
+        const int kb1 = min(p.k_blocks, kb0 + p.kb_split);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(full0 + 8 * stage, ph, p.err)) {
             ok = false;
             break;
@@ -1153,7 +1158,7 @@ __global__ void __launch_bounds__(NF4_THREADS, 1)
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t ad = ad0 + static_cast<uint64_t>(k) * (32 >> 4);
             const uint64_t bd = bd0 + static_cast<uint64_t>(k) * ((B_MN ? 2048 : 32) >> 4);
-            tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
+            tc_mma_bf16_pair(d_tmem, ad, bd, idesc, kb != kb0 || k != 0);
           }
           tc_commit_pair_mc(empty0 + 8 * stage, 0x3);
           if (++stage == STAGES) {
@@ -1178,12 +1183,14 @@ __global__ void __launch_bounds__(NF4_THREADS, 1)
     uint32_t ucnt = 0, eph = 0;
     int acc = 0;
     uint32_t acc_ph = 0;
-    for (int t = pair; t < ntiles; t += npairs) {
+    for (int u = pair; u < nunits; u += npairs) {
       int mt, nt;
+      const int t = u % ntiles;
       tile_coords(t, p, mt, nt);
       const int mrow = 2 * mt + static_cast<int>(rank);
+      const int row0 = (u / ntiles) * p.m_pad + mrow * BM + q * 32;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      if (!epilogue_tile<EPI, BN, OS::BYTES>(p, om, tbase, mrow * BM + q * 32, nt, half, st,
+      if (!epilogue_tile<EPI, BN, OS::BYTES>(p, om, tbase, row0, nt, half, st,
                                              ucnt, eph, tfull0 + 8 * acc, acc_ph, t,
                                              static_cast<int>(rank) * 8 + (warp - 2)))
         break;
@@ -1201,8 +1208,10 @@ __global__ void __launch_bounds__(NF4_THREADS, 1)
     int stage = 0;
     uint32_t ph = 0;
     bool ok = true;
-    for (int t = pair; t < ntiles && ok; t += npairs) {
-      for (int kb = 0; kb < p.k_blocks; ++kb) {
+    for (int u = pair; u < nunits && ok; u += npairs) {
+      const int kb0 = (u / ntiles) * p.kb_split;
+      const int kb1 = min(p.k_blocks, kb0 + p.kb_split);
+      for (int kb = kb0; kb < kb1; ++kb) {
         if (!warp_wait(raw0 + 8 * stage, ph, p.err)) {
           ok = false;
           break;
@@ -1669,13 +1678,14 @@ int64_t gemm_sq_slots_bound(int M, int N) {
 }
 
 // Sum of the split-K partials (fp32 slabs of m_pad x ldw, added in split
-// order) with the F32 or BF16 epilogue, four columns per thread (N % 4 == 0;
-// the host falls back to one); F32 also writes one fp64 squared-sum slot per
-// block (fixed grid and order: deterministic).
+// order) with the F32, F32_RESID or BF16 epilogue, four columns per thread
+// (N % 4 == 0; the host falls back to one); F32 also writes one fp64
+// squared-sum slot per block (fixed grid and order: deterministic).
 template <int V>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(
     const float* __restrict__ ws, int splits, int64_t slab, int64_t ldw, int M, int N, int kind,
-    void* __restrict__ out, int64_t ld_out, float scale, double* __restrict__ sq_part) {
+    void* __restrict__ out, int64_t ld_out, float scale, const float* __restrict__ resid,
+    int64_t ld_resid, double* __restrict__ sq_part) {
   __shared__ double red[8];
   double acc = 0.0;
   const int nv = N / V;
@@ -1700,7 +1710,16 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(
         v[0] += w[sp * slab];
       }
     }
-    if (kind == EPI_F32) {
+    if (kind == EPI_F32_RESID) {
+      const float* rs = resid + r * ld_resid + c;
+      if constexpr (V == 4) {
+        const float4 a = *reinterpret_cast<const float4*>(rs);
+        v[0] = a.x + v[0]; v[1] = a.y + v[1]; v[2] = a.z + v[2]; v[3] = a.w + v[3];
+      } else {
+        v[0] = rs[0] + v[0];
+      }
+    }
+    if (kind == EPI_F32 || kind == EPI_F32_RESID) {
       float* o = static_cast<float*>(out) + r * ld_out + c;
       if constexpr (V == 4) *reinterpret_cast<float4*>(o) = make_float4(v[0], v[1], v[2], v[3]);
       else o[0] = v[0];
@@ -1725,6 +1744,33 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(
     for (int w = 0; w < 8; ++w) t += red[w];
     sq_part[blockIdx.x] = t;
   }
+}
+
+// Launches splitk_reduce_kernel over partial slabs of m_pad x ldw in epi.split_ws.
+static cudaError_t splitk_reduce(const Epi& epi, int splits, int64_t m_pad, int64_t ldw, int M,
+                                 int N, cudaStream_t s) {
+  // four columns per thread when every row stays 16 (fp32) / 8 (bf16) byte aligned
+  const int es = epi.kind == EPI_BF16 ? 2 : 4;
+  bool vec = N % 4 == 0 && epi.ld_out % 4 == 0 &&
+             (reinterpret_cast<uintptr_t>(epi.out) % (4 * es)) == 0;
+  if (epi.kind == EPI_F32_RESID)
+    vec = vec && epi.ld_resid % 4 == 0 && (reinterpret_cast<uintptr_t>(epi.resid) % 16) == 0;
+  const int64_t items = static_cast<int64_t>(M) * (vec ? N / 4 : N);
+  const bool sq = epi.kind == EPI_F32 && epi.sq_part;
+  int64_t nblk = (items + 255) / 256;
+  nblk = std::max<int64_t>(1, std::min<int64_t>(nblk, sq ? gemm_sq_slots_bound(M, N)
+                                                         : 8LL * num_sms()));
+  if (sq) *epi.sq_count = nblk;
+  note_launch();
+  if (vec)
+    splitk_reduce_kernel<4><<<static_cast<unsigned>(nblk), 256, 0, s>>>(
+        epi.split_ws, splits, m_pad * ldw, ldw, M, N, epi.kind, epi.out, epi.ld_out, epi.scale,
+        epi.resid, epi.ld_resid, sq ? epi.sq_part : nullptr);
+  else
+    splitk_reduce_kernel<1><<<static_cast<unsigned>(nblk), 256, 0, s>>>(
+        epi.split_ws, splits, m_pad * ldw, ldw, M, N, epi.kind, epi.out, epi.ld_out, epi.scale,
+        epi.resid, epi.ld_resid, sq ? epi.sq_part : nullptr);
+  return cudaGetLastError();
 }
 
 // C = A' B'^T as `splits` K-slices on single-CTA 128 x 256 tiles whose fp32
@@ -1775,26 +1821,7 @@ static cudaError_t gemm_splitk(const Mat& A, bool a_mn, const Mat& B, bool b_mn,
   else if (a_mn && b_mn) e = launch<1, 1, EPI_F32, 256>(ta, tb, om, p, s);
   else *why = "gemm: unsupported operand-major combination for split-K";
   if (e != cudaSuccess) return e;
-  // four columns per thread when rows of the output stay 16 (fp32) / 8 (bf16) byte aligned
-  const int es = epi.kind == EPI_F32 ? 4 : 2;
-  const bool vec = N % 4 == 0 && (epi.ld_out * es) % (4 * es) == 0 &&
-                   (reinterpret_cast<uintptr_t>(epi.out) % (4 * es)) == 0;
-  const int64_t items = static_cast<int64_t>(M) * (vec ? N / 4 : N);
-  const bool sq = epi.kind == EPI_F32 && epi.sq_part;
-  int64_t nblk = (items + 255) / 256;
-  nblk = std::max<int64_t>(1, std::min<int64_t>(nblk, sq ? gemm_sq_slots_bound(M, N)
-                                                         : 8LL * num_sms()));
-  if (sq) *epi.sq_count = nblk;
-  note_launch();
-  if (vec)
-    splitk_reduce_kernel<4><<<static_cast<unsigned>(nblk), 256, 0, s>>>(
-        epi.split_ws, splits, m_pad * ldw, ldw, M, N, epi.kind, epi.out, epi.ld_out, epi.scale,
-        sq ? epi.sq_part : nullptr);
-  else
-    splitk_reduce_kernel<1><<<static_cast<unsigned>(nblk), 256, 0, s>>>(
-        epi.split_ws, splits, m_pad * ldw, ldw, M, N, epi.kind, epi.out, epi.ld_out, epi.scale,
-        sq ? epi.sq_part : nullptr);
-  return cudaGetLastError();
+  return splitk_reduce(epi, splits, m_pad, ldw, M, N, s);
 }
 
 cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N, int K,
@@ -1972,8 +1999,8 @@ static cudaError_t launch_nf4_pair(const CUtensorMap& ta, const CUtensorMap& tb2
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  const int ntiles = p.m_tiles * p.n_tiles;
-  const int pairs = ntiles < max_pairs ? ntiles : max_pairs;
+  const int nunits = p.m_tiles * p.n_tiles * p.splits;
+  const int pairs = nunits < max_pairs ? nunits : max_pairs;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs, 1, 1);
   cfg.blockDim = dim3(NF4_THREADS, 1, 1);
@@ -2124,6 +2151,54 @@ cudaError_t gemm_nf4(const Mat& A, const Nf4Mat& W, bool b_mn, const Mat* A2, co
       return cudaErrorInvalidValue;
     }
     *epi.sq_count = static_cast<int64_t>(p.m_tiles) * p.n_tiles * p.sq_slots;
+  }
+  // K-slices for pair tiles that would leave most of a wave idle (the N = 2560
+  // outputs of a 2048-token step: 80 tiles on 76 pairs). Estimated time =
+  // rounds of work units x one slice's share of a tile (a pair-tile at about
+  // 1 PFLOP/s over the pairs) + the partials' round trip through memory; the
+  // fp32 partials are then summed in slice order with the epilogue applied.
+  if (pair_tiles && (epi.kind == EPI_F32 || epi.kind == EPI_F32_RESID) && !epi.sq_part &&
+      epi.split_ws) {
+    const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+    const int64_t m_pad = static_cast<int64_t>(p.m_tiles) * 2 * BM;
+    const int64_t ldw = (N + 3) / 4 * 4;
+    const double tile_us = 2.0 * 256 * 256 * p.K * pairs_max / 1.0e15 * 1e6;
+    auto cost = [&](int sl) {
+      const double rounds = static_cast<double>((tiles * sl + pairs_max - 1) / pairs_max);
+      double c = rounds * tile_us / sl;
+      if (sl > 1) c += (sl + 2) * static_cast<double>(M) * N * 4 / 5.0e12 * 1e6 + 3.0;
+      return c;
+    };
+    int best = 1;
+    double best_cost = cost(1);
+    for (int sl = 2; sl <= 4; ++sl) {
+      if (sl * m_pad * ldw > epi.split_ws_floats || p.k_blocks < 4 * sl) break;
+      const double c = cost(sl);
+      if (c < 0.97 * best_cost) {
+        best_cost = c;
+        best = sl;
+      }
+    }
+    if (best > 1) {
+      Epi pe;
+      pe.kind = EPI_F32;
+      pe.out = epi.split_ws;
+      pe.ld_out = ldw;
+      OutMaps oms;
+      p.kb_split = (p.k_blocks + best - 1) / best;
+      p.splits = (p.k_blocks + p.kb_split - 1) / p.kb_split;  // no empty slice
+      p.m_pad = static_cast<int>(m_pad);
+      p.m_epi = static_cast<int>(p.splits * m_pad);
+      if (!make_out_maps(&oms, pe, p.m_epi, N, OutStageBytes(NF4_BN))) {
+        *why = "gemm_nf4: split-K scratch needs 16-byte alignment";
+        return cudaErrorInvalidValue;
+      }
+      p.epi = pe;
+      const cudaError_t e = b_mn ? launch_nf4_pair<1, EPI_F32>(ta, tb2, nm, oms, p, pairs_max, s)
+                                 : launch_nf4_pair<0, EPI_F32>(ta, tb2, nm, oms, p, pairs_max, s);
+      if (e != cudaSuccess) return e;
+      return splitk_reduce(epi, p.splits, m_pad, ldw, M, N, s);
+    }
   }
 #define RDT_NF4_CASE(BMJ, E)                                                   \
   if (b_mn == (BMJ) && epi.kind == (E))                                        \

@@ -76,7 +76,7 @@ def _load() -> ctypes.CDLL:
         "rdt_clip_scale": (I32, [P, F32, P, P, P]),
         "rdt_adamw_step": (I32, [P, P, P, P, I64, P, P, I32, F32, F32, F32, F32, F32, P, P]),
         "rdt_gemm": (I32, [P, I32, I64, P, I32, I64, I32, I32, I32, P, I64, P, I64, P]),
-        "rdt_gemm_nf4": (I32, [P, I64, P, P, I64, I64, I32, P, I64, P, I64, I32, I32, P, I64,
+        "rdt_gemm_nf4": (I32, [P, I64, P, P, I64, I64, I32, P, I64, P, I64, I32, I32, P, I64, P, I64,
                                P]),
         "rdt_cast_bf16": (I32, [P, P, I64, P]),
         "rdt_last_error": (ctypes.c_char_p, []),
@@ -237,14 +237,17 @@ def gemm(a, a_mn, b, b_mn, M, N, K, c, split_ws=None, stream=None):
                           0 if split_ws is None else split_ws.numel(), _stream(stream)))
 
 
-def gemm_nf4(a, codes, scales, w_rows, w_cols, b_mn, c, a2=None, b2=None, stream=None):
+def gemm_nf4(a, codes, scales, w_rows, w_cols, b_mn, c, a2=None, b2=None, split_ws=None,
+             stream=None):
     """c[M, N] = a B^T (+ a2 b2'^T) with B decoded from NF4 (see include/rdt.h);
-    a, a2, b2 bf16 2-D, codes uint8, scales fp32, c fp32 2-D."""
+    a, a2, b2 bf16 2-D, codes uint8, scales fp32, c fp32 2-D; split_ws:
+    optional fp32 scratch for the split-K path."""
     k2 = 0 if a2 is None else a2.shape[1]
     _check(lib().rdt_gemm_nf4(_ptr(a), a.stride(0), _ptr(codes), _ptr(scales), w_rows, w_cols,
                               int(b_mn), _ptr(a2), 0 if a2 is None else a2.stride(0), _ptr(b2),
                               0 if b2 is None else b2.stride(0), k2, a.shape[0], _ptr(c),
-                              c.stride(0), _stream(stream)))
+                              c.stride(0), _ptr(split_ws),
+                              0 if split_ws is None else split_ws.numel(), _stream(stream)))
 
 
 # ------------------------------------------------- NF4 + LoRA block

@@ -66,6 +66,43 @@ def test_nf4_gemm_matches_fp64_of_decoded_weights(b_mn, k2, M, rows, cols):
     assert rel_l2(out.numpy(), ref.numpy()) < 1e-5
 
 
+@pytest.mark.parametrize("b_mn,rows,cols,k2", [(0, 2560, 9728, 16), (1, 19456, 2560, 32),
+                                              (0, 2560, 4096, 0), (1, 6144, 2560, 48)])
+def test_nf4_gemm_split_k_matches_fp64(b_mn, rows, cols, k2):
+    """2048 rows against a 2560-wide output: 80 pair tiles, so the GEMM runs as
+    K-slices (the LoRA tail in the last slice) summed in slice order."""
+    M = 2048
+    g = torch.Generator().manual_seed(rows + cols + k2 + b_mn)
+    codes, scales = _nf4_weight(rows, cols, g)
+    w = _decoded(codes, scales, rows, cols)
+    N, K1 = (cols, rows) if b_mn else (rows, cols)
+    a = torch.randn(M, K1, generator=g).to(torch.bfloat16)
+    ref = a.double() @ (w if b_mn else w.T)
+    a2 = b2 = None
+    if k2:
+        a2 = torch.randn(M, k2, generator=g).to(torch.bfloat16)
+        b2 = torch.randn(k2, N, generator=g).to(torch.bfloat16) if b_mn else \
+            torch.randn(N, k2, generator=g).to(torch.bfloat16)
+        ref = ref + a2.double() @ (b2.double() if b_mn else b2.double().T)
+    ws = torch.empty(4 * M * N, device="cuda")
+    outs = []
+    for split in (ws, ws, None):
+        c = torch.full((M, N + 4), float("nan"), device="cuda")
+        rdt.gemm_nf4(a.cuda(), codes.cuda(), scales.cuda(), rows, cols, b_mn, c,
+                     None if a2 is None else a2.cuda(), None if b2 is None else b2.cuda(),
+                     split_ws=split)
+        torch.cuda.synchronize()
+        outs.append(c)
+    # fp32 accumulation over K up to 19456: typical error sqrt(K) 2^-24 = 8e-6
+    tol = 2e-5
+    out = outs[0][:, :N].double().cpu()
+    assert torch.isfinite(out).all()
+    assert rel_l2(out.numpy(), ref.numpy()) < tol
+    assert torch.isnan(outs[0][:, N:]).all()
+    assert torch.equal(outs[0][:, :N], outs[1][:, :N])  # fixed summation order
+    assert rel_l2(outs[2][:, :N].double().cpu().numpy(), ref.numpy()) < tol
+
+
 # ------------------------------------------------------- NF4 + LoRA block
 def _nf4_shape(**kw):
     base = dict(layers=1, hidden=256, n_heads=4, n_kv_heads=2, head_dim=64, intermediate=512,
