@@ -40,6 +40,16 @@ UNIT = "tokens/s"
 # it was measured on; reported only while gemm.cu is unchanged.
 GEMM_TRAFFIC_BYTES = 254737678
 GEMM_TRAFFIC_SRC_SHA = "36d847e5d51ba2e1"
+# The same for the NF4 GEMM launches of one q4b_nf4 step.
+NF4_TRAFFIC_BYTES = 75606000
+NF4_TRAFFIC_SRC_SHA = "16a70095fa1257b0"
+
+
+def traffic_if_current(nbytes, sha):
+    """nbytes while gemm.cu is the source the counters were taken on, else None."""
+    import hashlib
+    with open(os.path.join(ROOT, "resident_decoder_trainer_gb300", "csrc", "gemm.cu"), "rb") as fh:
+        return nbytes if hashlib.sha256(fh.read()).hexdigest()[:16] == sha else None
 
 
 def parse_args():
@@ -254,13 +264,7 @@ def run_rdt(args, rank, world, local_rank):
     peak_tf = float(peaks.get("bf16_tflops_sustained") or peaks.get("bf16_tflops"))
     achieved = gemm_flops / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else None
     n_launch = len(res)
-    traffic = None
-    if GEMM_TRAFFIC_BYTES is not None:
-        import hashlib
-        with open(os.path.join(ROOT, "resident_decoder_trainer_gb300", "csrc", "gemm.cu"),
-                  "rb") as fh:
-            if hashlib.sha256(fh.read()).hexdigest()[:16] == GEMM_TRAFFIC_SRC_SHA:
-                traffic = GEMM_TRAFFIC_BYTES
+    traffic = traffic_if_current(GEMM_TRAFFIC_BYTES, GEMM_TRAFFIC_SRC_SHA)
     roofline = {
         "kernel": "gemm_kernel / gemm2_kernel (tcgen05 BF16 single-CTA 128x192/256 and CTA-pair 256x256 tiles, TMEM fp32 accumulators, TMA)",
         "bound": "tensor", "achieved": round(achieved, 1) if achieved else None,
@@ -476,7 +480,7 @@ def run_nf4(args, rank, world, local_rank):
         "peak": peak_tf, "unit": "TFLOP/s",
         "frac": round(achieved / peak_tf, 4) if achieved else None,
         "peak_source": f"bf16_tflops_sustained of {peak_kind}",
-        "traffic": None,
+        "traffic": traffic_if_current(NF4_TRAFFIC_BYTES, NF4_TRAFFIC_SRC_SHA),
         "launches_timed": len(nf4),
         "flops_per_launch": nf4_flops / max(len(nf4), 1),
         "ms_per_launch": nf4_ms / max(len(nf4), 1),
