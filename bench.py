@@ -63,6 +63,12 @@ def parse_args():
     ap.add_argument("--kernel", choices=["block", "head"], default=None,
                     help="time one block forward+backward, or the LM head + CE, alone "
                          "(small device footprint, for per-kernel numbers and ncu captures)")
+    ap.add_argument("--checkpoint-segments", type=int, default=0,
+                    help="activation checkpointing: hold one of N layer segments' activations "
+                         "and recompute the rest in the backward (0: off)")
+    ap.add_argument("--accumulation-steps", type=int, default=1,
+                    help="gradient accumulation: micro-batches (of the workload's batch) per "
+                         "optimizer step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -217,13 +223,16 @@ def run_rdt(args, rank, world, local_rank):
     if args.layers:
         shape = shape.replace(layers=args.layers)
     T = shape.tokens
-    tr = DecoderTrainer(shape, device=dev)
+    n_acc = max(1, args.accumulation_steps)
+    tr = DecoderTrainer(shape, device=dev, checkpoint_segments=args.checkpoint_segments,
+                        accumulation_steps=n_acc)
     tr.init_random(seed=1234 + rank)
     gen = torch.Generator(device=dev)
     gen.manual_seed(4321 + rank)
     nb = 4
-    xs = [torch.randn(T, shape.hidden, device=dev, generator=gen) for _ in range(nb)]
-    tgs = [torch.randint(0, shape.vocab, (T,), device=dev, generator=gen, dtype=torch.int32)
+    Ts = n_acc * T  # tokens per optimizer step
+    xs = [torch.randn(Ts, shape.hidden, device=dev, generator=gen) for _ in range(nb)]
+    tgs = [torch.randint(0, shape.vocab, (Ts,), device=dev, generator=gen, dtype=torch.int32)
            for _ in range(nb)]
     stream = torch.cuda.current_stream()
 
@@ -235,7 +244,7 @@ def run_rdt(args, rank, world, local_rank):
     first_loss = float(tr.train_step(xs[0], tgs[0]).mean())
     for i in range(1, args.warmup):
         tr.train_step(xs[i % nb], tgs[i % nb])
-    gemms_per_step = 12 * shape.layers + 3
+    gemms_per_step = (17 * shape.layers + 3) * n_acc  # 12 per layer, 5 more when recomputed
     timer = rdt.GemmTimer(gemms_per_step * args.steps)
     barrier()
     clk = start_clock_sampler(local_rank)
@@ -255,7 +264,7 @@ def run_rdt(args, rank, world, local_rank):
     if world > 1:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
     max_ms = float(t.item())
-    value = world * T * args.steps / (max_ms / 1e3)
+    value = world * Ts * args.steps / (max_ms / 1e3)
 
     res = timer.results()
     gemm_flops = sum(f for f, _ in res)
@@ -277,7 +286,7 @@ def run_rdt(args, rank, world, local_rank):
         "ms_per_launch": gemm_ms / max(n_launch, 1),
         "gemm_share_of_step": round(gemm_ms / max_ms, 4) if max_ms else None,
     }
-    step_flops = algorithmic_flops(shape)
+    step_flops = algorithmic_flops(shape) * n_acc
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 3),
@@ -293,6 +302,15 @@ def run_rdt(args, rank, world, local_rank):
     }
     out["config"]["params"] = tr.n_params
     out["config"]["algorithmic_tflop_per_step"] = round(step_flops / 1e12, 2)
+    out["config"]["activation_gb_held"] = round(tr.saved.numel() / 1e9, 2)
+    if n_acc > 1:
+        out["config"]["tokens_per_step"] = Ts
+        out["config"]["global_batch"] = shape.batch * n_acc
+        out["config"]["accumulation_steps"] = n_acc
+    if args.checkpoint_segments:
+        out["config"]["activation_checkpointing"] = {
+            "segments": args.checkpoint_segments, "layers_per_segment": tr.segment_size,
+            "activation_gb_without": round(shape.layers * tr.saved_bytes / 1e9, 2)}
 
     if not args.no_e2e:
         out["e2e"] = run_e2e(tr, shape, args, dev, world)
@@ -305,7 +323,7 @@ def run_e2e(tr, shape, args, dev, world):
     """Same metric through the public API with HOST buffers: every step copies
     its inputs from pinned host memory and reads its loss partials back."""
     import torch
-    T = shape.tokens
+    T = shape.tokens * tr.accumulation_steps
     xh = torch.randn(T, shape.hidden).pin_memory()
     th = torch.randint(0, shape.vocab, (T,), dtype=torch.int32).pin_memory()
     lh = torch.empty(T, dtype=torch.float32).pin_memory()

@@ -132,18 +132,23 @@ rdt_status rdt_block_forward(const rdt_config* cfg, int32_t batch, int32_t seq,
  * saved  what rdt_block_forward wrote for the same x and w
  * dy     upstream gradient fp32 [T, H]
  * dx     gradient w.r.t. x, fp32 [T, H] (overwritten; may alias dy)
- * grads  fp32 flat array in the block layout, every tensor overwritten
+ * grads  fp32 flat array in the block layout: every tensor overwritten
+ *        (accumulate == 0) or added to (accumulate == 1: gradient
+ *        accumulation over micro-batches, GpuGradientAccumulator in
+ *        cuda_trainer.rs, here done in place by the gradient producers)
  * grad_sq  optional (may be null) fp64 device scalar: *grad_sq += the sum of
- *          the squares of every gradient this call writes (the global-norm
- *          clip's squared sum, accumulated by the weight-gradient GEMMs'
- *          epilogues and the gain reductions as they produce the values;
- *          fixed summation order, so the same inputs give the same bits)
+ *          the squares of every gradient this call leaves in grads (after
+ *          the accumulation, so pass it on a step's last micro-batch only;
+ *          the global-norm clip's squared sum, accumulated by the
+ *          weight-gradient GEMMs' epilogues and the gain reductions as they
+ *          produce the values; fixed summation order, so the same inputs give
+ *          the same bits)
  * ------------------------------------------------------------------------- */
 rdt_status rdt_block_backward(const rdt_config* cfg, int32_t batch, int32_t seq,
                               const float* w, const rdt_bf16* w_bf16,
                               const float* x, const void* saved, size_t saved_bytes,
-                              const float* dy, float* dx, float* grads, double* grad_sq,
-                              void* ws, size_t ws_bytes, void* stream);
+                              const float* dy, float* dx, float* grads, int32_t accumulate,
+                              double* grad_sq, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Final RMSNorm + LM head + cross-entropy, forward and backward in one call
@@ -159,19 +164,23 @@ rdt_status rdt_block_backward(const rdt_config* cfg, int32_t batch, int32_t seq,
  * gamma_f  fp32 [H]; w_lm bf16 [V, H]
  * targets  int32 [tokens], device; each must lie in [0, V) (not checked on
  *          the device: the caller validates ids before upload)
- * loss_scale  normally 1/tokens (loss = mean NLL)
- * dh fp32 [tokens, H]; dgamma_f fp32 [H]; dw_lm fp32 [V, H] (all overwritten)
+ * loss_scale  normally 1/tokens (loss = mean NLL); 1/(tokens * n) for each of
+ *          n accumulated micro-batches (train_step_inner divides by
+ *          accumulation_steps)
+ * dh fp32 [tokens, H] (overwritten); dgamma_f fp32 [H] and dw_lm fp32 [V, H]
+ *          overwritten (accumulate == 0) or added to (accumulate == 1)
  * grad_sq  optional (may be null) fp64 device scalar: *grad_sq = the sum of
- *          the squares of dgamma_f and dw_lm (a step's backward starts here,
- *          so this call starts the clip's squared sum that each
- *          rdt_block_backward then adds to)
+ *          the squares of dgamma_f and dw_lm as this call leaves them (a
+ *          step's backward starts here, so this call starts the clip's
+ *          squared sum that each rdt_block_backward then adds to; pass it on
+ *          the last micro-batch only when accumulating)
  * ------------------------------------------------------------------------- */
 rdt_status rdt_fused_cross_entropy(const rdt_config* cfg, int32_t tokens,
                                    const float* h, const float* gamma_f,
                                    const rdt_bf16* w_lm, const int32_t* targets,
                                    float loss_scale, float* loss_partials,
-                                   float* dh, float* dgamma_f, float* dw_lm, double* grad_sq,
-                                   void* ws, size_t ws_bytes, void* stream);
+                                   float* dh, float* dgamma_f, float* dw_lm, int32_t accumulate,
+                                   double* grad_sq, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Squared-sum gradient clip (compute_workspace_clip_scale_gpu,

@@ -22,7 +22,9 @@ Sources (aprender-train docs.rs pages, module ``entrenar``):
   loss scale 1/T), ``gpu_forward`` (final RMSNorm, LM head), ``gpu_backward``
   (LM-head backward, final-norm backward), ``compute_workspace_clip_scale_gpu``
   / ``fused_clip_workspace_gradients`` (squared-sum clip, C-CLIP-001),
-  ``run_nonblock_optimizer_step`` (AdamW, step counted from 1).
+  ``run_nonblock_optimizer_step`` (AdamW, step counted from 1); R-038 gradient
+  accumulation (loss scale 1/seq_len/accumulation_steps in
+  ``train_step_inner``, micro-batch gradients summed before one step).
 * wgpu_trainer.rs (0.38.0) -- ``train_step`` CPU cross-entropy loop (loss and
   softmax-minus-one-hot gradient) and ``ffn_backward`` (SiLU derivative).
 
@@ -333,16 +335,16 @@ def adamw(w, g, m, v, step, lr, beta1, beta2, eps, weight_decay, scale=1.0):
 # ----------------------------------------------------------------------------
 # The whole step
 # ----------------------------------------------------------------------------
-def model_forward_backward(blocks, head, x, targets, shape):
+def model_forward_backward(blocks, head, x, targets, shape, loss_scale=None):
     """Forward through every block and the head, then the full backward.
-    Returns (head result dict, list of per-block grads dicts, list of layer
-    outputs)."""
+    Returns (head result dict, list of per-block grads dicts)."""
     h = _f64(x)
     caches = []
     for p in blocks:
         h, cache = block_forward(p, h, shape)
         caches.append(cache)
-    res = head_forward_backward(h, head["g_final"], head["w_lm"], targets, shape)
+    res = head_forward_backward(h, head["g_final"], head["w_lm"], targets, shape,
+                                loss_scale=loss_scale)
     dh = res["dh"]
     block_grads = [None] * len(blocks)
     for i in reversed(range(len(blocks))):
@@ -359,7 +361,6 @@ def train_step(blocks, head, x, targets, shape, state=None, step=1, optim=None):
     missing entries start at zero. Returns a dict with the loss, the per-token
     loss partials, the gradients, the clip norm/scale and the updated
     parameters and moments."""
-    o = dict(optim)
     res, bgrads = model_forward_backward(blocks, head, x, targets, shape)
     named = []
     for i, g in enumerate(bgrads):
@@ -367,6 +368,48 @@ def train_step(blocks, head, x, targets, shape, state=None, step=1, optim=None):
             named.append(((i, k_), blocks[i][k_], v_))
     named.append((("head", "g_final"), head["g_final"], res["g_final"]))
     named.append((("head", "w_lm"), head["w_lm"], res["w_lm"]))
+    out = _clip_adamw(named, state, step, optim)
+    out.update(loss=res["loss"], loss_partials=res["loss_partials"], dx=res["dx"])
+    return out
+
+
+def accumulated_gradients(blocks, head, micro_xs, micro_targets, shape):
+    """Gradient accumulation over n micro-batches (cuda_trainer.rs: R-038,
+    ``train_step_inner`` scales the CE loss by 1/seq_len/accumulation_steps;
+    the accumulator sums the micro-batch gradients before one optimizer step):
+    each micro-batch runs the full forward and backward with the loss scaled
+    by 1/(T n), T its token count, and the gradients are summed in micro-batch
+    order. Returns (list of (key, parameter, gradient) like ``train_step``'s,
+    concatenated per-token loss partials)."""
+    n = len(micro_xs)
+    total, partials = {}, []
+    for x, tg in zip(micro_xs, micro_targets):
+        T = np.asarray(x).shape[0]
+        res, bgrads = model_forward_backward(blocks, head, x, tg, shape,
+                                             loss_scale=1.0 / (T * n))
+        partials.append(res["loss_partials"])
+        items = [((i, k_), v_) for i, g in enumerate(bgrads) for k_, v_ in g.items()]
+        items += [(("head", "g_final"), res["g_final"]), (("head", "w_lm"), res["w_lm"])]
+        for key, g in items:
+            total[key] = g if key not in total else total[key] + g
+    named = [(key, blocks[key[0]][key[1]] if key[0] != "head" else head[key[1]], g)
+             for key, g in total.items()]
+    return named, np.concatenate(partials)
+
+
+def train_step_accumulated(blocks, head, micro_xs, micro_targets, shape, state=None, step=1,
+                           optim=None):
+    """One step over n micro-batches: accumulated gradients, then the same
+    global clip and AdamW as ``train_step``."""
+    named, partials = accumulated_gradients(blocks, head, micro_xs, micro_targets, shape)
+    out = _clip_adamw(named, state, step, optim)
+    out.update(loss=float(partials.mean()), loss_partials=partials)
+    return out
+
+
+def _clip_adamw(named, state, step, optim):
+    """The global clip over every (key, parameter, gradient) and AdamW on each."""
+    o = dict(optim)
     sq = [squared_sum(g) for _, _, g in named]
     scale, norm, finite = clip_scale(sq, o["max_norm"])
     state = {} if state is None else state
@@ -381,6 +424,5 @@ def train_step(blocks, head, x, targets, shape, state=None, step=1, optim=None):
             w2, m2, v2 = w, _f64(m), _f64(v)
         new_params[key] = w2
         new_state[key] = (m2, v2)
-    return dict(loss=res["loss"], loss_partials=res["loss_partials"],
-                grads={key: g for key, _, g in named}, sq_sums=sq, norm=norm, scale=scale,
-                finite=finite, params=new_params, state=new_state, dx=res["dx"])
+    return dict(grads={key: g for key, _, g in named}, sq_sums=sq, norm=norm, scale=scale,
+                finite=finite, params=new_params, state=new_state)

@@ -584,7 +584,8 @@ rdt_status rdt_block_forward(const rdt_config* cfg, int32_t batch, int32_t seq, 
 rdt_status rdt_block_backward(const rdt_config* cfg, int32_t batch, int32_t seq, const float* w,
                               const rdt_bf16* w_bf16, const float* x, const void* saved,
                               size_t saved_bytes, const float* dy, float* dx, float* grads,
-                              double* grad_sq, void* ws, size_t ws_bytes, void* stream) {
+                              int32_t accumulate, double* grad_sq, void* ws, size_t ws_bytes,
+                              void* stream) {
   std::string why;
   if (!cfg_ok(cfg, &why)) return fail(RDT_EINVAL, "config: %s", why.c_str());
   if (batch < 1 || seq < 1) return fail(RDT_EINVAL, "batch and seq must be >= 1");
@@ -626,7 +627,14 @@ rdt_status rdt_block_backward(const rdt_config* cfg, int32_t batch, int32_t seq,
   }
   // squared sums of the weight gradients, written by their GEMMs' epilogues
   int64_t sq_n = 0, sq_cnt = 0;
+  // a weight gradient: fp32 (+= the previous micro-batches' when accumulating)
+  // with its squared-sum slots
   auto sq_slots = [&](Epi& e) {
+    if (accumulate) {
+      e.kind = EPI_F32_RESID;
+      e.resid = static_cast<const float*>(e.out);
+      e.ld_resid = e.ld_out;
+    }
     if (!grad_sq) return;
     e.sq_part = wk.sqp + sq_n;
     e.sq_count = &sq_cnt;
@@ -664,7 +672,7 @@ rdt_status rdt_block_backward(const rdt_config* cfg, int32_t batch, int32_t seq,
   }
   // post-attention RMSNorm backward, identity skip added after it
   RDT_CHECK_CUDA(rmsnorm_bwd(wk.dxn, sv.r1, sv.rstd2, w + off[RDT_G_FFN], dy, wk.dr1, wk.dr1_b,
-                             grads + off[RDT_G_FFN], wk.partials, T, (int)m.H, s));
+                             grads + off[RDT_G_FFN], wk.partials, T, (int)m.H, s, accumulate != 0));
   // do = dr1 Wo
   {
     Epi e;
@@ -711,7 +719,7 @@ rdt_status rdt_block_backward(const rdt_config* cfg, int32_t batch, int32_t seq,
   RDT_CHECK_CUDA(qknorm_rope_bwd(wk.dq, wk.dk, sv.qkv, m.nqkv, sv.rstd_q, sv.rstd_k,
                                  w + off[RDT_G_Q], w + off[RDT_G_K], wk.cs, wk.dqkv,
                                  grads + off[RDT_G_Q], wk.partials, T, seq, (int)m.nh, (int)m.nkv,
-                                 (int)m.d, s));
+                                 (int)m.d, s, accumulate != 0));
   // dxn = [dq dk dv] [Wq; Wk; Wv]
   {
     Epi e;
@@ -734,7 +742,7 @@ rdt_status rdt_block_backward(const rdt_config* cfg, int32_t batch, int32_t seq,
   }
   // input RMSNorm backward + identity skip
   RDT_CHECK_CUDA(rmsnorm_bwd(wk.dxn, x, sv.rstd1, w + off[RDT_G_ATTN], wk.dr1, dx, nullptr,
-                             grads + off[RDT_G_ATTN], wk.partials, T, (int)m.H, s));
+                             grads + off[RDT_G_ATTN], wk.partials, T, (int)m.H, s, accumulate != 0));
   if (grad_sq) {
     // += the weight-gradient slots and the four gains, in a fixed order
     const float* gains[4] = {grads + off[RDT_G_ATTN], grads + off[RDT_G_FFN],
@@ -749,8 +757,8 @@ rdt_status rdt_block_backward(const rdt_config* cfg, int32_t batch, int32_t seq,
 rdt_status rdt_fused_cross_entropy(const rdt_config* cfg, int32_t tokens, const float* h,
                                    const float* gamma_f, const rdt_bf16* w_lm,
                                    const int32_t* targets, float loss_scale, float* loss_partials,
-                                   float* dh, float* dgamma_f, float* dw_lm, double* grad_sq,
-                                   void* ws, size_t ws_bytes, void* stream) {
+                                   float* dh, float* dgamma_f, float* dw_lm, int32_t accumulate,
+                                   double* grad_sq, void* ws, size_t ws_bytes, void* stream) {
   std::string why;
   if (!cfg_ok(cfg, &why)) return fail(RDT_EINVAL, "config: %s", why.c_str());
   if (tokens < 1) return fail(RDT_EINVAL, "tokens must be >= 1");
@@ -799,9 +807,11 @@ rdt_status rdt_fused_cross_entropy(const rdt_config* cfg, int32_t tokens, const 
   int64_t sq_n = 0;
   {
     Epi e;
-    e.kind = EPI_F32;
+    e.kind = accumulate ? EPI_F32_RESID : EPI_F32;
     e.out = dw_lm;
     e.ld_out = m.H;
+    e.resid = dw_lm;
+    e.ld_resid = m.H;
     if (grad_sq) {
       e.sq_part = wk.sqp;
       e.sq_count = &sq_n;
@@ -810,7 +820,7 @@ rdt_status rdt_fused_cross_entropy(const rdt_config* cfg, int32_t tokens, const 
              err, s);
   }
   RDT_CHECK_CUDA(rmsnorm_bwd(wk.dhn, h, wk.rstd, gamma_f, nullptr, dh, nullptr, dgamma_f,
-                             wk.partials, T, (int)m.H, s));
+                             wk.partials, T, (int)m.H, s, accumulate != 0));
   if (grad_sq) {
     // = the dW_lm slots and the final gain's squares (the first gradients of a step)
     const float* gains[1] = {dgamma_f};

@@ -130,10 +130,11 @@ __global__ void __launch_bounds__(512) rmsnorm_bwd_kernel(
   }
 }
 
-// out[c] = sum_p partials[p, c]: 8 row-strided partial sums per column, then
-// those 8 in order (deterministic).
+// out[c] (= or, with accumulate, +=) sum_p partials[p, c]: 8 row-strided
+// partial sums per column, then those 8 in order (deterministic).
 __global__ void __launch_bounds__(256) reduce_cols_kernel(const float* __restrict__ partials,
-                                                          int P, int W, float* __restrict__ out) {
+                                                          int P, int W, float* __restrict__ out,
+                                                          int accumulate) {
   __shared__ float red[8][33];
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int c = blockIdx.x * 32 + tx;
@@ -146,7 +147,7 @@ __global__ void __launch_bounds__(256) reduce_cols_kernel(const float* __restric
     float t = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) t += red[i][tx];
-    out[c] = t;
+    out[c] = accumulate ? out[c] + t : t;
   }
 }
 
@@ -174,22 +175,23 @@ cudaError_t rmsnorm_fwd(const float* x, const float* gamma, bf16* y, float* rstd
 
 int rmsnorm_bwd_partial_rows(int T) { return T < kMaxPartialRows ? T : kMaxPartialRows; }
 
-static cudaError_t reduce_cols(const float* partials, int P, int W, float* out, cudaStream_t s) {
+static cudaError_t reduce_cols(const float* partials, int P, int W, float* out, cudaStream_t s,
+                               bool accumulate) {
   note_launch();
-  reduce_cols_kernel<<<(W + 31) / 32, 256, 0, s>>>(partials, P, W, out);
+  reduce_cols_kernel<<<(W + 31) / 32, 256, 0, s>>>(partials, P, W, out, accumulate ? 1 : 0);
   return cudaGetLastError();
 }
 
 cudaError_t rmsnorm_bwd(const float* dy, const float* x, const float* rstd, const float* gamma,
                         const float* resid, float* dx, bf16* dx_bf16, float* dgamma,
-                        float* partials, int T, int H, cudaStream_t s) {
+                        float* partials, int T, int H, cudaStream_t s, bool accumulate) {
   const int P = rmsnorm_bwd_partial_rows(T);
   const int threads = ((H / 8 + 31) / 32) * 32;
   note_launch();
   rmsnorm_bwd_kernel<<<P, threads, 0, s>>>(dy, x, rstd, gamma, resid, dx, dx_bf16, partials, T, H);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return reduce_cols(partials, P, H, dgamma, s);
+  return reduce_cols(partials, P, H, dgamma, s, accumulate);
 }
 
 // ----------------------------------------------------------------- RoPE table
@@ -433,7 +435,7 @@ cudaError_t qknorm_rope_bwd(const float* dq, const float* dk, const float* qkv, 
                             const float* rstd_q, const float* rstd_k, const float* gq,
                             const float* gk, const float* cs, bf16* dqkv, float* dg_qk,
                             float* partials, int T, int S, int nh, int nkv, int d,
-                            cudaStream_t s) {
+                            cudaStream_t s, bool accumulate) {
   const int P = qknorm_bwd_partial_rows(T, nh + nkv);
   const float2* c2 = reinterpret_cast<const float2*>(cs);
   note_launch();
@@ -447,7 +449,7 @@ cudaError_t qknorm_rope_bwd(const float* dq, const float* dk, const float* qkv, 
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // columns [0, d) -> q gain, [d, 2d) -> k gain
-  return reduce_cols(partials, P, 2 * d, dg_qk, s);
+  return reduce_cols(partials, P, 2 * d, dg_qk, s, accumulate);
 }
 
 // ----------------------------------------------------- fused squared sums

@@ -242,7 +242,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const OutMaps
 
   uint32_t r[32];
   uint32_t r2[EPI == EPI_SWIGLU ? 32 : 1];
-  float sq = 0.f;  // EPI_F32 with sq_part: sum of squares of this warp's values
+  float sq = 0.f;  // F32 / F32_RESID with sq_part: sum of squares of this warp's stored values
   float mx = -INFINITY, sum = 0.f;
   const int tgt = (EPI == EPI_CE && row_ok) ? e.targets[row] : -1;
 #pragma unroll 1
@@ -323,7 +323,10 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const OutMaps
               const float* res = e.resid + (int64_t)row * e.ld_resid + col;
 #pragma unroll
               for (int k = 0; k < UNIT; ++k)
-                if (col + k < ncols) v[k] += res[k];
+                if (col + k < ncols) {
+                  v[k] += res[k];
+                  if (e.sq_part) sq = fmaf(v[k], v[k], sq);
+                }
             }
           }
           if (row_ok) {
@@ -344,6 +347,11 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const OutMaps
           get_f32<RB, UNIT>(buf, lane, q);
 #pragma unroll
           for (int k = 0; k < UNIT; ++k) v[k] += q[k];
+          // out-of-range rows and columns: zero accumulator + zero-filled load
+          if (e.sq_part) {
+#pragma unroll
+            for (int k = 0; k < UNIT; ++k) sq = fmaf(v[k], v[k], sq);
+          }
         }
         if constexpr (EPI == EPI_F32 || EPI == EPI_F32_RESID) put_f32<RB, UNIT>(buf, lane, v);
         else put_bf16<RB, UNIT>(buf, lane, v);
@@ -409,7 +417,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const OutMaps
   if constexpr (EPI == EPI_CE) {
     if (row_ok) e.part[(int64_t)row * e.part_ld + 2 * nt + half] = make_float2(mx, sum);
   }
-  if constexpr (EPI == EPI_F32) {
+  if constexpr (EPI == EPI_F32 || EPI == EPI_F32_RESID) {
     if (e.sq_part) {
       double d = sq;
 #pragma unroll
@@ -1679,7 +1687,7 @@ int64_t gemm_sq_slots_bound(int M, int N) {
 
 // Sum of the split-K partials (fp32 slabs of m_pad x ldw, added in split
 // order) with the F32, F32_RESID or BF16 epilogue, four columns per thread
-// (N % 4 == 0; the host falls back to one); F32 also writes one fp64
+// (N % 4 == 0; the host falls back to one); F32 / F32_RESID also write one fp64
 // squared-sum slot per block (fixed grid and order: deterministic).
 template <int V>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(
@@ -1756,7 +1764,7 @@ static cudaError_t splitk_reduce(const Epi& epi, int splits, int64_t m_pad, int6
   if (epi.kind == EPI_F32_RESID)
     vec = vec && epi.ld_resid % 4 == 0 && (reinterpret_cast<uintptr_t>(epi.resid) % 16) == 0;
   const int64_t items = static_cast<int64_t>(M) * (vec ? N / 4 : N);
-  const bool sq = epi.kind == EPI_F32 && epi.sq_part;
+  const bool sq = (epi.kind == EPI_F32 || epi.kind == EPI_F32_RESID) && epi.sq_part;
   int64_t nblk = (items + 255) / 256;
   nblk = std::max<int64_t>(1, std::min<int64_t>(nblk, sq ? gemm_sq_slots_bound(M, N)
                                                          : 8LL * num_sms()));
@@ -1872,7 +1880,7 @@ cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N,
       pair_tiles = true;
     }
   }
-  if (epi.split_ws && (epi.kind == EPI_F32 || epi.kind == EPI_BF16)) {
+  if (epi.split_ws && (epi.kind == EPI_F32 || epi.kind == EPI_F32_RESID || epi.kind == EPI_BF16)) {
     const int64_t tiles1 = (int64_t)((M + BM - 1) / BM) * ((N + 255) / 256);
     const int kbs = (K + BK - 1) / BK;
     const int64_t m_pad = (int64_t)((M + BM - 1) / BM) * BM;
@@ -1912,8 +1920,8 @@ cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N,
   p.epi.sq_count = nullptr;
   p.err = err;
   if (epi.sq_part) {
-    if (epi.kind != EPI_F32 || !epi.sq_count) {
-      *why = "gemm: squared-sum slots need the fp32 epilogue and a count";
+    if ((epi.kind != EPI_F32 && epi.kind != EPI_F32_RESID) || !epi.sq_count) {
+      *why = "gemm: squared-sum slots need an fp32 epilogue and a count";
       return cudaErrorInvalidValue;
     }
     *epi.sq_count = static_cast<int64_t>(p.m_tiles) * p.n_tiles * p.sq_slots;
@@ -1951,9 +1959,12 @@ cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N,
   // weight gradients dW = dY^T X: A MN-major, B MN-major
   RDT_GEMM_CASE(1, 1, EPI_F32, 256)
   RDT_GEMM_CASE(1, 1, EPI_F32, 192)
+  RDT_GEMM_CASE(1, 1, EPI_F32_RESID, 256)  // gradient accumulation: dW += dY^T X
+  RDT_GEMM_CASE(1, 1, EPI_F32_RESID, 192)
   RDT_GEMM_CASE(1, 1, EPI_BF16, 256)
   RDT_GEMM_CASE(1, 1, EPI_BF16, 192)
   RDT_GEMM2_CASE(1, 1, EPI_F32, 256)
+  RDT_GEMM2_CASE(1, 1, EPI_F32_RESID, 256)
   RDT_GEMM2_CASE(1, 1, EPI_BF16, 256)
 #undef RDT_GEMM2_CASE
 #undef RDT_GEMM_CASE

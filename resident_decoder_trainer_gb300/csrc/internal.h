@@ -35,14 +35,15 @@ struct Epi {
   int part_ld = 0;
   const int32_t* targets = nullptr;
   float* tgt_logit = nullptr;
-  // EPI_F32 only: when set, every epilogue warp writes the fp64 sum of the
-  // squares of the values it stored, one slot per (tile, warp), and the host
-  // gemm() sets *sq_count to the number of slots written (tiles x 8 or 16).
+  // EPI_F32 / EPI_F32_RESID: when set, every epilogue warp writes the fp64
+  // sum of the squares of the values it stored, one slot per (tile, warp),
+  // and the host gemm() sets *sq_count to the number of slots written (tiles
+  // x 8 or 16; or the split-K reduce's blocks).
   double* sq_part = nullptr;
   int64_t* sq_count = nullptr;
   // EPI_BF16 only: out = bf16(scale * acc)
   float scale = 1.0f;
-  // F32 / BF16: fp32 scratch gemm() may use to split K across CTAs when the
+  // F32 / F32_RESID / BF16: fp32 scratch gemm() may use to split K across CTAs when the
   // problem has too few output tiles to fill the GPU (split_ws_floats floats,
   // 16-byte aligned); the partials are summed in a fixed order.
   float* split_ws = nullptr;
@@ -116,10 +117,11 @@ constexpr int kMaxSqSumPartials = 4096;
 cudaError_t rmsnorm_fwd(const float* x, const float* gamma, bf16* y, float* rstd, int T, int H,
                         float eps, cudaStream_t s);
 // dx = rstd*(dy*g - xhat*mean(dy*g*xhat)) + resid (resid may be null);
-// dx_bf16 optional; dgamma partials [nblk, H] then reduced into dgamma.
+// dx_bf16 optional; dgamma partials [nblk, H] then reduced into dgamma
+// (dgamma = sum, or dgamma += sum when accumulate).
 cudaError_t rmsnorm_bwd(const float* dy, const float* x, const float* rstd, const float* gamma,
                         const float* resid, float* dx, bf16* dx_bf16, float* dgamma,
-                        float* partials, int T, int H, cudaStream_t s);
+                        float* partials, int T, int H, cudaStream_t s, bool accumulate = false);
 int rmsnorm_bwd_partial_rows(int T);
 
 cudaError_t rope_table(float* cs, int S, int d, float theta, cudaStream_t s);
@@ -129,12 +131,13 @@ cudaError_t qknorm_rope_fwd(const float* qkv, int64_t ld_qkv, bf16* q_out, bf16*
                             bf16* v_out, float* rstd_q, float* rstd_k, const float* gq,
                             const float* gk, const float* cs, int T, int S, int nh, int nkv, int d,
                             float eps, cudaStream_t s);
-// dg_qk: 2*d floats, q-gain gradient then k-gain gradient.
+// dg_qk: 2*d floats, q-gain gradient then k-gain gradient (= or += when
+// accumulate).
 cudaError_t qknorm_rope_bwd(const float* dq, const float* dk, const float* qkv, int64_t ld_qkv,
                             const float* rstd_q, const float* rstd_k, const float* gq,
                             const float* gk, const float* cs, bf16* dqkv, float* dg_qk,
                             float* partials, int T, int S, int nh, int nkv, int d,
-                            cudaStream_t s);
+                            cudaStream_t s, bool accumulate = false);
 int qknorm_bwd_partial_rows(int T, int heads);
 
 // *out (= or +=, per `accumulate`) the fp64 sum of parts[0, n) plus the sums

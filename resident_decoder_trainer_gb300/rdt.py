@@ -70,8 +70,9 @@ def _load() -> ctypes.CDLL:
         "rdt_head_workspace_bytes": (SZ, [CP, I32]),
         "rdt_sq_sum_workspace_bytes": (SZ, []),
         "rdt_block_forward": (I32, [CP, I32, I32, P, P, P, P, P, SZ, P, SZ, P]),
-        "rdt_block_backward": (I32, [CP, I32, I32, P, P, P, P, SZ, P, P, P, P, P, SZ, P]),
-        "rdt_fused_cross_entropy": (I32, [CP, I32, P, P, P, P, F32, P, P, P, P, P, P, SZ, P]),
+        "rdt_block_backward": (I32, [CP, I32, I32, P, P, P, P, SZ, P, P, P, I32, P, P, SZ, P]),
+        "rdt_fused_cross_entropy": (I32, [CP, I32, P, P, P, P, F32, P, P, P, P, I32, P, P, SZ,
+                                          P]),
         "rdt_sq_sum": (I32, [P, P, I32, P, P, SZ, P]),
         "rdt_clip_scale": (I32, [P, F32, P, P, P]),
         "rdt_adamw_step": (I32, [P, P, P, P, I64, P, P, I32, F32, F32, F32, F32, F32, P, P]),
@@ -179,22 +180,24 @@ def block_forward(cfg, batch, seq, w, w_bf16, x, y, saved, ws, stream=None):
 
 
 def block_backward(cfg, batch, seq, w, w_bf16, x, saved, dy, dx, grads, ws, grad_sq=None,
-                   stream=None):
-    """grad_sq: optional fp64 device scalar; += the squared sum of grads."""
+                   accumulate=False, stream=None):
+    """grad_sq: optional fp64 device scalar; += the squared sum of grads.
+    accumulate: add to grads instead of overwriting them."""
     _check(lib().rdt_block_backward(ctypes.byref(cfg), batch, seq, _ptr(w), _ptr(w_bf16), _ptr(x),
                                     _ptr(saved), saved.numel() * saved.element_size(), _ptr(dy),
-                                    _ptr(dx), _ptr(grads),
+                                    _ptr(dx), _ptr(grads), int(bool(accumulate)),
                                     None if grad_sq is None else _ptr(grad_sq), _ptr(ws),
                                     ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def fused_cross_entropy(cfg, tokens, h, gamma_f, w_lm, targets, loss_scale, loss_partials, dh,
-                        dgamma_f, dw_lm, ws, grad_sq=None, stream=None):
-    """grad_sq: optional fp64 device scalar; = the squared sum of dgamma_f and dw_lm."""
+                        dgamma_f, dw_lm, ws, grad_sq=None, accumulate=False, stream=None):
+    """grad_sq: optional fp64 device scalar; = the squared sum of dgamma_f and
+    dw_lm. accumulate: add to dgamma_f and dw_lm instead of overwriting them."""
     _check(lib().rdt_fused_cross_entropy(ctypes.byref(cfg), tokens, _ptr(h), _ptr(gamma_f),
                                          _ptr(w_lm), _ptr(targets), float(loss_scale),
                                          _ptr(loss_partials), _ptr(dh), _ptr(dgamma_f),
-                                         _ptr(dw_lm), None if grad_sq is None else _ptr(grad_sq),
+                                         _ptr(dw_lm), int(bool(accumulate)), None if grad_sq is None else _ptr(grad_sq),
                                          _ptr(ws), ws.numel() * ws.element_size(),
                                          _stream(stream)))
 

@@ -11,7 +11,24 @@
 A step is: every block forward (saving its activations), the fused final
 norm + LM head + cross-entropy (forward and backward), every block backward
 in reverse, one squared sum over all gradients, the clip scale, and one AdamW
-launch over all parameters. The loss partials stay on the device until the
+launch over all parameters.
+
+Activation checkpointing (``checkpoint_segments`` = n > 0; the segmented
+recompute of cuda_trainer.rs, ``recompute_segment`` and the saved-layer mask
+of ``CudaTransformerTrainer::new``): the layers form n segments of
+ceil(L / n); activations are held for one segment only. Every layer input
+h[l] is kept, so the backward of a segment first re-runs that segment's block
+forwards from their inputs (the last segment's are still current from the
+forward pass), then runs its block backwards in reverse. The kernels are
+deterministic, so the gradients are bit-identical to the step without
+checkpointing.
+
+Gradient accumulation (``accumulation_steps`` = n > 1; cuda_trainer.rs
+R-038 / ``GpuGradientAccumulator``, loss scale 1/seq_len/accumulation_steps in
+``train_step_inner``): a step takes n micro-batches of the shape's tokens;
+each runs forward and backward with the CE loss scaled by 1/(T n), the
+gradient producers adding into ``g`` after the first; the clip's squared sum
+is taken from the accumulated values on the last micro-batch, then one AdamW. The loss partials stay on the device until the
 caller reads them. Every launch is a librdt kernel; torch is used only to
 allocate buffers and for the stream.
 """
@@ -28,8 +45,10 @@ def _align(n: int, a: int = 64) -> int:
 
 
 class DecoderTrainer:
-    def __init__(self, shape: DecoderShape, device="cuda", optim=None):
+    def __init__(self, shape: DecoderShape, device="cuda", optim=None, checkpoint_segments=0,
+                 accumulation_steps=1):
         self.shape = s = shape
+        self.accumulation_steps = n_acc = max(1, int(accumulation_steps))
         self.device = torch.device(device)
         self.optim = dict(OPTIM if optim is None else optim)
         self.cfg = rdt.Config.from_shape(s)
@@ -48,8 +67,16 @@ class DecoderTrainer:
         self.m = torch.zeros(self.n_params, **f32)
         self.v = torch.zeros(self.n_params, **f32)
         self.saved_bytes = rdt.block_saved_bytes(self.cfg, s.batch, s.seq)
-        self.saved = torch.empty(L * self.saved_bytes, dtype=torch.uint8, device=dev)
+        self.checkpoint_segments = int(checkpoint_segments)
+        if self.checkpoint_segments > 0:
+            self.segment_size = -(-L // min(self.checkpoint_segments, L))
+        else:
+            self.segment_size = L
+        self.saved = torch.empty(self.segment_size * self.saved_bytes, dtype=torch.uint8,
+                                 device=dev)
         self.h = torch.empty((L + 1, T, H), **f32)
+        # output of the recomputed block forwards (equal to h[l + 1]; never read)
+        self.h_rc = torch.empty((T, H), **f32) if self.checkpoint_segments > 0 else None
         self.dh = torch.empty((T, H), **f32)
         self.block_ws = torch.empty(rdt.block_workspace_bytes(self.cfg, s.batch, s.seq),
                                     dtype=torch.uint8, device=dev)
@@ -58,7 +85,7 @@ class DecoderTrainer:
         self.sumsq = torch.zeros(1, dtype=torch.float64, device=dev)
         self.scale = torch.ones(1, **f32)
         self.nonfinite = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.loss_partials = torch.zeros(T, **f32)
+        self.loss_partials = torch.zeros(n_acc * T, **f32)
         self.targets = torch.zeros(T, dtype=torch.int32, device=dev)
         self.step_count = 0
 
@@ -82,7 +109,10 @@ class DecoderTrainer:
         return flat.view(block_shapes(s)[name])
 
     def saved_slice(self, layer):
-        return self.saved[layer * self.saved_bytes:(layer + 1) * self.saved_bytes]
+        """Activation slot of a layer: its own without checkpointing, else its
+        position within its segment."""
+        slot = layer % self.segment_size
+        return self.saved[slot * self.saved_bytes:(slot + 1) * self.saved_bytes]
 
     # ------------------------------------------------------------- set-up
     def load(self, blocks, head):
@@ -120,11 +150,15 @@ class DecoderTrainer:
         self.step_count = 0
 
     # --------------------------------------------------------------- step
-    def forward_backward(self, x=None, targets=None):
-        """Forward, fused CE and full backward; gradients land in ``self.g``.
-        x [T, H] fp32 and targets [T] int32 on the device (or already copied
-        into ``self.h[0]`` / ``self.targets`` when None)."""
+    def forward_backward(self, x=None, targets=None, micro=0):
+        """Forward, fused CE and full backward of one (micro-)batch; gradients
+        land in ``self.g`` (added to it for micro > 0). x [T, H] fp32 and
+        targets [T] int32 on the device (or already copied into ``self.h[0]``
+        / ``self.targets`` when None)."""
         s, cfg = self.shape, self.cfg
+        n = self.accumulation_steps
+        acc = micro > 0
+        sq = self.sumsq if micro == n - 1 else None
         if x is not None:
             self.h[0].copy_(x)
         if targets is not None:
@@ -135,16 +169,27 @@ class DecoderTrainer:
                               self.saved_slice(li), self.block_ws)
         T = s.tokens
         rdt.fused_cross_entropy(cfg, T, self.h[s.layers], self.tensor(self.w, "head", "g_final"),
-                                self.tensor(self.wb, "head", "w_lm"), self.targets, 1.0 / T,
-                                self.loss_partials, self.dh,
-                                self.tensor(self.g, "head", "g_final"),
+                                self.tensor(self.wb, "head", "w_lm"), self.targets,
+                                1.0 / (T * n), self.loss_partials[micro * T:(micro + 1) * T],
+                                self.dh, self.tensor(self.g, "head", "g_final"),
                                 self.tensor(self.g, "head", "w_lm"), self.head_ws,
-                                grad_sq=self.sumsq)
-        for li in reversed(range(s.layers)):
-            rdt.block_backward(cfg, s.batch, s.seq, self.block_slice(self.w, li),
-                               self.block_slice(self.wb, li), self.h[li], self.saved_slice(li),
-                               self.dh, self.dh, self.block_slice(self.g, li), self.block_ws,
-                               grad_sq=self.sumsq)
+                                grad_sq=sq, accumulate=acc)
+        L, seg = s.layers, self.segment_size
+        nseg = -(-L // seg)
+        for k in reversed(range(nseg)):
+            lo, hi = k * seg, min(L, (k + 1) * seg)
+            if k != nseg - 1:
+                # recompute this segment's activations from the kept layer inputs
+                for li in range(lo, hi):
+                    rdt.block_forward(cfg, s.batch, s.seq, self.block_slice(self.w, li),
+                                      self.block_slice(self.wb, li), self.h[li], self.h_rc,
+                                      self.saved_slice(li), self.block_ws)
+            for li in reversed(range(lo, hi)):
+                rdt.block_backward(cfg, s.batch, s.seq, self.block_slice(self.w, li),
+                                   self.block_slice(self.wb, li), self.h[li],
+                                   self.saved_slice(li), self.dh, self.dh,
+                                   self.block_slice(self.g, li), self.block_ws,
+                                   grad_sq=sq, accumulate=acc)
         return self.loss_partials
 
     def clip_and_update(self):
@@ -159,7 +204,16 @@ class DecoderTrainer:
                        skip=self.nonfinite, w_bf16=self.wb)
 
     def train_step(self, x=None, targets=None):
-        """One full step; returns the device tensor of per-token loss partials."""
-        self.forward_backward(x, targets)
+        """One full step; returns the device tensor of per-token loss partials.
+        With accumulation, x is [n T, H] and targets [n T]: n micro-batches of
+        T tokens, in order."""
+        n, T = self.accumulation_steps, self.shape.tokens
+        if n == 1:
+            self.forward_backward(x, targets)
+        else:
+            for i in range(n):
+                self.forward_backward(None if x is None else x[i * T:(i + 1) * T],
+                                      None if targets is None else targets[i * T:(i + 1) * T],
+                                      micro=i)
         self.clip_and_update()
         return self.loss_partials

@@ -1,0 +1,124 @@
+"""GPU tests of the step driver's training modes beyond the plain step:
+activation checkpointing (segmented recompute, cuda_trainer.rs
+``recompute_segment``) and gradient accumulation over micro-batches (R-038,
+``GpuGradientAccumulator``). The kernels are deterministic, so a mode that
+only changes when or how often the same block calls run must reproduce the
+plain step bit for bit; accumulation is checked against the FP64 oracle's
+accumulated step."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import model as om
+from resident_decoder_trainer_gb300 import rdt, synth
+from resident_decoder_trainer_gb300.step import DecoderTrainer
+
+from gpu_helpers import GRAD_REL_L2, LOSS_REL, ensure_built, ragged_shape, rel_l2, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+    yield
+    assert rdt.device_error() == 0
+
+
+def _run(shape, steps=2, **kw):
+    blocks, head, x, tg = synth.make_model_inputs(shape, 5)
+    tr = DecoderTrainer(shape, **kw)
+    tr.load(blocks, head)
+    xd, td = x.cuda(), tg.cuda()
+    losses = []
+    for _ in range(steps):
+        losses.append(tr.train_step(xd, td).clone())
+    torch.cuda.synchronize()
+    return tr, losses
+
+
+@pytest.mark.parametrize("segments", [1, 2, 5])
+def test_checkpointing_is_bit_identical(segments):
+    """5 layers in 1, 2 (3 + 2) or 5 segments: the recomputed activations, and
+    so the losses, gradients, weights and moments after two steps, equal the
+    plain step's exactly."""
+    shape = ragged_shape(layers=5)
+    ref, ref_losses = _run(shape)
+    tr, losses = _run(shape, checkpoint_segments=segments)
+    assert tr.segment_size == -(-5 // segments)
+    assert tr.saved.numel() == tr.segment_size * tr.saved_bytes
+    for a, b in zip(losses, ref_losses):
+        assert torch.equal(a, b)
+    for name in ("g", "w", "m", "v", "wb"):
+        assert torch.equal(getattr(tr, name), getattr(ref, name)), name
+    assert float(tr.sumsq) == float(ref.sumsq)
+
+
+# ------------------------------------------------------- gradient accumulation
+def test_accumulated_step_matches_oracle():
+    """Two micro-batches of two 200-token sequences each: gradients summed in
+    place by the gradient producers (dW GEMM epilogues with the old value as
+    the residual, gain reductions adding), the clip's squared sum taken from
+    the accumulated values."""
+    shape = ragged_shape()
+    n, T = 2, shape.tokens
+    blocks, head, _, _ = synth.make_model_inputs(shape, 2)
+    g = torch.Generator().manual_seed(9)
+    x = torch.randn(n * T, shape.hidden, generator=g)
+    tg = torch.randint(0, shape.vocab, (n * T,), generator=g, dtype=torch.int64)
+    ref = om.train_step_accumulated(blocks, head, [x[:T], x[T:]],
+                                    [tg[:T].numpy(), tg[T:].numpy()], shape, step=1,
+                                    optim=synth.OPTIM)
+    tr = DecoderTrainer(shape, accumulation_steps=n)
+    tr.load(blocks, head)
+    for i in range(n):
+        tr.forward_backward(x[i * T:(i + 1) * T].cuda(), tg[i * T:(i + 1) * T].int().cuda(),
+                            micro=i)
+    torch.cuda.synchronize()
+    lp = to_np(tr.loss_partials)
+    assert abs(lp.mean() - ref["loss"]) / ref["loss"] < LOSS_REL
+    for (li, name), gref in ref["grads"].items():
+        err = rel_l2(to_np(tr.tensor(tr.g, li, name)), gref)
+        assert err < GRAD_REL_L2, f"{li}.{name}: rel L2 {err:.3e}"
+    g_all = to_np(tr.g)
+    want = float(np.sum(g_all * g_all))
+    assert abs(float(tr.sumsq) - want) / want < 1e-6
+    assert abs(np.sqrt(float(tr.sumsq)) - ref["norm"]) / ref["norm"] < GRAD_REL_L2
+
+
+def test_accumulation_of_sequences_matches_the_whole_batch_on_gpu():
+    """Micro-batches that are the sequences of one batch: the accumulated GPU
+    gradients equal the one-pass GPU gradients of that batch up to fp32
+    summation order."""
+    whole_shape = ragged_shape(batch=2)
+    micro_shape = ragged_shape(batch=1)
+    blocks, head, x, tg = synth.make_model_inputs(whole_shape, 3)
+    whole = DecoderTrainer(whole_shape)
+    whole.load(blocks, head)
+    whole.forward_backward(x.cuda(), tg.cuda())
+    acc = DecoderTrainer(micro_shape, accumulation_steps=2)
+    acc.load(blocks, head)
+    T = micro_shape.tokens
+    for i in range(2):
+        acc.forward_backward(x[i * T:(i + 1) * T].cuda(), tg[i * T:(i + 1) * T].cuda(), micro=i)
+    torch.cuda.synchronize()
+    # per-token losses: same rows, possibly another tiling of the vocabulary
+    assert torch.allclose(acc.loss_partials, whole.loss_partials, rtol=1e-6, atol=0)
+    assert rel_l2(to_np(acc.g), to_np(whole.g)) < 1e-4
+    assert abs(float(acc.sumsq) - float(whole.sumsq)) / float(whole.sumsq) < 1e-4
+
+
+def test_accumulated_train_step_runs_and_updates():
+    shape = ragged_shape()
+    tr, losses = _run(shape, steps=1, accumulation_steps=1)
+    tr2 = DecoderTrainer(shape, accumulation_steps=2)
+    blocks, head, x, tg = synth.make_model_inputs(shape, 5)
+    tr2.load(blocks, head)
+    xs = torch.cat([x, x]).cuda()
+    ts = torch.cat([tg, tg]).cuda()
+    tr2.train_step(xs, ts)
+    torch.cuda.synchronize()
+    # the same micro-batch twice with loss scale 1/(2T): the gradient of the
+    # single batch, so the update matches the plain step's closely
+    assert rel_l2(to_np(tr2.w), to_np(tr.w)) < 1e-6
+    assert torch.equal(tr2.loss_partials[:shape.tokens], losses[0])
