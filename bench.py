@@ -69,6 +69,9 @@ def parse_args():
     ap.add_argument("--accumulation-steps", type=int, default=1,
                     help="gradient accumulation: micro-batches (of the workload's batch) per "
                          "optimizer step")
+    ap.add_argument("--embedding", action="store_true",
+                    help="device embedding: the step takes token ids (lookup, scatter-add "
+                         "backward and the table's AdamW on the GPU)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -225,13 +228,18 @@ def run_rdt(args, rank, world, local_rank):
     T = shape.tokens
     n_acc = max(1, args.accumulation_steps)
     tr = DecoderTrainer(shape, device=dev, checkpoint_segments=args.checkpoint_segments,
-                        accumulation_steps=n_acc)
+                        accumulation_steps=n_acc, embedding=args.embedding)
     tr.init_random(seed=1234 + rank)
     gen = torch.Generator(device=dev)
     gen.manual_seed(4321 + rank)
     nb = 4
     Ts = n_acc * T  # tokens per optimizer step
-    xs = [torch.randn(Ts, shape.hidden, device=dev, generator=gen) for _ in range(nb)]
+    if args.embedding:
+        xs = [torch.randint(0, shape.vocab, (Ts,), device=dev, generator=gen, dtype=torch.int32)
+              for _ in range(nb)]
+    else:
+        xs = [torch.randn(Ts, shape.hidden, device=dev, generator=gen) for _ in range(nb)]
+    kw = "ids" if args.embedding else "x"
     tgs = [torch.randint(0, shape.vocab, (Ts,), device=dev, generator=gen, dtype=torch.int32)
            for _ in range(nb)]
     stream = torch.cuda.current_stream()
@@ -241,9 +249,9 @@ def run_rdt(args, rank, world, local_rank):
             dist.barrier()
         torch.cuda.synchronize()
 
-    first_loss = float(tr.train_step(xs[0], tgs[0]).mean())
+    first_loss = float(tr.train_step(targets=tgs[0], **{kw: xs[0]}).mean())
     for i in range(1, args.warmup):
-        tr.train_step(xs[i % nb], tgs[i % nb])
+        tr.train_step(targets=tgs[i % nb], **{kw: xs[i % nb]})
     gemms_per_step = (17 * shape.layers + 3) * n_acc  # 12 per layer, 5 more when recomputed
     timer = rdt.GemmTimer(gemms_per_step * args.steps)
     barrier()
@@ -253,7 +261,7 @@ def run_rdt(args, rank, world, local_rank):
     with timer:
         e0.record(stream)
         for i in range(args.steps):
-            tr.train_step(xs[i % nb], tgs[i % nb])
+            tr.train_step(targets=tgs[i % nb], **{kw: xs[i % nb]})
         e1.record(stream)
         barrier()
     launches = rdt.launch_count() - l0
@@ -303,6 +311,12 @@ def run_rdt(args, rank, world, local_rank):
     out["config"]["params"] = tr.n_params
     out["config"]["algorithmic_tflop_per_step"] = round(step_flops / 1e12, 2)
     out["config"]["activation_gb_held"] = round(tr.saved.numel() / 1e9, 2)
+    if args.embedding:
+        out["config"]["embedding"] = ("device lookup + deterministic scatter-add backward + "
+                                      "the table's own AdamW")
+        out["config"]["params"] = tr.n_params + shape.vocab * shape.hidden
+        out["data"] = ("synthetic (device-generated uniform token ids and targets; N(0,0.02) "
+                       "random-init weights, N(0,1) embedding table)")
     if n_acc > 1:
         out["config"]["tokens_per_step"] = Ts
         out["config"]["global_batch"] = shape.batch * n_acc
@@ -324,17 +338,21 @@ def run_e2e(tr, shape, args, dev, world):
     its inputs from pinned host memory and reads its loss partials back."""
     import torch
     T = shape.tokens * tr.accumulation_steps
-    xh = torch.randn(T, shape.hidden).pin_memory()
+    if tr.embedding:  # the inputs are token ids
+        xh = torch.randint(0, shape.vocab, (T,), dtype=torch.int32).pin_memory()
+    else:
+        xh = torch.randn(T, shape.hidden).pin_memory()
     th = torch.randint(0, shape.vocab, (T,), dtype=torch.int32).pin_memory()
     lh = torch.empty(T, dtype=torch.float32).pin_memory()
-    xd = torch.empty(T, shape.hidden, device=dev)
+    xd = torch.empty(xh.shape, dtype=xh.dtype, device=dev)
     td = torch.empty(T, dtype=torch.int32, device=dev)
+    kw = "ids" if tr.embedding else "x"
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         xd.copy_(xh, non_blocking=True)
         td.copy_(th, non_blocking=True)
-        loss = tr.train_step(xd, td)
+        loss = tr.train_step(targets=td, **{kw: xd})
         lh.copy_(loss, non_blocking=True)
     torch.cuda.synchronize()
     dt = time.perf_counter() - t0

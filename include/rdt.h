@@ -50,6 +50,8 @@ typedef enum rdt_status {
   RDT_ECUDA = 2,       /* a CUDA runtime call or kernel launch failed */
   RDT_ETIMEOUT = 3,    /* a bounded device wait gave up (rdt_device_error) */
   RDT_ENONFINITE = 4,  /* reserved for callers: non-finite gradient norm */
+  RDT_EINDEX = 5,      /* a token id outside [0, vocab) met on the device
+                          (rdt_device_error; its row was zeroed / skipped) */
 } rdt_status;
 
 /* Model shape. hidden, head_dim and intermediate must be multiples of 16,
@@ -357,6 +359,30 @@ rdt_status rdt_gemm_timing_arm(void* const* events, double* flops, int32_t* kind
                                int32_t capacity);
 int64_t rdt_gemm_timing_disarm(void);
 int64_t rdt_launch_count(void);
+
+/* ---------------------------------------------------------------------------
+ * Token embedding on the device (cuda_trainer.rs: gpu_forward's embedding
+ * lookup and embed_backward's scatter-add, C-EMBED-GRAD-001, both of which
+ * the pages run on the host).
+ * rdt_embedding_forward: x[t, :] = table[ids[t], :]; table fp32 [vocab,
+ *   hidden] (hidden % 4 == 0), ids int32 [tokens] on the device, x fp32
+ *   [tokens, hidden]. An id outside [0, vocab) gives a zero row and records
+ *   RDT_EINDEX in the device error word.
+ * rdt_embedding_backward: dtable[id, :] = (accumulate == 0: every row first
+ *   zeroed) or += scale * sum over the tokens t with ids[t] == id of
+ *   dx[t, :], the sum taken in token order (deterministic, no atomics);
+ *   scale an optional device fp32 scalar (null: 1), normally the activation
+ *   gradient's own clip scale from rdt_sq_sum + rdt_clip_scale
+ *   (C-EMBED-GRAD-001); ids outside [0, vocab) are skipped. ws: device
+ *   scratch of rdt_embedding_workspace_bytes(tokens) bytes, 256-byte aligned.
+ * ------------------------------------------------------------------------- */
+size_t rdt_embedding_workspace_bytes(int32_t tokens);
+rdt_status rdt_embedding_forward(const float* table, int64_t vocab, int32_t hidden,
+                                 const int32_t* ids, int32_t tokens, float* x, void* stream);
+rdt_status rdt_embedding_backward(const int32_t* ids, int32_t tokens, const float* dx,
+                                  int32_t hidden, const float* scale, float* dtable,
+                                  int64_t vocab, int32_t accumulate, void* ws, size_t ws_bytes,
+                                  void* stream);
 
 /* Thread-local description of the last failure on this thread ("" if none). */
 const char* rdt_last_error(void);

@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "librdt.so")
 SOURCES = ["api.cu", "gemm.cu", "attention.cu", "attention_tc.cu", "elementwise.cu",
-           "sq_sum_static.cu"]
+           "sq_sum_static.cu", "embedding.cu"]
 HEADERS = ["common.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

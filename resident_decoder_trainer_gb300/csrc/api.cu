@@ -937,6 +937,37 @@ rdt_status rdt_gemm_nf4(const rdt_bf16* A, int64_t lda, const uint8_t* codes,
   return RDT_OK;
 }
 
+// ---------------------------------------------------------------- embedding
+size_t rdt_embedding_workspace_bytes(int32_t tokens) {
+  return tokens < 1 ? 0 : embedding_workspace_bytes(tokens);
+}
+
+rdt_status rdt_embedding_forward(const float* table, int64_t vocab, int32_t hidden,
+                                 const int32_t* ids, int32_t tokens, float* x, void* stream) {
+  if (!table || !ids || !x) return fail(RDT_EINVAL, "null pointer");
+  if (vocab < 1 || hidden < 4 || hidden % 4 || tokens < 1)
+    return fail(RDT_EINVAL, "vocab >= 1, hidden a positive multiple of 4, tokens >= 1");
+  if (!aligned16(table) || !aligned16(x)) return fail(RDT_EINVAL, "table and x must be 16-byte aligned");
+  RDT_CHECK_CUDA(embedding_forward(table, vocab, hidden, ids, tokens, x, device_error_ptr(),
+                                   static_cast<cudaStream_t>(stream)));
+  return RDT_OK;
+}
+
+rdt_status rdt_embedding_backward(const int32_t* ids, int32_t tokens, const float* dx,
+                                  int32_t hidden, const float* scale, float* dtable,
+                                  int64_t vocab, int32_t accumulate, void* ws, size_t ws_bytes,
+                                  void* stream) {
+  if (!ids || !dx || !dtable || !ws) return fail(RDT_EINVAL, "null pointer");
+  if (vocab < 1 || hidden < 4 || hidden % 4 || tokens < 1)
+    return fail(RDT_EINVAL, "vocab >= 1, hidden a positive multiple of 4, tokens >= 1");
+  if (!aligned16(dx) || !aligned16(dtable) || (reinterpret_cast<uintptr_t>(ws) & 255))
+    return fail(RDT_EINVAL, "dx, dtable 16-byte and ws 256-byte aligned");
+  if (ws_bytes < embedding_workspace_bytes(tokens)) return fail(RDT_EINVAL, "workspace too small");
+  RDT_CHECK_CUDA(embedding_backward(ids, tokens, dx, hidden, scale, dtable, vocab,
+                                    accumulate != 0, ws, static_cast<cudaStream_t>(stream)));
+  return RDT_OK;
+}
+
 rdt_status rdt_cast_bf16(const float* src, rdt_bf16* dst, int64_t n, void* stream) {
   if (!src || !dst) return fail(RDT_EINVAL, "null pointer");
   if (n < 0) return fail(RDT_EINVAL, "n must be >= 0");

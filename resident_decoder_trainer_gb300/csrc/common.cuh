@@ -11,6 +11,7 @@ namespace rdt {
 
 // Error codes recorded in the device error word (match rdt_status).
 constexpr int kErrTimeout = 3;
+constexpr int kErrIndex = 5;  // a token id outside [0, vocab) met on the device
 
 // Upper bound of any spin on an mbarrier, in globaltimer nanoseconds.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;

@@ -151,6 +151,14 @@ cudaError_t lora_bstack(const float* const* pieces, const int64_t* rows, int np,
                         bf16* out, cudaStream_t s);
 cudaError_t cast_bf16(const float* src, bf16* dst, int64_t n, cudaStream_t s);
 
+// ---------------------------------------------------------------- embedding
+cudaError_t embedding_forward(const float* table, int64_t V, int H, const int32_t* ids, int T,
+                              float* x, int* err, cudaStream_t s);
+size_t embedding_workspace_bytes(int T);
+cudaError_t embedding_backward(const int32_t* ids, int T, const float* dx, int H,
+                               const float* scale, float* dtable, int64_t V, bool accumulate,
+                               void* ws, cudaStream_t s);
+
 cudaError_t ce_finalize(const float2* part, int part_ld, int ntiles, const float* tgt_logit,
                         float* lse, float* loss, int T, cudaStream_t s);
 cudaError_t ce_grad(bf16* z, const float* lse, const int32_t* targets, float scale, int T, int V,

@@ -15,7 +15,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "librdt.so")
 
-RDT_OK, RDT_EINVAL, RDT_ECUDA, RDT_ETIMEOUT, RDT_ENONFINITE = 0, 1, 2, 3, 4
+RDT_OK, RDT_EINVAL, RDT_ECUDA, RDT_ETIMEOUT, RDT_ENONFINITE, RDT_EINDEX = 0, 1, 2, 3, 4, 5
 TENSOR_NAMES = ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "g_attn", "g_ffn", "g_q", "g_k")
 NF4_NAMES = ("wq", "wk", "wv", "wo", "wg", "wu", "wd")
 LORA_NAMES = ("a_q", "a_k", "a_v", "a_o", "a_g", "a_u", "a_d",
@@ -31,7 +31,8 @@ EXPORTS = (
     "rdt_sq_sum_noalloc", "rdt_gemm_nf4", "rdt_nf4_check", "rdt_nf4_code_bytes",
     "rdt_nf4_scale_count", "rdt_nf4_offsets", "rdt_lora_param_count", "rdt_lora_param_offsets",
     "rdt_lora_shadow_count", "rdt_lora_shadow", "rdt_nf4_saved_bytes", "rdt_nf4_workspace_bytes",
-    "rdt_nf4_block_forward", "rdt_nf4_block_backward",
+    "rdt_nf4_block_forward", "rdt_nf4_block_backward", "rdt_embedding_workspace_bytes",
+    "rdt_embedding_forward", "rdt_embedding_backward",
 )
 
 
@@ -86,6 +87,9 @@ def _load() -> ctypes.CDLL:
         "rdt_gemm_timing_disarm": (I64, []),
         "rdt_launch_count": (I64, []),
         "rdt_sq_sum_noalloc": (I32, [P, P, I32, P, P]),
+        "rdt_embedding_workspace_bytes": (SZ, [I32]),
+        "rdt_embedding_forward": (I32, [P, I64, I32, P, I32, P, P]),
+        "rdt_embedding_backward": (I32, [P, I32, P, I32, P, P, I64, I32, P, SZ, P]),
         "rdt_nf4_check": (I32, [CP, I32]),
         "rdt_nf4_code_bytes": (I64, [CP]),
         "rdt_nf4_scale_count": (I64, [CP]),
@@ -328,6 +332,25 @@ def nf4_block_backward(cfg, rank, alpha, batch, seq, codes, scales, gains, shado
                                         _ptr(lora_grads),
                                         None if grad_sq is None else _ptr(grad_sq), _ptr(ws),
                                         ws.numel() * ws.element_size(), _stream(stream)))
+
+
+# ---------------------------------------------------------------- embedding
+def embedding_workspace_bytes(tokens: int) -> int:
+    return lib().rdt_embedding_workspace_bytes(int(tokens))
+
+
+def embedding_forward(table, ids, x, stream=None):
+    """x[t] = table[ids[t]]; table fp32 [V, H], ids int32 [T], x fp32 [T, H]."""
+    _check(lib().rdt_embedding_forward(_ptr(table), table.shape[0], table.shape[1], _ptr(ids),
+                                       ids.numel(), _ptr(x), _stream(stream)))
+
+
+def embedding_backward(ids, dx, dtable, ws, scale=None, accumulate=False, stream=None):
+    """dtable[id] (=, or += when accumulate) scale * sum of dx over the tokens with that id."""
+    _check(lib().rdt_embedding_backward(_ptr(ids), ids.numel(), _ptr(dx), dx.shape[1], _ptr(scale),
+                                        _ptr(dtable), dtable.shape[0], int(bool(accumulate)),
+                                        _ptr(ws), ws.numel() * ws.element_size(),
+                                        _stream(stream)))
 
 
 def cast_bf16(src, dst, n=None, stream=None):

@@ -28,7 +28,14 @@ R-038 / ``GpuGradientAccumulator``, loss scale 1/seq_len/accumulation_steps in
 ``train_step_inner``): a step takes n micro-batches of the shape's tokens;
 each runs forward and backward with the CE loss scaled by 1/(T n), the
 gradient producers adding into ``g`` after the first; the clip's squared sum
-is taken from the accumulated values on the last micro-batch, then one AdamW. The loss partials stay on the device until the
+is taken from the accumulated values on the last micro-batch, then one AdamW.
+
+Device embedding (``embedding=True``; cuda_trainer.rs ``gpu_forward`` lookup and
+``embed_backward``, C-EMBED-GRAD-001, both moved from the host to the GPU): the
+step takes token ids; x = E[ids] by a gather kernel; the activation gradient
+leaving the first block is clipped by its own norm and scatter-added into the
+table's gradient (deterministically, in token order); the table has its own
+AdamW, outside the global clip. The loss partials stay on the device until the
 caller reads them. Every launch is a librdt kernel; torch is used only to
 allocate buffers and for the stream.
 """
@@ -46,7 +53,7 @@ def _align(n: int, a: int = 64) -> int:
 
 class DecoderTrainer:
     def __init__(self, shape: DecoderShape, device="cuda", optim=None, checkpoint_segments=0,
-                 accumulation_steps=1):
+                 accumulation_steps=1, embedding=False):
         self.shape = s = shape
         self.accumulation_steps = n_acc = max(1, int(accumulation_steps))
         self.device = torch.device(device)
@@ -87,6 +94,18 @@ class DecoderTrainer:
         self.nonfinite = torch.zeros(1, dtype=torch.int32, device=dev)
         self.loss_partials = torch.zeros(n_acc * T, **f32)
         self.targets = torch.zeros(T, dtype=torch.int32, device=dev)
+        self.embedding = bool(embedding)
+        if self.embedding:
+            self.emb = torch.zeros((V, H), **f32)
+            self.emb_g = torch.zeros((V, H), **f32)
+            self.emb_m = torch.zeros((V, H), **f32)
+            self.emb_v = torch.zeros((V, H), **f32)
+            self.ids = torch.zeros(n_acc * T, dtype=torch.int32, device=dev)
+            self.emb_ws = torch.empty(rdt.embedding_workspace_bytes(T), dtype=torch.uint8,
+                                      device=dev)
+            self.emb_sumsq = torch.zeros(1, dtype=torch.float64, device=dev)
+            self.emb_scale = torch.ones(1, **f32)
+            self.emb_nonfinite = torch.zeros(1, dtype=torch.int32, device=dev)
         self.step_count = 0
 
     # -------------------------------------------------------------- views
@@ -115,14 +134,16 @@ class DecoderTrainer:
         return self.saved[slot * self.saved_bytes:(slot + 1) * self.saved_bytes]
 
     # ------------------------------------------------------------- set-up
-    def load(self, blocks, head):
+    def load(self, blocks, head, emb=None):
         """Copy parameter dicts (from ``synth``) into the flat masters and cast
-        the bf16 shadow."""
+        the bf16 shadow; emb: the embedding table [V, H] (device embedding)."""
         for li, p in enumerate(blocks):
             for name, t in p.items():
                 self.tensor(self.w, li, name).copy_(t)
         for name, t in head.items():
             self.tensor(self.w, "head", name).copy_(t)
+        if emb is not None:
+            self.emb.copy_(emb)
         self.refresh_shadow()
 
     def init_random(self, seed=0, std=0.02):
@@ -139,6 +160,9 @@ class DecoderTrainer:
                     t.normal_(0.0, std, generator=gen)
         self.tensor(self.w, "head", "g_final").fill_(1.0)
         self.tensor(self.w, "head", "w_lm").normal_(0.0, std, generator=gen)
+        if self.embedding:
+            # rows ~N(0, 1): the looked-up hidden states have the workloads' statistics
+            self.emb.normal_(0.0, 1.0, generator=gen)
         self.refresh_shadow()
 
     def refresh_shadow(self):
@@ -147,10 +171,13 @@ class DecoderTrainer:
     def reset_optimizer(self):
         self.m.zero_()
         self.v.zero_()
+        if self.embedding:
+            self.emb_m.zero_()
+            self.emb_v.zero_()
         self.step_count = 0
 
     # --------------------------------------------------------------- step
-    def forward_backward(self, x=None, targets=None, micro=0):
+    def forward_backward(self, x=None, targets=None, micro=0, ids=None):
         """Forward, fused CE and full backward of one (micro-)batch; gradients
         land in ``self.g`` (added to it for micro > 0). x [T, H] fp32 and
         targets [T] int32 on the device (or already copied into ``self.h[0]``
@@ -159,7 +186,12 @@ class DecoderTrainer:
         n = self.accumulation_steps
         acc = micro > 0
         sq = self.sumsq if micro == n - 1 else None
-        if x is not None:
+        T = s.tokens
+        if ids is not None:
+            self.ids[micro * T:(micro + 1) * T].copy_(ids)
+        if self.embedding:
+            rdt.embedding_forward(self.emb, self.ids[micro * T:(micro + 1) * T], self.h[0])
+        elif x is not None:
             self.h[0].copy_(x)
         if targets is not None:
             self.targets.copy_(targets)
@@ -167,7 +199,6 @@ class DecoderTrainer:
             rdt.block_forward(cfg, s.batch, s.seq, self.block_slice(self.w, li),
                               self.block_slice(self.wb, li), self.h[li], self.h[li + 1],
                               self.saved_slice(li), self.block_ws)
-        T = s.tokens
         rdt.fused_cross_entropy(cfg, T, self.h[s.layers], self.tensor(self.w, "head", "g_final"),
                                 self.tensor(self.wb, "head", "w_lm"), self.targets,
                                 1.0 / (T * n), self.loss_partials[micro * T:(micro + 1) * T],
@@ -190,6 +221,14 @@ class DecoderTrainer:
                                    self.saved_slice(li), self.dh, self.dh,
                                    self.block_slice(self.g, li), self.block_ws,
                                    grad_sq=sq, accumulate=acc)
+        if self.embedding:
+            # C-EMBED-GRAD-001: the activation gradient clipped by its own norm,
+            # then scatter-added into the table's gradient
+            rdt.sq_sum_noalloc([self.dh], self.emb_sumsq)
+            rdt.clip_scale(self.emb_sumsq, self.optim["max_norm"], self.emb_scale,
+                           self.emb_nonfinite)
+            rdt.embedding_backward(self.ids[micro * T:(micro + 1) * T], self.dh, self.emb_g,
+                                   self.emb_ws, scale=self.emb_scale, accumulate=acc)
         return self.loss_partials
 
     def clip_and_update(self):
@@ -202,18 +241,22 @@ class DecoderTrainer:
         rdt.adamw_step(self.w, self.g, self.m, self.v, self.step_count, o["lr"], o["beta1"],
                        o["beta2"], o["eps"], o["weight_decay"], scale=self.scale,
                        skip=self.nonfinite, w_bf16=self.wb)
+        if self.embedding:
+            rdt.adamw_step(self.emb, self.emb_g, self.emb_m, self.emb_v, self.step_count,
+                           o["lr"], o["beta1"], o["beta2"], o["eps"], o["weight_decay"],
+                           skip=self.emb_nonfinite)
 
-    def train_step(self, x=None, targets=None):
+    def train_step(self, x=None, targets=None, ids=None):
         """One full step; returns the device tensor of per-token loss partials.
-        With accumulation, x is [n T, H] and targets [n T]: n micro-batches of
-        T tokens, in order."""
+        x: hidden states [n T, H] (or, with the device embedding, ids: int32
+        token ids [n T]); targets [n T]: n micro-batches of T tokens, in order
+        (n = 1 without accumulation)."""
         n, T = self.accumulation_steps, self.shape.tokens
-        if n == 1:
-            self.forward_backward(x, targets)
-        else:
-            for i in range(n):
-                self.forward_backward(None if x is None else x[i * T:(i + 1) * T],
-                                      None if targets is None else targets[i * T:(i + 1) * T],
-                                      micro=i)
+
+        def part(a, i):
+            return None if a is None else a[i * T:(i + 1) * T]
+
+        for i in range(n):
+            self.forward_backward(part(x, i), part(targets, i), micro=i, ids=part(ids, i))
         self.clip_and_update()
         return self.loss_partials

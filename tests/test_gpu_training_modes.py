@@ -13,7 +13,8 @@ from oracle import model as om
 from resident_decoder_trainer_gb300 import rdt, synth
 from resident_decoder_trainer_gb300.step import DecoderTrainer
 
-from gpu_helpers import GRAD_REL_L2, LOSS_REL, ensure_built, ragged_shape, rel_l2, to_np
+from gpu_helpers import (ADAMW_REL, GRAD_REL_L2, LOSS_REL, ensure_built, ragged_shape, rel_l2,
+                         to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -122,3 +123,86 @@ def test_accumulated_train_step_runs_and_updates():
     # single batch, so the update matches the plain step's closely
     assert rel_l2(to_np(tr2.w), to_np(tr.w)) < 1e-6
     assert torch.equal(tr2.loss_partials[:shape.tokens], losses[0])
+
+
+# ------------------------------------------------------------ device embedding
+from oracle import embedding as oe  # noqa: E402
+
+
+def test_embedding_lookup_is_exact_and_flags_bad_ids():
+    g = torch.Generator().manual_seed(1)
+    V, H, T = 1000, 256, 777
+    table = torch.randn(V, H, generator=g).cuda()
+    ids = torch.randint(0, V, (T,), generator=g, dtype=torch.int32)
+    ids[5] = ids[9] = 17
+    x = torch.full((T, H), float("nan"), device="cuda")
+    rdt.embedding_forward(table, ids.cuda(), x)
+    torch.cuda.synchronize()
+    assert torch.equal(x, table[ids.long().cuda()])
+    assert rdt.device_error() == 0
+    ids[3] = V  # out of range: a zero row and RDT_EINDEX, no fault
+    rdt.embedding_forward(table, ids.cuda(), x)
+    assert rdt.device_error() == rdt.RDT_EINDEX
+    assert float(x[3].abs().max()) == 0.0
+    assert torch.equal(x[4:], table[ids[4:].long().cuda()])
+
+
+@pytest.mark.parametrize("V,H,T,distinct", [(5000, 512, 3000, 40), (300, 64, 1, 1),
+                                            (151936, 2560, 4096, 151936)])
+def test_embedding_scatter_add_matches_oracle(V, H, T, distinct):
+    """Duplicate-heavy, single-token and Qwen3-4B-sized cases: the scatter-add
+    against the oracle on the rows the tokens touch (compact re-indexing keeps
+    the oracle small), untouched rows exactly zero, accumulation adding, and
+    the same bits on a second run."""
+    g = torch.Generator().manual_seed(V + T)
+    ids = torch.randint(0, distinct, (T,), generator=g, dtype=torch.int32)
+    dx = torch.randn(T, H, generator=g)
+    scale = torch.tensor([0.37], device="cuda")
+    dtable = torch.full((V, H), float("nan"), device="cuda")
+    ws = torch.empty(rdt.embedding_workspace_bytes(T), dtype=torch.uint8, device="cuda")
+    idd, dxd = ids.cuda(), dx.cuda()
+    rdt.embedding_backward(idd, dxd, dtable, ws, scale=scale)
+    first = dtable.clone()
+    rdt.embedding_backward(idd, dxd, dtable, ws, scale=scale)
+    torch.cuda.synchronize()
+    assert torch.equal(first, dtable)  # deterministic
+    used, compact = torch.unique(ids.long(), return_inverse=True)
+    ref, _ = oe.embedding_grad(compact.numpy(), dx.numpy(), len(used))
+    got = dtable[used.cuda()].double().cpu().numpy()
+    assert np.max(np.abs(got - 0.37 * ref)) <= 1e-6 * max(1.0, np.max(np.abs(ref)))
+    mask = torch.ones(V, dtype=torch.bool)
+    mask[used] = False
+    assert float(dtable[mask.cuda()].abs().max() if mask.any() else 0.0) == 0.0
+    rdt.embedding_backward(idd, dxd, dtable, ws, scale=scale, accumulate=True)
+    torch.cuda.synchronize()
+    got2 = dtable[used.cuda()].double().cpu().numpy()
+    assert np.max(np.abs(got2 - 2 * 0.37 * ref)) <= 2e-6 * max(1.0, np.max(np.abs(ref)))
+
+
+def test_embedded_step_matches_oracle():
+    """The step fed by token ids: lookup, model, the first block's activation
+    gradient clipped by its own norm and scatter-added, the table's own AdamW
+    next to the global clip + AdamW of the rest."""
+    shape = ragged_shape()
+    blocks, head, _, tg = synth.make_model_inputs(shape, 4)
+    g = torch.Generator().manual_seed(8)
+    table = torch.randn(shape.vocab, shape.hidden, generator=g)
+    ids = torch.randint(0, 50, (shape.tokens,), generator=g, dtype=torch.int32)
+    ref = oe.train_step_embedded(table.numpy(), blocks, head, ids.numpy(), tg.numpy(), shape,
+                                 step=1, optim=synth.OPTIM)
+    tr = DecoderTrainer(shape, embedding=True)
+    tr.load(blocks, head, emb=table)
+    tr.train_step(targets=tg.cuda(), ids=ids.cuda())
+    torch.cuda.synchronize()
+    lp = to_np(tr.loss_partials)
+    assert abs(lp.mean() - ref["loss"]) / ref["loss"] < LOSS_REL
+    assert abs(float(tr.emb_scale) - ref["emb_scale"]) / ref["emb_scale"] < GRAD_REL_L2
+    err = rel_l2(to_np(tr.emb_g), ref["emb_grad"])
+    assert err < GRAD_REL_L2, err
+    # the table's AdamW given the same gradient (its own, no global scale)
+    o = synth.OPTIM
+    w0 = table.numpy().astype(np.float64)
+    want, _, _ = om.adamw(w0, to_np(tr.emb_g), np.zeros_like(w0), np.zeros_like(w0), 1, o["lr"],
+                          o["beta1"], o["beta2"], o["eps"], o["weight_decay"], 1.0)
+    assert np.max(np.abs(to_np(tr.emb) - want)) <= ADAMW_REL * np.max(np.abs(want))
+    assert rdt.device_error() == 0
