@@ -690,22 +690,37 @@ __device__ __forceinline__ void nf4_planes(float sc, uint32_t (&lo)[4], uint32_t
   }
 }
 
+// Multipliers that stand in for shifts (w * 16 = w << 4; umulhi(w, 2^16) =
+// w >> 16; umulhi(w, 2^20) = w >> 12): kept in constant memory so the
+// compiler issues integer multiplies, which run on the FMA pipe, and the
+// byte permutes and logic ops have the ALU pipe to themselves.
+__constant__ uint32_t kNf4ShiftMul[3] = {16u, 1u << 16, 1u << 20};
+
 // T[c] for the four codes in the low 16 bits of s (code j in bits 4j..4j+3)
-// as two bf16 pairs (code 0 in the low half of .x). A byte permute indexes 8
-// bytes, so each plane is looked up in its lower (codes 0-7) and upper
-// (8-15, selector bit 3 flipped) halves and the two merged on bit 3 of the code.
-__device__ __forceinline__ uint2 nf4_lookup4(uint32_t s, const uint32_t (&lo)[4],
-                                             const uint32_t (&hi)[4]) {
-  const uint32_t sx = s ^ 0x8888u;
+// as two bf16 pairs (code 0 in the low half of .x). sx = s with bit 3 of
+// every code flipped; t = s << 4 (the bytes of s and t carry the top bits
+// of the four codes). A byte permute indexes 8 bytes, so each plane is looked
+// up in its lower (codes 0-7, selector s) and upper (8-15, selector sx)
+// halves and the two merged on bit 3 of the code, replicated into a byte
+// mask by the permute's sign mode.
+__device__ __forceinline__ uint2 nf4_lookup4(uint32_t s, uint32_t sx, uint32_t t,
+                                             const uint32_t (&lo)[4], const uint32_t (&hi)[4]) {
+  const uint32_t m = prmt(t, s, 0xD9C8);
   const uint32_t la = prmt(lo[0], lo[1], s), lb = prmt(lo[2], lo[3], sx);
   const uint32_t ha = prmt(hi[0], hi[1], s), hb = prmt(hi[2], hi[3], sx);
-  // byte j of c carries bit 3 of code j in its top bit; replicate it
-  const uint32_t a = prmt(s, 0u, 0x1100);
-  const uint32_t c = (a & 0x80008000u) | ((a << 4) & 0x00800080u);
-  const uint32_t m = prmt(c, 0u, 0xBA98);
   const uint32_t l = (la & ~m) | (lb & m);
   const uint32_t h = (ha & ~m) | (hb & m);
   return make_uint2(prmt(l, h, 0x5140), prmt(l, h, 0x7362));
+}
+
+// The eight weights of one code word (element j in bits 4j..4j+3) as bf16.
+__device__ __forceinline__ uint4 nf4_lookup8(uint32_t w, const uint32_t (&lo)[4],
+                                             const uint32_t (&hi)[4]) {
+  const uint32_t sxw = w ^ 0x88888888u;
+  const uint2 e0 = nf4_lookup4(w, sxw, w * kNf4ShiftMul[0], lo, hi);
+  const uint2 e1 = nf4_lookup4(__umulhi(w, kNf4ShiftMul[1]), __umulhi(sxw, kNf4ShiftMul[1]),
+                               __umulhi(w, kNf4ShiftMul[2]), lo, hi);
+  return make_uint4(e0.x, e0.y, e1.x, e1.y);
 }
 
 // Decode one 64-weight run (32 code bytes as two 16-byte chunks c0, c1; one
@@ -718,9 +733,7 @@ __device__ __forceinline__ void nf4_decode_run(uint4 c0, uint4 c1, float sc, uin
 #pragma unroll
   for (int c8 = 0; c8 < 8; ++c8) {
     // 4 code bytes = 8 weights, element 2j in the low nibble of byte j
-    const uint2 e0 = nf4_lookup4(w[c8] & 0xFFFFu, lo, hi);
-    const uint2 e1 = nf4_lookup4(w[c8] >> 16, lo, hi);
-    *reinterpret_cast<uint4*>(dst + sw128_offset(row, c8)) = make_uint4(e0.x, e0.y, e1.x, e1.y);
+    *reinterpret_cast<uint4*>(dst + sw128_offset(row, c8)) = nf4_lookup8(w[c8], lo, hi);
   }
 }
 
