@@ -64,15 +64,17 @@ struct FwdCfg {
   static constexpr uint32_t CHUNK = 128 * 128;  // 64 cols x 128 rows of bf16
   static constexpr uint32_t Q_BYTES = BM * D * 2;
   static constexpr uint32_t KV_BYTES = BN * D * 2;
-  static constexpr uint32_t OFF_Q = 0;
-  static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;       // [2]
-  static constexpr uint32_t OFF_V = OFF_K + 2 * KV_BYTES;  // [2]
+  static constexpr uint32_t OFF_Q = 0;                       // [2]
+  static constexpr uint32_t OFF_K = OFF_Q + 2 * Q_BYTES;     // [2]
+  static constexpr uint32_t OFF_V = OFF_K + 2 * KV_BYTES;    // [2]
   static constexpr uint32_t OFF_RED = OFF_V + 2 * KV_BYTES;  // float [2][2][128] maxima, [2][128] sums
   static constexpr uint32_t OFF_BAR = OFF_RED + 3 * 2 * 128 * 4;
   static constexpr size_t SMEM = OFF_BAR + 256 + 1024;
   // TMEM: two S buffers (128 fp32 columns each; P is written over the first
-  // 64 columns of its S buffer as packed bf16), O after them
+  // 64 columns of its S buffer as packed bf16), then two O buffers (work
+  // items alternate, so one item's output is read while the next accumulates)
   static constexpr uint32_t TMEM_S = 0, TMEM_O = 256, TMEM_COLS = 512;
+  static_assert(TMEM_O + 2 * D <= TMEM_COLS, "two O buffers must fit in TMEM");
 };
 
 // Rows rescale O only when their running maximum grows by more than 2^8 (in
@@ -80,6 +82,20 @@ struct FwdCfg {
 // the result is the same (O and l are both relative to the stale maximum).
 constexpr float kRescaleLog2 = 8.f;
 
+// Work item idx (longest causal rows first) -> query tile, head, sequence.
+__device__ __forceinline__ void fwd_item(int idx, int n_qt, int nh, int B, int& mt, int& h,
+                                         int& b) {
+  const int per = nh * B;
+  mt = n_qt - 1 - idx / per;
+  const int rem = idx % per;
+  h = rem % nh;
+  b = rem / nh;
+}
+
+// Persistent: each CTA takes work items blockIdx.x, blockIdx.x + gridDim.x,
+// ... Barrier phases run over the CTA's whole sequence of key tiles (jg) and
+// items (it), so the next item's Q and first key tiles are loaded and its
+// first scores computed while this item's output is written.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -93,30 +109,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + C::OFF_BAR;
-  const uint32_t q_full = bar0, k_full = bar0 + 8, v_full = bar0 + 24, kv_empty = bar0 + 40,
-                 s_full = bar0 + 56, p_full = bar0 + 72, o_done = bar0 + 80, drain = bar0 + 88;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 128);
+  const uint32_t q_full = bar0, q_empty = bar0 + 16, k_full = bar0 + 32, v_full = bar0 + 48,
+                 kv_empty = bar0 + 64, s_full = bar0 + 80, p_full = bar0 + 96,
+                 o_done = bar0 + 104, o_free = bar0 + 112, drain = bar0 + 128;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 192);
   float* red_max = reinterpret_cast<float*>(smem + C::OFF_RED);  // [2 parity][2 half][128 rows]
   float* red_sum = red_max + 2 * 2 * 128;                        // [2 half][128 rows]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_qt = (S + BM - 1) / BM;
-  const int per = nh * B;
-  const int mt = n_qt - 1 - static_cast<int>(blockIdx.x) / per;  // longest rows first
-  const int rem = static_cast<int>(blockIdx.x) % per;
-  const int h = rem % nh, b = rem / nh;
-  const int g = h / (nh / nkv);
-  const int m0 = mt * BM;
-  const int n_tiles = min(n_qt, mt + 1);
-  const int tok0 = b * S;
+  const int n_items = n_qt * nh * B;
+  const int grp = nh / nkv;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(q_full + 8 * i, 1);
+      mbar_init(q_empty + 8 * i, 1);
       mbar_init(k_full + 8 * i, 1);
       mbar_init(v_full + 8 * i, 1);
       mbar_init(kv_empty + 8 * i, 1);
       mbar_init(s_full + 8 * i, 1);
+      mbar_init(o_free + 8 * i, kEltThreads);
     }
     mbar_init(p_full, kEltThreads);
     mbar_init(o_done, 1);
@@ -137,37 +150,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // --------------------------------------------------------- producer
-      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
-      for (int c = 0; c < DCH; ++c)
-        tma_load_2d(sbase + C::OFF_Q + c * C::CHUNK, &tq, q_full, h * D + c * 64, tok0 + m0);
-      uint32_t pending = 0;
       bool ok = true;
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait(kv_empty + 8 * st, ph ^ 1, err)) {
+      int jg = 0;
+      for (int idx = blockIdx.x, it = 0; idx < n_items && ok; idx += gridDim.x, ++it) {
+        int mt, h, b;
+        fwd_item(idx, n_qt, nh, B, mt, h, b);
+        const int g = h / grp, tok0 = b * S, n_tiles = min(n_qt, mt + 1);
+        const int qb = it & 1;
+        if (!mbar_wait(q_empty + 8 * qb, ((it >> 1) & 1) ^ 1, err)) {
           ok = false;
           break;
         }
-        const int n0 = j * BN;
-        mbar_arrive_expect_tx(k_full + 8 * st, C::KV_BYTES);
+        mbar_arrive_expect_tx(q_full + 8 * qb, C::Q_BYTES);
         for (int c = 0; c < DCH; ++c)
-          tma_load_2d(sbase + C::OFF_K + st * C::KV_BYTES + c * C::CHUNK, &tk, k_full + 8 * st,
-                      g * D + c * 64, tok0 + n0);
-        mbar_arrive_expect_tx(v_full + 8 * st, C::KV_BYTES);
-        for (int c = 0; c < DCH; ++c)
-          tma_load_2d(sbase + C::OFF_V + st * C::KV_BYTES + c * C::CHUNK, &tv, v_full + 8 * st,
-                      g * D + c * 64, tok0 + n0);
-        pending = (pending & ~(3u << (2 * st))) | ((1u | (ph << 1)) << (2 * st));
-      }
-      if (!ok) {
-        for (int st = 0; st < 2; ++st)
-          if ((pending >> (2 * st)) & 1u) {
-            const uint32_t ph = (pending >> (2 * st + 1)) & 1u;
-            mbar_wait(k_full + 8 * st, ph, nullptr);
-            mbar_wait(v_full + 8 * st, ph, nullptr);
+          tma_load_2d(sbase + C::OFF_Q + qb * C::Q_BYTES + c * C::CHUNK, &tq, q_full + 8 * qb,
+                      h * D + c * 64, tok0 + mt * BM);
+        for (int j = 0; j < n_tiles; ++j, ++jg) {
+          const int st = jg & 1;
+          const uint32_t ph = (jg >> 1) & 1;
+          if (!mbar_wait(kv_empty + 8 * st, ph ^ 1, err)) {
+            ok = false;
+            break;
           }
-        mbar_wait(q_full, 0, nullptr);
+          const int n0 = j * BN;
+          mbar_arrive_expect_tx(k_full + 8 * st, C::KV_BYTES);
+          for (int c = 0; c < DCH; ++c)
+            tma_load_2d(sbase + C::OFF_K + st * C::KV_BYTES + c * C::CHUNK, &tk, k_full + 8 * st,
+                        g * D + c * 64, tok0 + n0);
+          mbar_arrive_expect_tx(v_full + 8 * st, C::KV_BYTES);
+          for (int c = 0; c < DCH; ++c)
+            tma_load_2d(sbase + C::OFF_V + st * C::KV_BYTES + c * C::CHUNK, &tv, v_full + 8 * st,
+                        g * D + c * 64, tok0 + n0);
+        }
       }
     }
   } else if (warp == 1) {
@@ -175,48 +189,78 @@ __global__ void __launch_bounds__(kThreads, 1)
       // -------------------------------------------------------------- MMA
       constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0, 0);
       constexpr uint32_t idesc_o = idesc_bf16_f32(BM, D, 0, 1);
-      bool ok = mbar_wait(q_full, 0, err);
-      auto issue_s = [&](int j) -> bool {
-        const int st = j & 1;
-        if (!mbar_wait(k_full + 8 * st, (j >> 1) & 1, err)) return false;
-        tc_fence_after();
-        const uint32_t kb = sbase + C::OFF_K + st * C::KV_BYTES;
+      bool ok = true;
+      int jg = 0;
+      for (int idx = blockIdx.x, it = 0; idx < n_items && ok; idx += gridDim.x, ++it) {
+        int mt, h, b;
+        fwd_item(idx, n_qt, nh, B, mt, h, b);
+        const int n_tiles = min(n_qt, mt + 1);
+        const int qb = it & 1;
+        const uint32_t qaddr = sbase + C::OFF_Q + qb * C::Q_BYTES;
+        const uint32_t t_o = tmem + C::TMEM_O + qb * D;
+        auto issue_s = [&](int jj) -> bool {
+          const int st = jj & 1;
+          if (!mbar_wait(k_full + 8 * st, (jj >> 1) & 1, err)) return false;
+          tc_fence_after();
+          const uint32_t kb = sbase + C::OFF_K + st * C::KV_BYTES;
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * C::CHUNK + (k & 3) * 32;
-          tc_mma_bf16(tmem + C::TMEM_S + st * BN, sdesc_sw128(sbase + C::OFF_Q + off, 16, 1024),
-                      sdesc_sw128(kb + off, 16, 1024), idesc_s, k > 0);
-        }
-        tc_commit(s_full + 8 * st);
-        return true;
-      };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const int st = j & 1;
-        if (j + 1 < n_tiles) {
-          // S buffer (j+1)&1 still holds P_{j-1}, read by P_{j-1} V
-          if (j >= 1 && !mbar_wait(o_done, (j - 1) & 1, err)) {
-            ok = false;
-            break;
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k >> 2) * C::CHUNK + (k & 3) * 32;
+            tc_mma_bf16(tmem + C::TMEM_S + st * BN, sdesc_sw128(qaddr + off, 16, 1024),
+                        sdesc_sw128(kb + off, 16, 1024), idesc_s, k > 0);
           }
-          if (!issue_s(j + 1)) {
-            ok = false;
-            break;
-          }
-        }
-        if (!mbar_wait(p_full, j & 1, err) || !mbar_wait(v_full + 8 * st, (j >> 1) & 1, err)) {
+          tc_commit(s_full + 8 * st);
+          return true;
+        };
+        if (!mbar_wait(q_full + 8 * qb, (it >> 1) & 1, err)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const uint32_t vb = sbase + C::OFF_V + st * C::KV_BYTES;
-        // O += P V with P (bf16, in TMEM over S buffer st) as the A operand
+        // both S buffers held P of the previous item's last two tiles: wait
+        // for the last P V issued (tcgen05 operations complete in order)
+        if (jg >= 1 && !mbar_wait(o_done, (jg - 1) & 1, err)) {
+          ok = false;
+          break;
+        }
+        if (!issue_s(jg)) {
+          ok = false;
+          break;
+        }
+        if (n_tiles == 1) tc_commit(q_empty + 8 * qb);
+        // this O buffer was read out by item it - 2
+        if (!mbar_wait(o_free + 8 * qb, ((it >> 1) & 1) ^ 1, err)) {
+          ok = false;
+          break;
+        }
+        for (int j = 0; j < n_tiles && ok; ++j) {
+          const int jj = jg + j, st = jj & 1;
+          if (j + 1 < n_tiles) {
+            // S buffer (jj+1)&1 still holds P_{jj-1}, read by P_{jj-1} V
+            if (j >= 1 && !mbar_wait(o_done, (jj - 1) & 1, err)) {
+              ok = false;
+              break;
+            }
+            if (!issue_s(jj + 1)) {
+              ok = false;
+              break;
+            }
+            if (j + 2 == n_tiles) tc_commit(q_empty + 8 * qb);  // the item's last Q K^T
+          }
+          if (!mbar_wait(p_full, jj & 1, err) || !mbar_wait(v_full + 8 * st, (jj >> 1) & 1, err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t vb = sbase + C::OFF_V + st * C::KV_BYTES;
+          // O += P V with P (bf16, in TMEM over S buffer st) as the A operand
 #pragma unroll
-        for (int k = 0; k < BN / 16; ++k)
-          tc_mma_bf16_ts(tmem + C::TMEM_O, tmem + C::TMEM_S + st * BN + k * 8,
-                         sdesc_sw128(vb + k * 2048, C::CHUNK, 1024), idesc_o, (j | k) != 0);
-        tc_commit(o_done);
-        tc_commit(kv_empty + 8 * st);
+          for (int k = 0; k < BN / 16; ++k)
+            tc_mma_bf16_ts(t_o, tmem + C::TMEM_S + st * BN + k * 8,
+                           sdesc_sw128(vb + k * 2048, C::CHUNK, 1024), idesc_o, (j | k) != 0);
+          tc_commit(o_done);
+          tc_commit(kv_empty + 8 * st);
+        }
+        jg += n_tiles;
       }
       tc_commit(drain);
       mbar_wait(drain, 0, nullptr);
@@ -226,77 +270,87 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
-    const int qpos = m0 + row;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    float m_run = -INFINITY, l_part = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int st = j & 1;
-      if (!warp_wait(s_full + 8 * st, (j >> 1) & 1, err)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sv[64];
-      const uint32_t ts = tmem + lane_base + C::TMEM_S + st * BN;
-      tmem_ld32(ts + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-      tmem_ld32(ts + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-      tmem_ld_wait();
-      const int c0 = j * BN + half * 64;  // key position of sv[0]
-      float mx = -INFINITY;
-      const bool edge = (c0 + 64 > qpos) || (c0 + 64 > S);
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        float x = __uint_as_float(sv[c]) * scale_log2;
-        if (edge && (c0 + c > qpos || c0 + c >= S)) x = -INFINITY;
-        sv[c] = __float_as_uint(x);
-        mx = fmaxf(mx, x);
-      }
-      // row maximum over both halves of the row (both halves have finished
-      // reading this S buffer once past the barrier, so P may overwrite it)
-      red_max[(st * 2 + half) * 128 + row] = mx;
-      named_bar_sync(1 + quarter, 64);
-      mx = fmaxf(mx, red_max[(st * 2 + (half ^ 1)) * 128 + row]);
-      float alpha = 1.f;
-      if (mx > m_run + kRescaleLog2) {
-        alpha = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - mx);
-        m_run = mx;
-      }
-      float sum = 0.f;
-#pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        const float p0 = ex2_approx(__uint_as_float(sv[c]) - m_run);
-        const float p1 = ex2_approx(__uint_as_float(sv[c + 1]) - m_run);
-        sum += p0 + p1;
-        sv[c / 2] = pack_bf16x2(p0, p1);
-      }
-      l_part = l_part * alpha + sum;
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        // O is being accumulated by P_{j-1} V until it completes
-        if (!warp_wait(o_done, (j - 1) & 1, err)) {
+    int jg = 0;
+    for (int idx = blockIdx.x, it = 0; idx < n_items && ok; idx += gridDim.x, ++it) {
+      int mt, h, b;
+      fwd_item(idx, n_qt, nh, B, mt, h, b);
+      const int n_tiles = min(n_qt, mt + 1);
+      const int qpos = mt * BM + row;
+      const int tok0 = b * S;
+      const uint32_t t_o = tmem + lane_base + C::TMEM_O + (it & 1) * D;
+      float m_run = -INFINITY, l_part = 0.f;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int jj = jg + j, st = jj & 1;
+        if (!warp_wait(s_full + 8 * st, (jj >> 1) & 1, err)) {
           ok = false;
           break;
         }
         tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t ov[32];
-          const uint32_t to = tmem + lane_base + C::TMEM_O + half * (D / 2) + c * 32;
-          tmem_ld32(to, ov);
-          tmem_ld_wait();
+        uint32_t sv[64];
+        const uint32_t ts = tmem + lane_base + C::TMEM_S + st * BN;
+        tmem_ld32(ts + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tmem_ld32(ts + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+        tmem_ld_wait();
+        const int c0 = j * BN + half * 64;  // key position of sv[0]
+        float mx = -INFINITY;
+        const bool edge = (c0 + 64 > qpos) || (c0 + 64 > S);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-          tmem_st32(to, ov);
+        for (int c = 0; c < 64; ++c) {
+          float x = __uint_as_float(sv[c]) * scale_log2;
+          if (edge && (c0 + c > qpos || c0 + c >= S)) x = -INFINITY;
+          sv[c] = __float_as_uint(x);
+          mx = fmaxf(mx, x);
         }
+        // row maximum over both halves of the row (both halves have finished
+        // reading this S buffer once past the barrier, so P may overwrite it)
+        red_max[(st * 2 + half) * 128 + row] = mx;
+        named_bar_sync(1 + quarter, 64);
+        mx = fmaxf(mx, red_max[(st * 2 + (half ^ 1)) * 128 + row]);
+        float alpha = 1.f;
+        if (mx > m_run + kRescaleLog2) {
+          alpha = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - mx);
+          m_run = mx;
+        }
+        float sum = 0.f;
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          const float p0 = ex2_approx(__uint_as_float(sv[c]) - m_run);
+          const float p1 = ex2_approx(__uint_as_float(sv[c + 1]) - m_run);
+          sum += p0 + p1;
+          sv[c / 2] = pack_bf16x2(p0, p1);
+        }
+        l_part = l_part * alpha + sum;
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          // O is being accumulated by P_{jj-1} V until it completes
+          if (!warp_wait(o_done, (jj - 1) & 1, err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < D / 64; ++c) {
+            uint32_t ov[32];
+            const uint32_t to = t_o + half * (D / 2) + c * 32;
+            tmem_ld32(to, ov);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tmem_st32(to, ov);
+          }
+        }
+        // P (bf16 pairs) over the first 64 columns of this S buffer: keys
+        // [64 half, 64 half + 64) -> columns [32 half, 32 half + 32)
+        tmem_st32(ts + half * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_full);
       }
-      // P (bf16 pairs) over the first 64 columns of this S buffer: keys
-      // [64 half, 64 half + 64) -> columns [32 half, 32 half + 32)
-      tmem_st32(ts + half * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(p_full);
-    }
-    if (ok && warp_wait(o_done, (n_tiles - 1) & 1, err)) {
+      if (!ok || !warp_wait(o_done, (jg + n_tiles - 1) & 1, err)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       red_sum[half * 128 + row] = l_part;
       named_bar_sync(1 + quarter, 64);
@@ -306,17 +360,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         uint32_t ov[32];
-        tmem_ld32(tmem + lane_base + C::TMEM_O + half * (D / 2) + c * 32, ov);
+        tmem_ld32(t_o + half * (D / 2) + c * 32, ov);
         tmem_ld_wait();
         if (qpos < S) store_row32_bf16(orow + c * 32, ov, inv);
       }
+      // this O buffer is free for item it + 2
+      tc_fence_before();
+      mbar_arrive(o_free + 8 * (it & 1));
       if (half == 0 && qpos < S)
         lse[((int64_t)b * nh + h) * S + qpos] = (m_run + __log2f(l)) * kLn2F;
+      jg += n_tiles;
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if (err && *reinterpret_cast<volatile int*>(err) != 0) {
+    // after a timed-out wait, copies issued just before may still be landing
+    // in this CTA's shared memory: let them finish before it exits
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 200000ull) {
+    }
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
@@ -851,7 +916,9 @@ static cudaError_t fwd_tc_d(const bf16* q, int64_t ldq, const bf16* k, int64_t l
   const int n_qt = (S + 127) / 128;
   const float scale_log2 = kLog2eF / sqrtf((float)D);
   note_launch();
-  attn_fwd_tc_kernel<D><<<n_qt * nh * B, kThreads, FwdCfg<D>::SMEM, s>>>(
+  const int n_items = n_qt * nh * B;
+  const int grid = n_items < num_sms() ? n_items : num_sms();
+  attn_fwd_tc_kernel<D><<<grid, kThreads, FwdCfg<D>::SMEM, s>>>(
       tq, tk, tv, o, lse, B, S, nh, nkv, scale_log2, err);
   return cudaGetLastError();
 }
