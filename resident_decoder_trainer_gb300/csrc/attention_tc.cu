@@ -64,9 +64,10 @@ struct FwdCfg {
   static constexpr uint32_t CHUNK = 128 * 128;  // 64 cols x 128 rows of bf16
   static constexpr uint32_t Q_BYTES = BM * D * 2;
   static constexpr uint32_t KV_BYTES = BN * D * 2;
-  static constexpr uint32_t OFF_Q = 0;                       // [2]
-  static constexpr uint32_t OFF_K = OFF_Q + 2 * Q_BYTES;     // [2]
-  static constexpr uint32_t OFF_V = OFF_K + 2 * KV_BYTES;    // [2]
+  static constexpr int K_STAGES = 3;  // K runs further ahead than V (Q K^T comes first)
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;                // [K_STAGES]
+  static constexpr uint32_t OFF_V = OFF_K + K_STAGES * KV_BYTES;    // [2]
   static constexpr uint32_t OFF_RED = OFF_V + 2 * KV_BYTES;  // float [2][2][128] maxima, [2][128] sums
   static constexpr uint32_t OFF_BAR = OFF_RED + 3 * 2 * 128 * 4;
   static constexpr size_t SMEM = OFF_BAR + 256 + 1024;
@@ -75,6 +76,7 @@ struct FwdCfg {
   // items alternate, so one item's output is read while the next accumulates)
   static constexpr uint32_t TMEM_S = 0, TMEM_O = 256, TMEM_COLS = 512;
   static_assert(TMEM_O + 2 * D <= TMEM_COLS, "two O buffers must fit in TMEM");
+  static_assert(SMEM <= 232448, "attention forward tile exceeds the shared memory of a CTA");
 };
 
 // Rows rescale O only when their running maximum grows by more than 2^8 (in
@@ -94,8 +96,9 @@ __device__ __forceinline__ void fwd_item(int idx, int n_qt, int nh, int B, int& 
 
 // Persistent: each CTA takes work items blockIdx.x, blockIdx.x + gridDim.x,
 // ... Barrier phases run over the CTA's whole sequence of key tiles (jg) and
-// items (it), so the next item's Q and first key tiles are loaded and its
-// first scores computed while this item's output is written.
+// items (it), so the next item's first key tiles are loaded while this
+// item's output is written. K tiles sit in a 3-deep ring whose slots free
+// when their Q K^T completes, V tiles in a 2-deep ring freed by P V.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -109,9 +112,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + C::OFF_BAR;
-  const uint32_t q_full = bar0, q_empty = bar0 + 16, k_full = bar0 + 32, v_full = bar0 + 48,
-                 kv_empty = bar0 + 64, s_full = bar0 + 80, p_full = bar0 + 96,
-                 o_done = bar0 + 104, o_free = bar0 + 112, drain = bar0 + 128;
+  const uint32_t q_full = bar0, q_empty = bar0 + 8, k_full = bar0 + 16, k_empty = bar0 + 40,
+                 v_full = bar0 + 64, v_empty = bar0 + 80, s_full = bar0 + 96,
+                 p_full = bar0 + 112, o_done = bar0 + 120, o_free = bar0 + 128,
+                 drain = bar0 + 144;
+  constexpr int KS = C::K_STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 192);
   float* red_max = reinterpret_cast<float*>(smem + C::OFF_RED);  // [2 parity][2 half][128 rows]
   float* red_sum = red_max + 2 * 2 * 128;                        // [2 half][128 rows]
@@ -122,12 +127,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int grp = nh / nkv;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(q_full + 8 * i, 1);
-      mbar_init(q_empty + 8 * i, 1);
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int i = 0; i < KS; ++i) {
       mbar_init(k_full + 8 * i, 1);
+      mbar_init(k_empty + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(v_full + 8 * i, 1);
-      mbar_init(kv_empty + 8 * i, 1);
+      mbar_init(v_empty + 8 * i, 1);
       mbar_init(s_full + 8 * i, 1);
       mbar_init(o_free + 8 * i, kEltThreads);
     }
@@ -156,32 +164,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         int mt, h, b;
         fwd_item(idx, n_qt, nh, B, mt, h, b);
         const int g = h / grp, tok0 = b * S, n_tiles = min(n_qt, mt + 1);
-        const int qb = it & 1;
-        if (!mbar_wait(q_empty + 8 * qb, ((it >> 1) & 1) ^ 1, err)) {
+        if (!mbar_wait(q_empty, (it & 1) ^ 1, err)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(q_full + 8 * qb, C::Q_BYTES);
+        mbar_arrive_expect_tx(q_full, C::Q_BYTES);
         for (int c = 0; c < DCH; ++c)
-          tma_load_2d(sbase + C::OFF_Q + qb * C::Q_BYTES + c * C::CHUNK, &tq, q_full + 8 * qb,
-                      h * D + c * 64, tok0 + mt * BM);
-        for (int j = 0; j < n_tiles; ++j, ++jg) {
-          const int st = jg & 1;
-          const uint32_t ph = (jg >> 1) & 1;
-          if (!mbar_wait(kv_empty + 8 * st, ph ^ 1, err)) {
-            ok = false;
-            break;
-          }
-          const int n0 = j * BN;
+          tma_load_2d(sbase + C::OFF_Q + c * C::CHUNK, &tq, q_full, h * D + c * 64,
+                      tok0 + mt * BM);
+        // K of tile j + 2 goes out before V of tile j: a K slot frees when its
+        // Q K^T completes, a V slot only when its P V does
+        auto load_k = [&](int j) -> bool {
+          const int jj = jg + j, st = jj % KS;
+          if (!mbar_wait(k_empty + 8 * st, ((jj / KS) & 1) ^ 1, err)) return false;
           mbar_arrive_expect_tx(k_full + 8 * st, C::KV_BYTES);
           for (int c = 0; c < DCH; ++c)
             tma_load_2d(sbase + C::OFF_K + st * C::KV_BYTES + c * C::CHUNK, &tk, k_full + 8 * st,
-                        g * D + c * 64, tok0 + n0);
+                        g * D + c * 64, tok0 + j * BN);
+          return true;
+        };
+        auto load_v = [&](int j) -> bool {
+          const int jj = jg + j, st = jj & 1;
+          if (!mbar_wait(v_empty + 8 * st, ((jj >> 1) & 1) ^ 1, err)) return false;
           mbar_arrive_expect_tx(v_full + 8 * st, C::KV_BYTES);
           for (int c = 0; c < DCH; ++c)
             tma_load_2d(sbase + C::OFF_V + st * C::KV_BYTES + c * C::CHUNK, &tv, v_full + 8 * st,
-                        g * D + c * 64, tok0 + n0);
+                        g * D + c * 64, tok0 + j * BN);
+          return true;
+        };
+        for (int j = 0; j < KS - 1 && j < n_tiles && ok; ++j) ok = load_k(j);
+        for (int j = 0; j < n_tiles && ok; ++j) {
+          if (j + KS - 1 < n_tiles) ok = load_k(j + KS - 1);
+          if (ok) ok = load_v(j);
         }
+        jg += n_tiles;
       }
     }
   } else if (warp == 1) {
@@ -195,14 +211,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         int mt, h, b;
         fwd_item(idx, n_qt, nh, B, mt, h, b);
         const int n_tiles = min(n_qt, mt + 1);
-        const int qb = it & 1;
-        const uint32_t qaddr = sbase + C::OFF_Q + qb * C::Q_BYTES;
+        const int qb = it & 1;  // this item's O buffer
+        const uint32_t qaddr = sbase + C::OFF_Q;
         const uint32_t t_o = tmem + C::TMEM_O + qb * D;
         auto issue_s = [&](int jj) -> bool {
-          const int st = jj & 1;
-          if (!mbar_wait(k_full + 8 * st, (jj >> 1) & 1, err)) return false;
+          const int st = jj & 1, ks = jj % KS;
+          if (!mbar_wait(k_full + 8 * ks, (jj / KS) & 1, err)) return false;
           tc_fence_after();
-          const uint32_t kb = sbase + C::OFF_K + st * C::KV_BYTES;
+          const uint32_t kb = sbase + C::OFF_K + ks * C::KV_BYTES;
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t off = (k >> 2) * C::CHUNK + (k & 3) * 32;
@@ -210,9 +226,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sdesc_sw128(kb + off, 16, 1024), idesc_s, k > 0);
           }
           tc_commit(s_full + 8 * st);
+          tc_commit(k_empty + 8 * ks);
           return true;
         };
-        if (!mbar_wait(q_full + 8 * qb, (it >> 1) & 1, err)) {
+        if (!mbar_wait(q_full, it & 1, err)) {
           ok = false;
           break;
         }
@@ -226,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        if (n_tiles == 1) tc_commit(q_empty + 8 * qb);
+        if (n_tiles == 1) tc_commit(q_empty);
         // this O buffer was read out by item it - 2
         if (!mbar_wait(o_free + 8 * qb, ((it >> 1) & 1) ^ 1, err)) {
           ok = false;
@@ -244,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            if (j + 2 == n_tiles) tc_commit(q_empty + 8 * qb);  // the item's last Q K^T
+            if (j + 2 == n_tiles) tc_commit(q_empty);  // the item's last Q K^T
           }
           if (!mbar_wait(p_full, jj & 1, err) || !mbar_wait(v_full + 8 * st, (jj >> 1) & 1, err)) {
             ok = false;
@@ -258,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_mma_bf16_ts(t_o, tmem + C::TMEM_S + st * BN + k * 8,
                            sdesc_sw128(vb + k * 2048, C::CHUNK, 1024), idesc_o, (j | k) != 0);
           tc_commit(o_done);
-          tc_commit(kv_empty + 8 * st);
+          tc_commit(v_empty + 8 * st);
         }
         jg += n_tiles;
       }
@@ -294,15 +311,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(ts + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
         tmem_ld_wait();
         const int c0 = j * BN + half * 64;  // key position of sv[0]
-        float mx = -INFINITY;
+        // the row maximum of the raw scores (the scale is positive, so it
+        // commutes with the maximum), in four independent chains
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         const bool edge = (c0 + 64 > qpos) || (c0 + 64 > S);
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
-          float x = __uint_as_float(sv[c]) * scale_log2;
-          if (edge && (c0 + c > qpos || c0 + c >= S)) x = -INFINITY;
-          sv[c] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
+          if (edge && (c0 + c > qpos || c0 + c >= S)) sv[c] = __float_as_uint(-INFINITY);
+          m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sv[c]));
         }
+        float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * scale_log2;
         // row maximum over both halves of the row (both halves have finished
         // reading this S buffer once past the barrier, so P may overwrite it)
         red_max[(st * 2 + half) * 128 + row] = mx;
@@ -314,10 +332,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_run = mx;
         }
         float sum = 0.f;
+        // p = 2^(s scale - m): one FMA per score (masked scores are -inf;
+        // m is finite, every row has an unmasked key in its first tile)
+        const float nm = -m_run;
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
-          const float p0 = ex2_approx(__uint_as_float(sv[c]) - m_run);
-          const float p1 = ex2_approx(__uint_as_float(sv[c + 1]) - m_run);
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sv[c]), scale_log2, nm));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sv[c + 1]), scale_log2, nm));
           sum += p0 + p1;
           sv[c / 2] = pack_bf16x2(p0, p1);
         }
