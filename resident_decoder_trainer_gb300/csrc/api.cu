@@ -161,7 +161,11 @@ struct BlockWs {
   bf16 *dy_b, *dgu, *dr1_b, *dout, *dqkv;
   float *dxn, *dr1, *Dd, *lse2, *dq, *dk, *partials;
   double* sqp;  // squared-sum slots of the weight-gradient GEMMs
+  float* split;  // split-K partials of the [T, hidden] projections
+  int64_t split_floats;
 };
+// fp32 scratch for four K-slices of a [T, H] GEMM output on 256-row tiles
+inline int64_t split_floats_for(int64_t T, int64_t H) { return 4 * ((T + 255) / 256 * 256) * H; }
 size_t carve_block_ws(const Dims& m, int64_t B, int64_t S, void* base, BlockWs* w) {
   const int64_t T = B * S;
   Carver c(base);
@@ -184,6 +188,8 @@ size_t carve_block_ws(const Dims& m, int64_t B, int64_t S, void* base, BlockWs* 
                          gemm_sq_slots_bound((int)(2 * m.I), (int)m.H) +
                          gemm_sq_slots_bound((int)m.H, (int)m.qd) +
                          gemm_sq_slots_bound((int)m.nqkv, (int)m.H));
+  t.split_floats = split_floats_for(T, m.H);
+  t.split = c.take<float>(t.split_floats);
   if (w) *w = t;
   return c.off;
 }
@@ -193,6 +199,8 @@ struct HeadWs {
   float *rstd, *tgt, *lse, *dhn, *partials;
   float2* part;
   double* sqp;  // squared-sum slots of the dW_lm GEMM
+  float* split;  // split-K partials of dh_n
+  int64_t split_floats;
 };
 size_t carve_head_ws(const Dims& m, int64_t T, void* base, HeadWs* w) {
   Carver c(base);
@@ -206,6 +214,8 @@ size_t carve_head_ws(const Dims& m, int64_t T, void* base, HeadWs* w) {
   t.dhn = c.take<float>(T * m.H);
   t.partials = c.take<float>(kMaxPartialRows * m.H);
   t.sqp = c.take<double>(gemm_sq_slots_bound((int)m.V, (int)m.H));
+  t.split_floats = split_floats_for(T, m.H);
+  t.split = c.take<float>(t.split_floats);
   if (w) *w = t;
   return c.off;
 }
@@ -548,6 +558,8 @@ rdt_status rdt_block_forward(const rdt_config* cfg, int32_t batch, int32_t seq, 
     e.ld_out = m.H;
     e.resid = x;
     e.ld_resid = m.H;
+    e.split_ws = wk.split;
+    e.split_ws_floats = wk.split_floats;
     RDT_GEMM(Mat{sv.o, T, m.qd, m.qd}, false, Mat{wb + off[RDT_WO], m.H, m.qd, m.qd}, false, T,
              (int)m.H, (int)m.qd, e, err, s);
   }
@@ -574,6 +586,8 @@ rdt_status rdt_block_forward(const rdt_config* cfg, int32_t batch, int32_t seq, 
     e.ld_out = m.H;
     e.resid = sv.r1;
     e.ld_resid = m.H;
+    e.split_ws = wk.split;
+    e.split_ws_floats = wk.split_floats;
     RDT_GEMM(Mat{sv.s, T, m.I, m.I}, false, Mat{wb + off[RDT_WD], m.H, m.I, m.I}, false, T,
              (int)m.H, (int)m.I, e, err, s);
   }
@@ -656,6 +670,8 @@ rdt_status rdt_block_backward(const rdt_config* cfg, int32_t batch, int32_t seq,
     e.kind = EPI_F32;
     e.out = wk.dxn;
     e.ld_out = m.H;
+    e.split_ws = wk.split;
+    e.split_ws_floats = wk.split_floats;
     RDT_GEMM(Mat{wk.dgu, T, 2 * m.I, 2 * m.I}, false, Mat{wb + off[RDT_WG], 2 * m.I, m.H, m.H},
              true, T, (int)m.H, (int)(2 * m.I), e, err, s);
   }
@@ -726,6 +742,8 @@ rdt_status rdt_block_backward(const rdt_config* cfg, int32_t batch, int32_t seq,
     e.kind = EPI_F32;
     e.out = wk.dxn;
     e.ld_out = m.H;
+    e.split_ws = wk.split;
+    e.split_ws_floats = wk.split_floats;
     RDT_GEMM(Mat{wk.dqkv, T, m.nqkv, m.nqkv}, false, Mat{wb + off[RDT_WQ], m.nqkv, m.H, m.H}, true,
              T, (int)m.H, (int)m.nqkv, e, err, s);
   }
@@ -800,6 +818,8 @@ rdt_status rdt_fused_cross_entropy(const rdt_config* cfg, int32_t tokens, const 
     e.kind = EPI_F32;
     e.out = wk.dhn;
     e.ld_out = m.H;
+    e.split_ws = wk.split;
+    e.split_ws_floats = wk.split_floats;
     RDT_GEMM(Mat{wk.z, T, m.V, m.V}, false, Mat{wl, m.V, m.H, m.H}, true, T, (int)m.H, (int)m.V,
              e, err, s);
   }

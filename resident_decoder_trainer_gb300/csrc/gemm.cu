@@ -1363,6 +1363,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const uint32_t tempty_even = mapa_shared(tempty0, 0);
 
   const int ntiles = p.m_tiles * p.n_tiles;  // m_tiles counts 256-row pair tiles
+  const int nunits = ntiles * p.splits;       // tiles x K-slices
   const uint32_t smem_base = smem_u32(smem);
 
   if (warp == 0) {
@@ -1371,11 +1372,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       int stage = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int t = pair; t < ntiles && ok; t += npairs) {
+      for (int u = pair; u < nunits && ok; u += npairs) {
         int mt, nt;
-        tile_coords(t, p, mt, nt);
+        tile_coords(u % ntiles, p, mt, nt);
         const int m0 = (2 * mt + static_cast<int>(rank)) * BM;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        const int kb0 = (u / ntiles) * p.kb_split;
+        const int kb1 = min(p.k_blocks, kb0 + p.kb_split);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, ph ^ 1, p.err)) {
             ok = false;
             break;
@@ -1421,14 +1424,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       int acc = 0;
       uint32_t acc_ph = 0;
       bool ok = true;
-      for (int t = pair; t < ntiles && ok; t += npairs) {
+      for (int u = pair; u < nunits && ok; u += npairs) {
         if (!mbar_wait_cluster(tempty0 + 8 * acc, acc_ph ^ 1, p.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        const int kb0 = (u / ntiles) * p.kb_split;
+        const int kb1 = min(p.k_blocks, kb0 + p.kb_split);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(full0 + 8 * stage, ph, p.err)) {
             ok = false;
             break;
@@ -1442,7 +1447,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t ad = ad0 + static_cast<uint64_t>(k) * ((A_MN ? 2048 : 32) >> 4);
             const uint64_t bd = bd0 + static_cast<uint64_t>(k) * ((B_MN ? 2048 : 32) >> 4);
-            tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
+            tc_mma_bf16_pair(d_tmem, ad, bd, idesc, kb != kb0 || k != 0);
           }
           tc_commit_pair_mc(empty0 + 8 * stage, 0x3);
           if (++stage == STAGES) {
@@ -1468,12 +1473,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     uint32_t ucnt = 0, eph = 0;
     int acc = 0;
     uint32_t acc_ph = 0;
-    for (int t = pair; t < ntiles; t += npairs) {
+    for (int u = pair; u < nunits; u += npairs) {
       int mt, nt;
+      const int t = u % ntiles;
       tile_coords(t, p, mt, nt);
       const int mrow = 2 * mt + static_cast<int>(rank);
+      const int row0 = (u / ntiles) * p.m_pad + mrow * BM + q * 32;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      if (!epilogue_tile<EPI, BN, OS::BYTES>(p, om, tbase, mrow * BM + q * 32, nt, half, st,
+      if (!epilogue_tile<EPI, BN, OS::BYTES>(p, om, tbase, row0, nt, half, st,
                                              ucnt, eph, tfull0 + 8 * acc, acc_ph, t,
                                              static_cast<int>(rank) * 8 + (warp - 2)))
         break;
@@ -1630,8 +1637,8 @@ static cudaError_t launch2(const CUtensorMap& ta, const CUtensorMap& tb, const O
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  const int ntiles = p.m_tiles * p.n_tiles;
-  const int pairs = ntiles < max_pairs ? ntiles : max_pairs;
+  const int nunits = p.m_tiles * p.n_tiles * p.splits;
+  const int pairs = nunits < max_pairs ? nunits : max_pairs;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs, 1, 1);
   cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
@@ -1845,6 +1852,57 @@ static cudaError_t gemm_splitk(const Mat& A, bool a_mn, const Mat& B, bool b_mn,
   return splitk_reduce(epi, splits, m_pad, ldw, M, N, s);
 }
 
+// C = A' B'^T as `splits` K-slices on CTA-pair 256 x 256 tiles whose fp32
+// partials go to epi.split_ws, then splitk_reduce_kernel.
+static cudaError_t gemm_splitk_pair(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N,
+                                    int K, int splits, int pairs_max, const Epi& epi, int* err,
+                                    cudaStream_t s, const char** why) {
+  const int kbs = (K + BK - 1) / BK;
+  const int kb_split = (kbs + splits - 1) / splits;
+  splits = (kbs + kb_split - 1) / kb_split;  // no empty slice
+  const int m_tiles = (M + 2 * BM - 1) / (2 * BM);
+  const int64_t m_pad = static_cast<int64_t>(m_tiles) * 2 * BM;
+  const int64_t ldw = (N + 3) / 4 * 4;
+  Epi pe;
+  pe.kind = EPI_F32;
+  pe.out = epi.split_ws;
+  pe.ld_out = ldw;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, A, a_mn ? 64 : 128) || !make_map(&tb, B, b_mn ? 64 : 128)) {
+    *why = "gemm: cuTensorMapEncodeTiled failed";
+    return cudaErrorInvalidValue;
+  }
+  OutMaps om;
+  if (!make_out_maps(&om, pe, static_cast<int>(splits * m_pad), N, OutStageBytes(256))) {
+    *why = "gemm: split-K scratch needs 16-byte alignment";
+    return cudaErrorInvalidValue;
+  }
+  GemmParams p;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.m_tiles = m_tiles;
+  p.n_tiles = (N + 255) / 256;
+  p.k_blocks = kbs;
+  p.swiglu_half = 0;
+  p.group = raster_group(p.m_tiles, p.n_tiles, 2 * BM, 256, K);
+  p.sq_slots = 16;
+  p.kb_main = kbs;
+  p.splits = splits;
+  p.kb_split = kb_split;
+  p.m_pad = static_cast<int>(m_pad);
+  p.m_epi = static_cast<int>(splits * m_pad);
+  p.epi = pe;
+  p.err = err;
+  cudaError_t e = cudaErrorInvalidValue;
+  if (!a_mn && !b_mn) e = launch2<0, 0, EPI_F32, 256>(ta, tb, om, p, pairs_max, s);
+  else if (!a_mn && b_mn) e = launch2<0, 1, EPI_F32, 256>(ta, tb, om, p, pairs_max, s);
+  else if (a_mn && b_mn) e = launch2<1, 1, EPI_F32, 256>(ta, tb, om, p, pairs_max, s);
+  else *why = "gemm: unsupported operand-major combination for split-K";
+  if (e != cudaSuccess) return e;
+  return splitk_reduce(epi, splits, m_pad, ldw, M, N, s);
+}
+
 cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N, int K,
                  const Epi& epi, int* err, cudaStream_t s, const char** why) {
   if (M <= 0 || N <= 0 || K <= 0) {
@@ -1902,6 +1960,33 @@ cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N,
     while (splits > 1 && splits * m_pad * ldw > epi.split_ws_floats) --splits;
     if (splits >= 2)
       return gemm_splitk(A, a_mn, B, b_mn, M, N, K, static_cast<int>(splits), epi, err, s, why);
+  }
+  // K-slices for CTA-pair tiles that would leave much of a wave idle (the
+  // N = 2560 outputs of a 4096-token step: 160 tiles on 76 pairs): estimated
+  // time = rounds of work units x one slice's share of a pair-tile (about
+  // 1.6 PFLOP/s over the pairs) + the partials' round trip through memory.
+  if (pair_tiles && epi.split_ws && (epi.kind == EPI_F32 || epi.kind == EPI_F32_RESID)) {
+    const int64_t tiles = static_cast<int64_t>((M + 2 * BM - 1) / (2 * BM)) * ((N + 255) / 256);
+    const int64_t m_pad = static_cast<int64_t>((M + 2 * BM - 1) / (2 * BM)) * 2 * BM;
+    const int64_t ldw = (N + 3) / 4 * 4;
+    const int kbs = (K + BK - 1) / BK;
+    const double tile_us = 2.0 * 256 * 256 * K * pairs_max / 1.6e15 * 1e6;
+    auto cost = [&](int sl) {
+      double c = static_cast<double>((tiles * sl + pairs_max - 1) / pairs_max) * tile_us / sl;
+      if (sl > 1) c += (sl + 2) * static_cast<double>(M) * N * 4 / 5.0e12 * 1e6 + 3.0;
+      return c;
+    };
+    int bs = 1;
+    double bc = cost(1);
+    for (int sl = 2; sl <= 4; ++sl) {
+      if (sl * m_pad * ldw > epi.split_ws_floats || kbs < 4 * sl) break;
+      if (cost(sl) < 0.97 * bc) {
+        bc = cost(sl);
+        bs = sl;
+      }
+    }
+    if (bs > 1)
+      return gemm_splitk_pair(A, a_mn, B, b_mn, M, N, K, bs, pairs_max, epi, err, s, why);
   }
   CUtensorMap ta, tb;
   const int b_box = (pair_tiles && !b_mn) ? bn / 2 : 64;

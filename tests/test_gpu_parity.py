@@ -93,6 +93,29 @@ def test_split_k_gemm_matches_fp64(M, N, K, a_mn, b_mn):
     assert torch.equal(outs[0][:, :N], outs[1][:, :N])
 
 
+@pytest.mark.parametrize("b_mn", [0, 1])
+def test_pair_split_k_gemm_matches_fp64(b_mn):
+    """A 2048 x 2560 output (80 CTA-pair tiles on 76 pairs) over K = 8192
+    runs as K-slices on the pair kernel; same values as the fp64 product,
+    nothing written past N, bit-identical on a second run."""
+    M, N, K = 2048, 2560, 8192
+    g = torch.Generator(device="cpu").manual_seed(17 + b_mn)
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    Bm = torch.randn(N, K, generator=g).to(torch.bfloat16)
+    ref = A.double() @ Bm.double().T
+    b = (Bm.T.contiguous() if b_mn else Bm).cuda()
+    ws = torch.empty(4 * M * N, device="cuda")
+    outs = []
+    for _ in range(2):
+        c = torch.full((M, N + 4), float("nan"), device="cuda")
+        rdt.gemm(A.cuda(), 0, b, b_mn, M, N, K, c, split_ws=ws)
+        torch.cuda.synchronize()
+        outs.append(c)
+    assert rel_l2(outs[0][:, :N].double().cpu().numpy(), ref.numpy()) < 1e-5
+    assert torch.isnan(outs[0][:, N:]).all()
+    assert torch.equal(outs[0][:, :N], outs[1][:, :N])
+
+
 # ------------------------------------------------------------------ block
 def _block_case(shape, seed=0):
     blk, x, dy = synth.make_block_inputs(shape, seed)
