@@ -72,6 +72,9 @@ def parse_args():
     ap.add_argument("--embedding", action="store_true",
                     help="device embedding: the step takes token ids (lookup, scatter-add "
                          "backward and the table's AdamW on the GPU)")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch the step's kernels one by one instead of replaying the "
+                         "captured CUDA graph of the step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -250,21 +253,44 @@ def run_rdt(args, rank, world, local_rank):
         torch.cuda.synchronize()
 
     first_loss = float(tr.train_step(targets=tgs[0], **{kw: xs[0]}).mean())
-    for i in range(1, args.warmup):
-        tr.train_step(targets=tgs[i % nb], **{kw: xs[i % nb]})
     gemms_per_step = (17 * shape.layers + 3) * n_acc  # 12 per layer, 5 more when recomputed
-    timer = rdt.GemmTimer(gemms_per_step * args.steps)
+    use_graph = not args.no_graph
+    if use_graph:
+        # capture the step once (the first call captures, then replays)
+        lc0 = rdt.launch_count()
+        tr.train_step_graph(targets=tgs[1 % nb], **{kw: xs[1 % nb]})
+        launches_per_step = rdt.launch_count() - lc0
+        step_fn, first_warm = tr.train_step_graph, 2
+    else:
+        timer = rdt.GemmTimer(gemms_per_step * args.steps)
+        step_fn, first_warm = tr.train_step, 1
+    for i in range(first_warm, args.warmup):
+        step_fn(targets=tgs[i % nb], **{kw: xs[i % nb]})
     barrier()
     clk = start_clock_sampler(local_rank)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     l0 = rdt.launch_count()
-    with timer:
+    if use_graph:
         e0.record(stream)
         for i in range(args.steps):
-            tr.train_step(targets=tgs[i % nb], **{kw: xs[i % nb]})
+            step_fn(targets=tgs[i % nb], **{kw: xs[i % nb]})
         e1.record(stream)
         barrier()
-    launches = rdt.launch_count() - l0
+        launches = launches_per_step * args.steps
+        # per-GEMM durations: events recorded inside a graph cannot be timed,
+        # so the same step runs once more with its kernels launched one by one
+        timer = rdt.GemmTimer(gemms_per_step)
+        with timer:
+            tr.train_step(targets=tgs[0], **{kw: xs[0]})
+        torch.cuda.synchronize()
+    else:
+        with timer:
+            e0.record(stream)
+            for i in range(args.steps):
+                step_fn(targets=tgs[i % nb], **{kw: xs[i % nb]})
+            e1.record(stream)
+            barrier()
+        launches = rdt.launch_count() - l0
     clocks = stop_clock_sampler(clk)
     dev_ms = e0.elapsed_time(e1)
     last_loss = float(tr.loss_partials.mean())
@@ -292,7 +318,8 @@ def run_rdt(args, rank, world, local_rank):
         "launches_timed": n_launch,
         "flops_per_launch": gemm_flops / max(n_launch, 1),
         "ms_per_launch": gemm_ms / max(n_launch, 1),
-        "gemm_share_of_step": round(gemm_ms / max_ms, 4) if max_ms else None,
+        "gemm_share_of_step": round(gemm_ms / (max_ms * (1 if use_graph else args.steps)
+                                               / args.steps), 4) if max_ms else None,
     }
     step_flops = algorithmic_flops(shape) * n_acc
     out = {
@@ -307,6 +334,7 @@ def run_rdt(args, rank, world, local_rank):
         "gpu_launches": int(launches),
         "clocks": clocks,
         "loss_first_step": round(first_loss, 5), "loss_last_step": round(last_loss, 5),
+        "launch": "one CUDA graph replay per step" if use_graph else "eager kernel launches",
     }
     out["config"]["params"] = tr.n_params
     out["config"]["algorithmic_tflop_per_step"] = round(step_flops / 1e12, 2)
@@ -352,7 +380,8 @@ def run_e2e(tr, shape, args, dev, world):
     for _ in range(args.steps):
         xd.copy_(xh, non_blocking=True)
         td.copy_(th, non_blocking=True)
-        loss = tr.train_step(targets=td, **{kw: xd})
+        loss = (tr.train_step if args.no_graph else tr.train_step_graph)(targets=td,
+                                                                          **{kw: xd})
         lh.copy_(loss, non_blocking=True)
     torch.cuda.synchronize()
     dt = time.perf_counter() - t0

@@ -224,12 +224,18 @@ rdt_status rdt_sq_sum_noalloc(const float* const* bufs, const int64_t* lens, int
  * scale     device fp32 scalar from rdt_clip_scale, or NULL for 1
  * skip_flag device int32, or NULL; when *skip_flag != 0 nothing is written
  * w_bf16    if not NULL, receives the bf16 (RNE) copy of the updated w
- * w, g, m, v, w_bf16 16-byte aligned. step >= 1.
+ * step_dev  if not NULL, a device int32 holding the step (>= 1) that the
+ *           kernel reads instead of `step` (which is then ignored): a step
+ *           count that lives on the device, so a captured CUDA graph of the
+ *           training step can be replayed unchanged (see rdt_step_advance)
+ * w, g, m, v, w_bf16 16-byte aligned. step >= 1 unless step_dev is given.
+ * rdt_step_advance: *step += 1 on the device, in stream order.
  * ------------------------------------------------------------------------- */
 rdt_status rdt_adamw_step(float* w, const float* g, float* m, float* v, int64_t n,
                           const float* scale, const int32_t* skip_flag, int32_t step,
-                          float lr, float beta1, float beta2, float eps, float weight_decay,
-                          rdt_bf16* w_bf16, void* stream);
+                          const int32_t* step_dev, float lr, float beta1, float beta2,
+                          float eps, float weight_decay, rdt_bf16* w_bf16, void* stream);
+rdt_status rdt_step_advance(int32_t* step, void* stream);
 
 /* The tensor-core GEMM every projection of the path runs on, exposed so it
  * can be tested on its own: C[M, N] (fp32, row stride ldc) = A' B'^T over K,

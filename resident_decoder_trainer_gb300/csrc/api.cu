@@ -877,12 +877,13 @@ rdt_status rdt_clip_scale(const double* sumsq, float max_norm, float* scale, int
 }
 
 rdt_status rdt_adamw_step(float* w, const float* g, float* m, float* v, int64_t n,
-                          const float* scale, const int32_t* skip_flag, int32_t step, float lr,
-                          float beta1, float beta2, float eps, float weight_decay,
-                          rdt_bf16* w_bf16, void* stream) {
+                          const float* scale, const int32_t* skip_flag, int32_t step,
+                          const int32_t* step_dev, float lr, float beta1, float beta2, float eps,
+                          float weight_decay, rdt_bf16* w_bf16, void* stream) {
   if (!w || !g || !m || !v) return fail(RDT_EINVAL, "null pointer");
   if (n < 0) return fail(RDT_EINVAL, "n must be >= 0");
-  if (step < 1) return fail(RDT_EINVAL, "step must be >= 1 (bias correction)");
+  if (!step_dev && step < 1) return fail(RDT_EINVAL, "step must be >= 1 (bias correction)");
+  if (step < 1) step = 1;  // ignored: the kernel reads *step_dev
   if (!aligned16(w) || !aligned16(g) || !aligned16(m) || !aligned16(v) ||
       (w_bf16 && !aligned16(w_bf16)))
     return fail(RDT_EINVAL, "buffers must be 16-byte aligned");
@@ -891,7 +892,14 @@ rdt_status rdt_adamw_step(float* w, const float* g, float* m, float* v, int64_t 
   const double bc2 = 1.0 - std::pow(static_cast<double>(beta2), step);
   RDT_CHECK_CUDA(adamw(w, g, m, v, n, scale, skip_flag, lr, beta1, beta2, eps, weight_decay,
                        static_cast<float>(bc1), static_cast<float>(bc2),
-                       reinterpret_cast<bf16*>(w_bf16), static_cast<cudaStream_t>(stream)));
+                       reinterpret_cast<bf16*>(w_bf16), static_cast<cudaStream_t>(stream),
+                       step_dev));
+  return RDT_OK;
+}
+
+rdt_status rdt_step_advance(int32_t* step, void* stream) {
+  if (!step) return fail(RDT_EINVAL, "null pointer");
+  RDT_CHECK_CUDA(step_advance(step, static_cast<cudaStream_t>(stream)));
   return RDT_OK;
 }
 

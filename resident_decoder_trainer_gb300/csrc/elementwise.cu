@@ -747,6 +747,21 @@ cudaError_t clip_scale(const double* sumsq, float max_norm, float* scale, int32_
 }
 
 // -------------------------------------------------------------------- AdamW
+// 1 - b^step in double, rounded to float (as the host does for a host step).
+__device__ __forceinline__ void bias_corrections(int step, float b1, float b2, float& bc1,
+                                                 float& bc2) {
+  bc1 = static_cast<float>(1.0 - pow(static_cast<double>(b1), static_cast<double>(step)));
+  bc2 = static_cast<float>(1.0 - pow(static_cast<double>(b2), static_cast<double>(step)));
+}
+
+__global__ void step_advance_kernel(int32_t* step) { *step += 1; }
+
+cudaError_t step_advance(int32_t* step, cudaStream_t s) {
+  note_launch();
+  step_advance_kernel<<<1, 1, 0, s>>>(step);
+  return cudaGetLastError();
+}
+
 __device__ __forceinline__ float adamw_one(float& w, float g, float& m, float& v, float sc,
                                            float lr, float b1, float b2, float eps, float wd,
                                            float bc1, float bc2) {
@@ -765,9 +780,11 @@ __global__ void __launch_bounds__(256) adamw_kernel(float4* __restrict__ w,
                                                     int64_t n4, const float* __restrict__ scale,
                                                     const int32_t* __restrict__ skip, float lr,
                                                     float b1, float b2, float eps, float wd,
-                                                    float bc1, float bc2, uint2* __restrict__ wb) {
+                                                    float bc1, float bc2, uint2* __restrict__ wb,
+                                                    const int32_t* __restrict__ step_dev) {
   if (skip && *skip) return;
   const float sc = scale ? *scale : 1.0f;
+  if (step_dev) bias_corrections(*step_dev, b1, b2, bc1, bc2);
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
        i += (int64_t)gridDim.x * blockDim.x) {
     float4 wv = w[i], mv = m[i], vv = v[i];
@@ -787,11 +804,13 @@ __global__ void adamw_tail_kernel(float* __restrict__ w, const float* __restrict
                                   float* __restrict__ m, float* __restrict__ v, int64_t start,
                                   int64_t n, const float* __restrict__ scale,
                                   const int32_t* __restrict__ skip, float lr, float b1, float b2,
-                                  float eps, float wd, float bc1, float bc2, bf16* __restrict__ wb) {
+                                  float eps, float wd, float bc1, float bc2, bf16* __restrict__ wb,
+                                  const int32_t* __restrict__ step_dev) {
   if (skip && *skip) return;
   const int64_t i = start + threadIdx.x;
   if (i >= n) return;
   const float sc = scale ? *scale : 1.0f;
+  if (step_dev) bias_corrections(*step_dev, b1, b2, bc1, bc2);
   float wv = w[i], mv = m[i], vv = v[i];
   adamw_one(wv, g[i], mv, vv, sc, lr, b1, b2, eps, wd, bc1, bc2);
   w[i] = wv;
@@ -802,7 +821,7 @@ __global__ void adamw_tail_kernel(float* __restrict__ w, const float* __restrict
 
 cudaError_t adamw(float* w, const float* g, float* m, float* v, int64_t n, const float* scale,
                   const int32_t* skip, float lr, float b1, float b2, float eps, float wd,
-                  float bc1, float bc2, bf16* wb, cudaStream_t s) {
+                  float bc1, float bc2, bf16* wb, cudaStream_t s, const int32_t* step_dev) {
   const int64_t n4 = n / 4;
   if (n4 > 0) {
     int64_t blocks = (n4 + 255) / 256;
@@ -812,12 +831,12 @@ cudaError_t adamw(float* w, const float* g, float* m, float* v, int64_t n, const
     adamw_kernel<<<(unsigned)blocks, 256, 0, s>>>(
         reinterpret_cast<float4*>(w), reinterpret_cast<const float4*>(g),
         reinterpret_cast<float4*>(m), reinterpret_cast<float4*>(v), n4, scale, skip, lr, b1, b2,
-        eps, wd, bc1, bc2, reinterpret_cast<uint2*>(wb));
+        eps, wd, bc1, bc2, reinterpret_cast<uint2*>(wb), step_dev);
   }
   if (n % 4) {
     note_launch();
     adamw_tail_kernel<<<1, 32, 0, s>>>(w, g, m, v, n4 * 4, n, scale, skip, lr, b1, b2, eps, wd,
-                                       bc1, bc2, wb);
+                                       bc1, bc2, wb, step_dev);
   }
   return cudaGetLastError();
 }

@@ -170,7 +170,11 @@ cudaError_t clip_scale(const double* sumsq, float max_norm, float* scale, int32_
                        cudaStream_t s);
 cudaError_t adamw(float* w, const float* g, float* m, float* v, int64_t n, const float* scale,
                   const int32_t* skip, float lr, float b1, float b2, float eps, float wd,
-                  float bc1, float bc2, bf16* wb, cudaStream_t s);
+                  float bc1, float bc2, bf16* wb, cudaStream_t s,
+                  const int32_t* step_dev = nullptr);
+// *step += 1 on the device (the optimizer's step count, read by adamw when
+// its step lives on the device, e.g. under graph replay).
+cudaError_t step_advance(int32_t* step, cudaStream_t s);
 
 // ---------------------------------------------------------------- attention
 // mma.sync flash attention (attention.cu) for head_dim 16 and 32.

@@ -32,7 +32,7 @@ EXPORTS = (
     "rdt_nf4_scale_count", "rdt_nf4_offsets", "rdt_lora_param_count", "rdt_lora_param_offsets",
     "rdt_lora_shadow_count", "rdt_lora_shadow", "rdt_nf4_saved_bytes", "rdt_nf4_workspace_bytes",
     "rdt_nf4_block_forward", "rdt_nf4_block_backward", "rdt_embedding_workspace_bytes",
-    "rdt_embedding_forward", "rdt_embedding_backward",
+    "rdt_embedding_forward", "rdt_embedding_backward", "rdt_step_advance",
 )
 
 
@@ -76,7 +76,8 @@ def _load() -> ctypes.CDLL:
                                           P]),
         "rdt_sq_sum": (I32, [P, P, I32, P, P, SZ, P]),
         "rdt_clip_scale": (I32, [P, F32, P, P, P]),
-        "rdt_adamw_step": (I32, [P, P, P, P, I64, P, P, I32, F32, F32, F32, F32, F32, P, P]),
+        "rdt_adamw_step": (I32, [P, P, P, P, I64, P, P, I32, P, F32, F32, F32, F32, F32, P, P]),
+        "rdt_step_advance": (I32, [P, P]),
         "rdt_gemm": (I32, [P, I32, I64, P, I32, I64, I32, I32, I32, P, I64, P, I64, P]),
         "rdt_gemm_nf4": (I32, [P, I64, P, P, I64, I64, I32, P, I64, P, I64, I32, I32, P, I64, P, I64,
                                P]),
@@ -229,11 +230,18 @@ def clip_scale(sumsq, max_norm, scale, nonfinite=None, stream=None):
 
 
 def adamw_step(w, g, m, v, step, lr, beta1, beta2, eps, weight_decay, scale=None, skip=None,
-               w_bf16=None, n=None, stream=None):
+               w_bf16=None, n=None, step_dev=None, stream=None):
+    """step: host int (>= 1), or None with step_dev: a device int32 holding it."""
     n = w.numel() if n is None else n
     _check(lib().rdt_adamw_step(_ptr(w), _ptr(g), _ptr(m), _ptr(v), n, _ptr(scale), _ptr(skip),
-                                int(step), float(lr), float(beta1), float(beta2), float(eps),
-                                float(weight_decay), _ptr(w_bf16), _stream(stream)))
+                                int(step or 0), _ptr(step_dev), float(lr), float(beta1),
+                                float(beta2), float(eps), float(weight_decay), _ptr(w_bf16),
+                                _stream(stream)))
+
+
+def step_advance(step_dev, stream=None):
+    """step_dev (device int32) += 1."""
+    _check(lib().rdt_step_advance(_ptr(step_dev), _stream(stream)))
 
 
 def gemm(a, a_mn, b, b_mn, M, N, K, c, split_ws=None, stream=None):

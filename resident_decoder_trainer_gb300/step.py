@@ -35,7 +35,13 @@ Device embedding (``embedding=True``; cuda_trainer.rs ``gpu_forward`` lookup and
 step takes token ids; x = E[ids] by a gather kernel; the activation gradient
 leaving the first block is clipped by its own norm and scatter-added into the
 table's gradient (deterministically, in token order); the table has its own
-AdamW, outside the global clip. The loss partials stay on the device until the
+AdamW, outside the global clip.
+
+CUDA graph (``train_step_graph``): the whole step (every micro-batch, the clip
+and AdamW) is captured once into one graph that reads its inputs from the
+trainer's staging buffers and is replayed each step; the optimizer's step
+count lives on the device (``rdt_step_advance``), so the replayed graph needs
+no host-side update. The loss partials stay on the device until the
 caller reads them. Every launch is a librdt kernel; torch is used only to
 allocate buffers and for the stream.
 """
@@ -92,6 +98,8 @@ class DecoderTrainer:
         self.sumsq = torch.zeros(1, dtype=torch.float64, device=dev)
         self.scale = torch.ones(1, **f32)
         self.nonfinite = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.step_dev = torch.zeros(1, dtype=torch.int32, device=dev)  # AdamW's step count
+        self.graph = None
         self.loss_partials = torch.zeros(n_acc * T, **f32)
         self.targets = torch.zeros(T, dtype=torch.int32, device=dev)
         self.embedding = bool(embedding)
@@ -171,6 +179,7 @@ class DecoderTrainer:
     def reset_optimizer(self):
         self.m.zero_()
         self.v.zero_()
+        self.step_dev.zero_()
         if self.embedding:
             self.emb_m.zero_()
             self.emb_v.zero_()
@@ -238,13 +247,14 @@ class DecoderTrainer:
         o = self.optim
         rdt.clip_scale(self.sumsq, o["max_norm"], self.scale, self.nonfinite)
         self.step_count += 1
-        rdt.adamw_step(self.w, self.g, self.m, self.v, self.step_count, o["lr"], o["beta1"],
-                       o["beta2"], o["eps"], o["weight_decay"], scale=self.scale,
-                       skip=self.nonfinite, w_bf16=self.wb)
+        rdt.step_advance(self.step_dev)
+        rdt.adamw_step(self.w, self.g, self.m, self.v, None, o["lr"], o["beta1"], o["beta2"],
+                       o["eps"], o["weight_decay"], scale=self.scale, skip=self.nonfinite,
+                       w_bf16=self.wb, step_dev=self.step_dev)
         if self.embedding:
-            rdt.adamw_step(self.emb, self.emb_g, self.emb_m, self.emb_v, self.step_count,
-                           o["lr"], o["beta1"], o["beta2"], o["eps"], o["weight_decay"],
-                           skip=self.emb_nonfinite)
+            rdt.adamw_step(self.emb, self.emb_g, self.emb_m, self.emb_v, None, o["lr"],
+                           o["beta1"], o["beta2"], o["eps"], o["weight_decay"],
+                           skip=self.emb_nonfinite, step_dev=self.step_dev)
 
     def train_step(self, x=None, targets=None, ids=None):
         """One full step; returns the device tensor of per-token loss partials.
@@ -258,5 +268,39 @@ class DecoderTrainer:
 
         for i in range(n):
             self.forward_backward(part(x, i), part(targets, i), micro=i, ids=part(ids, i))
+        self.clip_and_update()
+        return self.loss_partials
+
+    # --------------------------------------------------------- CUDA graph
+    def train_step_graph(self, x=None, targets=None, ids=None):
+        """train_step as one CUDA graph replay. The inputs (as for train_step)
+        are copied into staging buffers first; the graph is captured on the
+        first call, which must follow at least one eager train_step (the
+        library's one-time set-up runs there, outside any capture)."""
+        n, T = self.accumulation_steps, self.shape.tokens
+        if self.graph is None:
+            self.tg_stage = torch.zeros(n * T, dtype=torch.int32, device=self.device)
+            if not self.embedding:
+                self.x_stage = torch.zeros((n * T, self.shape.hidden), dtype=torch.float32,
+                                           device=self.device)
+            torch.cuda.synchronize(self.device)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self._staged_step()
+            self.graph = g
+        if x is not None:
+            self.x_stage.copy_(x, non_blocking=True)
+        if ids is not None:
+            self.ids.copy_(ids, non_blocking=True)
+        if targets is not None:
+            self.tg_stage.copy_(targets, non_blocking=True)
+        self.graph.replay()
+        return self.loss_partials
+
+    def _staged_step(self):
+        n, T = self.accumulation_steps, self.shape.tokens
+        for i in range(n):
+            x = None if self.embedding else self.x_stage[i * T:(i + 1) * T]
+            self.forward_backward(x, self.tg_stage[i * T:(i + 1) * T], micro=i)
         self.clip_and_update()
         return self.loss_partials

@@ -206,3 +206,46 @@ def test_embedded_step_matches_oracle():
                           o["beta1"], o["beta2"], o["eps"], o["weight_decay"], 1.0)
     assert np.max(np.abs(to_np(tr.emb) - want)) <= ADAMW_REL * np.max(np.abs(want))
     assert rdt.device_error() == 0
+
+
+# ------------------------------------------------------------------ CUDA graph
+@pytest.mark.parametrize("mode", [{}, {"accumulation_steps": 2}, {"embedding": True},
+                                  {"checkpoint_segments": 2}])
+def test_graph_replay_is_bit_identical(mode):
+    """One eager step, then the captured step replayed twice on new inputs:
+    losses, gradients, weights and moments equal three eager steps exactly
+    (the AdamW step count lives on the device)."""
+    shape = ragged_shape(layers=3)
+    n = mode.get("accumulation_steps", 1)
+    T = shape.tokens
+    blocks, head, _, _ = synth.make_model_inputs(shape, 7)
+    g = torch.Generator().manual_seed(11)
+    table = torch.randn(shape.vocab, shape.hidden, generator=g)
+    steps = []
+    for _ in range(3):
+        tg = torch.randint(0, shape.vocab, (n * T,), generator=g, dtype=torch.int32).cuda()
+        if mode.get("embedding"):
+            steps.append(dict(targets=tg, ids=torch.randint(0, shape.vocab, (n * T,),
+                                                            generator=g,
+                                                            dtype=torch.int32).cuda()))
+        else:
+            steps.append(dict(targets=tg, x=torch.randn(n * T, shape.hidden,
+                                                         generator=g).cuda()))
+    runs = []
+    for graph in (False, True):
+        tr = DecoderTrainer(shape, **mode)
+        tr.load(blocks, head, emb=table if mode.get("embedding") else None)
+        losses = []
+        for i, kw in enumerate(steps):
+            fn = tr.train_step_graph if (graph and i > 0) else tr.train_step
+            losses.append(fn(**kw).clone())
+        torch.cuda.synchronize()
+        runs.append((tr, losses))
+    (a, la), (b, lb) = runs
+    for x, y in zip(la, lb):
+        assert torch.equal(x, y)
+    for name in ("w", "wb", "g", "m", "v", "step_dev"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
+    if mode.get("embedding"):
+        assert torch.equal(a.emb, b.emb)
+    assert int(b.step_dev) == 3

@@ -84,11 +84,11 @@ def test_null_and_misaligned_arguments_fail_before_any_launch(lib):
     st = lib.rdt_block_forward(ctypes.byref(cfg), 1, 32, None, None, None, None, None, 0, None,
                                0, None)
     assert st == rdt.RDT_EINVAL and b"null" in lib.rdt_last_error()
-    st = lib.rdt_adamw_step(P(16), P(16), P(16), P(16), 4, None, None, 0, 1e-3, 0.9, 0.95, 1e-8,
-                            0.0, None, None)
+    st = lib.rdt_adamw_step(P(16), P(16), P(16), P(16), 4, None, None, 0, None, 1e-3, 0.9, 0.95,
+                            1e-8, 0.0, None, None)
     assert st == rdt.RDT_EINVAL and b"step" in lib.rdt_last_error()
-    st = lib.rdt_adamw_step(P(18), P(16), P(16), P(16), 4, None, None, 1, 1e-3, 0.9, 0.95, 1e-8,
-                            0.0, None, None)
+    st = lib.rdt_adamw_step(P(18), P(16), P(16), P(16), 4, None, None, 1, None, 1e-3, 0.9, 0.95,
+                            1e-8, 0.0, None, None)
     assert st == rdt.RDT_EINVAL and b"aligned" in lib.rdt_last_error()
     st = lib.rdt_clip_scale(P(16), ctypes.c_float(0.0), P(16), None, None)
     assert st == rdt.RDT_EINVAL
