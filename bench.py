@@ -506,22 +506,43 @@ def run_nf4(args, rank, world, local_rank):
             dist.barrier()
         torch.cuda.synchronize()
 
-    for i in range(args.warmup):
-        tr.train_step(xs[i % nb], dys[i % nb])
-    timer = rdt.GemmTimer(32 * args.steps)
+    use_graph = not args.no_graph
+    tr.train_step(xs[0], dys[0])
+    if use_graph:
+        lc0 = rdt.launch_count()
+        tr.train_step_graph(xs[1 % nb], dys[1 % nb])  # captures, then replays
+        launches_per_step = rdt.launch_count() - lc0
+    for i in range(2 if use_graph else 1, args.warmup):
+        (tr.train_step_graph if use_graph else tr.train_step)(xs[i % nb], dys[i % nb])
+    timer = rdt.GemmTimer(32 * (1 if use_graph else args.steps))
     barrier()
     clk = start_clock_sampler(local_rank)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
     l0 = rdt.launch_count()
-    with timer:
+    if use_graph:
         for i in range(args.steps):
-            flush.fill_(i & 0xFF)  # outside the timed events: evicts the previous step
+            # inputs staged and L2 flushed outside the timed events
+            tr.x_stage.copy_(xs[i % nb])
+            tr.dy_stage.copy_(dys[i % nb])
+            flush.fill_(i & 0xFF)
             evs[i][0].record(stream)
-            tr.train_step(xs[i % nb], dys[i % nb])
+            tr.train_step_graph()
             evs[i][1].record(stream)
         barrier()
-    launches = rdt.launch_count() - l0
+        launches = launches_per_step * args.steps
+        with timer:  # per-GEMM durations on one eager step (graph events cannot be timed)
+            tr.train_step(xs[0], dys[0])
+        torch.cuda.synchronize()
+    else:
+        with timer:
+            for i in range(args.steps):
+                flush.fill_(i & 0xFF)  # outside the timed events: evicts the previous step
+                evs[i][0].record(stream)
+                tr.train_step(xs[i % nb], dys[i % nb])
+                evs[i][1].record(stream)
+            barrier()
+        launches = rdt.launch_count() - l0
     clocks = stop_clock_sampler(clk)
     dev_ms = sum(a.elapsed_time(b) for a, b in evs)
     t = torch.tensor([dev_ms], device=dev, dtype=torch.float64)
@@ -549,9 +570,10 @@ def run_nf4(args, rank, world, local_rank):
         "launches_timed": len(nf4),
         "flops_per_launch": nf4_flops / max(len(nf4), 1),
         "ms_per_launch": nf4_ms / max(len(nf4), 1),
-        "nf4_gemm_share_of_step": round(nf4_ms / max_ms, 4) if max_ms else None,
-        "adapter_gemm_share_of_step": round(sum(ms for _, ms in other) / max_ms, 4)
-        if max_ms else None,
+        "nf4_gemm_share_of_step": round(nf4_ms / (max_ms / args.steps * (
+            1 if use_graph else args.steps)), 4) if max_ms else None,
+        "adapter_gemm_share_of_step": round(sum(ms for _, ms in other) / (
+            max_ms / args.steps * (1 if use_graph else args.steps)), 4) if max_ms else None,
     }
     step_flops = nf4_algorithmic_flops(shape, tr.rank)
     out = {
@@ -566,6 +588,7 @@ def run_nf4(args, rank, world, local_rank):
         "step_tflops": round(step_flops / (max_ms / args.steps / 1e3) / 1e12, 1),
         "gpu_launches": int(launches),
         "clocks": clocks,
+        "launch": "one CUDA graph replay per step" if use_graph else "eager kernel launches",
     }
     out["config"]["params"] = tr.n_params
     out["config"]["algorithmic_tflop_per_step"] = round(step_flops / 1e12, 3)
@@ -579,7 +602,7 @@ def run_nf4(args, rank, world, local_rank):
         for i in range(args.steps):
             xd.copy_(xh[i % 2], non_blocking=True)
             dyd.copy_(dyh[i % 2], non_blocking=True)
-            tr.train_step(xd, dyd)
+            (tr.train_step_graph if use_graph else tr.train_step)(xd, dyd)
             sq_h.copy_(tr.sumsq, non_blocking=True)
         torch.cuda.synchronize()
         dt = time.perf_counter() - t0

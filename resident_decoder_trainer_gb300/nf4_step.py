@@ -56,7 +56,9 @@ class Nf4LoraTrainer:
         self.sumsq = torch.zeros(1, dtype=torch.float64, device=dev)
         self.scale = torch.ones(1, **f32)
         self.nonfinite = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.step_dev = torch.zeros(1, dtype=torch.int32, device=dev)  # AdamW's step count
         self.step_count = 0
+        self.graph = None
 
     # ------------------------------------------------------------- views
     def adapter(self, name):
@@ -126,9 +128,10 @@ class Nf4LoraTrainer:
         self.step_count += 1
         rdt.sq_sum_noalloc([self.g], self.sumsq)
         rdt.clip_scale(self.sumsq, o["max_norm"], self.scale, self.nonfinite)
-        rdt.adamw_step(self.lora, self.g, self.m, self.v, self.step_count, o["lr"], o["beta1"],
+        rdt.step_advance(self.step_dev)
+        rdt.adamw_step(self.lora, self.g, self.m, self.v, None, o["lr"], o["beta1"],
                        o["beta2"], o["eps"], o["weight_decay"], scale=self.scale,
-                       skip=self.nonfinite)
+                       skip=self.nonfinite, step_dev=self.step_dev)
         self.refresh_shadow()
 
     def train_step(self, x, dy):
@@ -136,4 +139,24 @@ class Nf4LoraTrainer:
         [tokens, hidden], on the device). Returns the block output y."""
         self.forward_backward(x, dy)
         self.clip_and_update()
+        return self.y
+
+    def train_step_graph(self, x=None, dy=None):
+        """train_step as one CUDA graph replay: x and dy (when given) are
+        copied into staging buffers, then the step captured on the first call
+        (which must follow an eager train_step) replays."""
+        if self.graph is None:
+            self.x_stage = torch.zeros_like(self.y)
+            self.dy_stage = torch.zeros_like(self.y)
+            torch.cuda.synchronize(self.device)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self.forward_backward(self.x_stage, self.dy_stage)
+                self.clip_and_update()
+            self.graph = g
+        if x is not None:
+            self.x_stage.copy_(x, non_blocking=True)
+        if dy is not None:
+            self.dy_stage.copy_(dy, non_blocking=True)
+        self.graph.replay()
         return self.y
