@@ -38,8 +38,8 @@ UNIT = "tokens/s"
 # DRAM traffic per tensor-core GEMM launch, from `ncu` (dram__bytes_read.sum +
 # dram__bytes_write.sum) averaged over the step's launch mix, and the source
 # it was measured on; reported only while gemm.cu is unchanged.
-GEMM_TRAFFIC_BYTES = 254737678
-GEMM_TRAFFIC_SRC_SHA = "36d847e5d51ba2e1"
+GEMM_TRAFFIC_BYTES = 261122248
+GEMM_TRAFFIC_SRC_SHA = "fc348891de0434a8"
 # The same for the NF4 GEMM launches of one q4b_nf4 step.
 NF4_TRAFFIC_BYTES = 75606000
 NF4_TRAFFIC_SRC_SHA = "16a70095fa1257b0"
