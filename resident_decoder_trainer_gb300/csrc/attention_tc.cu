@@ -8,21 +8,25 @@
 // columns of the rows it owns. Work items are launched longest-first (the
 // causal triangle makes items unequal).
 //
-// Forward (head_dim 64 or 128), one CTA per (128-query tile, query head,
-// sequence): S = Q K^T goes to one of two TMEM buffers, so the next tile's
-// scores are computed while this tile's online softmax (log2 domain) runs;
-// O += P V accumulates in TMEM, rescaled in place when the row maximum moves;
-// P is written as bf16 into a 128-byte-swizzled shared tile that the MMA
-// reads as its A operand. The log-sum-exp of every row is saved.
+// Forward (head_dim 64 or 128), persistent: each CTA walks (128-query tile,
+// query head, sequence) work items longest first. S = Q K^T goes to one of
+// two TMEM buffers, so the next tile's scores are computed while this tile's
+// online softmax (log2 domain) runs; P is written back over its S buffer as
+// packed bf16 and read from TMEM as the A operand of O += P V; O lives in one
+// of two TMEM buffers (items alternate) and is rescaled in place only when a
+// row maximum grows by more than 2^8. K tiles come through a 3-deep ring
+// freed as each Q K^T completes, V through a 2-deep ring freed by P V. The
+// log-sum-exp of every row is saved.
 //
 // Backward (head_dim 64 or 128) in two kernels, so no dQ atomics are needed
 // and the result does not depend on scheduling:
 //  * dK/dV, one CTA per (128-key tile, kv head, sequence), loops over the
 //    query heads of its group and the 64-query tiles at or below the
 //    diagonal: S^T = K Q^T and dP^T = V dO^T into one of two TMEM buffer
-//    pairs; P^T and dS^T = P^T o (dP^T - D) go to swizzled shared tiles;
-//    dV += P^T dO and dK += dS^T Q accumulate in TMEM over the whole group
-//    (the GQA reduction costs nothing);
+//    pairs; P^T and dS^T = P^T o (dP^T - D) are written back over their own
+//    TMEM columns as packed bf16 and read as the A operands of dV += P^T dO
+//    and dK += dS^T Q, which accumulate in TMEM over the whole group (the
+//    GQA reduction costs nothing);
 //  * dQ, one CTA per (128-query tile, head, sequence): S and dP are
 //    recomputed per key tile, dQ += dS K accumulates in TMEM and is written
 //    once.
