@@ -645,6 +645,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 // raw bytes, turn them into the bf16 B tile, and arrive on the stage's full
 // barrier, which the MMA waits for.
 constexpr int NF4_THREADS = 448;
+// The pair kernel runs two decode groups of 4 warps (warps 10-13 and 14-17)
+// that take alternate k-blocks, so one group's decode latency (the permute
+// chains, the proxy fence, the arrive) overlaps the other's.
+constexpr int NF4P_THREADS = 576;
 constexpr int NF4_BN = 256;
 
 struct TileN4 {
@@ -1017,7 +1021,7 @@ static_assert(TileN4P::SMEM <= 232448, "NF4 pair tile exceeds the shared memory 
 static_assert(TileN4P::STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
 
 template <int B_MN, int EPI>
-__global__ void __launch_bounds__(NF4_THREADS, 1)
+__global__ void __launch_bounds__(NF4P_THREADS, 1)
     gemm2_nf4_kernel(const __grid_constant__ CUtensorMap tma_a,
                      const __grid_constant__ CUtensorMap tma_b2,
                      const __grid_constant__ Nf4Maps nm, const __grid_constant__ OutMaps om,
@@ -1225,14 +1229,24 @@ __global__ void __launch_bounds__(NF4_THREADS, 1)
     __syncwarp();
   } else {
     // -------------------------------------------------------------- decode
-    const int dt = static_cast<int>(threadIdx.x) - 320;  // 0..127
+    const int dg = static_cast<int>(threadIdx.x) - 320;
+    const int dt = dg & 127;  // thread within the group
+    const uint32_t grp = static_cast<uint32_t>(dg >> 7);
     int stage = 0;
     uint32_t ph = 0;
+    uint32_t it = 0;  // k-blocks this CTA has passed, across units
     bool ok = true;
     for (int u = pair; u < nunits && ok; u += npairs) {
       const int kb0 = (u / ntiles) * p.kb_split;
       const int kb1 = min(p.k_blocks, kb0 + p.kb_split);
-      for (int kb = kb0; kb < kb1; ++kb) {
+      for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        if ((it & 1) != grp) {  // the other group's k-block
+          if (++stage == STAGES) {
+            stage = 0;
+            ph ^= 1;
+          }
+          continue;
+        }
         if (!warp_wait(raw0 + 8 * stage, ph, p.err)) {
           ok = false;
           break;
@@ -2112,7 +2126,7 @@ static cudaError_t launch_nf4_pair(const CUtensorMap& ta, const CUtensorMap& tb2
   const int pairs = nunits < max_pairs ? nunits : max_pairs;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs, 1, 1);
-  cfg.blockDim = dim3(NF4_THREADS, 1, 1);
+  cfg.blockDim = dim3(NF4P_THREADS, 1, 1);
   cfg.dynamicSmemBytes = TileN4P::SMEM;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -2137,7 +2151,7 @@ static int max_active_nf4_pairs() {
   std::call_once(once, [] {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * num_sms(), 1, 1);
-    cfg.blockDim = dim3(NF4_THREADS, 1, 1);
+    cfg.blockDim = dim3(NF4P_THREADS, 1, 1);
     cfg.dynamicSmemBytes = TileN4P::SMEM;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
