@@ -559,9 +559,9 @@ def run_nf4(args, rank, world, local_rank):
     peak_tf = float(peaks.get("bf16_tflops_sustained") or peaks.get("bf16_tflops"))
     achieved = nf4_flops / (nf4_ms / 1e3) / 1e12 if nf4_ms > 0 else None
     roofline = {
-        "kernel": "gemm_nf4_kernel (tcgen05 BF16 128x256 tiles, B decoded from 4-bit NF4 codes "
-                  "+ per-64 fp32 scales into shared memory by four decode warps, LoRA term "
-                  "as a bf16 tail k-block)",
+        "kernel": "gemm2_nf4_kernel (tcgen05 BF16 CTA pairs, 256x256 tiles, B decoded from "
+                  "4-bit NF4 codes + per-64 fp32 scales into shared memory by two groups of "
+                  "four decode warps on alternate k-blocks, LoRA term as a bf16 tail k-block)",
         "bound": "tensor", "achieved": round(achieved, 1) if achieved else None,
         "peak": peak_tf, "unit": "TFLOP/s",
         "frac": round(achieved / peak_tf, 4) if achieved else None,

@@ -1035,10 +1035,11 @@ __global__ void __launch_bounds__(NF4P_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + TileN4P::OFF_OUT + OS::TOTAL);
-  // bars: raw[S], full[S], empty[S], tfull[2], tempty[2], drain, epilogue inputs[8][2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 21);
+  // bars: raw[2][S] (one set per decode group), full[S], empty[S], tfull[2],
+  // tempty[2], drain, epilogue inputs[8][2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4 * STAGES + 21);
   const uint32_t raw0 = smem_u32(bars);
-  const uint32_t full0 = raw0 + 8 * STAGES;
+  const uint32_t full0 = raw0 + 8 * 2 * STAGES;
   const uint32_t empty0 = full0 + 8 * STAGES;
   const uint32_t tfull0 = empty0 + 8 * STAGES;
   const uint32_t tempty0 = tfull0 + 16;
@@ -1052,8 +1053,8 @@ __global__ void __launch_bounds__(NF4P_THREADS, 1)
   const int npairs = static_cast<int>(gridDim.x) >> 1;
 
   if (threadIdx.x == 0) {
+    for (int s = 0; s < 2 * STAGES; ++s) mbar_init(raw0 + 8 * s, 1);
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(raw0 + 8 * s, 1);
       mbar_init(full0 + 8 * s, 1 + 2 * 4);  // even producer + both CTAs' decode warps
       mbar_init(empty0 + 8 * s, 1);
     }
@@ -1089,6 +1090,7 @@ __global__ void __launch_bounds__(NF4P_THREADS, 1)
       // ------------------------------------------------------------ producer
       int stage = 0;
       uint32_t ph = 0;
+      uint32_t it = 0;  // k-blocks issued, across units: group it & 1 decodes it
       bool ok = true;
       for (int u = pair; u < nunits && ok; u += npairs) {
         int mt, nt;
@@ -1099,12 +1101,12 @@ __global__ void __launch_bounds__(NF4P_THREADS, 1)
         // first of this CTA's 128 B rows (K-major) / columns (MN-major)
         const int r0 = (EPI == EPI_SWIGLU) ? nt * 128 + static_cast<int>(rank) * p.swiglu_half
                                            : nt * BN + static_cast<int>(rank) * BH;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           if (!mbar_wait(empty0 + 8 * stage, ph ^ 1, p.err)) {
             ok = false;
             break;
           }
-          const uint32_t rb = raw0 + 8 * stage;
+          const uint32_t rb = raw0 + 8 * ((it & 1) * STAGES + stage);
           const uint32_t fb = full_even + 8 * stage;
           const uint32_t sa = smem_base + stage * STAGE_BYTES;
           const uint32_t sb = sa + TileN4P::OFF_B;
@@ -1233,7 +1235,6 @@ __global__ void __launch_bounds__(NF4P_THREADS, 1)
     const int dt = dg & 127;  // thread within the group
     const uint32_t grp = static_cast<uint32_t>(dg >> 7);
     int stage = 0;
-    uint32_t ph = 0;
     uint32_t it = 0;  // k-blocks this CTA has passed, across units
     bool ok = true;
     for (int u = pair; u < nunits && ok; u += npairs) {
@@ -1241,13 +1242,15 @@ __global__ void __launch_bounds__(NF4P_THREADS, 1)
       const int kb1 = min(p.k_blocks, kb0 + p.kb_split);
       for (int kb = kb0; kb < kb1; ++kb, ++it) {
         if ((it & 1) != grp) {  // the other group's k-block
-          if (++stage == STAGES) {
-            stage = 0;
-            ph ^= 1;
-          }
+          if (++stage == STAGES) stage = 0;
           continue;
         }
-        if (!warp_wait(raw0 + 8 * stage, ph, p.err)) {
+        // this group's raw barrier of the stage: the group's uses of it are the
+        // k-blocks it = c + 2 S n (one residue c mod 2 S), use n completing its
+        // phase n, so the group sees every phase in order (with one barrier
+        // per stage and S odd, a group would skip phases, and a parity wait
+        // could pass on the phase before the one it waits for)
+        if (!warp_wait(raw0 + 8 * (grp * STAGES + stage), (it / (2 * STAGES)) & 1, p.err)) {
           ok = false;
           break;
         }
@@ -1274,10 +1277,7 @@ __global__ void __launch_bounds__(NF4P_THREADS, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(full_even + 8 * stage);
-        if (++stage == STAGES) {
-          stage = 0;
-          ph ^= 1;
-        }
+        if (++stage == STAGES) stage = 0;
       }
     }
   }
