@@ -173,7 +173,25 @@ cudaError_t rmsnorm_fwd(const float* x, const float* gamma, bf16* y, float* rstd
   return cudaGetLastError();
 }
 
-int rmsnorm_bwd_partial_rows(int T) { return T < kMaxPartialRows ? T : kMaxPartialRows; }
+// CTAs (= partial rows) of rmsnorm_bwd: one per row up to one full wave, the
+// resident CTAs of all SMs (the row loop is uniform, so a second partial wave
+// would only add a tail), within kMaxPartialRows.
+int rmsnorm_bwd_partial_rows(int T, int threads) {
+  static int per_sm[17] = {};  // by threads / 32 (threads <= 512)
+  const int w = threads / 32;
+  if (w < 1 || w > 16) return 1;
+  if (per_sm[w] == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, rmsnorm_bwd_kernel, threads, 0) !=
+            cudaSuccess || n < 1)
+      n = 1;
+    per_sm[w] = n;
+  }
+  int cap = per_sm[w] * num_sms();
+  if (cap > kMaxPartialRows) cap = kMaxPartialRows / num_sms() * num_sms();
+  if (cap < 1) cap = 1;
+  return T < cap ? (T > 0 ? T : 1) : cap;
+}
 
 static cudaError_t reduce_cols(const float* partials, int P, int W, float* out, cudaStream_t s,
                                bool accumulate) {
@@ -185,8 +203,8 @@ static cudaError_t reduce_cols(const float* partials, int P, int W, float* out, 
 cudaError_t rmsnorm_bwd(const float* dy, const float* x, const float* rstd, const float* gamma,
                         const float* resid, float* dx, bf16* dx_bf16, float* dgamma,
                         float* partials, int T, int H, cudaStream_t s, bool accumulate) {
-  const int P = rmsnorm_bwd_partial_rows(T);
   const int threads = ((H / 8 + 31) / 32) * 32;
+  const int P = rmsnorm_bwd_partial_rows(T, threads);
   note_launch();
   rmsnorm_bwd_kernel<<<P, threads, 0, s>>>(dy, x, rstd, gamma, resid, dx, dx_bf16, partials, T, H);
   cudaError_t e = cudaGetLastError();
@@ -323,7 +341,7 @@ cudaError_t qknorm_rope_fwd(const float* qkv, int64_t ld_qkv, bf16* q_out, bf16*
 // in registers; lanes of different head slots are combined by shuffles, warps
 // in a fixed order, and each CTA writes one partial row [q gains | k gains].
 template <int D>
-__global__ void __launch_bounds__(256) qknorm_rope_bwd_kernel(
+__global__ void __launch_bounds__(256, 3) qknorm_rope_bwd_kernel(
     const float* __restrict__ dq, const float* __restrict__ dk, const float* __restrict__ qkv,
     int64_t ld, const float* __restrict__ rq, const float* __restrict__ rk,
     const float* __restrict__ gq, const float* __restrict__ gk, const float2* __restrict__ cs,
@@ -336,8 +354,6 @@ __global__ void __launch_bounds__(256) qknorm_rope_bwd_kernel(
   const int i0 = 4 * (first ? sub : sub - PX);
   const int heads = nh + nkv;
   const int groups = (heads + HPW - 1) / HPW;
-  const float4 gq4 = reinterpret_cast<const float4*>(gq)[sub];
-  const float4 gk4 = reinterpret_cast<const float4*>(gk)[sub];
   float accq[4] = {}, acck[4] = {};
   struct In {
     float4 d, x;
@@ -363,7 +379,7 @@ __global__ void __launch_bounds__(256) qknorm_rope_bwd_kernel(
 #pragma unroll
     for (int e = 0; e < 4; ++e) dp[e] = __shfl_xor_sync(0xffffffffu, din[e], PX);
     const float cv[4] = {c01.x, c01.z, c23.x, c23.z}, sv[4] = {c01.y, c01.w, c23.y, c23.w};
-    const float4 g4 = isq ? gq4 : gk4;
+    const float4 g4 = reinterpret_cast<const float4*>(isq ? gq : gk)[sub];  // L1-resident
     const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
     float xh[4], dxh[4];
     float dot = 0.f;
@@ -390,15 +406,25 @@ __global__ void __launch_bounds__(256) qknorm_rope_bwd_kernel(
           make_uint2(pack_bf16x2(o4[0], o4[1]), pack_bf16x2(o4[2], o4[3]));
     }
   };
+  // a warp takes head groups warp, warp + 8, ...: all of a token's loads
+  // (up to MAXJ groups) are issued before any is used, so each warp keeps
+  // several rows of both inputs in flight
+  constexpr int MAXJ = 5;
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
     const float4* c4 = reinterpret_cast<const float4*>(cs + (int64_t)(t % S) * HALF + i0);
     const float4 c01 = c4[0], c23 = c4[1];
-    for (int g0 = warp; g0 < groups; g0 += 16) {
-      const int h0 = g0 * HPW + slot, h1 = (g0 + 8) * HPW + slot;
-      const In in0 = load(t, h0);
-      const In in1 = load(t, g0 + 8 < groups ? h1 : heads);
-      head_grad(t, h0, in0, c01, c23);
-      if (g0 + 8 < groups) head_grad(t, h1, in1, c01, c23);
+    for (int gb = warp; gb < groups; gb += 8 * MAXJ) {
+      In in[MAXJ];
+#pragma unroll
+      for (int j = 0; j < MAXJ; ++j) {
+        const int gi = gb + 8 * j;
+        in[j] = load(t, gi < groups ? gi * HPW + slot : heads);
+      }
+#pragma unroll
+      for (int j = 0; j < MAXJ; ++j) {
+        const int gi = gb + 8 * j;
+        if (gi < groups) head_grad(t, gi * HPW + slot, in[j], c01, c23);  // warp-uniform
+      }
     }
   }
   // combine head slots of the warp (lanes with equal sub), fixed order
@@ -426,8 +452,12 @@ __global__ void __launch_bounds__(256) qknorm_rope_bwd_kernel(
 }
 
 int qknorm_bwd_partial_rows(int T, int) {
-  // one CTA (and one partial row) per token, at most kMaxPartialRows
-  const int cap = kMaxPartialRows;
+  // one CTA (and one partial row) per token up to a whole number of CTAs per
+  // SM (3, the kernel's occupancy by its launch bounds) within
+  // kMaxPartialRows, so every SM gets the same share of tokens
+  int per_sm = kMaxPartialRows / num_sms();
+  if (per_sm > 3) per_sm = 3;
+  const int cap = per_sm >= 1 ? per_sm * num_sms() : kMaxPartialRows;
   return T < cap ? (T > 0 ? T : 1) : cap;
 }
 

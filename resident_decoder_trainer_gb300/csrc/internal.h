@@ -122,7 +122,7 @@ cudaError_t rmsnorm_fwd(const float* x, const float* gamma, bf16* y, float* rstd
 cudaError_t rmsnorm_bwd(const float* dy, const float* x, const float* rstd, const float* gamma,
                         const float* resid, float* dx, bf16* dx_bf16, float* dgamma,
                         float* partials, int T, int H, cudaStream_t s, bool accumulate = false);
-int rmsnorm_bwd_partial_rows(int T);
+int rmsnorm_bwd_partial_rows(int T, int threads);
 
 cudaError_t rope_table(float* cs, int S, int d, float theta, cudaStream_t s);
 // qkv: fp32 raw projections [T, ld] (q | k | v); writes the normalised and
