@@ -22,7 +22,8 @@
 // and the result does not depend on scheduling:
 //  * dK/dV, one CTA per (128-key tile, kv head, sequence), loops over the
 //    query heads of its group and the 64-query tiles at or below the
-//    diagonal: S^T = K Q^T and dP^T = V dO^T into one of two TMEM buffer
+//    diagonal (Q, dO and their lse / D rows through a 4-deep ring, so the
+//    copies run well ahead of the two TMEM buffer pairs): S^T = K Q^T and dP^T = V dO^T into one of two TMEM buffer
 //    pairs; P^T and dS^T = P^T o (dP^T - D) are written back over their own
 //    TMEM columns as packed bf16 and read as the A operands of dV += P^T dO
 //    and dK += dS^T Q, which accumulate in TMEM over the whole group (the
@@ -425,10 +426,14 @@ struct BwdCfg {
   static constexpr uint32_t Q_BYTES = BQ * D * 2;
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = OFF_K + KV_BYTES;
-  static constexpr uint32_t OFF_Q = OFF_V + KV_BYTES;      // [2]
-  static constexpr uint32_t OFF_DO = OFF_Q + 2 * Q_BYTES;  // [2]
-  static constexpr uint32_t OFF_LD = OFF_DO + 2 * Q_BYTES;  // float [2 stages][lse2, D][64]
-  static constexpr uint32_t OFF_BAR = OFF_LD + 2 * 2 * 64 * 4;
+  // Q / dO / (lse, D) stages: the loads for query tile it + 2 wait for dV/dK
+  // of tile it - QST + 2 to free their stage, so with QST = 4 their latency
+  // stays off the path S -> P -> dV/dK that the two TMEM buffer pairs allow
+  static constexpr int QST = 4;
+  static constexpr uint32_t OFF_Q = OFF_V + KV_BYTES;        // [QST]
+  static constexpr uint32_t OFF_DO = OFF_Q + QST * Q_BYTES;  // [QST]
+  static constexpr uint32_t OFF_LD = OFF_DO + QST * Q_BYTES;  // float [QST][lse2, D][64]
+  static constexpr uint32_t OFF_BAR = OFF_LD + QST * 2 * 64 * 4;
   static constexpr size_t SMEM = OFF_BAR + 256 + 1024;
   // TMEM columns: dK, dV, then two (S^T, dP^T) buffer pairs of 64 + 64
   // columns; P^T and dS^T (packed bf16) are written back over their own S^T /
@@ -437,6 +442,7 @@ struct BwdCfg {
   static constexpr uint32_t T_DK = 0, T_DV = 128, T_S = 256;
   static constexpr uint32_t TMEM_COLS = 512;
 };
+static_assert(BwdCfg<128>::SMEM <= 232448, "dK/dV stages exceed the shared memory of a CTA");
 
 // TMEM column (relative to an S^T / dP^T block) of the packed bf16 A operand
 // for K step kk (16 queries): the lanes of warp half h pack their 32 queries
@@ -462,9 +468,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + C::OFF_BAR;
-  const uint32_t kv_full = bar0, q_full = bar0 + 8, q_empty = bar0 + 24, s_full = bar0 + 40,
-                 p_ready = bar0 + 56, done = bar0 + 72, fin = bar0 + 88, drain = bar0 + 96;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 128);
+  constexpr int QST = C::QST;
+  // bars: kv_full, q_full[QST], q_empty[QST], s_full[2], p_ready[2], done[2], fin, drain
+  const uint32_t kv_full = bar0, q_full = bar0 + 8, q_empty = q_full + 8 * QST,
+                 s_full = q_empty + 8 * QST, p_ready = s_full + 16, done = p_ready + 16,
+                 fin = done + 16, drain = fin + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 192);
+  static_assert(8 * (4 + 2 * QST + 6) <= 192, "dK/dV barriers overlap the TMEM slot");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int per = nkv * B;
@@ -481,9 +491,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < QST; ++i) {
       mbar_init(q_full + 8 * i, 1);
       mbar_init(q_empty + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(s_full + 8 * i, 1);
       mbar_init(p_ready + 8 * i, kEltThreads);
       mbar_init(done + 8 * i, 1);
@@ -515,32 +527,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pending = 0;
       bool ok = true;
       for (int it = 0; it < iters && ok; ++it) {
-        const int st = it & 1;
-        const uint32_t ph = (it >> 1) & 1;
-        if (!mbar_wait(q_empty + 8 * st, ph ^ 1, err)) {
+        const int qs = it % QST;
+        const uint32_t ph = (it / QST) & 1;
+        if (!mbar_wait(q_empty + 8 * qs, ph ^ 1, err)) {
           ok = false;
           break;
         }
         const int hh = g * rep + it / per_head;
         const int m0 = (first_qt + it % per_head) * BQ;
-        const uint32_t qf = q_full + 8 * st;
+        const uint32_t qf = q_full + 8 * qs;
         mbar_arrive_expect_tx(qf, 2 * C::Q_BYTES + 512);
         for (int c = 0; c < DCH; ++c) {
-          tma_load_2d(sbase + C::OFF_Q + st * C::Q_BYTES + c * C::Q_CHUNK, &tq, qf,
+          tma_load_2d(sbase + C::OFF_Q + qs * C::Q_BYTES + c * C::Q_CHUNK, &tq, qf,
                       hh * D + c * 64, tok0 + m0);
-          tma_load_2d(sbase + C::OFF_DO + st * C::Q_BYTES + c * C::Q_CHUNK, &tdo, qf,
+          tma_load_2d(sbase + C::OFF_DO + qs * C::Q_BYTES + c * C::Q_CHUNK, &tdo, qf,
                       hh * D + c * 64, tok0 + m0);
         }
         const int64_t seg = ((int64_t)b * nh + hh) * S_pad + m0;
-        bulk_load_1d(sbase + C::OFF_LD + st * 512, lse2 + seg, 256, qf);
-        bulk_load_1d(sbase + C::OFF_LD + st * 512 + 256, Dd + seg, 256, qf);
-        pending = (pending & ~(3u << (2 * st))) | ((1u | (ph << 1)) << (2 * st));
+        bulk_load_1d(sbase + C::OFF_LD + qs * 512, lse2 + seg, 256, qf);
+        bulk_load_1d(sbase + C::OFF_LD + qs * 512 + 256, Dd + seg, 256, qf);
+        pending = (pending & ~(3u << (2 * qs))) | ((1u | (ph << 1)) << (2 * qs));
       }
       if (!ok) {
         mbar_wait(kv_full, 0, nullptr);
-        for (int st = 0; st < 2; ++st)
-          if ((pending >> (2 * st)) & 1u)
-            mbar_wait(q_full + 8 * st, (pending >> (2 * st + 1)) & 1u, nullptr);
+        for (int qs = 0; qs < QST; ++qs)
+          if ((pending >> (2 * qs)) & 1u)
+            mbar_wait(q_full + 8 * qs, (pending >> (2 * qs + 1)) & 1u, nullptr);
       }
     }
   } else if (warp == 1) {
@@ -552,14 +564,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t v_desc = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
       bool ok = mbar_wait(kv_full, 0, err);
       auto issue_s = [&](int it) -> bool {
-        const int st = it & 1;
-        const uint32_t ph = (it >> 1) & 1;
-        if (!mbar_wait(q_full + 8 * st, ph, err)) return false;
+        const int st = it & 1, qs = it % QST;
+        if (!mbar_wait(q_full + 8 * qs, (it / QST) & 1, err)) return false;
         // buffer pair st still holds P^T / dS^T of iteration it - 2
-        if (it >= 2 && !mbar_wait(done + 8 * st, ph ^ 1, err)) return false;
+        if (it >= 2 && !mbar_wait(done + 8 * st, ((it >> 1) & 1) ^ 1, err)) return false;
         tc_fence_after();
-        const uint64_t q_desc = sdesc_sw128(sbase + C::OFF_Q + st * C::Q_BYTES, 16, 1024);
-        const uint64_t o_desc = sdesc_sw128(sbase + C::OFF_DO + st * C::Q_BYTES, 16, 1024);
+        const uint64_t q_desc = sdesc_sw128(sbase + C::OFF_Q + qs * C::Q_BYTES, 16, 1024);
+        const uint64_t o_desc = sdesc_sw128(sbase + C::OFF_DO + qs * C::Q_BYTES, 16, 1024);
         const uint32_t ts = tmem + C::T_S + st * 128;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
@@ -583,8 +594,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t qb = sbase + C::OFF_Q + st * C::Q_BYTES;
-        const uint32_t ob = sbase + C::OFF_DO + st * C::Q_BYTES;
+        const int qs = it % QST;
+        const uint32_t qb = sbase + C::OFF_Q + qs * C::Q_BYTES;
+        const uint32_t ob = sbase + C::OFF_DO + qs * C::Q_BYTES;
         const uint32_t ts = tmem + C::T_S + st * 128;
 #pragma unroll
         for (int k = 0; k < BQ / 16; ++k) {
@@ -595,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          sdesc_sw128(qb + k * 2048, C::Q_CHUNK, 1024), id_kv, (it | k) != 0);
         }
         tc_commit(done + 8 * st);
-        tc_commit(q_empty + 8 * st);
+        tc_commit(q_empty + 8 * qs);
       }
       tc_commit(fin);
       tc_commit(drain);
@@ -622,9 +634,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(ts, sv);
       tmem_ld32(ts + 64, dp);
       tmem_ld_wait();
-      const float4* l4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + st * 512) + half * 8;
+      const int qs = it % QST;
+      const float4* l4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + qs * 512) + half * 8;
       const float4* d4 =
-          reinterpret_cast<const float4*>(smem + C::OFF_LD + st * 512 + 256) + half * 8;
+          reinterpret_cast<const float4*>(smem + C::OFF_LD + qs * 512 + 256) + half * 8;
       const int q0 = m0 + half * 32;
       // bf16 pairs of P^T / dS^T are packed in place into sv / dp [0, 16)
 #pragma unroll
