@@ -29,8 +29,11 @@
 //    and dK += dS^T Q, which accumulate in TMEM over the whole group (the
 //    GQA reduction costs nothing);
 //  * dQ, one CTA per (128-query tile, head, sequence): S and dP are
-//    recomputed per key tile, dQ += dS K accumulates in TMEM and is written
-//    once.
+//    recomputed per key tile, dS is written to TMEM as packed bf16 (two
+//    buffers) and read as the A operand of dQ += dS K, which accumulates in
+//    TMEM and is written once; K comes through a 3-deep ring (it is read
+//    again by dQ += dS K after the elementwise pass), V through a 2-deep one
+//    freed as soon as dP = dO V^T completes.
 // Every operand transposition is a shared-memory descriptor, never a copy.
 #include "common.cuh"
 #include "internal.h"
@@ -701,13 +704,19 @@ struct DqCfg {
   static constexpr int D = D_, BM = 128, BN = 128;
   static constexpr uint32_t CHUNK = 128 * 128;  // 64 cols x 128 rows of bf16
   static constexpr uint32_t T_BYTES = 128 * D * 2;
-  static constexpr uint32_t DS_BYTES = BM * BN * 2;
-  static constexpr uint32_t OFF_Q = 0, OFF_DO = T_BYTES, OFF_K = 2 * T_BYTES,  // K[2]
-      OFF_V = 4 * T_BYTES,                                                       // V[2]
-      OFF_DS = 6 * T_BYTES, OFF_BAR = OFF_DS + DS_BYTES;
+  // K runs three tiles deep (it is read by S = Q K^T and again, a whole
+  // elementwise pass later, by dQ += dS K); V two (only dP = dO V^T reads it)
+  static constexpr int KST = 3, VST = 2;
+  static constexpr uint32_t OFF_Q = 0, OFF_DO = T_BYTES, OFF_K = 2 * T_BYTES,  // K[KST]
+      OFF_V = OFF_K + KST * T_BYTES,                                             // V[VST]
+      OFF_BAR = OFF_V + VST * T_BYTES;
   static constexpr size_t SMEM = OFF_BAR + 256 + 1024;
-  static constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 256, TMEM_COLS = 512;
+  // TMEM: S, dP (128 fp32 columns each), dQ (D columns), then two dS buffers
+  // of 64 columns (128 keys as packed bf16 pairs, key 2i and 2i + 1 in
+  // column i), the A operand of dQ += dS K.
+  static constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 256, T_DS = 384, TMEM_COLS = 512;
 };
+static_assert(DqCfg<128>::SMEM <= 232448, "dQ stages exceed the shared memory of a CTA");
 
 template <int DH>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -717,16 +726,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                           const float* __restrict__ Dd, int S_pad, float* __restrict__ dq, int B,
                           int S, int nh, int nkv, float scale, float scale_log2, int* err) {
   using C = DqCfg<DH>;
-  constexpr int D = C::D, BM = C::BM, BN = C::BN, DCH = D / 64;
+  constexpr int D = C::D, BM = C::BM, BN = C::BN, DCH = D / 64, KST = C::KST, VST = C::VST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + C::OFF_BAR;
-  const uint32_t qd_full = bar0, k_full = bar0 + 8, v_full = bar0 + 24, kv_empty = bar0 + 40,
-                 s_full = bar0 + 56, s_used = bar0 + 64, ds_ready = bar0 + 72, ds_free = bar0 + 80,
-                 fin = bar0 + 88, drain = bar0 + 96;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 128);
+  // bars: qd_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full, s_used,
+  // ds_ready, ds_free[2], fin, drain
+  const uint32_t qd_full = bar0, k_full = bar0 + 8, k_empty = k_full + 8 * KST,
+                 v_full = k_empty + 8 * KST, v_empty = v_full + 8 * VST,
+                 s_full = v_empty + 8 * VST, s_used = s_full + 8, ds_ready = s_used + 8,
+                 ds_free = ds_ready + 8, fin = ds_free + 16, drain = fin + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 192);
+  static_assert(8 * (1 + 2 * KST + 2 * VST + 7) <= 192, "dQ barriers overlap the TMEM slot");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_qt = (S + BM - 1) / BM;
@@ -741,15 +754,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(qd_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < KST; ++i) {
       mbar_init(k_full + 8 * i, 1);
+      mbar_init(k_empty + 8 * i, 1);
+    }
+    for (int i = 0; i < VST; ++i) {
       mbar_init(v_full + 8 * i, 1);
-      mbar_init(kv_empty + 8 * i, 1);
+      mbar_init(v_empty + 8 * i, 1);
     }
     mbar_init(s_full, 1);
     mbar_init(s_used, kEltThreads);
     mbar_init(ds_ready, kEltThreads);
     mbar_init(ds_free, 1);
+    mbar_init(ds_free + 8, 1);
     mbar_init(fin, 1);
     mbar_init(drain, 1);
     fence_mbar_init();
@@ -773,49 +790,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sbase + C::OFF_Q + c * C::CHUNK, &tq, qd_full, h * D + c * 64, tok0 + m0);
         tma_load_2d(sbase + C::OFF_DO + c * C::CHUNK, &tdo, qd_full, h * D + c * 64, tok0 + m0);
       }
-      uint32_t pending = 0;
+      // per stage: bit 0 a copy was issued, bit 1 the parity it completes
+      uint32_t pend_k = 0, pend_v = 0;
       bool ok = true;
       for (int j = 0; j < n_tiles && ok; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait(kv_empty + 8 * st, ph ^ 1, err)) {
+        const int ks = j % KST, vs = j % VST;
+        const uint32_t kph = (j / KST) & 1, vph = (j / VST) & 1;
+        if (!mbar_wait(k_empty + 8 * ks, kph ^ 1, err)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(k_full + 8 * st, C::T_BYTES);
+        mbar_arrive_expect_tx(k_full + 8 * ks, C::T_BYTES);
         for (int c = 0; c < DCH; ++c)
-          tma_load_2d(sbase + C::OFF_K + st * C::T_BYTES + c * C::CHUNK, &tk, k_full + 8 * st,
+          tma_load_2d(sbase + C::OFF_K + ks * C::T_BYTES + c * C::CHUNK, &tk, k_full + 8 * ks,
                       g * D + c * 64, tok0 + j * BN);
-        mbar_arrive_expect_tx(v_full + 8 * st, C::T_BYTES);
+        pend_k = (pend_k & ~(3u << (2 * ks))) | ((1u | (kph << 1)) << (2 * ks));
+        if (!mbar_wait(v_empty + 8 * vs, vph ^ 1, err)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(v_full + 8 * vs, C::T_BYTES);
         for (int c = 0; c < DCH; ++c)
-          tma_load_2d(sbase + C::OFF_V + st * C::T_BYTES + c * C::CHUNK, &tv, v_full + 8 * st,
+          tma_load_2d(sbase + C::OFF_V + vs * C::T_BYTES + c * C::CHUNK, &tv, v_full + 8 * vs,
                       g * D + c * 64, tok0 + j * BN);
-        pending = (pending & ~(3u << (2 * st))) | ((1u | (ph << 1)) << (2 * st));
+        pend_v = (pend_v & ~(3u << (2 * vs))) | ((1u | (vph << 1)) << (2 * vs));
       }
       if (!ok) {
         mbar_wait(qd_full, 0, nullptr);
-        for (int st = 0; st < 2; ++st)
-          if ((pending >> (2 * st)) & 1u) {
-            const uint32_t ph = (pending >> (2 * st + 1)) & 1u;
-            mbar_wait(k_full + 8 * st, ph, nullptr);
-            mbar_wait(v_full + 8 * st, ph, nullptr);
-          }
+        for (int st = 0; st < KST; ++st)
+          if ((pend_k >> (2 * st)) & 1u) mbar_wait(k_full + 8 * st, (pend_k >> (2 * st + 1)) & 1u, nullptr);
+        for (int st = 0; st < VST; ++st)
+          if ((pend_v >> (2 * st)) & 1u) mbar_wait(v_full + 8 * st, (pend_v >> (2 * st + 1)) & 1u, nullptr);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(BM, BN, 0, 0);  // S, dP
-      constexpr uint32_t id_q = idesc_bf16_f32(BM, D, 0, 1);   // dQ
+      constexpr uint32_t id_q = idesc_bf16_f32(BM, D, 0, 1);   // dQ (A = dS from TMEM)
       bool ok = mbar_wait(qd_full, 0, err);
       auto issue_s = [&](int j) -> bool {
-        const int st = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait(k_full + 8 * st, ph, err) || !mbar_wait(v_full + 8 * st, ph, err) ||
+        const int ks = j % KST, vs = j % VST;
+        if (!mbar_wait(k_full + 8 * ks, (j / KST) & 1, err) ||
+            !mbar_wait(v_full + 8 * vs, (j / VST) & 1, err) ||
             !mbar_wait(s_used, (j & 1) ^ 1, err))
           return false;
         tc_fence_after();
-        const uint32_t kb = sbase + C::OFF_K + st * C::T_BYTES;
-        const uint32_t vb = sbase + C::OFF_V + st * C::T_BYTES;
+        const uint32_t kb = sbase + C::OFF_K + ks * C::T_BYTES;
+        const uint32_t vb = sbase + C::OFF_V + vs * C::T_BYTES;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * C::CHUNK + (k & 3) * 32;
@@ -825,11 +846,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                       sdesc_sw128(vb + off, 16, 1024), id_s, k > 0);
         }
         tc_commit(s_full);
+        tc_commit(v_empty + 8 * vs);  // V is read by dP only
         return true;
       };
       if (ok) ok = issue_s(0);
       for (int j = 0; j < n_tiles && ok; ++j) {
-        const int st = j & 1;
+        const int ks = j % KST;
         if (j + 1 < n_tiles && !issue_s(j + 1)) {
           ok = false;
           break;
@@ -839,14 +861,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t kb = sbase + C::OFF_K + st * C::T_BYTES;
+        const uint32_t kb = sbase + C::OFF_K + ks * C::T_BYTES;
+        const uint32_t ds = tmem + C::T_DS + (j & 1) * 64;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
-          tc_mma_bf16(tmem + C::T_DQ,
-                      sdesc_sw128(sbase + C::OFF_DS + (k >> 2) * C::CHUNK + (k & 3) * 32, 16, 1024),
-                      sdesc_sw128(kb + k * 2048, C::CHUNK, 1024), id_q, (j | k) != 0);
-        tc_commit(ds_free);
-        tc_commit(kv_empty + 8 * st);
+          tc_mma_bf16_ts(tmem + C::T_DQ, ds + 8 * k, sdesc_sw128(kb + k * 2048, C::CHUNK, 1024),
+                         id_q, (j | k) != 0);
+        tc_commit(ds_free + 8 * (j & 1));
+        tc_commit(k_empty + 8 * ks);
       }
       tc_commit(fin);
       tc_commit(drain);
@@ -863,7 +885,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t seg = ((int64_t)b * nh + h) * S_pad + qpos;
     const float l2 = qvalid ? lse2[seg] : 0.f;
     const float drow = qvalid ? Dd[seg] : 0.f;
-    uint8_t* ds_tile = smem + C::OFF_DS;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
       if (!warp_wait(s_full, j & 1, err)) {
@@ -895,15 +916,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(s_used);
-      if (j > 0 && !warp_wait(ds_free, (j - 1) & 1, err)) {
+      // dS buffer j & 1 was last read by dQ += dS K of tile j - 2
+      if (j >= 2 && !warp_wait(ds_free + 8 * (j & 1), ((j >> 1) & 1) ^ 1, err)) {
         ok = false;
         break;
       }
-#pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8)
-        *reinterpret_cast<uint4*>(ds_tile + half * C::CHUNK + sw128_offset(row, c8)) =
-            make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
-      fence_proxy_async_smem();
+      tc_fence_after();
+      // keys c0 .. c0 + 63 as bf16 pairs: columns half * 32 .. + 31 of the buffer
+      tmem_st32(tmem + lane_base + C::T_DS + (j & 1) * 64 + half * 32, pk);
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(ds_ready);
     }
