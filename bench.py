@@ -38,11 +38,11 @@ UNIT = "tokens/s"
 # DRAM traffic per tensor-core GEMM launch, from `ncu` (dram__bytes_read.sum +
 # dram__bytes_write.sum) averaged over the step's launch mix, and the source
 # it was measured on; reported only while gemm.cu is unchanged.
-GEMM_TRAFFIC_BYTES = 261122248
-GEMM_TRAFFIC_SRC_SHA = "fc348891de0434a8"
+GEMM_TRAFFIC_BYTES = 259571819
+GEMM_TRAFFIC_SRC_SHA = "86feded81900402b"
 # The same for the NF4 GEMM launches of one q4b_nf4 step.
-NF4_TRAFFIC_BYTES = 75606000
-NF4_TRAFFIC_SRC_SHA = "16a70095fa1257b0"
+NF4_TRAFFIC_BYTES = 75418272
+NF4_TRAFFIC_SRC_SHA = "86feded81900402b"
 
 
 def traffic_if_current(nbytes, sha):
