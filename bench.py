@@ -52,6 +52,31 @@ def traffic_if_current(nbytes, sha):
         return nbytes if hashlib.sha256(fh.read()).hexdigest()[:16] == sha else None
 
 
+def max_over_ranks(value, world, device="cpu"):
+    """The maximum of a rank's value over all ranks (the value itself at N = 1):
+    the slowest rank sets the job's time."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_barrier(world):
+    """All ranks reach this point before any goes on (no-op at N = 1)."""
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def job_throughput(max_seconds, world, units_per_rank):
+    """Whole-job throughput: the units every rank processed over the slowest
+    rank's time (replicas: each rank does the same work)."""
+    return world * units_per_rank / max_seconds
+
+
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -294,11 +319,8 @@ def run_rdt(args, rank, world, local_rank):
     clocks = stop_clock_sampler(clk)
     dev_ms = e0.elapsed_time(e1)
     last_loss = float(tr.loss_partials.mean())
-    t = torch.tensor([dev_ms], device=dev, dtype=torch.float64)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    max_ms = float(t.item())
-    value = world * Ts * args.steps / (max_ms / 1e3)
+    max_ms = max_over_ranks(dev_ms, world, dev)
+    value = job_throughput(max_ms / 1e3, world, Ts * args.steps)
 
     res = timer.results()
     gemm_flops = sum(f for f, _ in res)
@@ -375,6 +397,7 @@ def run_e2e(tr, shape, args, dev, world):
     xd = torch.empty(xh.shape, dtype=xh.dtype, device=dev)
     td = torch.empty(T, dtype=torch.int32, device=dev)
     kw = "ids" if tr.embedding else "x"
+    rank_barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(args.steps):
@@ -384,8 +407,8 @@ def run_e2e(tr, shape, args, dev, world):
                                                                           **{kw: xd})
         lh.copy_(loss, non_blocking=True)
     torch.cuda.synchronize()
-    dt = time.perf_counter() - t0
-    return {"value": round(world * T * args.steps / dt, 1), "unit": UNIT,
+    dt = max_over_ranks(time.perf_counter() - t0, world, dev)
+    return {"value": round(job_throughput(dt, world, T * args.steps), 1), "unit": UNIT,
             "h2d_bytes_per_step": xh.numel() * 4 + th.numel() * 4,
             "d2h_bytes_per_step": lh.numel() * 4}
 
@@ -545,11 +568,8 @@ def run_nf4(args, rank, world, local_rank):
         launches = rdt.launch_count() - l0
     clocks = stop_clock_sampler(clk)
     dev_ms = sum(a.elapsed_time(b) for a, b in evs)
-    t = torch.tensor([dev_ms], device=dev, dtype=torch.float64)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    max_ms = float(t.item())
-    value = world * T * args.steps / (max_ms / 1e3)
+    max_ms = max_over_ranks(dev_ms, world, dev)
+    value = job_throughput(max_ms / 1e3, world, T * args.steps)
 
     res = timer.results(with_kind=True)
     nf4 = [(f, ms) for f, ms, k in res if k == "nf4"]
@@ -597,6 +617,7 @@ def run_nf4(args, rank, world, local_rank):
         dyh = [d.cpu().pin_memory() for d in dys[:2]]
         sq_h = torch.empty(1, dtype=torch.float64).pin_memory()
         xd, dyd = torch.empty_like(xs[0]), torch.empty_like(dys[0])
+        rank_barrier(world)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for i in range(args.steps):
@@ -605,8 +626,8 @@ def run_nf4(args, rank, world, local_rank):
             (tr.train_step_graph if use_graph else tr.train_step)(xd, dyd)
             sq_h.copy_(tr.sumsq, non_blocking=True)
         torch.cuda.synchronize()
-        dt = time.perf_counter() - t0
-        out["e2e"] = {"value": round(world * T * args.steps / dt, 1), "unit": UNIT,
+        dt = max_over_ranks(time.perf_counter() - t0, world, dev)
+        out["e2e"] = {"value": round(job_throughput(dt, world, T * args.steps), 1), "unit": UNIT,
                       "h2d_bytes_per_step": 2 * T * shape.hidden * 4,
                       "d2h_bytes_per_step": 8}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
