@@ -156,3 +156,32 @@ def test_product_path_has_no_oracle_or_cpu_fallback():
     with open(os.path.join(pkg, "rdt.py")) as fh:
         src = fh.read()
     assert "raise ImportError" in src  # a missing library fails loudly
+
+
+def test_newer_entry_points_validate_before_any_launch(lib):
+    """The embedding, NF4 GEMM and step-counter calls reject bad arguments on
+    the host with RDT_EINVAL and a message (no device is touched)."""
+    P = ctypes.c_void_p
+
+    def einval(st, text):
+        assert st == rdt.RDT_EINVAL, st
+        assert text in lib.rdt_last_error(), lib.rdt_last_error()
+
+    einval(lib.rdt_step_advance(None, None), b"null")
+    # embedding: null ids, hidden not a multiple of 4, misaligned table, short workspace
+    einval(lib.rdt_embedding_forward(P(16), 8, 8, None, 4, P(16), None), b"null")
+    einval(lib.rdt_embedding_forward(P(16), 8, 6, P(16), 4, P(16), None), b"multiple of 4")
+    einval(lib.rdt_embedding_forward(P(20), 8, 8, P(16), 4, P(16), None), b"aligned")
+    einval(lib.rdt_embedding_backward(P(16), 4, P(16), 8, None, P(16), 8, 0, P(256), 0, None),
+           b"workspace")
+    # NF4 GEMM: a tail wider than one 64-deep step, W not a multiple of 256 columns,
+    # misaligned codes
+    einval(lib.rdt_gemm_nf4(P(16), 256, P(16), P(16), 64, 256, 0, P(16), 72, P(16), 72, 72, 8,
+                            P(16), 64, None, 0, None), b"K2")
+    einval(lib.rdt_gemm_nf4(P(16), 256, P(16), P(16), 64, 200, 0, None, 0, None, 0, 0, 8,
+                            P(16), 64, None, 0, None), b"cols % 256")
+    einval(lib.rdt_gemm_nf4(P(16), 256, P(24), P(16), 64, 256, 0, None, 0, None, 0, 0, 8,
+                            P(16), 64, None, 0, None), b"16-byte")
+    # NF4 block: rank outside {8, 16}
+    cfg = rdt.Config.from_shape(synth.WORKLOADS["q4b_nf4"])
+    einval(lib.rdt_lora_shadow(ctypes.byref(cfg), 12, P(16), P(16), None), b"rank")
