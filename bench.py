@@ -115,11 +115,20 @@ def workload_config(shape, name):
         "layers": shape.layers,
         "global_batch": shape.batch,
         "seq_len": shape.seq,
-        "params": None,
+        "params": param_count(shape),
         "optimizer": "global-norm clip 1.0 + AdamW (fp32 master, m, v)",
         "l2": "inputs larger than L2: each step streams ~150 GB of weights/grads/moments",
         "parallelism": "replicas",
     }
+
+
+def param_count(shape):
+    """Trainable parameters of the stack: every block's seven matrices and
+    four gains, the final norm gain and the LM head."""
+    s = shape
+    blk = ((s.q_dim + 2 * s.kv_dim) * s.hidden + s.hidden * s.q_dim
+           + 3 * s.intermediate * s.hidden + 2 * s.hidden + 2 * s.head_dim)
+    return s.layers * blk + s.hidden + s.vocab * s.hidden
 
 
 def load_peaks():
@@ -178,6 +187,11 @@ def stop_clock_sampler(handle):
 
 
 # ------------------------------------------------------------- CPU oracle
+# The one bounded oracle sample both the cpu_baseline leg and the reference
+# arm time (about 5 s on 16 host cores at the q4b_full shape).
+ORACLE_SAMPLE = dict(seq_tokens=1024, head_tokens=512, opt_params=1 << 25)
+
+
 class OracleSample:
     """The FP64 oracle timed on a bounded sample of one step, scaled to the
     whole step: one block forward+backward on one sequence of `seq_tokens`
@@ -358,13 +372,12 @@ def run_rdt(args, rank, world, local_rank):
         "loss_first_step": round(first_loss, 5), "loss_last_step": round(last_loss, 5),
         "launch": "one CUDA graph replay per step" if use_graph else "eager kernel launches",
     }
-    out["config"]["params"] = tr.n_params
     out["config"]["algorithmic_tflop_per_step"] = round(step_flops / 1e12, 2)
     out["config"]["activation_gb_held"] = round(tr.saved.numel() / 1e9, 2)
     if args.embedding:
         out["config"]["embedding"] = ("device lookup + deterministic scatter-add backward + "
                                       "the table's own AdamW")
-        out["config"]["params"] = tr.n_params + shape.vocab * shape.hidden
+        out["config"]["params"] = param_count(shape) + shape.vocab * shape.hidden
         out["data"] = ("synthetic (device-generated uniform token ids and targets; N(0,0.02) "
                        "random-init weights, N(0,1) embedding table)")
     if n_acc > 1:
@@ -379,7 +392,7 @@ def run_rdt(args, rank, world, local_rank):
     if not args.no_e2e:
         out["e2e"] = run_e2e(tr, shape, args, dev, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = OracleSample(shape).run()
+        out["cpu_baseline"] = OracleSample(shape, **ORACLE_SAMPLE).run()
     return out
 
 
@@ -406,6 +419,7 @@ def run_e2e(tr, shape, args, dev, world):
         loss = (tr.train_step if args.no_graph else tr.train_step_graph)(targets=td,
                                                                           **{kw: xd})
         lh.copy_(loss, non_blocking=True)
+        torch.cuda.current_stream().synchronize()  # the caller reads this step's loss
     torch.cuda.synchronize()
     dt = max_over_ranks(time.perf_counter() - t0, world, dev)
     return {"value": round(job_throughput(dt, world, T * args.steps), 1), "unit": UNIT,
@@ -439,7 +453,11 @@ def nf4_workload_config(shape, name, rank, alpha):
         "layers": shape.layers,
         "global_batch": shape.batch,
         "seq_len": shape.seq,
-        "params": None,
+        "params": rank * sum(o + i for o, i in (
+            (shape.q_dim, shape.hidden), (shape.kv_dim, shape.hidden),
+            (shape.kv_dim, shape.hidden), (shape.hidden, shape.q_dim),
+            (shape.intermediate, shape.hidden), (shape.intermediate, shape.hidden),
+            (shape.hidden, shape.intermediate))),
         "optimizer": "global-norm clip 1.0 + AdamW over the adapters (fp32 master, m, v)",
         "l2": "flushed: a 256 MB buffer is written between timed steps",
         "parallelism": "replicas",
@@ -610,7 +628,6 @@ def run_nf4(args, rank, world, local_rank):
         "clocks": clocks,
         "launch": "one CUDA graph replay per step" if use_graph else "eager kernel launches",
     }
-    out["config"]["params"] = tr.n_params
     out["config"]["algorithmic_tflop_per_step"] = round(step_flops / 1e12, 3)
     if not args.no_e2e:
         xh = [x.cpu().pin_memory() for x in xs[:2]]
@@ -712,7 +729,7 @@ def run_reference_nf4(args, world):
     from resident_decoder_trainer_gb300 import synth
     shape = synth.WORKLOADS[args.workload]
     rank_, alpha = synth.LORA["rank"], synth.LORA["alpha"]
-    sampler = Nf4OracleSample(shape, rank_, alpha, seq_tokens=256)
+    sampler = Nf4OracleSample(shape, rank_, alpha)
     samples = []
     for i in range(args.warmup + args.steps):
         r = sampler.run()
@@ -721,10 +738,15 @@ def run_reference_nf4(args, world):
     value = statistics.median(r["value"] for r in samples)
     cpu = dict(samples[-1])
     cpu["value"] = value
+    sample_ms = statistics.mean(r["sample_seconds"] for r in samples) * 1e3
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(shape.tokens / value * 1e3, 1), "higher_is_better": True,
+        "ms_per_step": round(sample_ms, 1),
+        "step": ("one bounded oracle sample (cpu_baseline.sample); value scales it to the "
+                 "whole step"),
+        "whole_step_s_extrapolated": round(shape.tokens / value, 1),
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": nf4_workload_config(shape, args.workload, rank_, alpha),
         "cpu_baseline": cpu,
@@ -740,7 +762,7 @@ def run_reference(args, rank, world):
     shape = synth.WORKLOADS[args.workload]
     if args.layers:
         shape = shape.replace(layers=args.layers)
-    sampler = OracleSample(shape, seq_tokens=256, head_tokens=64, opt_params=1 << 22)
+    sampler = OracleSample(shape, **ORACLE_SAMPLE)
     samples = []
     for i in range(args.warmup + args.steps):
         r = sampler.run()
@@ -750,10 +772,16 @@ def run_reference(args, rank, world):
     value = statistics.median(vals)
     cpu = dict(samples[-1])
     cpu["value"] = value
+    # a reference step is one bounded oracle sample; its wall time is what ran
+    sample_ms = statistics.mean(r["sample_seconds"] for r in samples) * 1e3
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(shape.tokens / value * 1e3, 1), "higher_is_better": True,
+        "ms_per_step": round(sample_ms, 1),
+        "step": ("one bounded oracle sample (cpu_baseline.sample); value scales it to the "
+                 "whole step"),
+        "whole_step_s_extrapolated": round(shape.tokens / value, 1),
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(shape, args.workload),
         "cpu_baseline": cpu,

@@ -194,26 +194,43 @@ size_t carve_block_ws(const Dims& m, int64_t B, int64_t S, void* base, BlockWs* 
   return c.off;
 }
 
+// Vocabulary columns per chunk of the LM head: the chunk's bf16 dz [T, Vc]
+// is about 64 MB (or the whole vocabulary, if smaller), so it is still in L2
+// when the dh and dW_lm GEMMs read it right after the GEMM that wrote it.
+int64_t ce_chunk_cols(int64_t T, int64_t V) {
+  int64_t vc = ((int64_t)32 << 20) / T / 256 * 256;
+  if (vc < 256) vc = 256;
+  return vc < V ? vc : V;
+}
+
 struct HeadWs {
-  bf16 *hn, *z;
+  bf16 *hn, *dz;
   float *rstd, *tgt, *lse, *dhn, *partials;
-  float2* part;
-  double* sqp;  // squared-sum slots of the dW_lm GEMM
+  float2 *part, *run;
+  int64_t vc;    // vocabulary columns per chunk
+  int part_ld;   // (max, sum exp) partials per row of one chunk
+  double* sqp;   // squared-sum slots of the dW_lm GEMMs
   float* split;  // split-K partials of dh_n
   int64_t split_floats;
 };
 size_t carve_head_ws(const Dims& m, int64_t T, void* base, HeadWs* w) {
   Carver c(base);
   HeadWs t;
+  t.vc = ce_chunk_cols(T, m.V);
+  t.part_ld = ce_partials_per_row((int)t.vc);
   t.hn = c.take<bf16>(T * m.H);
   t.rstd = c.take<float>(T);
-  t.z = c.take<bf16>(T * m.V);
-  t.part = c.take<float2>(T * ce_partials_per_row((int)m.V));
+  t.dz = c.take<bf16>(T * t.vc);
+  t.part = c.take<float2>(T * t.part_ld);
+  t.run = c.take<float2>(T);
   t.tgt = c.take<float>(T);
   t.lse = c.take<float>(T);
   t.dhn = c.take<float>(T * m.H);
   t.partials = c.take<float>(kMaxPartialRows * m.H);
-  t.sqp = c.take<double>(gemm_sq_slots_bound((int)m.V, (int)m.H));
+  int64_t slots = 0;
+  for (int64_t v0 = 0; v0 < m.V; v0 += t.vc)
+    slots += gemm_sq_slots_bound((int)std::min(t.vc, m.V - v0), (int)m.H);
+  t.sqp = c.take<double>(slots);
   t.split_floats = split_floats_for(T, m.H);
   t.split = c.take<float>(t.split_floats);
   if (w) *w = t;
@@ -794,50 +811,73 @@ rdt_status rdt_fused_cross_entropy(const rdt_config* cfg, int32_t tokens, const 
   HeadWs wk;
   carve_head_ws(m, T, ws, &wk);
   const bf16* wl = reinterpret_cast<const bf16*>(w_lm);
-  const int ntiles = ce_partials_per_row((int)m.V);
 
   RDT_CHECK_CUDA(rmsnorm_fwd(h, gamma_f, wk.hn, wk.rstd, T, (int)m.H, cfg->rms_eps, s));
-  // logits tile by tile: bf16 copy + per-tile (max, sum exp) + target logit
-  {
+  // The logits z = hn W_lm^T are never stored: each GEMM below recomputes a
+  // vocabulary chunk of them in its tensor-memory accumulator and its
+  // epilogue keeps only what the loss or the gradient needs.
+  // Forward: per-row log-sum-exp over the chunks, and the target's logit.
+  for (int64_t v0 = 0; v0 < m.V; v0 += wk.vc) {
+    const int nv = (int)std::min(wk.vc, m.V - v0);
     Epi e;
     e.kind = EPI_CE;
-    e.out = wk.z;
-    e.ld_out = m.V;
     e.part = wk.part;
-    e.part_ld = ntiles;
+    e.part_ld = wk.part_ld;
     e.targets = targets;
     e.tgt_logit = wk.tgt;
-    RDT_GEMM(Mat{wk.hn, T, m.H, m.H}, false, Mat{wl, m.V, m.H, m.H}, false, T, (int)m.V, (int)m.H,
-             e, err, s);
+    e.col_off = (int)v0;
+    RDT_GEMM(Mat{wk.hn, T, m.H, m.H}, false, Mat{wl + v0 * m.H, nv, m.H, m.H}, false, T, nv,
+             (int)m.H, e, err, s);
+    RDT_CHECK_CUDA(ce_merge(wk.part, wk.part_ld, ce_partials_per_row(nv), wk.run, v0 == 0,
+                            v0 + nv >= m.V, wk.tgt, wk.lse, loss_partials, T, s));
   }
-  RDT_CHECK_CUDA(ce_finalize(wk.part, ntiles, ntiles, wk.tgt, wk.lse, loss_partials, T, s));
-  RDT_CHECK_CUDA(ce_grad(wk.z, wk.lse, targets, loss_scale, T, (int)m.V, s));
-  // dhn = dz W_lm
-  {
-    Epi e;
-    e.kind = EPI_F32;
-    e.out = wk.dhn;
-    e.ld_out = m.H;
-    e.split_ws = wk.split;
-    e.split_ws_floats = wk.split_floats;
-    RDT_GEMM(Mat{wk.z, T, m.V, m.V}, false, Mat{wl, m.V, m.H, m.H}, true, T, (int)m.H, (int)m.V,
-             e, err, s);
-  }
-  // dW_lm = dz^T hn
+  // Backward, chunk by chunk: dz = loss_scale (softmax(z) - onehot(target))
+  // from the recomputed fp32 logits, then dhn += dz W_lm[chunk] and
+  // dW_lm[chunk] = dz^T hn.
   int64_t sq_n = 0;
-  {
-    Epi e;
-    e.kind = accumulate ? EPI_F32_RESID : EPI_F32;
-    e.out = dw_lm;
-    e.ld_out = m.H;
-    e.resid = dw_lm;
-    e.ld_resid = m.H;
-    if (grad_sq) {
-      e.sq_part = wk.sqp;
-      e.sq_count = &sq_n;
+  for (int64_t v0 = 0; v0 < m.V; v0 += wk.vc) {
+    const int nv = (int)std::min(wk.vc, m.V - v0);
+    const bf16* wc = wl + v0 * m.H;
+    {
+      Epi e;
+      e.kind = EPI_CE_GRAD;
+      e.out = wk.dz;
+      e.ld_out = wk.vc;
+      e.lse = wk.lse;
+      e.targets = targets;
+      e.col_off = (int)v0;
+      e.scale = loss_scale;
+      RDT_GEMM(Mat{wk.hn, T, m.H, m.H}, false, Mat{wc, nv, m.H, m.H}, false, T, nv, (int)m.H, e,
+               err, s);
     }
-    RDT_GEMM(Mat{wk.z, T, m.V, m.V}, true, Mat{wk.hn, T, m.H, m.H}, true, (int)m.V, (int)m.H, T, e,
-             err, s);
+    {
+      Epi e;
+      e.kind = v0 == 0 ? EPI_F32 : EPI_F32_RESID;
+      e.out = wk.dhn;
+      e.ld_out = m.H;
+      e.resid = wk.dhn;
+      e.ld_resid = m.H;
+      e.split_ws = wk.split;
+      e.split_ws_floats = wk.split_floats;
+      RDT_GEMM(Mat{wk.dz, T, nv, wk.vc}, false, Mat{wc, nv, m.H, m.H}, true, T, (int)m.H, nv, e,
+               err, s);
+    }
+    {
+      Epi e;
+      e.kind = accumulate ? EPI_F32_RESID : EPI_F32;
+      e.out = dw_lm + v0 * m.H;
+      e.ld_out = m.H;
+      e.resid = dw_lm + v0 * m.H;
+      e.ld_resid = m.H;
+      int64_t cnt = 0;
+      if (grad_sq) {
+        e.sq_part = wk.sqp + sq_n;
+        e.sq_count = &cnt;
+      }
+      RDT_GEMM(Mat{wk.dz, T, nv, wk.vc}, true, Mat{wk.hn, T, m.H, m.H}, true, nv, (int)m.H, T, e,
+               err, s);
+      sq_n += cnt;
+    }
   }
   RDT_CHECK_CUDA(rmsnorm_bwd(wk.dhn, h, wk.rstd, gamma_f, nullptr, dh, nullptr, dgamma_f,
                              wk.partials, T, (int)m.H, s, accumulate != 0));

@@ -609,12 +609,16 @@ cudaError_t cast_bf16(const float* src, bf16* dst, int64_t n, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-// -------------------------------------------------------------- CE finalise
-// lse[t] = log-sum-exp over the per-tile (max, sum exp) partials;
-// loss[t] = lse[t] - z[t, target[t]] (the target logit kept in fp32).
-__global__ void ce_finalize_kernel(const float2* __restrict__ part, int part_ld, int ntiles,
-                                   const float* __restrict__ tgt, float* __restrict__ lse,
-                                   float* __restrict__ loss, int T) {
+// ---------------------------------------------------------------- CE merge
+// The log-sum-exp of a row's logits, built chunk by chunk over the vocabulary:
+// a chunk's per-tile (max, sum exp) partials are combined around their max,
+// then folded into the running (max, sum) of the chunks before it; after the
+// last chunk lse = max + log(sum) and loss = lse - z[target] (the target's
+// logit kept in fp32 by the chunk that holds it).
+__global__ void ce_merge_kernel(const float2* __restrict__ part, int part_ld, int ntiles,
+                                float2* __restrict__ run, int first, int last,
+                                const float* __restrict__ tgt, float* __restrict__ lse,
+                                float* __restrict__ loss, int T) {
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= T) return;
@@ -626,53 +630,28 @@ __global__ void ce_finalize_kernel(const float2* __restrict__ part, int part_ld,
   for (int i = lane; i < ntiles; i += 32) s += p[i].y * __expf(p[i].x - m);
   s = warp_sum(s);
   if (lane == 0) {
-    const float l = m + logf(s);
-    lse[row] = l;
-    loss[row] = l - tgt[row];
-  }
-}
-
-cudaError_t ce_finalize(const float2* part, int part_ld, int ntiles, const float* tgt_logit,
-                        float* lse, float* loss, int T, cudaStream_t s) {
-  note_launch();
-  ce_finalize_kernel<<<(T + 7) / 8, 256, 0, s>>>(part, part_ld, ntiles, tgt_logit, lse, loss, T);
-  return cudaGetLastError();
-}
-
-// dz = (exp(z - lse) - onehot(target)) * scale, in place over the bf16 logits.
-__global__ void ce_grad_kernel(uint4* __restrict__ z, const float* __restrict__ lse,
-                               const int32_t* __restrict__ targets, float scale, int T, int V8) {
-  const int64_t n = (int64_t)T * V8;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int row = static_cast<int>(i / V8);
-    const int c0 = static_cast<int>(i % V8) * 8;
-    const float l = lse[row];
-    const int tg = targets[row];
-    uint4 v = z[i];
-    uint32_t* w = &v.x;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      float a = __expf(bf16lo(w[k]) - l);
-      float b = __expf(bf16hi(w[k]) - l);
-      if (c0 + 2 * k == tg) a -= 1.f;
-      if (c0 + 2 * k + 1 == tg) b -= 1.f;
-      w[k] = pack_bf16x2(a * scale, b * scale);
+    if (!first) {
+      const float2 r = run[row];
+      const float nm = fmaxf(r.x, m);
+      s = r.y * __expf(r.x - nm) + s * __expf(m - nm);
+      m = nm;
     }
-    z[i] = v;
+    if (last) {
+      const float l = m + logf(s);
+      lse[row] = l;
+      loss[row] = l - tgt[row];
+    } else {
+      run[row] = make_float2(m, s);
+    }
   }
 }
 
-cudaError_t ce_grad(bf16* z, const float* lse, const int32_t* targets, float scale, int T, int V,
-                    cudaStream_t s) {
-  const int V8 = V / 8;
-  const int64_t n = (int64_t)T * V8;
-  int64_t blocks = (n + 255) / 256;
-  const int64_t cap = 8LL * num_sms();
-  if (blocks > cap) blocks = cap;
+cudaError_t ce_merge(const float2* part, int part_ld, int ntiles, float2* run, bool first,
+                     bool last, const float* tgt_logit, float* lse, float* loss, int T,
+                     cudaStream_t s) {
   note_launch();
-  ce_grad_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<uint4*>(z), lse, targets, scale,
-                                                  T, V8);
+  ce_merge_kernel<<<(T + 7) / 8, 256, 0, s>>>(part, part_ld, ntiles, run, first ? 1 : 0,
+                                             last ? 1 : 0, tgt_logit, lse, loss, T);
   return cudaGetLastError();
 }
 

@@ -106,7 +106,7 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)
 //     flight while the current unit is computed in place.
 __host__ __device__ constexpr int epi_unit(int kind, uint32_t stg) {
   return kind == EPI_SWIGLU ? 32                                      // g+u, then s
-         : (kind == EPI_BF16 || kind == EPI_CE) ? (stg >= 4096 ? 32 : 16)
+         : (kind == EPI_BF16 || kind == EPI_CE || kind == EPI_CE_GRAD) ? (stg >= 4096 ? 32 : 16)
                                                : (stg >= 4096 ? 16 : 8);  // fp32; g+u in, dg+du out
 }
 __host__ __device__ constexpr int epi_elem_bytes(int kind) {
@@ -244,7 +244,10 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const OutMaps
   uint32_t r2[EPI == EPI_SWIGLU ? 32 : 1];
   float sq = 0.f;  // F32 / F32_RESID with sq_part: sum of squares of this warp's stored values
   float mx = -INFINITY, sum = 0.f;
-  const int tgt = (EPI == EPI_CE && row_ok) ? e.targets[row] : -1;
+  // the target's column within this GEMM (the logits start at vocabulary index col_off)
+  const int tgt = ((EPI == EPI_CE || EPI == EPI_CE_GRAD) && row_ok) ? e.targets[row] - e.col_off
+                                                                     : -1;
+  const float lse_row = (EPI == EPI_CE_GRAD && row_ok) ? e.lse[row] : 0.f;
 #pragma unroll 1
   for (int c = 0; c < NCH; ++c) {
     const int ccol = col_w + c * 32;
@@ -270,6 +273,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const OutMaps
         for (int j = 0; j < 32; ++j)
           if (j == tgt - ccol) e.tgt_logit[row] = __uint_as_float(r[j]);
       }
+      continue;  // statistics only: the logits are not stored
     }
 #pragma unroll
     for (int j = 0; j < UPC; ++j) {
@@ -285,6 +289,13 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const OutMaps
       if constexpr (EPI == EPI_BF16) {
 #pragma unroll
         for (int k = 0; k < UNIT; ++k) v[k] *= e.scale;
+      }
+      if constexpr (EPI == EPI_CE_GRAD) {
+        // softmax minus the target's one-hot, from the fp32 logit and the row's LSE
+        const int tc = tgt - col;
+#pragma unroll
+        for (int k = 0; k < UNIT; ++k)
+          v[k] = (__expf(v[k] - lse_row) - (k == tc ? 1.f : 0.f)) * e.scale;
       }
       if constexpr (EPI == EPI_F32) {
         // out-of-range rows and columns hold exact zeros (zero-filled operands)
@@ -314,7 +325,8 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const OutMaps
         if (lane == 0) bulk_wait_read1();
         __syncwarp();
       }
-      if constexpr (EPI == EPI_F32 || EPI == EPI_F32_RESID || EPI == EPI_BF16 || EPI == EPI_CE) {
+      if constexpr (EPI == EPI_F32 || EPI == EPI_F32_RESID || EPI == EPI_BF16 ||
+                    EPI == EPI_CE_GRAD) {
         if (col + UNIT > ncols && (ncols & (EPI == EPI_F32 || EPI == EPI_F32_RESID ? 3 : 7))) {
           // a bulk store's bounds check works in 16-byte units, so a last unit
           // whose row end is not 16-byte aligned is written with plain stores
@@ -1604,8 +1616,10 @@ static bool make_out_maps(OutMaps* om, const Epi& e, int M, int N, uint32_t stg)
       return make_box_map(&om->o1, e.out, M, N, e.ld_out, true, u) &&
              make_box_map(&om->i1, e.resid, M, N, e.ld_resid, true, u);
     case EPI_BF16:
-    case EPI_CE:
+    case EPI_CE_GRAD:
       return make_box_map(&om->o1, e.out, M, N, e.ld_out, false, u);
+    case EPI_CE:
+      return true;  // statistics only
     case EPI_SWIGLU:
       return make_box_map(&om->o1, out, M, e.half, e.ld_out, false, u) &&
              make_box_map(&om->o2, out + e.half, M, e.half, e.ld_out, false, u) &&
@@ -1620,9 +1634,16 @@ static bool make_out_maps(OutMaps* om, const Epi& e, int M, int N, uint32_t stg)
   }
 }
 
+// Multiply-add FLOPs of one launch: 2 M N K, where the SwiGLU epilogue's
+// N counts one half of the [gate | up] columns the tiles compute.
+template <int EPI>
+static double launch_flops(const GemmParams& p) {
+  return 2.0 * p.M * static_cast<double>(p.N) * p.K * (EPI == EPI_SWIGLU ? 2.0 : 1.0);
+}
+
 template <int A_MN, int B_MN, int EPI, int BN>
 static cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const OutMaps& om,
-                          const GemmParams& p, cudaStream_t s) {
+                          const GemmParams& p, cudaStream_t s, bool timed = true) {
   static bool attr_done = false;  // per instantiation; the attribute is per function
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<A_MN, B_MN, EPI, BN>,
@@ -1633,7 +1654,7 @@ static cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const Ou
   }
   const int nunits = p.m_tiles * p.n_tiles * p.splits;
   const int grid = nunits < num_sms() ? nunits : num_sms();
-  const int64_t slot = gemm_timing_before(s, 2.0 * p.M * (double)p.N * p.K, GEMM_KIND_SINGLE);
+  const int64_t slot = timed ? gemm_timing_before(s, launch_flops<EPI>(p), GEMM_KIND_SINGLE) : -1;
   note_launch();
   gemm_kernel<A_MN, B_MN, EPI, BN><<<grid, GEMM_THREADS, Tile<BN>::SMEM, s>>>(ta, tb, om, p);
   gemm_timing_after(s, slot);
@@ -1642,7 +1663,8 @@ static cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const Ou
 
 template <int A_MN, int B_MN, int EPI, int BN>
 static cudaError_t launch2(const CUtensorMap& ta, const CUtensorMap& tb, const OutMaps& om,
-                           const GemmParams& p, int max_pairs, cudaStream_t s) {
+                           const GemmParams& p, int max_pairs, cudaStream_t s,
+                           bool timed = true) {
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(gemm2_kernel<A_MN, B_MN, EPI, BN>,
@@ -1665,7 +1687,7 @@ static cudaError_t launch2(const CUtensorMap& ta, const CUtensorMap& tb, const O
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const int64_t slot = gemm_timing_before(s, 2.0 * p.M * (double)p.N * p.K, GEMM_KIND_PAIR);
+  const int64_t slot = timed ? gemm_timing_before(s, launch_flops<EPI>(p), GEMM_KIND_PAIR) : -1;
   note_launch();
   cudaError_t e = cudaLaunchKernelEx(&cfg, gemm2_kernel<A_MN, B_MN, EPI, BN>, ta, tb, om, p);
   gemm_timing_after(s, slot);
@@ -1858,12 +1880,15 @@ static cudaError_t gemm_splitk(const Mat& A, bool a_mn, const Mat& B, bool b_mn,
   p.epi = pe;
   p.err = err;
   cudaError_t e = cudaErrorInvalidValue;
-  if (!a_mn && !b_mn) e = launch<0, 0, EPI_F32, 256>(ta, tb, om, p, s);
-  else if (!a_mn && b_mn) e = launch<0, 1, EPI_F32, 256>(ta, tb, om, p, s);
-  else if (a_mn && b_mn) e = launch<1, 1, EPI_F32, 256>(ta, tb, om, p, s);
+  // the timed interval covers the K-slices and their reduce
+  const int64_t slot = gemm_timing_before(s, launch_flops<EPI_F32>(p), GEMM_KIND_SINGLE);
+  if (!a_mn && !b_mn) e = launch<0, 0, EPI_F32, 256>(ta, tb, om, p, s, false);
+  else if (!a_mn && b_mn) e = launch<0, 1, EPI_F32, 256>(ta, tb, om, p, s, false);
+  else if (a_mn && b_mn) e = launch<1, 1, EPI_F32, 256>(ta, tb, om, p, s, false);
   else *why = "gemm: unsupported operand-major combination for split-K";
-  if (e != cudaSuccess) return e;
-  return splitk_reduce(epi, splits, m_pad, ldw, M, N, s);
+  if (e == cudaSuccess) e = splitk_reduce(epi, splits, m_pad, ldw, M, N, s);
+  gemm_timing_after(s, slot);
+  return e;
 }
 
 // C = A' B'^T as `splits` K-slices on CTA-pair 256 x 256 tiles whose fp32
@@ -1909,12 +1934,15 @@ static cudaError_t gemm_splitk_pair(const Mat& A, bool a_mn, const Mat& B, bool 
   p.epi = pe;
   p.err = err;
   cudaError_t e = cudaErrorInvalidValue;
-  if (!a_mn && !b_mn) e = launch2<0, 0, EPI_F32, 256>(ta, tb, om, p, pairs_max, s);
-  else if (!a_mn && b_mn) e = launch2<0, 1, EPI_F32, 256>(ta, tb, om, p, pairs_max, s);
-  else if (a_mn && b_mn) e = launch2<1, 1, EPI_F32, 256>(ta, tb, om, p, pairs_max, s);
+  // the timed interval covers the K-slices and their reduce
+  const int64_t slot = gemm_timing_before(s, launch_flops<EPI_F32>(p), GEMM_KIND_PAIR);
+  if (!a_mn && !b_mn) e = launch2<0, 0, EPI_F32, 256>(ta, tb, om, p, pairs_max, s, false);
+  else if (!a_mn && b_mn) e = launch2<0, 1, EPI_F32, 256>(ta, tb, om, p, pairs_max, s, false);
+  else if (a_mn && b_mn) e = launch2<1, 1, EPI_F32, 256>(ta, tb, om, p, pairs_max, s, false);
   else *why = "gemm: unsupported operand-major combination for split-K";
-  if (e != cudaSuccess) return e;
-  return splitk_reduce(epi, splits, m_pad, ldw, M, N, s);
+  if (e == cudaSuccess) e = splitk_reduce(epi, splits, m_pad, ldw, M, N, s);
+  gemm_timing_after(s, slot);
+  return e;
 }
 
 cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N, int K,
@@ -2058,15 +2086,21 @@ cudaError_t gemm(const Mat& A, bool a_mn, const Mat& B, bool b_mn, int M, int N,
   RDT_GEMM2_CASE(0, 0, EPI_F32_RESID, 256)
   RDT_GEMM2_CASE(0, 0, EPI_SWIGLU, 256)
   RDT_GEMM2_CASE(0, 0, EPI_CE, 256)
+  RDT_GEMM_CASE(0, 0, EPI_CE_GRAD, 256)
+  RDT_GEMM_CASE(0, 0, EPI_CE_GRAD, 192)
+  RDT_GEMM2_CASE(0, 0, EPI_CE_GRAD, 256)
   // activation gradients dX = dY W: A K-major, B MN-major
   RDT_GEMM_CASE(0, 1, EPI_BF16, 256)
   RDT_GEMM_CASE(0, 1, EPI_BF16, 192)
   RDT_GEMM_CASE(0, 1, EPI_F32, 256)
   RDT_GEMM_CASE(0, 1, EPI_F32, 192)
+  RDT_GEMM_CASE(0, 1, EPI_F32_RESID, 256)  // the LM head's dh, summed over vocabulary chunks
+  RDT_GEMM_CASE(0, 1, EPI_F32_RESID, 192)
   RDT_GEMM_CASE(0, 1, EPI_SWIGLU_BWD, 256)
   RDT_GEMM_CASE(0, 1, EPI_SWIGLU_BWD, 192)
   RDT_GEMM2_CASE(0, 1, EPI_BF16, 256)
   RDT_GEMM2_CASE(0, 1, EPI_F32, 256)
+  RDT_GEMM2_CASE(0, 1, EPI_F32_RESID, 256)
   RDT_GEMM2_CASE(0, 1, EPI_SWIGLU_BWD, 256)
   // weight gradients dW = dY^T X: A MN-major, B MN-major
   RDT_GEMM_CASE(1, 1, EPI_F32, 256)
@@ -2113,7 +2147,7 @@ static bool make_f32_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t 
 template <int B_MN, int EPI>
 static cudaError_t launch_nf4_pair(const CUtensorMap& ta, const CUtensorMap& tb2,
                                    const Nf4Maps& nm, const OutMaps& om, const GemmParams& p,
-                                   int max_pairs, cudaStream_t s) {
+                                   int max_pairs, cudaStream_t s, bool timed = true) {
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(gemm2_nf4_kernel<B_MN, EPI>,
@@ -2136,7 +2170,7 @@ static cudaError_t launch_nf4_pair(const CUtensorMap& ta, const CUtensorMap& tb2
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const int64_t slot = gemm_timing_before(s, 2.0 * p.M * (double)p.N * p.K, GEMM_KIND_NF4);
+  const int64_t slot = timed ? gemm_timing_before(s, launch_flops<EPI>(p), GEMM_KIND_NF4) : -1;
   note_launch();
   cudaError_t e = cudaLaunchKernelEx(&cfg, gemm2_nf4_kernel<B_MN, EPI>, ta, tb2, nm, om, p);
   gemm_timing_after(s, slot);
@@ -2174,7 +2208,8 @@ static int max_active_nf4_pairs() {
 
 template <int B_MN, int EPI>
 static cudaError_t launch_nf4(const CUtensorMap& ta, const CUtensorMap& tb2, const Nf4Maps& nm,
-                              const OutMaps& om, const GemmParams& p, cudaStream_t s) {
+                              const OutMaps& om, const GemmParams& p, cudaStream_t s,
+                              bool timed = true) {
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(gemm_nf4_kernel<B_MN, EPI>,
@@ -2185,7 +2220,7 @@ static cudaError_t launch_nf4(const CUtensorMap& ta, const CUtensorMap& tb2, con
   }
   const int ntiles = p.m_tiles * p.n_tiles;
   const int grid = ntiles < num_sms() ? ntiles : num_sms();
-  const int64_t slot = gemm_timing_before(s, 2.0 * p.M * (double)p.N * p.K, GEMM_KIND_NF4);
+  const int64_t slot = timed ? gemm_timing_before(s, launch_flops<EPI>(p), GEMM_KIND_NF4) : -1;
   note_launch();
   gemm_nf4_kernel<B_MN, EPI><<<grid, NF4_THREADS, TileN4::SMEM, s>>>(ta, tb2, nm, om, p);
   gemm_timing_after(s, slot);
@@ -2317,10 +2352,14 @@ cudaError_t gemm_nf4(const Mat& A, const Nf4Mat& W, bool b_mn, const Mat* A2, co
         return cudaErrorInvalidValue;
       }
       p.epi = pe;
-      const cudaError_t e = b_mn ? launch_nf4_pair<1, EPI_F32>(ta, tb2, nm, oms, p, pairs_max, s)
-                                 : launch_nf4_pair<0, EPI_F32>(ta, tb2, nm, oms, p, pairs_max, s);
-      if (e != cudaSuccess) return e;
-      return splitk_reduce(epi, p.splits, m_pad, ldw, M, N, s);
+      // the timed interval covers the K-slices and their reduce
+      const int64_t slot = gemm_timing_before(s, launch_flops<EPI_F32>(p), GEMM_KIND_NF4);
+      cudaError_t e =
+          b_mn ? launch_nf4_pair<1, EPI_F32>(ta, tb2, nm, oms, p, pairs_max, s, false)
+               : launch_nf4_pair<0, EPI_F32>(ta, tb2, nm, oms, p, pairs_max, s, false);
+      if (e == cudaSuccess) e = splitk_reduce(epi, p.splits, m_pad, ldw, M, N, s);
+      gemm_timing_after(s, slot);
+      return e;
     }
   }
 #define RDT_NF4_CASE(BMJ, E)                                                   \

@@ -17,7 +17,9 @@ enum EpiKind : int {
   EPI_F32_RESID = 2,   // out(f32)[r, c] = resid[r, c] + acc
   EPI_SWIGLU = 3,      // B = [Wg; Wu]: gu[r, c] = g, gu[r, half + c] = u, out2[r, c] = silu(g) u
   EPI_SWIGLU_BWD = 4,  // acc = ds: out[r, c] = dg, out[r, half + c] = du from aux = gu
-  EPI_CE = 5,          // acc = logits: out(bf16) = z, part[r, 2*tile+half] = (max, sum exp), tgt_logit
+  // acc = logits of vocabulary columns col_off + c:
+  EPI_CE = 5,       // part[r, 2*tile+half] = (max, sum exp), tgt_logit[r] if the target is here
+  EPI_CE_GRAD = 6,  // out(bf16) = scale * (exp(z - lse[r]) - [col_off + c == targets[r]])
 };
 
 struct Epi {
@@ -41,8 +43,11 @@ struct Epi {
   // x 8 or 16; or the split-K reduce's blocks).
   double* sq_part = nullptr;
   int64_t* sq_count = nullptr;
-  // EPI_BF16 only: out = bf16(scale * acc)
+  // EPI_BF16: out = bf16(scale * acc); EPI_CE_GRAD: the loss scale
   float scale = 1.0f;
+  // EPI_CE_GRAD: per-row log-sum-exp; EPI_CE / EPI_CE_GRAD: vocabulary index of column 0
+  const float* lse = nullptr;
+  int col_off = 0;
   // F32 / F32_RESID / BF16: fp32 scratch gemm() may use to split K across CTAs when the
   // problem has too few output tiles to fill the GPU (split_ws_floats floats,
   // 16-byte aligned); the partials are summed in a fixed order.
@@ -159,10 +164,12 @@ cudaError_t embedding_backward(const int32_t* ids, int T, const float* dx, int H
                                const float* scale, float* dtable, int64_t V, bool accumulate,
                                void* ws, cudaStream_t s);
 
-cudaError_t ce_finalize(const float2* part, int part_ld, int ntiles, const float* tgt_logit,
-                        float* lse, float* loss, int T, cudaStream_t s);
-cudaError_t ce_grad(bf16* z, const float* lse, const int32_t* targets, float scale, int T, int V,
-                    cudaStream_t s);
+// Folds one vocabulary chunk's per-tile (max, sum exp) partials [T, part_ld]
+// (ntiles used) into the running per-row statistics run[T]; the first chunk
+// starts them, the last writes lse[T] and loss[T] = lse - tgt_logit.
+cudaError_t ce_merge(const float2* part, int part_ld, int ntiles, float2* run, bool first,
+                     bool last, const float* tgt_logit, float* lse, float* loss, int T,
+                     cudaStream_t s);
 
 cudaError_t sq_sum(const float* const* bufs, const int64_t* lens, int nbuf, double* out,
                    double* partials, int max_partials, cudaStream_t s);
