@@ -399,6 +399,19 @@ rdt_status rdt_embedding_backward(const int32_t* ids, int32_t tokens, const floa
 /* Thread-local description of the last failure on this thread ("" if none). */
 const char* rdt_last_error(void);
 
+/* Test hook for the bounded device waits (the error path the tensor-core
+ * kernels take when a wait gives up; cuda_trainer.rs train_step_inner
+ * reports a poisoned CUDA context after a device failure, which these bounds
+ * avoid). Launches one warp on `stream` that holds 32 tensor-memory columns,
+ * waits on an mbarrier with a limit of limit_ns nanoseconds (in [1e3, 1e10]),
+ * then frees the columns and returns whatever the outcome. arrive != 0: the
+ * warp arrives on the barrier first, so the wait completes at once;
+ * arrive == 0: nothing arrives, the wait gives up after limit_ns and records
+ * RDT_ETIMEOUT in the device error word (read it with rdt_device_error).
+ * waited_ns: optional device uint64 that receives the wait's duration.
+ * RDT_EINVAL for an out-of-range limit or a misaligned waited_ns. */
+rdt_status rdt_wait_probe(int64_t limit_ns, int32_t arrive, uint64_t* waited_ns, void* stream);
+
 /* Synchronises the current device, then reads and clears the device error
  * word of the current device (0 = none, else an rdt_status such as
  * RDT_ETIMEOUT). Writes it to *code (host). */

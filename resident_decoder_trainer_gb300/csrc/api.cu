@@ -1045,6 +1045,19 @@ rdt_status rdt_cast_bf16(const float* src, rdt_bf16* dst, int64_t n, void* strea
   return RDT_OK;
 }
 
+rdt_status rdt_wait_probe(int64_t limit_ns, int32_t arrive, uint64_t* waited_ns, void* stream) {
+  if (limit_ns < 1000 || limit_ns > 10000000000LL)
+    return fail(RDT_EINVAL, "limit_ns must be in [1 us, 10 s]");
+  if (waited_ns && (reinterpret_cast<uintptr_t>(waited_ns) & 7))
+    return fail(RDT_EINVAL, "waited_ns must be 8-byte aligned");
+  int* err = device_error_ptr();
+  if (!err) return fail(RDT_ECUDA, "device error word not available");
+  RDT_CHECK_CUDA(wait_probe(err, static_cast<uint64_t>(limit_ns), arrive != 0,
+                            reinterpret_cast<unsigned long long*>(waited_ns),
+                            static_cast<cudaStream_t>(stream)));
+  return RDT_OK;
+}
+
 rdt_status rdt_device_error(int32_t* code) {
   if (!code) return fail(RDT_EINVAL, "null pointer");
   RDT_CHECK_CUDA(cudaDeviceSynchronize());

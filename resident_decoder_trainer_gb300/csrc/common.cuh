@@ -87,13 +87,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait for the phase of parity `parity` to complete. Returns false
-// (and records kErrTimeout) if it has not after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err) {
+// (and records kErrTimeout) if it has not after limit_ns (the kernels use
+// kWaitLimitNs; the wait probe passes its own).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       record_error(err, kErrTimeout);
       return false;
     }
@@ -103,8 +105,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* er
 // Warp-uniform bounded wait: every lane waits, and the warp proceeds only if
 // all lanes saw the phase complete (so warp-collective tcgen05 accesses that
 // follow are never executed by a partial warp).
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* err) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, err));
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* err,
+                                          uint64_t limit_ns = kWaitLimitNs) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, err, limit_ns));
 }
 
 // ----------------------------------------------------------------------- TMA

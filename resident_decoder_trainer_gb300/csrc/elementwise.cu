@@ -655,6 +655,45 @@ cudaError_t ce_merge(const float2* part, int part_ld, int ntiles, float2* run, b
   return cudaGetLastError();
 }
 
+// --------------------------------------------------------------- wait probe
+// The bounded-wait error path of the tensor-core kernels, in one warp: it
+// holds 32 TMEM columns, waits on an mbarrier (phase 0, one expected arrival)
+// with the given limit, and whatever the wait's outcome frees the columns and
+// returns. With `arrive` unset nothing ever arrives, so the wait gives up,
+// records kErrTimeout in err and the kernel still exits cleanly.
+__global__ void __launch_bounds__(32) wait_probe_kernel(int* err, uint64_t limit_ns, int arrive,
+                                                        unsigned long long* waited_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t tmem_base;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  tmem_alloc(smem_u32(&tmem_base), 32);
+  tc_fence_before();
+  __syncwarp();
+  tc_fence_after();
+  const uint32_t taddr = tmem_base;
+  if (arrive && threadIdx.x == 0) mbar_arrive(b);
+  __syncwarp();
+  const uint64_t t0 = global_timer_ns();
+  warp_wait(b, 0, err, limit_ns);
+  if (threadIdx.x == 0 && waited_ns) *waited_ns = global_timer_ns() - t0;
+  tc_fence_before();
+  __syncwarp();
+  tc_fence_after();
+  tmem_dealloc(taddr, 32);
+}
+
+cudaError_t wait_probe(int* err, uint64_t limit_ns, bool arrive, unsigned long long* waited_ns,
+                       cudaStream_t s) {
+  note_launch();
+  wait_probe_kernel<<<1, 32, 0, s>>>(err, limit_ns, arrive ? 1 : 0, waited_ns);
+  return cudaGetLastError();
+}
+
 // -------------------------------------------------------------- squared sum
 constexpr int kMaxBufs = 64;
 struct BufTable {

@@ -171,6 +171,13 @@ cudaError_t ce_merge(const float2* part, int part_ld, int ntiles, float2* run, b
                      bool last, const float* tgt_logit, float* lse, float* loss, int T,
                      cudaStream_t s);
 
+// One-warp kernel that waits on an mbarrier with limit_ns (arrived on first
+// when `arrive`), holding and then freeing 32 TMEM columns; a wait that gives
+// up records the timeout code in *err. waited_ns (device, nullable) receives
+// the wait's duration.
+cudaError_t wait_probe(int* err, uint64_t limit_ns, bool arrive, unsigned long long* waited_ns,
+                       cudaStream_t s);
+
 cudaError_t sq_sum(const float* const* bufs, const int64_t* lens, int nbuf, double* out,
                    double* partials, int max_partials, cudaStream_t s);
 cudaError_t clip_scale(const double* sumsq, float max_norm, float* scale, int32_t* nonfinite,

@@ -32,7 +32,7 @@ EXPORTS = (
     "rdt_nf4_scale_count", "rdt_nf4_offsets", "rdt_lora_param_count", "rdt_lora_param_offsets",
     "rdt_lora_shadow_count", "rdt_lora_shadow", "rdt_nf4_saved_bytes", "rdt_nf4_workspace_bytes",
     "rdt_nf4_block_forward", "rdt_nf4_block_backward", "rdt_embedding_workspace_bytes",
-    "rdt_embedding_forward", "rdt_embedding_backward", "rdt_step_advance",
+    "rdt_embedding_forward", "rdt_embedding_backward", "rdt_step_advance", "rdt_wait_probe",
 )
 
 
@@ -84,6 +84,7 @@ def _load() -> ctypes.CDLL:
         "rdt_cast_bf16": (I32, [P, P, I64, P]),
         "rdt_last_error": (ctypes.c_char_p, []),
         "rdt_device_error": (I32, [P]),
+        "rdt_wait_probe": (I32, [I64, I32, P, P]),
         "rdt_gemm_timing_arm": (I32, [P, P, P, I32]),
         "rdt_gemm_timing_disarm": (I64, []),
         "rdt_launch_count": (I64, []),
@@ -364,6 +365,13 @@ def embedding_backward(ids, dx, dtable, ws, scale=None, accumulate=False, stream
 def cast_bf16(src, dst, n=None, stream=None):
     n = src.numel() if n is None else n
     _check(lib().rdt_cast_bf16(_ptr(src), _ptr(dst), n, _stream(stream)))
+
+
+def wait_probe(limit_ns, arrive, waited=None, stream=None):
+    """One warp waits on an mbarrier for at most limit_ns (see rdt_wait_probe);
+    waited: optional int64 device tensor of one element for the duration."""
+    _check(lib().rdt_wait_probe(int(limit_ns), 1 if arrive else 0,
+                                None if waited is None else _ptr(waited), _stream(stream)))
 
 
 def device_error() -> int:

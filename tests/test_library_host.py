@@ -191,3 +191,14 @@ def test_newer_entry_points_validate_before_any_launch(lib):
     # NF4 block: rank outside {8, 16}
     cfg = rdt.Config.from_shape(synth.WORKLOADS["q4b_nf4"])
     einval(lib.rdt_lora_shadow(ctypes.byref(cfg), 12, P(16), P(16), None), b"rank")
+
+
+def test_wait_probe_validates_its_limit_before_any_launch(lib):
+    """The bounded-wait test hook rejects limits outside [1 us, 10 s] and a
+    misaligned duration pointer on the host (no device is touched)."""
+    P = ctypes.c_void_p
+    for bad in (0, 999, 10_000_000_001):
+        assert lib.rdt_wait_probe(bad, 1, None, None) == rdt.RDT_EINVAL
+        assert b"limit_ns" in lib.rdt_last_error()
+    assert lib.rdt_wait_probe(1_000_000, 0, P(12), None) == rdt.RDT_EINVAL
+    assert b"aligned" in lib.rdt_last_error()
