@@ -59,6 +59,11 @@ class Nf4LoraTrainer:
         self.step_dev = torch.zeros(1, dtype=torch.int32, device=dev)  # AdamW's step count
         self.step_count = 0
         self.graph = None
+        # rdt_sq_sum_noalloc looks up the device address of its static
+        # scratch on its first call on a device; make that call now, on the
+        # trainer's device, so that no later call (a captured step's) does it
+        with torch.cuda.device(dev):
+            rdt.sq_sum_noalloc([self.scale], self.sumsq)
 
     # ------------------------------------------------------------- views
     def adapter(self, name):

@@ -114,6 +114,12 @@ class DecoderTrainer:
             self.emb_sumsq = torch.zeros(1, dtype=torch.float64, device=dev)
             self.emb_scale = torch.ones(1, **f32)
             self.emb_nonfinite = torch.zeros(1, dtype=torch.int32, device=dev)
+            # rdt_sq_sum_noalloc looks up the device address of its static
+            # scratch on its first call on a device; make that call now, on
+            # the trainer's device, so that no later call (a captured step's)
+            # does it
+            with torch.cuda.device(dev):
+                rdt.sq_sum_noalloc([self.emb_scale], self.emb_sumsq)
         self.step_count = 0
 
     # -------------------------------------------------------------- views
