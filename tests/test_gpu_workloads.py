@@ -1,10 +1,25 @@
 """Parity of the CUDA path with the FP64 oracle at the full sizes of every
-workload the step is defined on (slow: each case runs the oracle on up to a
-few TFLOP of fp64 work). Where the oracle cannot redo a whole full-size step,
-it checks outputs it can compute one by one (loss partials of sequence
-prefixes, which causality makes exact) and properties that hold at any size
-(the squared sum and clip scale over all 4.02 B gradients, AdamW on sampled
-elements given the same gradients)."""
+workload the step is defined on (slow: the oracle runs up to ~100 TFLOP of
+fp64 work on the host cores).
+
+The oracle always takes the same seeded fp32 inputs as the GPU (the fp32
+master weights, not their bf16 copies), and the bounds are the stated ones:
+loss relative error 1e-3 (each token's loss partial, and the mean), per-tensor
+gradient relative L2 1e-2, AdamW updated weights 1e-5 given identical
+gradients.
+
+Gradients at depth. The GPU computes with bf16 copies of the weights and of
+every contraction operand (fp32 accumulation), the precision scheme the step
+is specified with. A stack of blocks amplifies those roundings: measured
+against an fp32 reference on the GPU, rounding only the weights of the
+36-block Qwen3-4B stack to bf16 (every other value exact) already moves its
+gradients by 2-3 %, and the whole scheme by 4.2 % (8 blocks of the small
+workload: 1.1 %); one block stays below 1 %. Where a workload's gradients
+cannot meet 1e-2 under that scheme, the test keeps the 1e-2 bound and is
+marked as an expected failure (strict: it fails if the bound is ever met),
+with the measured floor in its reason. The same gradients are also compared,
+as a diagnostic, with the oracle evaluated at the bf16 weights the GPU
+multiplies by."""
 import math
 
 import numpy as np
@@ -28,35 +43,58 @@ def _built():
     assert rdt.device_error() == 0
 
 
-def _check_grads(tr, ref_grads, tol=GRAD_REL_L2):
+def _grad_errors(tr, ref_grads):
     errs = {key: rel_l2(to_np(tr.tensor(tr.g, *key)), gref) for key, gref in ref_grads.items()}
     worst = max(errs, key=errs.get)
     print(f"worst per-tensor gradient rel L2: {errs[worst]:.3e} at {worst}")
+    return errs
+
+
+def _assert_grads(errs, tol=GRAD_REL_L2):
     for key, err in errs.items():
         assert err < tol, f"{key}: rel L2 {err:.3e}"
-    return errs[worst]
+
+
+def _assert_loss(lp, ref, per_token=True):
+    """The mean loss, and (per_token) every token's loss partial, within 1e-3
+    (relative)."""
+    lp = np.asarray(lp, dtype=np.float64)
+    assert abs(lp.mean() - ref["loss"]) / ref["loss"] < LOSS_REL
+    if per_token:
+        want = np.asarray(ref["loss_partials"], dtype=np.float64)
+        assert np.max(np.abs(lp - want) / np.abs(want)) < LOSS_REL
+
+
+def _depth_floor(measured):
+    """Expected failure of a stated bound that the bf16-operand scheme cannot
+    meet at this depth (strict: an unexpected pass fails)."""
+    return pytest.mark.xfail(
+        strict=True,
+        reason=("bf16 GEMM operands, amplified through the stacked blocks, put the "
+                f"gradients at {measured} from the fp64 oracle on the fp32 masters; "
+                "rounding only the weights to bf16, every other value exact, moves them "
+                "by most of that already"))
 
 
 def _bf16(a):
-    """The bf16 operand copy the GPU computes with (round to nearest even)."""
+    """The bf16 copy the GPU multiplies by (round to nearest even)."""
     t = a if isinstance(a, torch.Tensor) else torch.from_numpy(np.asarray(a, dtype=np.float32))
     return t.float().to(torch.bfloat16).double().numpy()
 
 
 def _operand_model(blocks, head):
-    """Matrices as the bf16 operands the GPU's GEMMs read; gains stay fp32
-    (the norms read the fp32 masters)."""
+    """Matrices as the bf16 operands the GPU's GEMMs read; gains stay fp32."""
     ob = [{k: (_bf16(v) if not k.startswith("g_") else om._f64(v)) for k, v in p.items()}
           for p in blocks]
     oh = {"g_final": om._f64(head["g_final"]), "w_lm": _bf16(head["w_lm"])}
     return ob, oh
 
 
-def _oracle_step(blocks, head, x, tg, shape, state, step):
-    """Oracle gradients of the model the GPU evaluates (bf16 operand weights),
-    then the global clip and AdamW applied to the fp32 masters."""
-    ob, oh = _operand_model(blocks, head)
-    res, bgrads = om.model_forward_backward(ob, oh, x, tg, shape)
+def _oracle_step(blocks, head, x, tg, shape, state, step, operand_weights=False):
+    """Oracle gradients on the same fp32 inputs (or, as a diagnostic, at the
+    bf16 operand weights), then the global clip and AdamW on the fp32 masters."""
+    wb, wh = _operand_model(blocks, head) if operand_weights else (blocks, head)
+    res, bgrads = om.model_forward_backward(wb, wh, x, tg, shape)
     grads = {}
     for i, g in enumerate(bgrads):
         for k, v in g.items():
@@ -93,8 +131,21 @@ def _state_from_gpu(tr, shape):
     return blocks, head, state
 
 
+def _adamw_given(tr, ref):
+    """AdamW on the GPU fed the oracle's gradients: updated weights within 1e-5."""
+    for key, gref in ref["grads"].items():
+        tr.tensor(tr.g, *key).copy_(torch.from_numpy(gref).float())
+    tr.sumsq.fill_(float(ref["norm"]) ** 2)
+    tr.clip_and_update()
+    torch.cuda.synchronize()
+    assert abs(float(tr.scale) - ref["scale"]) / ref["scale"] < 1e-6
+    for key, wref in ref["params"].items():
+        assert rel_l2(to_np(tr.tensor(tr.w, *key)), wref) < ADAMW_REL, key
+
+
 # ------------------------------------------------------------------- small
-def test_small_workload_first_step():
+@pytest.fixture(scope="module")
+def small_first_step():
     shape = synth.WORKLOADS["small"]
     blocks, head, x, tg = synth.make_model_inputs(shape, seed=0)
     ref = _oracle_step(blocks, head, x, tg.numpy(), shape, None, 1)
@@ -102,17 +153,31 @@ def test_small_workload_first_step():
     tr.load(blocks, head)
     loss = tr.forward_backward(x.cuda(), tg.cuda())
     torch.cuda.synchronize()
-    assert abs(float(loss.double().mean()) - ref["loss"]) / ref["loss"] < LOSS_REL
-    _check_grads(tr, ref["grads"])
-    for key, gref in ref["grads"].items():  # AdamW given identical gradients
-        tr.tensor(tr.g, *key).copy_(torch.from_numpy(gref).float())
-    tr.clip_and_update()
-    torch.cuda.synchronize()
-    for key, wref in ref["params"].items():
-        assert rel_l2(to_np(tr.tensor(tr.w, *key)), wref) < ADAMW_REL, key
+    errs = _grad_errors(tr, ref["grads"])
+    diag = _oracle_step(blocks, head, x, tg.numpy(), shape, None, 1, operand_weights=True)
+    errs_op = _grad_errors(tr, diag["grads"])
+    return dict(tr=tr, ref=ref, lp=to_np(loss), errs=errs, errs_op=errs_op)
 
 
-def test_small_workload_ten_steps():
+def test_small_workload_first_step_loss_and_adamw(small_first_step):
+    r = small_first_step
+    _assert_loss(r["lp"], r["ref"])
+    _adamw_given(r["tr"], r["ref"])
+
+
+@_depth_floor("1.10 % worst (layer 4 g_k; 8 blocks)")
+def test_small_workload_first_step_gradients(small_first_step):
+    _assert_grads(small_first_step["errs"])
+
+
+def test_small_workload_first_step_gradients_at_operand_weights(small_first_step):
+    """Diagnostic: the oracle's exact gradients of the model the GPU
+    evaluates (its bf16 operand weights)."""
+    _assert_grads(small_first_step["errs_op"])
+
+
+@pytest.fixture(scope="module")
+def small_tenth_step():
     """Ten full steps on new batches; the tenth is checked against the oracle
     started from the GPU's own state after nine updates."""
     shape = synth.WORKLOADS["small"]
@@ -123,116 +188,144 @@ def test_small_workload_ten_steps():
     for step in range(1, 10):
         x, tg = synth.draw_batch(shape, synth.make_generator(step))
         losses.append(float(tr.train_step(x.cuda(), tg.cuda()).double().mean()))
-    assert all(math.isfinite(v) for v in losses)
-    assert all(abs(v - math.log(shape.vocab)) < 1.0 for v in losses)
     b_np, h_np, state = _state_from_gpu(tr, shape)
     x, tg = synth.draw_batch(shape, synth.make_generator(10))
     ref = _oracle_step(b_np, h_np, x, tg.numpy(), shape, state, 10)
     loss = tr.forward_backward(x.cuda(), tg.cuda())
     torch.cuda.synchronize()
-    assert abs(float(loss.double().mean()) - ref["loss"]) / ref["loss"] < LOSS_REL
-    _check_grads(tr, ref["grads"])
-    for key, gref in ref["grads"].items():
-        tr.tensor(tr.g, *key).copy_(torch.from_numpy(gref).float())
-    tr.clip_and_update()
-    assert tr.step_count == 10
-    torch.cuda.synchronize()
-    for key, wref in ref["params"].items():
-        assert rel_l2(to_np(tr.tensor(tr.w, *key)), wref) < ADAMW_REL, key
+    errs = _grad_errors(tr, ref["grads"])
+    return dict(tr=tr, ref=ref, lp=to_np(loss), errs=errs, losses=losses, shape=shape)
+
+
+def test_small_workload_ten_steps_loss_and_adamw(small_tenth_step):
+    r = small_tenth_step
+    assert all(math.isfinite(v) for v in r["losses"])
+    assert all(abs(v - math.log(r["shape"].vocab)) < 1.0 for v in r["losses"])
+    _assert_loss(r["lp"], r["ref"])
+    _adamw_given(r["tr"], r["ref"])
+    assert r["tr"].step_count == 10
+
+
+@_depth_floor("1.33 % worst (layer 5 g_k; 8 blocks, tenth step)")
+def test_small_workload_ten_steps_gradients(small_tenth_step):
+    _assert_grads(small_tenth_step["errs"])
 
 
 # --------------------------------------------------------------- q4b block
 def test_q4b_block_forward_backward():
     shape = synth.WORKLOADS["q4b_block"]
     blk, x, dy = synth.make_block_inputs(shape, seed=0)
-    (ob,), _ = _operand_model([blk], {"g_final": np.ones(1), "w_lm": np.zeros((1, 1))})
-    y_ref, cache = om.block_forward(ob, x, shape)
-    dx_ref, g_ref = om.block_backward(cache, dy, shape)
     y, dx, g = gpu_block(shape, blk, x, dy)
     x64 = to_np(x)
-    errs = {name: rel_l2(to_np(g[name]), g_ref[name]) for name in g_ref}
-    print("q4b block: y-x %.3e dx %.3e " % (rel_l2(to_np(y) - x64, y_ref - x64),
-                                            rel_l2(to_np(dx), dx_ref)) +
-          " ".join(f"{k}:{v:.3e}" for k, v in errs.items()))
-    assert rel_l2(to_np(y) - x64, y_ref - x64) < FWD_REL_L2
-    assert rel_l2(to_np(dx), dx_ref) < GRAD_REL_L2
-    for name, err in errs.items():
-        assert err < GRAD_REL_L2, f"{name}: rel L2 {err:.3e}"
+    for operand_weights in (False, True):
+        p = _operand_model([blk], {"g_final": np.ones(1), "w_lm": np.zeros((1, 1))})[0][0] \
+            if operand_weights else blk
+        y_ref, cache = om.block_forward(p, x, shape)
+        dx_ref, g_ref = om.block_backward(cache, dy, shape)
+        errs = {name: rel_l2(to_np(g[name]), g_ref[name]) for name in g_ref}
+        print(("operand weights " if operand_weights else "fp32 masters ") +
+              "q4b block: y-x %.3e dx %.3e " % (rel_l2(to_np(y) - x64, y_ref - x64),
+                                                rel_l2(to_np(dx), dx_ref)) +
+              " ".join(f"{k}:{v:.3e}" for k, v in errs.items()))
+        assert rel_l2(to_np(y) - x64, y_ref - x64) < FWD_REL_L2
+        assert rel_l2(to_np(dx), dx_ref) < GRAD_REL_L2
+        for name, err in errs.items():
+            assert err < GRAD_REL_L2, f"{name}: rel L2 {err:.3e}"
 
 
 # ---------------------------------------------------------------- q4b full
+C4_BLOCKS = (0, 17, 35)
+
+
+def _oracle_q4b_full(blocks, head, x, tg, shape, keep):
+    """The oracle's full step, layer by layer: the forward keeps only each
+    layer's input; the backward re-runs a layer's forward from its input
+    before its backward (the same oracle functions, in the same order of
+    operations as model_forward_backward). Returns the loss partials, the
+    gradients of the blocks in `keep` and of the head, and the sum of the
+    squares of every gradient."""
+    h = om._f64(x)
+    inputs = []
+    for p in blocks:
+        inputs.append(h)
+        h, _ = om.block_forward(p, h, shape)
+    res = om.head_forward_backward(h, head["g_final"], head["w_lm"], tg, shape)
+    grads = {("head", "g_final"): res["g_final"], ("head", "w_lm"): res["w_lm"]}
+    sq = [om.squared_sum(res["g_final"]), om.squared_sum(res["w_lm"])]
+    dh = res["dh"]
+    for li in reversed(range(len(blocks))):
+        _, cache = om.block_forward(blocks[li], inputs[li], shape)
+        dh, g = om.block_backward(cache, dh, shape)
+        del cache
+        sq += [om.squared_sum(v) for v in g.values()]
+        if li in keep:
+            for k, v in g.items():
+                grads[(li, k)] = v
+    return dict(loss=res["loss"], loss_partials=res["loss_partials"], grads=grads,
+                sumsq=float(np.sum(sq)))
+
+
 @pytest.fixture(scope="module")
-def q4b_full_inputs():
+def q4b_full_step():
     shape = synth.WORKLOADS["q4b_full"]
     blocks, head, x, tg = synth.make_model_inputs(shape, seed=0)
-    return shape, blocks, head, x, tg
-
-
-def test_q4b_full_step_at_full_size(q4b_full_inputs):
-    """The whole 36-block, 4096-token step on the GPU. The oracle checks the
-    loss partials of the first 16 tokens of every sequence (exact by
-    causality), the squared sum and clip scale over all 4.02 B gradients, and
-    AdamW on a million sampled elements."""
-    shape, blocks, head, x, tg = q4b_full_inputs
     tr = DecoderTrainer(shape)
     tr.load(blocks, head)
     loss = tr.forward_backward(x.cuda(), tg.cuda())
     torch.cuda.synchronize()
-    lp = to_np(loss)
-    assert np.all(np.isfinite(lp))
-    # prefixes of every sequence through all 36 blocks and the head
-    P = 16
-    pshape = shape.replace(seq=P)
-    rows = np.concatenate([np.arange(b * shape.seq, b * shape.seq + P) for b in range(shape.batch)])
-    h = om._f64(x)[rows]
-    ob, oh = _operand_model(blocks, head)
-    for p in ob:
-        h, _ = om.block_forward(p, h, pshape)
-    ref = om.head_forward_backward(h, oh["g_final"], oh["w_lm"], tg.numpy()[rows], pshape)
-    assert np.max(np.abs(lp[rows] - ref["loss_partials"]) / ref["loss_partials"]) < 10 * LOSS_REL
-    assert abs(lp[rows].mean() - ref["loss"]) / ref["loss"] < LOSS_REL
-    # squared sum over every gradient (fused into the backward's gradient
-    # producers) against fp64 on the host, chunk by chunk
+    ref = _oracle_q4b_full(blocks, head, x, tg.numpy(), shape, C4_BLOCKS)
+    errs = _grad_errors(tr, ref["grads"])
+    print("q4b_full gradient rel L2: " + " ".join(f"{k}:{v:.3e}" for k, v in errs.items()))
+    return dict(tr=tr, ref=ref, lp=to_np(loss), errs=errs, shape=shape, blocks=blocks,
+                head=head)
+
+
+def test_q4b_full_loss(q4b_full_step):
+    """The loss (the mean over all 4096 tokens) through the 36 blocks and the
+    vocabulary-151936 head, against the oracle."""
+    _assert_loss(q4b_full_step["lp"], q4b_full_step["ref"], per_token=False)
+
+
+@pytest.mark.xfail(strict=True, reason=(
+    "each token's loss differs by up to 0.62 % (the mean by 4e-5): the last hidden "
+    "state carries the forward's amplified bf16-operand error (about 2 %), which "
+    "moves single target logits"))
+def test_q4b_full_token_losses(q4b_full_step):
+    """Every token's loss partial within 1e-3 of the oracle's."""
+    _assert_loss(q4b_full_step["lp"], q4b_full_step["ref"])
+
+
+@_depth_floor("1.2-4.1 % (worst layer 35 wq; 36 blocks)")
+def test_q4b_full_gradients(q4b_full_step):
+    """Per-tensor gradients of blocks 0, 17 and 35, the LM head and the final
+    norm gain against the oracle."""
+    _assert_grads(q4b_full_step["errs"])
+
+
+def test_q4b_full_squared_sum_and_adamw(q4b_full_step):
+    """The clip's squared sum the backward fused into its gradient producers
+    (against the fp64 sum of the squares of the gradients it returned), then
+    the clip and AdamW fed the oracle's gradients of the kept tensors and the
+    oracle's global squared sum: the updated weights within 1e-5."""
+    r = q4b_full_step
+    tr, ref, shape = r["tr"], r["ref"], r["shape"]
     want = 0.0
     chunk = 1 << 26
     for i in range(0, tr.n_params, chunk):
         want += om.squared_sum(tr.g[i:i + chunk].cpu().numpy())
     assert abs(float(tr.sumsq) - want) / want < 1e-6
-    # AdamW on sampled elements, given the GPU's own gradients and clip scale
-    gen = torch.Generator().manual_seed(5)
-    idx = torch.randint(0, tr.n_params, (1 << 20,), generator=gen).cuda()
-    w0, g0 = tr.w[idx].double().cpu().numpy(), tr.g[idx].double().cpu().numpy()
+    print(f"squared sum: GPU {want:.6e}, oracle {ref['sumsq']:.6e}")
+    scale, norm, ok = om.clip_scale([ref["sumsq"]], synth.OPTIM["max_norm"])
+    assert ok
+    for key, gref in ref["grads"].items():
+        tr.tensor(tr.g, *key).copy_(torch.from_numpy(gref).float())
+    tr.sumsq.fill_(ref["sumsq"])
     tr.clip_and_update()
     torch.cuda.synchronize()
-    s_ref, _, ok = om.clip_scale([want], synth.OPTIM["max_norm"])
-    assert ok and abs(float(tr.scale) - s_ref) / s_ref < 1e-6
+    assert abs(float(tr.scale) - scale) / scale < 1e-6
     o = synth.OPTIM
-    w1, _, _ = om.adamw(w0, g0, np.zeros_like(w0), np.zeros_like(w0), 1, o["lr"], o["beta1"],
-                        o["beta2"], o["eps"], o["weight_decay"], s_ref)
-    got = tr.w[idx].double().cpu().numpy()
-    assert rel_l2(got, w1) < ADAMW_REL
-
-
-def test_q4b_full_widths_gradients_on_a_short_sequence(q4b_full_inputs):
-    """The full model's widths (hidden 2560, 32/8 heads, SwiGLU 9728, vocab
-    151936) with its first four blocks and one of its 1024-token sequences:
-    gradient parity on every tensor. This stack is not one of the defined
-    workloads; it guards the full-width multi-layer backward against
-    regressions. Its measured per-tensor errors (0.7-1.2 %, growing with
-    depth) are the compounded bf16-operand rounding floor of four stacked
-    blocks, so the bound here is twice the per-workload tolerance."""
-    shape, blocks, head, x, tg = q4b_full_inputs
-    s64 = shape.replace(layers=4, batch=1)
-    xs, ts = x[:shape.seq], tg[:shape.seq]
-    ob, oh = _operand_model(blocks[:4], head)
-    res, bgrads = om.model_forward_backward(ob, oh, xs, ts.numpy(), s64)
-    tr = DecoderTrainer(s64)
-    tr.load(blocks[:4], head)
-    loss = tr.forward_backward(xs.cuda(), ts.cuda())
-    torch.cuda.synchronize()
-    assert abs(float(loss.double().mean()) - res["loss"]) / res["loss"] < LOSS_REL
-    ref = {("head", "g_final"): res["g_final"], ("head", "w_lm"): res["w_lm"]}
-    for li in range(4):
-        for name, gref in bgrads[li].items():
-            ref[(li, name)] = gref
-    _check_grads(tr, ref, tol=2 * GRAD_REL_L2)
+    for key, gref in ref["grads"].items():
+        w0 = (r["head"] if key[0] == "head" else r["blocks"][key[0]])[key[1]]
+        w1, _, _ = om.adamw(w0, gref, np.zeros(gref.shape), np.zeros(gref.shape), 1, o["lr"],
+                            o["beta1"], o["beta2"], o["eps"], o["weight_decay"], scale)
+        assert rel_l2(to_np(tr.tensor(tr.w, *key)), w1) < ADAMW_REL, key
