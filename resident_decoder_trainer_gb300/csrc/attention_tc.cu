@@ -417,6 +417,334 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------- forward, two tiles
+// Each work item is a pair of 128-query tiles (A: queries [256 i, 256 i + 128),
+// B: the next 128) of one query head and sequence; both read the same K/V
+// tiles. Warps 2-5 run the online softmax of tile A and warps 6-9 that of
+// tile B, one thread per query row (whole rows: no cross-warp reduction).
+// The MMA thread interleaves the two tiles,
+//   S_A(0) S_B(0) | PV_A(0) S_A(1) | PV_B(0) S_B(1) | PV_A(1) S_A(2) | ...
+// so one tile's scores and P V run on the tensor cores while the other tile's
+// softmax runs. Each tile has one S buffer in TMEM (P is written back over it
+// as packed bf16 and read as the A operand of P V; tcgen05 operations of one
+// thread complete in order, so S(j+1) issued after P V(j) cannot overwrite P
+// early) and one O buffer, read out by its softmax group after the item's
+// last P V. K and V tiles come through rings freed by tile B's S and P V.
+template <int D>
+struct Fwd2Cfg {
+  static constexpr int BM = 128, BN = 128;
+  static constexpr uint32_t CHUNK = 128 * 128;  // 64 cols x 128 rows of bf16
+  static constexpr uint32_t Q_BYTES = BM * D * 2;
+  static constexpr uint32_t KV_BYTES = BN * D * 2;
+  static constexpr int KS = D == 128 ? 2 : 3;
+  static constexpr int VS = D == 128 ? 2 : 3;
+  static constexpr uint32_t OFF_Q = 0;                       // [2]: tiles A, B
+  static constexpr uint32_t OFF_K = OFF_Q + 2 * Q_BYTES;     // [KS]
+  static constexpr uint32_t OFF_V = OFF_K + KS * KV_BYTES;   // [VS]
+  static constexpr uint32_t OFF_BAR = OFF_V + VS * KV_BYTES;
+  static constexpr size_t SMEM = OFF_BAR + 512 + 1024;
+  // TMEM: S_A, S_B (128 fp32 columns each), then O_A, O_B (D columns each)
+  static constexpr uint32_t TMEM_S = 0, TMEM_O = 256, TMEM_COLS = 512;
+  static_assert(TMEM_O + 2 * D <= TMEM_COLS, "two O buffers must fit in TMEM");
+  static_assert(SMEM <= 232448, "attention forward tile exceeds the shared memory of a CTA");
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                     const __grid_constant__ CUtensorMap tv, bf16* __restrict__ o,
+                     float* __restrict__ lse, int B, int S, int nh, int nkv, float scale_log2,
+                     int* err) {
+  using C = Fwd2Cfg<D>;
+  constexpr int BM = C::BM, BN = C::BN, DCH = D / 64, KS = C::KS, VS = C::VS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  // barriers: q_full, q_empty, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS],
+  // s_full[2], p_full[2], o_done[2], o_free[2], drain
+  const uint32_t q_full = bar0, q_empty = bar0 + 8, k_full = bar0 + 16,
+                 k_empty = k_full + 8 * KS, v_full = k_empty + 8 * KS, v_empty = v_full + 8 * VS,
+                 s_full = v_empty + 8 * VS, p_full = s_full + 16, o_done = p_full + 16,
+                 o_free = o_done + 16, drain = o_free + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 384);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_qp = (S + 2 * BM - 1) / (2 * BM);
+  const int n_kvt = (S + BN - 1) / BN;
+  const int per = nh * B;
+  const int n_items = n_qp * per;
+  const int grp = nh / nkv;
+  // item idx -> pair i (longest first), head h, sequence b; tiles of A and B
+  auto item = [&](int idx, int& i, int& h, int& b, int& nA, int& nB) {
+    i = n_qp - 1 - idx / per;
+    const int rem = idx % per;
+    h = rem % nh;
+    b = rem / nh;
+    nA = min(2 * i + 1, n_kvt);
+    nB = min(2 * i + 2, n_kvt);
+  };
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int x = 0; x < KS; ++x) {
+      mbar_init(k_full + 8 * x, 1);
+      mbar_init(k_empty + 8 * x, 1);
+    }
+    for (int x = 0; x < VS; ++x) {
+      mbar_init(v_full + 8 * x, 1);
+      mbar_init(v_empty + 8 * x, 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(s_full + 8 * x, 1);
+      mbar_init(p_full + 8 * x, 128);
+      mbar_init(o_done + 8 * x, 1);
+      mbar_init(o_free + 8 * x, 128);
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tk);
+    tma_prefetch_desc(&tv);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // --------------------------------------------------------- producer
+      bool ok = true;
+      int jg = 0;
+      for (int idx = blockIdx.x, it = 0; idx < n_items && ok; idx += gridDim.x, ++it) {
+        int i, h, b, nA, nB;
+        item(idx, i, h, b, nA, nB);
+        const int g = h / grp, tok0 = b * S;
+        if (!mbar_wait(q_empty, (it & 1) ^ 1, err)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(q_full, 2 * C::Q_BYTES);
+        for (int x = 0; x < 2; ++x)
+          for (int c = 0; c < DCH; ++c)
+            tma_load_2d(sbase + C::OFF_Q + x * C::Q_BYTES + c * C::CHUNK, &tq, q_full,
+                        h * D + c * 64, tok0 + 2 * BM * i + BM * x);
+        auto load_k = [&](int j) -> bool {
+          const int jj = jg + j, st = jj % KS;
+          if (!mbar_wait(k_empty + 8 * st, ((jj / KS) & 1) ^ 1, err)) return false;
+          mbar_arrive_expect_tx(k_full + 8 * st, C::KV_BYTES);
+          for (int c = 0; c < DCH; ++c)
+            tma_load_2d(sbase + C::OFF_K + st * C::KV_BYTES + c * C::CHUNK, &tk, k_full + 8 * st,
+                        g * D + c * 64, tok0 + j * BN);
+          return true;
+        };
+        auto load_v = [&](int j) -> bool {
+          const int jj = jg + j, st = jj % VS;
+          if (!mbar_wait(v_empty + 8 * st, ((jj / VS) & 1) ^ 1, err)) return false;
+          mbar_arrive_expect_tx(v_full + 8 * st, C::KV_BYTES);
+          for (int c = 0; c < DCH; ++c)
+            tma_load_2d(sbase + C::OFF_V + st * C::KV_BYTES + c * C::CHUNK, &tv, v_full + 8 * st,
+                        g * D + c * 64, tok0 + j * BN);
+          return true;
+        };
+        for (int j = 0; j < KS - 1 && j < nB && ok; ++j) ok = load_k(j);
+        for (int j = 0; j < nB && ok; ++j) {
+          if (j + KS - 1 < nB) ok = load_k(j + KS - 1);
+          if (ok) ok = load_v(j);
+        }
+        jg += nB;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // -------------------------------------------------------------- MMA
+      constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0, 0);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(BM, D, 0, 1);
+      bool ok = true;
+      int jg = 0, jt0 = 0, jt1 = 0;  // KV tiles so far; P V issued so far per tile
+      for (int idx = blockIdx.x, it = 0; idx < n_items && ok; idx += gridDim.x, ++it) {
+        int i, h, b, nA, nB;
+        item(idx, i, h, b, nA, nB);
+        // S_x(j) = Q_x K_j^T into tile x's S buffer
+        auto issue_s = [&](int x, int j) -> bool {
+          const int jj = jg + j, ks = jj % KS;
+          if (!mbar_wait(k_full + 8 * ks, (jj / KS) & 1, err)) return false;
+          tc_fence_after();
+          const uint32_t kb = sbase + C::OFF_K + ks * C::KV_BYTES;
+          const uint32_t qb = sbase + C::OFF_Q + x * C::Q_BYTES;
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k >> 2) * C::CHUNK + (k & 3) * 32;
+            tc_mma_bf16(tmem + C::TMEM_S + x * BN, sdesc_sw128(qb + off, 16, 1024),
+                        sdesc_sw128(kb + off, 16, 1024), idesc_s, k > 0);
+          }
+          tc_commit(s_full + 8 * x);
+          return true;
+        };
+        // O_x += P_x(j) V_j with P (bf16, over tile x's S buffer) from TMEM
+        auto issue_pv = [&](int x, int j) -> bool {
+          const int jj = jg + j, vs = jj % VS;
+          if (j == 0 && !mbar_wait(o_free + 8 * x, (it & 1) ^ 1, err)) return false;
+          if (!mbar_wait(p_full + 8 * x, (x ? jt1 : jt0) & 1, err) ||
+              !mbar_wait(v_full + 8 * vs, (jj / VS) & 1, err))
+            return false;
+          tc_fence_after();
+          const uint32_t vb = sbase + C::OFF_V + vs * C::KV_BYTES;
+#pragma unroll
+          for (int k = 0; k < BN / 16; ++k)
+            tc_mma_bf16_ts(tmem + C::TMEM_O + x * D, tmem + C::TMEM_S + x * BN + k * 8,
+                           sdesc_sw128(vb + k * 2048, C::CHUNK, 1024), idesc_o, (j | k) != 0);
+          tc_commit(o_done + 8 * x);
+          if (x) ++jt1;
+          else ++jt0;
+          return true;
+        };
+        if (!mbar_wait(q_full, it & 1, err)) {
+          ok = false;
+          break;
+        }
+        ok = issue_s(0, 0) && issue_s(1, 0);
+        if (!ok) break;
+        tc_commit(k_empty + 8 * (jg % KS));
+        if (nB == 1) tc_commit(q_empty);
+        for (int j = 0; j < nB && ok; ++j) {
+          if (j < nA) {
+            ok = issue_pv(0, j) && (j + 1 >= nA || issue_s(0, j + 1));
+            if (!ok) break;
+          }
+          ok = issue_pv(1, j);
+          if (!ok) break;
+          tc_commit(v_empty + 8 * ((jg + j) % VS));
+          if (j + 1 < nB) {
+            ok = issue_s(1, j + 1);
+            if (!ok) break;
+            tc_commit(k_empty + 8 * ((jg + j + 1) % KS));
+            if (j + 2 == nB) tc_commit(q_empty);  // the item's last Q K^T
+          }
+        }
+        jg += nB;
+      }
+      tc_commit(drain);
+      mbar_wait(drain, 0, nullptr);
+    }
+  } else {
+    // ------------------------------- softmax: one query row per thread
+    const int x = (warp - 2) >> 2;  // 0: tile A, 1: tile B
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t ts = tmem + lane_base + C::TMEM_S + x * BN;
+    const uint32_t t_o = tmem + lane_base + C::TMEM_O + x * D;
+    bool ok = true;
+    int jx = 0;  // tiles of this softmax group so far
+    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+      int i, h, b, nA, nB;
+      item(idx, i, h, b, nA, nB);
+      const int n_tiles = x ? nB : nA;
+      const int qpos = 2 * BM * i + BM * x + row;
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < n_tiles; ++j, ++jx) {
+        if (!warp_wait(s_full + 8 * x, jx & 1, err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sv[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tmem_ld32(ts + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * c]));
+        tmem_ld_wait();
+        const int c0 = j * BN;  // key position of sv[0]
+        const bool edge = (c0 + BN - 1 > qpos) || (c0 + BN > S);
+        // row maximum of the raw scores (the scale is positive), four chains
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          if (edge && (c0 + c > qpos || c0 + c >= S)) sv[c] = __float_as_uint(-INFINITY);
+          m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sv[c]));
+        }
+        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * scale_log2;
+        float alpha = 1.f;
+        if (mx > m_run + kRescaleLog2) {
+          alpha = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - mx);
+          m_run = mx;
+        }
+        // p = 2^(s scale - m), one FMA per score; bf16 pairs in place
+        const float nm = -m_run;
+        float s2[2] = {0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 128; c += 2) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sv[c]), scale_log2, nm));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sv[c + 1]), scale_log2, nm));
+          s2[(c >> 1) & 1] += p0 + p1;
+          sv[c / 2] = pack_bf16x2(p0, p1);
+        }
+        l_run = l_run * alpha + (s2[0] + s2[1]);
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          // O is being accumulated by P V of the previous tile until it completes
+          if (!warp_wait(o_done + 8 * x, (jx - 1) & 1, err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(t_o + c * 32, ov);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tmem_st32(t_o + c * 32, ov);
+          }
+        }
+        // P: 128 keys as 64 bf16 pairs over the first 64 columns of S
+        tmem_st32(ts, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tmem_st32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_full + 8 * x);
+      }
+      if (!ok || !warp_wait(o_done + 8 * x, (jx - 1) & 1, err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      bf16* orow = o + (int64_t)(b * S + qpos) * (nh * D) + h * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(t_o + c * 32, ov);
+        tmem_ld_wait();
+        if (qpos < S) store_row32_bf16(orow + c * 32, ov, inv);
+      }
+      // this O buffer is free for the next item
+      tc_fence_before();
+      mbar_arrive(o_free + 8 * x);
+      if (qpos < S) lse[((int64_t)b * nh + h) * S + qpos] = (m_run + __log2f(l_run)) * kLn2F;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (err && *reinterpret_cast<volatile int*>(err) != 0) {
+    // after a timed-out wait, copies issued just before may still be landing
+    // in this CTA's shared memory: let them finish before it exits
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 200000ull) {
+    }
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
 // ============================================================= backward
 // The log2-domain LSE and D = rowsum(dO o O) are read from [B*nh, S_pad]
 // arrays (S_pad a multiple of 64) so that 64-query segments are aligned.
@@ -966,18 +1294,18 @@ static cudaError_t fwd_tc_d(const bf16* q, int64_t ldq, const bf16* k, int64_t l
     return cudaErrorInvalidValue;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd2_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)FwdCfg<D>::SMEM);
+                                         (int)Fwd2Cfg<D>::SMEM);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const int n_qt = (S + 127) / 128;
+  const int n_qp = (S + 255) / 256;
   const float scale_log2 = kLog2eF / sqrtf((float)D);
   note_launch();
-  const int n_items = n_qt * nh * B;
+  const int n_items = n_qp * nh * B;
   const int grid = n_items < num_sms() ? n_items : num_sms();
-  attn_fwd_tc_kernel<D><<<grid, kThreads, FwdCfg<D>::SMEM, s>>>(
+  attn_fwd2_kernel<D><<<grid, kThreads, Fwd2Cfg<D>::SMEM, s>>>(
       tq, tk, tv, o, lse, B, S, nh, nkv, scale_log2, err);
   return cudaGetLastError();
 }
