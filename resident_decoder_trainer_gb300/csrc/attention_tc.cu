@@ -35,6 +35,8 @@
 //    again by dQ += dS K after the elementwise pass), V through a 2-deep one
 //    freed as soon as dP = dO V^T completes.
 // Every operand transposition is a shared-memory descriptor, never a copy.
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -659,15 +661,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 4; ++c)
           tmem_ld32(ts + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * c]));
         tmem_ld_wait();
-        const int c0 = j * BN;  // key position of sv[0]
-        const bool edge = (c0 + BN - 1 > qpos) || (c0 + BN > S);
+        // keys j BN + c with c < lim are visible to this row (causal, and
+        // inside the sequence): only tiles on or past the diagonal mask
+        const int lim = min(qpos + 1, S) - j * BN;
+        if (__any_sync(0xffffffffu, lim < BN)) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= lim) sv[c] = __float_as_uint(-INFINITY);
+        }
         // row maximum of the raw scores (the scale is positive), four chains
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          if (edge && (c0 + c > qpos || c0 + c >= S)) sv[c] = __float_as_uint(-INFINITY);
-          m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sv[c]));
-        }
+        for (int c = 0; c < 128; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sv[c]));
         const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * scale_log2;
         float alpha = 1.f;
         if (mx > m_run + kRescaleLog2) {
@@ -970,26 +975,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float4* d4 =
           reinterpret_cast<const float4*>(smem + C::OFF_LD + qs * 512 + 256) + half * 8;
       const int q0 = m0 + half * 32;
+      // queries q0 + c with lo <= c < hi see this key row (causal, inside the
+      // sequence); the mask is applied only where some row of the warp needs it
+      const int lo = kpos - q0, hi = kpos < S ? S - q0 : 0;
+      const bool full = __all_sync(0xffffffffu, lo <= 0 && hi >= 32);
       // bf16 pairs of P^T / dS^T are packed in place into sv / dp [0, 16)
+      auto pass = [&](auto masked) {
 #pragma unroll
-      for (int c4 = 0; c4 < 8; ++c4) {
-        const float4 lv = l4[c4], dv4 = d4[c4];
-        const float la[4] = {lv.x, lv.y, lv.z, lv.w}, da[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
-        float pv[4], dsv[4];
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 lv = l4[c4], dv4 = d4[c4];
+          const float la[4] = {lv.x, lv.y, lv.z, lv.w}, da[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
+          float pv[4], dsv[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = 4 * c4 + e;
-          const int qpos = q0 + c;
-          const bool valid = qpos < S && qpos >= kpos && kpos < S;
-          const float p = valid ? ex2_approx(__uint_as_float(sv[c]) * scale_log2 - la[e]) : 0.f;
-          pv[e] = p;
-          dsv[e] = p * (__uint_as_float(dp[c]) - da[e]);
+          for (int e = 0; e < 4; ++e) {
+            const int c = 4 * c4 + e;
+            const float x = __uint_as_float(sv[c]) * scale_log2 - la[e];
+            float p;
+            if constexpr (decltype(masked)::value)
+              p = (c >= lo && c < hi) ? ex2_approx(x) : 0.f;
+            else
+              p = ex2_approx(x);
+            pv[e] = p;
+            dsv[e] = p * (__uint_as_float(dp[c]) - da[e]);
+          }
+          sv[2 * c4] = pack_bf16x2(pv[0], pv[1]);
+          sv[2 * c4 + 1] = pack_bf16x2(pv[2], pv[3]);
+          dp[2 * c4] = pack_bf16x2(dsv[0], dsv[1]);
+          dp[2 * c4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
         }
-        sv[2 * c4] = pack_bf16x2(pv[0], pv[1]);
-        sv[2 * c4 + 1] = pack_bf16x2(pv[2], pv[3]);
-        dp[2 * c4] = pack_bf16x2(dsv[0], dsv[1]);
-        dp[2 * c4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
-      }
+      };
+      if (full)
+        pass(std::false_type{});
+      else
+        pass(std::true_type{});
       // over this warp's own S^T / dP^T columns (no other warp reads them)
       tmem_st16(ts, *reinterpret_cast<uint32_t(*)[16]>(&sv[0]));
       tmem_st16(ts + 64, *reinterpret_cast<uint32_t(*)[16]>(&dp[0]));
@@ -1221,6 +1239,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const int c0 = j * BN + half * 64;
+      // keys c0 + c with c < lim are visible to this query row; the mask is
+      // applied only where some row of the warp needs it (diagonal tiles)
+      const int lim = qvalid ? qpos + 1 - c0 : 0;
+      const bool full = __all_sync(0xffffffffu, lim >= 64);
       uint32_t pk[32];
 #pragma unroll
       for (int qt = 0; qt < 2; ++qt) {
@@ -1229,17 +1251,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(t0 + C::T_S, sv);
         tmem_ld32(t0 + C::T_DP, dp);
         tmem_ld_wait();
+        if (full) {
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float d2[2];
+          for (int c = 0; c < 32; c += 2) {
+            float d2[2];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int kp = c0 + qt * 32 + c + e;
-            const bool valid = qvalid && kp <= qpos;
-            const float p = valid ? ex2_approx(__uint_as_float(sv[c + e]) * scale_log2 - l2) : 0.f;
-            d2[e] = p * (__uint_as_float(dp[c + e]) - drow);
+            for (int e = 0; e < 2; ++e) {
+              const float p = ex2_approx(__uint_as_float(sv[c + e]) * scale_log2 - l2);
+              d2[e] = p * (__uint_as_float(dp[c + e]) - drow);
+            }
+            pk[qt * 16 + c / 2] = pack_bf16x2(d2[0], d2[1]);
           }
-          pk[qt * 16 + c / 2] = pack_bf16x2(d2[0], d2[1]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float d2[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float p = qt * 32 + c + e < lim
+                                  ? ex2_approx(__uint_as_float(sv[c + e]) * scale_log2 - l2)
+                                  : 0.f;
+              d2[e] = p * (__uint_as_float(dp[c + e]) - drow);
+            }
+            pk[qt * 16 + c / 2] = pack_bf16x2(d2[0], d2[1]);
+          }
         }
       }
       tc_fence_before();
