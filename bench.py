@@ -35,14 +35,16 @@ if ROOT not in sys.path:
 METRIC = "train tokens/s (fwd+bwd+clip+AdamW) at Qwen3-4B shape; % of BF16/HBM roofline"
 UNIT = "tokens/s"
 
-# DRAM traffic per tensor-core GEMM launch, from `ncu` (dram__bytes_read.sum +
-# dram__bytes_write.sum) averaged over the step's launch mix, and the source
-# it was measured on; reported only while gemm.cu is unchanged.
-GEMM_TRAFFIC_BYTES = 259571819
-GEMM_TRAFFIC_SRC_SHA = "86feded81900402b"
-# The same for the NF4 GEMM launches of one q4b_nf4 step.
-NF4_TRAFFIC_BYTES = 75418272
-NF4_TRAFFIC_SRC_SHA = "86feded81900402b"
+# DRAM traffic per tensor-core GEMM launch (dram__bytes_read.sum +
+# dram__bytes_write.sum), averaged over the q4b_full step's launch mix: 36 x
+# the 12 launches of one q4b_full-shaped block + the LM head's 76, each
+# captured alone on that small case (the shapes are the step's), and the
+# gemm.cu source it was measured on; reported only while gemm.cu is unchanged.
+GEMM_TRAFFIC_BYTES = 224659493
+GEMM_TRAFFIC_SRC_SHA = "828139ae5caebe33"
+# The same for the 8 NF4 GEMM launches of one q4b_nf4 step.
+NF4_TRAFFIC_BYTES = 75663168
+NF4_TRAFFIC_SRC_SHA = "828139ae5caebe33"
 
 
 def traffic_if_current(nbytes, sha):
