@@ -4,18 +4,18 @@
 //
 // Every kernel has 10 warps: warp 0 issues the TMA copies, warp 1 (one lane)
 // the tcgen05.mma instructions, and warps 2-9 do the elementwise work: TMEM
-// lane quarter q is served by warps 2+q and 6+q, each taking half of the
-// columns of the rows it owns. Work items are launched longest-first (the
-// causal triangle makes items unequal).
+// lane quarter q is served by warps 2+q and 6+q (in the backward each takes
+// half of the columns of the rows it owns; in the forward each serves its own
+// query tile). Work items are launched longest-first (the causal triangle
+// makes items unequal).
 //
-// Forward (head_dim 64 or 128), persistent: each CTA walks (128-query tile,
-// query head, sequence) work items longest first. S = Q K^T goes to one of
-// two TMEM buffers, so the next tile's scores are computed while this tile's
-// online softmax (log2 domain) runs; P is written back over its S buffer as
-// packed bf16 and read from TMEM as the A operand of O += P V; O lives in one
-// of two TMEM buffers (items alternate) and is rescaled in place only when a
-// row maximum grows by more than 2^8. K tiles come through a 3-deep ring
-// freed as each Q K^T completes, V through a 2-deep ring freed by P V. The
+// Forward (head_dim 64 or 128), persistent: each CTA walks work items
+// longest first, an item being two 128-query tiles of one head and sequence
+// that share their K/V tiles; warps 2-5 run one tile's online softmax and
+// warps 6-9 the other's, one thread per query row, while the MMA thread
+// interleaves the two tiles' Q K^T and P V. P is written back over its S
+// columns as packed bf16 and read from TMEM as the A operand of O += P V; O
+// is rescaled in place only when a row maximum grows by more than 2^8. The
 // log-sum-exp of every row is saved.
 //
 // Backward (head_dim 64 or 128) in two kernels, so no dQ atomics are needed
@@ -68,356 +68,10 @@ __device__ __forceinline__ void store_row32_bf16(bf16* dst, const uint32_t (&a)[
 }
 
 // ============================================================== forward
-template <int D>
-struct FwdCfg {
-  static constexpr int BM = 128, BN = 128;
-  static constexpr uint32_t CHUNK = 128 * 128;  // 64 cols x 128 rows of bf16
-  static constexpr uint32_t Q_BYTES = BM * D * 2;
-  static constexpr uint32_t KV_BYTES = BN * D * 2;
-  static constexpr int K_STAGES = 3;  // K runs further ahead than V (Q K^T comes first)
-  static constexpr uint32_t OFF_Q = 0;
-  static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;                // [K_STAGES]
-  static constexpr uint32_t OFF_V = OFF_K + K_STAGES * KV_BYTES;    // [2]
-  static constexpr uint32_t OFF_RED = OFF_V + 2 * KV_BYTES;  // float [2][2][128] maxima, [2][128] sums
-  static constexpr uint32_t OFF_BAR = OFF_RED + 3 * 2 * 128 * 4;
-  static constexpr size_t SMEM = OFF_BAR + 256 + 1024;
-  // TMEM: two S buffers (128 fp32 columns each; P is written over the first
-  // 64 columns of its S buffer as packed bf16), then two O buffers (work
-  // items alternate, so one item's output is read while the next accumulates)
-  static constexpr uint32_t TMEM_S = 0, TMEM_O = 256, TMEM_COLS = 512;
-  static_assert(TMEM_O + 2 * D <= TMEM_COLS, "two O buffers must fit in TMEM");
-  static_assert(SMEM <= 232448, "attention forward tile exceeds the shared memory of a CTA");
-};
-
 // Rows rescale O only when their running maximum grows by more than 2^8 (in
 // the log2 domain): below that the stale maximum is kept, P stays <= 2^8 and
 // the result is the same (O and l are both relative to the stale maximum).
 constexpr float kRescaleLog2 = 8.f;
-
-// Work item idx (longest causal rows first) -> query tile, head, sequence.
-__device__ __forceinline__ void fwd_item(int idx, int n_qt, int nh, int B, int& mt, int& h,
-                                         int& b) {
-  const int per = nh * B;
-  mt = n_qt - 1 - idx / per;
-  const int rem = idx % per;
-  h = rem % nh;
-  b = rem / nh;
-}
-
-// Persistent: each CTA takes work items blockIdx.x, blockIdx.x + gridDim.x,
-// ... Barrier phases run over the CTA's whole sequence of key tiles (jg) and
-// items (it), so the next item's first key tiles are loaded while this
-// item's output is written. K tiles sit in a 3-deep ring whose slots free
-// when their Q K^T completes, V tiles in a 2-deep ring freed by P V.
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
-    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                       const __grid_constant__ CUtensorMap tv, bf16* __restrict__ o,
-                       float* __restrict__ lse, int B, int S, int nh, int nkv, float scale_log2,
-                       int* err) {
-  using C = FwdCfg<D>;
-  constexpr int BM = C::BM, BN = C::BN, DCH = D / 64;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar0 = sbase + C::OFF_BAR;
-  const uint32_t q_full = bar0, q_empty = bar0 + 8, k_full = bar0 + 16, k_empty = bar0 + 40,
-                 v_full = bar0 + 64, v_empty = bar0 + 80, s_full = bar0 + 96,
-                 p_full = bar0 + 112, o_done = bar0 + 120, o_free = bar0 + 128,
-                 drain = bar0 + 144;
-  constexpr int KS = C::K_STAGES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 192);
-  float* red_max = reinterpret_cast<float*>(smem + C::OFF_RED);  // [2 parity][2 half][128 rows]
-  float* red_sum = red_max + 2 * 2 * 128;                        // [2 half][128 rows]
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_qt = (S + BM - 1) / BM;
-  const int n_items = n_qt * nh * B;
-  const int grp = nh / nkv;
-
-  if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
-    for (int i = 0; i < KS; ++i) {
-      mbar_init(k_full + 8 * i, 1);
-      mbar_init(k_empty + 8 * i, 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(v_full + 8 * i, 1);
-      mbar_init(v_empty + 8 * i, 1);
-      mbar_init(s_full + 8 * i, 1);
-      mbar_init(o_free + 8 * i, kEltThreads);
-    }
-    mbar_init(p_full, kEltThreads);
-    mbar_init(o_done, 1);
-    mbar_init(drain, 1);
-    fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tq);
-    tma_prefetch_desc(&tk);
-    tma_prefetch_desc(&tv);
-  }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // --------------------------------------------------------- producer
-      bool ok = true;
-      int jg = 0;
-      for (int idx = blockIdx.x, it = 0; idx < n_items && ok; idx += gridDim.x, ++it) {
-        int mt, h, b;
-        fwd_item(idx, n_qt, nh, B, mt, h, b);
-        const int g = h / grp, tok0 = b * S, n_tiles = min(n_qt, mt + 1);
-        if (!mbar_wait(q_empty, (it & 1) ^ 1, err)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(q_full, C::Q_BYTES);
-        for (int c = 0; c < DCH; ++c)
-          tma_load_2d(sbase + C::OFF_Q + c * C::CHUNK, &tq, q_full, h * D + c * 64,
-                      tok0 + mt * BM);
-        // K of tile j + 2 goes out before V of tile j: a K slot frees when its
-        // Q K^T completes, a V slot only when its P V does
-        auto load_k = [&](int j) -> bool {
-          const int jj = jg + j, st = jj % KS;
-          if (!mbar_wait(k_empty + 8 * st, ((jj / KS) & 1) ^ 1, err)) return false;
-          mbar_arrive_expect_tx(k_full + 8 * st, C::KV_BYTES);
-          for (int c = 0; c < DCH; ++c)
-            tma_load_2d(sbase + C::OFF_K + st * C::KV_BYTES + c * C::CHUNK, &tk, k_full + 8 * st,
-                        g * D + c * 64, tok0 + j * BN);
-          return true;
-        };
-        auto load_v = [&](int j) -> bool {
-          const int jj = jg + j, st = jj & 1;
-          if (!mbar_wait(v_empty + 8 * st, ((jj >> 1) & 1) ^ 1, err)) return false;
-          mbar_arrive_expect_tx(v_full + 8 * st, C::KV_BYTES);
-          for (int c = 0; c < DCH; ++c)
-            tma_load_2d(sbase + C::OFF_V + st * C::KV_BYTES + c * C::CHUNK, &tv, v_full + 8 * st,
-                        g * D + c * 64, tok0 + j * BN);
-          return true;
-        };
-        for (int j = 0; j < KS - 1 && j < n_tiles && ok; ++j) ok = load_k(j);
-        for (int j = 0; j < n_tiles && ok; ++j) {
-          if (j + KS - 1 < n_tiles) ok = load_k(j + KS - 1);
-          if (ok) ok = load_v(j);
-        }
-        jg += n_tiles;
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // -------------------------------------------------------------- MMA
-      constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0, 0);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(BM, D, 0, 1);
-      bool ok = true;
-      int jg = 0;
-      for (int idx = blockIdx.x, it = 0; idx < n_items && ok; idx += gridDim.x, ++it) {
-        int mt, h, b;
-        fwd_item(idx, n_qt, nh, B, mt, h, b);
-        const int n_tiles = min(n_qt, mt + 1);
-        const int qb = it & 1;  // this item's O buffer
-        const uint32_t qaddr = sbase + C::OFF_Q;
-        const uint32_t t_o = tmem + C::TMEM_O + qb * D;
-        auto issue_s = [&](int jj) -> bool {
-          const int st = jj & 1, ks = jj % KS;
-          if (!mbar_wait(k_full + 8 * ks, (jj / KS) & 1, err)) return false;
-          tc_fence_after();
-          const uint32_t kb = sbase + C::OFF_K + ks * C::KV_BYTES;
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (k >> 2) * C::CHUNK + (k & 3) * 32;
-            tc_mma_bf16(tmem + C::TMEM_S + st * BN, sdesc_sw128(qaddr + off, 16, 1024),
-                        sdesc_sw128(kb + off, 16, 1024), idesc_s, k > 0);
-          }
-          tc_commit(s_full + 8 * st);
-          tc_commit(k_empty + 8 * ks);
-          return true;
-        };
-        if (!mbar_wait(q_full, it & 1, err)) {
-          ok = false;
-          break;
-        }
-        // both S buffers held P of the previous item's last two tiles: wait
-        // for the last P V issued (tcgen05 operations complete in order)
-        if (jg >= 1 && !mbar_wait(o_done, (jg - 1) & 1, err)) {
-          ok = false;
-          break;
-        }
-        if (!issue_s(jg)) {
-          ok = false;
-          break;
-        }
-        if (n_tiles == 1) tc_commit(q_empty);
-        // this O buffer was read out by item it - 2
-        if (!mbar_wait(o_free + 8 * qb, ((it >> 1) & 1) ^ 1, err)) {
-          ok = false;
-          break;
-        }
-        for (int j = 0; j < n_tiles && ok; ++j) {
-          const int jj = jg + j, st = jj & 1;
-          if (j + 1 < n_tiles) {
-            // S buffer (jj+1)&1 still holds P_{jj-1}, read by P_{jj-1} V
-            if (j >= 1 && !mbar_wait(o_done, (jj - 1) & 1, err)) {
-              ok = false;
-              break;
-            }
-            if (!issue_s(jj + 1)) {
-              ok = false;
-              break;
-            }
-            if (j + 2 == n_tiles) tc_commit(q_empty);  // the item's last Q K^T
-          }
-          if (!mbar_wait(p_full, jj & 1, err) || !mbar_wait(v_full + 8 * st, (jj >> 1) & 1, err)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t vb = sbase + C::OFF_V + st * C::KV_BYTES;
-          // O += P V with P (bf16, in TMEM over S buffer st) as the A operand
-#pragma unroll
-          for (int k = 0; k < BN / 16; ++k)
-            tc_mma_bf16_ts(t_o, tmem + C::TMEM_S + st * BN + k * 8,
-                           sdesc_sw128(vb + k * 2048, C::CHUNK, 1024), idesc_o, (j | k) != 0);
-          tc_commit(o_done);
-          tc_commit(v_empty + 8 * st);
-        }
-        jg += n_tiles;
-      }
-      tc_commit(drain);
-      mbar_wait(drain, 0, nullptr);
-    }
-  } else {
-    // ------------------------------------------- softmax (half a row each)
-    const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
-    const int row = quarter * 32 + lane;
-    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    bool ok = true;
-    int jg = 0;
-    for (int idx = blockIdx.x, it = 0; idx < n_items && ok; idx += gridDim.x, ++it) {
-      int mt, h, b;
-      fwd_item(idx, n_qt, nh, B, mt, h, b);
-      const int n_tiles = min(n_qt, mt + 1);
-      const int qpos = mt * BM + row;
-      const int tok0 = b * S;
-      const uint32_t t_o = tmem + lane_base + C::TMEM_O + (it & 1) * D;
-      float m_run = -INFINITY, l_part = 0.f;
-      for (int j = 0; j < n_tiles; ++j) {
-        const int jj = jg + j, st = jj & 1;
-        if (!warp_wait(s_full + 8 * st, (jj >> 1) & 1, err)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        uint32_t sv[64];
-        const uint32_t ts = tmem + lane_base + C::TMEM_S + st * BN;
-        tmem_ld32(ts + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-        tmem_ld32(ts + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-        tmem_ld_wait();
-        const int c0 = j * BN + half * 64;  // key position of sv[0]
-        // the row maximum of the raw scores (the scale is positive, so it
-        // commutes with the maximum), in four independent chains
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        const bool edge = (c0 + 64 > qpos) || (c0 + 64 > S);
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          if (edge && (c0 + c > qpos || c0 + c >= S)) sv[c] = __float_as_uint(-INFINITY);
-          m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sv[c]));
-        }
-        float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * scale_log2;
-        // row maximum over both halves of the row (both halves have finished
-        // reading this S buffer once past the barrier, so P may overwrite it)
-        red_max[(st * 2 + half) * 128 + row] = mx;
-        named_bar_sync(1 + quarter, 64);
-        mx = fmaxf(mx, red_max[(st * 2 + (half ^ 1)) * 128 + row]);
-        float alpha = 1.f;
-        if (mx > m_run + kRescaleLog2) {
-          alpha = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - mx);
-          m_run = mx;
-        }
-        float sum = 0.f;
-        // p = 2^(s scale - m): one FMA per score (masked scores are -inf;
-        // m is finite, every row has an unmasked key in its first tile)
-        const float nm = -m_run;
-#pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sv[c]), scale_log2, nm));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sv[c + 1]), scale_log2, nm));
-          sum += p0 + p1;
-          sv[c / 2] = pack_bf16x2(p0, p1);
-        }
-        l_part = l_part * alpha + sum;
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          // O is being accumulated by P_{jj-1} V until it completes
-          if (!warp_wait(o_done, (jj - 1) & 1, err)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll 1
-          for (int c = 0; c < D / 64; ++c) {
-            uint32_t ov[32];
-            const uint32_t to = t_o + half * (D / 2) + c * 32;
-            tmem_ld32(to, ov);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tmem_st32(to, ov);
-          }
-        }
-        // P (bf16 pairs) over the first 64 columns of this S buffer: keys
-        // [64 half, 64 half + 64) -> columns [32 half, 32 half + 32)
-        tmem_st32(ts + half * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(p_full);
-      }
-      if (!ok || !warp_wait(o_done, (jg + n_tiles - 1) & 1, err)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      red_sum[half * 128 + row] = l_part;
-      named_bar_sync(1 + quarter, 64);
-      const float l = l_part + red_sum[(half ^ 1) * 128 + row];
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      bf16* orow = o + (int64_t)(tok0 + qpos) * (nh * D) + h * D + half * (D / 2);
-#pragma unroll 1
-      for (int c = 0; c < D / 64; ++c) {
-        uint32_t ov[32];
-        tmem_ld32(t_o + half * (D / 2) + c * 32, ov);
-        tmem_ld_wait();
-        if (qpos < S) store_row32_bf16(orow + c * 32, ov, inv);
-      }
-      // this O buffer is free for item it + 2
-      tc_fence_before();
-      mbar_arrive(o_free + 8 * (it & 1));
-      if (half == 0 && qpos < S)
-        lse[((int64_t)b * nh + h) * S + qpos] = (m_run + __log2f(l)) * kLn2F;
-      jg += n_tiles;
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (err && *reinterpret_cast<volatile int*>(err) != 0) {
-    // after a timed-out wait, copies issued just before may still be landing
-    // in this CTA's shared memory: let them finish before it exits
-    const uint64_t t0 = global_timer_ns();
-    while (global_timer_ns() - t0 < 200000ull) {
-    }
-  }
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, C::TMEM_COLS);
-  }
-}
 
 // ---------------------------------------------------- forward, two tiles
 // Each work item is a pair of 128-query tiles (A: queries [256 i, 256 i + 128),
