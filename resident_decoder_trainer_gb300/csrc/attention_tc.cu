@@ -28,12 +28,14 @@
 //    TMEM columns as packed bf16 and read as the A operands of dV += P^T dO
 //    and dK += dS^T Q, which accumulate in TMEM over the whole group (the
 //    GQA reduction costs nothing);
-//  * dQ, one CTA per (128-query tile, head, sequence): S and dP are
-//    recomputed per key tile, dS is written to TMEM as packed bf16 (two
-//    buffers) and read as the A operand of dQ += dS K, which accumulates in
-//    TMEM and is written once; K comes through a 3-deep ring (it is read
-//    again by dQ += dS K after the elementwise pass), V through a 2-deep one
-//    freed as soon as dP = dO V^T completes.
+//  * dQ, persistent: each CTA walks (128-query tile, head, sequence) items
+//    longest first; S and dP are recomputed per key tile, dS is written to
+//    TMEM as packed bf16 (two buffers) and read as the A operand of
+//    dQ += dS K, which accumulates in TMEM and is written once per item
+//    while the next item's first scores are computed; K comes through a
+//    3-deep ring (it is read again by dQ += dS K after the elementwise
+//    pass), V through a 2-deep one freed as soon as dP = dO V^T completes;
+//    both rings run across items.
 // Every operand transposition is a shared-memory descriptor, never a copy.
 #include <type_traits>
 
@@ -732,28 +734,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + C::OFF_BAR;
-  // bars: qd_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full, s_used,
-  // ds_ready, ds_free[2], fin, drain
-  const uint32_t qd_full = bar0, k_full = bar0 + 8, k_empty = k_full + 8 * KST,
-                 v_full = k_empty + 8 * KST, v_empty = v_full + 8 * VST,
-                 s_full = v_empty + 8 * VST, s_used = s_full + 8, ds_ready = s_used + 8,
-                 ds_free = ds_ready + 8, fin = ds_free + 16, drain = fin + 8;
+  // bars: q_full, q_empty, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full,
+  // s_used, ds_ready, ds_free[2], dq_done, dq_free, drain
+  const uint32_t q_full = bar0, q_empty = bar0 + 8, k_full = bar0 + 16,
+                 k_empty = k_full + 8 * KST, v_full = k_empty + 8 * KST,
+                 v_empty = v_full + 8 * VST, s_full = v_empty + 8 * VST, s_used = s_full + 8,
+                 ds_ready = s_used + 8, ds_free = ds_ready + 8, dq_done = ds_free + 16,
+                 dq_free = dq_done + 8, drain = dq_free + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 192);
-  static_assert(8 * (1 + 2 * KST + 2 * VST + 7) <= 192, "dQ barriers overlap the TMEM slot");
+  static_assert(8 * (2 + 2 * KST + 2 * VST + 8) <= 192, "dQ barriers overlap the TMEM slot");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_qt = (S + BM - 1) / BM;
   const int per = nh * B;
-  const int mt = n_qt - 1 - static_cast<int>(blockIdx.x) / per;  // longest rows first
-  const int rem = static_cast<int>(blockIdx.x) % per;
-  const int h = rem % nh, b = rem / nh;
-  const int g = h / (nh / nkv);
-  const int m0 = mt * BM;
-  const int n_tiles = min(n_qt, mt + 1);
-  const int tok0 = b * S;
+  const int n_items = n_qt * per;
+  const int grp = nh / nkv;
+  // item idx (longest rows first) -> query tile mt, head h, sequence b
+  auto item = [&](int idx, int& mt, int& h, int& b) {
+    mt = n_qt - 1 - idx / per;
+    const int rem = idx % per;
+    h = rem % nh;
+    b = rem / nh;
+  };
 
   if (threadIdx.x == 0) {
-    mbar_init(qd_full, 1);
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int i = 0; i < KST; ++i) {
       mbar_init(k_full + 8 * i, 1);
       mbar_init(k_empty + 8 * i, 1);
@@ -767,7 +773,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(ds_ready, kEltThreads);
     mbar_init(ds_free, 1);
     mbar_init(ds_free + 8, 1);
-    mbar_init(fin, 1);
+    mbar_init(dq_done, 1);
+    mbar_init(dq_free, kEltThreads);
     mbar_init(drain, 1);
     fence_mbar_init();
   }
@@ -785,92 +792,114 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(qd_full, 2 * C::T_BYTES);
-      for (int c = 0; c < DCH; ++c) {
-        tma_load_2d(sbase + C::OFF_Q + c * C::CHUNK, &tq, qd_full, h * D + c * 64, tok0 + m0);
-        tma_load_2d(sbase + C::OFF_DO + c * C::CHUNK, &tdo, qd_full, h * D + c * 64, tok0 + m0);
-      }
-      // per stage: bit 0 a copy was issued, bit 1 the parity it completes
-      uint32_t pend_k = 0, pend_v = 0;
+      // --------------------------------------------------------- producer
       bool ok = true;
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const int ks = j % KST, vs = j % VST;
-        const uint32_t kph = (j / KST) & 1, vph = (j / VST) & 1;
-        if (!mbar_wait(k_empty + 8 * ks, kph ^ 1, err)) {
+      int jg = 0;  // key tiles loaded so far (the rings run across items)
+      for (int idx = blockIdx.x, it = 0; idx < n_items && ok; idx += gridDim.x, ++it) {
+        int mt, h, b;
+        item(idx, mt, h, b);
+        const int g = h / grp, tok0 = b * S, n_tiles = min(n_qt, mt + 1);
+        // Q and dO of this item once the previous item's last S / dP have read theirs
+        if (!mbar_wait(q_empty, (it & 1) ^ 1, err)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(k_full + 8 * ks, C::T_BYTES);
-        for (int c = 0; c < DCH; ++c)
-          tma_load_2d(sbase + C::OFF_K + ks * C::T_BYTES + c * C::CHUNK, &tk, k_full + 8 * ks,
-                      g * D + c * 64, tok0 + j * BN);
-        pend_k = (pend_k & ~(3u << (2 * ks))) | ((1u | (kph << 1)) << (2 * ks));
-        if (!mbar_wait(v_empty + 8 * vs, vph ^ 1, err)) {
-          ok = false;
-          break;
+        mbar_arrive_expect_tx(q_full, 2 * C::T_BYTES);
+        for (int c = 0; c < DCH; ++c) {
+          tma_load_2d(sbase + C::OFF_Q + c * C::CHUNK, &tq, q_full, h * D + c * 64,
+                      tok0 + mt * BM);
+          tma_load_2d(sbase + C::OFF_DO + c * C::CHUNK, &tdo, q_full, h * D + c * 64,
+                      tok0 + mt * BM);
         }
-        mbar_arrive_expect_tx(v_full + 8 * vs, C::T_BYTES);
-        for (int c = 0; c < DCH; ++c)
-          tma_load_2d(sbase + C::OFF_V + vs * C::T_BYTES + c * C::CHUNK, &tv, v_full + 8 * vs,
-                      g * D + c * 64, tok0 + j * BN);
-        pend_v = (pend_v & ~(3u << (2 * vs))) | ((1u | (vph << 1)) << (2 * vs));
-      }
-      if (!ok) {
-        mbar_wait(qd_full, 0, nullptr);
-        for (int st = 0; st < KST; ++st)
-          if ((pend_k >> (2 * st)) & 1u) mbar_wait(k_full + 8 * st, (pend_k >> (2 * st + 1)) & 1u, nullptr);
-        for (int st = 0; st < VST; ++st)
-          if ((pend_v >> (2 * st)) & 1u) mbar_wait(v_full + 8 * st, (pend_v >> (2 * st + 1)) & 1u, nullptr);
+        for (int j = 0; j < n_tiles && ok; ++j) {
+          const int jj = jg + j, ks = jj % KST, vs = jj % VST;
+          if (!mbar_wait(k_empty + 8 * ks, ((jj / KST) & 1) ^ 1, err)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(k_full + 8 * ks, C::T_BYTES);
+          for (int c = 0; c < DCH; ++c)
+            tma_load_2d(sbase + C::OFF_K + ks * C::T_BYTES + c * C::CHUNK, &tk, k_full + 8 * ks,
+                        g * D + c * 64, tok0 + j * BN);
+          if (!mbar_wait(v_empty + 8 * vs, ((jj / VST) & 1) ^ 1, err)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(v_full + 8 * vs, C::T_BYTES);
+          for (int c = 0; c < DCH; ++c)
+            tma_load_2d(sbase + C::OFF_V + vs * C::T_BYTES + c * C::CHUNK, &tv, v_full + 8 * vs,
+                        g * D + c * 64, tok0 + j * BN);
+        }
+        jg += n_tiles;
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
+      // -------------------------------------------------------------- MMA
       constexpr uint32_t id_s = idesc_bf16_f32(BM, BN, 0, 0);  // S, dP
       constexpr uint32_t id_q = idesc_bf16_f32(BM, D, 0, 1);   // dQ (A = dS from TMEM)
-      bool ok = mbar_wait(qd_full, 0, err);
-      auto issue_s = [&](int j) -> bool {
-        const int ks = j % KST, vs = j % VST;
-        if (!mbar_wait(k_full + 8 * ks, (j / KST) & 1, err) ||
-            !mbar_wait(v_full + 8 * vs, (j / VST) & 1, err) ||
-            !mbar_wait(s_used, (j & 1) ^ 1, err))
-          return false;
-        tc_fence_after();
-        const uint32_t kb = sbase + C::OFF_K + ks * C::T_BYTES;
-        const uint32_t vb = sbase + C::OFF_V + vs * C::T_BYTES;
+      bool ok = true;
+      int jg = 0;
+      for (int idx = blockIdx.x, it = 0; idx < n_items && ok; idx += gridDim.x, ++it) {
+        int mt, h, b;
+        item(idx, mt, h, b);
+        const int n_tiles = min(n_qt, mt + 1);
+        // S = Q K^T and dP = dO V^T of key tile j, once the elementwise warps
+        // have read the previous tile's S and dP
+        auto issue_s = [&](int j) -> bool {
+          const int jj = jg + j, ks = jj % KST, vs = jj % VST;
+          if (!mbar_wait(k_full + 8 * ks, (jj / KST) & 1, err) ||
+              !mbar_wait(v_full + 8 * vs, (jj / VST) & 1, err) ||
+              !mbar_wait(s_used, (jj & 1) ^ 1, err))
+            return false;
+          tc_fence_after();
+          const uint32_t kb = sbase + C::OFF_K + ks * C::T_BYTES;
+          const uint32_t vb = sbase + C::OFF_V + vs * C::T_BYTES;
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * C::CHUNK + (k & 3) * 32;
-          tc_mma_bf16(tmem + C::T_S, sdesc_sw128(sbase + C::OFF_Q + off, 16, 1024),
-                      sdesc_sw128(kb + off, 16, 1024), id_s, k > 0);
-          tc_mma_bf16(tmem + C::T_DP, sdesc_sw128(sbase + C::OFF_DO + off, 16, 1024),
-                      sdesc_sw128(vb + off, 16, 1024), id_s, k > 0);
-        }
-        tc_commit(s_full);
-        tc_commit(v_empty + 8 * vs);  // V is read by dP only
-        return true;
-      };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const int ks = j % KST;
-        if (j + 1 < n_tiles && !issue_s(j + 1)) {
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k >> 2) * C::CHUNK + (k & 3) * 32;
+            tc_mma_bf16(tmem + C::T_S, sdesc_sw128(sbase + C::OFF_Q + off, 16, 1024),
+                        sdesc_sw128(kb + off, 16, 1024), id_s, k > 0);
+            tc_mma_bf16(tmem + C::T_DP, sdesc_sw128(sbase + C::OFF_DO + off, 16, 1024),
+                        sdesc_sw128(vb + off, 16, 1024), id_s, k > 0);
+          }
+          tc_commit(s_full);
+          tc_commit(v_empty + 8 * vs);  // V is read by dP only
+          if (j + 1 == n_tiles) tc_commit(q_empty);  // the item's last read of Q and dO
+          return true;
+        };
+        if (!mbar_wait(q_full, it & 1, err) || !issue_s(0)) {
           ok = false;
           break;
         }
-        if (!mbar_wait(ds_ready, j & 1, err)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t kb = sbase + C::OFF_K + ks * C::T_BYTES;
-        const uint32_t ds = tmem + C::T_DS + (j & 1) * 64;
+        for (int j = 0; j < n_tiles && ok; ++j) {
+          const int jj = jg + j, ks = jj % KST;
+          if (j + 1 < n_tiles && !issue_s(j + 1)) {
+            ok = false;
+            break;
+          }
+          // dQ of the previous item has been read out of TMEM
+          if (j == 0 && !mbar_wait(dq_free, (it & 1) ^ 1, err)) {
+            ok = false;
+            break;
+          }
+          if (!mbar_wait(ds_ready, jj & 1, err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t kb = sbase + C::OFF_K + ks * C::T_BYTES;
+          const uint32_t ds = tmem + C::T_DS + (jj & 1) * 64;
 #pragma unroll
-        for (int k = 0; k < BN / 16; ++k)
-          tc_mma_bf16_ts(tmem + C::T_DQ, ds + 8 * k, sdesc_sw128(kb + k * 2048, C::CHUNK, 1024),
-                         id_q, (j | k) != 0);
-        tc_commit(ds_free + 8 * (j & 1));
-        tc_commit(k_empty + 8 * ks);
+          for (int k = 0; k < BN / 16; ++k)
+            tc_mma_bf16_ts(tmem + C::T_DQ, ds + 8 * k, sdesc_sw128(kb + k * 2048, C::CHUNK, 1024),
+                           id_q, (j | k) != 0);
+          tc_commit(ds_free + 8 * (jj & 1));
+          tc_commit(k_empty + 8 * ks);
+        }
+        if (ok) tc_commit(dq_done);
+        jg += n_tiles;
       }
-      tc_commit(fin);
       tc_commit(drain);
       mbar_wait(drain, 0, nullptr);
     }
@@ -879,75 +908,85 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
-    const int qpos = m0 + row;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const bool qvalid = qpos < S;
-    const int64_t seg = ((int64_t)b * nh + h) * S_pad + qpos;
-    const float l2 = qvalid ? lse2[seg] : 0.f;
-    const float drow = qvalid ? Dd[seg] : 0.f;
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      if (!warp_wait(s_full, j & 1, err)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int c0 = j * BN + half * 64;
-      // keys c0 + c with c < lim are visible to this query row; the mask is
-      // applied only where some row of the warp needs it (diagonal tiles)
-      const int lim = qvalid ? qpos + 1 - c0 : 0;
-      const bool full = __all_sync(0xffffffffu, lim >= 64);
-      uint32_t pk[32];
+    int jg = 0;
+    for (int idx = blockIdx.x, it = 0; idx < n_items && ok; idx += gridDim.x, ++it) {
+      int mt, h, b;
+      item(idx, mt, h, b);
+      const int n_tiles = min(n_qt, mt + 1);
+      const int qpos = mt * BM + row;
+      const bool qvalid = qpos < S;
+      const int64_t seg = ((int64_t)b * nh + h) * S_pad + qpos;
+      const float l2 = qvalid ? lse2[seg] : 0.f;
+      const float drow = qvalid ? Dd[seg] : 0.f;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int jj = jg + j;
+        if (!warp_wait(s_full, jj & 1, err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int c0 = j * BN + half * 64;
+        // keys c0 + c with c < lim are visible to this query row; the mask is
+        // applied only where some row of the warp needs it (diagonal tiles)
+        const int lim = qvalid ? qpos + 1 - c0 : 0;
+        const bool full = __all_sync(0xffffffffu, lim >= 64);
+        uint32_t pk[32];
 #pragma unroll
-      for (int qt = 0; qt < 2; ++qt) {
-        uint32_t sv[32], dp[32];
-        const uint32_t t0 = tmem + lane_base + half * 64 + qt * 32;
-        tmem_ld32(t0 + C::T_S, sv);
-        tmem_ld32(t0 + C::T_DP, dp);
-        tmem_ld_wait();
-        if (full) {
+        for (int qt = 0; qt < 2; ++qt) {
+          uint32_t sv[32], dp[32];
+          const uint32_t t0 = tmem + lane_base + half * 64 + qt * 32;
+          tmem_ld32(t0 + C::T_S, sv);
+          tmem_ld32(t0 + C::T_DP, dp);
+          tmem_ld_wait();
+          if (full) {
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            float d2[2];
+            for (int c = 0; c < 32; c += 2) {
+              float d2[2];
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float p = ex2_approx(__uint_as_float(sv[c + e]) * scale_log2 - l2);
-              d2[e] = p * (__uint_as_float(dp[c + e]) - drow);
+              for (int e = 0; e < 2; ++e) {
+                const float p = ex2_approx(__uint_as_float(sv[c + e]) * scale_log2 - l2);
+                d2[e] = p * (__uint_as_float(dp[c + e]) - drow);
+              }
+              pk[qt * 16 + c / 2] = pack_bf16x2(d2[0], d2[1]);
             }
-            pk[qt * 16 + c / 2] = pack_bf16x2(d2[0], d2[1]);
-          }
-        } else {
+          } else {
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            float d2[2];
+            for (int c = 0; c < 32; c += 2) {
+              float d2[2];
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float p = qt * 32 + c + e < lim
-                                  ? ex2_approx(__uint_as_float(sv[c + e]) * scale_log2 - l2)
-                                  : 0.f;
-              d2[e] = p * (__uint_as_float(dp[c + e]) - drow);
+              for (int e = 0; e < 2; ++e) {
+                const float p = qt * 32 + c + e < lim
+                                    ? ex2_approx(__uint_as_float(sv[c + e]) * scale_log2 - l2)
+                                    : 0.f;
+                d2[e] = p * (__uint_as_float(dp[c + e]) - drow);
+              }
+              pk[qt * 16 + c / 2] = pack_bf16x2(d2[0], d2[1]);
             }
-            pk[qt * 16 + c / 2] = pack_bf16x2(d2[0], d2[1]);
           }
         }
+        tc_fence_before();
+        mbar_arrive(s_used);
+        // dS buffer jj & 1 was last read by dQ += dS K of tile jj - 2
+        if (!warp_wait(ds_free + 8 * (jj & 1), ((jj >> 1) & 1) ^ 1, err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // keys c0 .. c0 + 63 as bf16 pairs: columns half * 32 .. + 31 of the buffer
+        tmem_st32(tmem + lane_base + C::T_DS + (jj & 1) * 64 + half * 32, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(ds_ready);
       }
-      tc_fence_before();
-      mbar_arrive(s_used);
-      // dS buffer j & 1 was last read by dQ += dS K of tile j - 2
-      if (j >= 2 && !warp_wait(ds_free + 8 * (j & 1), ((j >> 1) & 1) ^ 1, err)) {
+      jg += n_tiles;
+      if (!ok || !warp_wait(dq_done, it & 1, err)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // keys c0 .. c0 + 63 as bf16 pairs: columns half * 32 .. + 31 of the buffer
-      tmem_st32(tmem + lane_base + C::T_DS + (j & 1) * 64 + half * 32, pk);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(ds_ready);
-    }
-    if (ok && warp_wait(fin, 0, err)) {
-      tc_fence_after();
-      float* out = dq + (int64_t)(tok0 + qpos) * (nh * D) + h * D + half * (D / 2);
+      float* out = dq + (int64_t)(b * S + qpos) * (nh * D) + h * D + half * (D / 2);
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         uint32_t a[32];
@@ -955,11 +994,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         if (qvalid) store_row32_f32(out + c * 32, a, scale);
       }
+      // the dQ accumulator is free for the next item
+      tc_fence_before();
+      mbar_arrive(dq_free);
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if (err && *reinterpret_cast<volatile int*>(err) != 0) {
+    // after a timed-out wait, copies issued just before may still be landing
+    // in this CTA's shared memory: let them finish before it exits
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 200000ull) {
+    }
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
@@ -1042,8 +1091,10 @@ static cudaError_t bwd_tc_d(const bf16* q, int64_t ldq, const bf16* k, int64_t l
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   note_launch();
-  attn_bwd_dq_tc_kernel<D><<<n_t * nh * B, kThreads, DqCfg<D>::SMEM, s>>>(
-      tq128, tk, tv, tdo128, lse2, Dd, S_pad, dq, B, S, nh, nkv, scale, scale * kLog2eF, err);
+  const int dq_items = n_t * nh * B;  // persistent: one CTA per SM walks the items
+  attn_bwd_dq_tc_kernel<D><<<dq_items < num_sms() ? dq_items : num_sms(), kThreads,
+                             DqCfg<D>::SMEM, s>>>(tq128, tk, tv, tdo128, lse2, Dd, S_pad, dq, B,
+                                                  S, nh, nkv, scale, scale * kLog2eF, err);
   return cudaGetLastError();
 }
 
