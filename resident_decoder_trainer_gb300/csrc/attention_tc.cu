@@ -940,6 +940,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(t0 + C::T_S, sv);
           tmem_ld32(t0 + C::T_DP, dp);
           tmem_ld_wait();
+          if (qt == 1) {
+            // every S / dP column this thread reads is in registers: the next
+            // tile's S and dP may overwrite them while this half is computed
+            tc_fence_before();
+            mbar_arrive(s_used);
+          }
           if (full) {
 #pragma unroll
             for (int c = 0; c < 32; c += 2) {
@@ -966,8 +972,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        tc_fence_before();
-        mbar_arrive(s_used);
         // dS buffer jj & 1 was last read by dQ += dS K of tile jj - 2
         if (!warp_wait(ds_free + 8 * (jj & 1), ((jj >> 1) & 1) ^ 1, err)) {
           ok = false;

@@ -305,14 +305,18 @@ __global__ void __launch_bounds__(256) qknorm_rope_fwd_kernel(
     const float4* c4 = reinterpret_cast<const float4*>(cs + (int64_t)(t % S) * HALF + i0);
     const float4 c01 = c4[0], c23 = c4[1];
     const float* row = qkv + (int64_t)t * ld + 4 * sub;
-    for (int g0 = warp; g0 < groups; g0 += 16) {
-      const int h0 = g0 * HPW + slot, h1 = (g0 + 8) * HPW + slot;
-      const float4 x0 = h0 < heads ? *reinterpret_cast<const float4*>(row + h0 * D)
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-      const float4 x1 = h1 < heads ? *reinterpret_cast<const float4*>(row + h1 * D)
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-      head_out(t, h0, x0, c01, c23);
-      if (g0 + 8 < groups) head_out(t, h1, x1, c01, c23);
+    // three heads' loads in flight per warp
+    for (int g0 = warp; g0 < groups; g0 += 24) {
+      float4 x[3];
+#pragma unroll
+      for (int u = 0; u < 3; ++u) {
+        const int hu = (g0 + 8 * u) * HPW + slot;
+        x[u] = hu < heads ? *reinterpret_cast<const float4*>(row + hu * D)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 3; ++u)
+        if (g0 + 8 * u < groups) head_out(t, (g0 + 8 * u) * HPW + slot, x[u], c01, c23);
     }
   }
 }
