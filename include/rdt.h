@@ -100,8 +100,8 @@ size_t rdt_block_saved_bytes(const rdt_config* cfg, int32_t batch, int32_t seq);
 /* Scratch bytes of rdt_block_forward / rdt_block_backward (256-byte aligned). */
 size_t rdt_block_workspace_bytes(const rdt_config* cfg, int32_t batch, int32_t seq);
 /* Scratch bytes of rdt_fused_cross_entropy for `tokens` tokens: O(tokens *
- * H) plus a fixed ~64 MB vocabulary chunk; it does not grow with tokens * V
- * (the logits are never stored whole). */
+ * H) plus one vocabulary chunk of at most 256 MB; it does not grow with
+ * tokens * V (the logits are never stored whole). */
 size_t rdt_head_workspace_bytes(const rdt_config* cfg, int32_t tokens);
 /* Scratch bytes of rdt_sq_sum. */
 size_t rdt_sq_sum_workspace_bytes(void);
@@ -159,7 +159,7 @@ rdt_status rdt_block_backward(const rdt_config* cfg, int32_t batch, int32_t seq,
  * (train_step_inner's fused cross-entropy; gpu_forward's final norm and LM
  * head; gpu_backward's LM-head and final-norm backward; KAIZEN-050/052's
  * fused CE). The logits are never stored whole, on the device or the host:
- * the vocabulary is walked in chunks of about 64 MB of bf16 dz; each chunk's
+ * the vocabulary is walked in chunks of at most 256 MB of bf16 dz; each chunk's
  * logits are formed in the GEMMs' fp32 tensor-memory accumulators, once for
  * the log-sum-exp and the target's logit (forward) and once more for dz,
  * computed in fp32 from the saved log-sum-exp (backward). Nothing but the

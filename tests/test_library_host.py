@@ -61,10 +61,11 @@ def test_sizes_are_positive_and_aligned(lib):
               rdt.head_workspace_bytes(cfg, s.tokens)):
         assert n > 0 and n % 256 == 0
     # the head never holds the logits of every token: its scratch is a few
-    # [T, H] buffers and one vocabulary chunk, far below the bf16 [T, V] logits
+    # [T, H] buffers and one vocabulary chunk (at most 256 MB), well below the
+    # bf16 [T, V] logits
     head = rdt.head_workspace_bytes(cfg, s.tokens)
-    assert head < 2 * s.tokens * s.vocab // 4
-    assert head < 32 * s.tokens * s.hidden + (80 << 20)
+    assert head < 2 * s.tokens * s.vocab // 2
+    assert head < 32 * s.tokens * s.hidden + (272 << 20)
     # ... and it grows with the vocabulary only by the clip's per-tile slots
     wide = rdt.Config.from_shape(s.replace(vocab=4 * s.vocab))
     assert rdt.head_workspace_bytes(wide, s.tokens) - head < (16 << 20)
