@@ -161,6 +161,7 @@ struct BlockWs {
   bf16 *dy_b, *dgu, *dr1_b, *dout, *dqkv;
   float *dxn, *dr1, *Dd, *lse2, *dq, *dk, *partials;
   double* sqp;  // squared-sum slots of the weight-gradient GEMMs
+  double* sq2;  // their per-CTA partial sums (kSqCtas)
   float* split;  // split-K partials of the [T, hidden] projections
   int64_t split_floats;
 };
@@ -188,6 +189,7 @@ size_t carve_block_ws(const Dims& m, int64_t B, int64_t S, void* base, BlockWs* 
                          gemm_sq_slots_bound((int)(2 * m.I), (int)m.H) +
                          gemm_sq_slots_bound((int)m.H, (int)m.qd) +
                          gemm_sq_slots_bound((int)m.nqkv, (int)m.H));
+  t.sq2 = c.take<double>(kSqCtas);
   t.split_floats = split_floats_for(T, m.H);
   t.split = c.take<float>(t.split_floats);
   if (w) *w = t;
@@ -213,6 +215,7 @@ struct HeadWs {
   int64_t vc;    // vocabulary columns per chunk
   int part_ld;   // (max, sum exp) partials per row of one chunk
   double* sqp;   // squared-sum slots of the dW_lm GEMMs
+  double* sq2;   // their per-CTA partial sums (kSqCtas)
   float* split;  // split-K partials of dh_n
   int64_t split_floats;
 };
@@ -234,6 +237,7 @@ size_t carve_head_ws(const Dims& m, int64_t T, void* base, HeadWs* w) {
   for (int64_t v0 = 0; v0 < m.V; v0 += t.vc)
     slots += gemm_sq_slots_bound((int)std::min(t.vc, m.V - v0), (int)m.H);
   t.sqp = c.take<double>(slots);
+  t.sq2 = c.take<double>(kSqCtas);
   t.split_floats = split_floats_for(T, m.H);
   t.split = c.take<float>(t.split_floats);
   if (w) *w = t;
@@ -405,6 +409,7 @@ struct Nf4Ws {
   bf16 *du_qkv, *du_o, *du_gu, *du_d;
   float* gain_sink;
   double* sqp;  // squared-sum slots of the adapter-gradient GEMMs
+  double* sq2;  // their per-CTA partial sums (kSqCtas)
   float* split;  // split-K partials of the adapter GEMMs (few output tiles, long K)
   int64_t split_floats;
 };
@@ -429,6 +434,7 @@ size_t carve_nf4_ws(const Dims& m, int64_t r, int64_t B, int64_t S, void* base, 
   t.du_d = c.take<bf16>(T * r);
   t.gain_sink = c.take<float>(2 * m.H + 2 * m.d);
   t.sqp = c.take<double>(lora_sq_slots_bound(m, r));
+  t.sq2 = c.take<double>(kSqCtas);
   // room for 8 K-slices of the widest [r..3r, out] adapter gradient, 16 of
   // the [T, 3r] down-projections
   const int64_t wide = std::max(std::max(m.H, m.I), std::max(m.qd, m.nqkv));
@@ -786,7 +792,7 @@ rdt_status rdt_block_backward(const rdt_config* cfg, int32_t batch, int32_t seq,
     const float* gains[4] = {grads + off[RDT_G_ATTN], grads + off[RDT_G_FFN],
                              grads + off[RDT_G_Q], grads + off[RDT_G_K]};
     const int64_t lens[4] = {m.H, m.H, m.d, m.d};
-    RDT_CHECK_CUDA(sq_reduce(wk.sqp, sq_n, gains, lens, 4, grad_sq, true, s));
+    RDT_CHECK_CUDA(sq_reduce(wk.sqp, sq_n, gains, lens, 4, grad_sq, true, wk.sq2, s));
   }
   return RDT_OK;
 }
@@ -888,7 +894,7 @@ rdt_status rdt_fused_cross_entropy(const rdt_config* cfg, int32_t tokens, const 
     // = the dW_lm slots and the final gain's squares (the first gradients of a step)
     const float* gains[1] = {dgamma_f};
     const int64_t lens[1] = {m.H};
-    RDT_CHECK_CUDA(sq_reduce(wk.sqp, sq_n, gains, lens, 1, grad_sq, false, s));
+    RDT_CHECK_CUDA(sq_reduce(wk.sqp, sq_n, gains, lens, 1, grad_sq, false, wk.sq2, s));
   }
   return RDT_OK;
 }
@@ -1476,7 +1482,8 @@ rdt_status rdt_nf4_block_backward(const rdt_config* cfg, int32_t rank, float alp
   // input RMSNorm backward (frozen gain) + identity skip
   RDT_CHECK_CUDA(rmsnorm_bwd(wk.dxn, x, sv.rstd1, g_attn, wk.dr1, dx, nullptr, nw.gain_sink,
                              wk.partials, T, (int)m.H, s));
-  if (grad_sq) RDT_CHECK_CUDA(sq_reduce(nw.sqp, sq_n, nullptr, nullptr, 0, grad_sq, true, s));
+  if (grad_sq)
+    RDT_CHECK_CUDA(sq_reduce(nw.sqp, sq_n, nullptr, nullptr, 0, grad_sq, true, nw.sq2, s));
   return RDT_OK;
 }
 

@@ -493,45 +493,55 @@ struct SmallBufs {
   const float* p[4];
   int64_t n[4];
 };
-__global__ void __launch_bounds__(1024) sq_reduce_kernel(const double* __restrict__ parts,
-                                                         int64_t n, const SmallBufs sb, int nsmall,
-                                                         double* out, int accumulate) {
-  __shared__ double red[1024];
+// Squared-sum slots -> one fp64 total in two launches (latency, not bytes,
+// bounds this: ~26 k slots per block backward): kSqCtas CTAs each add a fixed
+// slice of the slots and a fixed stride of the gain buffers' squares, then one
+// warp adds the kSqCtas partials in index order (deterministic).
+__global__ void __launch_bounds__(256) sq_part_kernel(const double* __restrict__ parts,
+                                                      int64_t n, const SmallBufs sb, int nsmall,
+                                                      double* __restrict__ part2) {
+  __shared__ double red[8];
+  const int64_t per = (n + kSqCtas - 1) / kSqCtas;
+  const int64_t lo = (int64_t)blockIdx.x * per;
+  const int64_t hi = lo + per < n ? lo + per : n;
   double acc = 0.0;
-  // eight independent loads in flight per thread, then the remainder
-  int64_t i = threadIdx.x;
-  for (; i + 7 * 1024 < n; i += 8 * 1024) {
-    double a[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) a[k] = parts[i + k * 1024];
-    acc += ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
-  }
-  for (; i < n; i += 1024) acc += parts[i];
-  for (int b = 0; b < nsmall; ++b)
-    for (int64_t i = threadIdx.x; i < sb.n[b]; i += blockDim.x) {
-      const double v = sb.p[b][i];
+  for (int64_t i = lo + threadIdx.x; i < hi; i += 256) acc += parts[i];
+  const int64_t gt = (int64_t)blockIdx.x * 256 + threadIdx.x;
+  for (int k = 0; k < nsmall; ++k)
+    for (int64_t i = gt; i < sb.n[k]; i += (int64_t)kSqCtas * 256) {
+      const double v = sb.p[k][i];
       acc += v * v;
     }
-  red[threadIdx.x] = acc;
+  acc = warp_sum_d(acc);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
   __syncthreads();
-  for (int h = 512; h > 0; h >>= 1) {
-    if (static_cast<int>(threadIdx.x) < h) red[threadIdx.x] += red[threadIdx.x + h];
-    __syncthreads();
+  if (threadIdx.x == 0) {
+    double t = 0.0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) t += red[w];
+    part2[blockIdx.x] = t;
   }
-  if (threadIdx.x == 0) *out = (accumulate ? *out : 0.0) + red[0];
+}
+
+__global__ void __launch_bounds__(32) sq_final2_kernel(const double* __restrict__ part2,
+                                                       double* out, int accumulate) {
+  double v = part2[threadIdx.x] + part2[threadIdx.x + 32];
+  v = warp_sum_d(v);
+  if (threadIdx.x == 0) *out = (accumulate ? *out : 0.0) + v;
 }
 
 cudaError_t sq_reduce(const double* parts, int64_t n, const float* const* small,
                       const int64_t* small_len, int nsmall, double* out, bool accumulate,
-                      cudaStream_t s) {
-  if (nsmall < 0 || nsmall > 4) return cudaErrorInvalidValue;
+                      double* scratch, cudaStream_t s) {
+  if (nsmall < 0 || nsmall > 4 || !scratch) return cudaErrorInvalidValue;
   SmallBufs sb = {};
   for (int i = 0; i < nsmall; ++i) {
     sb.p[i] = small[i];
     sb.n[i] = small_len[i];
   }
-  note_launch();
-  sq_reduce_kernel<<<1, 1024, 0, s>>>(parts, n, sb, nsmall, out, accumulate ? 1 : 0);
+  note_launch(2);
+  sq_part_kernel<<<kSqCtas, 256, 0, s>>>(parts, n, sb, nsmall, scratch);
+  sq_final2_kernel<<<1, 32, 0, s>>>(scratch, out, accumulate ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -146,10 +146,12 @@ cudaError_t qknorm_rope_bwd(const float* dq, const float* dk, const float* qkv, 
 int qknorm_bwd_partial_rows(int T, int heads);
 
 // *out (= or +=, per `accumulate`) the fp64 sum of parts[0, n) plus the sums
-// of squares of up to 4 small fp32 arrays, in a fixed order (one CTA).
+// of squares of up to 4 small fp32 arrays, in a fixed order: kSqCtas CTAs
+// write slice sums to scratch[kSqCtas], one warp adds them in index order.
+constexpr int kSqCtas = 64;
 cudaError_t sq_reduce(const double* parts, int64_t n, const float* const* small,
                       const int64_t* small_len, int nsmall, double* out, bool accumulate,
-                      cudaStream_t s);
+                      double* scratch, cudaStream_t s);
 // out [sum of rows, np*r] bf16, block diagonal: rows of piece p (fp32
 // [rows_p, r], row-major) land in columns [p r, (p+1) r), zeros elsewhere.
 cudaError_t lora_bstack(const float* const* pieces, const int64_t* rows, int np, int r,
