@@ -39,7 +39,8 @@ UNIT = "tokens/s"
 # dram__bytes_write.sum), averaged over the q4b_full step's launch mix: 36 x
 # the 12 launches of one q4b_full-shaped block + the LM head's 76, each
 # captured alone on that small case (the shapes are the step's), and the
-# gemm.cu source it was measured on; reported only while gemm.cu is unchanged.
+# gemm.cu + api.cu sources it was measured on; reported only while they are
+# unchanged.
 GEMM_TRAFFIC_BYTES = 224659493
 GEMM_TRAFFIC_SRC_SHA = "828139ae5caebe33"
 # The same for the 8 NF4 GEMM launches of one q4b_nf4 step.
@@ -47,11 +48,21 @@ NF4_TRAFFIC_BYTES = 75663168
 NF4_TRAFFIC_SRC_SHA = "828139ae5caebe33"
 
 
-def traffic_if_current(nbytes, sha):
-    """nbytes while gemm.cu is the source the counters were taken on, else None."""
+def source_sha():
+    """sha256 prefix of the GEMM kernels (gemm.cu) and of the launch sequence
+    that picks their shapes (api.cu): the traffic figures below hold for it."""
     import hashlib
-    with open(os.path.join(ROOT, "resident_decoder_trainer_gb300", "csrc", "gemm.cu"), "rb") as fh:
-        return nbytes if hashlib.sha256(fh.read()).hexdigest()[:16] == sha else None
+    h = hashlib.sha256()
+    for name in ("gemm.cu", "api.cu"):
+        with open(os.path.join(ROOT, "resident_decoder_trainer_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_if_current(nbytes, sha):
+    """nbytes while gemm.cu and api.cu are the sources the counters were
+    taken on, else None."""
+    return nbytes if source_sha() == sha else None
 
 
 def max_over_ranks(value, world, device="cpu"):
