@@ -200,27 +200,31 @@ def stop_clock_sampler(handle):
 
 
 # ------------------------------------------------------------- CPU oracle
-# The one bounded oracle sample both the cpu_baseline leg and the reference
-# arm time (about 5 s on 16 host cores at the q4b_full shape).
-ORACLE_SAMPLE = dict(seq_tokens=1024, head_tokens=512, opt_params=1 << 25)
+# Bounded oracle samples of one q4b_full step, on 16 host cores: the
+# cpu_baseline leg times one of about 11 s; the reference arm times one of
+# about 5 s per step, so that its warm-up and timed steps end within minutes.
+CPU_BASELINE_SAMPLE = dict(seqs=2, head_tokens=1024, opt_params=1 << 26)
+ORACLE_SAMPLE = dict(seqs=1, head_tokens=512, opt_params=1 << 25)
 
 
 class OracleSample:
     """The FP64 oracle timed on a bounded sample of one step, scaled to the
-    whole step: one block forward+backward on one sequence of `seq_tokens`
-    tokens (x layers), the final norm + LM head + CE forward and backward on
+    whole step: one block forward+backward on `seqs` of the workload's
+    sequences (x layers; at most its batch), the final norm + LM head + CE
+    forward and backward on
     `head_tokens` tokens (x tokens per step), and clip + AdamW on `opt_params`
     parameters (x total parameters). Inputs are drawn once (seeded)."""
 
-    def __init__(self, shape, seq_tokens=1024, head_tokens=512, opt_params=1 << 25, seed=0):
+    def __init__(self, shape, seqs=1, head_tokens=512, opt_params=1 << 25, seed=0):
         import numpy as np
         import torch
         from oracle import model as om
         from resident_decoder_trainer_gb300 import synth
 
         self.om, self.shape = om, shape
-        self.seq_tokens, self.head_tokens, self.opt_params = seq_tokens, head_tokens, opt_params
-        self.s_blk = shape.replace(layers=1, batch=1, seq=seq_tokens)
+        self.s_blk = shape.replace(layers=1, batch=min(seqs, shape.batch))
+        self.seq_tokens = self.s_blk.tokens
+        self.head_tokens, self.opt_params = head_tokens, opt_params
         blk, x, dy = synth.make_block_inputs(self.s_blk, seed)
         self.blk = {k: om._f64(v) for k, v in blk.items()}
         self.x, self.dy = om._f64(x), om._f64(dy)
@@ -259,7 +263,7 @@ class OracleSample:
             cores = max(int(i.get("num_threads", 1)) for i in threadpool_info()) or os.cpu_count()
         except Exception:
             cores = os.cpu_count()
-        sample = (f"FP64 oracle: 1 block fwd+bwd on 1x{self.seq_tokens} tokens "
+        sample = (f"FP64 oracle: 1 block fwd+bwd on {self.s_blk.batch}x{self.s_blk.seq} tokens "
                   f"(x{shape.layers} layers), head+CE fwd+bwd on {self.head_tokens} tokens, "
                   f"clip+AdamW on {self.opt_params} params; scaled to {shape.tokens} tokens "
                   f"and {self.n_params} params per step")
@@ -405,7 +409,7 @@ def run_rdt(args, rank, world, local_rank):
     if not args.no_e2e:
         out["e2e"] = run_e2e(tr, shape, args, dev, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = OracleSample(shape, **ORACLE_SAMPLE).run()
+        out["cpu_baseline"] = OracleSample(shape, **CPU_BASELINE_SAMPLE).run()
     return out
 
 
@@ -494,17 +498,19 @@ def nf4_algorithmic_flops(shape, rank):
 
 class Nf4OracleSample:
     """The FP64 NF4 + LoRA oracle timed on a bounded sample of one step: the
-    block forward+backward on one sequence of `seq_tokens` tokens (scaled to
-    the step's tokens) plus the adapters' clip + AdamW (the full adapter set)."""
+    block forward+backward on `seqs` of the workload's sequences (at most its
+    batch; scaled to the step's tokens) plus the adapters' clip + AdamW (the
+    full adapter set)."""
 
-    def __init__(self, shape, rank, alpha, seq_tokens=1024, seed=0):
+    def __init__(self, shape, rank, alpha, seqs=1, seed=0):
         import numpy as np
         from oracle import model as om
         from oracle import nf4 as on
         from resident_decoder_trainer_gb300 import synth
         self.om, self.on, self.np = om, on, np
-        self.shape, self.rank, self.alpha, self.seq_tokens = shape, rank, alpha, seq_tokens
-        self.s_blk = shape.replace(layers=1, batch=1, seq=seq_tokens)
+        self.shape, self.rank, self.alpha = shape, rank, alpha
+        self.s_blk = shape.replace(layers=1, batch=min(seqs, shape.batch))
+        self.seq_tokens = self.s_blk.tokens
         base, gains, lora, x, dy = synth.make_nf4_inputs(self.s_blk, seed=seed, rank=rank,
                                                          b_std=0.02)
         shp = synth.block_shapes(self.s_blk)
@@ -528,7 +534,8 @@ class Nf4OracleSample:
         except Exception:
             cores = os.cpu_count()
         sample = (f"FP64 NF4+LoRA oracle: block fwd+bwd + adapter clip+AdamW on "
-                  f"1x{self.seq_tokens} tokens, scaled to {self.shape.tokens} tokens per step")
+                  f"{self.s_blk.batch}x{self.s_blk.seq} tokens, scaled to {self.shape.tokens} "
+                  "tokens per step")
         return {"value": round(self.shape.tokens / step_s, 3), "unit": UNIT, "cores": cores,
                 "kind": "oracle", "sample": sample, "sample_seconds": round(dt, 2)}
 
