@@ -200,11 +200,10 @@ def stop_clock_sampler(handle):
 
 
 # ------------------------------------------------------------- CPU oracle
-# Bounded oracle samples of one q4b_full step, on 16 host cores: the
-# cpu_baseline leg times one of about 11 s; the reference arm times one of
-# about 5 s per step, so that its warm-up and timed steps end within minutes.
-CPU_BASELINE_SAMPLE = dict(seqs=2, head_tokens=1024, opt_params=1 << 26)
-ORACLE_SAMPLE = dict(seqs=1, head_tokens=512, opt_params=1 << 25)
+# The one bounded oracle sample both the cpu_baseline leg and each step of the
+# reference arm time: about 11 s on 16 host cores at the q4b_full shape (a
+# 5 + 20 step reference run takes about 4.5 minutes).
+ORACLE_SAMPLE = dict(seqs=2, head_tokens=1024, opt_params=1 << 26)
 
 
 class OracleSample:
@@ -409,7 +408,7 @@ def run_rdt(args, rank, world, local_rank):
     if not args.no_e2e:
         out["e2e"] = run_e2e(tr, shape, args, dev, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = OracleSample(shape, **CPU_BASELINE_SAMPLE).run()
+        out["cpu_baseline"] = OracleSample(shape, **ORACLE_SAMPLE).run()
     return out
 
 
