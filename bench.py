@@ -206,6 +206,26 @@ def stop_clock_sampler(handle):
 ORACLE_SAMPLE = dict(seqs=2, head_tokens=1024, opt_params=1 << 26)
 
 
+def host_cpu():
+    """Threads the oracle's BLAS uses and the host CPU's model name."""
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max(int(i.get("num_threads", 1)) for i in threadpool_info()) or os.cpu_count()
+    except Exception:
+        cores = os.cpu_count()
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        model = next((l.split(":", 1)[1].strip() for l in out.splitlines()
+                      if l.strip().lower().startswith("model name")), None)
+    except Exception:
+        pass
+    if not model:
+        import platform
+        model = platform.processor() or platform.machine()
+    return cores, model
+
+
 class OracleSample:
     """The FP64 oracle timed on a bounded sample of one step, scaled to the
     whole step: one block forward+backward on `seqs` of the workload's
@@ -257,17 +277,14 @@ class OracleSample:
         step_s = (shape.tokens * (shape.layers * (t1 - t0) / self.seq_tokens
                                   + (t2 - t1) / self.head_tokens)
                   + (t3 - t2) * self.n_params / self.opt_params)
-        try:
-            from threadpoolctl import threadpool_info
-            cores = max(int(i.get("num_threads", 1)) for i in threadpool_info()) or os.cpu_count()
-        except Exception:
-            cores = os.cpu_count()
+        cores, model = host_cpu()
         sample = (f"FP64 oracle: 1 block fwd+bwd on {self.s_blk.batch}x{self.s_blk.seq} tokens "
                   f"(x{shape.layers} layers), head+CE fwd+bwd on {self.head_tokens} tokens, "
                   f"clip+AdamW on {self.opt_params} params; scaled to {shape.tokens} tokens "
                   f"and {self.n_params} params per step")
         return {"value": round(shape.tokens / step_s, 3), "unit": UNIT, "cores": cores,
-                "kind": "oracle", "sample": sample, "sample_seconds": round(t3 - t0, 2)}
+                "cpu_model": model, "kind": "oracle", "sample": sample,
+                "sample_seconds": round(t3 - t0, 2)}
 
 
 # ------------------------------------------------------------- GPU arm
@@ -527,16 +544,13 @@ class Nf4OracleSample:
                           self.rank, self.alpha, synth.OPTIM)
         dt = _t.perf_counter() - t0
         step_s = dt * self.shape.tokens / self.seq_tokens
-        try:
-            from threadpoolctl import threadpool_info
-            cores = max(int(i.get("num_threads", 1)) for i in threadpool_info()) or os.cpu_count()
-        except Exception:
-            cores = os.cpu_count()
+        cores, model = host_cpu()
         sample = (f"FP64 NF4+LoRA oracle: block fwd+bwd + adapter clip+AdamW on "
                   f"{self.s_blk.batch}x{self.s_blk.seq} tokens, scaled to {self.shape.tokens} "
                   "tokens per step")
         return {"value": round(self.shape.tokens / step_s, 3), "unit": UNIT, "cores": cores,
-                "kind": "oracle", "sample": sample, "sample_seconds": round(dt, 2)}
+                "cpu_model": model, "kind": "oracle", "sample": sample,
+                "sample_seconds": round(dt, 2)}
 
 
 def run_nf4(args, rank, world, local_rank):
