@@ -211,36 +211,64 @@ __global__ void __launch_bounds__(256) attn_fwd_kernel(const bf16* __restrict__ 
 }
 
 // ------------------------------------------------------ backward: D = rowsum(dO o O)
-// d/8 lanes per (token, head), 8 bf16 (16 bytes) per lane and operand.
-// Writes D[(b*nh + h)*S_ld + s] and, if lse2 is given, lse2 (same index) =
-// lse[(b*nh + h)*S + s] * log2(e).
+// d/8 lanes per (token, head) item, 16 bytes of each operand per lane; each
+// thread takes kPreRounds items spaced one grid apart, so every round streams
+// one contiguous stretch of O and dO, with all loads issued before the first
+// product. Writes D[(b*nh + h)*S_ld + s] and, if lse2 is given, lse2 (same
+// index) = lse[(b*nh + h)*S + s] * log2(e); positions S <= s < S_ld get 0 in
+// both, so the padded segments the tensor-core backward reads are finite.
+constexpr int kPreRounds = 4;
+
+template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const bf16* __restrict__ o,
                                                            const bf16* __restrict__ dout,
                                                            const float* __restrict__ lse,
                                                            float* __restrict__ Dd,
-                                                           float* __restrict__ lse2, int T, int S,
-                                                           int S_ld, int nh, int d) {
-  const int lph = d / 8;
-  const int64_t gthread = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t item = gthread / lph;  // (token, head)
-  const int sub = static_cast<int>(gthread % lph);
-  const bool valid = item < (int64_t)T * nh;
-  float acc = 0.f;
-  if (valid) {
-    const uint4 a = *reinterpret_cast<const uint4*>(o + item * d + 8 * sub);
-    const uint4 c = *reinterpret_cast<const uint4*>(dout + item * d + 8 * sub);
-    const uint32_t* pa = &a.x;
-    const uint32_t* pc = &c.x;
+                                                           float* __restrict__ lse2, int B, int S,
+                                                           int S_ld, int nh) {
+  constexpr int L = D / 8;  // lanes per item
+  const int items = B * S * nh;
+  const int g = static_cast<int>(blockIdx.x) * 256 + static_cast<int>(threadIdx.x);
+  const int stride = static_cast<int>(gridDim.x) * (256 / L);  // items per round
+  const int base = g / L, sub = g % L;
+  uint4 a[kPreRounds], c[kPreRounds];
+#pragma unroll
+  for (int r = 0; r < kPreRounds; ++r) {
+    const int it = base + r * stride;
+    if (it < items) {
+      const int64_t off = static_cast<int64_t>(it) * D + 8 * sub;
+      a[r] = *reinterpret_cast<const uint4*>(o + off);
+      c[r] = *reinterpret_cast<const uint4*>(dout + off);
+    } else {
+      a[r] = make_uint4(0u, 0u, 0u, 0u);
+      c[r] = a[r];
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < kPreRounds; ++r) {
+    const uint32_t* pa = &a[r].x;
+    const uint32_t* pc = &c[r].x;
+    float acc = 0.f;
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc += bf16lo(pa[e]) * bf16lo(pc[e]) + bf16hi(pa[e]) * bf16hi(pc[e]);
+#pragma unroll
+    for (int off = L / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    const int it = base + r * stride;
+    if (sub == 0 && it < items) {
+      const int t = it / nh, h = it - t * nh;
+      const int b = t / S, s = t - b * S;
+      const int64_t bh = static_cast<int64_t>(b) * nh + h;
+      Dd[bh * S_ld + s] = acc;
+      if (lse2) lse2[bh * S_ld + s] = lse[bh * S + s] * kLog2e;
+    }
   }
-  for (int off = lph / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (valid && sub == 0) {
-    const int t = static_cast<int>(item / nh), h = static_cast<int>(item % nh);
-    const int b = t / S, s = t % S;
-    const int64_t bh = (int64_t)b * nh + h;
-    Dd[bh * S_ld + s] = acc;
-    if (lse2) lse2[bh * S_ld + s] = lse[bh * S + s] * kLog2e;
+  // the padding of every (sequence, head) row
+  const int pad = S_ld - S;
+  for (int i = g; i < B * nh * pad; i += static_cast<int>(gridDim.x) * 256) {
+    const int64_t bh = i / pad;
+    const int s = S + i % pad;
+    Dd[bh * S_ld + s] = 0.f;
+    if (lse2) lse2[bh * S_ld + s] = 0.f;
   }
 }
 
@@ -515,11 +543,18 @@ cudaError_t attn_fwd(const bf16* q, int64_t ldq, const bf16* k, int64_t ldk, con
 
 cudaError_t attn_bwd_pre(const bf16* o, const bf16* dout, const float* lse, float* Dd,
                          float* lse2, int B, int S, int S_ld, int nh, int d, cudaStream_t s) {
-  const int T = B * S;
-  const int64_t threads = (int64_t)T * nh * (d / 8);
-  const int blocks = (int)((threads + 255) / 256);
+  const int64_t threads = (int64_t)B * S * nh * (d / 8);
+  if (threads >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;  // 32-bit thread indices
+  const int per_block = 256 * kPreRounds;
+  const dim3 grid(static_cast<unsigned>((threads + per_block - 1) / per_block));
   note_launch();
-  attn_bwd_pre_kernel<<<blocks, 256, 0, s>>>(o, dout, lse, Dd, lse2, T, S, S_ld, nh, d);
+  switch (d) {
+    case 16: attn_bwd_pre_kernel<16><<<grid, 256, 0, s>>>(o, dout, lse, Dd, lse2, B, S, S_ld, nh); break;
+    case 32: attn_bwd_pre_kernel<32><<<grid, 256, 0, s>>>(o, dout, lse, Dd, lse2, B, S, S_ld, nh); break;
+    case 64: attn_bwd_pre_kernel<64><<<grid, 256, 0, s>>>(o, dout, lse, Dd, lse2, B, S, S_ld, nh); break;
+    case 128: attn_bwd_pre_kernel<128><<<grid, 256, 0, s>>>(o, dout, lse, Dd, lse2, B, S, S_ld, nh); break;
+    default: return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 

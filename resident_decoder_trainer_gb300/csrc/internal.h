@@ -200,7 +200,8 @@ cudaError_t attn_fwd(const bf16* q, int64_t ldq, const bf16* k, int64_t ldk, con
                      int64_t ldv, bf16* o, float* lse, int B, int S, int nh, int nkv, int d,
                      cudaStream_t s);
 // D[(b*nh + h)*S_ld + s] = sum_d dO * O; if lse2 != null also
-// lse2[same] = lse[(b*nh + h)*S + s] * log2(e).
+// lse2[same] = lse[(b*nh + h)*S + s] * log2(e); 0 in both for S <= s < S_ld.
+// d in {16, 32, 64, 128}.
 cudaError_t attn_bwd_pre(const bf16* o, const bf16* dout, const float* lse, float* D,
                          float* lse2, int B, int S, int S_ld, int nh, int d, cudaStream_t s);
 // Row stride (>= S, multiple of 64) of the D / lse2 arrays the tensor-core backward reads.
