@@ -34,10 +34,11 @@ def to_np(t):
 SQ_START = 0.25  # grad_sq value before a block backward adds its squared sum
 
 
-def gpu_block(shape, p, x, dy, with_sq=False):
+def gpu_block(shape, p, x, dy, with_sq=False, fill=None):
     """Block forward + backward on the GPU. p: dict of CPU fp32 tensors.
     with_sq: also return the fused squared sum the backward added to a
-    scalar that held SQ_START."""
+    scalar that held SQ_START. fill: a byte value the saved-activation and
+    workspace buffers are filled with first (default: left uninitialised)."""
     cfg = rdt.Config.from_shape(shape)
     n = rdt.block_param_count(cfg)
     offs = rdt.block_param_offsets(cfg)
@@ -50,6 +51,9 @@ def gpu_block(shape, p, x, dy, with_sq=False):
                         device="cuda")
     ws = torch.empty(rdt.block_workspace_bytes(cfg, shape.batch, shape.seq), dtype=torch.uint8,
                      device="cuda")
+    if fill is not None:
+        saved.fill_(fill)
+        ws.fill_(fill)
     xd = x.to("cuda").contiguous()
     y = torch.empty_like(xd)
     rdt.block_forward(cfg, shape.batch, shape.seq, w, wb, xd, y, saved, ws)
@@ -67,7 +71,9 @@ def gpu_block(shape, p, x, dy, with_sq=False):
     return y, dx, g
 
 
-def gpu_head(shape, h, g_final, w_lm, targets):
+def gpu_head(shape, h, g_final, w_lm, targets, fill=None):
+    """Fused LM-head cross-entropy on the GPU; fill: a byte value the
+    workspace is filled with first (default: left uninitialised)."""
     cfg = rdt.Config.from_shape(shape)
     T = h.shape[0]
     hd = h.to("cuda").contiguous()
@@ -75,6 +81,8 @@ def gpu_head(shape, h, g_final, w_lm, targets):
     wl = w_lm.to("cuda").to(torch.bfloat16).contiguous()
     tg = targets.to("cuda").to(torch.int32).contiguous()
     ws = torch.empty(rdt.head_workspace_bytes(cfg, T), dtype=torch.uint8, device="cuda")
+    if fill is not None:
+        ws.fill_(fill)
     loss = torch.empty(T, dtype=torch.float32, device="cuda")
     dh = torch.empty_like(hd)
     dgf = torch.empty_like(gf)

@@ -164,19 +164,54 @@ def test_block_parity_head_dim_64_gqa4_long_sequence():
                              intermediate=512, seq=650, batch=1), seed=13)
 
 
+@pytest.mark.parametrize("shape", [
+    ragged_shape(layers=1, hidden=512, n_heads=4, n_kv_heads=4, head_dim=128, intermediate=1376,
+                 seq=131, batch=1),
+    ragged_shape(layers=1, hidden=256, n_heads=8, n_kv_heads=2, head_dim=64, intermediate=512,
+                 seq=650, batch=1),
+    ragged_shape(layers=1, hidden=128, n_heads=8, n_kv_heads=2, head_dim=32, intermediate=352,
+                 seq=97, batch=3),
+], ids=["d128-s131", "d64-s650", "d32-s97"])
+def test_block_ignores_stale_workspace_contents(shape):
+    """Whatever the saved-activation and workspace buffers held before the
+    call (zeros, or all-ones bytes: NaN in fp32 and bf16), the block's output,
+    input gradient and weight gradients are the same to the bit: no kernel
+    reads a position it did not write first (padded segments included)."""
+    blk, x, dy = synth.make_block_inputs(shape, 11)
+    runs = [gpu_block(shape, blk, x, dy, fill=f) for f in (0x00, 0xFF)]
+    (y0, dx0, g0), (y1, dx1, g1) = runs
+    assert torch.isfinite(y1).all() and torch.isfinite(dx1).all()
+    assert torch.equal(y0, y1) and torch.equal(dx0, dx1)
+    for name in g0:
+        assert torch.equal(g0[name], g1[name]), name
+
+
 def test_block_parity_head_dim_32_gqa4():
     _block_case(ragged_shape(layers=1, hidden=128, n_heads=8, n_kv_heads=2, head_dim=32,
                              intermediate=352, seq=97, batch=3), seed=5)
 
 
 # ------------------------------------------------------------------- head
-@pytest.mark.parametrize("shape", [synth.WORKLOADS["tiny"], ragged_shape()])
-def test_fused_cross_entropy_parity(shape):
+# 2048 tokens x 70,000 entries: two vocabulary chunks (the library keeps a
+# chunk's bf16 dz at or below 128 M elements: 65,536 columns here), the second
+# ragged, so the running log-sum-exp merge and the dh accumulation across
+# chunks are exercised
+TWO_CHUNKS = ragged_shape(hidden=256, vocab=70000, seq=1024, batch=2)
+
+
+def _head_inputs(shape):
     g = torch.Generator().manual_seed(11)
     h = torch.randn(shape.tokens, shape.hidden, generator=g)
     gf = 1.0 + 0.1 * torch.randn(shape.hidden, generator=g)
     wl = 0.02 * torch.randn(shape.vocab, shape.hidden, generator=g)
     tg = torch.randint(0, shape.vocab, (shape.tokens,), generator=g)
+    return h, gf, wl, tg
+
+
+@pytest.mark.parametrize("shape", [synth.WORKLOADS["tiny"], ragged_shape(), TWO_CHUNKS],
+                         ids=["tiny", "ragged", "two-chunks"])
+def test_fused_cross_entropy_parity(shape):
+    h, gf, wl, tg = _head_inputs(shape)
     ref = om.head_forward_backward(h, gf, wl, tg.numpy(), shape)
     loss, dh, dgf, dwl = gpu_head(shape, h, gf, wl, tg)
     lp = to_np(loss)
@@ -187,6 +222,21 @@ def test_fused_cross_entropy_parity(shape):
     assert rel_l2(to_np(dwl), ref["w_lm"]) < GRAD_REL_L2
     ref_sq = float(np.sum(to_np(dgf) ** 2) + np.sum(to_np(dwl) ** 2))
     assert abs(gpu_head.last_sq - ref_sq) / ref_sq < 1e-6
+
+
+@pytest.mark.parametrize("shape", [ragged_shape(), TWO_CHUNKS], ids=["ragged", "two-chunks"])
+def test_head_ignores_stale_workspace_contents(shape):
+    """The loss partials and gradients of the fused cross-entropy do not
+    depend on what its workspace held before the call (zeros, or all-ones
+    bytes: NaN in fp32 and bf16)."""
+    h, gf, wl, tg = _head_inputs(shape)
+    r0 = gpu_head(shape, h, gf, wl, tg, fill=0x00)
+    sq0 = gpu_head.last_sq
+    r1 = gpu_head(shape, h, gf, wl, tg, fill=0xFF)
+    assert gpu_head.last_sq == sq0
+    for a, b in zip(r0, r1):
+        assert torch.isfinite(b).all()
+        assert torch.equal(a, b)
 
 
 def test_cross_entropy_of_zero_head_is_log_vocab():
