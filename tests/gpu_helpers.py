@@ -126,13 +126,17 @@ def nf4_buffers(shape, rank, base, gains, lora):
     return cfg, codes.cuda(), scales.cuda(), g.cuda(), lw, shadow
 
 
-def gpu_nf4_block(shape, rank, alpha, base, gains, lora, x, dy):
+def gpu_nf4_block(shape, rank, alpha, base, gains, lora, x, dy, fill=None):
     """NF4 + LoRA block forward + backward on the GPU: (y, dx, adapter grads
-    {name: tensor}, fused squared sum added to SQ_START)."""
+    {name: tensor}, fused squared sum added to SQ_START). fill: a byte value
+    the saved-activation and workspace buffers are filled with first."""
     cfg, codes, scales, g, lw, shadow = nf4_buffers(shape, rank, base, gains, lora)
     B, S = shape.batch, shape.seq
     saved = torch.empty(rdt.nf4_saved_bytes(cfg, rank, B, S), dtype=torch.uint8, device="cuda")
     ws = torch.empty(rdt.nf4_workspace_bytes(cfg, rank, B, S), dtype=torch.uint8, device="cuda")
+    if fill is not None:
+        saved.fill_(fill)
+        ws.fill_(fill)
     xd = x.to("cuda").contiguous()
     y = torch.empty_like(xd)
     rdt.nf4_block_forward(cfg, rank, alpha, B, S, codes, scales, g, shadow, xd, y, saved, ws)

@@ -155,6 +155,26 @@ def test_nf4_block_parity_head_dim_128_odd_seq():
                                intermediate=768, seq=131, batch=1), 16, 32.0, b_std=0.05, seed=4)
 
 
+@pytest.mark.parametrize("shape", [
+    _nf4_shape(),
+    _nf4_shape(hidden=512, n_heads=4, n_kv_heads=1, head_dim=128, intermediate=768, seq=131,
+               batch=1),
+], ids=["d64-s200", "d128-s131"])
+def test_nf4_block_ignores_stale_workspace_contents(shape):
+    """Zeros or all-ones bytes (NaN) in the saved-activation and workspace
+    buffers before the call give bit-identical outputs, input gradients,
+    adapter gradients and squared sums."""
+    base, gains, lora, x, dy = synth.make_nf4_inputs(shape, seed=2, rank=16, b_std=0.05)
+    gains = _random_gains(shape, gains, 3)
+    r0 = gpu_nf4_block(shape, 16, 32.0, base, gains, lora, x, dy, fill=0x00)
+    r1 = gpu_nf4_block(shape, 16, 32.0, base, gains, lora, x, dy, fill=0xFF)
+    assert torch.isfinite(r1[0]).all() and torch.isfinite(r1[1]).all()
+    assert torch.equal(r0[0], r1[0]) and torch.equal(r0[1], r1[1])
+    for name in r0[2]:
+        assert torch.equal(r0[2][name], r1[2][name]), name
+    assert r0[3] == r1[3]
+
+
 def test_nf4_block_zero_b_gives_exactly_zero_da():
     """B = 0 (the adapters' initial state): U = s dY B vanishes exactly, so every
     dA is exactly zero and dB, y, dx are those of the plain NF4 block."""
