@@ -737,12 +737,9 @@ rdt_status rdt_block_backward(const rdt_config* cfg, int32_t batch, int32_t seq,
   }
   // attention backward (GQA reduction inside), dq accumulated in fp32
   if (attn_tc_supported((int)m.d, true)) {
-    // tensor-core backward: padded log2-LSE / D rows; every dq element written once
+    // tensor-core backward: padded log2-LSE / D rows (the pre-pass writes the
+    // padding as 0); every dq element written once
     const int S_pad = attn_lse_pad(seq);
-    if (S_pad != seq) {
-      RDT_CHECK_CUDA(cudaMemsetAsync(wk.Dd, 0, sizeof(float) * batch * m.nh * S_pad, s));
-      RDT_CHECK_CUDA(cudaMemsetAsync(wk.lse2, 0, sizeof(float) * batch * m.nh * S_pad, s));
-    }
     RDT_CHECK_CUDA(attn_bwd_pre(sv.o, wk.dout, sv.lse, wk.Dd, wk.lse2, batch, seq, S_pad,
                                 (int)m.nh, (int)m.d, s));
     RDT_CHECK_CUDA(attn_bwd_tc(sv.qr, m.qd, sv.kr, m.kd, sv.vb, m.kd, wk.dout,
@@ -1435,11 +1432,7 @@ rdt_status rdt_nf4_block_backward(const rdt_config* cfg, int32_t rank, float alp
   if ((st = tn(nw.du_o, r, r, sv.o, m.qd, m.qd, RDT_LORA_A_O)) != RDT_OK) return st;
   // attention backward
   if (attn_tc_supported((int)m.d, true)) {
-    const int S_pad = attn_lse_pad(seq);
-    if (S_pad != seq) {
-      RDT_CHECK_CUDA(cudaMemsetAsync(wk.Dd, 0, sizeof(float) * batch * m.nh * S_pad, s));
-      RDT_CHECK_CUDA(cudaMemsetAsync(wk.lse2, 0, sizeof(float) * batch * m.nh * S_pad, s));
-    }
+    const int S_pad = attn_lse_pad(seq);  // the pre-pass writes the padding as 0
     RDT_CHECK_CUDA(attn_bwd_pre(sv.o, wk.dout, sv.lse, wk.Dd, wk.lse2, batch, seq, S_pad,
                                 (int)m.nh, (int)m.d, s));
     RDT_CHECK_CUDA(attn_bwd_tc(sv.qr, m.qd, sv.kr, m.kd, sv.vb, m.kd, wk.dout, wk.lse2, wk.Dd,

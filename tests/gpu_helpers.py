@@ -38,7 +38,8 @@ def gpu_block(shape, p, x, dy, with_sq=False, fill=None):
     """Block forward + backward on the GPU. p: dict of CPU fp32 tensors.
     with_sq: also return the fused squared sum the backward added to a
     scalar that held SQ_START. fill: a byte value the saved-activation and
-    workspace buffers are filled with first (default: left uninitialised)."""
+    workspace buffers are filled with first, and the workspace again between
+    the forward and the backward (default: left uninitialised)."""
     cfg = rdt.Config.from_shape(shape)
     n = rdt.block_param_count(cfg)
     offs = rdt.block_param_offsets(cfg)
@@ -57,6 +58,8 @@ def gpu_block(shape, p, x, dy, with_sq=False, fill=None):
     xd = x.to("cuda").contiguous()
     y = torch.empty_like(xd)
     rdt.block_forward(cfg, shape.batch, shape.seq, w, wb, xd, y, saved, ws)
+    if fill is not None:
+        ws.fill_(fill)  # the backward keeps nothing of the forward's scratch
     dyd = dy.to("cuda").contiguous()
     dx = torch.empty_like(xd)
     grads = torch.full((n,), float("nan"), dtype=torch.float32, device="cuda")
@@ -129,7 +132,8 @@ def nf4_buffers(shape, rank, base, gains, lora):
 def gpu_nf4_block(shape, rank, alpha, base, gains, lora, x, dy, fill=None):
     """NF4 + LoRA block forward + backward on the GPU: (y, dx, adapter grads
     {name: tensor}, fused squared sum added to SQ_START). fill: a byte value
-    the saved-activation and workspace buffers are filled with first."""
+    the saved-activation and workspace buffers are filled with first, and the
+    workspace again between the forward and the backward."""
     cfg, codes, scales, g, lw, shadow = nf4_buffers(shape, rank, base, gains, lora)
     B, S = shape.batch, shape.seq
     saved = torch.empty(rdt.nf4_saved_bytes(cfg, rank, B, S), dtype=torch.uint8, device="cuda")
@@ -140,6 +144,8 @@ def gpu_nf4_block(shape, rank, alpha, base, gains, lora, x, dy, fill=None):
     xd = x.to("cuda").contiguous()
     y = torch.empty_like(xd)
     rdt.nf4_block_forward(cfg, rank, alpha, B, S, codes, scales, g, shadow, xd, y, saved, ws)
+    if fill is not None:
+        ws.fill_(fill)  # the backward keeps nothing of the forward's scratch
     dx = torch.empty_like(xd)
     grads = torch.full_like(lw, float("nan"))
     sq = torch.full((1,), SQ_START, dtype=torch.float64, device="cuda")
