@@ -1,14 +1,18 @@
 // HBM-bound kernels of the training step: RMSNorm forward/backward (with the
 // residual add and deterministic gain-gradient reduction), per-head QK
-// RMSNorm + RoPE-neox forward/backward, the cross-entropy finalise and
-// softmax-gradient passes, the multi-buffer squared sum, the clip scale and
-// AdamW. All are single-pass (or two-pass where a row statistic is needed),
-// 128-bit vectorised, with warp-shuffle reductions; every reduction runs in a
-// fixed order, so results are bitwise reproducible run to run.
+// RMSNorm + RoPE-neox forward/backward, the merge of the LM head's
+// per-chunk cross-entropy statistics, the multi-buffer squared sum, the clip
+// scale and AdamW. All are single-pass (or two-pass where a row statistic is
+// needed), 128-bit vectorised, with warp-shuffle reductions; every reduction
+// runs in a fixed order, so results are bitwise reproducible run to run.
 #include <cmath>
+
+#include <cooperative_groups.h>
 
 #include "common.cuh"
 #include "internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace rdt {
 
@@ -130,23 +134,37 @@ __global__ void __launch_bounds__(512) rmsnorm_bwd_kernel(
   }
 }
 
-// out[c] (= or, with accumulate, +=) sum_p partials[p, c]: 8 row-strided
-// partial sums per column, then those 8 in order (deterministic).
+// out[c] (= or, with accumulate, +=) sum_p partials[p, c]. A cluster of
+// `split` CTAs (1..8) serves 32 columns: CTA r of the cluster sums the rows
+// p = r*8 + ty, r*8 + ty + 8*split, ... (8 row-strided sums per column, added
+// in order), and CTA 0 adds the split CTAs' column sums in rank order, read
+// through distributed shared memory. Deterministic for a given split.
+constexpr int kRcMaxSplit = 8;
 __global__ void __launch_bounds__(256) reduce_cols_kernel(const float* __restrict__ partials,
                                                           int P, int W, float* __restrict__ out,
                                                           int accumulate) {
   __shared__ float red[8][33];
+  __shared__ float part[kRcMaxSplit][32];
+  cg::cluster_group cl = cg::this_cluster();
+  const int split = static_cast<int>(cl.num_blocks());
+  const int r = static_cast<int>(cl.block_rank());
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int c = blockIdx.x * 32 + tx;
   float s = 0.f;
   if (c < W)
-    for (int p = ty; p < P; p += 8) s += partials[(int64_t)p * W + c];
+    for (int p = r * 8 + ty; p < P; p += 8 * split) s += partials[(int64_t)p * W + c];
   red[ty][tx] = s;
   __syncthreads();
-  if (ty == 0 && c < W) {
+  if (ty == 0) {
     float t = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) t += red[i][tx];
+    cl.map_shared_rank(&part[0][0], 0)[r * 32 + tx] = t;
+  }
+  cl.sync();  // the column sums have landed in CTA 0; no CTA leaves before
+  if (r == 0 && ty == 0 && c < W) {
+    float t = 0.f;
+    for (int q = 0; q < split; ++q) t += part[q][tx];
     out[c] = accumulate ? out[c] + t : t;
   }
 }
@@ -195,9 +213,25 @@ int rmsnorm_bwd_partial_rows(int T, int threads) {
 
 static cudaError_t reduce_cols(const float* partials, int P, int W, float* out, cudaStream_t s,
                                bool accumulate) {
+  // about two CTAs per SM, the rows split over up to 8 CTAs per column block
+  const int ncol = (W + 31) / 32;
+  int split = (2 * num_sms() + ncol - 1) / ncol;
+  if (split > kRcMaxSplit) split = kRcMaxSplit;
+  if (split > (P + 7) / 8) split = (P + 7) / 8;
+  if (split < 1) split = 1;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(static_cast<unsigned>(ncol), static_cast<unsigned>(split), 1);
+  lc.blockDim = dim3(256, 1, 1);
+  lc.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 1;
+  at[0].val.clusterDim.y = static_cast<unsigned>(split);
+  at[0].val.clusterDim.z = 1;
+  lc.attrs = at;
+  lc.numAttrs = 1;
   note_launch();
-  reduce_cols_kernel<<<(W + 31) / 32, 256, 0, s>>>(partials, P, W, out, accumulate ? 1 : 0);
-  return cudaGetLastError();
+  return cudaLaunchKernelEx(&lc, reduce_cols_kernel, partials, P, W, out, accumulate ? 1 : 0);
 }
 
 cudaError_t rmsnorm_bwd(const float* dy, const float* x, const float* rstd, const float* gamma,
