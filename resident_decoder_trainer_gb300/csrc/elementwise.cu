@@ -249,7 +249,7 @@ cudaError_t rmsnorm_bwd(const float* dy, const float* x, const float* rstd, cons
 // ----------------------------------------------------------------- RoPE table
 // cs[s, i] = (cos, sin)(s * inv_freq[i]) with inv_freq[i] = theta^(-2i/d)
 // computed in fp64 on the host; the angle is formed and reduced modulo 2*pi
-// in fp64, then evaluated with the fp32 sincosf on |r| <= pi.
+// in fp64, then evaluated with the fp32 sincosf on |r| <= pi (+ rounding).
 struct InvFreq {
   double v[64];
 };
@@ -258,8 +258,11 @@ __global__ void rope_table_kernel(float2* __restrict__ cs, int S, int half, cons
   if (idx >= S * half) return;
   const int s = idx / half, i = idx % half;
   const double two_pi = 6.283185307179586476925286766559;
+  const double inv_two_pi = 0.15915494309189533576888376337251;
   const double ang = static_cast<double>(s) * f.v[i];
-  const double k = rint(ang / two_pi);
+  // nearest multiple of 2 pi; off by one only where ang / (2 pi) sits within
+  // rounding of a half-integer, and then |r| is still about pi
+  const double k = rint(ang * inv_two_pi);
   const float rr = static_cast<float>(fma(-k, two_pi, ang));
   float sn, cn;
   sincosf(rr, &sn, &cn);
