@@ -443,21 +443,33 @@ def run_e2e(tr, shape, args, dev, world):
     xd = torch.empty(xh.shape, dtype=xh.dtype, device=dev)
     td = torch.empty(T, dtype=torch.int32, device=dev)
     kw = "ids" if tr.embedding else "x"
+    # events around the copies (on the step's stream) show their share of the
+    # wall time; they do not change what is timed
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     rank_barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(args.steps):
+    for i in range(args.steps):
+        ev[i][0].record()
         xd.copy_(xh, non_blocking=True)
         td.copy_(th, non_blocking=True)
+        ev[i][1].record()
         loss = (tr.train_step if args.no_graph else tr.train_step_graph)(targets=td,
                                                                           **{kw: xd})
+        ev[i][2].record()
         lh.copy_(loss, non_blocking=True)
+        ev[i][3].record()
         torch.cuda.current_stream().synchronize()  # the caller reads this step's loss
     torch.cuda.synchronize()
-    dt = max_over_ranks(time.perf_counter() - t0, world, dev)
+    wall = time.perf_counter() - t0
+    dt = max_over_ranks(wall, world, dev)
+    h2d = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    d2h = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
     return {"value": round(job_throughput(dt, world, T * args.steps), 1), "unit": UNIT,
             "h2d_bytes_per_step": xh.numel() * 4 + th.numel() * 4,
-            "d2h_bytes_per_step": lh.numel() * 4}
+            "d2h_bytes_per_step": lh.numel() * 4,
+            "wall_ms_per_step": round(wall * 1e3 / args.steps, 3),
+            "h2d_ms_per_step": round(h2d, 4), "d2h_ms_per_step": round(d2h, 4)}
 
 
 def algorithmic_flops(shape):
@@ -667,19 +679,31 @@ def run_nf4(args, rank, world, local_rank):
         dyh = [d.cpu().pin_memory() for d in dys[:2]]
         sq_h = torch.empty(1, dtype=torch.float64).pin_memory()
         xd, dyd = torch.empty_like(xs[0]), torch.empty_like(dys[0])
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
         rank_barrier(world)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for i in range(args.steps):
+            ev[i][0].record()
             xd.copy_(xh[i % 2], non_blocking=True)
             dyd.copy_(dyh[i % 2], non_blocking=True)
+            ev[i][1].record()
             (tr.train_step_graph if use_graph else tr.train_step)(xd, dyd)
+            ev[i][2].record()
             sq_h.copy_(tr.sumsq, non_blocking=True)
+            ev[i][3].record()
+            torch.cuda.current_stream().synchronize()  # the caller reads this step's result
         torch.cuda.synchronize()
-        dt = max_over_ranks(time.perf_counter() - t0, world, dev)
+        wall = time.perf_counter() - t0
+        dt = max_over_ranks(wall, world, dev)
         out["e2e"] = {"value": round(job_throughput(dt, world, T * args.steps), 1), "unit": UNIT,
                       "h2d_bytes_per_step": 2 * T * shape.hidden * 4,
-                      "d2h_bytes_per_step": 8}
+                      "d2h_bytes_per_step": 8,
+                      "wall_ms_per_step": round(wall * 1e3 / args.steps, 3),
+                      "h2d_ms_per_step": round(statistics.mean(
+                          e[0].elapsed_time(e[1]) for e in ev), 4),
+                      "d2h_ms_per_step": round(statistics.mean(
+                          e[2].elapsed_time(e[3]) for e in ev), 4)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = Nf4OracleSample(shape, tr.rank, tr.alpha).run()
     return out
